@@ -1,0 +1,447 @@
+#!/usr/bin/env python
+"""Benchmark of the KIVI hot path on one GB300.
+
+Main line (the JSON ``value``): the Llama-3-8B-shaped decode step -- batch 8,
+32 query / 8 KV heads, head_dim 128, fp16, 2-bit, group 32, residual 32,
+context 4096 -- one step = append one token (flushing when the residual
+fills) + fused dequantize decode attention.  ``value`` is the decode
+attention's effective HBM bandwidth: algorithmic bytes (packed codes +
+scale/zero + fp16 residual + q/out) over the attention time.  The L2 cache
+is flushed (a 256 MB write) before every timed step, outside the timed
+events.  The same line carries tokens/s, the prefill quantizer on the
+32k-token bf16 workload (2- and 4-bit), the 131k-token long-context
+attention and the 2048+512-step streaming decode.
+
+``--impl reference`` times the CPU oracle (the plain C implementation the
+tests check against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "2-bit decode-attn effective HBM GB/s (% of peak), tokens/s; quantize GB/s"
+WORKLOAD = ("llama3_8b_decode: batch 8, 32 q heads / 8 kv heads, head_dim 128, fp16, "
+            "2-bit, group 32, residual 32, context 4096; step = append 1 token + decode attention")
+G = 32
+FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------ bytes
+
+def nq(l, R):
+    return l - l % R, max(l - R, 0)
+
+
+def attn_bytes(B, Hkv, Hq, D, l, R, bits, q_bytes=2):
+    """Algorithmic bytes of one decode attention: packed codes, fp16 scale/zero,
+    fp16 residual rows, the query and the output."""
+    nqk, nqv = nq(l, R)
+    unit = (nqk * D * bits // 8 + (nqk // G) * D * 4 + (l - nqk) * D * 2
+            + nqv * D * bits // 8 + nqv * (D // G) * 4 + (l - nqv) * D * 2)
+    return B * Hkv * unit + 2 * B * Hq * D * q_bytes
+
+
+def append_bytes(B, Hkv, D, t, R, bits, in_bytes=2):
+    """Algorithmic bytes of appending token t: read k, v; write two ring rows;
+    quantize the value row leaving the window; every R steps the key ring."""
+    unit = 2 * D * in_bytes + 2 * D * 2
+    if t >= R:
+        unit += D * 2 + D * bits // 8 + (D // G) * 4
+    if (t + 1) % R == 0:
+        unit += R * D * 2 + R * D * bits // 8 + (R // G) * D * 4
+    return B * Hkv * unit
+
+
+def prefill_bytes(B, Hkv, D, T, R, bits, in_bytes):
+    """Read K and V once; write codes, scale/zero and the residual rows."""
+    nqk, nqv = nq(T, R)
+    wr = (nqk * D * bits // 8 + (nqk // G) * D * 4 + nqv * D * bits // 8 + nqv * (D // G) * 4
+          + (T - nqk) * D * 2 + (T - nqv) * D * 2)
+    return B * Hkv * (2 * T * D * in_bytes + wr)
+
+
+def peak_hbm():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_traffic():
+    """Per-launch DRAM bytes of the attention kernel from a committed ncu
+    capture, valid only while the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    src = os.path.join(ROOT, "bit_kv_cache_kivi_gb300", "csrc", "attention.cu")
+    try:
+        with open(p) as f:
+            rec = json.load(f)
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        return rec["bytes_per_launch"] if rec.get("source_sha256") == h else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while the GPU work runs."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.rows, self.proc = [], None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+                for n, v in zip(names, r[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_gpu(args):
+    import torch
+    from bit_kv_cache_kivi_gb300 import build, workloads as W
+    from bit_kv_cache_kivi_gb300.kivi import KiviCache
+
+    build.build()
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak, peak_src = peak_hbm()
+    clocks = ClockSampler(0)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    # ---------------- main: decode step at context 4096 (+ a rewind window)
+    K, Wm = args.steps, args.warmup
+    window = 256
+    wl = W.llama3_8b_decode(steps=window)
+    B, Hq, Hkv, D, R, T0 = wl.B, wl.Hq, wl.Hkv, wl.D, wl.R, wl.T
+    cache = KiviCache(batch=B, n_kv_heads=Hkv, n_q_heads=Hq, max_tokens=T0 + window,
+                      bits=2, residual=R)
+    k0, v0 = W.to_torch(wl.k, "f16", dev), W.to_torch(wl.v, "f16", dev)
+    kn, vn = W.to_torch(wl.k_new, "f16", dev), W.to_torch(wl.v_new, "f16", dev)
+    q = W.to_torch(wl.q, "f16", dev)
+    out = torch.empty_like(q)
+
+    def rewind_if_needed():
+        if cache.length - T0 >= window:
+            cache.reset()
+            cache.prefill(k0, v0)
+
+    cache.prefill(k0, v0)
+    for _ in range(Wm):
+        rewind_if_needed()
+        i = cache.length - T0
+        cache.append(kn[i], vn[i])
+        cache.attention(q, out)
+    torch.cuda.synchronize()
+
+    recs = []
+    for _ in range(K):
+        rewind_if_needed()
+        i = cache.length - T0
+        t = cache.length
+        flush.zero_()
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        cache.append(kn[i], vn[i])
+        e1.record(stream)
+        cache.attention(q, out)
+        e2.record(stream)
+        recs.append((t, e0, e1, e2))
+    torch.cuda.synchronize()
+    t_app = np.array([a.elapsed_time(b) for _, a, b, _ in recs]) * 1e-3
+    t_att = np.array([b.elapsed_time(c) for _, _, b, c in recs]) * 1e-3
+    att_b = np.array([attn_bytes(B, Hkv, Hq, D, t + 1, R, 2) for t, *_ in recs], float)
+    app_b = np.array([append_bytes(B, Hkv, D, t, R, 2) for t, *_ in recs], float)
+    attn_gbs = att_b.sum() / t_att.sum() / 1e9
+    step_s = t_app + t_att
+    tokens_per_s = B * K / step_s.sum()
+
+    # ---------------- end to end: pinned host inputs -> device -> host result
+    kh = torch.empty((B, Hkv, D), dtype=torch.float16).pin_memory()
+    vh = torch.empty_like(kh).pin_memory()
+    qh = q.cpu().pin_memory()
+    oh = torch.empty_like(qh).pin_memory()
+    kd, vd = torch.empty_like(kn[0]), torch.empty_like(vn[0])
+    qd = torch.empty_like(q)
+    e2e = []
+    for _ in range(K):
+        rewind_if_needed()
+        i = cache.length - T0
+        t = cache.length
+        kh.copy_(kn[i].cpu())
+        vh.copy_(vn[i].cpu())
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        qd.copy_(qh, non_blocking=True)
+        cache.append(kd, vd)
+        cache.attention(qd, out)
+        oh.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        e2e.append((t, e0.elapsed_time(e1) * 1e-3))
+    e2e_bytes = sum(attn_bytes(B, Hkv, Hq, D, t + 1, R, 2) for t, _ in e2e)
+    e2e_gbs = e2e_bytes / sum(s for _, s in e2e) / 1e9
+
+    result = {
+        "metric": METRIC, "value": round(attn_gbs, 2), "unit": "GB/s", "n_gpus": 1,
+        "steps": K, "warmup": Wm, "ms_per_step": round(float(step_s.mean()) * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,1) K/V with 4 outlier channels x5 per KV head)",
+        "config": {"workload": WORKLOAD, "l2": "flushed (256 MB write) before every timed step",
+                   "context": [int(recs[0][0]), int(recs[-1][0]) + 1]},
+        "pct_of_peak": round(100 * attn_gbs / peak, 2),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "attention_us": round(float(t_att.mean()) * 1e6, 3),
+        "append_us": round(float(t_app.mean()) * 1e6, 3),
+        "append_gbs": round(app_b.sum() / t_app.sum() / 1e9, 2),
+        "gpu_launches": 2 * K,
+    }
+    achieved = float(att_b.mean() / t_att.mean() / 1e9)
+    result["roofline"] = {"kernel": "attn_split_kernel (fused split-combine)", "bound": "hbm",
+                          "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                          "frac": round(achieved / peak, 4), "traffic": kernel_traffic(),
+                          "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                          if peak_src == "measured" else "fallback 6800 GB/s",
+                          "algorithmic_bytes_per_launch": int(att_b.mean())}
+    result["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s",
+                     "h2d_bytes_per_step": int(kh.numel() * 2 * 2 + qh.numel() * 2),
+                     "d2h_bytes_per_step": int(oh.numel() * 2)}
+
+    if not args.main_only:
+        result["workloads"] = extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev,
+                                              peak)
+    result["clocks"] = clocks.stop()
+    del cache
+    return result
+
+
+def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
+    res = {}
+    # ---- prefill quantizer: batch 4, 8 KV heads, 32768 bf16 tokens
+    for bits in (2, 4):
+        wl = W.prefill_quantize(bits)
+        c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.T,
+                      bits=bits, residual=wl.R)
+        k, v = W.to_torch(wl.k, "bf16", dev), W.to_torch(wl.v, "bf16", dev)
+        times = []
+        for rep in range(3 + args.quant_reps):
+            c.reset()
+            e0, e1 = ev(), ev()
+            e0.record(stream)
+            c.prefill(k, v)
+            e1.record(stream)
+            e1.synchronize()
+            if rep >= 3:
+                times.append(e0.elapsed_time(e1) * 1e-3)
+        nbytes = prefill_bytes(wl.B, wl.Hkv, wl.D, wl.T, wl.R, bits, 2)
+        gbs = nbytes / np.mean(times) / 1e9
+        res[f"prefill_quantize_{bits}bit"] = {
+            "what": "batch 4, 8 KV heads, 32768 bf16 tokens, V spikes; one quantize/pack launch",
+            "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
+            "us": round(float(np.mean(times)) * 1e6, 2), "bytes": nbytes}
+        del c, k, v
+    # ---- long context attention: batch 1, 32/8 heads, 131072 tokens, R = 128
+    wl = W.long_context()
+    c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.T,
+                  bits=2, residual=wl.R)
+    c.prefill(W.to_torch(wl.k, "f16", dev), W.to_torch(wl.v, "f16", dev))
+    q = W.to_torch(wl.q, "f16", dev)
+    out = torch.empty_like(q)
+    for _ in range(3):
+        c.attention(q, out)
+    times = []
+    for _ in range(args.attn_reps):
+        flush.zero_()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        c.attention(q, out)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e-3)
+    nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T, wl.R, 2)
+    gbs = nbytes / np.mean(times) / 1e9
+    res["long_context_attention"] = {
+        "what": "batch 1, 32/8 heads, context 131072, R 128; split-K decode attention",
+        "splits": c.splits(), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
+        "us": round(float(np.mean(times)) * 1e6, 2), "bytes": nbytes}
+    del c
+    # ---- streaming decode: batch 64, 28/4 heads, 2048 prefill + 512 steps
+    wl = W.streaming()
+    c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.capacity,
+                  bits=2, residual=wl.R)
+    c.prefill(W.to_torch(wl.k, "f16", dev), W.to_torch(wl.v, "f16", dev))
+    kn, vn = W.to_torch(wl.k_new, "f16", dev), W.to_torch(wl.v_new, "f16", dev)
+    q = W.to_torch(wl.q, "f16", dev)
+    out = torch.empty_like(q)
+    recs = []
+    for i in range(wl.steps):
+        flush.zero_()
+        t = c.length
+        e0, e1, e2 = ev(), ev(), ev()
+        e0.record(stream)
+        c.append(kn[i], vn[i])
+        e1.record(stream)
+        c.attention(q, out)
+        e2.record(stream)
+        recs.append((t, e0, e1, e2))
+    torch.cuda.synchronize()
+    ta = np.array([a.elapsed_time(b) for _, a, b, _ in recs]) * 1e-3
+    tt = np.array([b.elapsed_time(c_) for _, _, b, c_ in recs]) * 1e-3
+    ab = sum(attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, t + 1, wl.R, 2) for t, *_ in recs)
+    res["streaming_decode"] = {
+        "what": "batch 64, 28/4 heads (GQA 7), 2048 prefill then 512 x (append + attention), "
+                "L2 flushed before each step",
+        "tokens_per_s": round(wl.B * wl.steps / (ta.sum() + tt.sum()), 1),
+        "attention_gbs": round(ab / tt.sum() / 1e9, 2),
+        "pct_of_peak": round(100 * ab / tt.sum() / 1e9 / peak, 2),
+        "ms_total": round(float(ta.sum() + tt.sum()) * 1e3, 3)}
+    del c
+    return res
+
+
+# ------------------------------------------------------------------ oracle arm
+
+def run_oracle(steps, warmup, budget_s=None):
+    """The CPU oracle on a bounded sample of the main workload: the decode
+    steps (append + attention) of batch element 0 (8 KV heads, 32 query
+    heads) at context ~4096, single-threaded."""
+    from bit_kv_cache_kivi_gb300 import workloads as W
+    from oracle.kivi_oracle import OracleCache
+    wl = W.llama3_8b_decode(steps=warmup + steps)
+    o = OracleCache(2, G, wl.R, wl.D, 1, wl.Hkv, wl.capacity)
+    o.prefill(np.ascontiguousarray(wl.k[:1]), np.ascontiguousarray(wl.v[:1]))
+    q = np.ascontiguousarray(wl.q[:1].astype(np.float32))
+    done, t_att, t_app, nbytes = 0, 0.0, 0.0, 0
+    t_start = time.perf_counter()
+    for i in range(warmup + steps):
+        t = o.length
+        a0 = time.perf_counter()
+        o.append(np.ascontiguousarray(wl.k_new[i, :1]), np.ascontiguousarray(wl.v_new[i, :1]))
+        a1 = time.perf_counter()
+        o.attention(q)
+        a2 = time.perf_counter()
+        if i >= warmup:
+            done += 1
+            t_app += a1 - a0
+            t_att += a2 - a1
+            nbytes += attn_bytes(1, wl.Hkv, wl.Hq, wl.D, t + 1, wl.R, 2)
+        if budget_s is not None and done >= 1 and time.perf_counter() - t_start > budget_s:
+            break
+    return {"value": round(nbytes / t_att / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{done} decode steps (append + attention) of batch element 0 "
+                      f"(8 KV heads, 32 query heads) at context ~{wl.T + warmup}; single thread",
+            "tokens_per_s": round(done / (t_app + t_att), 3), "steps": done}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quant-reps", type=int, default=10)
+    ap.add_argument("--attn-reps", type=int, default=30)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        cb = run_oracle(args.steps, args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
+                "n_gpus": args.gpus, "steps": cb["steps"], "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+                "data": "synthetic", "config": {"workload": WORKLOAD},
+                "cpu_baseline": cb,
+                "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        # Replicas only: every rank runs the same single-GPU workload on its own
+        # device; no data-path collective exists.
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.barrier()
+    result = run_gpu(args)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        ms = torch.tensor([result["ms_per_step"]], device="cuda")
+        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
+        result["ms_per_step"] = float(ms.item())
+        result["value"] = round(result["value"] * world, 2)
+        result["n_gpus"] = world
+        dist.destroy_process_group()
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            result["cpu_baseline"] = run_oracle(args.steps, 2, budget_s=12.0)
+        print(json.dumps(result))
+
+
+if __name__ == "__main__":
+    main()

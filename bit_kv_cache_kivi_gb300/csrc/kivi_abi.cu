@@ -1,0 +1,260 @@
+// kivi_abi.cu -- host side of the C ABI declared in include/kivi.h:
+// configuration checks, the residual policy (a pure function of the length,
+// so no device readback is ever needed), the context-split policy, and the
+// kernel launches.
+#include <math.h>
+#include <stdlib.h>
+
+#include "../../include/kivi.h"
+#include "kivi_internal.cuh"
+
+#define KIVI_API extern "C" __attribute__((visibility("default")))
+
+struct kivi_cache {
+  kivi_config cfg;
+  kivi_buffers buf;
+  int length;
+  int splits_override;      // 0 = automatic
+  const void* ws_ready;     // workspace whose counter area is known to be zero
+};
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+kivi_status cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return KIVI_OK;
+  g_last_cuda_error = (int)e;
+  return KIVI_ECUDA;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+kivi_status check_config(const kivi_config* c) {
+  if (!c) return KIVI_EINVAL;
+  if (c->bits != 2 && c->bits != 4) return KIVI_EINVAL;
+  if (c->group != kivi::kGroup || c->head_dim != kivi::kHeadDim) return KIVI_EINVAL;
+  if (c->residual <= 0 || c->residual % c->group) return KIVI_ESHAPE;
+  if (c->batch <= 0 || c->n_kv_heads <= 0 || c->n_q_heads <= 0) return KIVI_ESHAPE;
+  if (c->n_q_heads % c->n_kv_heads) return KIVI_ESHAPE;
+  if (c->max_tokens <= 0 || c->max_tokens % c->residual) return KIVI_ESHAPE;
+  if (c->batch > 65535 || c->n_kv_heads > 4096) return KIVI_ESHAPE;  // grid limits
+  return KIVI_OK;
+}
+
+// Algorithm 1 (chooblog KIVI review §3.2.2): keys X_K[:l - l mod R],
+// values X_V[:l - R] are held quantized.
+int nq_k(int l, int R) { return l - l % R; }
+int nq_v(int l, int R) { return l > R ? l - R : 0; }
+
+kivi::CacheView view(const kivi_cache* c) {
+  kivi::CacheView v;
+  v.codes_k = static_cast<uint8_t*>(c->buf.codes_k);
+  v.scale_k = static_cast<__half*>(c->buf.scale_k);
+  v.zero_k = static_cast<__half*>(c->buf.zero_k);
+  v.codes_v = static_cast<uint8_t*>(c->buf.codes_v);
+  v.scale_v = static_cast<__half*>(c->buf.scale_v);
+  v.zero_v = static_cast<__half*>(c->buf.zero_v);
+  v.ring_k = static_cast<__half*>(c->buf.ring_k);
+  v.ring_v = static_cast<__half*>(c->buf.ring_v);
+  v.B = c->cfg.batch;
+  v.H = c->cfg.n_kv_heads;
+  v.R = c->cfg.residual;
+  v.Tcap = c->cfg.max_tokens;
+  v.bits = c->cfg.bits;
+  return v;
+}
+
+// Work units of the attention grid besides the split: (b, kv-head, head chunk).
+long attention_units(const kivi_config& c) {
+  const int grp = c.n_q_heads / c.n_kv_heads;
+  const int nhc = grp <= 8 ? 1 : (grp + 7) / 8;
+  return (long)c.batch * c.n_kv_heads * nhc;
+}
+
+// Upper bound on the splits: about two CTAs per SM of a GB300 in total.
+int max_splits(const kivi_config& c) {
+  const long u = attention_units(c);
+  long s = (2L * kivi::kTargetSMs + u - 1) / u;
+  if (s < 1) s = 1;
+  const long by_len = (c.max_tokens + 31) / 32;
+  return (int)(s < by_len ? s : by_len);
+}
+
+// Splits used at length l and the (32-aligned) tokens per split.
+void split_plan(const kivi_cache* c, int l, int* splits, int* chunk) {
+  int s = c->splits_override > 0 ? c->splits_override : max_splits(c->cfg);
+  if (s > max_splits(c->cfg)) s = max_splits(c->cfg);
+  if (c->splits_override <= 0) {
+    const int by_work = (l + 255) / 256;  // at least 256 tokens per split when automatic
+    if (s > by_work) s = by_work;
+  }
+  const int tiles = (l + 31) / 32;
+  if (s > tiles) s = tiles;
+  if (s < 1) s = 1;
+  int ch = ((tiles + s - 1) / s) * 32;
+  *chunk = ch;
+  *splits = (l + ch - 1) / ch;  // no empty split
+}
+
+// Workspace layout: partial outputs [B][Hq][S_max][D] f32, partial (max, sum)
+// [B][Hq][S_max][2] f32, then one int counter per attention group.
+struct WsLayout {
+  size_t o_off, ml_off, cnt_off, total;
+};
+
+WsLayout ws_layout(const kivi_config& c) {
+  const size_t rows = (size_t)c.batch * c.n_q_heads * max_splits(c);
+  WsLayout w;
+  w.o_off = 0;
+  w.ml_off = rows * c.head_dim * 4;
+  w.cnt_off = w.ml_off + rows * 2 * 4;
+  w.total = w.cnt_off + ((size_t)attention_units(c) * 4 + 15) / 16 * 16;
+  return w;
+}
+
+}  // namespace
+
+KIVI_API kivi_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes[8]) {
+  kivi_status st = check_config(cfg);
+  if (st != KIVI_OK) return st;
+  if (!bytes) return KIVI_EINVAL;
+  const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
+  const size_t T = cfg->max_tokens, D = cfg->head_dim, G = cfg->group, R = cfg->residual;
+  const size_t codes = units * T * (D * cfg->bits / 8);
+  bytes[0] = codes;                      // codes_k
+  bytes[1] = units * (T / G) * D * 2;    // scale_k
+  bytes[2] = bytes[1];                   // zero_k
+  bytes[3] = codes;                      // codes_v
+  bytes[4] = units * T * (D / G) * 2;    // scale_v
+  bytes[5] = bytes[4];                   // zero_v
+  bytes[6] = units * R * D * 2;          // ring_k
+  bytes[7] = bytes[6];                   // ring_v
+  return KIVI_OK;
+}
+
+KIVI_API kivi_status kivi_cache_init(const kivi_config* cfg, const kivi_buffers* bufs,
+                                     kivi_cache** out) {
+  if (!out) return KIVI_EINVAL;
+  *out = nullptr;
+  kivi_status st = check_config(cfg);
+  if (st != KIVI_OK) return st;
+  if (!bufs) return KIVI_EINVAL;
+  const void* ptrs[8] = {bufs->codes_k, bufs->scale_k, bufs->zero_k, bufs->codes_v,
+                         bufs->scale_v, bufs->zero_v, bufs->ring_k, bufs->ring_v};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return KIVI_EINVAL;
+  kivi_cache* c = static_cast<kivi_cache*>(calloc(1, sizeof(kivi_cache)));
+  if (!c) return KIVI_EINVAL;
+  c->cfg = *cfg;
+  c->buf = *bufs;
+  *out = c;
+  return KIVI_OK;
+}
+
+KIVI_API kivi_status kivi_quantize_prefill(kivi_cache* c, const void* k, const void* v,
+                                           kivi_dtype dtype, int n_tokens, void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (c->length != 0) return KIVI_ESTATE;
+  if (n_tokens < 0) return KIVI_ESHAPE;
+  if (n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  if (n_tokens == 0) return KIVI_OK;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
+  const int R = c->cfg.residual;
+  kivi_status st = cuda_status(kivi::launch_quantize_prefill(
+      view(c), k, v, (int)dtype, n_tokens, nq_k(n_tokens, R), nq_v(n_tokens, R),
+      static_cast<cudaStream_t>(stream)));
+  if (st == KIVI_OK) c->length = n_tokens;
+  return st;
+}
+
+KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const void* v_new,
+                                        kivi_dtype dtype, void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!k_new || !v_new) return KIVI_EINVAL;
+  if (c->length >= c->cfg.max_tokens) return KIVI_ECAPACITY;
+  kivi_status st = cuda_status(kivi::launch_append(view(c), k_new, v_new, (int)dtype,
+                                                   c->length, static_cast<cudaStream_t>(stream)));
+  if (st == KIVI_OK) c->length += 1;
+  return st;
+}
+
+KIVI_API size_t kivi_attention_workspace_bytes(const kivi_cache* c) {
+  if (!c) return 0;
+  return ws_layout(c->cfg).total;
+}
+
+KIVI_API kivi_status kivi_set_attention_splits(kivi_cache* c, int n_splits) {
+  if (!c || n_splits < 0) return KIVI_EINVAL;
+  c->splits_override = n_splits;
+  return KIVI_OK;
+}
+
+KIVI_API int kivi_attention_splits(const kivi_cache* c, int l) {
+  if (!c || l <= 0) return 0;
+  int s, ch;
+  split_plan(c, l, &s, &ch);
+  return s;
+}
+
+KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dtype q_dtype,
+                                           void* out, float softmax_scale, void* workspace,
+                                           size_t ws_bytes, void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (q_dtype != KIVI_F32 && q_dtype != KIVI_F16 && q_dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!q || !out) return KIVI_EINVAL;
+  if (c->length <= 0) return KIVI_ESTATE;
+  if (!workspace || !aligned16(workspace) || ws_bytes < kivi_attention_workspace_bytes(c))
+    return KIVI_EWORKSPACE;
+  kivi::AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.q_dtype = (int)q_dtype;
+  a.Hq = c->cfg.n_q_heads;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.l = c->length;
+  a.nq_k = nq_k(c->length, c->cfg.residual);
+  a.nq_v = nq_v(c->length, c->cfg.residual);
+  split_plan(c, c->length, &a.splits, &a.chunk);
+  const WsLayout w = ws_layout(c->cfg);
+  char* ws = static_cast<char*>(workspace);
+  a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
+  a.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  a.counters = reinterpret_cast<int*>(ws + w.cnt_off);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->ws_ready != workspace) {
+    kivi_status z = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, st));
+    if (z != KIVI_OK) return z;
+    c->ws_ready = workspace;
+  }
+  return cuda_status(kivi::launch_attention(view(c), a, st));
+}
+
+KIVI_API int kivi_cache_length(const kivi_cache* c) { return c ? c->length : -1; }
+
+KIVI_API kivi_status kivi_cache_reset(kivi_cache* c) {
+  if (!c) return KIVI_EINVAL;
+  c->length = 0;
+  return KIVI_OK;
+}
+
+KIVI_API void kivi_cache_destroy(kivi_cache* c) { free(c); }
+
+KIVI_API const char* kivi_status_string(kivi_status s) {
+  switch (s) {
+    case KIVI_OK: return "ok";
+    case KIVI_EINVAL: return "invalid argument (null, unsupported parameter or misaligned buffer)";
+    case KIVI_ESHAPE: return "inconsistent shape";
+    case KIVI_ECAPACITY: return "cache capacity exceeded";
+    case KIVI_EDTYPE: return "unknown dtype";
+    case KIVI_ECUDA: return "CUDA launch error";
+    case KIVI_ESTATE: return "invalid in the cache's current state";
+    case KIVI_EWORKSPACE: return "workspace missing, misaligned or too small";
+  }
+  return "unknown status";
+}
+
+KIVI_API int kivi_last_cuda_error(void) { return g_last_cuda_error; }

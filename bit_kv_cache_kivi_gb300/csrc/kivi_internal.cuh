@@ -1,0 +1,53 @@
+// kivi_internal.cuh -- shared definitions of the CUDA library (internal).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kivi {
+
+constexpr int kHeadDim = 128;  // D supported by the kernels
+constexpr int kGroup = 32;     // G supported by the kernels
+constexpr int kTargetSMs = 152;  // GB300 SM count used by the split policy
+
+// Device view of one cache: the eight buffers plus its shape.
+struct CacheView {
+  uint8_t* codes_k;
+  __half* scale_k;
+  __half* zero_k;
+  uint8_t* codes_v;
+  __half* scale_v;
+  __half* zero_v;
+  __half* ring_k;
+  __half* ring_v;
+  int B, H, R, Tcap, bits;
+};
+
+// Input dtype codes (same values as kivi_dtype).
+enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k,
+                                    const void* v, int dtype, int T, int nq_k,
+                                    int nq_v, cudaStream_t st);
+
+cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
+                          int dtype, int t, cudaStream_t st);
+
+struct AttnArgs {
+  const void* q;
+  void* out;
+  int q_dtype;
+  int Hq;
+  float scale_log2;  // softmax scale * log2(e)
+  int l, nq_k, nq_v;
+  int splits, chunk;  // context split: split s covers [s*chunk, min(l, (s+1)*chunk))
+  float* ws_o;        // [B][Hq][splits][D]
+  float* ws_ml;       // [B][Hq][splits][2]  (running max in log2 units, sum)
+  int* counters;      // [B][H * head_chunks] CTAs finished per group; 0 between calls
+};
+
+cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a,
+                             cudaStream_t st);
+
+}  // namespace kivi

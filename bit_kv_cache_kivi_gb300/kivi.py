@@ -1,0 +1,263 @@
+"""Thin Python binding of the C ABI in ``include/kivi.h`` (ctypes).
+
+The functions named ``kivi_*`` mirror the C entry points one to one and do
+argument marshalling only: every step of the hot path runs in the CUDA
+library.  ``KiviCache`` bundles a handle with its device buffers, allocated
+with PyTorch (PyTorch provides device memory and streams, nothing else).
+
+There is no fallback: if ``libkivi_gb300.so`` is missing this module raises
+on first use; build it with ``python -m bit_kv_cache_kivi_gb300.build``.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkivi_gb300.so")
+
+KIVI_OK, KIVI_EINVAL, KIVI_ESHAPE, KIVI_ECAPACITY = 0, 1, 2, 3
+KIVI_EDTYPE, KIVI_ECUDA, KIVI_ESTATE, KIVI_EWORKSPACE = 4, 5, 6, 7
+KIVI_F32, KIVI_F16, KIVI_BF16 = 0, 1, 2
+
+BUFFER_NAMES = ("codes_k", "scale_k", "zero_k", "codes_v", "scale_v", "zero_v",
+                "ring_k", "ring_v")
+
+_TORCH_DTYPE = {torch.float32: KIVI_F32, torch.float16: KIVI_F16, torch.bfloat16: KIVI_BF16}
+
+
+class KiviError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        msg = f"{what}: {kivi_status_string(status)} (status {status})"
+        if status == KIVI_ECUDA:
+            msg += f", cudaError {lib().kivi_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class kivi_config(C.Structure):
+    _fields_ = [("bits", C.c_int), ("group", C.c_int), ("residual", C.c_int),
+                ("head_dim", C.c_int), ("batch", C.c_int), ("n_kv_heads", C.c_int),
+                ("n_q_heads", C.c_int), ("max_tokens", C.c_int)]
+
+
+class kivi_buffers(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in BUFFER_NAMES]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing; build it with "
+                                  "`python -m bit_kv_cache_kivi_gb300.build`")
+            L = C.CDLL(LIB_PATH)
+            vp, i32, sz, f32 = C.c_void_p, C.c_int, C.c_size_t, C.c_float
+            sigs = {
+                "kivi_cache_sizes": (i32, [C.POINTER(kivi_config), C.POINTER(sz)]),
+                "kivi_cache_init": (i32, [C.POINTER(kivi_config), C.POINTER(kivi_buffers),
+                                          C.POINTER(vp)]),
+                "kivi_quantize_prefill": (i32, [vp, vp, vp, i32, i32, vp]),
+                "kivi_append_decode": (i32, [vp, vp, vp, i32, vp]),
+                "kivi_attention_workspace_bytes": (sz, [vp]),
+                "kivi_decode_attention": (i32, [vp, vp, i32, vp, f32, vp, sz, vp]),
+                "kivi_set_attention_splits": (i32, [vp, i32]),
+                "kivi_attention_splits": (i32, [vp, i32]),
+                "kivi_cache_length": (i32, [vp]),
+                "kivi_cache_reset": (i32, [vp]),
+                "kivi_cache_destroy": (None, [vp]),
+                "kivi_status_string": (C.c_char_p, [i32]),
+                "kivi_last_cuda_error": (i32, []),
+            }
+            for name, (res, args) in sigs.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != KIVI_OK:
+        raise KiviError(status, what)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t) -> int:
+    return t.data_ptr() if isinstance(t, torch.Tensor) else int(t)
+
+
+# ------------------------------------------------------------ C entry points
+
+def kivi_status_string(status: int) -> str:
+    return lib().kivi_status_string(status).decode()
+
+
+def kivi_cache_sizes(cfg: kivi_config) -> list[int]:
+    out = (C.c_size_t * 8)()
+    _check(lib().kivi_cache_sizes(C.byref(cfg), out), "kivi_cache_sizes")
+    return list(out)
+
+
+def kivi_cache_init(cfg: kivi_config, bufs: kivi_buffers) -> C.c_void_p:
+    h = C.c_void_p()
+    _check(lib().kivi_cache_init(C.byref(cfg), C.byref(bufs), C.byref(h)), "kivi_cache_init")
+    return h
+
+
+def kivi_quantize_prefill(h, k, v, dtype: int, n_tokens: int, stream=None) -> None:
+    _check(lib().kivi_quantize_prefill(h, _ptr(k), _ptr(v), dtype, n_tokens, _stream(stream)),
+           "kivi_quantize_prefill")
+
+
+def kivi_append_decode(h, k_new, v_new, dtype: int, stream=None) -> None:
+    _check(lib().kivi_append_decode(h, _ptr(k_new), _ptr(v_new), dtype, _stream(stream)),
+           "kivi_append_decode")
+
+
+def kivi_attention_workspace_bytes(h) -> int:
+    return int(lib().kivi_attention_workspace_bytes(h))
+
+
+def kivi_decode_attention(h, q, q_dtype: int, out, softmax_scale: float, workspace,
+                          ws_bytes: int, stream=None) -> None:
+    _check(lib().kivi_decode_attention(h, _ptr(q), q_dtype, _ptr(out), float(softmax_scale),
+                                       _ptr(workspace), ws_bytes, _stream(stream)),
+           "kivi_decode_attention")
+
+
+def kivi_set_attention_splits(h, n_splits: int) -> None:
+    _check(lib().kivi_set_attention_splits(h, n_splits), "kivi_set_attention_splits")
+
+
+def kivi_attention_splits(h, l: int) -> int:
+    return int(lib().kivi_attention_splits(h, l))
+
+
+def kivi_cache_length(h) -> int:
+    return int(lib().kivi_cache_length(h))
+
+
+def kivi_cache_reset(h) -> None:
+    _check(lib().kivi_cache_reset(h), "kivi_cache_reset")
+
+
+def kivi_cache_destroy(h) -> None:
+    lib().kivi_cache_destroy(h)
+
+
+# ------------------------------------------------------------ convenience
+
+class KiviCache:
+    """A KIVI cache: C handle + the eight device buffers + attention workspace."""
+
+    def __init__(self, *, batch: int, n_kv_heads: int, n_q_heads: int, max_tokens: int,
+                 bits: int = 2, group: int = 32, residual: int = 32, head_dim: int = 128,
+                 device="cuda"):
+        self.cfg = kivi_config(bits, group, residual, head_dim, batch, n_kv_heads,
+                               n_q_heads, max_tokens)
+        self.device = torch.device(device)
+        sizes = kivi_cache_sizes(self.cfg)
+        self.buffers = {n: torch.empty(max(s, 16), dtype=torch.uint8, device=self.device)
+                        for n, s in zip(BUFFER_NAMES, sizes)}
+        bufs = kivi_buffers(*[self.buffers[n].data_ptr() for n in BUFFER_NAMES])
+        self.handle = kivi_cache_init(self.cfg, bufs)
+        self.ws_bytes = kivi_attention_workspace_bytes(self.handle)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h:
+            kivi_cache_destroy(h)
+            self.handle = None
+
+    # -- shape helpers
+    @property
+    def length(self) -> int:
+        return kivi_cache_length(self.handle)
+
+    def _check_kv(self, x: torch.Tensor, T: int | None) -> int:
+        c = self.cfg
+        if x.device != self.device or not x.is_contiguous():
+            raise ValueError("K/V must be contiguous tensors on the cache's device")
+        want = (c.batch, c.n_kv_heads, T, c.head_dim) if T is not None else (
+            c.batch, c.n_kv_heads, c.head_dim)
+        if tuple(x.shape) != want:
+            raise ValueError(f"expected shape {want}, got {tuple(x.shape)}")
+        if x.dtype not in _TORCH_DTYPE:
+            raise ValueError(f"unsupported dtype {x.dtype}")
+        return _TORCH_DTYPE[x.dtype]
+
+    # -- the hot path
+    def prefill(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        T = k.shape[2]
+        dt = self._check_kv(k, T)
+        if self._check_kv(v, T) != dt:
+            raise ValueError("K and V dtypes differ")
+        kivi_quantize_prefill(self.handle, k, v, dt, T, stream)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
+        k_new = k_new.reshape(self.cfg.batch, self.cfg.n_kv_heads, self.cfg.head_dim)
+        v_new = v_new.reshape(self.cfg.batch, self.cfg.n_kv_heads, self.cfg.head_dim)
+        dt = self._check_kv(k_new, None)
+        if self._check_kv(v_new, None) != dt:
+            raise ValueError("K and V dtypes differ")
+        kivi_append_decode(self.handle, k_new, v_new, dt, stream)
+
+    def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
+                  softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+        c = self.cfg
+        if tuple(q.shape) != (c.batch, c.n_q_heads, c.head_dim) or not q.is_contiguous():
+            raise ValueError(f"q must be contiguous {(c.batch, c.n_q_heads, c.head_dim)}")
+        if q.dtype not in _TORCH_DTYPE:
+            raise ValueError(f"unsupported q dtype {q.dtype}")
+        if out is None:
+            out = torch.empty_like(q)
+        elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+            raise ValueError("out must match q")
+        kivi_decode_attention(self.handle, q, _TORCH_DTYPE[q.dtype], out, softmax_scale,
+                              self.workspace, self.ws_bytes, stream)
+        return out
+
+    def set_splits(self, n: int) -> None:
+        kivi_set_attention_splits(self.handle, n)
+
+    def splits(self, l: int | None = None) -> int:
+        return kivi_attention_splits(self.handle, self.length if l is None else l)
+
+    def reset(self) -> None:
+        kivi_cache_reset(self.handle)
+
+    def state_views(self) -> dict:
+        """The buffers as shaped tensors (fp16 buffers as int16 bit patterns)."""
+        c = self.cfg
+        B, H, T, D, G, R = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group, c.residual
+        rb = D * c.bits // 8
+        shapes = {"codes_k": (B, H, T, rb), "scale_k": (B, H, T // G, D),
+                  "zero_k": (B, H, T // G, D), "codes_v": (B, H, T, rb),
+                  "scale_v": (B, H, T, D // G), "zero_v": (B, H, T, D // G),
+                  "ring_k": (B, H, R, D), "ring_v": (B, H, R, D)}
+        out = {}
+        for n, shp in shapes.items():
+            buf = self.buffers[n]
+            n_el = 1
+            for s in shp:
+                n_el *= s
+            if n.startswith("codes"):
+                out[n] = buf[:n_el].view(*shp)
+            else:
+                out[n] = buf[:2 * n_el].view(torch.int16).view(*shp)
+        return out

@@ -1,0 +1,169 @@
+/*
+ * kivi.h -- C ABI of the GB300 (sm_103a) KIVI KV-cache library.
+ *
+ * KIVI keeps the KV cache of a decoder in 2- or 4-bit codes: keys are
+ * quantized per channel (groups of G tokens along the token axis), values
+ * per token (groups of G channels), each group with an fp16 scale and zero
+ * point; the most recent tokens stay in an fp16 residual window.  Decode
+ * attention reads the packed cache directly.
+ *
+ * Sources (page title, section):
+ *   - veloxquant-mlx docs, "KIVI", "How it works" items 1-4 and the
+ *     zero/scale/q/recon formulas (quantizer, grouping axes, residual
+ *     window, group-aligned flushes);
+ *   - chooblog review "KIVI: A Tuning-Free Asymmetric 2bit Quantization for
+ *     KV Cache (ICML'24)", §1.1 (quantization definition), §1.3 (prefill and
+ *     decoding phases: cache X_K, X_V; append t_K, t_V; softmax(t_Q X_K^T) X_V),
+ *     §3.2.2-3.2.3 (grouped + residual split, Algorithm 1), §3.2
+ *     "System-Level" (dequantization fused with the matrix product);
+ *   - "KIVI - 2-bit KV cache quantisation" notebook (attention scaled by
+ *     1/sqrt(head_dim); fp16 (min, scale) pair per group).
+ *
+ * Conventions shared by every call
+ *   - Device memory is owned by the caller; the library never allocates
+ *     device memory.  It allocates only the small host handle.
+ *   - All work is asynchronous on the given stream (a cudaStream_t passed as
+ *     void*; NULL is the legacy default stream).  No call synchronizes the
+ *     device or reads device memory back.
+ *   - Shapes and state are checked on the host before any launch; a call
+ *     that returns an error has launched nothing, except KIVI_ECUDA, which
+ *     reports a launch error (see kivi_last_cuda_error).
+ *   - A handle is not thread-safe; calls on one handle must be serialized
+ *     by the caller (the stream orders the device work).
+ *   - Supported by this build: bits 2 or 4, group 32, head_dim 128,
+ *     residual a multiple of 32, any batch / head counts with
+ *     n_q_heads a multiple of n_kv_heads.
+ *   - Inputs must be finite and within the fp16 range; every input element
+ *     is rounded to fp16 (nearest even) before it is quantized or stored.
+ *
+ * Storage layout (all buffers 16-byte aligned; B batch, H = n_kv_heads,
+ * T = max_tokens, D = head_dim, G = group, R = residual, b = bits):
+ *   codes_k [B][H][T][D*b/8] u8   packed key rows, token-major
+ *   scale_k [B][H][T/G][D]   f16  one (scale, zero) per channel per G tokens
+ *   zero_k  [B][H][T/G][D]   f16
+ *   codes_v [B][H][T][D*b/8] u8   packed value rows
+ *   scale_v [B][H][T][D/G]   f16  one (scale, zero) per G channels per token
+ *   zero_v  [B][H][T][D/G]   f16
+ *   ring_k  [B][H][R][D]     f16  residual keys, token t in slot t mod R
+ *   ring_v  [B][H][R][D]     f16  residual values, token t in slot t mod R
+ * Channel e of a packed row is bits [(e*b)%8, (e*b)%8 + b) of byte (e*b)/8.
+ * After l tokens (Algorithm 1): the first nq_k(l) = R*floor(l/R) keys and
+ * the first nq_v(l) = max(l-R, 0) values are quantized; the rest are in the
+ * rings.  Rows and slots that hold no live token are left untouched.
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KIVI_OK = 0,
+  KIVI_EINVAL = 1,     /* null pointer, unsupported parameter, misaligned buffer */
+  KIVI_ESHAPE = 2,     /* inconsistent sizes (divisibility, token counts) */
+  KIVI_ECAPACITY = 3,  /* the cache would exceed max_tokens */
+  KIVI_EDTYPE = 4,     /* unknown dtype code */
+  KIVI_ECUDA = 5,      /* a kernel launch failed; see kivi_last_cuda_error() */
+  KIVI_ESTATE = 6,     /* call not valid in the cache's current state */
+  KIVI_EWORKSPACE = 7  /* workspace missing, misaligned or too small */
+} kivi_status;
+
+typedef enum { KIVI_F32 = 0, KIVI_F16 = 1, KIVI_BF16 = 2 } kivi_dtype;
+
+/* Cache configuration (veloxquant-mlx "KIVI" usage: bit width, group size,
+ * residual length) plus the tensor shape. */
+typedef struct {
+  int bits;        /* 2 or 4 */
+  int group;       /* G: 32 in this build */
+  int residual;    /* R: fp16 window, a multiple of G */
+  int head_dim;    /* D: 128 in this build */
+  int batch;       /* B */
+  int n_kv_heads;  /* H */
+  int n_q_heads;   /* a multiple of n_kv_heads; query head j reads KV head j/(Hq/H) */
+  int max_tokens;  /* capacity T, a multiple of R */
+} kivi_config;
+
+/* The eight caller-owned device buffers, in the layout above. */
+typedef struct {
+  void *codes_k, *scale_k, *zero_k;
+  void *codes_v, *scale_v, *zero_v;
+  void *ring_k, *ring_v;
+} kivi_buffers;
+
+typedef struct kivi_cache kivi_cache; /* opaque host handle */
+
+/* Bytes each buffer needs, in kivi_buffers order.  Host only; no GPU.
+ * Returns KIVI_EINVAL / KIVI_ESHAPE for a config this build rejects. */
+kivi_status kivi_cache_sizes(const kivi_config *cfg, size_t bytes[8]);
+
+/* Validate cfg, bind the buffers and create an empty handle (length 0).
+ * Host only; the buffers' contents are not touched.  The buffers must stay
+ * valid until kivi_cache_destroy. */
+kivi_status kivi_cache_init(const kivi_config *cfg, const kivi_buffers *bufs,
+                            kivi_cache **out);
+
+/* Prefill (review §1.3 prefill phase; Algorithm 1 prefill steps B-D).
+ * k, v: device [B][H][n_tokens][D] of dtype, contiguous.  The cache must be
+ * empty (KIVI_ESTATE otherwise) and 0 <= n_tokens <= max_tokens.
+ * Quantizes the first nq_k keys per channel and the first nq_v values per
+ * token, stores the remaining tokens in the rings; length becomes n_tokens. */
+kivi_status kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v,
+                                  kivi_dtype dtype, int n_tokens, void *stream);
+
+/* Append one decoded token (review §1.3 decoding step 1; Algorithm 1
+ * decoding phase).  k_new, v_new: device [B][H][D] of dtype.  Token t = length
+ * goes to ring slot t mod R; if t >= R, the value token t-R leaves the
+ * window and is quantized per token; if t+1 is a multiple of R, the R keys of
+ * the ring (a whole number of groups) are quantized per channel.  The
+ * decision is taken on the host from the length alone.  KIVI_ECAPACITY when
+ * the cache is full. */
+kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
+                               const void *v_new, kivi_dtype dtype,
+                               void *stream);
+
+/* Device workspace (bytes) kivi_decode_attention needs for this handle's
+ * shape at any length: split-K partial results and per-group counters.
+ * Host only. */
+size_t kivi_attention_workspace_bytes(const kivi_cache *c);
+
+/* Decode attention over the cache (review §1.3 decoding step 2:
+ * out = softmax(q K^T * scale) V; §3.2 System-Level: dequantization fused
+ * into the products).  q: device [B][n_q_heads][D] of q_dtype; out: device
+ * [B][n_q_heads][D] of q_dtype.  softmax_scale <= 0 means 1/sqrt(D).
+ * The context is split along the tokens; the CTA that finishes last for a
+ * (batch, kv-head) merges the partial (max, sum, output) triples, all in one
+ * kernel launch.
+ * workspace: device, 16-byte aligned, ws_bytes >= kivi_attention_workspace_bytes.
+ * It carries a small counter area between calls: the first call that sees a
+ * given workspace pointer zeroes it (one cudaMemsetAsync on the stream) and
+ * every call leaves it zero.  Do not write to the workspace between calls,
+ * and do not share one workspace between calls that may overlap on the GPU.
+ * KIVI_ESTATE on an empty cache. */
+kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
+                                  kivi_dtype q_dtype, void *out,
+                                  float softmax_scale, void *workspace,
+                                  size_t ws_bytes, void *stream);
+
+/* Override the number of context splits (0 = automatic, which fills the GPU
+ * with about two CTAs per SM of a 152-SM GB300).  The value is clamped to
+ * the workspace bound and to one split per 32 tokens. */
+kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
+
+/* Splits the next kivi_decode_attention call will use at length l. */
+int kivi_attention_splits(const kivi_cache *c, int l);
+
+int kivi_cache_length(const kivi_cache *c); /* tokens held; -1 if c is NULL */
+kivi_status kivi_cache_reset(kivi_cache *c); /* length := 0; no device work */
+void kivi_cache_destroy(kivi_cache *c);      /* NULL is a no-op */
+
+const char *kivi_status_string(kivi_status s);
+int kivi_last_cuda_error(void); /* cudaError_t of the last failed launch on this thread */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIVI_H */

@@ -134,8 +134,9 @@ void orc_quantize_group(const uint16_t *x, long n, long stride, int bits,
     sb = 0x3c00; /* 1.0 */
     s = 1.0f;
   }
-  /* 4. zero point = the minimum (an fp16 value already, so exact) */
-  uint16_t zb = orc_f32_to_f16(mn);
+  /* 4. zero point = the minimum (an fp16 value already, so exact); -0 and
+   *    +0 are the same minimum, and adding +0 stores it as +0 */
+  uint16_t zb = orc_f32_to_f16(mn + 0.0f);
   float z = orc_f16_to_f32(zb);
   /* 5. codes: round half to even of (x - z) / s, then clamp */
   for (long i = 0; i < n; i++) {

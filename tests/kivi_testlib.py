@@ -1,0 +1,101 @@
+"""Shared helpers of the parity tests: run a workload through the CUDA path
+(via the C ABI binding) and through the oracle, and compare."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from bit_kv_cache_kivi_gb300 import workloads as W
+
+ATTN_TOL = 2e-3  # max_i |o_i - r_i| / max_i |r_i| per (batch, query head)
+
+
+def nq_k(l, R):
+    return l - l % R
+
+
+def nq_v(l, R):
+    return max(l - R, 0)
+
+
+def gpu_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None):
+    from bit_kv_cache_kivi_gb300.kivi import KiviCache
+    return KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq,
+                     max_tokens=capacity or wl.capacity, bits=bits or wl.bits,
+                     group=wl.G, residual=wl.R, head_dim=wl.D)
+
+
+def oracle_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None,
+                 units=None):
+    """Oracle cache of the whole batch, or of the (b, h) units listed (B=1, H=1 each)."""
+    from oracle.kivi_oracle import OracleCache
+    cap = capacity or wl.capacity
+    if units is None:
+        return OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, wl.B, wl.Hkv, cap)
+    return [OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, 1, 1, cap) for _ in units]
+
+
+def dev(x: np.ndarray, dtype: str) -> torch.Tensor:
+    return W.to_torch(x, dtype, "cuda")
+
+
+def gpu_state(cache) -> dict:
+    torch.cuda.synchronize()
+    out = {}
+    for n, t in cache.state_views().items():
+        a = t.cpu().numpy()
+        out[n] = a.view(np.uint16) if a.dtype == np.int16 else a
+    return out
+
+
+def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None) -> None:
+    """Bit-exact comparison of the live part of two cache states.
+
+    units: optional list of (b, h) selecting GPU units that correspond, in
+    order, to oracle states given as a list (one B=1, H=1 state each)."""
+    qk, qv = nq_k(l, R), nq_v(l, R)
+    pairs = []
+    if units is None:
+        B, H = gst["codes_k"].shape[:2]
+        pairs = [((b, h), (ost, b, h)) for b in range(B) for h in range(H)]
+    else:
+        pairs = [(u, (o, 0, 0)) for u, o in zip(units, ost)]
+    for (b, h), (o, ob, oh) in pairs:
+        def chk(name, sl_g, sl_o):
+            g, r = gst[name][b, h][sl_g], o[name][ob, oh][sl_o]
+            if not np.array_equal(g, r):
+                idx = np.argwhere(g != r)[:5]
+                raise AssertionError(f"{name} differs at unit {(b, h)} l={l}: first {idx.tolist()}")
+        chk("codes_k", slice(0, qk), slice(0, qk))
+        chk("scale_k", slice(0, qk // G), slice(0, qk // G))
+        chk("zero_k", slice(0, qk // G), slice(0, qk // G))
+        chk("codes_v", slice(0, qv), slice(0, qv))
+        chk("scale_v", slice(0, qv), slice(0, qv))
+        chk("zero_v", slice(0, qv), slice(0, qv))
+        for name, lo in (("ring_k", qk), ("ring_v", qv)):
+            slots = [t % R for t in range(lo, l)]
+            if slots:
+                chk(name, slots, slots)
+
+
+def attn_err(out: np.ndarray, ref: np.ndarray) -> float:
+    """Worst (over batch, head) of max |o - r| / max |r|."""
+    o = out.astype(np.float64).reshape(-1, out.shape[-1])
+    r = ref.astype(np.float64).reshape(-1, ref.shape[-1])
+    return float((np.abs(o - r).max(axis=1) / np.abs(r).max(axis=1)).max())
+
+
+def q_float(q: np.ndarray, dtype: str) -> np.ndarray:
+    """The query as the fp32 values the kernel reads."""
+    if dtype == "bf16":
+        return W.to_torch(q, "bf16").float().numpy()
+    return q.astype(np.float32)
+
+
+def out_float(out: torch.Tensor) -> np.ndarray:
+    return out.float().cpu().numpy()
+
+
+def slice_unit(x: np.ndarray, b: int, h: int) -> np.ndarray:
+    """[B, H, ...] -> [1, 1, ...] contiguous copy of one unit."""
+    return np.ascontiguousarray(x[b:b + 1, h:h + 1])

@@ -1,0 +1,136 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every
+entry point the header declares, and its host logic (sizes, validation,
+state checks, split plan) behaves as documented.  No GPU is needed: nothing
+here launches a kernel."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def K():
+    from bit_kv_cache_kivi_gb300 import build, kivi
+    build.build()
+    kivi.lib()
+    return kivi
+
+
+def _declared():
+    hdr = open(os.path.join(ROOT, "include", "kivi.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    return sorted(set(re.findall(r"\b(kivi_[a-z_0-9]+)\s*\(", hdr)))
+
+
+def test_every_declared_symbol_is_exported(K):
+    names = _declared()
+    assert "kivi_decode_attention" in names and len(names) >= 12
+    lib = C.CDLL(K.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_only_abi_symbols_are_exported(K):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", K.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    funcs = [l.split()[-1] for l in out.splitlines() if " T " in l]
+    ours = [f for f in funcs if f.startswith("kivi_")]
+    assert sorted(ours) == _declared()
+
+
+def cfg(K, **kw):
+    d = dict(bits=2, group=32, residual=32, head_dim=128, batch=2, n_kv_heads=4,
+             n_q_heads=16, max_tokens=4096)
+    d.update(kw)
+    return K.kivi_config(**d)
+
+
+def test_sizes(K):
+    s = K.kivi_cache_sizes(cfg(K))
+    units = 2 * 4
+    assert s[0] == s[3] == units * 4096 * 32
+    assert s[1] == s[2] == units * (4096 // 32) * 128 * 2
+    assert s[4] == s[5] == units * 4096 * 4 * 2
+    assert s[6] == s[7] == units * 32 * 128 * 2
+    s4 = K.kivi_cache_sizes(cfg(K, bits=4))
+    assert s4[0] == s4[3] == 2 * s[0] and s4[1:3] == s[1:3] and s4[4:] == s[4:]
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(bits=3), 1), (dict(bits=8), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
+    (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
+    (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
+])
+def test_config_validation(K, bad, status):
+    with pytest.raises(K.KiviError) as e:
+        K.kivi_cache_sizes(cfg(K, **bad))
+    assert e.value.status == status
+
+
+def _fake_buffers(K, base=1 << 20, misalign=None):
+    ptrs = [base + i * (1 << 16) for i in range(8)]
+    if misalign is not None:
+        ptrs[misalign] += 8
+    return K.kivi_buffers(*ptrs)
+
+
+def test_init_validation_and_host_state(K):
+    c = cfg(K)
+    with pytest.raises(K.KiviError) as e:
+        K.kivi_cache_init(c, K.kivi_buffers(*([None] * 8)))
+    assert e.value.status == K.KIVI_EINVAL
+    for i in range(8):
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_init(c, _fake_buffers(K, misalign=i))
+        assert e.value.status == K.KIVI_EINVAL
+    # binding never touches the buffers, so fake device addresses are fine here
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    try:
+        assert K.kivi_cache_length(h) == 0
+        lib = K.lib()
+        # checks that come before any launch
+        assert lib.kivi_quantize_prefill(h, 16, 16, 7, 10, None) == K.KIVI_EDTYPE
+        assert lib.kivi_quantize_prefill(h, 16, 16, K.KIVI_F16, 4097, None) == K.KIVI_ECAPACITY
+        assert lib.kivi_quantize_prefill(h, 16, 16, K.KIVI_F16, -1, None) == K.KIVI_ESHAPE
+        assert lib.kivi_quantize_prefill(h, 16, 16, K.KIVI_F16, 0, None) == K.KIVI_OK
+        assert lib.kivi_quantize_prefill(h, 0, 16, K.KIVI_F16, 5, None) == K.KIVI_EINVAL
+        assert lib.kivi_append_decode(h, 16, 16, 9, None) == K.KIVI_EDTYPE
+        assert lib.kivi_append_decode(h, 0, 16, K.KIVI_F16, None) == K.KIVI_EINVAL
+        ws = K.kivi_attention_workspace_bytes(h)
+        assert lib.kivi_decode_attention(h, 16, K.KIVI_F16, 16, 0.0, 16, ws, None) == K.KIVI_ESTATE
+        assert lib.kivi_decode_attention(h, 16, 5, 16, 0.0, 16, ws, None) == K.KIVI_EDTYPE
+        assert K.kivi_cache_length(None) == -1
+        K.kivi_cache_reset(h)
+    finally:
+        K.kivi_cache_destroy(h)
+    K.kivi_cache_destroy(None)
+    assert K.kivi_status_string(K.KIVI_ECAPACITY) == "cache capacity exceeded"
+
+
+def test_split_plan_and_workspace(K):
+    # Llama-3-8B decode shape: 64 (b, kv-head) units -> 5 splits fill ~2 CTAs/SM
+    c = cfg(K, batch=8, n_kv_heads=8, n_q_heads=32, max_tokens=4128)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    try:
+        assert K.kivi_attention_splits(h, 4097) == 5
+        assert K.kivi_attention_splits(h, 100) == 1
+        assert K.kivi_attention_workspace_bytes(h) == 8 * 32 * 5 * (128 + 2) * 4 + 64 * 4
+        K.kivi_set_attention_splits(h, 3)
+        assert K.kivi_attention_splits(h, 4097) == 3
+        K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
+        assert K.kivi_attention_splits(h, 4097) == 5
+    finally:
+        K.kivi_cache_destroy(h)
+    # long context: 8 units -> 38 splits; GQA 18 -> three head chunks
+    c = cfg(K, batch=1, n_kv_heads=8, n_q_heads=32, residual=128, max_tokens=131072)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    assert K.kivi_attention_splits(h, 131072) == 38
+    K.kivi_cache_destroy(h)
+    c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=18, max_tokens=1024)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    assert K.kivi_attention_splits(h, 1024) == 4
+    K.kivi_cache_destroy(h)

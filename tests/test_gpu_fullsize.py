@@ -1,0 +1,112 @@
+"""Parity at the full sizes of the five workloads, in the launch configuration
+the benchmark times.  Where the oracle would take minutes on the whole batch,
+whole (batch, kv-head) units are sampled and the oracle runs on those alone."""
+import numpy as np
+import pytest
+import torch
+
+from bit_kv_cache_kivi_gb300 import workloads as W
+import kivi_testlib as T
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from bit_kv_cache_kivi_gb300 import build, kivi
+    build.build()
+    kivi.lib()
+    torch.cuda.init()
+
+
+def unit_oracles(wl, units, capacity=None, bits=None, T_=None):
+    """One B=1, H=1 oracle cache per sampled unit, prefilled with that unit."""
+    outs = T.oracle_cache(wl, capacity, bits, units=units)
+    for (b, h), o in zip(units, outs):
+        k, v = T.slice_unit(wl.k, b, h), T.slice_unit(wl.v, b, h)
+        if T_ is not None:
+            k, v = np.ascontiguousarray(k[:, :, :T_]), np.ascontiguousarray(v[:, :, :T_])
+        o.prefill(k, v)
+    return outs
+
+
+def unit_attention_err(out, wl, units, oracles, q):
+    grp = wl.Hq // wl.Hkv
+    worst = 0.0
+    for (b, h), o in zip(units, oracles):
+        qs = np.ascontiguousarray(T.q_float(q, wl.q_dtype)[b:b + 1, h * grp:(h + 1) * grp])
+        ref = o.attention(qs)
+        worst = max(worst, T.attn_err(out[b:b + 1, h * grp:(h + 1) * grp], ref))
+    return worst
+
+
+def test_llama3_8b_decode_step():
+    """batch 8, 32/8 heads, context 4096 fp16: prefill, one append, attention;
+    the whole batch against the oracle."""
+    wl = W.llama3_8b_decode()
+    g = T.gpu_cache(wl)
+    g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
+    o = T.oracle_cache(wl)
+    o.prefill(wl.k, wl.v)
+    T.compare_state(T.gpu_state(g), o.export(), 4096, 32, 32)
+    g.append(T.dev(wl.k_new[0], "f16"), T.dev(wl.v_new[0], "f16"))
+    o.append(wl.k_new[0], wl.v_new[0])
+    T.compare_state(T.gpu_state(g), o.export(), 4097, 32, 32)
+    out = T.out_float(g.attention(T.dev(wl.q, "f16")))
+    assert T.attn_err(out, o.attention(T.q_float(wl.q, "f16"))) <= T.ATTN_TOL
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_prefill_quantize_bf16_32k(bits):
+    """batch 4, 8 KV heads, 32768 tokens of bf16 with V spikes: sampled units."""
+    wl = W.prefill_quantize(bits)
+    g = T.gpu_cache(wl)
+    g.prefill(T.dev(wl.k, "bf16"), T.dev(wl.v, "bf16"))
+    units = [(0, 0), (3, 7), (1, 5)]
+    orc = unit_oracles(wl, units)
+    T.compare_state(T.gpu_state(g), [o.export() for o in orc], wl.T, wl.R, wl.G, units=units)
+
+
+def test_long_context_131k():
+    """batch 1, 32/8 heads, 131072 tokens, R=128: sampled units, split-K attention."""
+    wl = W.long_context()
+    g = T.gpu_cache(wl)
+    g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
+    assert g.splits() > 16
+    units = [(0, 0), (0, 5)]
+    orc = unit_oracles(wl, units)
+    T.compare_state(T.gpu_state(g), [o.export() for o in orc], wl.T, wl.R, wl.G, units=units)
+    out = T.out_float(g.attention(T.dev(wl.q, "f16")))
+    assert unit_attention_err(out, wl, units, orc, wl.q) <= T.ATTN_TOL
+
+
+def test_streaming_2048_plus_512():
+    """batch 64, 28/4 heads: 512 decode steps after a 2048 prefill.  Attention
+    at the flush boundaries against the oracle (sampled units); the final cache
+    bit-identical to a one-shot prefill of the same 2560 tokens."""
+    wl = W.streaming()
+    g = T.gpu_cache(wl)
+    g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
+    units = [(0, 0), (37, 3)]
+    orc = unit_oracles(wl, units)
+    check_at = {0, 1, 31, 32, 63, 64, 255, 511}
+    kn_all = T.dev(wl.k_new, "f16")
+    vn_all = T.dev(wl.v_new, "f16")
+    for i in range(wl.steps):
+        g.append(kn_all[i], vn_all[i])
+        for (b, h), o in zip(units, orc):
+            o.append(T.slice_unit(wl.k_new[i], b, h), T.slice_unit(wl.v_new[i], b, h))
+        if i in check_at:
+            q = wl.q_for_step(i)
+            out = T.out_float(g.attention(T.dev(q, "f16")))
+            assert unit_attention_err(out, wl, units, orc, q) <= T.ATTN_TOL, i
+        else:
+            g.attention(T.dev(wl.q, "f16"))
+    l = wl.T + wl.steps
+    st = T.gpu_state(g)
+    T.compare_state(st, [o.export() for o in orc], l, wl.R, wl.G, units=units)
+    k_all = np.concatenate([wl.k, wl.k_new.transpose(1, 2, 0, 3)], axis=2)
+    v_all = np.concatenate([wl.v, wl.v_new.transpose(1, 2, 0, 3)], axis=2)
+    one = T.gpu_cache(wl)
+    one.prefill(T.dev(np.ascontiguousarray(k_all), "f16"), T.dev(np.ascontiguousarray(v_all), "f16"))
+    T.compare_state(st, T.gpu_state(one), l, wl.R, wl.G)
