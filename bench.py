@@ -264,7 +264,7 @@ def run_gpu(args):
                      "h2d_bytes_per_step": int(kh.numel() * 2 * 2 + qh.numel() * 2),
                      "d2h_bytes_per_step": int(oh.numel() * 2)}
 
-    if not args.main_only:
+    if not args.main_only and args.only is None:
         result["workloads"] = extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev,
                                               peak)
     result["clocks"] = clocks.stop()
@@ -272,10 +272,11 @@ def run_gpu(args):
     return result
 
 
-def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
+def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak, which=None):
     res = {}
+    want = (lambda n: which is None or which == n)
     # ---- prefill quantizer: batch 4, 8 KV heads, 32768 bf16 tokens
-    for bits in (2, 4):
+    for bits in ((2, 4) if want("quantize") else ()):
         wl = W.prefill_quantize(bits)
         c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.T,
                       bits=bits, residual=wl.R)
@@ -297,6 +298,15 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
             "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
             "us": round(float(np.mean(times)) * 1e6, 2), "bytes": nbytes}
         del c, k, v
+    if want("long"):
+        res.update(long_context(args, torch, W, KiviCache, dev, stream, flush, ev, peak))
+    if want("streaming"):
+        res.update(streaming(args, torch, W, KiviCache, dev, stream, flush, ev, peak))
+    return res
+
+
+def long_context(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
+    res = {}
     # ---- long context attention: batch 1, 32/8 heads, 131072 tokens, R = 128
     wl = W.long_context()
     c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.T,
@@ -322,6 +332,11 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
         "splits": c.splits(), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
         "us": round(float(np.mean(times)) * 1e6, 2), "bytes": nbytes}
     del c
+    return res
+
+
+def streaming(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
+    res = {}
     # ---- streaming decode: batch 64, 28/4 heads, 2048 prefill + 512 steps
     wl = W.streaming()
     c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.capacity,
@@ -354,6 +369,23 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, flush, ev, peak):
         "ms_total": round(float(ta.sum() + tt.sum()) * 1e3, 3)}
     del c
     return res
+
+
+def run_only(args):
+    """One of the secondary workloads alone (used for profiling captures)."""
+    import torch
+    from bit_kv_cache_kivi_gb300 import build, workloads as W
+    from bit_kv_cache_kivi_gb300.kivi import KiviCache
+    build.build()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peak, _ = peak_hbm()
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    return extra_workloads(args, torch, W, KiviCache, dev, torch.cuda.current_stream(), flush,
+                           ev, peak, which=args.only)
 
 
 # ------------------------------------------------------------------ oracle arm
@@ -397,6 +429,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
+    ap.add_argument("--only", choices=["main", "quantize", "long", "streaming"],
+                    help="run one workload alone (for profiling); prints its numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quant-reps", type=int, default=10)
     ap.add_argument("--attn-reps", type=int, default=30)
@@ -427,6 +461,10 @@ def main():
         dist.init_process_group("nccl")
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
         dist.barrier()
+    if args.only and args.only != "main":
+        result = run_only(args)
+        print(json.dumps(result))
+        return
     result = run_gpu(args)
     if world > 1:
         import torch

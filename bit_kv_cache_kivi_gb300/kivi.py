@@ -169,7 +169,10 @@ class KiviCache:
                  device="cuda"):
         self.cfg = kivi_config(bits, group, residual, head_dim, batch, n_kv_heads,
                                n_q_heads, max_tokens)
-        self.device = torch.device(device)
+        d = torch.device(device)
+        if d.type == "cuda" and d.index is None:
+            d = torch.device("cuda", torch.cuda.current_device())
+        self.device = d
         sizes = kivi_cache_sizes(self.cfg)
         self.buffers = {n: torch.empty(max(s, 16), dtype=torch.uint8, device=self.device)
                         for n, s in zip(BUFFER_NAMES, sizes)}
