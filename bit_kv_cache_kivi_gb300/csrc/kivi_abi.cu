@@ -65,36 +65,47 @@ kivi::CacheView view(const kivi_cache* c) {
   return v;
 }
 
-// Work units of the attention grid besides the split: (b, kv-head, head chunk).
+// Work units of the attention grid besides the split: (b, kv-head, chunk of
+// four query heads).
 long attention_units(const kivi_config& c) {
   const int grp = c.n_q_heads / c.n_kv_heads;
-  const int nhc = grp <= 8 ? 1 : (grp + 7) / 8;
-  return (long)c.batch * c.n_kv_heads * nhc;
+  return (long)c.batch * c.n_kv_heads * ((grp + 3) / 4);
 }
 
-// Upper bound on the splits: about two CTAs per SM of a GB300 in total.
-int max_splits(const kivi_config& c) {
+// Upper bound on the packed-tile splits: about three CTAs per SM of a GB300.
+int max_tile_splits(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (2L * kivi::kTargetSMs + u - 1) / u;
+  long s = (3L * kivi::kTargetSMs + u - 1) / u;
   if (s < 1) s = 1;
   const long by_len = (c.max_tokens + 31) / 32;
   return (int)(s < by_len ? s : by_len);
 }
 
-// Splits used at length l and the (32-aligned) tokens per split.
-void split_plan(const kivi_cache* c, int l, int* splits, int* chunk) {
-  int s = c->splits_override > 0 ? c->splits_override : max_splits(c->cfg);
-  if (s > max_splits(c->cfg)) s = max_splits(c->cfg);
+// Split 0 is the tail, splits 1.. the packed tiles.
+int max_splits(const kivi_config& c) { return 1 + max_tile_splits(c); }
+
+// Splits used at length l, the tail start and the (32-aligned) tokens per
+// packed split.
+void split_plan(const kivi_cache* c, int l, int* splits, int* chunk, int* t_tail) {
+  const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
+  *t_tail = tt;
+  const int tiles = tt / 32;
+  if (tiles == 0) {
+    *splits = 1;
+    *chunk = 32;
+    return;
+  }
+  int s = c->splits_override > 0 ? c->splits_override - 1 : max_tile_splits(c->cfg);
+  if (s > max_tile_splits(c->cfg)) s = max_tile_splits(c->cfg);
   if (c->splits_override <= 0) {
-    const int by_work = (l + 255) / 256;  // at least 256 tokens per split when automatic
+    const int by_work = (tt + 255) / 256;  // at least 256 tokens per split when automatic
     if (s > by_work) s = by_work;
   }
-  const int tiles = (l + 31) / 32;
   if (s > tiles) s = tiles;
   if (s < 1) s = 1;
-  int ch = ((tiles + s - 1) / s) * 32;
+  const int ch = ((tiles + s - 1) / s) * 32;
   *chunk = ch;
-  *splits = (l + ch - 1) / ch;  // no empty split
+  *splits = 1 + (tt + ch - 1) / ch;  // no empty split
 }
 
 // Workspace layout: partial outputs [B][Hq][S_max][D] f32, partial (max, sum)
@@ -194,8 +205,8 @@ KIVI_API kivi_status kivi_set_attention_splits(kivi_cache* c, int n_splits) {
 
 KIVI_API int kivi_attention_splits(const kivi_cache* c, int l) {
   if (!c || l <= 0) return 0;
-  int s, ch;
-  split_plan(c, l, &s, &ch);
+  int s, ch, tt;
+  split_plan(c, l, &s, &ch, &tt);
   return s;
 }
 
@@ -218,7 +229,7 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   a.l = c->length;
   a.nq_k = nq_k(c->length, c->cfg.residual);
   a.nq_v = nq_v(c->length, c->cfg.residual);
-  split_plan(c, c->length, &a.splits, &a.chunk);
+  split_plan(c, c->length, &a.splits, &a.chunk, &a.t_tail);
   const WsLayout w = ws_layout(c->cfg);
   char* ws = static_cast<char*>(workspace);
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);

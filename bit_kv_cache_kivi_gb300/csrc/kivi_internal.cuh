@@ -41,7 +41,11 @@ struct AttnArgs {
   int Hq;
   float scale_log2;  // softmax scale * log2(e)
   int l, nq_k, nq_v;
-  int splits, chunk;  // context split: split s covers [s*chunk, min(l, (s+1)*chunk))
+  // Context split: split 0 covers the tail [t_tail, l) (t_tail = nq_v rounded
+  // down to 32); split s >= 1 covers the packed tiles [(s-1)*chunk,
+  // min(t_tail, s*chunk)).
+  int t_tail;
+  int splits, chunk;
   float* ws_o;        // [B][Hq][splits][D]
   float* ws_ml;       // [B][Hq][splits][2]  (running max in log2 units, sum)
   int* counters;      // [B][H * head_chunks] CTAs finished per group; 0 between calls

@@ -13,6 +13,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Value rows are group-interleaved: the unit of 4 channels 32*gp + 4*w .. +3
+// (bits/2 bytes) is stored at unit position 4*w + gp.
+__device__ __forceinline__ int v_unit_pos(int unit) { return 4 * (unit & 7) + (unit >> 3); }
+
 __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
@@ -144,9 +148,15 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
           packed |= encode(f.x, p, L) << (BITS * (2 * i));
           packed |= encode(f.y, p, L) << (BITS * (2 * i + 1));
         }
-        uint8_t* dst = &s_codes[1][(2 * k + par) * RB + cl * LB];
-        if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-        else *reinterpret_cast<uint32_t*>(dst) = packed;
+        // this lane's 8 channels are the units 2*cl and 2*cl + 1
+        uint8_t* row = &s_codes[1][(2 * k + par) * RB];
+        if constexpr (BITS == 2) {
+          row[v_unit_pos(2 * cl)] = (uint8_t)packed;
+          row[v_unit_pos(2 * cl + 1)] = (uint8_t)(packed >> 8);
+        } else {
+          reinterpret_cast<uint16_t*>(row)[v_unit_pos(2 * cl)] = (uint16_t)packed;
+          reinterpret_cast<uint16_t*>(row)[v_unit_pos(2 * cl + 1)] = (uint16_t)(packed >> 16);
+        }
         if ((lane & 3) == 0) {
           s_sz[2 * k + par][cl >> 2] = p.sh;
           s_sz[2 * k + par][4 + (cl >> 2)] = p.zh;
@@ -205,7 +215,9 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
     uint32_t q = encode(x, p, L) << (BITS * (d % PER_BYTE));
 #pragma unroll
     for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-    if (d % PER_BYTE == 0) cv.codes_v[(unit * cv.Tcap + u) * RB + d / PER_BYTE] = (uint8_t)q;
+    // value rows are group-interleaved: channel d is in unit d / 4
+    const int vbyte = v_unit_pos(d / 4) * (BITS / 2) + (d % 4) / PER_BYTE;
+    if (d % PER_BYTE == 0) cv.codes_v[(unit * cv.Tcap + u) * RB + vbyte] = (uint8_t)q;
     if (lane == 0) {
       cv.scale_v[(unit * cv.Tcap + u) * (kHeadDim / kGroup) + warp] = p.sh;
       cv.zero_v[(unit * cv.Tcap + u) * (kHeadDim / kGroup) + warp] = p.zh;

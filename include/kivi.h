@@ -148,9 +148,12 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
                                   float softmax_scale, void *workspace,
                                   size_t ws_bytes, void *stream);
 
-/* Override the number of context splits (0 = automatic, which fills the GPU
- * with about two CTAs per SM of a 152-SM GB300).  The value is clamped to
- * the workspace bound and to one split per 32 tokens. */
+/* Override the number of context splits (0 = automatic).  Split 0 always
+ * takes the tail of the context that is still fp16 (plus the partial value
+ * group before it); the other splits share the packed 32-token tiles.  The
+ * automatic choice aims at about three CTAs per SM of a 152-SM GB300 and at
+ * least 256 tokens per split.  The value is clamped to the workspace bound
+ * and to one split per 32-token tile. */
 kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 
 /* Splits the next kivi_decode_attention call will use at length l. */

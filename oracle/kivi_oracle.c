@@ -170,6 +170,34 @@ void orc_unpack_row(const uint8_t *in, int D, int bits, uint8_t *codes) {
     codes[e] = (uint8_t)((in[(e * bits) / 8] >> ((e * bits) % 8)) & mask);
 }
 
+/* Value rows are stored group-interleaved: the row is split into units of 4
+ * consecutive channels (bits/2 bytes each); unit w of channel group gp
+ * (channels G*gp + 4*w .. +3) is stored at unit position w*(D/G) + gp.
+ * With D = 128 and G = 32 one 32-bit word at 2 bits (two at 4 bits) holds
+ * the same 4-channel slice of all four groups.  Within a unit the layout is
+ * LSB-first like a key row.  The permutation is a storage choice only. */
+int orc_v_unit_pos(int unit, int D, int G) {
+  const int per_group = G / 4; /* units of 4 channels in a group */
+  int gp = unit / per_group, w = unit % per_group;
+  return w * (D / G) + gp;
+}
+
+void orc_pack_row_v(const uint8_t *codes, int D, int bits, int G, uint8_t *out) {
+  uint8_t tmp[4096];
+  orc_pack_row(codes, D, bits, tmp);
+  const int ub = bits / 2; /* bytes per unit of 4 channels */
+  for (int u = 0; u < D / 4; u++)
+    memcpy(out + orc_v_unit_pos(u, D, G) * ub, tmp + u * ub, (size_t)ub);
+}
+
+void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes) {
+  uint8_t tmp[4096];
+  const int ub = bits / 2;
+  for (int u = 0; u < D / 4; u++)
+    memcpy(tmp + u * ub, in + orc_v_unit_pos(u, D, G) * ub, (size_t)ub);
+  orc_unpack_row(tmp, D, bits, codes);
+}
+
 /* ------------------------------------------------------------------ */
 /* Residual policy.
  * ALG1 ([RV] §3.2.2, Algorithm 1): K grouped part X_K[:l-r], r = l mod R;
@@ -220,7 +248,7 @@ orc_cache *orc_cache_new(int bits, int G, int R, int D, int B, int Hkv,
   if ((bits != 2 && bits != 4 && bits != 8) || G <= 0 || R <= 0 || D <= 0 ||
       B <= 0 || Hkv <= 0 || Tcap <= 0)
     return NULL;
-  if (D % G || R % G || Tcap % G || (D * bits) % 8) return NULL;
+  if (D % G || R % G || Tcap % G || G % 4 || (D * bits) % 8) return NULL;
   orc_cache *c = (orc_cache *)calloc(1, sizeof *c);
   if (!c) return NULL;
   c->bits = bits;
@@ -300,8 +328,8 @@ static void quantize_v_token(orc_cache *c, int b, int h, long t) {
                        &c->sv[(u * c->Tcap + t) * (D / G) + gg],
                        &c->zv[(u * c->Tcap + t) * (D / G) + gg], NULL);
   }
-  orc_pack_row(codes, D, c->bits,
-               c->codes_v + (u * c->Tcap + t) * c->rowbytes);
+  orc_pack_row_v(codes, D, c->bits, G,
+                 c->codes_v + (u * c->Tcap + t) * c->rowbytes);
 }
 
 /* Bring the quantized parts up to the policy's counts for length l.
@@ -425,8 +453,8 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
         khat[t * D + d] = orc_f16_to_f32(c->x16_k[(u * c->Tcap + t) * D + d]);
     }
     if (t < c->nqv) {
-      orc_unpack_row(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
-                     codes);
+      orc_unpack_row_v(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
+                       G, codes);
       for (int d = 0; d < D; d++)
         vhat[t * D + d] =
             orc_dequant(codes[d], c->sv[(u * c->Tcap + t) * (D / G) + d / G],

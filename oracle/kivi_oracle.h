@@ -19,7 +19,10 @@
  *   codes_v [B][Hkv][Tcap][D*bits/8]
  *   scale_v, zero_v [B][Hkv][Tcap][D/G] fp16 bit patterns
  *   ring_k, ring_v  [B][Hkv][R][D]      fp16, token t in slot t mod R
- * Channel e of a packed row sits in byte (e*bits)/8 at bit (e*bits)%8.
+ * Channel e of a packed key row sits in byte (e*bits)/8 at bit (e*bits)%8.
+ * Value rows use the same bit order within units of 4 channels, with the
+ * units group-interleaved: the unit holding channels G*gp + 4*w .. +3 is
+ * stored at unit position w * (D/G) + gp (see orc_pack_row_v).
  */
 #ifndef KIVI_ORACLE_H
 #define KIVI_ORACLE_H
@@ -59,6 +62,11 @@ float orc_dequant(int q, uint16_t scale16, uint16_t zero16);
 /* Pack / unpack a row of D codes (LSB-first, channel e at bit e*bits). */
 void orc_pack_row(const uint8_t *codes, int D, int bits, uint8_t *out);
 void orc_unpack_row(const uint8_t *in, int D, int bits, uint8_t *codes);
+
+/* Value rows: group-interleaved units of 4 channels (see the header). */
+int orc_v_unit_pos(int unit, int D, int G);
+void orc_pack_row_v(const uint8_t *codes, int D, int bits, int G, uint8_t *out);
+void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes);
 
 /* Token counts held quantized after l tokens under a policy. */
 long orc_nq_k(long l, int R, int G, int policy);

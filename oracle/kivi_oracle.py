@@ -56,6 +56,9 @@ def lib():
                 "orc_dequant": (f32, [i32, C.c_uint16, C.c_uint16]),
                 "orc_pack_row": (None, [vp, i32, i32, vp]),
                 "orc_unpack_row": (None, [vp, i32, i32, vp]),
+                "orc_v_unit_pos": (i32, [i32, i32, i32]),
+                "orc_pack_row_v": (None, [vp, i32, i32, i32, vp]),
+                "orc_unpack_row_v": (None, [vp, i32, i32, i32, vp]),
                 "orc_nq_k": (i64, [i64, i32, i32, i32]),
                 "orc_nq_v": (i64, [i64, i32, i32, i32]),
                 "orc_cache_new": (vp, [i32, i32, i32, i32, i32, i32, i64, i32]),
@@ -128,6 +131,20 @@ def unpack_row(packed: np.ndarray, D: int, bits: int) -> np.ndarray:
     p = np.ascontiguousarray(packed, dtype=np.uint8)
     out = np.zeros(D, np.uint8)
     lib().orc_unpack_row(_p(p), D, bits, _p(out))
+    return out
+
+
+def pack_row_v(codes: np.ndarray, bits: int, G: int = 32) -> np.ndarray:
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.size * bits // 8, np.uint8)
+    lib().orc_pack_row_v(_p(c), c.size, bits, G, _p(out))
+    return out
+
+
+def unpack_row_v(packed: np.ndarray, D: int, bits: int, G: int = 32) -> np.ndarray:
+    p = np.ascontiguousarray(packed, dtype=np.uint8)
+    out = np.zeros(D, np.uint8)
+    lib().orc_unpack_row_v(_p(p), D, bits, G, _p(out))
     return out
 
 

@@ -135,6 +135,31 @@ def test_pack_layout_lsb_first(oracle):
         assert np.array_equal(oracle.unpack_row(oracle.pack_row(c, bits), 128, bits), c)
 
 
+def test_value_row_interleave(oracle):
+    """Value rows: the unit of channels 32*gp + 4*w .. +3 sits at unit 4*w + gp.
+
+    At 2 bits a unit is one byte: give channel e the code (e // 4) % 4 and the
+    group index in a recognisable pattern, then check byte positions."""
+    codes = np.array([(e // 32 + (e % 32) // 4) % 4 for e in range(128)], np.uint8)
+    row = oracle.pack_row_v(codes, 2)
+    for gp in range(4):
+        for w in range(8):
+            want = oracle.pack_row(codes[32 * gp + 4 * w: 32 * gp + 4 * w + 4], 2)[0]
+            assert row[4 * w + gp] == want
+    row4 = oracle.pack_row_v(codes, 4)
+    for gp in range(4):
+        for w in range(8):
+            want = oracle.pack_row(codes[32 * gp + 4 * w: 32 * gp + 4 * w + 4], 4)
+            assert list(row4[2 * (4 * w + gp): 2 * (4 * w + gp) + 2]) == list(want)
+    rng = np.random.default_rng(4)
+    for bits in (2, 4):
+        c = rng.integers(0, 1 << bits, 128).astype(np.uint8)
+        assert np.array_equal(oracle.unpack_row_v(oracle.pack_row_v(c, bits), 128, bits), c)
+    # with one channel group per unit the interleave is the identity
+    c = rng.integers(0, 4, 8).astype(np.uint8)
+    assert np.array_equal(oracle.pack_row_v(c, 2, G=4), oracle.pack_row(c, 2))
+
+
 def test_key_per_channel_value_per_token_orientation(oracle):
     """Structured K/V whose per-channel (K) and per-token (V) ranges are known.
 
@@ -164,7 +189,7 @@ def test_key_per_channel_value_per_token_orientation(oracle):
     expect = np.array([0] * 6 + [1] * 10 + [2] * 10 + [3] * 6)
     assert np.array_equal(ck, np.broadcast_to(expect[:, None], ck.shape))
     # codes of V depend only on d mod 32, the same pattern along channels
-    cv = oracle.unpack_row(st["codes_v"][0, 0, 5], D, 2)
+    cv = oracle.unpack_row_v(st["codes_v"][0, 0, 5], D, 2)
     assert np.array_equal(cv, np.tile(expect, 4))
 
 
