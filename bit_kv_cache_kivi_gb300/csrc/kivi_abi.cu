@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdlib.h>
 
+#include <mutex>
+
 #include "../../include/kivi.h"
 #include "kivi_internal.cuh"
 
@@ -269,3 +271,79 @@ KIVI_API const char* kivi_status_string(kivi_status s) {
 }
 
 KIVI_API int kivi_last_cuda_error(void) { return g_last_cuda_error; }
+
+// ---------------------------------------------------------------------------
+// Decode attention without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory at the point where they run
+// attention: a step being recorded into a CUDA graph (an allocation there
+// would break or serialize the capture), a plugin inside a host framework
+// whose memory is handed out only by that framework's own pool, or a latency
+// path that must not pay cudaMalloc's implicit synchronization.  For them the
+// library keeps one fixed scratch area in device global memory, declared
+// below, and kivi_decode_attention_static uses it instead of a workspace
+// argument.  Every GPU that loads this library holds the area until the
+// process exits.
+
+static __device__ __align__(256) unsigned char g_static_ws[KIVI_STATIC_WORKSPACE_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices];  // device address of g_static_ws, per device
+
+// Device address of the scratch area on the current device, looked up once
+// per device (the symbol's host-side name is not a device address).
+cudaError_t static_ws_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_ws);
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+
+KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
+                                                  kivi_dtype q_dtype, void* out,
+                                                  float softmax_scale, void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (q_dtype != KIVI_F32 && q_dtype != KIVI_F16 && q_dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!q || !out) return KIVI_EINVAL;
+  if (c->length <= 0) return KIVI_ESTATE;
+  const WsLayout w = ws_layout(c->cfg);
+  if (w.total > (size_t)KIVI_STATIC_WORKSPACE_BYTES) return KIVI_EWORKSPACE;
+  void* ws = nullptr;
+  kivi_status st = cuda_status(static_ws_address(&ws));
+  if (st != KIVI_OK) return st;
+  kivi::AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.q_dtype = (int)q_dtype;
+  a.Hq = c->cfg.n_q_heads;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.l = c->length;
+  a.nq_k = nq_k(c->length, c->cfg.residual);
+  a.nq_v = nq_v(c->length, c->cfg.residual);
+  split_plan(c, c->length, &a.splits, &a.chunk, &a.t_tail);
+  char* base = static_cast<char*>(ws);
+  a.ws_o = reinterpret_cast<float*>(base + w.o_off);
+  a.ws_ml = reinterpret_cast<float*>(base + w.ml_off);
+  a.counters = reinterpret_cast<int*>(base + w.cnt_off);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The area keeps whatever the previous call left; the split counters must
+  // start at zero, so clear them on every call (a memset, not an allocation).
+  st = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, s));
+  if (st != KIVI_OK) return st;
+  return cuda_status(kivi::launch_attention(view(c), a, s));
+}

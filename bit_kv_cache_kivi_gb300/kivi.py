@@ -76,6 +76,7 @@ def lib() -> C.CDLL:
                 "kivi_cache_destroy": (None, [vp]),
                 "kivi_status_string": (C.c_char_p, [i32]),
                 "kivi_last_cuda_error": (i32, []),
+                "kivi_decode_attention_static": (i32, [vp, vp, i32, vp, f32, vp]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -137,6 +138,15 @@ def kivi_decode_attention(h, q, q_dtype: int, out, softmax_scale: float, workspa
     _check(lib().kivi_decode_attention(h, _ptr(q), q_dtype, _ptr(out), float(softmax_scale),
                                        _ptr(workspace), ws_bytes, _stream(stream)),
            "kivi_decode_attention")
+
+
+def kivi_decode_attention_static(h, q, q_dtype: int, out, softmax_scale: float,
+                                 stream=None) -> None:
+    """Decode attention using the library's fixed device scratch area instead
+    of a workspace argument (for callers that cannot allocate; see kivi.h)."""
+    _check(lib().kivi_decode_attention_static(h, _ptr(q), q_dtype, _ptr(out),
+                                              float(softmax_scale), _stream(stream)),
+           "kivi_decode_attention_static")
 
 
 def kivi_set_attention_splits(h, n_splits: int) -> None:

@@ -166,6 +166,33 @@ void kivi_cache_destroy(kivi_cache *c);      /* NULL is a no-op */
 const char *kivi_status_string(kivi_status s);
 int kivi_last_cuda_error(void); /* cudaError_t of the last failed launch on this thread */
 
+/* Size of the library's fixed device scratch area used by
+ * kivi_decode_attention_static: 8 MiB, held on every GPU that loads the
+ * library until the process exits. */
+#define KIVI_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* Decode attention for callers that cannot allocate device memory where they
+ * run it -- for example while recording a CUDA graph, inside a plugin whose
+ * memory must come from its host framework's pool, or on a path that cannot
+ * afford cudaMalloc's synchronization.  No counterpart on the pages: it is
+ * kivi_decode_attention with the split-K scratch taken from the library's
+ * own fixed device area (KIVI_STATIC_WORKSPACE_BYTES) instead of a caller
+ * workspace.  Same q/out/scale contract and results as kivi_decode_attention.
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - Needs kivi_attention_workspace_bytes(c) <= KIVI_STATIC_WORKSPACE_BYTES,
+ *   else KIVI_EWORKSPACE and nothing is launched.
+ * - Runs on the calling thread's current device.  The first call on a device
+ *   looks up the area's device address (cudaGetSymbolAddress) and caches it;
+ *   make that first call before any stream capture.
+ * - Each call clears the area's counters with one cudaMemsetAsync on stream.
+ * - All calls share the one area and it keeps the last call's contents:
+ *   calls that may overlap on the GPU (different streams, or different
+ *   handles without ordering between them) race on it and must not be
+ *   issued; serialize them on one stream. */
+kivi_status kivi_decode_attention_static(kivi_cache *c, const void *q,
+                                         kivi_dtype q_dtype, void *out,
+                                         float softmax_scale, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
