@@ -17,167 +17,390 @@ constexpr unsigned kFull = 0xffffffffu;
 // (bits/2 bytes) is stored at unit position 4*w + gp.
 __device__ __forceinline__ int v_unit_pos(int unit) { return 4 * (unit & 7) + (unit >> 3); }
 
-__device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
-  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+
+// ---------------------------------------------------------------------------
+// Prefill fast path.
+//
+// For a group with zero point z and stored fp16 scale s, the code of x is
+// computed as rint(y') with y' = fma(x, inv, nzi), inv ~ 1/s (rcp.approx,
+// relative error below 2^-22) and nzi = fl(-z * inv).  When |z| * inv <= 64
+// and s is an fp16 normal number, |y' - (x - z)/s| < 2^-17.4 (the rounding of
+// nzi contributes at most 2^-18, the reciprocal 2^-19 for y < 16, the fma
+// 2^-20) and the IEEE quotient fl(fl(x - z) / s) is within 2^-19 of
+// (x - z)/s, so both round to the same integer unless y' lies within 2^-16 of
+// a half-integer; such elements take tie_code, which decides the IEEE
+// rounding exactly without a division.  Groups outside the safe range use
+// the exact division throughout.  In the safe range y' < L + 2^-10, so the
+// clamp is never needed.
+//
+// rint(y') is read off t = y' + 1.5 * 2^23, whose bit pattern is
+// 0x4B400000 + rint(y'); the codes of a word are summed as t_bits << shift
+// (mod 2^32) and the constant sum of the 0x4B400000 << shift terms removed.
+
+constexpr float kNearHalfFast = 0.4999847412109375f;  // 0.5 - 2^-16
+
+struct FastParams {
+  float inv, nzi;
+  bool safe;
+};
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ FastParams fast_params(const GroupParams& p) {
+  FastParams f;
+  f.inv = rcp_approx(p.s);
+  f.nzi = -p.z * f.inv;
+  f.safe = fabsf(p.z) * f.inv <= 64.0f && p.s >= 6.103515625e-05f;
+  return f;
+}
+
+// Exact code of an element whose estimate y lies within 2^-16 of k + 1/2.
+// With d = fl(x - z) and h = k + 1/2, s*h is exact (an fp16 scale times a
+// number of at most 5 significant bits) and d is within a factor 2 of it, so
+// e = fma(-s, h, d) = d - s*h exactly (Sterbenz).  The IEEE quotient
+// fl(d / s) equals h exactly when d/s lies in [h - lo, h + hi] (lo = hi =
+// ulp(h)/2, except lo = ulp(h)/4 at h = 1/2; the end points round to h, whose
+// last mantissa bit is 0), is below h when e < -s*lo and above when e > s*hi.
+// rint(fl(d/s)) follows: k, k + 1, or the even one of them for the tie.
+__device__ __noinline__ uint32_t tie_code(float x, float z, float s, float y) {
+  const float k = floorf(y);
+  const float h = k + 0.5f;
+  const float d = __fsub_rn(x, z);
+  const float e = fmaf(-s, h, d);
+  const float half_ulp = __uint_as_float(((__float_as_uint(h) >> 23) - 24u) << 23);  // ulp(h) / 2
+  const float lo = (k == 0.0f ? 0.5f : 1.0f) * half_ulp * s;
+  const float hi = half_ulp * s;
+  const int ki = (int)k;
+  int q;
+  if (e < -lo) q = ki;
+  else if (e > hi) q = ki + 1;
+  else q = (ki & 1) ? ki + 1 : ki;
+  return kRoundMagicBits + (uint32_t)q;
+}
+
+// Bits of t = y' + 1.5 * 2^23 for the code of x: the fast estimate, or the
+// exact decision when y' is within 2^-16 of a half-integer.
+__device__ __forceinline__ uint32_t fast_bits(float x, float inv, float nzi, float z, float s) {
+  const float y = fmaf(x, inv, nzi);
+  const float t = __fadd_rn(y, kRoundMagic);
+  const float r = __fsub_rn(t, kRoundMagic);
+  if (fabsf(__fsub_rn(y, r)) > kNearHalfFast) return tie_code(x, z, s, y);
+  return __float_as_uint(t);
+}
+
+// sum over e < n of (0x4B400000 << (bits * e)) mod 2^32
+__host__ __device__ constexpr uint32_t magic_sum(int n, int bits) {
+  uint32_t c = 0;
+  for (int e = 0; e < n; ++e) c += kRoundMagicBits << (bits * e);
+  return c;
+}
+
+__device__ __forceinline__ uint32_t exact_code(float x, float z, float s, int L) {
+  const int q = __float2int_rn(__fdiv_rn(__fsub_rn(x, z), s));
+  return (uint32_t)min(max(q, 0), L);
+}
+
+// Exact codes of 8 key channels of one token (each channel its own group).
+template <int BITS>
+__device__ __noinline__ uint32_t exact_key_slice(uint4 xb, const float* z, const float* s) {
+  constexpr int L = (1 << BITS) - 1;
+  const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
+  uint32_t acc = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const float x = __half2float(__ushort_as_half((unsigned short)(w[e >> 1] >> (16 * (e & 1)))));
+    acc |= exact_code(x, z[e], s[e], L) << (BITS * e);
+  }
+  return acc;
+}
+
+// Exact codes of one value group (32 channels, one scale/zero).
+template <int BITS>
+__device__ __noinline__ void exact_value_group(const uint32_t* xw, float z, float s,
+                                               uint32_t* words) {
+  constexpr int L = (1 << BITS) - 1;
+  constexpr int CPW = 32 / BITS;  // codes per word
+#pragma unroll
+  for (int w = 0; w < BITS; ++w) words[w] = 0;
+#pragma unroll
+  for (int e = 0; e < 32; ++e) {
+    const float x = __half2float(__ushort_as_half((unsigned short)(xw[e >> 1] >> (16 * (e & 1)))));
+    words[e / CPW] |= exact_code(x, z, s, L) << (BITS * (e % CPW));
+  }
 }
 
 __device__ __forceinline__ uint32_t h2_bits(__half2 v) {
-  return pack_halves(__low2half(v), __high2half(v));
+  return (uint32_t)__half_as_ushort(__low2half(v)) | ((uint32_t)__half_as_ushort(__high2half(v)) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
+  return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
 __device__ __forceinline__ uint4 h2x4_bits(const __half2 (&v)[4]) {
   return make_uint4(h2_bits(v[0]), h2_bits(v[1]), h2_bits(v[2]), h2_bits(v[3]));
 }
 
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = (uint32_t)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem));
+}
+
+// 8 consecutive input elements staged in shared memory -> fp16 (nearest even).
+template <int DT>
+__device__ __forceinline__ void smem8(const uint4* p, __half2 (&h)[4]);
+
+template <>
+__device__ __forceinline__ void smem8<kF16>(const uint4* p, __half2 (&h)[4]) {
+  const uint4 u = *p;
+  h[0] = *reinterpret_cast<const __half2*>(&u.x);
+  h[1] = *reinterpret_cast<const __half2*>(&u.y);
+  h[2] = *reinterpret_cast<const __half2*>(&u.z);
+  h[3] = *reinterpret_cast<const __half2*>(&u.w);
+}
+
+template <>
+__device__ __forceinline__ void smem8<kBF16>(const uint4* p, __half2 (&h)[4]) {
+  const uint4 u = *p;
+  h[0] = bf16x2_to_half2(u.x);
+  h[1] = bf16x2_to_half2(u.y);
+  h[2] = bf16x2_to_half2(u.z);
+  h[3] = bf16x2_to_half2(u.w);
+}
+
+template <>
+__device__ __forceinline__ void smem8<kF32>(const uint4* p, __half2 (&h)[4]) {
+  const uint4 a = p[0], b = p[1];
+  h[0] = __floats2half2_rn(__uint_as_float(a.x), __uint_as_float(a.y));
+  h[1] = __floats2half2_rn(__uint_as_float(a.z), __uint_as_float(a.w));
+  h[2] = __floats2half2_rn(__uint_as_float(b.x), __uint_as_float(b.y));
+  h[3] = __floats2half2_rn(__uint_as_float(b.z), __uint_as_float(b.w));
+}
+
+// Store the 8 packed units of value group g (channels 32g + 4u .. +3) of one
+// row at their interleaved positions 4u + g.
+template <int BITS>
+__device__ __forceinline__ void store_value_units(uint8_t* row, int g, const uint32_t (&words)[BITS]) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if constexpr (BITS == 2)
+      row[v_unit_pos(8 * g + u)] = (uint8_t)(words[u >> 2] >> (8 * (u & 3)));
+    else
+      reinterpret_cast<uint16_t*>(row)[v_unit_pos(8 * g + u)] = (uint16_t)(words[u >> 1] >> (16 * (u & 1)));
+  }
+}
+
 // One CTA = one 32-token chunk of one (b, kv-head): warp 0 quantizes the
-// chunk's keys (one K group: 128 channels x 32 tokens), warp 1 its values
-// (32 tokens x 4 channel groups).  Lane l holds channels 8*(l%16) .. +7 of
-// the tokens of parity l/16 (16-byte loads, a token row per half-warp).
+// chunk's keys (one K group per channel: 128 channels x 32 tokens), warp 1
+// its values (32 tokens x 4 channel groups).  Each warp first stages its raw
+// 32-row input tile in shared memory with cp.async (rows 16-byte chunked;
+// the value tile's chunks XOR-swizzled so that the group reads below are
+// bank-conflict free), then:
+//   keys:   lane l owns channels 8*(l%16) .. +7 of the rows of parity l/16;
+//           the two parities' min/max meet in one shuffle;
+//   values: lane l owns, in round rr, the whole 32-channel group l%4 of row
+//           8*rr + l/4, so min, max and the scale are computed once per group.
 template <int BITS, int DT>
 __global__ void __launch_bounds__(64)
 quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
                         const void* __restrict__ vin, int T, int nq_k, int nq_v) {
   constexpr int L = (1 << BITS) - 1;
-  constexpr int RB = kHeadDim * BITS / 8;  // packed bytes per token row
-  constexpr int LB = BITS;                 // packed bytes of a lane's 8 channels
-  __shared__ __align__(16) uint8_t s_codes[2][32 * RB];
-  __shared__ __align__(16) __half s_sz[32][8];  // V rows: scale[4], zero[4]
+  constexpr int RB = kHeadDim * BITS / 8;          // packed bytes per token row
+  constexpr int EB = DT == kF32 ? 4 : 2;           // input bytes per element
+  constexpr int CPR = kHeadDim * EB / 16;          // 16-byte chunks per input row
+  constexpr int CPG = CPR / 4;                     // chunks per 32-channel group
+  constexpr int CPE = EB / 2;                      // chunks per 8 elements
+  __shared__ __align__(16) uint4 s_in_all[2][32 * CPR];
+  __shared__ __align__(16) uint8_t s_codes_all[2][32 * RB];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4* s_in = s_in_all[warp];
+  uint8_t* s_codes = s_codes_all[warp];
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
-  const int cl = lane & 15, par = lane >> 4;
-  const int c8 = cl * 8;
-  const void* src = warp == 0 ? kin : vin;
+  const int rows = min(32, T - t0);
 
-  __half2 x[16][4];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const int t = t0 + 2 * k + par;
-    if (t < T) {
-      load8<DT>(src, (unit * T + t) * kHeadDim + c8, x[k]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) x[k][i] = __float2half2_rn(0.0f);
+  // value-tile swizzle (16-bit inputs): chunk j of group g of row r sits at
+  // 4g + (j ^ ((g >> 1) | ((r & 1) << 1))), so the 8 lanes of a shared-memory
+  // phase (rows r, r+1; groups 0..3) hit distinct 16-byte bank slots.  fp32
+  // rows (two chunks per 8 elements) are left unswizzled.
+  auto vswz = [](int r, int c) {
+    if (CPG != 4) return c;
+    const int g = c >> 2, j = c & 3;
+    return 4 * g + (j ^ ((g >> 1) | ((r & 1) << 1)));
+  };
+
+  {
+    const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * T + t0) * (long)(kHeadDim * EB);
+    for (int i = lane; i < rows * CPR; i += 32) {
+      const int r = i / CPR, c = i % CPR;
+      cp_async16(&s_in[r * CPR + (warp == 0 ? c : vswz(r, c))], src + 16L * i);
     }
+    asm volatile("cp.async.commit_group;");
+    asm volatile("cp.async.wait_group 0;");
+    __syncwarp();
   }
 
   if (warp == 0) {
+    // ---------------- keys ----------------
+    const int cl = lane & 15, par = lane >> 4;
+    const int c8 = cl * 8;
     if (t0 + 32 <= nq_k) {
-      // ---- per-channel key group: min/max over 32 tokens ----
-      __half2 mn[4], mx[4];
+      __half2 mn[4], mx[4], x[4];
+      smem8<DT>(&s_in[par * CPR + cl * CPE], x);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mn[i] = mx[i] = x[0][i];
+      for (int i = 0; i < 4; ++i) mn[i] = mx[i] = x[i];
 #pragma unroll
-      for (int k = 1; k < 16; ++k)
+      for (int k = 1; k < 16; ++k) {
+        smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          mn[i] = __hmin2(mn[i], x[k][i]);
-          mx[i] = __hmax2(mx[i], x[k][i]);
+          mn[i] = __hmin2(mn[i], x[i]);
+          mx[i] = __hmax2(mx[i], x[i]);
         }
+      }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {  // the other token parity
         mn[i] = __hmin2(mn[i], __shfl_xor_sync(kFull, mn[i], 16));
         mx[i] = __hmax2(mx[i], __shfl_xor_sync(kFull, mx[i], 16));
       }
-      GroupParams p[8];
+      GroupParams gp[8];
+      float inv[8], nzi[8], zf[8], sf[8];
+      bool safe = true;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        p[2 * i] = group_params(__low2float(mn[i]), __low2float(mx[i]), L);
-        p[2 * i + 1] = group_params(__high2float(mn[i]), __high2float(mx[i]), L);
+        gp[2 * i] = group_params(__low2float(mn[i]), __low2float(mx[i]), L);
+        gp[2 * i + 1] = group_params(__high2float(mn[i]), __high2float(mx[i]), L);
       }
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        uint32_t packed = 0;
+      for (int e = 0; e < 8; ++e) {
+        const FastParams f = fast_params(gp[e]);
+        inv[e] = f.inv;
+        nzi[e] = f.nzi;
+        zf[e] = gp[e].z;
+        sf[e] = gp[e].s;
+        safe = safe && f.safe;
+      }
+      constexpr uint32_t C = magic_sum(8, BITS);
+      if (safe) {
+#pragma unroll 4
+        for (int k = 0; k < 16; ++k) {
+          smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
+          uint32_t acc = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(x[k][i]);
-          packed |= encode(f.x, p[2 * i], L) << (BITS * (2 * i));
-          packed |= encode(f.y, p[2 * i + 1], L) << (BITS * (2 * i + 1));
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(x[i]);
+            acc += fast_bits(f.x, inv[2 * i], nzi[2 * i], zf[2 * i], sf[2 * i]) << (BITS * (2 * i));
+            acc += fast_bits(f.y, inv[2 * i + 1], nzi[2 * i + 1], zf[2 * i + 1], sf[2 * i + 1])
+                   << (BITS * (2 * i + 1));
+          }
+          acc -= C;
+          uint8_t* dst = &s_codes[(2 * k + par) * RB + cl * BITS];
+          if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)acc;
+          else *reinterpret_cast<uint32_t*>(dst) = acc;
         }
-        uint8_t* dst = &s_codes[0][(2 * k + par) * RB + cl * LB];
-        if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-        else *reinterpret_cast<uint32_t*>(dst) = packed;
+      } else {
+        // a channel group outside the fast path's range: exact division
+        for (int k = 0; k < 16; ++k) {
+          smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
+          const uint32_t acc = exact_key_slice<BITS>(h2x4_bits(x), zf, sf);
+          uint8_t* dst = &s_codes[(2 * k + par) * RB + cl * BITS];
+          if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)acc;
+          else *reinterpret_cast<uint32_t*>(dst) = acc;
+        }
       }
       __syncwarp();
       uint4* gdst = reinterpret_cast<uint4*>(cv.codes_k + (unit * cv.Tcap + t0) * RB);
-      const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes[0]);
+      const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
 #pragma unroll
       for (int i = lane; i < 32 * RB / 16; i += 32) gdst[i] = ssrc[i];
       if (par == 0) {
         const long so = (unit * (cv.Tcap / kGroup) + chunk) * kHeadDim + c8;
         *reinterpret_cast<uint4*>(cv.scale_k + so) =
-            make_uint4(pack_halves(p[0].sh, p[1].sh), pack_halves(p[2].sh, p[3].sh),
-                       pack_halves(p[4].sh, p[5].sh), pack_halves(p[6].sh, p[7].sh));
+            make_uint4(pack_halves(gp[0].sh, gp[1].sh), pack_halves(gp[2].sh, gp[3].sh),
+                       pack_halves(gp[4].sh, gp[5].sh), pack_halves(gp[6].sh, gp[7].sh));
         *reinterpret_cast<uint4*>(cv.zero_k + so) =
-            make_uint4(pack_halves(p[0].zh, p[1].zh), pack_halves(p[2].zh, p[3].zh),
-                       pack_halves(p[4].zh, p[5].zh), pack_halves(p[6].zh, p[7].zh));
+            make_uint4(pack_halves(gp[0].zh, gp[1].zh), pack_halves(gp[2].zh, gp[3].zh),
+                       pack_halves(gp[4].zh, gp[5].zh), pack_halves(gp[6].zh, gp[7].zh));
       }
     } else {
       // keys of a chunk that is not a whole quantized group stay fp16
-#pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int t = t0 + 2 * k + par;
-        if (t >= nq_k && t < T)
-          *reinterpret_cast<uint4*>(cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + c8) =
-              h2x4_bits(x[k]);
+        if (t >= nq_k && t < T) {
+          __half2 x[4];
+          smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
+          *reinterpret_cast<uint4*>(cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + c8) = h2x4_bits(x);
+        }
       }
     }
   } else {
-    // ---- per-token value groups: 4 lanes x 8 channels = 32 channels ----
+    // ---------------- values ----------------
+    const int g = lane & 3, tl = lane >> 2;
+    constexpr int CPW = 32 / BITS;  // codes per 32-bit word
+    constexpr uint32_t C = magic_sum(CPW, BITS);
+#pragma unroll 1
+    for (int rr = 0; rr < 4; ++rr) {
+      const int row = 8 * rr + tl;
+      const int t = t0 + row;
+      if (t >= T) continue;
+      __half2 x[4][4];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const int t = t0 + 2 * k + par;
-      const __half2 a = __hmin2(__hmin2(x[k][0], x[k][1]), __hmin2(x[k][2], x[k][3]));
-      const __half2 c = __hmax2(__hmax2(x[k][0], x[k][1]), __hmax2(x[k][2], x[k][3]));
-      __half2 mm = __halves2half2(__hmin(__low2half(a), __high2half(a)),
-                                  __hmax(__low2half(c), __high2half(c)));
-#pragma unroll
-      for (int off = 1; off <= 2; off <<= 1) {
-        const __half2 o = __shfl_xor_sync(kFull, mm, off);
-        mm = __halves2half2(__hmin(__low2half(mm), __low2half(o)),
-                            __hmax(__high2half(mm), __high2half(o)));
-      }
+      for (int j = 0; j < 4; ++j) smem8<DT>(&s_in[row * CPR + vswz(row, g * CPG + j * CPE)], x[j]);
       if (t < nq_v) {
-        const GroupParams p = group_params(__low2float(mm), __high2float(mm), L);
-        uint32_t packed = 0;
+        __half2 mn = x[0][0], mx = x[0][0];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = __half22float2(x[k][i]);
-          packed |= encode(f.x, p, L) << (BITS * (2 * i));
-          packed |= encode(f.y, p, L) << (BITS * (2 * i + 1));
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            mn = __hmin2(mn, x[j][i]);
+            mx = __hmax2(mx, x[j][i]);
+          }
+        const GroupParams p = group_params(fminf(__low2float(mn), __high2float(mn)),
+                                           fmaxf(__low2float(mx), __high2float(mx)), L);
+        const FastParams f = fast_params(p);
+        uint32_t words[BITS];
+        if (f.safe) {
+#pragma unroll
+          for (int w = 0; w < BITS; ++w) {
+            uint32_t acc = 0;
+#pragma unroll
+            for (int e2 = 0; e2 < CPW / 2; ++e2) {
+              const int e = w * CPW + 2 * e2;  // channel within the group
+              const float2 fv = __half22float2(x[e >> 3][(e & 7) >> 1]);
+              acc += fast_bits(fv.x, f.inv, f.nzi, p.z, p.s) << (BITS * (2 * e2));
+              acc += fast_bits(fv.y, f.inv, f.nzi, p.z, p.s) << (BITS * (2 * e2 + 1));
+            }
+            words[w] = acc - C;
+          }
+        } else {  // outside the fast path's range: exact division
+          uint32_t xw[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xw[4 * j + i] = h2_bits(x[j][i]);
+          exact_value_group<BITS>(xw, p.z, p.s, words);
         }
-        // this lane's 8 channels are the units 2*cl and 2*cl + 1
-        uint8_t* row = &s_codes[1][(2 * k + par) * RB];
-        if constexpr (BITS == 2) {
-          row[v_unit_pos(2 * cl)] = (uint8_t)packed;
-          row[v_unit_pos(2 * cl + 1)] = (uint8_t)(packed >> 8);
-        } else {
-          reinterpret_cast<uint16_t*>(row)[v_unit_pos(2 * cl)] = (uint16_t)packed;
-          reinterpret_cast<uint16_t*>(row)[v_unit_pos(2 * cl + 1)] = (uint16_t)(packed >> 16);
-        }
-        if ((lane & 3) == 0) {
-          s_sz[2 * k + par][cl >> 2] = p.sh;
-          s_sz[2 * k + par][4 + (cl >> 2)] = p.zh;
-        }
-      } else if (t < T) {
-        *reinterpret_cast<uint4*>(cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + c8) =
-            h2x4_bits(x[k]);
+        store_value_units<BITS>(&s_codes[row * RB], g, words);
+        const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup) + g;
+        cv.scale_v[so] = p.sh;
+        cv.zero_v[so] = p.zh;
+      } else {
+        __half* dst = cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 32 * g;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(dst + 8 * j) = h2x4_bits(x[j]);
       }
     }
     __syncwarp();
     const int nrows = min(max(nq_v - t0, 0), 32);
-    if (nrows > 0) {
-      uint4* gdst = reinterpret_cast<uint4*>(cv.codes_v + (unit * cv.Tcap + t0) * RB);
-      const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes[1]);
-      for (int i = lane; i < nrows * RB / 16; i += 32) gdst[i] = ssrc[i];
-      if (lane < nrows) {
-        const long so = (unit * cv.Tcap + t0 + lane) * (kHeadDim / kGroup);
-        *reinterpret_cast<uint2*>(cv.scale_v + so) = *reinterpret_cast<const uint2*>(&s_sz[lane][0]);
-        *reinterpret_cast<uint2*>(cv.zero_v + so) = *reinterpret_cast<const uint2*>(&s_sz[lane][4]);
-      }
-    }
+    uint4* gdst = reinterpret_cast<uint4*>(cv.codes_v + (unit * cv.Tcap + t0) * RB);
+    const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
+    for (int i = lane; i < nrows * RB / 16; i += 32) gdst[i] = ssrc[i];
   }
 }
 
