@@ -19,28 +19,27 @@ __device__ __forceinline__ int v_unit_pos(int unit) { return 4 * (unit & 7) + (u
 
 
 // ---------------------------------------------------------------------------
-// Prefill fast path.
+// Prefill quantizer arithmetic.
 //
-// For a group with zero point z and stored fp16 scale s, the code of x is
-// computed as rint(y') with y' = fma(x, inv, nzi), inv ~ 1/s (rcp.approx,
-// relative error below 2^-22) and nzi = fl(-z * inv).  When |z| * inv <= 64
-// and s is an fp16 normal number, |y' - (x - z)/s| < 2^-17.4 (the rounding of
-// nzi contributes at most 2^-18, the reciprocal 2^-19 for y < 16, the fma
-// 2^-20) and the IEEE quotient fl(fl(x - z) / s) is within 2^-19 of
-// (x - z)/s, so both round to the same integer unless y' lies within 2^-16 of
-// a half-integer; such elements take tie_code, which decides the IEEE
-// rounding exactly without a division.  Groups outside the safe range use
-// the exact division throughout.  In the safe range y' < L + 2^-10, so the
-// clamp is never needed.
+// The code of x is rint(fl(fl(x - z) / s)) with the stored fp16 scale s.  The
+// IEEE quotient is obtained without a division instruction by one residual
+// correction of a reciprocal estimate (Markstein's refinement of a quotient):
+// with d = fl(x - z), inv ~ 1/s (rcp.approx, relative error below 2^-22) and
+// y1 = fl(d * inv), the residual r = fma(-y1, s, d) is exact (d - y1*s has at
+// most 13 significant bits), and y2 = fma(r, inv, y1) is the rounding of a
+// value within 2^-44 (relative) of d / s.  d has 24 significant bits and s
+// 11, so d / s is never a rounding midpoint of fp32 and lies at least 2^-35
+// (relative) away from every midpoint; hence y2 = fl(d / s) exactly.  When s
+// is an fp16 normal number, y2 < L + 1/2 (s differs from (max - min)/L by at
+// most 2^-11 relative), so no clamp is needed; groups whose stored scale is an
+// fp16 subnormal use the IEEE division and the clamp.
 //
-// rint(y') is read off t = y' + 1.5 * 2^23, whose bit pattern is
-// 0x4B400000 + rint(y'); the codes of a word are summed as t_bits << shift
+// rint(y2) is read off t = y2 + 1.5 * 2^23, whose bit pattern is
+// 0x4B400000 + rint(y2); the codes of a word are summed as t_bits << shift
 // (mod 2^32) and the constant sum of the 0x4B400000 << shift terms removed.
 
-constexpr float kNearHalfFast = 0.4999847412109375f;  // 0.5 - 2^-16
-
 struct FastParams {
-  float inv, nzi;
+  float inv;
   bool safe;
 };
 
@@ -53,43 +52,16 @@ __device__ __forceinline__ float rcp_approx(float x) {
 __device__ __forceinline__ FastParams fast_params(const GroupParams& p) {
   FastParams f;
   f.inv = rcp_approx(p.s);
-  f.nzi = -p.z * f.inv;
-  f.safe = fabsf(p.z) * f.inv <= 64.0f && p.s >= 6.103515625e-05f;
+  f.safe = p.s >= 6.103515625e-05f;  // fp16 normal
   return f;
 }
 
-// Exact code of an element whose estimate y lies within 2^-16 of k + 1/2.
-// With d = fl(x - z) and h = k + 1/2, s*h is exact (an fp16 scale times a
-// number of at most 5 significant bits) and d is within a factor 2 of it, so
-// e = fma(-s, h, d) = d - s*h exactly (Sterbenz).  The IEEE quotient
-// fl(d / s) equals h exactly when d/s lies in [h - lo, h + hi] (lo = hi =
-// ulp(h)/2, except lo = ulp(h)/4 at h = 1/2; the end points round to h, whose
-// last mantissa bit is 0), is below h when e < -s*lo and above when e > s*hi.
-// rint(fl(d/s)) follows: k, k + 1, or the even one of them for the tie.
-__device__ __noinline__ uint32_t tie_code(float x, float z, float s, float y) {
-  const float k = floorf(y);
-  const float h = k + 0.5f;
+__device__ __forceinline__ uint32_t code_bits(float x, float z, float s, float inv) {
   const float d = __fsub_rn(x, z);
-  const float e = fmaf(-s, h, d);
-  const float half_ulp = __uint_as_float(((__float_as_uint(h) >> 23) - 24u) << 23);  // ulp(h) / 2
-  const float lo = (k == 0.0f ? 0.5f : 1.0f) * half_ulp * s;
-  const float hi = half_ulp * s;
-  const int ki = (int)k;
-  int q;
-  if (e < -lo) q = ki;
-  else if (e > hi) q = ki + 1;
-  else q = (ki & 1) ? ki + 1 : ki;
-  return kRoundMagicBits + (uint32_t)q;
-}
-
-// Bits of t = y' + 1.5 * 2^23 for the code of x: the fast estimate, or the
-// exact decision when y' is within 2^-16 of a half-integer.
-__device__ __forceinline__ uint32_t fast_bits(float x, float inv, float nzi, float z, float s) {
-  const float y = fmaf(x, inv, nzi);
-  const float t = __fadd_rn(y, kRoundMagic);
-  const float r = __fsub_rn(t, kRoundMagic);
-  if (fabsf(__fsub_rn(y, r)) > kNearHalfFast) return tie_code(x, z, s, y);
-  return __float_as_uint(t);
+  const float y1 = __fmul_rn(d, inv);
+  const float r = fmaf(-y1, s, d);
+  const float y2 = fmaf(r, inv, y1);
+  return __float_as_uint(__fadd_rn(y2, kRoundMagic));
 }
 
 // sum over e < n of (0x4B400000 << (bits * e)) mod 2^32
@@ -270,7 +242,7 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
         mx[i] = __hmax2(mx[i], __shfl_xor_sync(kFull, mx[i], 16));
       }
       GroupParams gp[8];
-      float inv[8], nzi[8], zf[8], sf[8];
+      float inv[8], zf[8], sf[8];
       bool safe = true;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -281,7 +253,6 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
       for (int e = 0; e < 8; ++e) {
         const FastParams f = fast_params(gp[e]);
         inv[e] = f.inv;
-        nzi[e] = f.nzi;
         zf[e] = gp[e].z;
         sf[e] = gp[e].s;
         safe = safe && f.safe;
@@ -295,9 +266,8 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 f = __half22float2(x[i]);
-            acc += fast_bits(f.x, inv[2 * i], nzi[2 * i], zf[2 * i], sf[2 * i]) << (BITS * (2 * i));
-            acc += fast_bits(f.y, inv[2 * i + 1], nzi[2 * i + 1], zf[2 * i + 1], sf[2 * i + 1])
-                   << (BITS * (2 * i + 1));
+            acc += code_bits(f.x, zf[2 * i], sf[2 * i], inv[2 * i]) << (BITS * (2 * i));
+            acc += code_bits(f.y, zf[2 * i + 1], sf[2 * i + 1], inv[2 * i + 1]) << (BITS * (2 * i + 1));
           }
           acc -= C;
           uint8_t* dst = &s_codes[(2 * k + par) * RB + cl * BITS];
@@ -305,7 +275,7 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
           else *reinterpret_cast<uint32_t*>(dst) = acc;
         }
       } else {
-        // a channel group outside the fast path's range: exact division
+        // a channel group with an fp16-subnormal scale: IEEE division + clamp
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
           const uint32_t acc = exact_key_slice<BITS>(h2x4_bits(x), zf, sf);
@@ -373,12 +343,12 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
             for (int e2 = 0; e2 < CPW / 2; ++e2) {
               const int e = w * CPW + 2 * e2;  // channel within the group
               const float2 fv = __half22float2(x[e >> 3][(e & 7) >> 1]);
-              acc += fast_bits(fv.x, f.inv, f.nzi, p.z, p.s) << (BITS * (2 * e2));
-              acc += fast_bits(fv.y, f.inv, f.nzi, p.z, p.s) << (BITS * (2 * e2 + 1));
+              acc += code_bits(fv.x, p.z, p.s, f.inv) << (BITS * (2 * e2));
+              acc += code_bits(fv.y, p.z, p.s, f.inv) << (BITS * (2 * e2 + 1));
             }
             words[w] = acc - C;
           }
-        } else {  // outside the fast path's range: exact division
+        } else {  // fp16-subnormal scale: IEEE division + clamp
           uint32_t xw[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j)

@@ -87,6 +87,25 @@ def test_prefill_extreme_values():
         T.compare_state(T.gpu_state(g), o.export(), 256, 32, 32)
 
 
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_prefill_tie_heavy_lattices(bits, dtype):
+    """Inputs on coarse dyadic lattices make (x - z)/s land exactly on, or
+    within a few ulps of, half-integers for many elements: every such
+    rounding decision must match the oracle's IEEE division bit for bit."""
+    rng = np.random.default_rng(77 + bits)
+    shape = (2, 2, 320, 128)
+    step = 2.0 ** rng.integers(-6, 3, size=(2, 2, 1, 128))
+    k = rng.integers(-8, 9, size=shape) * step / 2
+    v = rng.integers(-8, 9, size=shape) * (2.0 ** rng.integers(-6, 3, size=(2, 2, 320, 1))) / 4
+    k[:, :, ::7] *= 3.0      # ranges that give scales like 2.5 or 3.5
+    v[:, :, 1::5] += 0.125
+    wl = W.synthetic("ties", B=2, Hq=4, Hkv=2, T=320, bits=bits, dtype=dtype, seed=5)
+    wl.k, wl.v = W.cast(k, dtype), W.cast(v, dtype)
+    g, o = run_prefill(wl)
+    T.compare_state(T.gpu_state(g), o.export(), 320, 32, 32)
+
+
 # ---------------------------------------------------------------- append
 
 @pytest.mark.parametrize("bits", [2, 4])
