@@ -23,6 +23,8 @@
 // query heads per MMA, and the sum hi + lo recovers x to about 2^-22.
 #include <cuda_bf16.h>
 
+#include <cstddef>
+
 #include "kivi_internal.cuh"
 
 namespace kivi {
@@ -363,11 +365,16 @@ __device__ __forceinline__ uint32_t ext8(uint32_t w, uint32_t w_sh10) {
 
 __host__ __device__ constexpr int pow4_exp(int i) { return i <= 4 ? i : i - 5; }
 
-// Stage one packed tile (keys, values, scales, zeros: 192 chunks of 16 B,
-// six per lane) into the warp's stage buffer, whose layout follows the chunk
-// order.
-__device__ __forceinline__ void issue_tile(const CacheView& cv, long unit, int tile, TileStage& st,
-                                           int lane) {
+// Per-lane cp.async sources and destinations of one packed tile (keys,
+// values, scales, zeros: 192 chunks of 16 B, six per lane).  The sources of
+// the next tile of the same warp are the current ones plus a fixed stride.
+struct TileCopy {
+  const char* src[6];
+  uint32_t dst[6];  // shared-memory offsets inside a TileStage
+};
+
+__device__ __forceinline__ TileCopy tile_copy_plan(const CacheView& cv, long unit, int tile, int lane) {
+  TileCopy tc;
   const long row0 = unit * cv.Tcap + (long)tile * 32;
   const char* kc = reinterpret_cast<const char*>(cv.codes_k + row0 * 32);
   const char* vc = reinterpret_cast<const char*>(cv.codes_v + row0 * 32);
@@ -376,15 +383,40 @@ __device__ __forceinline__ void issue_tile(const CacheView& cv, long unit, int t
   const char* zk = reinterpret_cast<const char*>(cv.zero_k + g0);
   const char* sv = reinterpret_cast<const char*>(cv.scale_v + row0 * (kHeadDim / kGroup));
   const char* zv = reinterpret_cast<const char*>(cv.zero_v + row0 * (kHeadDim / kGroup));
-  cp_async16(&st.kc[4 * lane], kc + 16 * lane);
-  cp_async16(&st.kc[4 * (32 + lane)], kc + 16 * (32 + lane));
-  // value chunk c = 2 * row + half goes to row * 12 + 4 * half words
-  cp_async16(&st.vc[(lane >> 1) * 12 + 4 * (lane & 1)], vc + 16 * lane);
-  cp_async16(&st.vc[(16 + (lane >> 1)) * 12 + 4 * (lane & 1)], vc + 16 * (32 + lane));
   const int c = lane & 15;
-  cp_async16(lane < 16 ? &st.sk[kpad(4 * c)] : &st.zk[kpad(4 * c)],
-             lane < 16 ? sk + 16 * c : zk + 16 * c);
-  cp_async16(lane < 16 ? &st.sv[4 * c] : &st.zv[4 * c], lane < 16 ? sv + 16 * c : zv + 16 * c);
+  tc.src[0] = kc + 16 * lane;
+  tc.src[1] = kc + 16 * (32 + lane);
+  tc.src[2] = vc + 16 * lane;
+  tc.src[3] = vc + 16 * (32 + lane);
+  tc.src[4] = lane < 16 ? sk + 16 * c : zk + 16 * c;
+  tc.src[5] = lane < 16 ? sv + 16 * c : zv + 16 * c;
+  tc.dst[0] = (uint32_t)offsetof(TileStage, kc) + 16 * lane;
+  tc.dst[1] = (uint32_t)offsetof(TileStage, kc) + 16 * (32 + lane);
+  // value chunk 2*row + half goes to row * 48 + 16 * half bytes
+  tc.dst[2] = (uint32_t)offsetof(TileStage, vc) + (lane >> 1) * 48 + 16 * (lane & 1);
+  tc.dst[3] = (uint32_t)offsetof(TileStage, vc) + (16 + (lane >> 1)) * 48 + 16 * (lane & 1);
+  tc.dst[4] = (uint32_t)(lane < 16 ? offsetof(TileStage, sk) : offsetof(TileStage, zk)) + 4 * kpad(4 * c);
+  tc.dst[5] = (uint32_t)(lane < 16 ? offsetof(TileStage, sv) : offsetof(TileStage, zv)) + 16 * c;
+  return tc;
+}
+
+// Byte strides of the six sources when a warp moves on by kWarps tiles.
+__device__ __forceinline__ void tile_copy_advance(TileCopy& tc) {
+  constexpr long kCodes = (long)kWarps * 32 * 32;           // 32 rows of 32 B
+  constexpr long kKGroup = (long)kWarps * kHeadDim * 2;      // one group of fp16 [128]
+  constexpr long kVRows = (long)kWarps * 32 * (kHeadDim / kGroup) * 2;
+  tc.src[0] += kCodes;
+  tc.src[1] += kCodes;
+  tc.src[2] += kCodes;
+  tc.src[3] += kCodes;
+  tc.src[4] += kKGroup;
+  tc.src[5] += kVRows;
+}
+
+__device__ __forceinline__ void issue_tile(const TileCopy& tc, TileStage& st) {
+  char* base = reinterpret_cast<char*>(&st);
+#pragma unroll
+  for (int i = 0; i < 6; ++i) cp_async16(base + tc.dst[i], tc.src[i]);
 }
 
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
@@ -591,7 +623,7 @@ __device__ void build_q_tables(MmaSmem& s, const AttnArgs& a, int b, int j0, int
 
 // grid (splits, H * head_chunks, B), 128 threads.
 template <int BITS>
-__global__ void __launch_bounds__(128, 4) attn_kernel(CacheView cv, AttnArgs a) {
+__global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem)
   SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
@@ -643,11 +675,20 @@ __global__ void __launch_bounds__(128, 4) attn_kernel(CacheView cv, AttnArgs a) 
   } else {
     // ---- tensor cores: packed tiles [(s-1)*chunk, min(t_tail, s*chunk)) ----
     const int g = lane >> 2, tig = lane & 3;
-    build_q_tables(sm.mma, a, b, j0, nh);
-    __syncthreads();
     const int tile0 = (s - 1) * a.chunk / 32;
     const int tile1 = min(a.t_tail, s * a.chunk) / 32;
     const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
+    TileStage* stages = sm.mma.st[warp];
+    // start this warp's first tile copies before the CTA builds its q tables
+    TileCopy tc = tile_copy_plan(cv, unit, tile0 + warp, lane);
+#pragma unroll
+    for (int k = 0; k < kStages - 1; ++k) {
+      if (k < n_mine) issue_tile(tc, stages[k]);
+      cp_async_commit();
+      tile_copy_advance(tc);
+    }
+    build_q_tables(sm.mma, a, b, j0, nh);
+    __syncthreads();
     float O[8][4], Z[4], m_run = -INFINITY, lsum = 0.0f;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
@@ -655,19 +696,17 @@ __global__ void __launch_bounds__(128, 4) attn_kernel(CacheView cv, AttnArgs a) 
       for (int i = 0; i < 4; ++i) O[mt][i] = 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) Z[i] = 0.0f;
-#pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) {
-      if (k < n_mine) issue_tile(cv, unit, tile0 + warp + k * kWarps, sm.mma.st[warp][k], lane);
-      cp_async_commit();
-    }
+    int st_cur = 0, st_next = kStages - 1;
     for (int k = 0; k < n_mine; ++k) {
-      const int kn = k + kStages - 1;
-      if (kn < n_mine) issue_tile(cv, unit, tile0 + warp + kn * kWarps, sm.mma.st[warp][kn % kStages], lane);
+      if (k + kStages - 1 < n_mine) issue_tile(tc, stages[st_next]);
       cp_async_commit();
+      tile_copy_advance(tc);
       cp_async_wait<kStages - 1>();
       __syncwarp();
-      mma_tile(sm.mma, sm.mma.st[warp][k % kStages], g, tig, a.scale_log2, m_run, lsum, O, Z);
+      mma_tile(sm.mma, stages[st_cur], g, tig, a.scale_log2, m_run, lsum, O, Z);
       __syncwarp();
+      st_cur = st_cur == kStages - 1 ? 0 : st_cur + 1;
+      st_next = st_next == kStages - 1 ? 0 : st_next + 1;
     }
     cp_async_wait<0>();
     __syncwarp();

@@ -74,10 +74,11 @@ long attention_units(const kivi_config& c) {
   return (long)c.batch * c.n_kv_heads * ((grp + 3) / 4);
 }
 
-// Upper bound on the packed-tile splits: about three CTAs per SM of a GB300.
+// Upper bound on the packed-tile splits: the tail split plus the tile splits
+// of every unit fit one wave of kivi::kAttnCtasPerSm CTAs per SM of a GB300.
 int max_tile_splits(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (3L * kivi::kTargetSMs + u - 1) / u;
+  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u - 1;
   if (s < 1) s = 1;
   const long by_len = (c.max_tokens + 31) / 32;
   return (int)(s < by_len ? s : by_len);

@@ -9,7 +9,8 @@ namespace kivi {
 
 constexpr int kHeadDim = 128;  // D supported by the kernels
 constexpr int kGroup = 32;     // G supported by the kernels
-constexpr int kTargetSMs = 152;  // GB300 SM count used by the split policy
+constexpr int kTargetSMs = 152;    // GB300 SM count used by the split policy
+constexpr int kAttnCtasPerSm = 3;  // attention CTAs resident per SM (registers)
 
 // Device view of one cache: the eight buffers plus its shape.
 struct CacheView {

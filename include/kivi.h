@@ -151,8 +151,8 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
 /* Override the number of context splits (0 = automatic).  Split 0 always
  * takes the tail of the context that is still fp16 (plus the partial value
  * group before it); the other splits share the packed 32-token tiles.  The
- * automatic choice aims at about three CTAs per SM of a 152-SM GB300 and at
- * least 256 tokens per split.  The value is clamped to the workspace bound
+ * automatic choice keeps the whole grid within one wave of three CTAs per SM
+ * of a 152-SM GB300, with at least 256 tokens per split.  The value is clamped to the workspace bound
  * and to one split per 32-token tile. */
 kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 
