@@ -254,7 +254,7 @@ def run_gpu(args):
         "gpu_launches": 2 * K,
     }
     achieved = float(att_b.mean() / t_att.mean() / 1e9)
-    result["roofline"] = {"kernel": "attn_split_kernel (fused split-combine)", "bound": "hbm",
+    result["roofline"] = {"kernel": "attn_kernel<2> (fused split-combine)", "bound": "hbm",
                           "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                           "frac": round(achieved / peak, 4), "traffic": kernel_traffic(),
                           "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
