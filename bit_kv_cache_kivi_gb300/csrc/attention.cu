@@ -7,20 +7,27 @@
 //
 // The context is split along the tokens (flash-decoding).  Split 0 of every
 // (batch, kv-head, head chunk) takes the tail [t_tail, l) -- the tokens whose
-// keys or values are still fp16 in the residual rings, plus the partial
-// value group before them -- on CUDA cores.  Splits 1.. take the fully
-// packed 32-token tiles [0, t_tail).  The CTA that finishes last for a
-// (batch, kv-head, head chunk) merges the partial (max, sum, output) triples,
-// in the same launch; nothing ever waits.
+// keys or values are still fp16 in the residual rings, plus the partial value
+// group before them -- on CUDA cores.  Splits 1.. take the fully packed
+// 32-token tiles [0, t_tail).  Partials are merged in the same launch: the
+// CTA that finishes last in a group of up to kMergeGroup splits merges the
+// group, and with more than one group the last group merges the groups;
+// nothing ever waits on another CTA.
 //
 // Packed tiles at 2 bits run on the tensor cores (mma.sync m16n8k16, fp16
-// operands, fp32 accumulation):
+// operands, fp32 accumulation).  Each warp streams its tiles through its own
+// ring of staged tiles (one lane issues a bulk copy per array and tile,
+// completion on an mbarrier) and keeps an online softmax per head:
 //   scores  S[t, j] = sum_d c_td (q_jd s_d) + beta_j, beta_j = sum_d q_jd z_d
 //   output  O[d, j] = sum_t c_td (p_jt s_t,g(d)) + sum_t p_jt z_t,g(d)
-// The codes c are small integers, exact in fp16.  The fp32 factors q*s and
-// p*s enter as an fp16 hi/lo pair (hi = fp16(x), lo = fp16(x - hi)), which
-// fill the 8 columns of the n=8 operand as (head, hi) and (head, lo): four
-// query heads per MMA, and the sum hi + lo recovers x to about 2^-22.
+// The codes c enter the MMA as fp16 subnormals c * 4^i * 2^-24 (the masked
+// code bits are the whole encoding); the fp32 factors q*s and p*s enter as an
+// fp16 hi/lo pair (hi = fp16(x), lo = fp16(x - hi)) in the 8 columns of the
+// n=8 operand as (head, hi) and (head, lo): four query heads per MMA, and the
+// sum hi + lo recovers x to about 2^-22.  Each query head is first scaled by a
+// power of two so that max |q| < 1, and a head's running max trails its
+// scores by at most 0.5 (log2 units), so neither q*s nor p*s can overflow
+// fp16.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -32,8 +39,10 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
-constexpr int kNH = 4;      // query heads per CTA (one "head chunk")
-constexpr int kStages = 3;  // cp.async pipeline depth of each warp (tensor-core path)
+constexpr int kNH = kHeadChunk;  // query heads per CTA (one "head chunk")
+// A bounded wait for staged data gives up after this long (the copies take
+// microseconds); the CTA then records the failure in the status word.
+constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -74,15 +83,6 @@ __device__ __forceinline__ void halves4(uint2 u, float (&f)[4]) {
   f[3] = h_hi(u.y);
 }
 
-__device__ __forceinline__ uint32_t h2u(__half2 h) {
-  return (uint32_t)__half_as_ushort(__low2half(h)) | ((uint32_t)__half_as_ushort(__high2half(h)) << 16);
-}
-
-__device__ __forceinline__ __half2 u2h(uint32_t u) {
-  return __halves2half2(__ushort_as_half((unsigned short)(u & 0xffffu)),
-                        __ushort_as_half((unsigned short)(u >> 16)));
-}
-
 // fp16x2 arithmetic on raw 32-bit registers (round to nearest even).
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -116,60 +116,99 @@ __device__ __forceinline__ uint32_t split_mul(uint32_t xa, uint32_t xb, uint32_t
 // +3 sits at unit position 4*w + gp (units are bits/2 bytes).
 __device__ __forceinline__ int v_unit_pos(int unit) { return 4 * (unit & 7) + (unit >> 3); }
 
+// v[i] for a lane-dependent i without dynamic register indexing.
+__device__ __forceinline__ float pick4(const float (&v)[4], int i) {
+  float r = v[0];
+  r = i == 1 ? v[1] : r;
+  r = i == 2 ? v[2] : r;
+  r = i == 3 ? v[3] : r;
+  return r;
+}
+
 // ---------------------------------------------------------------------------
 // Shared memory.
 
-struct V1Smem {                           // CUDA-core path (tail, and 4-bit tiles)
+struct V1Smem {                           // CUDA-core path (4-bit packed tiles)
   float q[kNH][kHeadDim];                 // q * scale * log2(e)
-  // per warp: q * sK of its key group ([kNH][128] floats), or 32 fp16
-  // residual rows (256 B each, 16-byte chunks XOR-swizzled by row), or the
-  // merge area at the end
+  // per warp, 32 rows of 256 B: q * sK of the tile's key group ([kNH][128]
+  // floats), then fp16 residual rows (16-byte chunks XOR-swizzled by row) and
+  // packed value rows (codes at the row start, scale[4] and zero[4] at byte
+  // 64); the merge area at the end
   uint4 wbuf[kWarps][32 * 16];
-  uint8_t vc[kWarps][32 * 64];            // staged value codes (up to 4 bits)
-  __half vsz[kWarps][32][8];              // staged value scale[4], zero[4] per row
 };
-
-// One packed 32-token tile at 2 bits.  Padding keeps the lane access
-// patterns of the tensor-core path free of shared-memory bank conflicts:
-// value rows are 48 B apart, and the key scales / zeros of channels 64..127
-// start 16 B after those of channels 0..63.
-struct TileStage {
-  uint32_t kc[32 * 8];                    // key codes: 32 rows x 32 B
-  uint32_t vc[32 * 12];                   // value codes: 32 rows x 32 B, 48 B stride
-  uint32_t sk[68], zk[68];                // 128 fp16 key scales / zeros (+ 4-word gap)
-  uint32_t sv[64], zv[64];                // [32 tokens][4 groups] fp16
-};
-
-// word index of key scale / zero word w (0..63) in the padded layout
-__device__ __forceinline__ int kpad(int w) { return w + ((w >> 5) << 2); }
 
 // q tables in MMA fragment order.  Lane (g, tig) reads the 16 words of
 // column g (head g >> 1, part g & 1) for its tig, as four 16-byte quarters;
 // the layout [quarter][column][tig] spreads the 8 lanes of a shared-memory
 // phase over distinct banks.  Word w of (column, tig) holds channels
-// (16m + i, 16m + i + 8) with ks = w >> 1, m = 2*tig + (ks >> 2),
+// (16m + i, 16m + i + 8) with ks = w >> 1, m = tig + 4*(ks >> 2),
 // i = 2*(ks & 3) + (w & 1).
-struct MmaSmem {
-  uint4 qs[3][4][8][4];                   // q * 4^-e(d) as split_mul operands (xa, xb, xbn)
-  uint4 qb[4][8][4];                      // q (unscaled) hi / lo
-  TileStage st[kWarps][kStages];
+//
+// A staged packed tile keeps the cache's own layouts (one bulk copy per
+// array): codes as 32-byte rows, key scales / zeros as fp16 [128], value
+// scales / zeros as fp16 [32 tokens][4 groups].
+struct TileBuf {
+  uint32_t kc[256];                       // key codes
+  uint32_t vc[256];                       // value codes (group-interleaved rows)
+  uint32_t sk[64], zk[64];
+  uint32_t sv[64], zv[64];
+};
+constexpr int kStages = 3;                // tiles in flight per warp
+constexpr uint32_t kTileBytes = sizeof(TileBuf);
+
+struct WarpSmem {
+  TileBuf st[kWarps][kStages];            // per-warp rings of staged tiles
+  uint4 qs[2][4][8][4];                   // q * 4^-e(d) as split_mul operands (xa, xb)
+  uint4 qb[4][8][4];                      // q hi / lo
+  float pbuf[kWarps][kNH][34];            // one tile's weights per warp, token order
+                                          // 8 (t & 3) + 4 (t >> 4) + 2 ((t >> 3) & 1) + ((t >> 2) & 1)
+  float qv[kNH][kHeadDim];                // q, staged for the tables
+  float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
+  int qexp[kNH];                          // E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
+  unsigned long long bar[kWarps][kStages];
+};
+
+// The tail split: up to kTailTok tokens per round, each staged as a 256-byte
+// key row and a 256-byte value row -- an fp16 residual row (16-byte chunks
+// XOR-swizzled by row), or the packed codes at the row start (value rows
+// then carry scale[4] at byte RB and zero[4] at byte RB + 8).
+constexpr int kTailTok = 64;
+struct TailSmem {
+  float q[kNH][kHeadDim];                 // q * scale * log2(e)
+  uint4 krow[kTailTok][16];
+  uint4 vrow[kTailTok][16];
+  uint32_t kg[2][2][64];                  // scale / zero of the round's (at most two) key groups
+  float p[kNH][kTailTok];                 // scores, then weights
+  float mrun[kNH], lrun[kNH], corr[kNH];  // running max / sum, rescale of this round
 };
 
 union SplitSmem {
   V1Smem v1;
-  MmaSmem mma;
+  WarpSmem ws;
+  TailSmem tail;
 };
 
-// Per-warp merge area: [kNH][kHeadDim] floats inside the warp's own buffers,
-// written only after the warp has finished its tiles.
-__device__ __forceinline__ float* merge_area(SplitSmem& sm, int warp, bool mma_path) {
-  return mma_path ? reinterpret_cast<float*>(&sm.mma.st[warp][0])
-                  : reinterpret_cast<float*>(&sm.v1.wbuf[warp][0]);
+enum Path { kPathV1 = 0, kPathMma = 1, kPathTail = 2 };
+
+// Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the warp
+// (CUDA cores) or the CTA (tensor cores, tail, after their last round) is
+// done with.
+__device__ __forceinline__ float* merge_area(SplitSmem& sm, int warp, int path) {
+  if (path == kPathMma) return reinterpret_cast<float*>(&sm.ws.st[warp][0]);
+  if (path == kPathTail) return reinterpret_cast<float*>(&sm.tail.krow[0][0]) + warp * kNH * kHeadDim;
+  return reinterpret_cast<float*>(&sm.v1.wbuf[warp][0]);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+
+__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
@@ -187,6 +226,59 @@ __device__ __forceinline__ void stage_ring_rows(const __half* ring, long unit, i
                ring + (unit * R + (tt0 + r) % R) * kHeadDim + 8 * c);
   }
   cp_async_commit();
+}
+
+// mbarrier + bulk copy (one elected thread issues; the barrier's transaction
+// count completes the phase when every byte has landed).
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the completion of phase `parity` of an mbarrier, for at most
+// kWaitLimitNs.  Returns false on timeout.
+__device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -294,13 +386,16 @@ __device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, 
     __syncwarp();  // the key phase is done with wbuf
     if (max(vrows, r_lo) < r_hi) stage_ring_rows(cv.ring_v, unit, cv.R, tt0, max(vrows, r_lo), r_hi, wbuf, lane);
     {
+      // packed rows r < vrows: codes at the start of wbuf row r, then the
+      // row's value scales and zeros (16 B) at byte 64
+      constexpr int CPR = RB / 16;
       const uint4* gsrc = reinterpret_cast<const uint4*>(cv.codes_v + (unit * cv.Tcap + tt0) * RB);
-      uint4* sdst = reinterpret_cast<uint4*>(s.vc[warp]);
-      for (int i = lane; i < vrows * RB / 16; i += 32) sdst[i] = gsrc[i];
+      for (int i = lane; i < vrows * CPR; i += 32) wbuf[16 * (i / CPR) + (i % CPR)] = gsrc[i];
       if (lane < vrows) {
         const long so = (unit * cv.Tcap + tt0 + lane) * (kHeadDim / kGroup);
-        *reinterpret_cast<uint2*>(&s.vsz[warp][lane][0]) = *reinterpret_cast<const uint2*>(cv.scale_v + so);
-        *reinterpret_cast<uint2*>(&s.vsz[warp][lane][4]) = *reinterpret_cast<const uint2*>(cv.zero_v + so);
+        const uint2 sv2 = *reinterpret_cast<const uint2*>(cv.scale_v + so);
+        const uint2 zv2 = *reinterpret_cast<const uint2*>(cv.zero_v + so);
+        wbuf[16 * lane + 4] = make_uint4(sv2.x, sv2.y, zv2.x, zv2.y);
       }
     }
     cp_async_wait<0>();
@@ -309,11 +404,13 @@ __device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, 
     for (int r = r_lo; r < r_hi; ++r) {
       float vh[4];
       if (r < vrows) {
+        const uint8_t* rowb = reinterpret_cast<const uint8_t*>(&wbuf[16 * r]);
         uint32_t cb;
-        if constexpr (BITS == 2) cb = s.vc[warp][r * RB + vpos];
-        else cb = *reinterpret_cast<const uint16_t*>(&s.vc[warp][r * RB + 2 * vpos]);
-        const float sv = __half2float(s.vsz[warp][r][lane >> 3]);
-        const float zv = __half2float(s.vsz[warp][r][4 + (lane >> 3)]);
+        if constexpr (BITS == 2) cb = rowb[vpos];
+        else cb = *reinterpret_cast<const uint16_t*>(rowb + 2 * vpos);
+        const __half* svz = reinterpret_cast<const __half*>(&wbuf[16 * r + 4]);
+        const float sv = __half2float(svz[lane >> 3]);
+        const float zv = __half2float(svz[4 + (lane >> 3)]);
 #pragma unroll
         for (int i = 0; i < 4; ++i) vh[i] = (float)((cb >> (BITS * i)) & L) * sv + zv;
       } else {
@@ -332,7 +429,179 @@ __device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, 
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core path helpers.
+// The tail split on CUDA cores: tokens [t_tail, l) in rounds of up to
+// kTailTok, each staged in one round of copies (fp16 residual rows, packed
+// rows and the key groups' scales / zeros); then scores with four threads per
+// token (32 channels each), the softmax of a head per warp, and the value
+// sum with one thread per channel.  Keys and values of packed rows are
+// dequantized as fl(fl(c * s) + z), the reconstruction of the notebook
+// "KIVI - 2-bit KV cache quantisation".  Leaves the partial of the whole CTA
+// in warp 0's slots (the other warps' slots empty).
+template <int BITS>
+__device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit, int b,
+                           int j0, int nh, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
+  constexpr int L = (1 << BITS) - 1;
+  constexpr int RB = kHeadDim * BITS / 8;  // packed row bytes
+  constexpr int CPR = RB / 16;             // 16-byte chunks per packed row
+  TailSmem& ts = sm.tail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = tid;  // value phase: this thread's channel
+
+  for (int i = tid; i < kNH * kHeadDim; i += blockDim.x) {
+    const int j = i / kHeadDim, dd = i % kHeadDim;
+    ts.q[j][dd] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + dd, a.q_dtype) * a.scale_log2
+                         : 0.0f;
+  }
+  if (tid < kNH) {
+    ts.mrun[tid] = -INFINITY;
+    ts.lrun[tid] = 0.0f;
+  }
+  float o[kNH] = {0.0f, 0.0f, 0.0f, 0.0f};
+
+  for (int c0 = a.t_tail; c0 < a.l; c0 += kTailTok) {
+    const int n = min(kTailTok, a.l - c0);
+    const int nk = max(0, min(n, a.nq_k - c0));  // rows [0, nk) hold packed keys
+    const int nv = max(0, min(n, a.nq_v - c0));  // rows [0, nv) hold packed values
+    __syncthreads();  // the previous round is done with every buffer
+
+    // ---- stage the round (c0 is a multiple of 32, so its packed keys span
+    //      at most two key groups) ----
+    for (int i = tid; i < n * 16; i += blockDim.x) {
+      const int r = i >> 4, c = i & 15;
+      const long t = c0 + r;
+      if (r < nk) {
+        if (c < CPR) cp_async16(&ts.krow[r][c], cv.codes_k + (unit * cv.Tcap + t) * RB + 16 * c);
+      } else {
+        cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+      }
+      if (r < nv) {
+        if (c < CPR) {
+          cp_async16(&ts.vrow[r][c], cv.codes_v + (unit * cv.Tcap + t) * RB + 16 * c);
+        } else if (c == CPR) {
+          const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup);
+          char* dst = reinterpret_cast<char*>(&ts.vrow[r][c]);
+          cp_async8(dst, cv.scale_v + so);
+          cp_async8(dst + 8, cv.zero_v + so);
+        }
+      } else {
+        cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+      }
+    }
+    const int ngk = (nk + kGroup - 1) / kGroup;
+    for (int i = tid; i < ngk * 32; i += blockDim.x) {
+      const int gi = i >> 5, arr = (i >> 4) & 1, c = i & 15;
+      const long go = (unit * (cv.Tcap / kGroup) + c0 / kGroup + gi) * kHeadDim + 8 * c;
+      cp_async16(&ts.kg[gi][arr][4 * c], (arr ? cv.zero_k : cv.scale_k) + go);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- scores: thread (token r, quarter qq) sums channels 32qq .. +31 ----
+#pragma unroll 1
+    for (int it = 0; it < kTailTok / 32; ++it) {
+      const int r = (tid >> 2) + 32 * it, qq = tid & 3;
+      float acc[kNH] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (r < nk) {
+        const int gi = r >> 5;
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.krow[r][0]) + qq * 32 * BITS / 8;
+        const __half* sk = reinterpret_cast<const __half*>(ts.kg[gi][0]) + 32 * qq;
+        const __half* zk = reinterpret_cast<const __half*>(ts.kg[gi][1]) + 32 * qq;
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
+          const uint32_t cw = reinterpret_cast<const uint32_t*>(row)[w];
+#pragma unroll
+          for (int e = 0; e < 32 / BITS; ++e) {
+            const int dq = w * (32 / BITS) + e;
+            const float kx = __fadd_rn(__fmul_rn((float)((cw >> (BITS * e)) & L), __half2float(sk[dq])),
+                                       __half2float(zk[dq]));
+#pragma unroll
+            for (int j = 0; j < kNH; ++j) acc[j] = fmaf(kx, ts.q[j][32 * qq + dq], acc[j]);
+          }
+        }
+      } else if (r < n) {
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int c = 4 * qq + c4;
+          const uint4 kv = ts.krow[r][c ^ (r & 7)];
+          const float kf[8] = {h_lo(kv.x), h_hi(kv.x), h_lo(kv.y), h_hi(kv.y),
+                               h_lo(kv.z), h_hi(kv.z), h_lo(kv.w), h_hi(kv.w)};
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+#pragma unroll
+            for (int j = 0; j < kNH; ++j) acc[j] = fmaf(kf[e], ts.q[j][8 * c + e], acc[j]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) {
+        acc[j] += __shfl_xor_sync(kFull, acc[j], 1);
+        acc[j] += __shfl_xor_sync(kFull, acc[j], 2);
+      }
+      if (qq == 0 && r < n)
+#pragma unroll
+        for (int j = 0; j < kNH; ++j) ts.p[j][r] = acc[j];
+    }
+    __syncthreads();
+
+    // ---- softmax over the round, one warp per head ----
+    {
+      const int j = warp;  // kWarps == kNH
+      const float x0 = lane < n ? ts.p[j][lane] : -INFINITY;
+      const float x1 = lane + 32 < n ? ts.p[j][lane + 32] : -INFINITY;
+      const float mo = ts.mrun[j];
+      const float mn = fmaxf(mo, warp_max(fmaxf(x0, x1)));
+      const float e0 = lane < n ? fast_exp2(x0 - mn) : 0.0f;
+      const float e1 = lane + 32 < n ? fast_exp2(x1 - mn) : 0.0f;
+      ts.p[j][lane] = e0;
+      ts.p[j][lane + 32] = e1;
+      const float sum = warp_sum(e0 + e1);
+      __syncwarp();
+      if (lane == 0) {
+        const float corr = mo == -INFINITY ? 0.0f : fast_exp2(mo - mn);
+        ts.corr[j] = corr;
+        ts.mrun[j] = mn;
+        ts.lrun[j] = ts.lrun[j] * corr + sum;
+      }
+    }
+    __syncthreads();
+
+    // ---- values: thread d accumulates channel d of the kNH heads ----
+#pragma unroll
+    for (int j = 0; j < kNH; ++j) o[j] *= ts.corr[j];
+    const int vpos = v_unit_pos(d >> 2);
+    const int vsh = BITS * (d & 3);
+#pragma unroll 4
+    for (int r = 0; r < n; ++r) {
+      float vx;
+      if (r < nv) {
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
+        uint32_t cb;
+        if constexpr (BITS == 2) cb = row[vpos];
+        else cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
+        const __half* svz = reinterpret_cast<const __half*>(row + RB);
+        vx = __fadd_rn(__fmul_rn((float)((cb >> vsh) & L), __half2float(svz[d >> 5])),
+                       __half2float(svz[4 + (d >> 5)]));
+      } else {
+        const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
+        vx = __half2float(row[d & 7]);
+      }
+#pragma unroll
+      for (int j = 0; j < kNH; ++j) o[j] = fmaf(ts.p[j][r], vx, o[j]);
+    }
+  }
+  __syncthreads();  // every thread is done with the staged rows (the merge area)
+
+  float* mo0 = merge_area(sm, 0, kPathTail);
+#pragma unroll
+  for (int j = 0; j < kNH; ++j) mo0[j * kHeadDim + d] = o[j];
+  if (lane < kNH) {
+    s_m[warp][lane] = warp == 0 ? ts.mrun[lane] : -INFINITY;
+    s_l[warp][lane] = warp == 0 ? ts.lrun[lane] : 0.0f;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core path (2-bit packed tiles).
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -343,16 +612,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// The 2-bit codes at bit pair I of both 16-bit halves of w, as the exact
-// fp16 pair {c_lo * 4^I, c_hi * 4^I} (I <= 4): OR the masked bits into the
-// mantissa of 1024.0 (0x6400) and subtract 1024.
+// The 2-bit codes at bit pair I of both 16-bit halves of w, kept in place:
+// read as fp16 (exponent field zero) the pair is the exact subnormal pair
+// {c_lo * 4^I * 2^-24, c_hi * 4^I * 2^-24} for I <= 4.
 template <int I>
 __device__ __forceinline__ uint32_t ext(uint32_t w) {
   static_assert(I >= 0 && I <= 4, "bit pair must stay inside the fp16 mantissa");
-  uint32_t v, r;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(w), "n"(0x00030003u << (2 * I)), "n"(0x64006400u));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64006400u));
-  return r;
+  return w & (0x00030003u << (2 * I));
 }
 
 // Bit pair i in 0..7 of each half of w: pairs 0..4 directly, 5..7 from w >> 10
@@ -365,79 +631,31 @@ __device__ __forceinline__ uint32_t ext8(uint32_t w, uint32_t w_sh10) {
 
 __host__ __device__ constexpr int pow4_exp(int i) { return i <= 4 ? i : i - 5; }
 
-// Per-lane cp.async sources and destinations of one packed tile (keys,
-// values, scales, zeros: 192 chunks of 16 B, six per lane).  The sources of
-// the next tile of the same warp are the current ones plus a fixed stride.
-struct TileCopy {
-  const char* src[6];
-  uint32_t dst[6];  // shared-memory offsets inside a TileStage
-};
-
-__device__ __forceinline__ TileCopy tile_copy_plan(const CacheView& cv, long unit, int tile, int lane) {
-  TileCopy tc;
-  const long row0 = unit * cv.Tcap + (long)tile * 32;
-  const char* kc = reinterpret_cast<const char*>(cv.codes_k + row0 * 32);
-  const char* vc = reinterpret_cast<const char*>(cv.codes_v + row0 * 32);
-  const long g0 = (unit * (cv.Tcap / kGroup) + tile) * kHeadDim;
-  const char* sk = reinterpret_cast<const char*>(cv.scale_k + g0);
-  const char* zk = reinterpret_cast<const char*>(cv.zero_k + g0);
-  const char* sv = reinterpret_cast<const char*>(cv.scale_v + row0 * (kHeadDim / kGroup));
-  const char* zv = reinterpret_cast<const char*>(cv.zero_v + row0 * (kHeadDim / kGroup));
-  const int c = lane & 15;
-  tc.src[0] = kc + 16 * lane;
-  tc.src[1] = kc + 16 * (32 + lane);
-  tc.src[2] = vc + 16 * lane;
-  tc.src[3] = vc + 16 * (32 + lane);
-  tc.src[4] = lane < 16 ? sk + 16 * c : zk + 16 * c;
-  tc.src[5] = lane < 16 ? sv + 16 * c : zv + 16 * c;
-  tc.dst[0] = (uint32_t)offsetof(TileStage, kc) + 16 * lane;
-  tc.dst[1] = (uint32_t)offsetof(TileStage, kc) + 16 * (32 + lane);
-  // value chunk 2*row + half goes to row * 48 + 16 * half bytes
-  tc.dst[2] = (uint32_t)offsetof(TileStage, vc) + (lane >> 1) * 48 + 16 * (lane & 1);
-  tc.dst[3] = (uint32_t)offsetof(TileStage, vc) + (16 + (lane >> 1)) * 48 + 16 * (lane & 1);
-  tc.dst[4] = (uint32_t)(lane < 16 ? offsetof(TileStage, sk) : offsetof(TileStage, zk)) + 4 * kpad(4 * c);
-  tc.dst[5] = (uint32_t)(lane < 16 ? offsetof(TileStage, sv) : offsetof(TileStage, zv)) + 16 * c;
-  return tc;
-}
-
-// Byte strides of the six sources when a warp moves on by kWarps tiles.
-__device__ __forceinline__ void tile_copy_advance(TileCopy& tc) {
-  constexpr long kCodes = (long)kWarps * 32 * 32;           // 32 rows of 32 B
-  constexpr long kKGroup = (long)kWarps * kHeadDim * 2;      // one group of fp16 [128]
-  constexpr long kVRows = (long)kWarps * 32 * (kHeadDim / kGroup) * 2;
-  tc.src[0] += kCodes;
-  tc.src[1] += kCodes;
-  tc.src[2] += kCodes;
-  tc.src[3] += kCodes;
-  tc.src[4] += kKGroup;
-  tc.src[5] += kVRows;
-}
-
-__device__ __forceinline__ void issue_tile(const TileCopy& tc, TileStage& st) {
-  char* base = reinterpret_cast<char*>(&st);
-#pragma unroll
-  for (int i = 0; i < 6; ++i) cp_async16(base + tc.dst[i], tc.src[i]);
-}
+constexpr float kTwo24 = 16777216.0f;  // undoes the 2^-24 of the subnormal codes
+// The running max of a head is raised only when a tile's scores exceed it by
+// more than this (log2 units), so p <= 2^0.5 and p * s stays below the fp16
+// maximum for any fp16 scale s = range / 3.
+constexpr float kLazyMax = 0.5f;
 
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
-// (head g >> 1, part g & 1).  Fragment order: k-step ks uses word m = 2*tig +
-// (ks >> 2) of each key row and bit pairs i = 2*(ks & 3) and i + 1; the k
+// (head g >> 1, part g & 1).  Fragment order: k-step ks uses word m = tig +
+// 4*(ks >> 2) of each key row and bit pairs i = 2*(ks & 3) and i + 1; the k
 // rows (2tig, 2tig+1) hold channels (16m+i, 16m+i+8) and (2tig+8, 2tig+9) hold
 // (16m+i+1, 16m+i+9).  The q table is pre-scaled by 4^-e(i) to cancel the
 // power of four that the code extraction leaves in the A operand.
-__device__ __forceinline__ void build_qprime(const MmaSmem& s, const TileStage& st, int hh,
-                                             int part, int tig, uint32_t (&bq)[8][2]) {
+__device__ __forceinline__ void build_qprime(const WarpSmem& ws, const uint32_t* sk, int g, int tig,
+                                             uint32_t (&bq)[8][2]) {
 #pragma unroll
   for (int mh = 0; mh < 2; ++mh) {
-    const int m = 2 * tig + mh;
-    const uint4 wa = *reinterpret_cast<const uint4*>(&st.sk[kpad(8 * m)]);
-    const uint4 wb = *reinterpret_cast<const uint4*>(&st.sk[kpad(8 * m + 4)]);
+    const int m = tig + 4 * mh;
+    const uint4 wa = *reinterpret_cast<const uint4*>(sk + 8 * m);
+    const uint4 wb = *reinterpret_cast<const uint4*>(sk + 8 * m + 4);
     const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, B[4] = {wb.x, wb.y, wb.z, wb.w};
-    uint32_t X[3][8];
+    uint32_t X[2][8];
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
-      const uint4 x0 = s.qs[c][2 * mh][2 * hh + part][tig];
-      const uint4 x1 = s.qs[c][2 * mh + 1][2 * hh + part][tig];
+    for (int c = 0; c < 2; ++c) {
+      const uint4 x0 = ws.qs[c][2 * mh][g][tig];
+      const uint4 x1 = ws.qs[c][2 * mh + 1][g][tig];
       X[c][0] = x0.x; X[c][1] = x0.y; X[c][2] = x0.z; X[c][3] = x0.w;
       X[c][4] = x1.x; X[c][5] = x1.y; X[c][6] = x1.z; X[c][7] = x1.w;
     }
@@ -448,31 +666,37 @@ __device__ __forceinline__ void build_qprime(const MmaSmem& s, const TileStage& 
       for (int r = 0; r < 2; ++r) {
         const uint32_t sp = __byte_perm(A[q4], B[q4], r ? 0x7632 : 0x5410);
         const int w = 2 * q4 + r;
-        bq[ks][r] = split_mul(X[0][w], X[1][w], X[2][w], sp);
+        bq[ks][r] = split_mul(X[0][w], X[1][w], X[1][w] ^ 0x80008000u, sp);
       }
     }
   }
 }
 
-// One 32-token packed tile on the tensor cores for the lane's head (tig).
-__device__ __forceinline__ void mma_tile(const MmaSmem& s, const TileStage& st, int g, int tig,
-                                         float scale_log2, float& m_run, float& lsum,
-                                         float (&O)[8][4], float (&Z)[4]) {
-  const int hh = g >> 1;
-  const int part = g & 1;
+// Position of token t (0..31) in a warp's weight buffer: the value product
+// reads tokens t0 = 16kk + 8aa + tig and t0 + 4 as one 8-byte pair.
+__device__ __forceinline__ int pbuf_pos(int t) {
+  return 8 * (t & 3) + 4 * (t >> 4) + 2 * ((t >> 3) & 1) + ((t >> 2) & 1);
+}
 
-  // ---- scores: S = codes x Q' (2 m-tiles of 16 tokens), beta = zK x q ----
-  uint32_t bq[8][2];
-  build_qprime(s, st, hh, part, tig, bq);
+// One staged 32-token tile for the four heads of the CTA, online softmax.
+// Scores: lane (g, tig) gets head tig at tokens g + 8r.  Values: the k rows
+// (2tig, 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows
+// (2tig+8, 2tig+9) tokens t0 + 8 and t0 + 12, so that the lanes of a
+// shared-memory phase read distinct banks.  m_run, lsum, O and Z belong to
+// head tig; ks = 2^E_tig * scale * log2(e).
+__device__ __forceinline__ void mma_tile(const WarpSmem& ws, const TileBuf& tb, float* pb, int g, int tig,
+                                         float ks, float& m_run, float& lsum, float (&O)[8][4],
+                                         float (&Z)[4]) {
+  // ---- beta = zK x q: every A row is the zero vector, so D[., (tig, part)] = beta ----
   float beta4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int mh = 0; mh < 2; ++mh) {
-    const int m = 2 * tig + mh;
-    const uint4 za = *reinterpret_cast<const uint4*>(&st.zk[kpad(8 * m)]);
-    const uint4 zb = *reinterpret_cast<const uint4*>(&st.zk[kpad(8 * m + 4)]);
+    const int m = tig + 4 * mh;
+    const uint4 za = *reinterpret_cast<const uint4*>(tb.zk + 8 * m);
+    const uint4 zb = *reinterpret_cast<const uint4*>(tb.zk + 8 * m + 4);
     const uint32_t A[4] = {za.x, za.y, za.z, za.w}, B[4] = {zb.x, zb.y, zb.z, zb.w};
-    const uint4 b0 = s.qb[2 * mh][2 * hh + part][tig];
-    const uint4 b1 = s.qb[2 * mh + 1][2 * hh + part][tig];
+    const uint4 b0 = ws.qb[2 * mh][g][tig];
+    const uint4 b1 = ws.qb[2 * mh + 1][g][tig];
     const uint32_t QB[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
     for (int q4 = 0; q4 < 4; ++q4) {
@@ -481,27 +705,32 @@ __device__ __forceinline__ void mma_tile(const MmaSmem& s, const TileStage& st, 
       mma16816(beta4, z0, z0, z1, z1, QB[2 * q4], QB[2 * q4 + 1]);
     }
   }
-  const float beta = beta4[0] + beta4[1];
+  const float kb = (beta4[0] + beta4[1]) * ks;
+  const float k24 = ks * kTwo24;
 
+  // ---- scores S = codes x Q' + beta (log2 units) ----
+  uint32_t bq[8][2];
+  build_qprime(ws, tb.sk, g, tig, bq);
   float sc[4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const uint2 r0 = *reinterpret_cast<const uint2*>(&st.kc[(16 * mt + g) * 8 + 2 * tig]);
-    const uint2 r1 = *reinterpret_cast<const uint2*>(&st.kc[(16 * mt + g + 8) * 8 + 2 * tig]);
-    const uint32_t r0x10 = r0.x >> 10, r0y10 = r0.y >> 10, r1x10 = r1.x >> 10, r1y10 = r1.y >> 10;
+    const uint32_t* rg = tb.kc + (16 * mt + g) * 8;      // key row 16mt + g
+    const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * 8;  // key row 16mt + g + 8
+    const uint32_t g0 = rg[tig], g1 = rg[tig + 4], e0 = r8[tig], e1 = r8[tig + 4];
+    const uint32_t g0s = g0 >> 10, g1s = g1 >> 10, e0s = e0 >> 10, e1s = e1 >> 10;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #define KIVI_KSTEP(KS, I)                                                                  \
   {                                                                                        \
-    const uint32_t wg = (KS) < 4 ? r0.x : r0.y, wgs = (KS) < 4 ? r0x10 : r0y10;           \
-    const uint32_t w8 = (KS) < 4 ? r1.x : r1.y, w8s = (KS) < 4 ? r1x10 : r1y10;           \
+    const uint32_t wg = (KS) < 4 ? g0 : g1, wgs = (KS) < 4 ? g0s : g1s;                   \
+    const uint32_t w8 = (KS) < 4 ? e0 : e1, w8s = (KS) < 4 ? e0s : e1s;                   \
     mma16816(acc, ext8<I>(wg, wgs), ext8<I>(w8, w8s), ext8<I + 1>(wg, wgs),                \
              ext8<I + 1>(w8, w8s), bq[KS][0], bq[KS][1]);                                  \
   }
     KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 4) KIVI_KSTEP(3, 6)
     KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 4) KIVI_KSTEP(7, 6)
 #undef KIVI_KSTEP
-    sc[2 * mt] = (acc[0] + acc[1] + beta) * scale_log2;      // token 16mt + g
-    sc[2 * mt + 1] = (acc[2] + acc[3] + beta) * scale_log2;  // token 16mt + g + 8
+    sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
+    sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
   }
 
   // ---- online softmax of head tig over the 32 tokens (8 lanes share it) ----
@@ -509,11 +738,9 @@ __device__ __forceinline__ void mma_tile(const MmaSmem& s, const TileStage& st, 
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-  // The running max is raised (and the accumulators rescaled) only when a
-  // score exceeds it by more than 8 in log2 units, so p <= 2^8 always.
-  if (__any_sync(kFull, tmax > m_run + 8.0f)) {
+  if (__any_sync(kFull, tmax > m_run + kLazyMax)) {
     const float mnew = fmaxf(m_run, tmax);
-    const float corr = fast_exp2(m_run - mnew);
+    const float corr = fast_exp2(m_run - mnew);  // 0 on the first tile
     m_run = mnew;
     lsum *= corr;
 #pragma unroll
@@ -523,53 +750,47 @@ __device__ __forceinline__ void mma_tile(const MmaSmem& s, const TileStage& st, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) Z[i] *= corr;
   }
-  float p[4];
+  float* prow = pb + tig * 34;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) p[r] = fast_exp2(sc[r] - m_run);  // token g + 8r
-  lsum += (p[0] + p[1]) + (p[2] + p[3]);
+  for (int r = 0; r < 4; ++r) {
+    const float p = fast_exp2(sc[r] - m_run);  // token g + 8r
+    lsum += p;
+    prow[pbuf_pos(g + 8 * r)] = p;
+  }
+  __syncwarp();
 
-  // ---- P for the value product: this lane needs head hh at tokens
-  // 2tig + {0, 1} + 8r, held by lanes (2tig + delta, hh), value r ----
-  float pv[2][4];
-#pragma unroll
-  for (int dl = 0; dl < 2; ++dl)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) pv[dl][r] = __shfl_sync(kFull, p[r], 4 * (2 * tig + dl) + hh);
-
+  // ---- values: O += codes^T x (p * sV), Z += zV^T x p ----
+  const int part = g & 1;
+  const float* pv = pb + (g >> 1) * 34 + 8 * tig;
+  const int zsel = (g >> 1) & 1;  // zero word of value group g & 3 within a token
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    uint32_t pa[2], Pp[4][2], az[2];
+    uint32_t pa[2], Pp[4][2], az[2], u[2][2];
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
-      const int r = 2 * kk + aa;  // tokens 16kk + 8aa + 2tig + {0, 1}
-      const uint32_t h = f2_to_h2(pv[0][r], pv[1][r]);
-      const uint32_t l = f2_to_h2(pv[0][r] - h_lo(h), pv[1][r] - h_hi(h));
+      const int t0 = 16 * kk + 8 * aa + tig;  // tokens t0, t0 + 4
+      const float2 x = *reinterpret_cast<const float2*>(pv + 4 * kk + 2 * aa);
+      const uint32_t h = f2_to_h2(x.x, x.y);
+      const uint32_t l = f2_to_h2(x.x - h_lo(h), x.y - h_hi(h));
       // split_mul operands of this lane's part (see split_mul)
       pa[aa] = part ? l : h;
-      const uint32_t pb = part ? h : 0u;
-      const uint32_t pbn = pb ^ 0x80008000u;
-      const int t0 = 16 * kk + 8 * aa + 2 * tig;
-      const uint4 S = *reinterpret_cast<const uint4*>(&st.sv[2 * t0]);   // rows t0, t0 + 1
-      const uint4 Zv = *reinterpret_cast<const uint4*>(&st.zv[2 * t0]);
-      Pp[0][aa] = split_mul(pa[aa], pb, pbn, __byte_perm(S.x, S.z, 0x5410));
-      Pp[1][aa] = split_mul(pa[aa], pb, pbn, __byte_perm(S.x, S.z, 0x7632));
-      Pp[2][aa] = split_mul(pa[aa], pb, pbn, __byte_perm(S.y, S.w, 0x5410));
-      Pp[3][aa] = split_mul(pa[aa], pb, pbn, __byte_perm(S.y, S.w, 0x7632));
-      az[aa] = __byte_perm((g & 2) ? Zv.y : Zv.x, (g & 2) ? Zv.w : Zv.z, (g & 1) ? 0x7632 : 0x5410);
-    }
-    // z-term: rows = value groups (g & 3), columns = (head, part) of p
-    mma16816(Z, az[0], az[0], az[1], az[1], pa[0], pa[1]);
-
-    // value codes: interleaved word g of rows t0, t0 + 1 holds, per byte,
-    // channels 4g..4g+3 of groups 0..3
-    uint32_t u[2][2];  // [aa][groups 01 / 23]
-#pragma unroll
-    for (int aa = 0; aa < 2; ++aa) {
-      const int t0 = 16 * kk + 8 * aa + 2 * tig;
-      const uint32_t w0 = st.vc[t0 * 12 + g], w1 = st.vc[(t0 + 1) * 12 + g];
+      const uint32_t pbh = part ? h : 0u;
+      const uint32_t pbn = pbh ^ 0x80008000u;
+      const uint2 S0 = *reinterpret_cast<const uint2*>(tb.sv + 2 * t0);        // token t0, groups 0..3
+      const uint2 S1 = *reinterpret_cast<const uint2*>(tb.sv + 2 * (t0 + 4));
+      Pp[0][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.x, S1.x, 0x5410));
+      Pp[1][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.x, S1.x, 0x7632));
+      Pp[2][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x5410));
+      Pp[3][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x7632));
+      az[aa] = __byte_perm(tb.zv[2 * t0 + zsel], tb.zv[2 * (t0 + 4) + zsel], (g & 1) ? 0x7632 : 0x5410);
+      // value codes: interleaved word g of a row holds, per byte, channels
+      // 4g..4g+3 of groups 0..3
+      const uint32_t w0 = tb.vc[t0 * 8 + g], w1 = tb.vc[(t0 + 4) * 8 + g];
       u[aa][0] = __byte_perm(w0, w1, 0x5410);
       u[aa][1] = __byte_perm(w0, w1, 0x7632);
     }
+    // z-term: rows = value groups (g & 3), columns = (head, part) of p
+    mma16816(Z, az[0], az[0], az[1], az[1], pa[0], pa[1]);
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const uint32_t x0 = u[0][half], x1 = u[1][half];
@@ -588,37 +809,191 @@ __device__ __forceinline__ void mma_tile(const MmaSmem& s, const TileStage& st, 
   }
 }
 
-// CTA prologue of the tensor-core path: q tables in fragment order.  Thread
-// (head, tig, word) builds the pair words of both parts.
-__device__ void build_q_tables(MmaSmem& s, const AttnArgs& a, int b, int j0, int nh) {
+// q of the CTA's heads: staged once in shared memory, per-head exponents
+// (warp w takes head w), then the tables in fragment order.  Thread (head,
+// tig, word) builds the pair words of both parts.
+__device__ void build_q_tables(WarpSmem& s, const AttnArgs& a, int b, int j0, int nh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < kNH) {
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[i] = warp < nh ? load_q(a.q, ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane + i, a.q_dtype)
+                       : 0.0f;
+    *reinterpret_cast<float4*>(&s.qv[warp][4 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+    if (lane == 0) {
+      const int be = (int)((__float_as_uint(amax) >> 23) & 0xffu);
+      // amax in [2^(be-127), 2^(be-126)) for normal amax; a subnormal amax is
+      // below 2^-126, a zero row keeps E = 0
+      const int E = amax == 0.0f ? 0 : (be == 0 ? -126 : be - 126);
+      s.qexp[warp] = E;
+      s.qscale[warp] = ldexpf(a.scale_log2, E);
+    }
+  }
+  __syncthreads();
   for (int idx = threadIdx.x; idx < kNH * 4 * 16; idx += blockDim.x) {
     const int word = idx & 15;                // ks * 2 + r
     const int tig = (idx >> 4) & 3;
     const int hh = idx >> 6;
     const int ks = word >> 1, r = word & 1;
-    const int m = 2 * tig + (ks >> 2);
+    const int m = tig + 4 * (ks >> 2);
     const int i = 2 * (ks & 3) + r;
     const float f = 1.0f / (float)(1 << (2 * pow4_exp(i)));
-    float q2[2] = {0.0f, 0.0f};
-    if (hh < nh)
+    float q2[2];
 #pragma unroll
-      for (int half = 0; half < 2; ++half)
-        q2[half] = load_q(a.q, ((long)b * a.Hq + j0 + hh) * kHeadDim + 16 * m + i + 8 * half, a.q_dtype);
+    for (int half = 0; half < 2; ++half) q2[half] = ldexpf(s.qv[hh][16 * m + i + 8 * half], -s.qexp[hh]);
     const uint32_t qh = f2_to_h2(q2[0], q2[1]);
     const uint32_t ql = f2_to_h2(q2[0] - h_lo(qh), q2[1] - h_hi(qh));
     const uint32_t sh = f2_to_h2(q2[0] * f, q2[1] * f);
     const uint32_t sl = f2_to_h2(q2[0] * f - h_lo(sh), q2[1] * f - h_hi(sh));
     const int quarter = word >> 2, wq = word & 3;
-    // hi lane: (xa, xb, xbn) = (hi, 0, -0); lo lane: (lo, hi, -hi)
+    // hi lane: (xa, xb) = (hi, 0); lo lane: (lo, hi)
     reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh][tig])[wq] = sh;
     reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh][tig])[wq] = 0u;
-    reinterpret_cast<uint32_t*>(&s.qs[2][quarter][2 * hh][tig])[wq] = 0x80008000u;
     reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh + 1][tig])[wq] = sl;
     reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh + 1][tig])[wq] = sh;
-    reinterpret_cast<uint32_t*>(&s.qs[2][quarter][2 * hh + 1][tig])[wq] = sh ^ 0x80008000u;
     reinterpret_cast<uint32_t*>(&s.qb[quarter][2 * hh][tig])[wq] = qh;
     reinterpret_cast<uint32_t*>(&s.qb[quarter][2 * hh + 1][tig])[wq] = ql;
   }
+}
+
+// Bulk copies of packed tile `tile` into a stage (one lane).
+__device__ __forceinline__ void issue_tile(TileBuf& tb, unsigned long long* bar, const CacheView& cv,
+                                           long unit, int tile) {
+  const long row0 = unit * cv.Tcap + (long)tile * 32;
+  const long g0 = (unit * (cv.Tcap / kGroup) + tile) * kHeadDim;
+  mbar_expect_tx(bar, kTileBytes);
+  bulk_g2s(tb.kc, cv.codes_k + row0 * 32, 1024u, bar);
+  bulk_g2s(tb.vc, cv.codes_v + row0 * 32, 1024u, bar);
+  bulk_g2s(tb.sk, cv.scale_k + g0, 256u, bar);
+  bulk_g2s(tb.zk, cv.zero_k + g0, 256u, bar);
+  bulk_g2s(tb.sv, cv.scale_v + row0 * (kHeadDim / kGroup), 256u, bar);
+  bulk_g2s(tb.zv, cv.zero_v + row0 * (kHeadDim / kGroup), 256u, bar);
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Packed tiles [tile0, tile1) of one (batch, kv-head, head chunk) on the
+// tensor cores.  Warp w takes tiles tile0 + w, + kWarps, ... through its own
+// ring of kStages staged tiles (lane 0 issues the copies; no CTA barrier in
+// the loop).  Leaves each warp's (max, sum) in s_m / s_l and its output in
+// its merge area.
+__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit, int b,
+                             int j0, int nh, int tile0, int tile1, float (&s_m)[kWarps][kNH],
+                             float (&s_l)[kWarps][kNH]) {
+  WarpSmem& ws = sm.ws;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+  const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
+  TileBuf* st = ws.st[warp];
+  unsigned long long* bars = ws.bar[warp];
+
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < kStages; ++k) mbar_init(&bars[k], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+  int issued = min(n_mine, kStages);
+  if (lane == 0)
+    for (int k = 0; k < issued; ++k) issue_tile(st[k], &bars[k], cv, unit, tile0 + warp + kWarps * k);
+  build_q_tables(ws, a, b, j0, nh);
+  __syncthreads();
+  const float ks = ws.qscale[tig];
+  float* pb = &ws.pbuf[warp][0][0];
+
+  float O[8][4], Z[4], m_run = -INFINITY, lsum = 0.0f;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) O[mt][i] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) Z[i] = 0.0f;
+
+  int done = 0;
+  for (int k = 0; k < n_mine; ++k) {
+    const int stage = k % kStages;
+    const bool ok = mbar_wait(&bars[stage], (uint32_t)((k / kStages) & 1));
+    if (__any_sync(kFull, !ok)) break;
+    done = k + 1;
+    mma_tile(ws, st[stage], pb, g, tig, ks, m_run, lsum, O, Z);
+    __syncwarp();  // every lane is done with the stage and the weight buffer
+    if (k + kStages < n_mine) {
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_tile(st[stage], &bars[stage], cv, unit, tile0 + warp + kWarps * (k + kStages));
+      }
+      ++issued;
+    }
+  }
+  if (done < n_mine) {
+    // A wait timed out: record it, and let every copy still in flight land
+    // before the warp's buffers are reused (each wait bounded again).
+    if (lane == 0) atomicOr(a.status, 1);
+    for (int k = done; k < issued; ++k) mbar_wait(&bars[k % kStages], (uint32_t)((k / kStages) & 1));
+    __syncwarp();
+  }
+
+  // ---- this warp's partial: max, sum and output of head tig ----
+  // lsum of head tig over tokens g + 8r: sum over g
+  lsum += __shfl_xor_sync(kFull, lsum, 4);
+  lsum += __shfl_xor_sync(kFull, lsum, 8);
+  lsum += __shfl_xor_sync(kFull, lsum, 16);
+  if (g == 0) {
+    s_m[warp][tig] = m_run;
+    s_l[warp][tig] = lsum;
+  }
+  // z-term of value group gp for head tig sits in lane (gp, tig)
+  const float zmine = Z[0] + Z[1];
+  float zt[4];
+#pragma unroll
+  for (int gp = 0; gp < 4; ++gp) zt[gp] = __shfl_sync(kFull, zmine, 4 * gp + tig);
+  float* orow = merge_area(sm, warp, kPathMma) + tig * kHeadDim;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const int gp = mt >> 1, hm = mt & 1;
+    const int i_lo = 4 * (gp & 1) + 2 * hm;
+    const int ch = 32 * gp + 4 * g + 2 * hm;
+    const float f_lo = kTwo24 / (float)(1 << (2 * pow4_exp(i_lo)));
+    const float f_hi = kTwo24 / (float)(1 << (2 * pow4_exp(i_lo + 1)));
+    orow[ch] = (O[mt][0] + O[mt][1]) * f_lo + zt[gp];
+    orow[ch + 1] = (O[mt][2] + O[mt][3]) * f_hi + zt[gp];
+  }
+}
+
+// Merge n <= kMergeGroup partials [n][kNH][D] (outputs) and [n][kNH][2]
+// (max, sum): warp w takes head w, lane l channels 4l..4l+3; every load is
+// issued before the first is used.  Returns the merged (unnormalized) output
+// quad, max and sum of head `warp`.
+__device__ __forceinline__ void merge_partials(const float* po, const float* pml, int n, int nh, float4& o4,
+                                               float& m_out, float& l_out) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  float4 v[kMergeGroup];
+#pragma unroll
+  for (int k = 0; k < kMergeGroup; ++k)
+    v[k] = (k < n && warp < nh)
+               ? __ldcg(reinterpret_cast<const float4*>(po + ((long)k * kNH + warp) * kHeadDim) + lane)
+               : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float2 ml = (lane < n && warp < nh)
+                        ? __ldcg(reinterpret_cast<const float2*>(pml + ((long)lane * kNH + warp) * 2))
+                        : make_float2(-INFINITY, 0.0f);
+  const float M = warp_max(ml.x);
+  const float e = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - M);
+  l_out = warp_sum(e * ml.y);
+  m_out = M;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int k = 0; k < kMergeGroup; ++k) {
+    const float ek = __shfl_sync(kFull, e, k);
+    acc.x = fmaf(ek, v[k].x, acc.x);
+    acc.y = fmaf(ek, v[k].y, acc.y);
+    acc.z = fmaf(ek, v[k].z, acc.z);
+    acc.w = fmaf(ek, v[k].w, acc.w);
+  }
+  o4 = acc;
 }
 
 // grid (splits, H * head_chunks, B), 128 threads.
@@ -638,13 +1013,14 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
   const int nh = min(kNH, grp - hc * kNH);
   const long unit = (long)b * cv.H + h;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool mma_path = (BITS == 2) && s > 0;
-  float* mo = merge_area(sm, warp, mma_path);
+  const int path = s == 0 ? kPathTail : (BITS == 2 ? kPathMma : kPathV1);
 
-  if (!mma_path) {
-    // ---- CUDA cores: the tail split, or any split at 4 bits ----
-    const int t_begin = s == 0 ? a.t_tail : (s - 1) * a.chunk;
-    const int t_end = s == 0 ? a.l : min(a.t_tail, s * a.chunk);
+  if (path == kPathTail) {
+    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, s_m, s_l);
+  } else if (path == kPathV1) {
+    // ---- CUDA cores: packed tiles at 4 bits ----
+    const int t_begin = (s - 1) * a.chunk;
+    const int t_end = min(a.t_tail, s * a.chunk);
     for (int i = threadIdx.x; i < kNH * kHeadDim; i += blockDim.x) {
       const int j = i / kHeadDim, d = i % kHeadDim;
       sm.v1.q[j][d] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + d, a.q_dtype) * a.scale_log2
@@ -669,76 +1045,21 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
         s_l[warp][j] = lsum[j];
       }
     }
+    float* mo = merge_area(sm, warp, kPathV1);
 #pragma unroll
     for (int j = 0; j < kNH; ++j)
       *reinterpret_cast<float4*>(&mo[j * kHeadDim + 4 * lane]) = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
   } else {
     // ---- tensor cores: packed tiles [(s-1)*chunk, min(t_tail, s*chunk)) ----
-    const int g = lane >> 2, tig = lane & 3;
     const int tile0 = (s - 1) * a.chunk / 32;
     const int tile1 = min(a.t_tail, s * a.chunk) / 32;
-    const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
-    TileStage* stages = sm.mma.st[warp];
-    // start this warp's first tile copies before the CTA builds its q tables
-    TileCopy tc = tile_copy_plan(cv, unit, tile0 + warp, lane);
-#pragma unroll
-    for (int k = 0; k < kStages - 1; ++k) {
-      if (k < n_mine) issue_tile(tc, stages[k]);
-      cp_async_commit();
-      tile_copy_advance(tc);
-    }
-    build_q_tables(sm.mma, a, b, j0, nh);
-    __syncthreads();
-    float O[8][4], Z[4], m_run = -INFINITY, lsum = 0.0f;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) O[mt][i] = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) Z[i] = 0.0f;
-    int st_cur = 0, st_next = kStages - 1;
-    for (int k = 0; k < n_mine; ++k) {
-      if (k + kStages - 1 < n_mine) issue_tile(tc, stages[st_next]);
-      cp_async_commit();
-      tile_copy_advance(tc);
-      cp_async_wait<kStages - 1>();
-      __syncwarp();
-      mma_tile(sm.mma, stages[st_cur], g, tig, a.scale_log2, m_run, lsum, O, Z);
-      __syncwarp();
-      st_cur = st_cur == kStages - 1 ? 0 : st_cur + 1;
-      st_next = st_next == kStages - 1 ? 0 : st_next + 1;
-    }
-    cp_async_wait<0>();
-    __syncwarp();
-    // lane (g, tig) holds head tig: its partial sum over tokens g + 8r
-    lsum += __shfl_xor_sync(kFull, lsum, 4);
-    lsum += __shfl_xor_sync(kFull, lsum, 8);
-    lsum += __shfl_xor_sync(kFull, lsum, 16);
-    if (g == 0) {
-      s_m[warp][tig] = m_run;
-      s_l[warp][tig] = lsum;
-    }
-    // z-term of value group gp for head tig sits in lane (gp, tig)
-    const float zmine = Z[0] + Z[1];
-    float zt[4];
-#pragma unroll
-    for (int gp = 0; gp < 4; ++gp) zt[gp] = __shfl_sync(kFull, zmine, 4 * gp + tig);
-    float* orow = mo + tig * kHeadDim;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int gp = mt >> 1, hm = mt & 1;
-      const int i_lo = 4 * (gp & 1) + 2 * hm;
-      const int ch = 32 * gp + 4 * g + 2 * hm;
-      const float f_lo = 1.0f / (float)(1 << (2 * pow4_exp(i_lo)));
-      const float f_hi = 1.0f / (float)(1 << (2 * pow4_exp(i_lo + 1)));
-      orow[ch] = (O[mt][0] + O[mt][1]) * f_lo + zt[gp];
-      orow[ch + 1] = (O[mt][2] + O[mt][3]) * f_hi + zt[gp];
-    }
+    packed_split(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;
+  const long gid = (long)b * gridDim.y + blockIdx.y;  // (batch, kv-head, head chunk)
   for (int j = 0; j < nh; ++j) {
     float M = -INFINITY;
 #pragma unroll
@@ -747,12 +1068,13 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
     if (M != -INFINITY) {
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) {
+        if (s_m[w][j] == -INFINITY) continue;  // an empty warp (its area is not written)
         const float e = fast_exp2(s_m[w][j] - M);
         lt += e * s_l[w][j];
-        ot += e * merge_area(sm, w, mma_path)[j * kHeadDim + d];
+        ot += e * merge_area(sm, w, path)[j * kHeadDim + d];
       }
     }
-    const long pidx = ((long)b * a.Hq + j0 + j) * a.splits + s;
+    const long pidx = (gid * a.splits + s) * kNH + j;
     a.ws_o[pidx * kHeadDim + d] = ot;
     if (d == 0) {
       a.ws_ml[pidx * 2] = M;
@@ -760,46 +1082,58 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
     }
   }
 
-  // ---- the last CTA of this (b, kv-head, head chunk) merges the splits ----
+  // ---- the last CTA of each group of kMergeGroup splits merges the group;
+  //      with more than one group, the last group merges the group results ----
+  const int n_grp = (a.splits + kMergeGroup - 1) / kMergeGroup;
+  const int grp_i = s / kMergeGroup;
+  const int g_lo = grp_i * kMergeGroup, g_n = min(kMergeGroup, a.splits - g_lo);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
-    int* counter = a.counters + (long)b * gridDim.y + blockIdx.y;
-    s_last = atomicAdd(counter, 1) == a.splits - 1;
+    int* counter = a.counters + gid * a.merge_groups + grp_i;
+    s_last = atomicAdd(counter, 1) == g_n - 1;
     if (s_last) *counter = 0;  // every other CTA of the group has counted in
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // weights of the splits, one warp per head: e_s = 2^(m_s - M) / sum
-  float* s_w = reinterpret_cast<float*>(&sm);  // [kNH][a.splits], the CTA's buffers are free now
-  if (warp < nh) {
-    const long base = ((long)b * a.Hq + j0 + warp) * a.splits;
-    float M = -INFINITY;
-    for (int sp = lane; sp < a.splits; sp += 32) M = fmaxf(M, __ldcg(a.ws_ml + (base + sp) * 2));
-    M = warp_max(M);
-    float den = 0.0f;
-    for (int sp = lane; sp < a.splits; sp += 32) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml + (base + sp) * 2));
-      const float e = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - M);
-      s_w[warp * a.splits + sp] = e;
-      den += e * ml.y;
+  float4 o4;
+  float lsum_h, m_h;
+  merge_partials(a.ws_o + (gid * a.splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.splits + g_lo) * kNH * 2,
+                 g_n, nh, o4, m_h, lsum_h);
+  if (n_grp > 1) {
+    // a group result: write it, then count the group in
+    if (warp < nh) {
+      const long pidx = (gid * a.merge_groups + grp_i) * kNH + warp;
+      *reinterpret_cast<float4*>(a.ws_o1 + pidx * kHeadDim + 4 * lane) = o4;
+      if (lane == 0) {
+        a.ws_ml1[pidx * 2] = m_h;
+        a.ws_ml1[pidx * 2 + 1] = lsum_h;
+      }
     }
-    den = warp_sum(den);
-    const float inv = 1.0f / den;
-    for (int sp = lane; sp < a.splits; sp += 32) s_w[warp * a.splits + sp] *= inv;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int* counter = a.counters2 + gid;
+      s_last = atomicAdd(counter, 1) == n_grp - 1;
+      if (s_last) *counter = 0;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    merge_partials(a.ws_o1 + gid * a.merge_groups * kNH * kHeadDim, a.ws_ml1 + gid * a.merge_groups * kNH * 2,
+                   n_grp, nh, o4, m_h, lsum_h);
   }
-  __syncthreads();
-  for (int j = 0; j < nh; ++j) {
-    const long base = ((long)b * a.Hq + j0 + j) * a.splits;
-    float num = 0.0f;
-#pragma unroll 8
-    for (int sp = 0; sp < a.splits; ++sp)
-      num += s_w[j * a.splits + sp] * __ldcg(a.ws_o + (base + sp) * kHeadDim + d);
-    const long oi = ((long)b * a.Hq + j0 + j) * kHeadDim + d;
-    if (a.q_dtype == kF32) static_cast<float*>(a.out)[oi] = num;
-    else if (a.q_dtype == kF16) static_cast<__half*>(a.out)[oi] = __float2half_rn(num);
-    else static_cast<__nv_bfloat16*>(a.out)[oi] = __float2bfloat16_rn(num);
+  if (warp < nh) {
+    const float inv = 1.0f / lsum_h;
+    const float r[4] = {o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv};
+    const long oi = ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (a.q_dtype == kF32) static_cast<float*>(a.out)[oi + i] = r[i];
+      else if (a.q_dtype == kF16) static_cast<__half*>(a.out)[oi + i] = __float2half_rn(r[i]);
+      else static_cast<__nv_bfloat16*>(a.out)[oi + i] = __float2bfloat16_rn(r[i]);
+    }
   }
 }
 

@@ -68,18 +68,20 @@ kivi::CacheView view(const kivi_cache* c) {
 }
 
 // Work units of the attention grid besides the split: (b, kv-head, chunk of
-// four query heads).
+// kHeadChunk query heads).
 long attention_units(const kivi_config& c) {
   const int grp = c.n_q_heads / c.n_kv_heads;
-  return (long)c.batch * c.n_kv_heads * ((grp + 3) / 4);
+  return (long)c.batch * c.n_kv_heads * ((grp + kivi::kHeadChunk - 1) / kivi::kHeadChunk);
 }
 
 // Upper bound on the packed-tile splits: the tail split plus the tile splits
-// of every unit fit one wave of kivi::kAttnCtasPerSm CTAs per SM of a GB300.
+// of every unit fit one wave of kivi::kAttnCtasPerSm CTAs per SM of a GB300,
+// and the partials merge in at most two levels.
 int max_tile_splits(const kivi_config& c) {
   const long u = attention_units(c);
   long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u - 1;
   if (s < 1) s = 1;
+  if (s > kivi::kMaxSplits - 1) s = kivi::kMaxSplits - 1;
   const long by_len = (c.max_tokens + 31) / 32;
   return (int)(s < by_len ? s : by_len);
 }
@@ -88,7 +90,8 @@ int max_tile_splits(const kivi_config& c) {
 int max_splits(const kivi_config& c) { return 1 + max_tile_splits(c); }
 
 // Splits used at length l, the tail start and the (32-aligned) tokens per
-// packed split.
+// packed split.  Automatic splits take at least 256 tokens and a multiple of
+// four tiles, so that the four warps of a CTA get equal shares.
 void split_plan(const kivi_cache* c, int l, int* splits, int* chunk, int* t_tail) {
   const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
   *t_tail = tt;
@@ -98,32 +101,51 @@ void split_plan(const kivi_cache* c, int l, int* splits, int* chunk, int* t_tail
     *chunk = 32;
     return;
   }
-  int s = c->splits_override > 0 ? c->splits_override - 1 : max_tile_splits(c->cfg);
-  if (s > max_tile_splits(c->cfg)) s = max_tile_splits(c->cfg);
-  if (c->splits_override <= 0) {
-    const int by_work = (tt + 255) / 256;  // at least 256 tokens per split when automatic
-    if (s > by_work) s = by_work;
+  const int smax = max_tile_splits(c->cfg);
+  int per;  // tiles per packed split
+  if (c->splits_override > 0) {
+    int s = c->splits_override - 1;
+    if (s > smax) s = smax;
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    per = (tiles + s - 1) / s;
+  } else {
+    per = (tiles + smax - 1) / smax;
+    per = (per + 3) / 4 * 4;
+    if (per < 8) per = 8;
   }
-  if (s > tiles) s = tiles;
-  if (s < 1) s = 1;
-  const int ch = ((tiles + s - 1) / s) * 32;
+  const int ch = per * 32;
   *chunk = ch;
   *splits = 1 + (tt + ch - 1) / ch;  // no empty split
 }
 
-// Workspace layout: partial outputs [B][Hq][S_max][D] f32, partial (max, sum)
-// [B][Hq][S_max][2] f32, then one int counter per attention group.
+// Workspace layout (attention group gid = (b, kv-head, head chunk), S = max
+// splits, G = ceil(S / kMergeGroup), C = kHeadChunk):
+//   partial outputs [gid][S][C][D] f32, partial (max, sum) [gid][S][C][2] f32,
+//   group outputs [gid][G][C][D] f32, group (max, sum) [gid][G][C][2] f32,
+//   split-group counters [gid][G] int, group counters [gid] int, then a
+//   16-byte slot whose first int is the status word (nonzero after a
+//   timed-out wait).
 struct WsLayout {
-  size_t o_off, ml_off, cnt_off, total;
+  size_t o_off, ml_off, o1_off, ml1_off, cnt_off, cnt2_off, status_off, total;
+  int groups;
 };
 
 WsLayout ws_layout(const kivi_config& c) {
-  const size_t rows = (size_t)c.batch * c.n_q_heads * max_splits(c);
+  const size_t units = (size_t)attention_units(c);
+  const size_t S = (size_t)max_splits(c);
+  const size_t G = (S + kivi::kMergeGroup - 1) / kivi::kMergeGroup;
+  const size_t C = kivi::kHeadChunk, D = (size_t)c.head_dim;
   WsLayout w;
+  w.groups = (int)G;
   w.o_off = 0;
-  w.ml_off = rows * c.head_dim * 4;
-  w.cnt_off = w.ml_off + rows * 2 * 4;
-  w.total = w.cnt_off + ((size_t)attention_units(c) * 4 + 15) / 16 * 16;
+  w.ml_off = w.o_off + units * S * C * D * 4;
+  w.o1_off = w.ml_off + units * S * C * 2 * 4;
+  w.ml1_off = w.o1_off + units * G * C * D * 4;
+  w.cnt_off = w.ml1_off + units * G * C * 2 * 4;
+  w.cnt2_off = w.cnt_off + units * G * 4;
+  w.status_off = (w.cnt2_off + units * 4 + 15) / 16 * 16;
+  w.total = w.status_off + 16;
   return w;
 }
 
@@ -237,7 +259,12 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   char* ws = static_cast<char*>(workspace);
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
   a.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  a.ws_o1 = reinterpret_cast<float*>(ws + w.o1_off);
+  a.ws_ml1 = reinterpret_cast<float*>(ws + w.ml1_off);
+  a.merge_groups = w.groups;
   a.counters = reinterpret_cast<int*>(ws + w.cnt_off);
+  a.counters2 = reinterpret_cast<int*>(ws + w.cnt2_off);
+  a.status = reinterpret_cast<int*>(ws + w.status_off);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->ws_ready != workspace) {
     kivi_status z = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, st));
@@ -340,7 +367,12 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   char* base = static_cast<char*>(ws);
   a.ws_o = reinterpret_cast<float*>(base + w.o_off);
   a.ws_ml = reinterpret_cast<float*>(base + w.ml_off);
+  a.ws_o1 = reinterpret_cast<float*>(base + w.o1_off);
+  a.ws_ml1 = reinterpret_cast<float*>(base + w.ml1_off);
+  a.merge_groups = w.groups;
   a.counters = reinterpret_cast<int*>(base + w.cnt_off);
+  a.counters2 = reinterpret_cast<int*>(base + w.cnt2_off);
+  a.status = reinterpret_cast<int*>(base + w.status_off);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left; the split counters must
   // start at zero, so clear them on every call (a memset, not an allocation).

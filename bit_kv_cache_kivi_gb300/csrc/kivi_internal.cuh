@@ -10,7 +10,10 @@ namespace kivi {
 constexpr int kHeadDim = 128;  // D supported by the kernels
 constexpr int kGroup = 32;     // G supported by the kernels
 constexpr int kTargetSMs = 152;    // GB300 SM count used by the split policy
-constexpr int kAttnCtasPerSm = 3;  // attention CTAs resident per SM (registers)
+constexpr int kAttnCtasPerSm = 4;  // attention CTAs resident per SM (registers, shared memory)
+constexpr int kHeadChunk = 4;      // query heads per attention CTA
+constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two levels at most)
+constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
 
 // Device view of one cache: the eight buffers plus its shape.
 struct CacheView {
@@ -47,9 +50,15 @@ struct AttnArgs {
   // min(t_tail, s*chunk)).
   int t_tail;
   int splits, chunk;
-  float* ws_o;        // [B][Hq][splits][D]
-  float* ws_ml;       // [B][Hq][splits][2]  (running max in log2 units, sum)
-  int* counters;      // [B][H * head_chunks] CTAs finished per group; 0 between calls
+  // Split partials of attention group gid = (b, kv-head, head chunk):
+  float* ws_o;        // [gid][splits][kHeadChunk][D]  output sums
+  float* ws_ml;       // [gid][splits][kHeadChunk][2]  (max in log2 units, sum)
+  float* ws_o1;       // [gid][merge_groups][kHeadChunk][D]  merged groups of kMergeGroup splits
+  float* ws_ml1;      // [gid][merge_groups][kHeadChunk][2]
+  int merge_groups;   // stride of the group arrays (ceil(max splits / kMergeGroup))
+  int* counters;      // [gid][merge_groups] CTAs finished per split group; 0 between calls
+  int* counters2;     // [gid] split groups finished; 0 between calls
+  int* status;        // set nonzero when a bounded wait for staged data timed out
 };
 
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a,

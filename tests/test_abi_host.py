@@ -113,26 +113,31 @@ def test_init_validation_and_host_state(K):
 
 def test_split_plan_and_workspace(K):
     """Split 0 is the fp16 tail; the packed tiles [0, floor32(l - R)) are
-    shared by up to floor(3 * 152 / units) - 1 splits of >= 256 tokens, so
-    the grid fits one wave of three CTAs per SM."""
-    # Llama-3-8B decode shape: 64 (b, kv-head) units -> up to 6 tile splits
+    shared by up to floor(4 * 152 / units) - 1 splits of >= 8 tiles, a
+    multiple of four tiles each, so the grid fits one wave of four CTAs per
+    SM and the four warps of a CTA get equal shares."""
+    # Llama-3-8B decode shape: 64 (b, kv-head) units -> up to 8 tile splits;
+    # 127 tiles -> 16 tiles per split -> 8 tile splits
     c = cfg(K, batch=8, n_kv_heads=8, n_q_heads=32, max_tokens=4128)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     try:
-        assert K.kivi_attention_splits(h, 4097) == 7
+        assert K.kivi_attention_splits(h, 4097) == 9
         assert K.kivi_attention_splits(h, 100) == 2   # tail + one 64-token split
         assert K.kivi_attention_splits(h, 40) == 1    # everything is tail
-        assert K.kivi_attention_workspace_bytes(h) == 8 * 32 * 7 * (128 + 2) * 4 + 64 * 4
+        # 64 groups x (9 split partials + 1 merged group) x 4 heads x (128 + 2)
+        # floats, one counter per split group and per group, the status slot
+        assert K.kivi_attention_workspace_bytes(h) == 64 * (9 + 1) * 4 * (128 + 2) * 4 + 64 * 4 * 2 + 16
         K.kivi_set_attention_splits(h, 3)
         assert K.kivi_attention_splits(h, 4097) == 3
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
-        assert K.kivi_attention_splits(h, 4097) == 7
+        assert K.kivi_attention_splits(h, 4097) == 9
     finally:
         K.kivi_cache_destroy(h)
-    # long context: 8 units -> 56 tile splits + the tail = 456 CTAs
+    # long context: 8 units -> up to 75 tile splits; 4092 tiles -> 56 tiles
+    # per split -> 74 tile splits + the tail = 600 CTAs
     c = cfg(K, batch=1, n_kv_heads=8, n_q_heads=32, residual=128, max_tokens=131072)
     h = K.kivi_cache_init(c, _fake_buffers(K))
-    assert K.kivi_attention_splits(h, 131072) == 57
+    assert K.kivi_attention_splits(h, 131072) == 75
     K.kivi_cache_destroy(h)
     # GQA 18 -> five chunks of four query heads
     c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=18, max_tokens=1024)
