@@ -168,18 +168,18 @@ struct WarpSmem {
   unsigned long long bar[kWarps][kStages];
 };
 
-// The tail split: up to kTailTok tokens per round, each staged as a 256-byte
-// key row and a 256-byte value row -- an fp16 residual row (16-byte chunks
-// XOR-swizzled by row), or the packed codes at the row start (value rows
-// then carry scale[4] at byte RB and zero[4] at byte RB + 8).
-constexpr int kTailTok = 64;
+// A tail split: up to kTailTok tokens, each staged as a 256-byte key row and
+// a 256-byte value row -- an fp16 residual row (16-byte chunks XOR-swizzled by
+// row), or the packed codes at the row start (value rows then carry scale[4]
+// at byte RB and zero[4] at byte RB + 8).
+static_assert(kNH == 4, "the tail split keeps the heads of a channel / token in one float4");
 struct TailSmem {
-  float q[kNH][kHeadDim];                 // q * scale * log2(e)
+  float4 q4[kHeadDim];                    // q * scale * log2(e): the kNH heads of channel d
   uint4 krow[kTailTok][16];
   uint4 vrow[kTailTok][16];
-  uint32_t kg[2][2][64];                  // scale / zero of the round's (at most two) key groups
-  float p[kNH][kTailTok];                 // scores, then weights
-  float mrun[kNH], lrun[kNH], corr[kNH];  // running max / sum, rescale of this round
+  uint32_t kg[2][2][64];                  // scale / zero of the (at most two) key groups
+  float4 p4[kTailTok];                    // per token: scores, then weights, of the kNH heads
+  float mh[kNH], lh[kNH];                 // per head: max and sum of the weights
 };
 
 union SplitSmem {
@@ -429,174 +429,180 @@ __device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, 
 }
 
 // ---------------------------------------------------------------------------
-// The tail split on CUDA cores: tokens [t_tail, l) in rounds of up to
-// kTailTok, each staged in one round of copies (fp16 residual rows, packed
-// rows and the key groups' scales / zeros); then scores with four threads per
-// token (32 channels each), the softmax of a head per warp, and the value
-// sum with one thread per channel.  Keys and values of packed rows are
-// dequantized as fl(fl(c * s) + z), the reconstruction of the notebook
-// "KIVI - 2-bit KV cache quantisation".  Leaves the partial of the whole CTA
-// in warp 0's slots (the other warps' slots empty).
+// A tail split on CUDA cores: tokens [c0, c0 + n), n <= kTailTok, of the tail
+// [t_tail, l), staged in one round of copies (fp16 residual rows, packed rows
+// and the key groups' scales / zeros); then scores with four threads per
+// token (32 channels each), the softmax of a head per warp, and the value sum
+// with one thread per channel.  Keys and values of packed rows are
+// dequantized as c * s + z with a single rounding, which equals the
+// notebook's fl(fl(c * s) + z) because c * s is exact in fp32.  Leaves the
+// partial of the CTA in warp 0's slots (the other warps' slots empty).
 template <int BITS>
 __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit, int b,
-                           int j0, int nh, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
+                           int j0, int nh, int c0, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;  // packed row bytes
   constexpr int CPR = RB / 16;             // 16-byte chunks per packed row
   TailSmem& ts = sm.tail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int d = tid;  // value phase: this thread's channel
+  const int n = min(kTailTok, a.l - c0);
+  const int nk = max(0, min(n, a.nq_k - c0));  // rows [0, nk) hold packed keys
+  const int nv = max(0, min(n, a.nq_v - c0));  // rows [0, nv) hold packed values
 
-  for (int i = tid; i < kNH * kHeadDim; i += blockDim.x) {
-    const int j = i / kHeadDim, dd = i % kHeadDim;
-    ts.q[j][dd] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + dd, a.q_dtype) * a.scale_log2
-                         : 0.0f;
-  }
-  if (tid < kNH) {
-    ts.mrun[tid] = -INFINITY;
-    ts.lrun[tid] = 0.0f;
-  }
-  float o[kNH] = {0.0f, 0.0f, 0.0f, 0.0f};
-
-  for (int c0 = a.t_tail; c0 < a.l; c0 += kTailTok) {
-    const int n = min(kTailTok, a.l - c0);
-    const int nk = max(0, min(n, a.nq_k - c0));  // rows [0, nk) hold packed keys
-    const int nv = max(0, min(n, a.nq_v - c0));  // rows [0, nv) hold packed values
-    __syncthreads();  // the previous round is done with every buffer
-
-    // ---- stage the round (c0 is a multiple of 32, so its packed keys span
-    //      at most two key groups) ----
-    for (int i = tid; i < n * 16; i += blockDim.x) {
-      const int r = i >> 4, c = i & 15;
-      const long t = c0 + r;
-      if (r < nk) {
-        if (c < CPR) cp_async16(&ts.krow[r][c], cv.codes_k + (unit * cv.Tcap + t) * RB + 16 * c);
-      } else {
-        cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
-      }
-      if (r < nv) {
-        if (c < CPR) {
-          cp_async16(&ts.vrow[r][c], cv.codes_v + (unit * cv.Tcap + t) * RB + 16 * c);
-        } else if (c == CPR) {
-          const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup);
-          char* dst = reinterpret_cast<char*>(&ts.vrow[r][c]);
-          cp_async8(dst, cv.scale_v + so);
-          cp_async8(dst + 8, cv.zero_v + so);
-        }
-      } else {
-        cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
-      }
+  // ---- stage the round (c0 is a multiple of 32, so its packed keys span at
+  //      most two key groups), and q ----
+  for (int i = tid; i < n * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    const long t = c0 + r;
+    if (r < nk) {
+      if (c < CPR) cp_async16(&ts.krow[r][c], cv.codes_k + (unit * cv.Tcap + t) * RB + 16 * c);
+    } else {
+      cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
     }
-    const int ngk = (nk + kGroup - 1) / kGroup;
-    for (int i = tid; i < ngk * 32; i += blockDim.x) {
-      const int gi = i >> 5, arr = (i >> 4) & 1, c = i & 15;
-      const long go = (unit * (cv.Tcap / kGroup) + c0 / kGroup + gi) * kHeadDim + 8 * c;
-      cp_async16(&ts.kg[gi][arr][4 * c], (arr ? cv.zero_k : cv.scale_k) + go);
+    if (r < nv) {
+      if (c < CPR) {
+        cp_async16(&ts.vrow[r][c], cv.codes_v + (unit * cv.Tcap + t) * RB + 16 * c);
+      } else if (c == CPR) {
+        const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup);
+        char* dst = reinterpret_cast<char*>(&ts.vrow[r][c]);
+        cp_async8(dst, cv.scale_v + so);
+        cp_async8(dst + 8, cv.zero_v + so);
+      }
+    } else {
+      cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
     }
-    cp_async_commit();
-    cp_async_wait<0>();
-    __syncthreads();
+  }
+  const int ngk = (nk + kGroup - 1) / kGroup;
+  for (int i = tid; i < ngk * 32; i += blockDim.x) {
+    const int gi = i >> 5, arr = (i >> 4) & 1, c = i & 15;
+    const long go = (unit * (cv.Tcap / kGroup) + c0 / kGroup + gi) * kHeadDim + 8 * c;
+    cp_async16(&ts.kg[gi][arr][4 * c], (arr ? cv.zero_k : cv.scale_k) + go);
+  }
+  cp_async_commit();
+  {
+    float qj[kNH];
+#pragma unroll
+    for (int j = 0; j < kNH; ++j)
+      qj[j] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + tid, a.q_dtype) * a.scale_log2 : 0.0f;
+    ts.q4[tid] = make_float4(qj[0], qj[1], qj[2], qj[3]);
+  }
+  cp_async_wait<0>();
+  __syncthreads();
 
-    // ---- scores: thread (token r, quarter qq) sums channels 32qq .. +31 ----
+  // ---- scores: thread (token r, quarter qq) sums channels 32qq .. +31 ----
 #pragma unroll 1
-    for (int it = 0; it < kTailTok / 32; ++it) {
-      const int r = (tid >> 2) + 32 * it, qq = tid & 3;
-      float acc[kNH] = {0.0f, 0.0f, 0.0f, 0.0f};
-      if (r < nk) {
-        const int gi = r >> 5;
-        const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.krow[r][0]) + qq * 32 * BITS / 8;
-        const __half* sk = reinterpret_cast<const __half*>(ts.kg[gi][0]) + 32 * qq;
-        const __half* zk = reinterpret_cast<const __half*>(ts.kg[gi][1]) + 32 * qq;
+  for (int it = 0; it < kTailTok / 32; ++it) {
+    const int r = (tid >> 2) + 32 * it, qq = tid & 3;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nk) {
+      const int gi = r >> 5;
+      const uint32_t* cw4 = reinterpret_cast<const uint32_t*>(&ts.krow[r][0]) + qq * BITS;
+      const uint32_t* sk = ts.kg[gi][0] + 16 * qq;  // fp16 pairs of channels 32qq ..
+      const uint32_t* zk = ts.kg[gi][1] + 16 * qq;
 #pragma unroll
-        for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
-          const uint32_t cw = reinterpret_cast<const uint32_t*>(row)[w];
+      for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
+        const uint32_t cw = cw4[w];
 #pragma unroll
-          for (int e = 0; e < 32 / BITS; ++e) {
-            const int dq = w * (32 / BITS) + e;
-            const float kx = __fadd_rn(__fmul_rn((float)((cw >> (BITS * e)) & L), __half2float(sk[dq])),
-                                       __half2float(zk[dq]));
+        for (int e = 0; e < 32 / BITS; e += 2) {
+          const int dq = w * (32 / BITS) + e;  // even channel of a scale / zero pair
+          const float2 sp = __half22float2(*reinterpret_cast<const __half2*>(&sk[dq >> 1]));
+          const float2 zp = __half22float2(*reinterpret_cast<const __half2*>(&zk[dq >> 1]));
 #pragma unroll
-            for (int j = 0; j < kNH; ++j) acc[j] = fmaf(kx, ts.q[j][32 * qq + dq], acc[j]);
+          for (int u = 0; u < 2; ++u) {
+            // the code as an exact float: its bits under the exponent of 2^23
+            const float cf = __uint_as_float(((cw >> (BITS * (e + u))) & L) | 0x4B000000u) - 8388608.0f;
+            const float kx = fmaf(cf, u ? sp.y : sp.x, u ? zp.y : zp.x);
+            const float4 qv = ts.q4[32 * qq + dq + u];
+            acc.x = fmaf(kx, qv.x, acc.x);
+            acc.y = fmaf(kx, qv.y, acc.y);
+            acc.z = fmaf(kx, qv.z, acc.z);
+            acc.w = fmaf(kx, qv.w, acc.w);
           }
         }
-      } else if (r < n) {
+      }
+    } else if (r < n) {
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          const int c = 4 * qq + c4;
-          const uint4 kv = ts.krow[r][c ^ (r & 7)];
-          const float kf[8] = {h_lo(kv.x), h_hi(kv.x), h_lo(kv.y), h_hi(kv.y),
-                               h_lo(kv.z), h_hi(kv.z), h_lo(kv.w), h_hi(kv.w)};
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int c = 4 * qq + c4;
+        const uint4 kv = ts.krow[r][c ^ (r & 7)];
+        const float kf[8] = {h_lo(kv.x), h_hi(kv.x), h_lo(kv.y), h_hi(kv.y),
+                             h_lo(kv.z), h_hi(kv.z), h_lo(kv.w), h_hi(kv.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-#pragma unroll
-            for (int j = 0; j < kNH; ++j) acc[j] = fmaf(kf[e], ts.q[j][8 * c + e], acc[j]);
+        for (int e = 0; e < 8; ++e) {
+          const float4 qv = ts.q4[8 * c + e];
+          acc.x = fmaf(kf[e], qv.x, acc.x);
+          acc.y = fmaf(kf[e], qv.y, acc.y);
+          acc.z = fmaf(kf[e], qv.z, acc.z);
+          acc.w = fmaf(kf[e], qv.w, acc.w);
         }
       }
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        acc[j] += __shfl_xor_sync(kFull, acc[j], 1);
-        acc[j] += __shfl_xor_sync(kFull, acc[j], 2);
-      }
-      if (qq == 0 && r < n)
-#pragma unroll
-        for (int j = 0; j < kNH; ++j) ts.p[j][r] = acc[j];
     }
-    __syncthreads();
-
-    // ---- softmax over the round, one warp per head ----
-    {
-      const int j = warp;  // kWarps == kNH
-      const float x0 = lane < n ? ts.p[j][lane] : -INFINITY;
-      const float x1 = lane + 32 < n ? ts.p[j][lane + 32] : -INFINITY;
-      const float mo = ts.mrun[j];
-      const float mn = fmaxf(mo, warp_max(fmaxf(x0, x1)));
-      const float e0 = lane < n ? fast_exp2(x0 - mn) : 0.0f;
-      const float e1 = lane + 32 < n ? fast_exp2(x1 - mn) : 0.0f;
-      ts.p[j][lane] = e0;
-      ts.p[j][lane + 32] = e1;
-      const float sum = warp_sum(e0 + e1);
-      __syncwarp();
-      if (lane == 0) {
-        const float corr = mo == -INFINITY ? 0.0f : fast_exp2(mo - mn);
-        ts.corr[j] = corr;
-        ts.mrun[j] = mn;
-        ts.lrun[j] = ts.lrun[j] * corr + sum;
-      }
-    }
-    __syncthreads();
-
-    // ---- values: thread d accumulates channel d of the kNH heads ----
 #pragma unroll
-    for (int j = 0; j < kNH; ++j) o[j] *= ts.corr[j];
-    const int vpos = v_unit_pos(d >> 2);
-    const int vsh = BITS * (d & 3);
+    for (int sh = 1; sh <= 2; sh <<= 1) {
+      acc.x += __shfl_xor_sync(kFull, acc.x, sh);
+      acc.y += __shfl_xor_sync(kFull, acc.y, sh);
+      acc.z += __shfl_xor_sync(kFull, acc.z, sh);
+      acc.w += __shfl_xor_sync(kFull, acc.w, sh);
+    }
+    if (qq == 0 && r < n) ts.p4[r] = acc;
+  }
+  __syncthreads();
+
+  // ---- softmax of head `warp` over the round ----
+  {
+    const int j = warp;  // kWarps == kNH
+    float* pj = reinterpret_cast<float*>(ts.p4) + j;
+    const float x0 = lane < n ? pj[4 * lane] : -INFINITY;
+    const float x1 = lane + 32 < n ? pj[4 * (lane + 32)] : -INFINITY;
+    const float mx = warp_max(fmaxf(x0, x1));
+    const float e0 = lane < n ? fast_exp2(x0 - mx) : 0.0f;
+    const float e1 = lane + 32 < n ? fast_exp2(x1 - mx) : 0.0f;
+    pj[4 * lane] = e0;
+    pj[4 * (lane + 32)] = e1;
+    const float sum = warp_sum(e0 + e1);
+    if (lane == 0) {
+      ts.mh[j] = mx;
+      ts.lh[j] = sum;
+    }
+  }
+  __syncthreads();
+
+  // ---- values: thread d accumulates channel d of the kNH heads ----
+  const int d = tid;
+  const int vpos = v_unit_pos(d >> 2);
+  const int vsh = BITS * (d & 3);
+  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-    for (int r = 0; r < n; ++r) {
-      float vx;
-      if (r < nv) {
-        const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
-        uint32_t cb;
-        if constexpr (BITS == 2) cb = row[vpos];
-        else cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
-        const __half* svz = reinterpret_cast<const __half*>(row + RB);
-        vx = __fadd_rn(__fmul_rn((float)((cb >> vsh) & L), __half2float(svz[d >> 5])),
-                       __half2float(svz[4 + (d >> 5)]));
-      } else {
-        const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
-        vx = __half2float(row[d & 7]);
-      }
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) o[j] = fmaf(ts.p[j][r], vx, o[j]);
+  for (int r = 0; r < n; ++r) {
+    float vx;
+    if (r < nv) {
+      const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
+      uint32_t cb;
+      if constexpr (BITS == 2) cb = row[vpos];
+      else cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
+      const __half* svz = reinterpret_cast<const __half*>(row + RB);
+      const float cf = __uint_as_float(((cb >> vsh) & L) | 0x4B000000u) - 8388608.0f;
+      vx = fmaf(cf, __half2float(svz[d >> 5]), __half2float(svz[4 + (d >> 5)]));
+    } else {
+      const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
+      vx = __half2float(row[d & 7]);
     }
+    const float4 pr = ts.p4[r];
+    o.x = fmaf(pr.x, vx, o.x);
+    o.y = fmaf(pr.y, vx, o.y);
+    o.z = fmaf(pr.z, vx, o.z);
+    o.w = fmaf(pr.w, vx, o.w);
   }
   __syncthreads();  // every thread is done with the staged rows (the merge area)
 
   float* mo0 = merge_area(sm, 0, kPathTail);
-#pragma unroll
-  for (int j = 0; j < kNH; ++j) mo0[j * kHeadDim + d] = o[j];
+  mo0[0 * kHeadDim + d] = o.x;
+  mo0[1 * kHeadDim + d] = o.y;
+  mo0[2 * kHeadDim + d] = o.z;
+  mo0[3 * kHeadDim + d] = o.w;
   if (lane < kNH) {
-    s_m[warp][lane] = warp == 0 ? ts.mrun[lane] : -INFINITY;
-    s_l[warp][lane] = warp == 0 ? ts.lrun[lane] : 0.0f;
+    s_m[warp][lane] = warp == 0 ? ts.mh[lane] : -INFINITY;
+    s_l[warp][lane] = warp == 0 ? ts.lh[lane] : 0.0f;
   }
 }
 
@@ -858,18 +864,33 @@ __device__ void build_q_tables(WarpSmem& s, const AttnArgs& a, int b, int j0, in
   }
 }
 
+// Copy sources of one (batch, kv-head) unit; tile t of each array starts at
+// base + t * (bytes per tile).
+struct UnitSrc {
+  const char *kc, *vc, *sk, *zk, *sv, *zv;
+};
+
+__device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
+  UnitSrc u;
+  u.kc = reinterpret_cast<const char*>(cv.codes_k + unit * cv.Tcap * 32);
+  u.vc = reinterpret_cast<const char*>(cv.codes_v + unit * cv.Tcap * 32);
+  u.sk = reinterpret_cast<const char*>(cv.scale_k + unit * (cv.Tcap / kGroup) * kHeadDim);
+  u.zk = reinterpret_cast<const char*>(cv.zero_k + unit * (cv.Tcap / kGroup) * kHeadDim);
+  u.sv = reinterpret_cast<const char*>(cv.scale_v + unit * cv.Tcap * (kHeadDim / kGroup));
+  u.zv = reinterpret_cast<const char*>(cv.zero_v + unit * cv.Tcap * (kHeadDim / kGroup));
+  return u;
+}
+
 // Bulk copies of packed tile `tile` into a stage (one lane).
-__device__ __forceinline__ void issue_tile(TileBuf& tb, unsigned long long* bar, const CacheView& cv,
-                                           long unit, int tile) {
-  const long row0 = unit * cv.Tcap + (long)tile * 32;
-  const long g0 = (unit * (cv.Tcap / kGroup) + tile) * kHeadDim;
+__device__ __forceinline__ void issue_tile(TileBuf& tb, unsigned long long* bar, const UnitSrc& u, int tile) {
+  const long o1k = (long)tile * 1024, o256 = (long)tile * 256;
   mbar_expect_tx(bar, kTileBytes);
-  bulk_g2s(tb.kc, cv.codes_k + row0 * 32, 1024u, bar);
-  bulk_g2s(tb.vc, cv.codes_v + row0 * 32, 1024u, bar);
-  bulk_g2s(tb.sk, cv.scale_k + g0, 256u, bar);
-  bulk_g2s(tb.zk, cv.zero_k + g0, 256u, bar);
-  bulk_g2s(tb.sv, cv.scale_v + row0 * (kHeadDim / kGroup), 256u, bar);
-  bulk_g2s(tb.zv, cv.zero_v + row0 * (kHeadDim / kGroup), 256u, bar);
+  bulk_g2s(tb.kc, u.kc + o1k, 1024u, bar);
+  bulk_g2s(tb.vc, u.vc + o1k, 1024u, bar);
+  bulk_g2s(tb.sk, u.sk + o256, 256u, bar);
+  bulk_g2s(tb.zk, u.zk + o256, 256u, bar);
+  bulk_g2s(tb.sv, u.sv + o256, 256u, bar);
+  bulk_g2s(tb.zv, u.zv + o256, 256u, bar);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -897,9 +918,11 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
     mbar_fence_init();
   }
   __syncwarp();
+  const UnitSrc us = unit_src(cv, unit);
+  const int t_first = tile0 + warp;  // this warp's tiles: t_first + kWarps * k
   int issued = min(n_mine, kStages);
   if (lane == 0)
-    for (int k = 0; k < issued; ++k) issue_tile(st[k], &bars[k], cv, unit, tile0 + warp + kWarps * k);
+    for (int k = 0; k < issued; ++k) issue_tile(st[k], &bars[k], us, t_first + kWarps * k);
   build_q_tables(ws, a, b, j0, nh);
   __syncthreads();
   const float ks = ws.qscale[tig];
@@ -913,20 +936,33 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
 #pragma unroll
   for (int i = 0; i < 4; ++i) Z[i] = 0.0f;
 
+  // The ring is walked kStages tiles per round so that every stage address
+  // is a constant.
   int done = 0;
-  for (int k = 0; k < n_mine; ++k) {
-    const int stage = k % kStages;
-    const bool ok = mbar_wait(&bars[stage], (uint32_t)((k / kStages) & 1));
-    if (__any_sync(kFull, !ok)) break;
-    done = k + 1;
-    mma_tile(ws, st[stage], pb, g, tig, ks, m_run, lsum, O, Z);
-    __syncwarp();  // every lane is done with the stage and the weight buffer
-    if (k + kStages < n_mine) {
-      if (lane == 0) {
-        fence_proxy_async();
-        issue_tile(st[stage], &bars[stage], cv, unit, tile0 + warp + kWarps * (k + kStages));
+  bool failed = false;
+  for (int k0 = 0; k0 < n_mine && !failed; k0 += kStages) {
+    const uint32_t parity = (uint32_t)((k0 / kStages) & 1);
+#pragma unroll
+    for (int sg = 0; sg < kStages; ++sg) {
+      const int k = k0 + sg;
+      if (k < n_mine && !failed) {
+        bool ok = mbar_try_wait(&bars[sg], parity);
+        if (!ok) ok = mbar_wait(&bars[sg], parity);
+        if (__any_sync(kFull, !ok)) {
+          failed = true;
+        } else {
+          done = k + 1;
+          mma_tile(ws, st[sg], pb, g, tig, ks, m_run, lsum, O, Z);
+          __syncwarp();  // every lane is done with the stage and the weight buffer
+          if (k + kStages < n_mine) {
+            if (lane == 0) {
+              fence_proxy_async();
+              issue_tile(st[sg], &bars[sg], us, t_first + kWarps * (k + kStages));
+            }
+            ++issued;
+          }
+        }
       }
-      ++issued;
     }
   }
   if (done < n_mine) {
@@ -1013,14 +1049,15 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
   const int nh = min(kNH, grp - hc * kNH);
   const long unit = (long)b * cv.H + h;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int path = s == 0 ? kPathTail : (BITS == 2 ? kPathMma : kPathV1);
+  const int path = s < a.tail_splits ? kPathTail : (BITS == 2 ? kPathMma : kPathV1);
+  const int sp = s - a.tail_splits;  // packed split index
 
   if (path == kPathTail) {
-    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, s_m, s_l);
+    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, a.t_tail + s * kTailTok, s_m, s_l);
   } else if (path == kPathV1) {
     // ---- CUDA cores: packed tiles at 4 bits ----
-    const int t_begin = (s - 1) * a.chunk;
-    const int t_end = min(a.t_tail, s * a.chunk);
+    const int t_begin = sp * a.chunk;
+    const int t_end = min(a.t_tail, (sp + 1) * a.chunk);
     for (int i = threadIdx.x; i < kNH * kHeadDim; i += blockDim.x) {
       const int j = i / kHeadDim, d = i % kHeadDim;
       sm.v1.q[j][d] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + d, a.q_dtype) * a.scale_log2
@@ -1050,9 +1087,9 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
     for (int j = 0; j < kNH; ++j)
       *reinterpret_cast<float4*>(&mo[j * kHeadDim + 4 * lane]) = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
   } else {
-    // ---- tensor cores: packed tiles [(s-1)*chunk, min(t_tail, s*chunk)) ----
-    const int tile0 = (s - 1) * a.chunk / 32;
-    const int tile1 = min(a.t_tail, s * a.chunk) / 32;
+    // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
+    const int tile0 = sp * a.chunk / 32;
+    const int tile1 = min(a.t_tail, (sp + 1) * a.chunk) / 32;
     packed_split(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();

@@ -74,37 +74,44 @@ long attention_units(const kivi_config& c) {
   return (long)c.batch * c.n_kv_heads * ((grp + kivi::kHeadChunk - 1) / kivi::kHeadChunk);
 }
 
-// Upper bound on the packed-tile splits: the tail split plus the tile splits
+// Tail splits at most: the tail [floor32(l - R), l) holds fewer than R + 32
+// tokens.
+int max_tail_splits(const kivi_config& c) {
+  return (c.residual + 31 + kivi::kTailTok - 1) / kivi::kTailTok;
+}
+
+// Upper bound on the packed-tile splits: the tail splits plus the tile splits
 // of every unit fit one wave of kivi::kAttnCtasPerSm CTAs per SM of a GB300,
 // and the partials merge in at most two levels.
 int max_tile_splits(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u - 1;
+  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u - max_tail_splits(c);
   if (s < 1) s = 1;
-  if (s > kivi::kMaxSplits - 1) s = kivi::kMaxSplits - 1;
+  if (s > kivi::kMaxSplits - max_tail_splits(c)) s = kivi::kMaxSplits - max_tail_splits(c);
   const long by_len = (c.max_tokens + 31) / 32;
   return (int)(s < by_len ? s : by_len);
 }
 
-// Split 0 is the tail, splits 1.. the packed tiles.
-int max_splits(const kivi_config& c) { return 1 + max_tile_splits(c); }
+int max_splits(const kivi_config& c) { return max_tail_splits(c) + max_tile_splits(c); }
 
-// Splits used at length l, the tail start and the (32-aligned) tokens per
-// packed split.  Automatic splits take at least 256 tokens and a multiple of
-// four tiles, so that the four warps of a CTA get equal shares.
-void split_plan(const kivi_cache* c, int l, int* splits, int* chunk, int* t_tail) {
+// Splits used at length l: tail splits of kTailTok tokens from t_tail, then
+// packed splits of `chunk` (32-aligned) tokens.  Automatic packed splits take
+// at least 256 tokens and a multiple of four tiles, so that the four warps of
+// a CTA get equal shares; an override n asks for n splits in all.
+void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail) {
   const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
   *t_tail = tt;
+  *tail_splits = (l - tt + kivi::kTailTok - 1) / kivi::kTailTok;
   const int tiles = tt / 32;
   if (tiles == 0) {
-    *splits = 1;
+    *splits = *tail_splits;
     *chunk = 32;
     return;
   }
   const int smax = max_tile_splits(c->cfg);
   int per;  // tiles per packed split
   if (c->splits_override > 0) {
-    int s = c->splits_override - 1;
+    int s = c->splits_override - *tail_splits;
     if (s > smax) s = smax;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
@@ -116,7 +123,7 @@ void split_plan(const kivi_cache* c, int l, int* splits, int* chunk, int* t_tail
   }
   const int ch = per * 32;
   *chunk = ch;
-  *splits = 1 + (tt + ch - 1) / ch;  // no empty split
+  *splits = *tail_splits + (tt + ch - 1) / ch;  // no empty split
 }
 
 // Workspace layout (attention group gid = (b, kv-head, head chunk), S = max
@@ -230,8 +237,8 @@ KIVI_API kivi_status kivi_set_attention_splits(kivi_cache* c, int n_splits) {
 
 KIVI_API int kivi_attention_splits(const kivi_cache* c, int l) {
   if (!c || l <= 0) return 0;
-  int s, ch, tt;
-  split_plan(c, l, &s, &ch, &tt);
+  int ts, s, ch, tt;
+  split_plan(c, l, &ts, &s, &ch, &tt);
   return s;
 }
 
@@ -254,7 +261,7 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   a.l = c->length;
   a.nq_k = nq_k(c->length, c->cfg.residual);
   a.nq_v = nq_v(c->length, c->cfg.residual);
-  split_plan(c, c->length, &a.splits, &a.chunk, &a.t_tail);
+  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail);
   const WsLayout w = ws_layout(c->cfg);
   char* ws = static_cast<char*>(workspace);
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
@@ -363,7 +370,7 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   a.l = c->length;
   a.nq_k = nq_k(c->length, c->cfg.residual);
   a.nq_v = nq_v(c->length, c->cfg.residual);
-  split_plan(c, c->length, &a.splits, &a.chunk, &a.t_tail);
+  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail);
   char* base = static_cast<char*>(ws);
   a.ws_o = reinterpret_cast<float*>(base + w.o_off);
   a.ws_ml = reinterpret_cast<float*>(base + w.ml_off);

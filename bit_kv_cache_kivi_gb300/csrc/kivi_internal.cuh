@@ -13,6 +13,7 @@ constexpr int kTargetSMs = 152;    // GB300 SM count used by the split policy
 constexpr int kAttnCtasPerSm = 4;  // attention CTAs resident per SM (registers, shared memory)
 constexpr int kHeadChunk = 4;      // query heads per attention CTA
 constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two levels at most)
+constexpr int kTailTok = 64;       // tail tokens per tail split
 constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
 
 // Device view of one cache: the eight buffers plus its shape.
@@ -45,11 +46,12 @@ struct AttnArgs {
   int Hq;
   float scale_log2;  // softmax scale * log2(e)
   int l, nq_k, nq_v;
-  // Context split: split 0 covers the tail [t_tail, l) (t_tail = nq_v rounded
-  // down to 32); split s >= 1 covers the packed tiles [(s-1)*chunk,
-  // min(t_tail, s*chunk)).
+  // Context split: splits s < tail_splits cover the tail [t_tail, l) (t_tail
+  // = nq_v rounded down to 32), kTailTok tokens each from t_tail + s*kTailTok;
+  // split tail_splits + i covers the packed tiles [i*chunk, min(t_tail,
+  // (i+1)*chunk)).
   int t_tail;
-  int splits, chunk;
+  int tail_splits, splits, chunk;
   // Split partials of attention group gid = (b, kv-head, head chunk):
   float* ws_o;        // [gid][splits][kHeadChunk][D]  output sums
   float* ws_ml;       // [gid][splits][kHeadChunk][2]  (max in log2 units, sum)

@@ -126,7 +126,10 @@ kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
                                void *stream);
 
 /* Device workspace (bytes) kivi_decode_attention needs for this handle's
- * shape at any length: split-K partial results and per-group counters.
+ * shape at any length: split-K partial results, merged groups of partials,
+ * counters, and a status word (the int at byte offset bytes - 16: nonzero
+ * after a kernel gave up waiting for its staged data, which only a device
+ * fault can cause; it stays set until the workspace is next cleared).
  * Host only. */
 size_t kivi_attention_workspace_bytes(const kivi_cache *c);
 
@@ -134,9 +137,10 @@ size_t kivi_attention_workspace_bytes(const kivi_cache *c);
  * out = softmax(q K^T * scale) V; §3.2 System-Level: dequantization fused
  * into the products).  q: device [B][n_q_heads][D] of q_dtype; out: device
  * [B][n_q_heads][D] of q_dtype.  softmax_scale <= 0 means 1/sqrt(D).
- * The context is split along the tokens; the CTA that finishes last for a
- * (batch, kv-head) merges the partial (max, sum, output) triples, all in one
- * kernel launch.
+ * The context is split along the tokens; the CTA that finishes last in a
+ * group of up to 16 splits of a (batch, kv-head) merges their partial (max,
+ * sum, output) triples, and with more groups the last group merges the
+ * groups, all in one kernel launch.
  * workspace: device, 16-byte aligned, ws_bytes >= kivi_attention_workspace_bytes.
  * It carries a small counter area between calls: the first call that sees a
  * given workspace pointer zeroes it (one cudaMemsetAsync on the stream) and
@@ -148,12 +152,14 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
                                   float softmax_scale, void *workspace,
                                   size_t ws_bytes, void *stream);
 
-/* Override the number of context splits (0 = automatic).  Split 0 always
- * takes the tail of the context that is still fp16 (plus the partial value
- * group before it); the other splits share the packed 32-token tiles.  The
- * automatic choice keeps the whole grid within one wave of three CTAs per SM
- * of a 152-SM GB300, with at least 256 tokens per split.  The value is clamped to the workspace bound
- * and to one split per 32-token tile. */
+/* Override the number of context splits (0 = automatic).  The first splits
+ * always take the tail of the context that is still fp16 (plus the partial
+ * value group before it), 64 tokens each; the others share the packed
+ * 32-token tiles.  The automatic choice keeps the whole grid within one wave
+ * of four CTAs per SM of a 152-SM GB300, with at least eight tiles per packed
+ * split and a multiple of four.  An override n asks for n splits in all; it
+ * is clamped to the workspace bound, to one packed split per 32-token tile
+ * and to at least one packed split. */
 kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 
 /* Splits the next kivi_decode_attention call will use at length l. */
