@@ -611,8 +611,7 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -642,6 +641,9 @@ constexpr float kTwo24 = 16777216.0f;  // undoes the 2^-24 of the subnormal code
 // more than this (log2 units), so p <= 2^0.5 and p * s stays below the fp16
 // maximum for any fp16 scale s = range / 3.
 constexpr float kLazyMax = 0.5f;
+// A raised running max is set this far above the tile max (log2 units), so
+// that later tiles rarely raise it again.
+constexpr float kLazySlack = 1.0f;
 
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
 // (head g >> 1, part g & 1).  Fragment order: k-step ks uses word m = tig +
@@ -684,15 +686,11 @@ __device__ __forceinline__ int pbuf_pos(int t) {
   return 8 * (t & 3) + 4 * (t >> 4) + 2 * ((t >> 3) & 1) + ((t >> 2) & 1);
 }
 
-// One staged 32-token tile for the four heads of the CTA, online softmax.
-// Scores: lane (g, tig) gets head tig at tokens g + 8r.  Values: the k rows
-// (2tig, 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows
-// (2tig+8, 2tig+9) tokens t0 + 8 and t0 + 12, so that the lanes of a
-// shared-memory phase read distinct banks.  m_run, lsum, O and Z belong to
-// head tig; ks = 2^E_tig * scale * log2(e).
-__device__ __forceinline__ void mma_tile(const WarpSmem& ws, const TileBuf& tb, float* pb, int g, int tig,
-                                         float ks, float& m_run, float& lsum, float (&O)[8][4],
-                                         float (&Z)[4]) {
+// Scores of one staged 32-token tile for the four heads of the CTA: lane
+// (g, tig) gets head tig at tokens g + 8r (sc[r], log2 units);
+// ks = 2^E_tig * scale * log2(e).
+__device__ __forceinline__ void key_scores(const WarpSmem& ws, const TileBuf& tb, int g, int tig, float ks,
+                                           float (&sc)[4]) {
   // ---- beta = zK x q: every A row is the zero vector, so D[., (tig, part)] = beta ----
   float beta4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -714,10 +712,9 @@ __device__ __forceinline__ void mma_tile(const WarpSmem& ws, const TileBuf& tb, 
   const float kb = (beta4[0] + beta4[1]) * ks;
   const float k24 = ks * kTwo24;
 
-  // ---- scores S = codes x Q' + beta (log2 units) ----
+  // ---- scores S = codes x Q' + beta ----
   uint32_t bq[8][2];
   build_qprime(ws, tb.sk, g, tig, bq);
-  float sc[4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
     const uint32_t* rg = tb.kc + (16 * mt + g) * 8;      // key row 16mt + g
@@ -738,14 +735,21 @@ __device__ __forceinline__ void mma_tile(const WarpSmem& ws, const TileBuf& tb, 
     sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
     sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
   }
+}
 
-  // ---- online softmax of head tig over the 32 tokens (8 lanes share it) ----
+// Online softmax of head tig over one tile's scores (8 lanes share a head):
+// when a score exceeds the running max by more than kLazyMax, the max is
+// raised to the tile max plus kLazySlack and what the earlier tiles left in
+// lsum, O and Z is rescaled.  The weights p = 2^(S - max) <= 2^kLazyMax go to
+// the warp's weight buffer.
+__device__ __forceinline__ void softmax_p(const float (&sc)[4], float* pb, int g, int tig, float& m_run,
+                                          float& lsum, float (&O)[8][4], float (&Z)[4]) {
   float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
   if (__any_sync(kFull, tmax > m_run + kLazyMax)) {
-    const float mnew = fmaxf(m_run, tmax);
+    const float mnew = tmax > m_run + kLazyMax ? tmax + kLazySlack : m_run;
     const float corr = fast_exp2(m_run - mnew);  // 0 on the first tile
     m_run = mnew;
     lsum *= corr;
@@ -763,9 +767,15 @@ __device__ __forceinline__ void mma_tile(const WarpSmem& ws, const TileBuf& tb, 
     lsum += p;
     prow[pbuf_pos(g + 8 * r)] = p;
   }
-  __syncwarp();
+}
 
-  // ---- values: O += codes^T x (p * sV), Z += zV^T x p ----
+// Values of one staged tile: O += codes^T x (p * sV), Z += zV^T x p, with p
+// from the warp's weight buffer (O and Z of head tig).  The k rows (2tig,
+// 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows (2tig+8,
+// 2tig+9) tokens t0 + 8 and t0 + 12, so that the lanes of a shared-memory
+// phase read distinct banks.
+__device__ __forceinline__ void value_acc(const TileBuf& tb, const float* pb, int g, int tig, float (&O)[8][4],
+                                          float (&Z)[4]) {
   const int part = g & 1;
   const float* pv = pb + (g >> 1) * 34 + 8 * tig;
   const int zsel = (g >> 1) & 1;  // zero word of value group g & 3 within a token
@@ -936,24 +946,43 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
 #pragma unroll
   for (int i = 0; i < 4; ++i) Z[i] = 0.0f;
 
-  // The ring is walked kStages tiles per round so that every stage address
-  // is a constant.
+  // Tile k's scores are computed one iteration ahead of its values: the
+  // scores of tile k + 1 and the values of tile k form one straight-line
+  // block (the wait for tile k + 1 comes first), so that their independent
+  // MMA chains can interleave.  The ring is walked kStages tiles per round so
+  // that every stage address is a constant.
   int done = 0;
   bool failed = false;
-  for (int k0 = 0; k0 < n_mine && !failed; k0 += kStages) {
-    const uint32_t parity = (uint32_t)((k0 / kStages) & 1);
+  float sc[4];
+  if (n_mine > 0) {
+    bool ok = mbar_try_wait(&bars[0], 0u);
+    if (!ok) ok = mbar_wait(&bars[0], 0u);
+    if (__any_sync(kFull, !ok)) {
+      failed = true;
+    } else {
+      key_scores(ws, st[0], g, tig, ks, sc);
+      softmax_p(sc, pb, g, tig, m_run, lsum, O, Z);
+      __syncwarp();
+    }
+  }
+  int k = 0;  // tile whose values are next
+  while (k + 1 < n_mine && !failed) {
 #pragma unroll
     for (int sg = 0; sg < kStages; ++sg) {
-      const int k = k0 + sg;
-      if (k < n_mine && !failed) {
-        bool ok = mbar_try_wait(&bars[sg], parity);
-        if (!ok) ok = mbar_wait(&bars[sg], parity);
+      // tile k sits in stage sg (k is a multiple of kStages at sg == 0)
+      if (k + 1 < n_mine && !failed) {
+        const int sn = sg + 1 == kStages ? 0 : sg + 1;  // stage of tile k + 1
+        const uint32_t parn = (uint32_t)(((k + 1) / kStages) & 1);
+        bool ok = mbar_try_wait(&bars[sn], parn);
+        if (!ok) ok = mbar_wait(&bars[sn], parn);
         if (__any_sync(kFull, !ok)) {
           failed = true;
         } else {
+          float scn[4];
+          key_scores(ws, st[sn], g, tig, ks, scn);
+          value_acc(st[sg], pb, g, tig, O, Z);
           done = k + 1;
-          mma_tile(ws, st[sg], pb, g, tig, ks, m_run, lsum, O, Z);
-          __syncwarp();  // every lane is done with the stage and the weight buffer
+          __syncwarp();  // every lane is done with stage sg and the weight buffer
           if (k + kStages < n_mine) {
             if (lane == 0) {
               fence_proxy_async();
@@ -961,9 +990,20 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
             }
             ++issued;
           }
+          softmax_p(scn, pb, g, tig, m_run, lsum, O, Z);
+          __syncwarp();
+          ++k;
         }
       }
     }
+  }
+  if (!failed && n_mine > 0) {
+    // the last tile's values (its stage: (n_mine - 1) % kStages)
+    const int sl = (n_mine - 1) % kStages;
+#pragma unroll
+    for (int sg = 0; sg < kStages; ++sg)
+      if (sg == sl) value_acc(st[sg], pb, g, tig, O, Z);
+    done = n_mine;
   }
   if (done < n_mine) {
     // A wait timed out: record it, and let every copy still in flight land

@@ -80,24 +80,35 @@ int max_tail_splits(const kivi_config& c) {
   return (c.residual + 31 + kivi::kTailTok - 1) / kivi::kTailTok;
 }
 
-// Upper bound on the packed-tile splits: the tail splits plus the tile splits
-// of every unit fit one wave of kivi::kAttnCtasPerSm CTAs per SM of a GB300,
-// and the partials merge in at most two levels.
-int max_tile_splits(const kivi_config& c) {
+// Splits per attention unit in one wave of kivi::kAttnCtasPerSm CTAs per SM
+// of a GB300, capped so that the partials merge in at most two levels.
+int split_budget(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u - max_tail_splits(c);
+  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u;
+  if (s > kivi::kMaxSplits) s = kivi::kMaxSplits;
+  return (int)s;
+}
+
+// Upper bound on the packed-tile splits at any length: what the budget leaves
+// beside the tail splits of a length with the fewest (one), at least one,
+// and at most one per 32-token tile.
+int max_tile_splits(const kivi_config& c) {
+  long s = split_budget(c) - 1;
   if (s < 1) s = 1;
-  if (s > kivi::kMaxSplits - max_tail_splits(c)) s = kivi::kMaxSplits - max_tail_splits(c);
   const long by_len = (c.max_tokens + 31) / 32;
   return (int)(s < by_len ? s : by_len);
 }
 
-int max_splits(const kivi_config& c) { return max_tail_splits(c) + max_tile_splits(c); }
+int max_splits(const kivi_config& c) {
+  const int a = max_tail_splits(c) + 1, b = 1 + max_tile_splits(c);
+  return a > b ? a : b;
+}
 
 // Splits used at length l: tail splits of kTailTok tokens from t_tail, then
-// packed splits of `chunk` (32-aligned) tokens.  Automatic packed splits take
-// at least 256 tokens and a multiple of four tiles, so that the four warps of
-// a CTA get equal shares; an override n asks for n splits in all.
+// packed splits of `chunk` (32-aligned) tokens.  Automatic packed splits fill
+// the budget beside this length's tail splits, with at least 256 tokens and a
+// multiple of four tiles each, so that the four warps of a CTA get equal
+// shares; an override n asks for n splits in all.
 void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail) {
   const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
   *t_tail = tt;
@@ -108,7 +119,9 @@ void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* 
     *chunk = 32;
     return;
   }
-  const int smax = max_tile_splits(c->cfg);
+  int smax = split_budget(c->cfg) - *tail_splits;
+  if (smax > max_splits(c->cfg) - *tail_splits) smax = max_splits(c->cfg) - *tail_splits;
+  if (smax < 1) smax = 1;
   int per;  // tiles per packed split
   if (c->splits_override > 0) {
     int s = c->splits_override - *tail_splits;

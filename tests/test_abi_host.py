@@ -114,7 +114,7 @@ def test_init_validation_and_host_state(K):
 def test_split_plan_and_workspace(K):
     """The first splits take the fp16 tail, 64 tokens each; the packed tiles
     [0, floor32(l - R)) are shared by up to floor(4 * 152 / units) - (tail
-    splits at most) splits of >= 8 tiles, a
+    splits) splits of >= 8 tiles, a
     multiple of four tiles each, so the grid fits one wave of four CTAs per
     SM and the four warps of a CTA get equal shares."""
     # Llama-3-8B decode shape: 64 (b, kv-head) units -> up to 8 tile splits;
@@ -134,12 +134,12 @@ def test_split_plan_and_workspace(K):
         assert K.kivi_attention_splits(h, 4097) == 9
     finally:
         K.kivi_cache_destroy(h)
-    # long context, R = 128: up to ceil(159 / 64) = 3 tail splits, so 8 units
-    # -> up to 73 tile splits; 4092 tiles -> 60 tiles per split -> 69 tile
-    # splits, plus 2 tail splits for the 128 tail tokens = 568 CTAs
+    # long context, R = 128: 8 units -> 76 splits per unit in one wave; the
+    # 128 tail tokens take 2, leaving 74 for 4092 tiles -> 56 tiles per split
+    # -> 74 tile splits: 608 CTAs, four per SM
     c = cfg(K, batch=1, n_kv_heads=8, n_q_heads=32, residual=128, max_tokens=131072)
     h = K.kivi_cache_init(c, _fake_buffers(K))
-    assert K.kivi_attention_splits(h, 131072) == 71
+    assert K.kivi_attention_splits(h, 131072) == 76
     K.kivi_cache_destroy(h)
     # GQA 18 -> five chunks of four query heads
     c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=18, max_tokens=1024)
