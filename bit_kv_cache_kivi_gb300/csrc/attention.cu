@@ -128,44 +128,40 @@ __device__ __forceinline__ float pick4(const float (&v)[4], int i) {
 // ---------------------------------------------------------------------------
 // Shared memory.
 
-struct V1Smem {                           // CUDA-core path (4-bit packed tiles)
-  float q[kNH][kHeadDim];                 // q * scale * log2(e)
-  // per warp, 32 rows of 256 B: q * sK of the tile's key group ([kNH][128]
-  // floats), then fp16 residual rows (16-byte chunks XOR-swizzled by row) and
-  // packed value rows (codes at the row start, scale[4] and zero[4] at byte
-  // 64); the merge area at the end
-  uint4 wbuf[kWarps][32 * 16];
-};
-
 // q tables in MMA fragment order.  Lane (g, tig) reads the 16 words of
 // column g (head g >> 1, part g & 1) for its tig, as four 16-byte quarters;
 // the layout [quarter][column][tig] spreads the 8 lanes of a shared-memory
-// phase over distinct banks.  Word w of (column, tig) holds channels
-// (16m + i, 16m + i + 8) with ks = w >> 1, m = tig + 4*(ks >> 2),
-// i = 2*(ks & 3) + (w & 1).
+// phase over distinct banks.  Word w (k-step ks = w >> 1) of (column, tig)
+// holds the channel pair of code position i:
+//   2 bits: word m = tig + 4*(ks >> 2) of a key row, i = 2*(ks & 3) + (w & 1),
+//           channels (16m + i, 16m + i + 8);
+//   4 bits: word m = tig + 4*(ks >> 1), i = 2*(ks & 1) + (w & 1),
+//           channels (8m + i, 8m + i + 4).
 //
 // A staged packed tile keeps the cache's own layouts (one bulk copy per
-// array): codes as 32-byte rows, key scales / zeros as fp16 [128], value
-// scales / zeros as fp16 [32 tokens][4 groups].
+// array): codes as (16 * BITS)-byte rows, key scales / zeros as fp16 [128],
+// value scales / zeros as fp16 [32 tokens][4 groups].
+template <int BITS>
 struct TileBuf {
-  uint32_t kc[256];                       // key codes
-  uint32_t vc[256];                       // value codes (group-interleaved rows)
+  uint32_t kc[128 * BITS];                // key codes
+  uint32_t vc[128 * BITS];                // value codes (group-interleaved rows)
   uint32_t sk[64], zk[64];
   uint32_t sv[64], zv[64];
 };
-constexpr int kStages = 3;                // tiles in flight per warp
-constexpr uint32_t kTileBytes = sizeof(TileBuf);
+template <int BITS>
+constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp
 
+template <int BITS>
 struct WarpSmem {
-  TileBuf st[kWarps][kStages];            // per-warp rings of staged tiles
-  uint4 qs[2][4][8][4];                   // q * 4^-e(d) as split_mul operands (xa, xb)
+  TileBuf<BITS> st[kWarps][kStagesOf<BITS>];  // per-warp rings of staged tiles
+  uint4 qs[2][4][8][4];                   // q * base^-e(i) as split_mul operands (xa, xb)
   uint4 qb[4][8][4];                      // q hi / lo
   float pbuf[kWarps][kNH][34];            // one tile's weights per warp, token order
                                           // 8 (t & 3) + 4 (t >> 4) + 2 ((t >> 3) & 1) + ((t >> 2) & 1)
   float qv[kNH][kHeadDim];                // q, staged for the tables
   float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
   int qexp[kNH];                          // E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
-  unsigned long long bar[kWarps][kStages];
+  unsigned long long bar[kWarps][kStagesOf<BITS>];
 };
 
 // A tail split: up to kTailTok tokens, each staged as a 256-byte key row and
@@ -182,21 +178,20 @@ struct TailSmem {
   float mh[kNH], lh[kNH];                 // per head: max and sum of the weights
 };
 
+template <int BITS>
 union SplitSmem {
-  V1Smem v1;
-  WarpSmem ws;
+  WarpSmem<BITS> ws;
   TailSmem tail;
 };
 
-enum Path { kPathV1 = 0, kPathMma = 1, kPathTail = 2 };
+enum Path { kPathMma = 1, kPathTail = 2 };
 
-// Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the warp
-// (CUDA cores) or the CTA (tensor cores, tail, after their last round) is
-// done with.
-__device__ __forceinline__ float* merge_area(SplitSmem& sm, int warp, int path) {
+// Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the CTA
+// is done with (its staged tiles or tail rows).
+template <int BITS>
+__device__ __forceinline__ float* merge_area(SplitSmem<BITS>& sm, int warp, int path) {
   if (path == kPathMma) return reinterpret_cast<float*>(&sm.ws.st[warp][0]);
-  if (path == kPathTail) return reinterpret_cast<float*>(&sm.tail.krow[0][0]) + warp * kNH * kHeadDim;
-  return reinterpret_cast<float*>(&sm.v1.wbuf[warp][0]);
+  return reinterpret_cast<float*>(&sm.tail.krow[0][0]) + warp * kNH * kHeadDim;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -215,18 +210,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
-
-// Stage residual rows [r0, r1) of a 32-token tile (ring slots (tt0 + r) mod R)
-// into a warp buffer: chunk c of row r goes to uint4 index 16r + (c ^ (r & 7)).
-__device__ __forceinline__ void stage_ring_rows(const __half* ring, long unit, int R, int tt0,
-                                                int r0, int r1, uint4* buf, int lane) {
-  for (int i = 16 * r0 + lane; i < 16 * r1; i += 32) {
-    const int r = i >> 4, c = i & 15;
-    cp_async16(&buf[16 * r + (c ^ (r & 7))],
-               ring + (unit * R + (tt0 + r) % R) * kHeadDim + 8 * c);
-  }
-  cp_async_commit();
-}
 
 // mbarrier + bulk copy (one elected thread issues; the barrier's transaction
 // count completes the phase when every byte has landed).
@@ -282,153 +265,6 @@ __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
 }
 
 // ---------------------------------------------------------------------------
-// CUDA-core path: tiles of [t_begin, t_end) that may hold fp16 residual rows.
-// Warp w walks 32-token tiles w, w+4, ...; in the key phase lane l owns token
-// tile+l, in the value phase lane l owns channels 4l..4l+3.
-template <int BITS>
-__device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit,
-                         int t_begin, int t_end, float (&m)[kNH], float (&lsum)[kNH],
-                         float (&o)[kNH][4]) {
-  constexpr int L = (1 << BITS) - 1;
-  constexpr int RB = kHeadDim * BITS / 8;
-  constexpr int CPW = 32 / BITS;
-  V1Smem& s = sm.v1;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint4* wbuf = s.wbuf[warp];
-  float* qk = reinterpret_cast<float*>(wbuf);
-  const int tile_end = (t_end + 31) / 32;
-  for (int tile = t_begin / 32 + warp; tile < tile_end; tile += kWarps) {
-    const int tt0 = tile * 32;
-    const int t = tt0 + lane;
-    const bool valid = t >= t_begin && t < t_end;
-    float sc[kNH];
-    if (tt0 + 32 <= a.nq_k) {
-      // packed keys: q' = q * sK[g] (to smem), beta = q . zK[g]
-      const long go = (unit * (cv.Tcap / kGroup) + tile) * kHeadDim + 4 * lane;
-      float skf[4], zkf[4];
-      halves4(*reinterpret_cast<const uint2*>(cv.scale_k + go), skf);
-      halves4(*reinterpret_cast<const uint2*>(cv.zero_k + go), zkf);
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        const float4 qv = *reinterpret_cast<const float4*>(&s.q[j][4 * lane]);
-        *reinterpret_cast<float4*>(&qk[j * kHeadDim + 4 * lane]) =
-            make_float4(qv.x * skf[0], qv.y * skf[1], qv.z * skf[2], qv.w * skf[3]);
-        sc[j] = warp_sum(qv.x * zkf[0] + qv.y * zkf[1] + qv.z * zkf[2] + qv.w * zkf[3]);
-      }
-      __syncwarp();
-      if (valid) {
-        const uint4* row = reinterpret_cast<const uint4*>(cv.codes_k + (unit * cv.Tcap + t) * RB);
-#pragma unroll
-        for (int w4 = 0; w4 < RB / 16; ++w4) {
-          const uint4 cw = row[w4];
-          const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-          for (int wi = 0; wi < 4; ++wi) {
-            const int dbase = (w4 * 4 + wi) * CPW;
-#pragma unroll
-            for (int e = 0; e < CPW; e += 4) {
-              const float c0 = (float)((words[wi] >> (BITS * (e + 0))) & L);
-              const float c1 = (float)((words[wi] >> (BITS * (e + 1))) & L);
-              const float c2 = (float)((words[wi] >> (BITS * (e + 2))) & L);
-              const float c3 = (float)((words[wi] >> (BITS * (e + 3))) & L);
-#pragma unroll
-              for (int j = 0; j < kNH; ++j) {
-                const float4 qkv = *reinterpret_cast<const float4*>(&qk[j * kHeadDim + dbase + e]);
-                sc[j] += qkv.x * c0 + qkv.y * c1 + qkv.z * c2 + qkv.w * c3;
-              }
-            }
-          }
-        }
-      }
-    } else {
-      // residual keys: stage the fp16 ring rows, then lane = token
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) sc[j] = 0.0f;
-      stage_ring_rows(cv.ring_k, unit, cv.R, tt0, max(t_begin - tt0, 0), min(32, t_end - tt0),
-                      wbuf, lane);
-      cp_async_wait<0>();
-      __syncwarp();
-      if (valid) {
-#pragma unroll 4
-        for (int d8 = 0; d8 < kHeadDim; d8 += 8) {
-          const uint4 kv = wbuf[16 * lane + ((d8 >> 3) ^ (lane & 7))];
-          const float kf[8] = {h_lo(kv.x), h_hi(kv.x), h_lo(kv.y), h_hi(kv.y),
-                               h_lo(kv.z), h_hi(kv.z), h_lo(kv.w), h_hi(kv.w)};
-#pragma unroll
-          for (int j = 0; j < kNH; ++j) {
-            const float4 q0 = *reinterpret_cast<const float4*>(&s.q[j][d8]);
-            const float4 q1 = *reinterpret_cast<const float4*>(&s.q[j][d8 + 4]);
-            sc[j] += q0.x * kf[0] + q0.y * kf[1] + q0.z * kf[2] + q0.w * kf[3] +
-                     q1.x * kf[4] + q1.y * kf[5] + q1.z * kf[6] + q1.w * kf[7];
-          }
-        }
-      }
-    }
-
-    // online softmax (log2 domain: q carries scale * log2 e)
-    float p[kNH];
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-      const float sj = valid ? sc[j] : -INFINITY;
-      const float mnew = fmaxf(m[j], warp_max(sj));
-      const float corr = fast_exp2(m[j] - mnew);
-      p[j] = fast_exp2(sj - mnew);
-      lsum[j] = lsum[j] * corr + p[j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[j][i] *= corr;
-      m[j] = mnew;
-    }
-
-    // values: stage the packed rows and the residual rows of this tile
-    const int vrows = min(max(a.nq_v - tt0, 0), 32);
-    const int r_lo = max(t_begin - tt0, 0);
-    const int r_hi = min(32, t_end - tt0);
-    __syncwarp();  // the key phase is done with wbuf
-    if (max(vrows, r_lo) < r_hi) stage_ring_rows(cv.ring_v, unit, cv.R, tt0, max(vrows, r_lo), r_hi, wbuf, lane);
-    {
-      // packed rows r < vrows: codes at the start of wbuf row r, then the
-      // row's value scales and zeros (16 B) at byte 64
-      constexpr int CPR = RB / 16;
-      const uint4* gsrc = reinterpret_cast<const uint4*>(cv.codes_v + (unit * cv.Tcap + tt0) * RB);
-      for (int i = lane; i < vrows * CPR; i += 32) wbuf[16 * (i / CPR) + (i % CPR)] = gsrc[i];
-      if (lane < vrows) {
-        const long so = (unit * cv.Tcap + tt0 + lane) * (kHeadDim / kGroup);
-        const uint2 sv2 = *reinterpret_cast<const uint2*>(cv.scale_v + so);
-        const uint2 zv2 = *reinterpret_cast<const uint2*>(cv.zero_v + so);
-        wbuf[16 * lane + 4] = make_uint4(sv2.x, sv2.y, zv2.x, zv2.y);
-      }
-    }
-    cp_async_wait<0>();
-    __syncwarp();
-    const int vpos = v_unit_pos(lane);  // unit of channels 4*lane .. +3
-    for (int r = r_lo; r < r_hi; ++r) {
-      float vh[4];
-      if (r < vrows) {
-        const uint8_t* rowb = reinterpret_cast<const uint8_t*>(&wbuf[16 * r]);
-        uint32_t cb;
-        if constexpr (BITS == 2) cb = rowb[vpos];
-        else cb = *reinterpret_cast<const uint16_t*>(rowb + 2 * vpos);
-        const __half* svz = reinterpret_cast<const __half*>(&wbuf[16 * r + 4]);
-        const float sv = __half2float(svz[lane >> 3]);
-        const float zv = __half2float(svz[4 + (lane >> 3)]);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) vh[i] = (float)((cb >> (BITS * i)) & L) * sv + zv;
-      } else {
-        const uint2* vr = reinterpret_cast<const uint2*>(&wbuf[16 * r + ((lane >> 1) ^ (r & 7))]);
-        halves4(vr[lane & 1], vh);
-      }
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        const float pr = __shfl_sync(kFull, p[j], r);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) o[j][i] += pr * vh[i];
-      }
-    }
-    __syncwarp();
-  }
-}
-
-// ---------------------------------------------------------------------------
 // A tail split on CUDA cores: tokens [c0, c0 + n), n <= kTailTok, of the tail
 // [t_tail, l), staged in one round of copies (fp16 residual rows, packed rows
 // and the key groups' scales / zeros); then scores with four threads per
@@ -438,7 +274,7 @@ __device__ void v1_tiles(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, 
 // notebook's fl(fl(c * s) + z) because c * s is exact in fp32.  Leaves the
 // partial of the CTA in warp 0's slots (the other warps' slots empty).
 template <int BITS>
-__device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit, int b,
+__device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
                            int j0, int nh, int c0, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;  // packed row bytes
@@ -607,7 +443,7 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core path (2-bit packed tiles).
+// Tensor-core path (packed tiles, 2 or 4 bits).
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -617,24 +453,38 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// The 2-bit codes at bit pair I of both 16-bit halves of w, kept in place:
-// read as fp16 (exponent field zero) the pair is the exact subnormal pair
-// {c_lo * 4^I * 2^-24, c_hi * 4^I * 2^-24} for I <= 4.
-template <int I>
-__device__ __forceinline__ uint32_t ext(uint32_t w) {
-  static_assert(I >= 0 && I <= 4, "bit pair must stay inside the fp16 mantissa");
-  return w & (0x00030003u << (2 * I));
+// Code position I (bit pair at 2 bits, nibble at 4 bits) of both 16-bit
+// halves of w, kept in place: read as fp16 (exponent field zero) the pair is
+// the exact subnormal pair {c_lo * base^e * 2^-24, c_hi * base^e * 2^-24}.
+// Positions whose bits would reach the exponent field come from w_sh (w >> 10
+// at 2 bits, w >> 8 at 4 bits).  code_exp(I) is the resulting e; the base is
+// 4 at 2 bits and 16 at 4 bits.
+template <int BITS, int I>
+__device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t w_sh) {
+  if constexpr (BITS == 2) {
+    static_assert(I >= 0 && I < 8, "eight bit pairs per half");
+    if constexpr (I <= 4) return w & (0x00030003u << (2 * I));
+    else return w_sh & (0x00030003u << (2 * (I - 5)));
+  } else {
+    static_assert(I >= 0 && I < 4, "four nibbles per half");
+    if constexpr (I <= 1) return w & (0x000F000Fu << (4 * I));
+    else return w_sh & (0x000F000Fu << (4 * (I - 2)));
+  }
 }
 
-// Bit pair i in 0..7 of each half of w: pairs 0..4 directly, 5..7 from w >> 10
-// (scaled by 4^(i-5)).  pow4_exp(i) is the resulting power of four.
-template <int I>
-__device__ __forceinline__ uint32_t ext8(uint32_t w, uint32_t w_sh10) {
-  if constexpr (I <= 4) return ext<I>(w);
-  else return ext<I - 5>(w_sh10);
+template <int BITS>
+__host__ __device__ constexpr int code_exp(int i) {
+  return BITS == 2 ? (i <= 4 ? i : i - 5) : (i & 1);
 }
 
-__host__ __device__ constexpr int pow4_exp(int i) { return i <= 4 ? i : i - 5; }
+template <int BITS>
+constexpr int kShift = BITS == 2 ? 10 : 8;  // w_sh = w >> kShift
+
+// base^-e(i) as a float
+template <int BITS>
+__host__ __device__ constexpr float code_scale(int i) {
+  return 1.0f / (float)(1 << (BITS * code_exp<BITS>(i)));
+}
 
 constexpr float kTwo24 = 16777216.0f;  // undoes the 2^-24 of the subnormal codes
 // The running max of a head is raised only when a tile's scores exceed it by
@@ -645,36 +495,70 @@ constexpr float kLazyMax = 0.5f;
 // that later tiles rarely raise it again.
 constexpr float kLazySlack = 1.0f;
 
+// The fp16 pair (x[c0], x[c1]) of the channel pair of code position i within
+// the 8 (2 bits: words W[0..3] hold channels 16m..16m+7, V[0..3] 16m+8..+15)
+// or 4 (4 bits: W[0..3] holds channels 8m..8m+7) words of a per-channel fp16
+// vector (key scales or zeros).
+template <int BITS>
+__device__ __forceinline__ uint32_t chan_pair(const uint32_t (&W)[4], const uint32_t (&V)[4], int i) {
+  if constexpr (BITS == 2) return __byte_perm(W[i >> 1], V[i >> 1], (i & 1) ? 0x7632 : 0x5410);
+  else return __byte_perm(W[i >> 1], W[2 + (i >> 1)], (i & 1) ? 0x7632 : 0x5410);
+}
+
+// The per-channel fp16 vector words (key scales or zeros) behind q-table
+// block `blk` of this lane: 2 bits -- block = quarters 2blk, 2blk+1, word m =
+// tig + 4blk of a key row, W = channels 16m..16m+7, V = 16m+8..16m+15;
+// 4 bits -- block = quarter blk, word m = tig + 4blk, W = channels 8m..8m+7.
+template <int BITS>
+__device__ __forceinline__ void chan_words(const uint32_t* vec, int tig, int blk, uint32_t (&W)[4],
+                                           uint32_t (&V)[4]) {
+  if constexpr (BITS == 2) {
+    const int m = tig + 4 * blk;
+    const uint4 wa = *reinterpret_cast<const uint4*>(vec + 8 * m);
+    const uint4 wb = *reinterpret_cast<const uint4*>(vec + 8 * m + 4);
+    W[0] = wa.x; W[1] = wa.y; W[2] = wa.z; W[3] = wa.w;
+    V[0] = wb.x; V[1] = wb.y; V[2] = wb.z; V[3] = wb.w;
+  } else {
+    const int m = tig + 4 * blk;
+    const uint4 wa = *reinterpret_cast<const uint4*>(vec + 4 * m);
+    W[0] = wa.x; W[1] = wa.y; W[2] = wa.z; W[3] = wa.w;
+    V[0] = V[1] = V[2] = V[3] = 0u;
+  }
+}
+
+template <int BITS>
+constexpr int kBlocks = BITS == 2 ? 2 : 4;       // q-table blocks
+template <int BITS>
+constexpr int kQuartersPerBlock = BITS == 2 ? 2 : 1;
+
+// Code position of q-table word w (0..15).
+template <int BITS>
+__host__ __device__ constexpr int word_pos(int w) {
+  return BITS == 2 ? (w & 7) : (w & 3);
+}
+
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
-// (head g >> 1, part g & 1).  Fragment order: k-step ks uses word m = tig +
-// 4*(ks >> 2) of each key row and bit pairs i = 2*(ks & 3) and i + 1; the k
-// rows (2tig, 2tig+1) hold channels (16m+i, 16m+i+8) and (2tig+8, 2tig+9) hold
-// (16m+i+1, 16m+i+9).  The q table is pre-scaled by 4^-e(i) to cancel the
-// power of four that the code extraction leaves in the A operand.
-__device__ __forceinline__ void build_qprime(const WarpSmem& ws, const uint32_t* sk, int g, int tig,
+// (head g >> 1, part g & 1), in the order of the q tables.  The q table is
+// pre-scaled by base^-e(i) to cancel the power that the code extraction
+// leaves in the A operand.
+template <int BITS>
+__device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uint32_t* sk, int g, int tig,
                                              uint32_t (&bq)[8][2]) {
 #pragma unroll
-  for (int mh = 0; mh < 2; ++mh) {
-    const int m = tig + 4 * mh;
-    const uint4 wa = *reinterpret_cast<const uint4*>(sk + 8 * m);
-    const uint4 wb = *reinterpret_cast<const uint4*>(sk + 8 * m + 4);
-    const uint32_t A[4] = {wa.x, wa.y, wa.z, wa.w}, B[4] = {wb.x, wb.y, wb.z, wb.w};
-    uint32_t X[2][8];
+  for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
+    uint32_t W[4], V[4];
+    chan_words<BITS>(sk, tig, blk, W, V);
 #pragma unroll
-    for (int c = 0; c < 2; ++c) {
-      const uint4 x0 = ws.qs[c][2 * mh][g][tig];
-      const uint4 x1 = ws.qs[c][2 * mh + 1][g][tig];
-      X[c][0] = x0.x; X[c][1] = x0.y; X[c][2] = x0.z; X[c][3] = x0.w;
-      X[c][4] = x1.x; X[c][5] = x1.y; X[c][6] = x1.z; X[c][7] = x1.w;
-    }
+    for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
+      const int quarter = kQuartersPerBlock<BITS> * blk + qq;
+      const uint4 x0 = ws.qs[0][quarter][g][tig];
+      const uint4 x1 = ws.qs[1][quarter][g][tig];
+      const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const int ks = 4 * mh + q4;
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const uint32_t sp = __byte_perm(A[q4], B[q4], r ? 0x7632 : 0x5410);
-        const int w = 2 * q4 + r;
-        bq[ks][r] = split_mul(X[0][w], X[1][w], X[1][w] ^ 0x80008000u, sp);
+      for (int wq = 0; wq < 4; ++wq) {
+        const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
+        bq[w >> 1][w & 1] =
+            split_mul(X0[wq], X1[wq], X1[wq] ^ 0x80008000u, chan_pair<BITS>(W, V, word_pos<BITS>(w)));
       }
     }
   }
@@ -689,24 +573,28 @@ __device__ __forceinline__ int pbuf_pos(int t) {
 // Scores of one staged 32-token tile for the four heads of the CTA: lane
 // (g, tig) gets head tig at tokens g + 8r (sc[r], log2 units);
 // ks = 2^E_tig * scale * log2(e).
-__device__ __forceinline__ void key_scores(const WarpSmem& ws, const TileBuf& tb, int g, int tig, float ks,
-                                           float (&sc)[4]) {
+template <int BITS>
+__device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileBuf<BITS>& tb, int g, int tig,
+                                           float ks, float (&sc)[4]) {
+  constexpr int RW = 4 * BITS;  // 32-bit words per code row
   // ---- beta = zK x q: every A row is the zero vector, so D[., (tig, part)] = beta ----
   float beta4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int mh = 0; mh < 2; ++mh) {
-    const int m = tig + 4 * mh;
-    const uint4 za = *reinterpret_cast<const uint4*>(tb.zk + 8 * m);
-    const uint4 zb = *reinterpret_cast<const uint4*>(tb.zk + 8 * m + 4);
-    const uint32_t A[4] = {za.x, za.y, za.z, za.w}, B[4] = {zb.x, zb.y, zb.z, zb.w};
-    const uint4 b0 = ws.qb[2 * mh][g][tig];
-    const uint4 b1 = ws.qb[2 * mh + 1][g][tig];
-    const uint32_t QB[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
+    uint32_t W[4], V[4];
+    chan_words<BITS>(tb.zk, tig, blk, W, V);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      const uint32_t z0 = __byte_perm(A[q4], B[q4], 0x5410);
-      const uint32_t z1 = __byte_perm(A[q4], B[q4], 0x7632);
-      mma16816(beta4, z0, z0, z1, z1, QB[2 * q4], QB[2 * q4 + 1]);
+    for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
+      const int quarter = kQuartersPerBlock<BITS> * blk + qq;
+      const uint4 qb = ws.qb[quarter][g][tig];
+      const uint32_t QB[4] = {qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {  // the quarter's two k-steps
+        const int w0 = 4 * quarter + 2 * kh;
+        const uint32_t z0 = chan_pair<BITS>(W, V, word_pos<BITS>(w0));
+        const uint32_t z1 = chan_pair<BITS>(W, V, word_pos<BITS>(w0 + 1));
+        mma16816(beta4, z0, z0, z1, z1, QB[2 * kh], QB[2 * kh + 1]);
+      }
     }
   }
   const float kb = (beta4[0] + beta4[1]) * ks;
@@ -714,24 +602,38 @@ __device__ __forceinline__ void key_scores(const WarpSmem& ws, const TileBuf& tb
 
   // ---- scores S = codes x Q' + beta ----
   uint32_t bq[8][2];
-  build_qprime(ws, tb.sk, g, tig, bq);
+  build_qprime<BITS>(ws, tb.sk, g, tig, bq);
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const uint32_t* rg = tb.kc + (16 * mt + g) * 8;      // key row 16mt + g
-    const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * 8;  // key row 16mt + g + 8
-    const uint32_t g0 = rg[tig], g1 = rg[tig + 4], e0 = r8[tig], e1 = r8[tig + 4];
-    const uint32_t g0s = g0 >> 10, g1s = g1 >> 10, e0s = e0 >> 10, e1s = e1 >> 10;
+    const uint32_t* rg = tb.kc + (16 * mt + g) * RW;      // key row 16mt + g
+    const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * RW;  // key row 16mt + g + 8
+    constexpr int NW = BITS;  // words of a row this lane reads: tig + 4j
+    uint32_t wg[NW], w8[NW], sg[NW], s8[NW];
+#pragma unroll
+    for (int j = 0; j < NW; ++j) {
+      wg[j] = rg[tig + 4 * j];
+      w8[j] = r8[tig + 4 * j];
+      sg[j] = wg[j] >> kShift<BITS>;
+      s8[j] = w8[j] >> kShift<BITS>;
+    }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#define KIVI_KSTEP(KS, I)                                                                  \
-  {                                                                                        \
-    const uint32_t wg = (KS) < 4 ? g0 : g1, wgs = (KS) < 4 ? g0s : g1s;                   \
-    const uint32_t w8 = (KS) < 4 ? e0 : e1, w8s = (KS) < 4 ? e0s : e1s;                   \
-    mma16816(acc, ext8<I>(wg, wgs), ext8<I>(w8, w8s), ext8<I + 1>(wg, wgs),                \
-             ext8<I + 1>(w8, w8s), bq[KS][0], bq[KS][1]);                                  \
-  }
-    KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 4) KIVI_KSTEP(3, 6)
-    KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 4) KIVI_KSTEP(7, 6)
+    if constexpr (BITS == 2) {
+#define KIVI_KSTEP(KS, I)                                                                       \
+  mma16816(acc, ext<2, I>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I>(w8[(KS) >> 2], s8[(KS) >> 2]), \
+           ext<2, I + 1>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I + 1>(w8[(KS) >> 2], s8[(KS) >> 2]), \
+           bq[KS][0], bq[KS][1]);
+      KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 4) KIVI_KSTEP(3, 6)
+      KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 4) KIVI_KSTEP(7, 6)
 #undef KIVI_KSTEP
+    } else {
+#define KIVI_KSTEP(KS, I)                                                                       \
+  mma16816(acc, ext<4, I>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I>(w8[(KS) >> 1], s8[(KS) >> 1]), \
+           ext<4, I + 1>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I + 1>(w8[(KS) >> 1], s8[(KS) >> 1]), \
+           bq[KS][0], bq[KS][1]);
+      KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 0) KIVI_KSTEP(3, 2)
+      KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 0) KIVI_KSTEP(7, 2)
+#undef KIVI_KSTEP
+    }
     sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
     sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
   }
@@ -772,16 +674,21 @@ __device__ __forceinline__ void softmax_p(const float (&sc)[4], float* pb, int g
 // Values of one staged tile: O += codes^T x (p * sV), Z += zV^T x p, with p
 // from the warp's weight buffer (O and Z of head tig).  The k rows (2tig,
 // 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows (2tig+8,
-// 2tig+9) tokens t0 + 8 and t0 + 12, so that the lanes of a shared-memory
-// phase read distinct banks.
-__device__ __forceinline__ void value_acc(const TileBuf& tb, const float* pb, int g, int tig, float (&O)[8][4],
-                                          float (&Z)[4]) {
+// 2tig+9) tokens t0 + 8 and t0 + 12.  M-tile 2gp + hm covers value group gp:
+// row g is channel 32gp + 4g + 2hm, row g + 8 the next channel.
+template <int BITS>
+__device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* pb, int g, int tig,
+                                          float (&O)[8][4], float (&Z)[4]) {
+  constexpr int RW = 4 * BITS;  // 32-bit words per code row
   const int part = g & 1;
   const float* pv = pb + (g >> 1) * 34 + 8 * tig;
   const int zsel = (g >> 1) & 1;  // zero word of value group g & 3 within a token
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
-    uint32_t pa[2], Pp[4][2], az[2], u[2][2];
+    // u[aa][gp]: the codes of channels 4g..4g+3 of group gp for tokens (t0,
+    // t0 + 4), as the two 16-bit halves (2 bits: a byte per group, two groups
+    // per word)
+    uint32_t pa[2], Pp[4][2], az[2], u[2][4];
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
       const int t0 = 16 * kk + 8 * aa + tig;  // tokens t0, t0 + 4
@@ -799,28 +706,51 @@ __device__ __forceinline__ void value_acc(const TileBuf& tb, const float* pb, in
       Pp[2][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x5410));
       Pp[3][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x7632));
       az[aa] = __byte_perm(tb.zv[2 * t0 + zsel], tb.zv[2 * (t0 + 4) + zsel], (g & 1) ? 0x7632 : 0x5410);
-      // value codes: interleaved word g of a row holds, per byte, channels
-      // 4g..4g+3 of groups 0..3
-      const uint32_t w0 = tb.vc[t0 * 8 + g], w1 = tb.vc[(t0 + 4) * 8 + g];
-      u[aa][0] = __byte_perm(w0, w1, 0x5410);
-      u[aa][1] = __byte_perm(w0, w1, 0x7632);
+      if constexpr (BITS == 2) {
+        // interleaved word g of a row holds, per byte, channels 4g..4g+3 of groups 0..3
+        const uint32_t w0 = tb.vc[t0 * RW + g], w1 = tb.vc[(t0 + 4) * RW + g];
+        u[aa][0] = __byte_perm(w0, w1, 0x5410);  // groups 0, 1
+        u[aa][1] = __byte_perm(w0, w1, 0x7632);  // groups 2, 3
+        u[aa][2] = u[aa][3] = 0u;
+      } else {
+        // interleaved words 2g, 2g+1 of a row hold, per 16-bit half,
+        // channels 4g..4g+3 of groups 0..3
+        const uint2 w0 = *reinterpret_cast<const uint2*>(tb.vc + t0 * RW + 2 * g);
+        const uint2 w1 = *reinterpret_cast<const uint2*>(tb.vc + (t0 + 4) * RW + 2 * g);
+        u[aa][0] = __byte_perm(w0.x, w1.x, 0x5410);
+        u[aa][1] = __byte_perm(w0.x, w1.x, 0x7632);
+        u[aa][2] = __byte_perm(w0.y, w1.y, 0x5410);
+        u[aa][3] = __byte_perm(w0.y, w1.y, 0x7632);
+      }
     }
     // z-term: rows = value groups (g & 3), columns = (head, part) of p
     mma16816(Z, az[0], az[0], az[1], az[1], pa[0], pa[1]);
+    if constexpr (BITS == 2) {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t x0 = u[0][half], x1 = u[1][half];
-      const uint32_t x0s = x0 >> 10, x1s = x1 >> 10;
-      // m-tiles 4*half + {0,1,2,3}: groups 2*half (bit pairs 0..3) and 2*half+1 (4..7)
-#define KIVI_VTILE(MT, I, GP)                                                             \
-  mma16816(O[MT], ext8<I>(x0, x0s), ext8<I + 1>(x0, x0s), ext8<I>(x1, x1s),               \
-           ext8<I + 1>(x1, x1s), Pp[GP][0], Pp[GP][1]);
-      if (half == 0) {
-        KIVI_VTILE(0, 0, 0) KIVI_VTILE(1, 2, 0) KIVI_VTILE(2, 4, 1) KIVI_VTILE(3, 6, 1)
-      } else {
-        KIVI_VTILE(4, 0, 2) KIVI_VTILE(5, 2, 2) KIVI_VTILE(6, 4, 3) KIVI_VTILE(7, 6, 3)
-      }
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t x0 = u[0][half], x1 = u[1][half];
+        const uint32_t x0s = x0 >> 10, x1s = x1 >> 10;
+        // m-tiles 4*half + {0,1,2,3}: groups 2*half (bit pairs 0..3) and 2*half+1 (4..7)
+#define KIVI_VTILE(MT, I, GP)                                                                     \
+  mma16816(O[MT], ext<2, I>(x0, x0s), ext<2, I + 1>(x0, x0s), ext<2, I>(x1, x1s),                 \
+           ext<2, I + 1>(x1, x1s), Pp[GP][0], Pp[GP][1]);
+        if (half == 0) {
+          KIVI_VTILE(0, 0, 0) KIVI_VTILE(1, 2, 0) KIVI_VTILE(2, 4, 1) KIVI_VTILE(3, 6, 1)
+        } else {
+          KIVI_VTILE(4, 0, 2) KIVI_VTILE(5, 2, 2) KIVI_VTILE(6, 4, 3) KIVI_VTILE(7, 6, 3)
+        }
 #undef KIVI_VTILE
+      }
+    } else {
+#pragma unroll
+      for (int gp = 0; gp < 4; ++gp) {
+        const uint32_t x0 = u[0][gp], x1 = u[1][gp];
+        const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
+        mma16816(O[2 * gp], ext<4, 0>(x0, x0s), ext<4, 1>(x0, x0s), ext<4, 0>(x1, x1s), ext<4, 1>(x1, x1s),
+                 Pp[gp][0], Pp[gp][1]);
+        mma16816(O[2 * gp + 1], ext<4, 2>(x0, x0s), ext<4, 3>(x0, x0s), ext<4, 2>(x1, x1s),
+                 ext<4, 3>(x1, x1s), Pp[gp][0], Pp[gp][1]);
+      }
     }
   }
 }
@@ -828,7 +758,8 @@ __device__ __forceinline__ void value_acc(const TileBuf& tb, const float* pb, in
 // q of the CTA's heads: staged once in shared memory, per-head exponents
 // (warp w takes head w), then the tables in fragment order.  Thread (head,
 // tig, word) builds the pair words of both parts.
-__device__ void build_q_tables(WarpSmem& s, const AttnArgs& a, int b, int j0, int nh) {
+template <int BITS>
+__device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, int b, int j0, int nh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp < kNH) {
     float v[4];
@@ -853,16 +784,24 @@ __device__ void build_q_tables(WarpSmem& s, const AttnArgs& a, int b, int j0, in
     const int tig = (idx >> 4) & 3;
     const int hh = idx >> 6;
     const int ks = word >> 1, r = word & 1;
-    const int m = tig + 4 * (ks >> 2);
-    const int i = 2 * (ks & 3) + r;
-    const float f = 1.0f / (float)(1 << (2 * pow4_exp(i)));
-    float q2[2];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) q2[half] = ldexpf(s.qv[hh][16 * m + i + 8 * half], -s.qexp[hh]);
-    const uint32_t qh = f2_to_h2(q2[0], q2[1]);
-    const uint32_t ql = f2_to_h2(q2[0] - h_lo(qh), q2[1] - h_hi(qh));
-    const uint32_t sh = f2_to_h2(q2[0] * f, q2[1] * f);
-    const uint32_t sl = f2_to_h2(q2[0] * f - h_lo(sh), q2[1] * f - h_hi(sh));
+    int c0, c1, i;  // the channel pair of the word and its code position
+    if constexpr (BITS == 2) {
+      const int m = tig + 4 * (ks >> 2);
+      i = 2 * (ks & 3) + r;
+      c0 = 16 * m + i;
+      c1 = c0 + 8;
+    } else {
+      const int m = tig + 4 * (ks >> 1);
+      i = 2 * (ks & 1) + r;
+      c0 = 8 * m + i;
+      c1 = c0 + 4;
+    }
+    const float f = code_scale<BITS>(i);
+    const float q0 = ldexpf(s.qv[hh][c0], -s.qexp[hh]), q1 = ldexpf(s.qv[hh][c1], -s.qexp[hh]);
+    const uint32_t qh = f2_to_h2(q0, q1);
+    const uint32_t ql = f2_to_h2(q0 - h_lo(qh), q1 - h_hi(qh));
+    const uint32_t sh = f2_to_h2(q0 * f, q1 * f);
+    const uint32_t sl = f2_to_h2(q0 * f - h_lo(sh), q1 * f - h_hi(sh));
     const int quarter = word >> 2, wq = word & 3;
     // hi lane: (xa, xb) = (hi, 0); lo lane: (lo, hi)
     reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh][tig])[wq] = sh;
@@ -880,10 +819,12 @@ struct UnitSrc {
   const char *kc, *vc, *sk, *zk, *sv, *zv;
 };
 
+template <int BITS>
 __device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
+  constexpr long RB = 16 * BITS;  // code bytes per token
   UnitSrc u;
-  u.kc = reinterpret_cast<const char*>(cv.codes_k + unit * cv.Tcap * 32);
-  u.vc = reinterpret_cast<const char*>(cv.codes_v + unit * cv.Tcap * 32);
+  u.kc = reinterpret_cast<const char*>(cv.codes_k + unit * cv.Tcap * RB);
+  u.vc = reinterpret_cast<const char*>(cv.codes_v + unit * cv.Tcap * RB);
   u.sk = reinterpret_cast<const char*>(cv.scale_k + unit * (cv.Tcap / kGroup) * kHeadDim);
   u.zk = reinterpret_cast<const char*>(cv.zero_k + unit * (cv.Tcap / kGroup) * kHeadDim);
   u.sv = reinterpret_cast<const char*>(cv.scale_v + unit * cv.Tcap * (kHeadDim / kGroup));
@@ -892,11 +833,14 @@ __device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
 }
 
 // Bulk copies of packed tile `tile` into a stage (one lane).
-__device__ __forceinline__ void issue_tile(TileBuf& tb, unsigned long long* bar, const UnitSrc& u, int tile) {
-  const long o1k = (long)tile * 1024, o256 = (long)tile * 256;
-  mbar_expect_tx(bar, kTileBytes);
-  bulk_g2s(tb.kc, u.kc + o1k, 1024u, bar);
-  bulk_g2s(tb.vc, u.vc + o1k, 1024u, bar);
+template <int BITS>
+__device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long* bar, const UnitSrc& u,
+                                           int tile) {
+  constexpr uint32_t kCode = 512u * BITS;  // code bytes per tile
+  const long oc = (long)tile * kCode, o256 = (long)tile * 256;
+  mbar_expect_tx(bar, (uint32_t)sizeof(TileBuf<BITS>));
+  bulk_g2s(tb.kc, u.kc + oc, kCode, bar);
+  bulk_g2s(tb.vc, u.vc + oc, kCode, bar);
   bulk_g2s(tb.sk, u.sk + o256, 256u, bar);
   bulk_g2s(tb.zk, u.zk + o256, 256u, bar);
   bulk_g2s(tb.sv, u.sv + o256, 256u, bar);
@@ -909,17 +853,19 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 // Packed tiles [tile0, tile1) of one (batch, kv-head, head chunk) on the
 // tensor cores.  Warp w takes tiles tile0 + w, + kWarps, ... through its own
-// ring of kStages staged tiles (lane 0 issues the copies; no CTA barrier in
-// the loop).  Leaves each warp's (max, sum) in s_m / s_l and its output in
-// its merge area.
-__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& sm, long unit, int b,
+// ring of staged tiles (lane 0 issues the copies; no CTA barrier in the
+// loop).  Leaves each warp's (max, sum) in s_m / s_l and its output in its
+// merge area.
+template <int BITS>
+__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
                              int j0, int nh, int tile0, int tile1, float (&s_m)[kWarps][kNH],
                              float (&s_l)[kWarps][kNH]) {
-  WarpSmem& ws = sm.ws;
+  constexpr int kStages = kStagesOf<BITS>;
+  WarpSmem<BITS>& ws = sm.ws;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
-  TileBuf* st = ws.st[warp];
+  TileBuf<BITS>* st = ws.st[warp];
   unsigned long long* bars = ws.bar[warp];
 
   if (lane == 0) {
@@ -928,12 +874,12 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
     mbar_fence_init();
   }
   __syncwarp();
-  const UnitSrc us = unit_src(cv, unit);
+  const UnitSrc us = unit_src<BITS>(cv, unit);
   const int t_first = tile0 + warp;  // this warp's tiles: t_first + kWarps * k
   int issued = min(n_mine, kStages);
   if (lane == 0)
-    for (int k = 0; k < issued; ++k) issue_tile(st[k], &bars[k], us, t_first + kWarps * k);
-  build_q_tables(ws, a, b, j0, nh);
+    for (int k = 0; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
+  build_q_tables<BITS>(ws, a, b, j0, nh);
   __syncthreads();
   const float ks = ws.qscale[tig];
   float* pb = &ws.pbuf[warp][0][0];
@@ -960,7 +906,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
     if (__any_sync(kFull, !ok)) {
       failed = true;
     } else {
-      key_scores(ws, st[0], g, tig, ks, sc);
+      key_scores<BITS>(ws, st[0], g, tig, ks, sc);
       softmax_p(sc, pb, g, tig, m_run, lsum, O, Z);
       __syncwarp();
     }
@@ -979,14 +925,14 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
           failed = true;
         } else {
           float scn[4];
-          key_scores(ws, st[sn], g, tig, ks, scn);
-          value_acc(st[sg], pb, g, tig, O, Z);
+          key_scores<BITS>(ws, st[sn], g, tig, ks, scn);
+          value_acc<BITS>(st[sg], pb, g, tig, O, Z);
           done = k + 1;
           __syncwarp();  // every lane is done with stage sg and the weight buffer
           if (k + kStages < n_mine) {
             if (lane == 0) {
               fence_proxy_async();
-              issue_tile(st[sg], &bars[sg], us, t_first + kWarps * (k + kStages));
+              issue_tile<BITS>(st[sg], &bars[sg], us, t_first + kWarps * (k + kStages));
             }
             ++issued;
           }
@@ -1002,14 +948,14 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
     const int sl = (n_mine - 1) % kStages;
 #pragma unroll
     for (int sg = 0; sg < kStages; ++sg)
-      if (sg == sl) value_acc(st[sg], pb, g, tig, O, Z);
+      if (sg == sl) value_acc<BITS>(st[sg], pb, g, tig, O, Z);
     done = n_mine;
   }
   if (done < n_mine) {
     // A wait timed out: record it, and let every copy still in flight land
     // before the warp's buffers are reused (each wait bounded again).
     if (lane == 0) atomicOr(a.status, 1);
-    for (int k = done; k < issued; ++k) mbar_wait(&bars[k % kStages], (uint32_t)((k / kStages) & 1));
+    for (int kk = done; kk < issued; ++kk) mbar_wait(&bars[kk % kStages], (uint32_t)((kk / kStages) & 1));
     __syncwarp();
   }
 
@@ -1031,10 +977,11 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem& 
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const int gp = mt >> 1, hm = mt & 1;
-    const int i_lo = 4 * (gp & 1) + 2 * hm;
+    // code positions of rows g and g + 8 of m-tile mt
+    const int i_lo = BITS == 2 ? 4 * (gp & 1) + 2 * hm : 2 * hm;
     const int ch = 32 * gp + 4 * g + 2 * hm;
-    const float f_lo = kTwo24 / (float)(1 << (2 * pow4_exp(i_lo)));
-    const float f_hi = kTwo24 / (float)(1 << (2 * pow4_exp(i_lo + 1)));
+    const float f_lo = kTwo24 * code_scale<BITS>(i_lo);
+    const float f_hi = kTwo24 * code_scale<BITS>(i_lo + 1);
     orow[ch] = (O[mt][0] + O[mt][1]) * f_lo + zt[gp];
     orow[ch + 1] = (O[mt][2] + O[mt][3]) * f_hi + zt[gp];
   }
@@ -1075,8 +1022,8 @@ __device__ __forceinline__ void merge_partials(const float* po, const float* pml
 // grid (splits, H * head_chunks, B), 128 threads.
 template <int BITS>
 __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem)
-  SplitSmem& sm = *reinterpret_cast<SplitSmem*>(smem_raw);
+  extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS>)
+  SplitSmem<BITS>& sm = *reinterpret_cast<SplitSmem<BITS>*>(smem_raw);
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
   __shared__ bool s_last;
 
@@ -1089,48 +1036,16 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
   const int nh = min(kNH, grp - hc * kNH);
   const long unit = (long)b * cv.H + h;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int path = s < a.tail_splits ? kPathTail : (BITS == 2 ? kPathMma : kPathV1);
-  const int sp = s - a.tail_splits;  // packed split index
+  const int path = s < a.tail_splits ? kPathTail : kPathMma;
 
   if (path == kPathTail) {
     tail_split<BITS>(cv, a, sm, unit, b, j0, nh, a.t_tail + s * kTailTok, s_m, s_l);
-  } else if (path == kPathV1) {
-    // ---- CUDA cores: packed tiles at 4 bits ----
-    const int t_begin = sp * a.chunk;
-    const int t_end = min(a.t_tail, (sp + 1) * a.chunk);
-    for (int i = threadIdx.x; i < kNH * kHeadDim; i += blockDim.x) {
-      const int j = i / kHeadDim, d = i % kHeadDim;
-      sm.v1.q[j][d] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + d, a.q_dtype) * a.scale_log2
-                             : 0.0f;
-    }
-    __syncthreads();
-    float m[kNH], lsum[kNH], o[kNH][4];
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) {
-      m[j] = -INFINITY;
-      lsum[j] = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[j][i] = 0.0f;
-    }
-    if (t_begin < t_end) v1_tiles<BITS>(cv, a, sm, unit, t_begin, t_end, m, lsum, o);
-#pragma unroll
-    for (int j = 0; j < kNH; ++j) lsum[j] = warp_sum(lsum[j]);
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < kNH; ++j) {
-        s_m[warp][j] = m[j];
-        s_l[warp][j] = lsum[j];
-      }
-    }
-    float* mo = merge_area(sm, warp, kPathV1);
-#pragma unroll
-    for (int j = 0; j < kNH; ++j)
-      *reinterpret_cast<float4*>(&mo[j * kHeadDim + 4 * lane]) = make_float4(o[j][0], o[j][1], o[j][2], o[j][3]);
   } else {
     // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
+    const int sp = s - a.tail_splits;
     const int tile0 = sp * a.chunk / 32;
     const int tile1 = min(a.t_tail, (sp + 1) * a.chunk) / 32;
-    packed_split(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
+    packed_split<BITS>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
 
@@ -1222,9 +1137,9 @@ cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a
   // on every call costs a host call only.
   const cudaError_t e = cudaFuncSetAttribute(attn_kernel<BITS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(SplitSmem));
+                                             (int)sizeof(SplitSmem<BITS>));
   if (e != cudaSuccess) return e;
-  attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem), st>>>(cv, a);
+  attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a);
   return cudaGetLastError();
 }
 

@@ -40,10 +40,11 @@ def unit_attention_err(out, wl, units, oracles, q):
     return worst
 
 
-def test_llama3_8b_decode_step():
+@pytest.mark.parametrize("bits", [2, 4])
+def test_llama3_8b_decode_step(bits):
     """batch 8, 32/8 heads, context 4096 fp16: prefill, one append, attention;
-    the whole batch against the oracle."""
-    wl = W.llama3_8b_decode()
+    the whole batch against the oracle (2 bits, and the same step at 4 bits)."""
+    wl = W.llama3_8b_decode(bits=bits)
     g = T.gpu_cache(wl)
     g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
     o = T.oracle_cache(wl)
