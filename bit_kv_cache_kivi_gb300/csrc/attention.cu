@@ -1019,6 +1019,62 @@ __device__ __forceinline__ void merge_partials(const float* po, const float* pml
   o4 = acc;
 }
 
+// The tail on the last packed split (when no tail split fits the budget):
+// the warps' packed partials are merged into registers, the tail rounds run
+// one after another and are folded in, and the result is left as warp 0's
+// slot (the other warps' slots empty) for the CTA merge.
+template <int BITS>
+__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
+                           int j0, int nh, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
+  const int d = threadIdx.x;
+  float pm[kNH], pl[kNH], po[kNH];
+#pragma unroll
+  for (int j = 0; j < kNH; ++j) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][j]);
+    float lt = 0.0f, ot = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        if (s_m[w][j] == -INFINITY) continue;
+        const float e = fast_exp2(s_m[w][j] - M);
+        lt += e * s_l[w][j];
+        ot += e * merge_area(sm, w, kPathMma)[j * kHeadDim + d];
+      }
+    }
+    pm[j] = M;
+    pl[j] = lt;
+    po[j] = ot;
+  }
+  __syncthreads();  // the warps' slots are read; the tail may overwrite them
+  for (int c0 = a.t_tail; c0 < a.l; c0 += kTailTok) {
+    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, c0, s_m, s_l);
+    __syncthreads();
+    const float* mo0 = merge_area(sm, 0, kPathTail);
+#pragma unroll
+    for (int j = 0; j < kNH; ++j) {
+      const float tm = s_m[0][j];
+      const float M = fmaxf(pm[j], tm);
+      const float e1 = pm[j] == -INFINITY ? 0.0f : fast_exp2(pm[j] - M);
+      const float e2 = tm == -INFINITY ? 0.0f : fast_exp2(tm - M);
+      po[j] = po[j] * e1 + mo0[j * kHeadDim + d] * e2;
+      pl[j] = pl[j] * e1 + s_l[0][j] * e2;
+      pm[j] = M;
+    }
+    __syncthreads();  // before the next round overwrites the staged rows
+  }
+  float* out0 = merge_area(sm, 0, kPathMma);
+#pragma unroll
+  for (int j = 0; j < kNH; ++j) out0[j * kHeadDim + d] = po[j];
+  if (d < kWarps * kNH) {
+    const int w = d / kNH, j = d % kNH;
+    s_m[w][j] = w == 0 ? pick4(pm, j) : -INFINITY;
+    s_l[w][j] = w == 0 ? pick4(pl, j) : 0.0f;
+  }
+  __syncthreads();
+}
+
 // grid (splits, H * head_chunks, B), 128 threads.
 template <int BITS>
 __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a) {
@@ -1048,6 +1104,7 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
     packed_split<BITS>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
+  if (path == kPathMma && a.tail_fused && s == a.splits - 1) fused_tail<BITS>(cv, a, sm, unit, b, j0, nh, s_m, s_l);
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;

@@ -108,18 +108,27 @@ int max_splits(const kivi_config& c) {
 // packed splits of `chunk` (32-aligned) tokens.  Automatic packed splits fill
 // the budget beside this length's tail splits, with at least 256 tokens and a
 // multiple of four tiles each, so that the four warps of a CTA get equal
-// shares; an override n asks for n splits in all.
-void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail) {
+// shares; an override n asks for n splits in all.  When the budget cannot
+// hold a tail split beside one packed split, the tail rides on the last
+// packed split (*tail_fused, no tail splits).
+void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail,
+                int* tail_fused) {
   const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
   *t_tail = tt;
   *tail_splits = (l - tt + kivi::kTailTok - 1) / kivi::kTailTok;
+  *tail_fused = 0;
   const int tiles = tt / 32;
   if (tiles == 0) {
     *splits = *tail_splits;
     *chunk = 32;
     return;
   }
-  int smax = split_budget(c->cfg) - *tail_splits;
+  const int budget = split_budget(c->cfg);
+  if (c->splits_override <= 0 && budget < *tail_splits + 1) {
+    *tail_fused = 1;
+    *tail_splits = 0;
+  }
+  int smax = budget - *tail_splits;
   if (smax > max_splits(c->cfg) - *tail_splits) smax = max_splits(c->cfg) - *tail_splits;
   if (smax < 1) smax = 1;
   int per;  // tiles per packed split
@@ -250,8 +259,8 @@ KIVI_API kivi_status kivi_set_attention_splits(kivi_cache* c, int n_splits) {
 
 KIVI_API int kivi_attention_splits(const kivi_cache* c, int l) {
   if (!c || l <= 0) return 0;
-  int ts, s, ch, tt;
-  split_plan(c, l, &ts, &s, &ch, &tt);
+  int ts, s, ch, tt, tf;
+  split_plan(c, l, &ts, &s, &ch, &tt, &tf);
   return s;
 }
 
@@ -274,7 +283,7 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   a.l = c->length;
   a.nq_k = nq_k(c->length, c->cfg.residual);
   a.nq_v = nq_v(c->length, c->cfg.residual);
-  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail);
+  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
   const WsLayout w = ws_layout(c->cfg);
   char* ws = static_cast<char*>(workspace);
   a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
@@ -383,7 +392,7 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   a.l = c->length;
   a.nq_k = nq_k(c->length, c->cfg.residual);
   a.nq_v = nq_v(c->length, c->cfg.residual);
-  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail);
+  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
   char* base = static_cast<char*>(ws);
   a.ws_o = reinterpret_cast<float*>(base + w.o_off);
   a.ws_ml = reinterpret_cast<float*>(base + w.ml_off);

@@ -50,8 +50,10 @@ struct AttnArgs {
   // = nq_v rounded down to 32), kTailTok tokens each from t_tail + s*kTailTok;
   // split tail_splits + i covers the packed tiles [i*chunk, min(t_tail,
   // (i+1)*chunk)).
+  // With tail_fused set there are no tail splits: the last packed split also
+  // takes the tail, after its tiles (when the one-wave budget leaves no room).
   int t_tail;
-  int tail_splits, splits, chunk;
+  int tail_splits, splits, chunk, tail_fused;
   // Split partials of attention group gid = (b, kv-head, head chunk):
   float* ws_o;        // [gid][splits][kHeadChunk][D]  output sums
   float* ws_ml;       // [gid][splits][kHeadChunk][2]  (max in log2 units, sum)

@@ -141,6 +141,16 @@ def test_split_plan_and_workspace(K):
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 131072) == 76
     K.kivi_cache_destroy(h)
+    # 320 units: one split per unit fits the wave, so the tail rides on the
+    # packed split
+    c = cfg(K, batch=80, n_kv_heads=4, n_q_heads=8, residual=128, max_tokens=512)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    assert K.kivi_attention_splits(h, 450) == 1
+    # an explicit count keeps separate tail splits: the 130 tail tokens take 3,
+    # plus at least one packed split
+    K.kivi_set_attention_splits(h, 3)
+    assert K.kivi_attention_splits(h, 450) == 4
+    K.kivi_cache_destroy(h)
     # GQA 18 -> five chunks of four query heads
     c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=18, max_tokens=1024)
     h = K.kivi_cache_init(c, _fake_buffers(K))

@@ -183,6 +183,18 @@ def test_attention_short_contexts(T_):
     check_attention(g, o, wl)
 
 
+@pytest.mark.parametrize("R", [32, 128])
+@pytest.mark.parametrize("bits", [2, 4])
+def test_attention_tail_on_last_packed_split(R, bits):
+    """320 (batch, kv-head) units leave no room in one wave for a tail split,
+    so the last packed split also takes the tail (one or three 64-token
+    rounds)."""
+    wl = W.synthetic("tf", B=80, Hq=8, Hkv=4, T=450, R=R, bits=bits, seed=R + bits)
+    g, o = run_prefill(wl)
+    assert g.splits() == 1
+    check_attention(g, o, wl)
+
+
 def test_attention_split_count_invariance():
     wl = W.synthetic("sp", B=1, Hq=8, Hkv=2, T=3000, R=128, seed=11)
     g, o = run_prefill(wl)
