@@ -246,6 +246,27 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
   return st;
 }
 
+KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void* v, kivi_dtype dtype,
+                                        int n_tokens, void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
+  if ((long)c->length + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  const int l0 = c->length, L = l0 + n_tokens, R = c->cfg.residual;
+  kivi_status st = cuda_status(kivi::launch_append_tokens(view(c), k, v, (int)dtype, l0, n_tokens,
+                                                          nq_k(l0, R), nq_k(L, R), nq_v(l0, R), nq_v(L, R),
+                                                          static_cast<cudaStream_t>(stream)));
+  if (st == KIVI_OK) c->length = L;
+  return st;
+}
+
+KIVI_API kivi_status kivi_cache_set_length(kivi_cache* c, int length) {
+  if (!c) return KIVI_EINVAL;
+  if (length < 0 || length > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  c->length = length;
+  return KIVI_OK;
+}
+
 KIVI_API size_t kivi_attention_workspace_bytes(const kivi_cache* c) {
   if (!c) return 0;
   return ws_layout(c->cfg).total;

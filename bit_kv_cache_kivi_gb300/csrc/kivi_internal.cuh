@@ -39,6 +39,13 @@ cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k,
 cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
                           int dtype, int t, cudaStream_t st);
 
+// n tokens appended to a cache of length l0 (k, v: [B][H][n][D] of dtype):
+// key groups [nq_k0, nq_k1) and value tokens [nq_v0, nq_v1) become
+// quantized, then the last min(n, R) tokens go to the ring.
+cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype,
+                                 int l0, int n, int nq_k0, int nq_k1, int nq_v0, int nq_v1,
+                                 cudaStream_t st);
+
 struct AttnArgs {
   const void* q;
   void* out;

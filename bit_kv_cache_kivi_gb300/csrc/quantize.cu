@@ -6,6 +6,8 @@
 // groups of G = 32 channels.  Residual split (chooblog KIVI review, §3.2.2
 // and Algorithm 1): the first nq_k = R*floor(l/R) keys and nq_v = max(l-R, 0)
 // values are quantized, the rest stay fp16 in a ring of R slots.
+#include <climits>
+
 #include "quant_common.cuh"
 
 namespace kivi {
@@ -176,53 +178,49 @@ __device__ __forceinline__ void store_value_units(uint8_t* row, int g, const uin
 //           the two parities' min/max meet in one shuffle;
 //   values: lane l owns, in round rr, the whole 32-channel group l%4 of row
 //           8*rr + l/4, so min, max and the scale are computed once per group.
+// Value-tile swizzle (16-bit inputs): chunk j of group g of row r sits at
+// 4g + (j ^ ((g >> 1) | ((r & 1) << 1))), so the 8 lanes of a shared-memory
+// phase (rows r, r+1; groups 0..3) hit distinct 16-byte bank slots.  fp32 rows
+// (two chunks per 8 elements, CPG = 8) are left unswizzled.
+template <int CPG>
+__device__ __forceinline__ int vswz(int r, int c) {
+  if constexpr (CPG != 4) {
+    return c;
+  } else {
+    const int g = c >> 2, j = c & 3;
+    return 4 * g + (j ^ ((g >> 1) | ((r & 1) << 1)));
+  }
+}
+
+// Quantizes this warp's half of one staged 32-token chunk t0 = 32 * chunk:
+// the keys for warp 0, the values for warp 1.  kq: quantize the chunk's key
+// group (one per channel); key rows t >= kring (t < T) go to the ring as
+// fp16.  Value rows t in [vlo, vhi) are quantized (one group per 32
+// channels); value rows t >= vring outside that range (t < T) go to the ring.
+// s_in holds the chunk's input rows in the layout of DT (value rows
+// swizzled by vswz).
+//   keys:   lane l owns channels 8*(l%16) .. +7 of the rows of parity l/16;
+//           the two parities' min/max meet in one shuffle;
+//   values: lane l owns, in round rr, the whole 32-channel group l%4 of row
+//           8*rr + l/4, so min, max and the scale are computed once per group.
 template <int BITS, int DT>
-__global__ void __launch_bounds__(64)
-quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
-                        const void* __restrict__ vin, int T, int nq_k, int nq_v) {
+__device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4* s_in, uint8_t* s_codes,
+                                               long unit, int chunk, int T, bool kq, int kring, int vlo,
+                                               int vhi, int vring) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;          // packed bytes per token row
   constexpr int EB = DT == kF32 ? 4 : 2;           // input bytes per element
   constexpr int CPR = kHeadDim * EB / 16;          // 16-byte chunks per input row
   constexpr int CPG = CPR / 4;                     // chunks per 32-channel group
   constexpr int CPE = EB / 2;                      // chunks per 8 elements
-  __shared__ __align__(16) uint4 s_in_all[2][32 * CPR];
-  __shared__ __align__(16) uint8_t s_codes_all[2][32 * RB];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint4* s_in = s_in_all[warp];
-  uint8_t* s_codes = s_codes_all[warp];
-  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
-  const int rows = min(32, T - t0);
-
-  // value-tile swizzle (16-bit inputs): chunk j of group g of row r sits at
-  // 4g + (j ^ ((g >> 1) | ((r & 1) << 1))), so the 8 lanes of a shared-memory
-  // phase (rows r, r+1; groups 0..3) hit distinct 16-byte bank slots.  fp32
-  // rows (two chunks per 8 elements) are left unswizzled.
-  auto vswz = [](int r, int c) {
-    if (CPG != 4) return c;
-    const int g = c >> 2, j = c & 3;
-    return 4 * g + (j ^ ((g >> 1) | ((r & 1) << 1)));
-  };
-
-  {
-    const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * T + t0) * (long)(kHeadDim * EB);
-    for (int i = lane; i < rows * CPR; i += 32) {
-      const int r = i / CPR, c = i % CPR;
-      cp_async16(&s_in[r * CPR + (warp == 0 ? c : vswz(r, c))], src + 16L * i);
-    }
-    asm volatile("cp.async.commit_group;");
-    asm volatile("cp.async.wait_group 0;");
-    __syncwarp();
-  }
 
   if (warp == 0) {
     // ---------------- keys ----------------
     const int cl = lane & 15, par = lane >> 4;
     const int c8 = cl * 8;
-    if (t0 + 32 <= nq_k) {
+    if (kq) {
       __half2 mn[4], mx[4], x[4];
       smem8<DT>(&s_in[par * CPR + cl * CPE], x);
 #pragma unroll
@@ -302,7 +300,7 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
       // keys of a chunk that is not a whole quantized group stay fp16
       for (int k = 0; k < 16; ++k) {
         const int t = t0 + 2 * k + par;
-        if (t >= nq_k && t < T) {
+        if (t >= kring && t < T) {
           __half2 x[4];
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
           *reinterpret_cast<uint4*>(cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + c8) = h2x4_bits(x);
@@ -321,8 +319,8 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
       if (t >= T) continue;
       __half2 x[4][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) smem8<DT>(&s_in[row * CPR + vswz(row, g * CPG + j * CPE)], x[j]);
-      if (t < nq_v) {
+      for (int j = 0; j < 4; ++j) smem8<DT>(&s_in[row * CPR + vswz<CPG>(row, g * CPG + j * CPE)], x[j]);
+      if (t >= vlo && t < vhi) {
         __half2 mn = x[0][0], mx = x[0][0];
 #pragma unroll
         for (int j = 0; j < 4; ++j)
@@ -360,18 +358,111 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
         const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup) + g;
         cv.scale_v[so] = p.sh;
         cv.zero_v[so] = p.zh;
-      } else {
+      } else if (t >= vring) {
         __half* dst = cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 32 * g;
 #pragma unroll
         for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(dst + 8 * j) = h2x4_bits(x[j]);
       }
     }
     __syncwarp();
-    const int nrows = min(max(nq_v - t0, 0), 32);
+    const int r_lo = min(max(vlo - t0, 0), 32), r_hi = min(max(vhi - t0, 0), 32);
     uint4* gdst = reinterpret_cast<uint4*>(cv.codes_v + (unit * cv.Tcap + t0) * RB);
     const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
-    for (int i = lane; i < nrows * RB / 16; i += 32) gdst[i] = ssrc[i];
+    for (int i = r_lo * RB / 16 + lane; i < r_hi * RB / 16; i += 32) gdst[i] = ssrc[i];
   }
+}
+
+// Prefill: one CTA per (32-token chunk, kv-head, b) stages the chunk's raw
+// key rows (warp 0) and value rows (warp 1) with cp.async and quantizes them
+// (keys of whole groups below nq_k, values below nq_v; the rest to the ring).
+template <int BITS, int DT>
+__global__ void __launch_bounds__(64)
+quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
+                        const void* __restrict__ vin, int T, int nq_k, int nq_v) {
+  constexpr int RB = kHeadDim * BITS / 8;
+  constexpr int EB = DT == kF32 ? 4 : 2;
+  constexpr int CPR = kHeadDim * EB / 16;
+  constexpr int CPG = CPR / 4;
+  __shared__ __align__(16) uint4 s_in_all[2][32 * CPR];
+  __shared__ __align__(16) uint8_t s_codes_all[2][32 * RB];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4* s_in = s_in_all[warp];
+  uint8_t* s_codes = s_codes_all[warp];
+  const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long unit = (long)b * cv.H + h;
+  const int t0 = chunk * 32;
+  const int rows = min(32, T - t0);
+  {
+    const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * T + t0) * (long)(kHeadDim * EB);
+    for (int i = lane; i < rows * CPR; i += 32) {
+      const int r = i / CPR, c = i % CPR;
+      cp_async16(&s_in[r * CPR + (warp == 0 ? c : vswz<CPG>(r, c))], src + 16L * i);
+    }
+    asm volatile("cp.async.commit_group;");
+    asm volatile("cp.async.wait_group 0;");
+    __syncwarp();
+  }
+  quantize_chunk<BITS, DT>(cv, s_in, s_codes, unit, chunk, T, t0 + 32 <= nq_k, nq_k, 0, nq_v, nq_v);
+}
+
+// Appending n tokens to a cache of length l0 (L = l0 + n), step 1: the key
+// groups that become whole, [nq_k0, nq_k1), and the value tokens that leave
+// the window, [nq_v0, nq_v1), are quantized from the chunks that hold them.
+// A token t < l0 is read from its ring slot, t >= l0 from the input (rounded
+// to fp16).  Nothing is written to the ring (step 2 does that after every
+// read of this step).  One CTA per (chunk c_lo + blockIdx.x, kv-head, b).
+template <int BITS, int DT>
+__global__ void __launch_bounds__(64)
+append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int l0, int n,
+                       int c_lo, int nq_k0, int nq_k1, int nq_v0, int nq_v1) {
+  constexpr int RB = kHeadDim * BITS / 8;
+  constexpr int CPR = 16;  // staged as fp16: 16-byte chunks per row
+  __shared__ __align__(16) uint4 s_in_all[2][32 * CPR];
+  __shared__ __align__(16) uint8_t s_codes_all[2][32 * RB];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint4* s_in = s_in_all[warp];
+  uint8_t* s_codes = s_codes_all[warp];
+  const int chunk = c_lo + blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const long unit = (long)b * cv.H + h;
+  const int t0 = chunk * 32;
+  const int L = l0 + n;
+  const int rows = min(32, L - t0);
+  const __half* ring = warp == 0 ? cv.ring_k : cv.ring_v;
+  const void* in = warp == 0 ? kin : vin;
+  for (int i = lane; i < rows * CPR; i += 32) {
+    const int r = i / CPR, c = i % CPR;
+    const int t = t0 + r;
+    uint4 x;
+    if (t < l0) {
+      x = *reinterpret_cast<const uint4*>(ring + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+    } else {
+      __half2 hx[4];
+      load8<DT>(in, (unit * n + (t - l0)) * kHeadDim + 8 * c, hx);
+      x = h2x4_bits(hx);
+    }
+    s_in[r * CPR + (warp == 0 ? c : vswz<4>(r, c))] = x;
+  }
+  __syncwarp();
+  const bool kq = t0 >= nq_k0 && t0 + 32 <= nq_k1;
+  quantize_chunk<BITS, kF16>(cv, s_in, s_codes, unit, chunk, L, kq, INT_MAX, max(nq_v0, t0), nq_v1, INT_MAX);
+}
+
+// Appending n tokens, step 2: the last min(n, R) of them go to their ring
+// slots (t mod R), keys and values, rounded to fp16.  One CTA per (token,
+// kv-head, b); thread d owns channel d.
+template <int DT>
+__global__ void __launch_bounds__(128)
+append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int l0, int n) {
+  const int m = min(n, cv.R);
+  const int i = n - m + blockIdx.x;  // input row
+  const int t = l0 + i, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const long unit = (long)b * cv.H + h;
+  const long src = (unit * n + i) * kHeadDim + d;
+  const long dst = (unit * cv.R + t % cv.R) * kHeadDim + d;
+  cv.ring_k[dst] = load1<DT>(kin, src);
+  cv.ring_v[dst] = load1<DT>(vin, src);
 }
 
 // One CTA per (kv-head, b); thread d owns channel d.  Appends token t:
@@ -472,7 +563,38 @@ cudaError_t append_bits(const CacheView& cv, const void* k, const void* v, int d
   return cudaGetLastError();
 }
 
+template <int BITS, int DT>
+cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, int l0, int n, int c_lo,
+                             int c_hi, int nq_k0, int nq_k1, int nq_v0, int nq_v1, cudaStream_t st) {
+  if (c_hi > c_lo)
+    append_quantize_kernel<BITS, DT><<<dim3(c_hi - c_lo, cv.H, cv.B), 64, 0, st>>>(cv, k, v, l0, n, c_lo, nq_k0,
+                                                                                  nq_k1, nq_v0, nq_v1);
+  append_ring_kernel<DT><<<dim3(min(n, cv.R), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, l0, n);
+  return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t append_tokens_bits(const CacheView& cv, const void* k, const void* v, int dtype, int l0, int n,
+                               int c_lo, int c_hi, int nq_k0, int nq_k1, int nq_v0, int nq_v1,
+                               cudaStream_t st) {
+  switch (dtype) {
+    case kF32: return append_tokens_dt<BITS, kF32>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+    case kF16: return append_tokens_dt<BITS, kF16>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+    default: return append_tokens_dt<BITS, kBF16>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype, int l0, int n,
+                                 int nq_k0, int nq_k1, int nq_v0, int nq_v1, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  // the chunks holding [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
+  const int lo = min(nq_k0, nq_v0), hi = max(nq_k1, nq_v1);
+  const int c_lo = lo / 32, c_hi = hi > lo ? (hi + 31) / 32 : c_lo;
+  return cv.bits == 2 ? append_tokens_bits<2>(cv, k, v, dtype, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st)
+                      : append_tokens_bits<4>(cv, k, v, dtype, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+}
 
 cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const void* v,
                                     int dtype, int T, int nq_k, int nq_v, cudaStream_t st) {

@@ -67,6 +67,8 @@ def lib() -> C.CDLL:
                                           C.POINTER(vp)]),
                 "kivi_quantize_prefill": (i32, [vp, vp, vp, i32, i32, vp]),
                 "kivi_append_decode": (i32, [vp, vp, vp, i32, vp]),
+                "kivi_append_tokens": (i32, [vp, vp, vp, i32, i32, vp]),
+                "kivi_cache_set_length": (i32, [vp, i32]),
                 "kivi_attention_workspace_bytes": (sz, [vp]),
                 "kivi_decode_attention": (i32, [vp, vp, i32, vp, f32, vp, sz, vp]),
                 "kivi_set_attention_splits": (i32, [vp, i32]),
@@ -127,6 +129,15 @@ def kivi_quantize_prefill(h, k, v, dtype: int, n_tokens: int, stream=None) -> No
 def kivi_append_decode(h, k_new, v_new, dtype: int, stream=None) -> None:
     _check(lib().kivi_append_decode(h, _ptr(k_new), _ptr(v_new), dtype, _stream(stream)),
            "kivi_append_decode")
+
+
+def kivi_append_tokens(h, k, v, dtype: int, n_tokens: int, stream=None) -> None:
+    _check(lib().kivi_append_tokens(h, _ptr(k), _ptr(v), dtype, n_tokens, _stream(stream)),
+           "kivi_append_tokens")
+
+
+def kivi_cache_set_length(h, length: int) -> None:
+    _check(lib().kivi_cache_set_length(h, length), "kivi_cache_set_length")
 
 
 def kivi_attention_workspace_bytes(h) -> int:
@@ -229,6 +240,18 @@ class KiviCache:
         if self._check_kv(v_new, None) != dt:
             raise ValueError("K and V dtypes differ")
         kivi_append_decode(self.handle, k_new, v_new, dt, stream)
+
+    def append_tokens(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        """Append k, v [B][H][n][D] (n >= 1) to a cache of any length."""
+        n = k.shape[2]
+        dt = self._check_kv(k, n)
+        if self._check_kv(v, n) != dt:
+            raise ValueError("K and V dtypes differ")
+        kivi_append_tokens(self.handle, k, v, dt, n, stream)
+
+    def set_length(self, length: int) -> None:
+        """The length of a state whose buffers were just restored."""
+        kivi_cache_set_length(self.handle, length)
 
     def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
                   softmax_scale: float = 0.0, stream=None) -> torch.Tensor:

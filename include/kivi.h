@@ -125,6 +125,26 @@ kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
                                const void *v_new, kivi_dtype dtype,
                                void *stream);
 
+/* Append n_tokens tokens at once (chunked prefill into a non-empty cache;
+ * the review §1.3 prefill step continued on a cache that already holds
+ * tokens).  k, v: device [B][H][n_tokens][D] of dtype, contiguous,
+ * 16-byte aligned.  The result is the cache that n_tokens calls of
+ * kivi_append_decode would leave (the review's Algorithm 1 applied token by
+ * token), bit for bit: the key groups that become whole and the value tokens
+ * that leave the window are quantized (old tokens read from the rings), then
+ * the last min(n_tokens, R) tokens go to their ring slots.  Two kernel
+ * launches on the stream.  KIVI_ECAPACITY if length + n_tokens > max_tokens,
+ * KIVI_EINVAL if n_tokens <= 0. */
+kivi_status kivi_append_tokens(kivi_cache *c, const void *k, const void *v,
+                               kivi_dtype dtype, int n_tokens, void *stream);
+
+/* Declare the cache's length after its eight buffers were restored from a
+ * saved state (the buffers are the caller's tensors, so saving and restoring
+ * a cache is copying them plus this length).
+ * The length of a state is kivi_cache_length() at save time.  Host only; no
+ * device work.  KIVI_ECAPACITY if length is outside [0, max_tokens]. */
+kivi_status kivi_cache_set_length(kivi_cache *c, int length);
+
 /* Device workspace (bytes) kivi_decode_attention needs for this handle's
  * shape at any length: split-K partial results, merged groups of partials,
  * counters, and a status word (the int at byte offset bytes - 16: nonzero

@@ -100,6 +100,14 @@ def test_init_validation_and_host_state(K):
         assert lib.kivi_quantize_prefill(h, 0, 16, K.KIVI_F16, 5, None) == K.KIVI_EINVAL
         assert lib.kivi_append_decode(h, 16, 16, 9, None) == K.KIVI_EDTYPE
         assert lib.kivi_append_decode(h, 0, 16, K.KIVI_F16, None) == K.KIVI_EINVAL
+        assert lib.kivi_append_tokens(h, 16, 16, 9, 3, None) == K.KIVI_EDTYPE
+        assert lib.kivi_append_tokens(h, 16, 16, K.KIVI_F16, 0, None) == K.KIVI_EINVAL
+        assert lib.kivi_append_tokens(h, 16, 24, K.KIVI_F16, 3, None) == K.KIVI_EINVAL  # misaligned
+        assert lib.kivi_append_tokens(h, 16, 16, K.KIVI_F16, 4097, None) == K.KIVI_ECAPACITY
+        assert lib.kivi_cache_set_length(h, 4097) == K.KIVI_ECAPACITY
+        assert lib.kivi_cache_set_length(h, -1) == K.KIVI_ECAPACITY
+        assert lib.kivi_cache_set_length(h, 100) == K.KIVI_OK and K.kivi_cache_length(h) == 100
+        assert lib.kivi_cache_set_length(h, 0) == K.KIVI_OK
         ws = K.kivi_attention_workspace_bytes(h)
         assert lib.kivi_decode_attention(h, 16, K.KIVI_F16, 16, 0.0, 16, ws, None) == K.KIVI_ESTATE
         assert lib.kivi_decode_attention(h, 16, 5, 16, 0.0, 16, ws, None) == K.KIVI_EDTYPE
