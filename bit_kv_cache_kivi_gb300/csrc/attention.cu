@@ -293,7 +293,7 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
     if (r < nk) {
       if (c < CPR) cp_async16(&ts.krow[r][c], cv.codes_k + (unit * cv.Tcap + t) * RB + 16 * c);
     } else {
-      cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+      cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     }
     if (r < nv) {
       if (c < CPR) {
@@ -305,7 +305,7 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
         cp_async8(dst + 8, cv.zero_v + so);
       }
     } else {
-      cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+      cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     }
   }
   const int ngk = (nk + kGroup - 1) / kGroup;

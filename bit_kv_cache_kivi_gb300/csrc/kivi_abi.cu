@@ -41,13 +41,26 @@ kivi_status check_config(const kivi_config* c) {
   if (c->n_q_heads % c->n_kv_heads) return KIVI_ESHAPE;
   if (c->max_tokens <= 0 || c->max_tokens % c->residual) return KIVI_ESHAPE;
   if (c->batch > 65535 || c->n_kv_heads > 4096) return KIVI_ESHAPE;  // grid limits
+  if (c->policy != KIVI_POLICY_ALG1 && c->policy != KIVI_POLICY_SHARED) return KIVI_EINVAL;
   return KIVI_OK;
 }
 
-// Algorithm 1 (chooblog KIVI review §3.2.2): keys X_K[:l - l mod R],
-// values X_V[:l - R] are held quantized.
-int nq_k(int l, int R) { return l - l % R; }
-int nq_v(int l, int R) { return l > R ? l - R : 0; }
+// Quantized counts after l tokens.  ALG1 (chooblog KIVI review §3.2.2,
+// Algorithm 1): keys X_K[:l - l mod R], values X_V[:l - R].  SHARED
+// (veloxquant-mlx "KIVI" How it works, items 3-4): both G*floor((l - R)/G).
+int nq_k(int l, const kivi_config& c) {
+  if (c.policy == KIVI_POLICY_SHARED) return l > c.residual ? (l - c.residual) / c.group * c.group : 0;
+  return l - l % c.residual;
+}
+int nq_v(int l, const kivi_config& c) {
+  if (c.policy == KIVI_POLICY_SHARED) return nq_k(l, c);
+  return l > c.residual ? l - c.residual : 0;
+}
+
+// Ring slots: R under ALG1, R + G under SHARED (up to R + G - 1 fp16 tokens).
+int ring_slots(const kivi_config& c) {
+  return c.policy == KIVI_POLICY_SHARED ? c.residual + c.group : c.residual;
+}
 
 kivi::CacheView view(const kivi_cache* c) {
   kivi::CacheView v;
@@ -62,6 +75,7 @@ kivi::CacheView view(const kivi_cache* c) {
   v.B = c->cfg.batch;
   v.H = c->cfg.n_kv_heads;
   v.R = c->cfg.residual;
+  v.W = ring_slots(c->cfg);
   v.Tcap = c->cfg.max_tokens;
   v.bits = c->cfg.bits;
   return v;
@@ -74,8 +88,8 @@ long attention_units(const kivi_config& c) {
   return (long)c.batch * c.n_kv_heads * ((grp + kivi::kHeadChunk - 1) / kivi::kHeadChunk);
 }
 
-// Tail splits at most: the tail [floor32(l - R), l) holds fewer than R + 32
-// tokens.
+// Tail splits at most: the tail [floor32(nq_v), l) holds fewer than R + 32
+// tokens under either policy.
 int max_tail_splits(const kivi_config& c) {
   return (c.residual + 31 + kivi::kTailTok - 1) / kivi::kTailTok;
 }
@@ -113,7 +127,7 @@ int max_splits(const kivi_config& c) {
 // packed split (*tail_fused, no tail splits).
 void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail,
                 int* tail_fused) {
-  const int tt = (nq_v(l, c->cfg.residual) / 32) * 32;
+  const int tt = (nq_v(l, c->cfg) / 32) * 32;
   *t_tail = tt;
   *tail_splits = (l - tt + kivi::kTailTok - 1) / kivi::kTailTok;
   *tail_fused = 0;
@@ -193,7 +207,7 @@ KIVI_API kivi_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes[8]) {
   bytes[3] = codes;                      // codes_v
   bytes[4] = units * T * (D / G) * 2;    // scale_v
   bytes[5] = bytes[4];                   // zero_v
-  bytes[6] = units * R * D * 2;          // ring_k
+  bytes[6] = units * ring_slots(*cfg) * D * 2;  // ring_k
   bytes[7] = bytes[6];                   // ring_v
   return KIVI_OK;
 }
@@ -226,9 +240,8 @@ KIVI_API kivi_status kivi_quantize_prefill(kivi_cache* c, const void* k, const v
   if (n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
   if (n_tokens == 0) return KIVI_OK;
   if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
-  const int R = c->cfg.residual;
   kivi_status st = cuda_status(kivi::launch_quantize_prefill(
-      view(c), k, v, (int)dtype, n_tokens, nq_k(n_tokens, R), nq_v(n_tokens, R),
+      view(c), k, v, (int)dtype, n_tokens, nq_k(n_tokens, c->cfg), nq_v(n_tokens, c->cfg),
       static_cast<cudaStream_t>(stream)));
   if (st == KIVI_OK) c->length = n_tokens;
   return st;
@@ -240,8 +253,19 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
   if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
   if (!k_new || !v_new) return KIVI_EINVAL;
   if (c->length >= c->cfg.max_tokens) return KIVI_ECAPACITY;
-  kivi_status st = cuda_status(kivi::launch_append(view(c), k_new, v_new, (int)dtype,
-                                                   c->length, static_cast<cudaStream_t>(stream)));
+  const int l0 = c->length;
+  const kivi_config& f = c->cfg;
+  cudaError_t e;
+  if (f.policy == KIVI_POLICY_SHARED) {
+    // the one-token case of the multi-token append: a whole group of keys and
+    // values is quantized when nq grows, then the token goes to the ring
+    if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_EINVAL;
+    e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, l0, 1, nq_k(l0, f), nq_k(l0 + 1, f),
+                                   nq_v(l0, f), nq_v(l0 + 1, f), static_cast<cudaStream_t>(stream));
+  } else {
+    e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, l0, static_cast<cudaStream_t>(stream));
+  }
+  kivi_status st = cuda_status(e);
   if (st == KIVI_OK) c->length += 1;
   return st;
 }
@@ -252,9 +276,10 @@ KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void
   if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
   if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
   if ((long)c->length + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
-  const int l0 = c->length, L = l0 + n_tokens, R = c->cfg.residual;
+  const int l0 = c->length, L = l0 + n_tokens;
+  const kivi_config& f = c->cfg;
   kivi_status st = cuda_status(kivi::launch_append_tokens(view(c), k, v, (int)dtype, l0, n_tokens,
-                                                          nq_k(l0, R), nq_k(L, R), nq_v(l0, R), nq_v(L, R),
+                                                          nq_k(l0, f), nq_k(L, f), nq_v(l0, f), nq_v(L, f),
                                                           static_cast<cudaStream_t>(stream)));
   if (st == KIVI_OK) c->length = L;
   return st;
@@ -302,8 +327,8 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.l = c->length;
-  a.nq_k = nq_k(c->length, c->cfg.residual);
-  a.nq_v = nq_v(c->length, c->cfg.residual);
+  a.nq_k = nq_k(c->length, c->cfg);
+  a.nq_v = nq_v(c->length, c->cfg);
   split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
   const WsLayout w = ws_layout(c->cfg);
   char* ws = static_cast<char*>(workspace);
@@ -411,8 +436,8 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
   a.scale_log2 = scale * 1.4426950408889634f;
   a.l = c->length;
-  a.nq_k = nq_k(c->length, c->cfg.residual);
-  a.nq_v = nq_v(c->length, c->cfg.residual);
+  a.nq_k = nq_k(c->length, c->cfg);
+  a.nq_v = nq_v(c->length, c->cfg);
   split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
   char* base = static_cast<char*>(ws);
   a.ws_o = reinterpret_cast<float*>(base + w.o_off);

@@ -27,6 +27,7 @@ struct CacheView {
   __half* ring_k;
   __half* ring_v;
   int B, H, R, Tcap, bits;
+  int W;  // ring slots: token t of a unit is in slot t mod W
 };
 
 // Input dtype codes (same values as kivi_dtype).

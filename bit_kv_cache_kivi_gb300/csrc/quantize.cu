@@ -303,7 +303,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         if (t >= kring && t < T) {
           __half2 x[4];
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
-          *reinterpret_cast<uint4*>(cv.ring_k + (unit * cv.R + t % cv.R) * kHeadDim + c8) = h2x4_bits(x);
+          *reinterpret_cast<uint4*>(cv.ring_k + (unit * cv.W + t % cv.W) * kHeadDim + c8) = h2x4_bits(x);
         }
       }
     }
@@ -359,7 +359,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         cv.scale_v[so] = p.sh;
         cv.zero_v[so] = p.zh;
       } else if (t >= vring) {
-        __half* dst = cv.ring_v + (unit * cv.R + t % cv.R) * kHeadDim + 32 * g;
+        __half* dst = cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 32 * g;
 #pragma unroll
         for (int j = 0; j < 4; ++j) *reinterpret_cast<uint4*>(dst + 8 * j) = h2x4_bits(x[j]);
       }
@@ -436,7 +436,7 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
     const int t = t0 + r;
     uint4 x;
     if (t < l0) {
-      x = *reinterpret_cast<const uint4*>(ring + (unit * cv.R + t % cv.R) * kHeadDim + 8 * c);
+      x = *reinterpret_cast<const uint4*>(ring + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     } else {
       __half2 hx[4];
       load8<DT>(in, (unit * n + (t - l0)) * kHeadDim + 8 * c, hx);
@@ -449,18 +449,18 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
   quantize_chunk<BITS, kF16>(cv, s_in, s_codes, unit, chunk, L, kq, INT_MAX, max(nq_v0, t0), nq_v1, INT_MAX);
 }
 
-// Appending n tokens, step 2: the last min(n, R) of them go to their ring
-// slots (t mod R), keys and values, rounded to fp16.  One CTA per (token,
+// Appending n tokens, step 2: the last min(n, W) of them go to their ring
+// slots (t mod W), keys and values, rounded to fp16.  One CTA per (token,
 // kv-head, b); thread d owns channel d.
 template <int DT>
 __global__ void __launch_bounds__(128)
 append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int l0, int n) {
-  const int m = min(n, cv.R);
+  const int m = min(n, cv.W);
   const int i = n - m + blockIdx.x;  // input row
   const int t = l0 + i, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
   const long unit = (long)b * cv.H + h;
   const long src = (unit * n + i) * kHeadDim + d;
-  const long dst = (unit * cv.R + t % cv.R) * kHeadDim + d;
+  const long dst = (unit * cv.W + t % cv.W) * kHeadDim + d;
   cv.ring_k[dst] = load1<DT>(kin, src);
   cv.ring_v[dst] = load1<DT>(vin, src);
 }
@@ -569,7 +569,7 @@ cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, 
   if (c_hi > c_lo)
     append_quantize_kernel<BITS, DT><<<dim3(c_hi - c_lo, cv.H, cv.B), 64, 0, st>>>(cv, k, v, l0, n, c_lo, nq_k0,
                                                                                   nq_k1, nq_v0, nq_v1);
-  append_ring_kernel<DT><<<dim3(min(n, cv.R), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, l0, n);
+  append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, l0, n);
   return cudaGetLastError();
 }
 

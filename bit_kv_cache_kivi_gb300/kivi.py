@@ -37,10 +37,13 @@ class KiviError(RuntimeError):
         super().__init__(msg)
 
 
+KIVI_POLICY_ALG1, KIVI_POLICY_SHARED = 0, 1
+
+
 class kivi_config(C.Structure):
     _fields_ = [("bits", C.c_int), ("group", C.c_int), ("residual", C.c_int),
                 ("head_dim", C.c_int), ("batch", C.c_int), ("n_kv_heads", C.c_int),
-                ("n_q_heads", C.c_int), ("max_tokens", C.c_int)]
+                ("n_q_heads", C.c_int), ("max_tokens", C.c_int), ("policy", C.c_int)]
 
 
 class kivi_buffers(C.Structure):
@@ -187,9 +190,9 @@ class KiviCache:
 
     def __init__(self, *, batch: int, n_kv_heads: int, n_q_heads: int, max_tokens: int,
                  bits: int = 2, group: int = 32, residual: int = 32, head_dim: int = 128,
-                 device="cuda"):
+                 policy: int = 0, device="cuda"):
         self.cfg = kivi_config(bits, group, residual, head_dim, batch, n_kv_heads,
-                               n_q_heads, max_tokens)
+                               n_q_heads, max_tokens, policy)
         d = torch.device(device)
         if d.type == "cuda" and d.index is None:
             d = torch.device("cuda", torch.cuda.current_device())
@@ -281,6 +284,7 @@ class KiviCache:
         """The buffers as shaped tensors (fp16 buffers as int16 bit patterns)."""
         c = self.cfg
         B, H, T, D, G, R = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group, c.residual
+        R = R + G if c.policy == KIVI_POLICY_SHARED else R  # ring slots
         rb = D * c.bits // 8
         shapes = {"codes_k": (B, H, T, rb), "scale_k": (B, H, T // G, D),
                   "zero_k": (B, H, T // G, D), "codes_v": (B, H, T, rb),

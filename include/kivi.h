@@ -44,12 +44,19 @@
  *   codes_v [B][H][T][D*b/8] u8   packed value rows
  *   scale_v [B][H][T][D/G]   f16  one (scale, zero) per G channels per token
  *   zero_v  [B][H][T][D/G]   f16
- *   ring_k  [B][H][R][D]     f16  residual keys, token t in slot t mod R
- *   ring_v  [B][H][R][D]     f16  residual values, token t in slot t mod R
+ *   ring_k  [B][H][W][D]     f16  residual keys, token t in slot t mod W
+ *   ring_v  [B][H][W][D]     f16  residual values, token t in slot t mod W
  * Channel e of a packed row is bits [(e*b)%8, (e*b)%8 + b) of byte (e*b)/8.
- * After l tokens (Algorithm 1): the first nq_k(l) = R*floor(l/R) keys and
- * the first nq_v(l) = max(l-R, 0) values are quantized; the rest are in the
- * rings.  Rows and slots that hold no live token are left untouched.
+ * Residual policy (kivi_config.policy):
+ *   KIVI_POLICY_ALG1 (the chooblog review's Algorithm 1): after l tokens the
+ *     first nq_k(l) = R*floor(l/R) keys and the first nq_v(l) = max(l-R, 0)
+ *     values are quantized; W = R ring slots.
+ *   KIVI_POLICY_SHARED (veloxquant-mlx "KIVI" How it works, items 3-4: at
+ *     least the R most recent tokens stay fp16, aged-out tokens are
+ *     quantized in whole groups): keys and values share nq(l) =
+ *     G*floor(max(l-R, 0)/G); W = R + G ring slots.
+ * The rest of the tokens are in the rings.  Rows and slots that hold no live
+ * token are left untouched.
  */
 #ifndef KIVI_H
 #define KIVI_H
@@ -74,6 +81,8 @@ typedef enum {
 
 typedef enum { KIVI_F32 = 0, KIVI_F16 = 1, KIVI_BF16 = 2 } kivi_dtype;
 
+typedef enum { KIVI_POLICY_ALG1 = 0, KIVI_POLICY_SHARED = 1 } kivi_policy;
+
 /* Cache configuration (veloxquant-mlx "KIVI" usage: bit width, group size,
  * residual length) plus the tensor shape. */
 typedef struct {
@@ -85,6 +94,7 @@ typedef struct {
   int n_kv_heads;  /* H */
   int n_q_heads;   /* a multiple of n_kv_heads; query head j reads KV head j/(Hq/H) */
   int max_tokens;  /* capacity T, a multiple of R */
+  int policy;      /* kivi_policy: KIVI_POLICY_ALG1 (0) or KIVI_POLICY_SHARED */
 } kivi_config;
 
 /* The eight caller-owned device buffers, in the layout above. */
@@ -116,11 +126,14 @@ kivi_status kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v,
 
 /* Append one decoded token (review §1.3 decoding step 1; Algorithm 1
  * decoding phase).  k_new, v_new: device [B][H][D] of dtype.  Token t = length
- * goes to ring slot t mod R; if t >= R, the value token t-R leaves the
+ * goes to ring slot t mod W.  ALG1: if t >= R, the value token t-R leaves the
  * window and is quantized per token; if t+1 is a multiple of R, the R keys of
- * the ring (a whole number of groups) are quantized per channel.  The
+ * the ring (a whole number of groups) are quantized per channel.  SHARED:
+ * when t+1-R reaches a positive multiple of G, the G oldest ring tokens are
+ * quantized, keys per channel (one group) and values per token.  The
  * decision is taken on the host from the length alone.  KIVI_ECAPACITY when
- * the cache is full. */
+ * the cache is full; under SHARED, KIVI_EINVAL unless k_new and v_new are
+ * 16-byte aligned. */
 kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
                                const void *v_new, kivi_dtype dtype,
                                void *stream);

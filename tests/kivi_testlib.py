@@ -10,29 +10,37 @@ from bit_kv_cache_kivi_gb300 import workloads as W
 ATTN_TOL = 2e-3  # max_i |o_i - r_i| / max_i |r_i| per (batch, query head)
 
 
-def nq_k(l, R):
+ALG1, SHARED = 0, 1  # residual policies
+
+
+def nq_k(l, R, G=32, policy=ALG1):
+    if policy == SHARED:
+        return max(l - R, 0) // G * G
     return l - l % R
 
 
-def nq_v(l, R):
+def nq_v(l, R, G=32, policy=ALG1):
+    if policy == SHARED:
+        return max(l - R, 0) // G * G
     return max(l - R, 0)
 
 
-def gpu_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None):
+def gpu_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None,
+              policy: int = ALG1):
     from bit_kv_cache_kivi_gb300.kivi import KiviCache
     return KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq,
                      max_tokens=capacity or wl.capacity, bits=bits or wl.bits,
-                     group=wl.G, residual=wl.R, head_dim=wl.D)
+                     group=wl.G, residual=wl.R, head_dim=wl.D, policy=policy)
 
 
 def oracle_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None,
-                 units=None):
+                 units=None, policy: int = ALG1):
     """Oracle cache of the whole batch, or of the (b, h) units listed (B=1, H=1 each)."""
     from oracle.kivi_oracle import OracleCache
     cap = capacity or wl.capacity
     if units is None:
-        return OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, wl.B, wl.Hkv, cap)
-    return [OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, 1, 1, cap) for _ in units]
+        return OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, wl.B, wl.Hkv, cap, policy)
+    return [OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, 1, 1, cap, policy) for _ in units]
 
 
 def dev(x: np.ndarray, dtype: str) -> torch.Tensor:
@@ -48,12 +56,14 @@ def gpu_state(cache) -> dict:
     return out
 
 
-def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None) -> None:
+def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None,
+                  policy: int = ALG1) -> None:
     """Bit-exact comparison of the live part of two cache states.
 
     units: optional list of (b, h) selecting GPU units that correspond, in
     order, to oracle states given as a list (one B=1, H=1 state each)."""
-    qk, qv = nq_k(l, R), nq_v(l, R)
+    qk, qv = nq_k(l, R, G, policy), nq_v(l, R, G, policy)
+    W_ = R + G if policy == SHARED else R  # ring slots
     pairs = []
     if units is None:
         B, H = gst["codes_k"].shape[:2]
@@ -73,7 +83,7 @@ def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None) -> N
         chk("scale_v", slice(0, qv), slice(0, qv))
         chk("zero_v", slice(0, qv), slice(0, qv))
         for name, lo in (("ring_k", qk), ("ring_v", qv)):
-            slots = [t % R for t in range(lo, l)]
+            slots = [t % W_ for t in range(lo, l)]
             if slots:
                 chk(name, slots, slots)
 

@@ -58,9 +58,13 @@ def test_sizes(K):
     assert s[6] == s[7] == units * 32 * 128 * 2
     s4 = K.kivi_cache_sizes(cfg(K, bits=4))
     assert s4[0] == s4[3] == 2 * s[0] and s4[1:3] == s[1:3] and s4[4:] == s[4:]
+    # the shared-window policy keeps up to R + G - 1 fp16 tokens: R + G slots
+    ss = K.kivi_cache_sizes(cfg(K, policy=1))
+    assert ss[:6] == s[:6] and ss[6] == ss[7] == units * (32 + 32) * 128 * 2
 
 
 @pytest.mark.parametrize("bad,status", [
+    (dict(policy=2), 1), (dict(policy=-1), 1),
     (dict(bits=3), 1), (dict(bits=8), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
