@@ -290,19 +290,20 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
   for (int i = tid; i < n * 16; i += blockDim.x) {
     const int r = i >> 4, c = i & 15;
     const long t = c0 + r;
+    const uint8_t* tile = tile_at<BITS>(cv, unit, t / kGroup);
+    const int tr = (int)(t % kGroup);  // row within the tile
     if (r < nk) {
-      if (c < CPR) cp_async16(&ts.krow[r][c], cv.codes_k + (unit * cv.Tcap + t) * RB + 16 * c);
+      if (c < CPR) cp_async16(&ts.krow[r][c], tile + tr * RB + 16 * c);
     } else {
       cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     }
     if (r < nv) {
       if (c < CPR) {
-        cp_async16(&ts.vrow[r][c], cv.codes_v + (unit * cv.Tcap + t) * RB + 16 * c);
+        cp_async16(&ts.vrow[r][c], tile + kOffVc<BITS> + tr * RB + 16 * c);
       } else if (c == CPR) {
-        const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup);
         char* dst = reinterpret_cast<char*>(&ts.vrow[r][c]);
-        cp_async8(dst, cv.scale_v + so);
-        cp_async8(dst + 8, cv.zero_v + so);
+        cp_async8(dst, tile + kOffSv<BITS> + tr * 8);  // the token's D / G = 4 scales
+        cp_async8(dst + 8, tile + kOffZv<BITS> + tr * 8);
       }
     } else {
       cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
@@ -311,8 +312,8 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
   const int ngk = (nk + kGroup - 1) / kGroup;
   for (int i = tid; i < ngk * 32; i += blockDim.x) {
     const int gi = i >> 5, arr = (i >> 4) & 1, c = i & 15;
-    const long go = (unit * (cv.Tcap / kGroup) + c0 / kGroup + gi) * kHeadDim + 8 * c;
-    cp_async16(&ts.kg[gi][arr][4 * c], (arr ? cv.zero_k : cv.scale_k) + go);
+    const uint8_t* tile = tile_at<BITS>(cv, unit, c0 / kGroup + gi);
+    cp_async16(&ts.kg[gi][arr][4 * c], tile + (arr ? kOffZk<BITS> : kOffSk<BITS>) + 16 * c);
   }
   cp_async_commit();
   {
@@ -813,38 +814,31 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, int b, int 
   }
 }
 
-// Copy sources of one (batch, kv-head) unit; tile t of each array starts at
-// base + t * (bytes per tile).
+// The stage buffer mirrors the packed tile byte for byte.
+static_assert(sizeof(TileBuf<2>) == kTileBytes<2> && sizeof(TileBuf<4>) == kTileBytes<4>, "stage = tile");
+static_assert(offsetof(TileBuf<2>, vc) == kOffVc<2> && offsetof(TileBuf<2>, sk) == kOffSk<2> &&
+              offsetof(TileBuf<2>, zk) == kOffZk<2> && offsetof(TileBuf<2>, sv) == kOffSv<2> &&
+              offsetof(TileBuf<2>, zv) == kOffZv<2>, "stage layout (2 bits)");
+static_assert(offsetof(TileBuf<4>, vc) == kOffVc<4> && offsetof(TileBuf<4>, sk) == kOffSk<4> &&
+              offsetof(TileBuf<4>, zk) == kOffZk<4> && offsetof(TileBuf<4>, sv) == kOffSv<4> &&
+              offsetof(TileBuf<4>, zv) == kOffZv<4>, "stage layout (4 bits)");
+
+// Copy source of one (batch, kv-head) unit: its first packed tile.
 struct UnitSrc {
-  const char *kc, *vc, *sk, *zk, *sv, *zv;
+  const uint8_t* tiles;
 };
 
 template <int BITS>
 __device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
-  constexpr long RB = 16 * BITS;  // code bytes per token
-  UnitSrc u;
-  u.kc = reinterpret_cast<const char*>(cv.codes_k + unit * cv.Tcap * RB);
-  u.vc = reinterpret_cast<const char*>(cv.codes_v + unit * cv.Tcap * RB);
-  u.sk = reinterpret_cast<const char*>(cv.scale_k + unit * (cv.Tcap / kGroup) * kHeadDim);
-  u.zk = reinterpret_cast<const char*>(cv.zero_k + unit * (cv.Tcap / kGroup) * kHeadDim);
-  u.sv = reinterpret_cast<const char*>(cv.scale_v + unit * cv.Tcap * (kHeadDim / kGroup));
-  u.zv = reinterpret_cast<const char*>(cv.zero_v + unit * cv.Tcap * (kHeadDim / kGroup));
-  return u;
+  return UnitSrc{tile_at<BITS>(cv, unit, 0)};
 }
 
-// Bulk copies of packed tile `tile` into a stage (one lane).
+// One bulk copy of packed tile `tile` into a stage (one lane).
 template <int BITS>
 __device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long* bar, const UnitSrc& u,
                                            int tile) {
-  constexpr uint32_t kCode = 512u * BITS;  // code bytes per tile
-  const long oc = (long)tile * kCode, o256 = (long)tile * 256;
-  mbar_expect_tx(bar, (uint32_t)sizeof(TileBuf<BITS>));
-  bulk_g2s(tb.kc, u.kc + oc, kCode, bar);
-  bulk_g2s(tb.vc, u.vc + oc, kCode, bar);
-  bulk_g2s(tb.sk, u.sk + o256, 256u, bar);
-  bulk_g2s(tb.zk, u.zk + o256, 256u, bar);
-  bulk_g2s(tb.sv, u.sv + o256, 256u, bar);
-  bulk_g2s(tb.zv, u.zv + o256, 256u, bar);
+  mbar_expect_tx(bar, (uint32_t)kTileBytes<BITS>);
+  bulk_g2s(&tb, u.tiles + (long)tile * kTileBytes<BITS>, (uint32_t)kTileBytes<BITS>, bar);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {

@@ -64,12 +64,7 @@ int ring_slots(const kivi_config& c) {
 
 kivi::CacheView view(const kivi_cache* c) {
   kivi::CacheView v;
-  v.codes_k = static_cast<uint8_t*>(c->buf.codes_k);
-  v.scale_k = static_cast<__half*>(c->buf.scale_k);
-  v.zero_k = static_cast<__half*>(c->buf.zero_k);
-  v.codes_v = static_cast<uint8_t*>(c->buf.codes_v);
-  v.scale_v = static_cast<__half*>(c->buf.scale_v);
-  v.zero_v = static_cast<__half*>(c->buf.zero_v);
+  v.tiles = static_cast<uint8_t*>(c->buf.tiles);
   v.ring_k = static_cast<__half*>(c->buf.ring_k);
   v.ring_v = static_cast<__half*>(c->buf.ring_v);
   v.B = c->cfg.batch;
@@ -194,21 +189,18 @@ WsLayout ws_layout(const kivi_config& c) {
 
 }  // namespace
 
-KIVI_API kivi_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes[8]) {
+KIVI_API kivi_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes[3]) {
   kivi_status st = check_config(cfg);
   if (st != KIVI_OK) return st;
   if (!bytes) return KIVI_EINVAL;
   const size_t units = (size_t)cfg->batch * cfg->n_kv_heads;
-  const size_t T = cfg->max_tokens, D = cfg->head_dim, G = cfg->group, R = cfg->residual;
-  const size_t codes = units * T * (D * cfg->bits / 8);
-  bytes[0] = codes;                      // codes_k
-  bytes[1] = units * (T / G) * D * 2;    // scale_k
-  bytes[2] = bytes[1];                   // zero_k
-  bytes[3] = codes;                      // codes_v
-  bytes[4] = units * T * (D / G) * 2;    // scale_v
-  bytes[5] = bytes[4];                   // zero_v
-  bytes[6] = units * ring_slots(*cfg) * D * 2;  // ring_k
-  bytes[7] = bytes[6];                   // ring_v
+  const size_t T = cfg->max_tokens, D = cfg->head_dim, G = cfg->group;
+  // a tile: key and value code rows of G tokens, key scale / zero [D], value
+  // scale / zero [G][D / G] (f16)
+  const size_t tile = 2 * G * (D * cfg->bits / 8) + 4 * D * 2;
+  bytes[0] = units * (T / G) * tile;            // tiles
+  bytes[1] = units * ring_slots(*cfg) * D * 2;  // ring_k
+  bytes[2] = bytes[1];                          // ring_v
   return KIVI_OK;
 }
 
@@ -219,8 +211,7 @@ KIVI_API kivi_status kivi_cache_init(const kivi_config* cfg, const kivi_buffers*
   kivi_status st = check_config(cfg);
   if (st != KIVI_OK) return st;
   if (!bufs) return KIVI_EINVAL;
-  const void* ptrs[8] = {bufs->codes_k, bufs->scale_k, bufs->zero_k, bufs->codes_v,
-                         bufs->scale_v, bufs->zero_v, bufs->ring_k, bufs->ring_v};
+  const void* ptrs[3] = {bufs->tiles, bufs->ring_k, bufs->ring_v};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return KIVI_EINVAL;
   kivi_cache* c = static_cast<kivi_cache*>(calloc(1, sizeof(kivi_cache)));

@@ -16,19 +16,45 @@ constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two leve
 constexpr int kTailTok = 64;       // tail tokens per tail split
 constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
 
-// Device view of one cache: the eight buffers plus its shape.
+// Device view of one cache: the packed tile store, the two rings and the shape.
 struct CacheView {
-  uint8_t* codes_k;
-  __half* scale_k;
-  __half* zero_k;
-  uint8_t* codes_v;
-  __half* scale_v;
-  __half* zero_v;
+  uint8_t* tiles;  // [B][H][Tcap / kGroup] tiles of kTileBytes<bits>
   __half* ring_k;
   __half* ring_v;
   int B, H, R, Tcap, bits;
   int W;  // ring slots: token t of a unit is in slot t mod W
 };
+
+// A packed tile holds everything quantized about tokens [32j, 32j + 32) of a
+// unit, so that one bulk copy stages it:
+//   [0, 32 RB)                key code rows (RB = D * bits / 8 bytes each)
+//   [32 RB, 64 RB)            value code rows (group-interleaved)
+//   kOffSk: scale[D] (f16)    of the tile's key group, one per channel
+//   kOffZk: zero[D]
+//   kOffSv: scale[32][D / G]  value groups, per token
+//   kOffZv: zero[32][D / G]
+template <int BITS>
+constexpr int kRowBytes = kHeadDim * BITS / 8;
+template <int BITS>
+constexpr int kOffVc = kGroup * kRowBytes<BITS>;
+template <int BITS>
+constexpr int kOffSk = 2 * kGroup * kRowBytes<BITS>;
+template <int BITS>
+constexpr int kOffZk = kOffSk<BITS> + 2 * kHeadDim;
+template <int BITS>
+constexpr int kOffSv = kOffSk<BITS> + 4 * kHeadDim;
+template <int BITS>
+constexpr int kOffZv = kOffSk<BITS> + 6 * kHeadDim;
+template <int BITS>
+constexpr int kTileBytes = kOffSk<BITS> + 8 * kHeadDim;
+static_assert(kTileBytes<2> == 3072 && kTileBytes<4> == 5120, "tile sizes");
+static_assert(kGroup * (kHeadDim / kGroup) * 2 == 2 * kHeadDim, "value scale block size");
+
+// Tile `tile` (tokens [32 tile, 32 tile + 32)) of unit `unit`.
+template <int BITS>
+__host__ __device__ __forceinline__ uint8_t* tile_at(const CacheView& cv, long unit, long tile) {
+  return cv.tiles + (unit * (cv.Tcap / kGroup) + tile) * (long)kTileBytes<BITS>;
+}
 
 // Input dtype codes (same values as kivi_dtype).
 enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };

@@ -283,16 +283,16 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         }
       }
       __syncwarp();
-      uint4* gdst = reinterpret_cast<uint4*>(cv.codes_k + (unit * cv.Tcap + t0) * RB);
+      uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
+      uint4* gdst = reinterpret_cast<uint4*>(tile);
       const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
 #pragma unroll
       for (int i = lane; i < 32 * RB / 16; i += 32) gdst[i] = ssrc[i];
       if (par == 0) {
-        const long so = (unit * (cv.Tcap / kGroup) + chunk) * kHeadDim + c8;
-        *reinterpret_cast<uint4*>(cv.scale_k + so) =
+        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + kOffSk<BITS>) + c8) =
             make_uint4(pack_halves(gp[0].sh, gp[1].sh), pack_halves(gp[2].sh, gp[3].sh),
                        pack_halves(gp[4].sh, gp[5].sh), pack_halves(gp[6].sh, gp[7].sh));
-        *reinterpret_cast<uint4*>(cv.zero_k + so) =
+        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + kOffZk<BITS>) + c8) =
             make_uint4(pack_halves(gp[0].zh, gp[1].zh), pack_halves(gp[2].zh, gp[3].zh),
                        pack_halves(gp[4].zh, gp[5].zh), pack_halves(gp[6].zh, gp[7].zh));
       }
@@ -355,9 +355,9 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
           exact_value_group<BITS>(xw, p.z, p.s, words);
         }
         store_value_units<BITS>(&s_codes[row * RB], g, words);
-        const long so = (unit * cv.Tcap + t) * (kHeadDim / kGroup) + g;
-        cv.scale_v[so] = p.sh;
-        cv.zero_v[so] = p.zh;
+        uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
+        reinterpret_cast<__half*>(tile + kOffSv<BITS>)[row * (kHeadDim / kGroup) + g] = p.sh;
+        reinterpret_cast<__half*>(tile + kOffZv<BITS>)[row * (kHeadDim / kGroup) + g] = p.zh;
       } else if (t >= vring) {
         __half* dst = cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 32 * g;
 #pragma unroll
@@ -366,7 +366,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
     }
     __syncwarp();
     const int r_lo = min(max(vlo - t0, 0), 32), r_hi = min(max(vhi - t0, 0), 32);
-    uint4* gdst = reinterpret_cast<uint4*>(cv.codes_v + (unit * cv.Tcap + t0) * RB);
+    uint4* gdst = reinterpret_cast<uint4*>(tile_at<BITS>(cv, unit, chunk) + kOffVc<BITS>);
     const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
     for (int i = r_lo * RB / 16 + lane; i < r_hi * RB / 16; i += 32) gdst[i] = ssrc[i];
   }
@@ -501,10 +501,12 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
     for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
     // value rows are group-interleaved: channel d is in unit d / 4
     const int vbyte = v_unit_pos(d / 4) * (BITS / 2) + (d % 4) / PER_BYTE;
-    if (d % PER_BYTE == 0) cv.codes_v[(unit * cv.Tcap + u) * RB + vbyte] = (uint8_t)q;
+    uint8_t* tile = tile_at<BITS>(cv, unit, u / kGroup);
+    const int row = (int)(u % kGroup);
+    if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vbyte] = (uint8_t)q;
     if (lane == 0) {
-      cv.scale_v[(unit * cv.Tcap + u) * (kHeadDim / kGroup) + warp] = p.sh;
-      cv.zero_v[(unit * cv.Tcap + u) * (kHeadDim / kGroup) + warp] = p.zh;
+      reinterpret_cast<__half*>(tile + kOffSv<BITS>)[row * (kHeadDim / kGroup) + warp] = p.sh;
+      reinterpret_cast<__half*>(tile + kOffZv<BITS>)[row * (kHeadDim / kGroup) + warp] = p.zh;
     }
   }
   // the same thread read the slot above, so program order protects it
@@ -524,17 +526,16 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
         mx = fmaxf(mx, xs[j]);
       }
       const GroupParams p = group_params(mn, mx, L);
-      const long row0 = unit * cv.Tcap + tb + gi * kGroup;
+      uint8_t* tile = tile_at<BITS>(cv, unit, tb / kGroup + gi);
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) {
         uint32_t q = encode(xs[j], p, L) << (BITS * (d % PER_BYTE));
 #pragma unroll
         for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-        if (d % PER_BYTE == 0) cv.codes_k[(row0 + j) * RB + d / PER_BYTE] = (uint8_t)q;
+        if (d % PER_BYTE == 0) tile[j * RB + d / PER_BYTE] = (uint8_t)q;
       }
-      const long so = (unit * (cv.Tcap / kGroup) + tb / kGroup + gi) * kHeadDim + d;
-      cv.scale_k[so] = p.sh;
-      cv.zero_k[so] = p.zh;
+      reinterpret_cast<__half*>(tile + kOffSk<BITS>)[d] = p.sh;
+      reinterpret_cast<__half*>(tile + kOffZk<BITS>)[d] = p.zh;
     }
   }
 }

@@ -22,8 +22,7 @@ KIVI_OK, KIVI_EINVAL, KIVI_ESHAPE, KIVI_ECAPACITY = 0, 1, 2, 3
 KIVI_EDTYPE, KIVI_ECUDA, KIVI_ESTATE, KIVI_EWORKSPACE = 4, 5, 6, 7
 KIVI_F32, KIVI_F16, KIVI_BF16 = 0, 1, 2
 
-BUFFER_NAMES = ("codes_k", "scale_k", "zero_k", "codes_v", "scale_v", "zero_v",
-                "ring_k", "ring_v")
+BUFFER_NAMES = ("tiles", "ring_k", "ring_v")
 
 _TORCH_DTYPE = {torch.float32: KIVI_F32, torch.float16: KIVI_F16, torch.bfloat16: KIVI_BF16}
 
@@ -113,7 +112,7 @@ def kivi_status_string(status: int) -> str:
 
 
 def kivi_cache_sizes(cfg: kivi_config) -> list[int]:
-    out = (C.c_size_t * 8)()
+    out = (C.c_size_t * len(BUFFER_NAMES))()
     _check(lib().kivi_cache_sizes(C.byref(cfg), out), "kivi_cache_sizes")
     return list(out)
 
@@ -186,7 +185,7 @@ def kivi_cache_destroy(h) -> None:
 # ------------------------------------------------------------ convenience
 
 class KiviCache:
-    """A KIVI cache: C handle + the eight device buffers + attention workspace."""
+    """A KIVI cache: C handle + the three device buffers + attention workspace."""
 
     def __init__(self, *, batch: int, n_kv_heads: int, n_q_heads: int, max_tokens: int,
                  bits: int = 2, group: int = 32, residual: int = 32, head_dim: int = 128,
@@ -280,24 +279,58 @@ class KiviCache:
     def reset(self) -> None:
         kivi_cache_reset(self.handle)
 
-    def state_views(self) -> dict:
-        """The buffers as shaped tensors (fp16 buffers as int16 bit patterns)."""
+    def _ring_slots(self) -> int:
         c = self.cfg
-        B, H, T, D, G, R = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group, c.residual
-        R = R + G if c.policy == KIVI_POLICY_SHARED else R  # ring slots
+        return c.residual + c.group if c.policy == KIVI_POLICY_SHARED else c.residual
+
+    def state_views(self) -> dict:
+        """The cache's state as its three raw buffers (saving and restoring a
+        cache is copying these plus ``length``): the packed tiles as bytes
+        [B][H][T/G][tile bytes], the rings as fp16 bit patterns (int16)."""
+        c = self.cfg
+        B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
+        tb = 2 * G * (D * c.bits // 8) + 8 * D
+        W = self._ring_slots()
+        return {"tiles": self.buffers["tiles"][:B * H * (T // G) * tb].view(B, H, T // G, tb),
+                "ring_k": self.buffers["ring_k"][:2 * B * H * W * D].view(torch.int16).view(B, H, W, D),
+                "ring_v": self.buffers["ring_v"][:2 * B * H * W * D].view(torch.int16).view(B, H, W, D)}
+
+    def layout_views(self) -> dict:
+        """Strided views of the arrays inside the tiles (no copies), with the
+        tile axis kept: codes_k / codes_v [B][H][T/G][G][RB] (u8), scale_k /
+        zero_k [B][H][T/G][D], scale_v / zero_v [B][H][T/G][G][D/G] (fp16
+        bit patterns as int16), plus the rings."""
+        c = self.cfg
+        B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
         rb = D * c.bits // 8
-        shapes = {"codes_k": (B, H, T, rb), "scale_k": (B, H, T // G, D),
-                  "zero_k": (B, H, T // G, D), "codes_v": (B, H, T, rb),
-                  "scale_v": (B, H, T, D // G), "zero_v": (B, H, T, D // G),
-                  "ring_k": (B, H, R, D), "ring_v": (B, H, R, D)}
+        tb = 2 * G * rb + 8 * D
+        nt = T // G
+        u8 = self.buffers["tiles"]
+        i16 = u8[:(u8.numel() // 2) * 2].view(torch.int16)
+        st8 = (H * nt * tb, nt * tb, tb)
+        st16 = tuple(x // 2 for x in st8)
+        o_sk = 2 * G * rb  # byte offset of the key scales in a tile
+        out = {"codes_k": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), 0),
+               "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), G * rb),
+               "scale_k": i16.as_strided((B, H, nt, D), st16 + (1,), o_sk // 2),
+               "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 2 * D) // 2),
+               "scale_v": i16.as_strided((B, H, nt, G, D // G), st16 + (D // G, 1), (o_sk + 4 * D) // 2),
+               "zero_v": i16.as_strided((B, H, nt, G, D // G), st16 + (D // G, 1), (o_sk + 6 * D) // 2)}
+        sv = self.state_views()
+        out["ring_k"], out["ring_v"] = sv["ring_k"], sv["ring_v"]
+        return out
+
+    def logical_state(self) -> dict:
+        """The arrays in token-major shapes (device copies): codes_k / codes_v
+        [B][H][T][RB], scale_k / zero_k [B][H][T/G][D], scale_v / zero_v
+        [B][H][T][D/G], ring_k / ring_v [B][H][W][D]."""
+        c = self.cfg
+        B, H, T = c.batch, c.n_kv_heads, c.max_tokens
+        lv = self.layout_views()
         out = {}
-        for n, shp in shapes.items():
-            buf = self.buffers[n]
-            n_el = 1
-            for s in shp:
-                n_el *= s
-            if n.startswith("codes"):
-                out[n] = buf[:n_el].view(*shp)
+        for n, t in lv.items():
+            if n in ("codes_k", "codes_v", "scale_v", "zero_v"):
+                out[n] = t.reshape(B, H, T, t.shape[-1])
             else:
-                out[n] = buf[:2 * n_el].view(torch.int16).view(*shp)
+                out[n] = t.clone()
         return out

@@ -37,16 +37,23 @@
  *     is rounded to fp16 (nearest even) before it is quantized or stored.
  *
  * Storage layout (all buffers 16-byte aligned; B batch, H = n_kv_heads,
- * T = max_tokens, D = head_dim, G = group, R = residual, b = bits):
- *   codes_k [B][H][T][D*b/8] u8   packed key rows, token-major
- *   scale_k [B][H][T/G][D]   f16  one (scale, zero) per channel per G tokens
- *   zero_k  [B][H][T/G][D]   f16
- *   codes_v [B][H][T][D*b/8] u8   packed value rows
- *   scale_v [B][H][T][D/G]   f16  one (scale, zero) per G channels per token
- *   zero_v  [B][H][T][D/G]   f16
+ * T = max_tokens, D = head_dim, G = group, R = residual, b = bits,
+ * RB = D*b/8 bytes per packed row):
+ *   tiles   [B][H][T/G] tiles of 2*G*RB + 8*D bytes: tile j holds all the
+ *           quantized state of tokens [G*j, G*j + G) of a (batch, kv-head):
+ *             [0, G*RB)            key code rows, token-major
+ *             [G*RB, 2*G*RB)       value code rows, token-major
+ *             then f16 arrays:     key scale [D], key zero [D] (the tile's
+ *                                  key group, one per channel),
+ *                                  value scale [G][D/G], value zero [G][D/G]
+ *                                  (one per G channels per token)
  *   ring_k  [B][H][W][D]     f16  residual keys, token t in slot t mod W
  *   ring_v  [B][H][W][D]     f16  residual values, token t in slot t mod W
- * Channel e of a packed row is bits [(e*b)%8, (e*b)%8 + b) of byte (e*b)/8.
+ * Channel e of a key row is bits [(e*b)%8, (e*b)%8 + b) of byte (e*b)/8.
+ * Value rows are group-interleaved in units of 4 channels (b/2 bytes): the
+ * unit of channels G*g + 4*w .. +3 sits at unit position 4*w + g, its
+ * channels in ascending bit order.  A tile is one contiguous block so that
+ * decode attention stages it with a single bulk copy.
  * Residual policy (kivi_config.policy):
  *   KIVI_POLICY_ALG1 (the chooblog review's Algorithm 1): after l tokens the
  *     first nq_k(l) = R*floor(l/R) keys and the first nq_v(l) = max(l-R, 0)
@@ -97,10 +104,9 @@ typedef struct {
   int policy;      /* kivi_policy: KIVI_POLICY_ALG1 (0) or KIVI_POLICY_SHARED */
 } kivi_config;
 
-/* The eight caller-owned device buffers, in the layout above. */
+/* The three caller-owned device buffers, in the layout above. */
 typedef struct {
-  void *codes_k, *scale_k, *zero_k;
-  void *codes_v, *scale_v, *zero_v;
+  void *tiles;
   void *ring_k, *ring_v;
 } kivi_buffers;
 
@@ -108,7 +114,7 @@ typedef struct kivi_cache kivi_cache; /* opaque host handle */
 
 /* Bytes each buffer needs, in kivi_buffers order.  Host only; no GPU.
  * Returns KIVI_EINVAL / KIVI_ESHAPE for a config this build rejects. */
-kivi_status kivi_cache_sizes(const kivi_config *cfg, size_t bytes[8]);
+kivi_status kivi_cache_sizes(const kivi_config *cfg, size_t bytes[3]);
 
 /* Validate cfg, bind the buffers and create an empty handle (length 0).
  * Host only; the buffers' contents are not touched.  The buffers must stay
@@ -151,7 +157,7 @@ kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
 kivi_status kivi_append_tokens(kivi_cache *c, const void *k, const void *v,
                                kivi_dtype dtype, int n_tokens, void *stream);
 
-/* Declare the cache's length after its eight buffers were restored from a
+/* Declare the cache's length after its three buffers were restored from a
  * saved state (the buffers are the caller's tensors, so saving and restoring
  * a cache is copying them plus this length).
  * The length of a state is kivi_cache_length() at save time.  Host only; no

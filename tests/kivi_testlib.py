@@ -50,7 +50,7 @@ def dev(x: np.ndarray, dtype: str) -> torch.Tensor:
 def gpu_state(cache) -> dict:
     torch.cuda.synchronize()
     out = {}
-    for n, t in cache.state_views().items():
+    for n, t in cache.logical_state().items():
         a = t.cpu().numpy()
         out[n] = a.view(np.uint16) if a.dtype == np.int16 else a
     return out

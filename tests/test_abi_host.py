@@ -50,17 +50,19 @@ def cfg(K, **kw):
 
 
 def test_sizes(K):
+    """Tiles of 2 G RB + 8 D bytes (key / value code rows of G tokens, key
+    scale / zero [D], value scale / zero [G][D/G]) per G tokens, and rings."""
     s = K.kivi_cache_sizes(cfg(K))
     units = 2 * 4
-    assert s[0] == s[3] == units * 4096 * 32
-    assert s[1] == s[2] == units * (4096 // 32) * 128 * 2
-    assert s[4] == s[5] == units * 4096 * 4 * 2
-    assert s[6] == s[7] == units * 32 * 128 * 2
+    assert len(s) == 3
+    assert s[0] == units * (4096 // 32) * (2 * 32 * 32 + 8 * 128)
+    assert s[0] == units * 4096 * 32 * 2 + units * (4096 // 32) * 128 * 2 * 2 + units * 4096 * 4 * 2 * 2
+    assert s[1] == s[2] == units * 32 * 128 * 2
     s4 = K.kivi_cache_sizes(cfg(K, bits=4))
-    assert s4[0] == s4[3] == 2 * s[0] and s4[1:3] == s[1:3] and s4[4:] == s[4:]
+    assert s4[0] == units * (4096 // 32) * (2 * 32 * 64 + 8 * 128) and s4[1:] == s[1:]
     # the shared-window policy keeps up to R + G - 1 fp16 tokens: R + G slots
     ss = K.kivi_cache_sizes(cfg(K, policy=1))
-    assert ss[:6] == s[:6] and ss[6] == ss[7] == units * (32 + 32) * 128 * 2
+    assert ss[0] == s[0] and ss[1] == ss[2] == units * (32 + 32) * 128 * 2
 
 
 @pytest.mark.parametrize("bad,status", [
@@ -76,7 +78,7 @@ def test_config_validation(K, bad, status):
 
 
 def _fake_buffers(K, base=1 << 20, misalign=None):
-    ptrs = [base + i * (1 << 16) for i in range(8)]
+    ptrs = [base + i * (1 << 16) for i in range(len(K.BUFFER_NAMES))]
     if misalign is not None:
         ptrs[misalign] += 8
     return K.kivi_buffers(*ptrs)
@@ -85,9 +87,9 @@ def _fake_buffers(K, base=1 << 20, misalign=None):
 def test_init_validation_and_host_state(K):
     c = cfg(K)
     with pytest.raises(K.KiviError) as e:
-        K.kivi_cache_init(c, K.kivi_buffers(*([None] * 8)))
+        K.kivi_cache_init(c, K.kivi_buffers(*([None] * len(K.BUFFER_NAMES))))
     assert e.value.status == K.KIVI_EINVAL
-    for i in range(8):
+    for i in range(len(K.BUFFER_NAMES)):
         with pytest.raises(K.KiviError) as e:
             K.kivi_cache_init(c, _fake_buffers(K, misalign=i))
         assert e.value.status == K.KIVI_EINVAL
