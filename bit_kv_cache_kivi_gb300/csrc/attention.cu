@@ -759,15 +759,22 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
 // q of the CTA's heads: staged once in shared memory, per-head exponents
 // (warp w takes head w), then the tables in fragment order.  Thread (head,
 // tig, word) builds the pair words of both parts.
-template <int BITS>
-__device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, int b, int j0, int nh) {
+static_assert(kWarps == kNH, "warp w loads and scales head w");
+
+// Channels 4 lane .. 4 lane + 3 of the CTA's head `warp` (zeros past the last
+// head).  Issued before the first tile copies, so that the load does not
+// queue behind them.
+__device__ __forceinline__ void load_q4(const AttnArgs& a, int b, int j0, int nh, float (&v)[4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < kNH) {
-    float v[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      v[i] = warp < nh ? load_q(a.q, ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane + i, a.q_dtype)
-                       : 0.0f;
+  for (int i = 0; i < 4; ++i)
+    v[i] = warp < nh ? load_q(a.q, ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane + i, a.q_dtype) : 0.0f;
+}
+
+template <int BITS>
+__device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float (&v)[4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
     *reinterpret_cast<float4*>(&s.qv[warp][4 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
     const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
     if (lane == 0) {
@@ -861,6 +868,8 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
   TileBuf<BITS>* st = ws.st[warp];
   unsigned long long* bars = ws.bar[warp];
+  float qv4[4];
+  load_q4(a, b, j0, nh, qv4);
 
   if (lane == 0) {
 #pragma unroll
@@ -873,7 +882,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   int issued = min(n_mine, kStages);
   if (lane == 0)
     for (int k = 0; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
-  build_q_tables<BITS>(ws, a, b, j0, nh);
+  build_q_tables<BITS>(ws, a, qv4);
   __syncthreads();
   const float ks = ws.qscale[tig];
   float* pb = &ws.pbuf[warp][0][0];
@@ -985,6 +994,17 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
 // (max, sum): warp w takes head w, lane l channels 4l..4l+3; every load is
 // issued before the first is used.  Returns the merged (unnormalized) output
 // quad, max and sum of head `warp`.
+// Count a CTA in (thread 0, after a CTA barrier that follows the CTA's
+// partial writes); returns the count before.  Release: the barrier orders
+// every thread's writes before this atomic, so they are visible to whichever
+// CTA sees the final count.  Acquire: the CTA that sees it reads the others'
+// partials after the next barrier (with L2 loads).
+__device__ __forceinline__ int count_in(int* counter) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void merge_partials(const float* po, const float* pml, int n, int nh, float4& o4,
                                                float& m_out, float& l_out) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1130,16 +1150,14 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
   const int n_grp = (a.splits + kMergeGroup - 1) / kMergeGroup;
   const int grp_i = s / kMergeGroup;
   const int g_lo = grp_i * kMergeGroup, g_n = min(kMergeGroup, a.splits - g_lo);
-  __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) {
     int* counter = a.counters + gid * a.merge_groups + grp_i;
-    s_last = atomicAdd(counter, 1) == g_n - 1;
+    s_last = count_in(counter) == g_n - 1;
     if (s_last) *counter = 0;  // every other CTA of the group has counted in
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   float4 o4;
   float lsum_h, m_h;
   merge_partials(a.ws_o + (gid * a.splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.splits + g_lo) * kNH * 2,
@@ -1154,16 +1172,14 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
         a.ws_ml1[pidx * 2 + 1] = lsum_h;
       }
     }
-    __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
       int* counter = a.counters2 + gid;
-      s_last = atomicAdd(counter, 1) == n_grp - 1;
+      s_last = count_in(counter) == n_grp - 1;
       if (s_last) *counter = 0;
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     merge_partials(a.ws_o1 + gid * a.merge_groups * kNH * kHeadDim, a.ws_ml1 + gid * a.merge_groups * kNH * 2,
                    n_grp, nh, o4, m_h, lsum_h);
   }
