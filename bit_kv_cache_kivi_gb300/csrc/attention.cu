@@ -166,14 +166,15 @@ struct WarpSmem {
 
 // A tail split: up to kTailTok tokens, each staged as a 256-byte key row and
 // a 256-byte value row -- an fp16 residual row (16-byte chunks XOR-swizzled by
-// row), or the packed codes at the row start (value rows then carry scale[4]
-// at byte RB and zero[4] at byte RB + 8).
+// row), or the packed codes at the row start; the scale / zero blocks of the
+// packed tiles involved are staged whole (kg, vg), in the tiles' order.
 static_assert(kNH == 4, "the tail split keeps the heads of a channel / token in one float4");
 struct TailSmem {
   float4 q4[kHeadDim];                    // q * scale * log2(e): the kNH heads of channel d
   uint4 krow[kTailTok][16];
   uint4 vrow[kTailTok][16];
   uint32_t kg[2][2][64];                  // scale / zero of the (at most two) key groups
+  uint32_t vg[2][2][64];                  // value scale / zero blocks of the (at most two) tiles
   float4 p4[kTailTok];                    // per token: scores, then weights, of the kNH heads
   float mh[kNH], lh[kNH];                 // per head: max and sum of the weights
 };
@@ -300,20 +301,21 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
     if (r < nv) {
       if (c < CPR) {
         cp_async16(&ts.vrow[r][c], tile + kOffVc<BITS> + tr * RB + 16 * c);
-      } else if (c == CPR) {
-        char* dst = reinterpret_cast<char*>(&ts.vrow[r][c]);
-        cp_async8(dst, tile + kOffSv<BITS> + tr * 8);  // the token's D / G = 4 scales
-        cp_async8(dst + 8, tile + kOffZv<BITS> + tr * 8);
       }
     } else {
       cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     }
   }
-  const int ngk = (nk + kGroup - 1) / kGroup;
-  for (int i = tid; i < ngk * 32; i += blockDim.x) {
-    const int gi = i >> 5, arr = (i >> 4) & 1, c = i & 15;
+  // key scale / zero blocks of the packed key tiles, value scale / zero
+  // blocks of the packed value tiles (at most two tiles each)
+  const int ngk = (nk + kGroup - 1) / kGroup, ngv = (nv + kGroup - 1) / kGroup;
+  for (int i = tid; i < (ngk + ngv) * 32; i += blockDim.x) {
+    const bool key = i < ngk * 32;
+    const int ii = key ? i : i - ngk * 32;
+    const int gi = ii >> 5, arr = (ii >> 4) & 1, c = ii & 15;
     const uint8_t* tile = tile_at<BITS>(cv, unit, c0 / kGroup + gi);
-    cp_async16(&ts.kg[gi][arr][4 * c], tile + (arr ? kOffZk<BITS> : kOffSk<BITS>) + 16 * c);
+    if (key) cp_async16(&ts.kg[gi][arr][4 * c], tile + (arr ? kOffZk<BITS> : kOffSk<BITS>) + 16 * c);
+    else cp_async16(&ts.vg[gi][arr][4 * c], tile + (arr ? kOffZv<BITS> : kOffSv<BITS>) + 16 * c);
   }
   cp_async_commit();
   {
@@ -334,16 +336,19 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
     if (r < nk) {
       const int gi = r >> 5;
       const uint32_t* cw4 = reinterpret_cast<const uint32_t*>(&ts.krow[r][0]) + qq * BITS;
-      const uint32_t* sk = ts.kg[gi][0] + 16 * qq;  // fp16 pairs of channels 32qq ..
-      const uint32_t* zk = ts.kg[gi][1] + 16 * qq;
+      // channels 32qq .. 32qq + 31 (kscale_pos keeps them in this block)
+      const __half* sk = reinterpret_cast<const __half*>(ts.kg[gi][0]) + 32 * qq;
+      const __half* zk = reinterpret_cast<const __half*>(ts.kg[gi][1]) + 32 * qq;
 #pragma unroll
       for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
         const uint32_t cw = cw4[w];
 #pragma unroll
         for (int e = 0; e < 32 / BITS; e += 2) {
-          const int dq = w * (32 / BITS) + e;  // even channel of a scale / zero pair
-          const float2 sp = __half22float2(*reinterpret_cast<const __half2*>(&sk[dq >> 1]));
-          const float2 zp = __half22float2(*reinterpret_cast<const __half2*>(&zk[dq >> 1]));
+          const int dq = w * (32 / BITS) + e;  // even channel of the quarter
+          const float2 sp = make_float2(__half2float(sk[kscale_pos<BITS>(dq)]),
+                                        __half2float(sk[kscale_pos<BITS>(dq + 1)]));
+          const float2 zp = make_float2(__half2float(zk[kscale_pos<BITS>(dq)]),
+                                        __half2float(zk[kscale_pos<BITS>(dq + 1)]));
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             // the code as an exact float: its bits under the exponent of 2^23
@@ -417,9 +422,11 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
       uint32_t cb;
       if constexpr (BITS == 2) cb = row[vpos];
       else cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
-      const __half* svz = reinterpret_cast<const __half*>(row + RB);
+      const int vs = vscale_pos(r & 31, d >> 5);
+      const float sv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][0])[vs]);
+      const float zv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][1])[vs]);
       const float cf = __uint_as_float(((cb >> vsh) & L) | 0x4B000000u) - 8388608.0f;
-      vx = fmaf(cf, __half2float(svz[d >> 5]), __half2float(svz[4 + (d >> 5)]));
+      vx = fmaf(cf, sv, zv);
     } else {
       const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
       vx = __half2float(row[d & 7]);
@@ -496,34 +503,23 @@ constexpr float kLazyMax = 0.5f;
 // that later tiles rarely raise it again.
 constexpr float kLazySlack = 1.0f;
 
-// The fp16 pair (x[c0], x[c1]) of the channel pair of code position i within
-// the 8 (2 bits: words W[0..3] hold channels 16m..16m+7, V[0..3] 16m+8..+15)
-// or 4 (4 bits: W[0..3] holds channels 8m..8m+7) words of a per-channel fp16
-// vector (key scales or zeros).
+// The channel-pair words of a per-channel fp16 vector stored in pair order
+// (key scales or zeros, see kscale_pos) behind q-table block `blk` of this
+// lane: pair block m = tig + 4 blk, whose word i is the pair of code position
+// i -- 2 bits: channels (16m + i, 16m + 8 + i), i < 8; 4 bits: (8m + i, 8m +
+// 4 + i), i < 4.
 template <int BITS>
-__device__ __forceinline__ uint32_t chan_pair(const uint32_t (&W)[4], const uint32_t (&V)[4], int i) {
-  if constexpr (BITS == 2) return __byte_perm(W[i >> 1], V[i >> 1], (i & 1) ? 0x7632 : 0x5410);
-  else return __byte_perm(W[i >> 1], W[2 + (i >> 1)], (i & 1) ? 0x7632 : 0x5410);
-}
-
-// The per-channel fp16 vector words (key scales or zeros) behind q-table
-// block `blk` of this lane: 2 bits -- block = quarters 2blk, 2blk+1, word m =
-// tig + 4blk of a key row, W = channels 16m..16m+7, V = 16m+8..16m+15;
-// 4 bits -- block = quarter blk, word m = tig + 4blk, W = channels 8m..8m+7.
-template <int BITS>
-__device__ __forceinline__ void chan_words(const uint32_t* vec, int tig, int blk, uint32_t (&W)[4],
-                                           uint32_t (&V)[4]) {
+__device__ __forceinline__ void pair_words(const uint32_t* vec, int tig, int blk, uint32_t (&P)[8]) {
+  const int m = tig + 4 * blk;
   if constexpr (BITS == 2) {
-    const int m = tig + 4 * blk;
     const uint4 wa = *reinterpret_cast<const uint4*>(vec + 8 * m);
     const uint4 wb = *reinterpret_cast<const uint4*>(vec + 8 * m + 4);
-    W[0] = wa.x; W[1] = wa.y; W[2] = wa.z; W[3] = wa.w;
-    V[0] = wb.x; V[1] = wb.y; V[2] = wb.z; V[3] = wb.w;
+    P[0] = wa.x; P[1] = wa.y; P[2] = wa.z; P[3] = wa.w;
+    P[4] = wb.x; P[5] = wb.y; P[6] = wb.z; P[7] = wb.w;
   } else {
-    const int m = tig + 4 * blk;
     const uint4 wa = *reinterpret_cast<const uint4*>(vec + 4 * m);
-    W[0] = wa.x; W[1] = wa.y; W[2] = wa.z; W[3] = wa.w;
-    V[0] = V[1] = V[2] = V[3] = 0u;
+    P[0] = wa.x; P[1] = wa.y; P[2] = wa.z; P[3] = wa.w;
+    P[4] = P[5] = P[6] = P[7] = 0u;
   }
 }
 
@@ -547,8 +543,8 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uin
                                              uint32_t (&bq)[8][2]) {
 #pragma unroll
   for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
-    uint32_t W[4], V[4];
-    chan_words<BITS>(sk, tig, blk, W, V);
+    uint32_t P[8];
+    pair_words<BITS>(sk, tig, blk, P);
 #pragma unroll
     for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
       const int quarter = kQuartersPerBlock<BITS> * blk + qq;
@@ -559,7 +555,7 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uin
       for (int wq = 0; wq < 4; ++wq) {
         const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
         bq[w >> 1][w & 1] =
-            split_mul(X0[wq], X1[wq], X1[wq] ^ 0x80008000u, chan_pair<BITS>(W, V, word_pos<BITS>(w)));
+            split_mul(X0[wq], X1[wq], X1[wq] ^ 0x80008000u, P[word_pos<BITS>(w)]);
       }
     }
   }
@@ -582,8 +578,8 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
   float beta4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
-    uint32_t W[4], V[4];
-    chan_words<BITS>(tb.zk, tig, blk, W, V);
+    uint32_t P[8];
+    pair_words<BITS>(tb.zk, tig, blk, P);
 #pragma unroll
     for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
       const int quarter = kQuartersPerBlock<BITS> * blk + qq;
@@ -592,8 +588,8 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
 #pragma unroll
       for (int kh = 0; kh < 2; ++kh) {  // the quarter's two k-steps
         const int w0 = 4 * quarter + 2 * kh;
-        const uint32_t z0 = chan_pair<BITS>(W, V, word_pos<BITS>(w0));
-        const uint32_t z1 = chan_pair<BITS>(W, V, word_pos<BITS>(w0 + 1));
+        const uint32_t z0 = P[word_pos<BITS>(w0)];
+        const uint32_t z1 = P[word_pos<BITS>(w0 + 1)];
         mma16816(beta4, z0, z0, z1, z1, QB[2 * kh], QB[2 * kh + 1]);
       }
     }
@@ -683,7 +679,6 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
   const int part = g & 1;
   const float* pv = pb + (g >> 1) * 34 + 8 * tig;
-  const int zsel = (g >> 1) & 1;  // zero word of value group g & 3 within a token
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
     // u[aa][gp]: the codes of channels 4g..4g+3 of group gp for tokens (t0,
@@ -700,13 +695,14 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
       pa[aa] = part ? l : h;
       const uint32_t pbh = part ? h : 0u;
       const uint32_t pbn = pbh ^ 0x80008000u;
-      const uint2 S0 = *reinterpret_cast<const uint2*>(tb.sv + 2 * t0);        // token t0, groups 0..3
-      const uint2 S1 = *reinterpret_cast<const uint2*>(tb.sv + 2 * (t0 + 4));
-      Pp[0][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.x, S1.x, 0x5410));
-      Pp[1][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.x, S1.x, 0x7632));
-      Pp[2][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x5410));
-      Pp[3][aa] = split_mul(pa[aa], pbh, pbn, __byte_perm(S0.y, S1.y, 0x7632));
-      az[aa] = __byte_perm(tb.zv[2 * t0 + zsel], tb.zv[2 * (t0 + 4) + zsel], (g & 1) ? 0x7632 : 0x5410);
+      // the scale / zero words of token pair (t0, t0 + 4) (see vscale_pos)
+      const int pw = 4 * (4 * (2 * kk + aa) + tig);
+      const uint4 S = *reinterpret_cast<const uint4*>(tb.sv + pw);  // groups 0..3
+      Pp[0][aa] = split_mul(pa[aa], pbh, pbn, S.x);
+      Pp[1][aa] = split_mul(pa[aa], pbh, pbn, S.y);
+      Pp[2][aa] = split_mul(pa[aa], pbh, pbn, S.z);
+      Pp[3][aa] = split_mul(pa[aa], pbh, pbn, S.w);
+      az[aa] = tb.zv[pw + (g & 3)];
       if constexpr (BITS == 2) {
         // interleaved word g of a row holds, per byte, channels 4g..4g+3 of groups 0..3
         const uint32_t w0 = tb.vc[t0 * RW + g], w1 = tb.vc[(t0 + 4) * RW + g];

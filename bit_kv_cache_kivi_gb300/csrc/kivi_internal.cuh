@@ -50,6 +50,25 @@ constexpr int kTileBytes = kOffSk<BITS> + 8 * kHeadDim;
 static_assert(kTileBytes<2> == 3072 && kTileBytes<4> == 5120, "tile sizes");
 static_assert(kGroup * (kHeadDim / kGroup) * 2 == 2 * kHeadDim, "value scale block size");
 
+// Key scales / zeros of a tile are stored in channel-pair order: 32-bit word
+// i of pair block m holds the fp16 pair (channel P m + i, channel P m + i +
+// P / 2), P = 16 at 2 bits and 8 at 4 bits -- the two values one B-fragment
+// register of the score product takes.  kscale_pos(c) is channel c's fp16
+// slot.
+template <int BITS>
+__host__ __device__ constexpr int kscale_pos(int c) {
+  constexpr int P = BITS == 2 ? 16 : 8;
+  return P * (c / P) + 2 * (c % (P / 2)) + (c % P) / (P / 2);
+}
+
+// Value scales / zeros of a tile are stored by token pair: with t = 8a + 4h +
+// r (r < 4), 32-bit word 4 (4a + r) + gp holds group gp of tokens (8a + r,
+// 8a + r + 4), the pair that one B-fragment register of the value product
+// takes.  vscale_pos(t, gp) is the fp16 slot of token t, group gp.
+__host__ __device__ constexpr int vscale_pos(int t, int gp) {
+  return 32 * (t / 8) + 8 * (t % 4) + 2 * gp + (t / 4) % 2;
+}
+
 // Tile `tile` (tokens [32 tile, 32 tile + 32)) of unit `unit`.
 template <int BITS>
 __host__ __device__ __forceinline__ uint8_t* tile_at(const CacheView& cv, long unit, long tile) {

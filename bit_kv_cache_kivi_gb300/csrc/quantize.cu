@@ -288,13 +288,35 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
       const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
 #pragma unroll
       for (int i = lane; i < 32 * RB / 16; i += 32) gdst[i] = ssrc[i];
-      if (par == 0) {
-        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + kOffSk<BITS>) + c8) =
-            make_uint4(pack_halves(gp[0].sh, gp[1].sh), pack_halves(gp[2].sh, gp[3].sh),
-                       pack_halves(gp[4].sh, gp[5].sh), pack_halves(gp[6].sh, gp[7].sh));
-        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + kOffZk<BITS>) + c8) =
-            make_uint4(pack_halves(gp[0].zh, gp[1].zh), pack_halves(gp[2].zh, gp[3].zh),
-                       pack_halves(gp[4].zh, gp[5].zh), pack_halves(gp[6].zh, gp[7].zh));
+      {
+        // scales (lanes of parity 0) and zeros (parity 1), in the tile's
+        // channel-pair order (kscale_pos); the 16-byte store lands at c8 either way
+        __half v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = par == 0 ? gp[e].sh : gp[e].zh;
+        uint32_t w[4];
+        if constexpr (BITS == 2) {
+          // pair block m = this lane's 8 channels and its neighbour's (cl ^ 1):
+          // word i = (channel 16m + i, 16m + 8 + i); the lower lane writes
+          // words 0..3, the upper one words 4..7, each sending the other the
+          // four values it lacks
+          const int hi = cl & 1;
+          const uint32_t s0 = hi ? pack_halves(v[0], v[1]) : pack_halves(v[4], v[5]);
+          const uint32_t s1 = hi ? pack_halves(v[2], v[3]) : pack_halves(v[6], v[7]);
+          const uint32_t r0 = __shfl_xor_sync(kFull, s0, 1), r1 = __shfl_xor_sync(kFull, s1, 1);
+          const __half o[4] = {__ushort_as_half((unsigned short)(r0 & 0xffffu)),
+                               __ushort_as_half((unsigned short)(r0 >> 16)),
+                               __ushort_as_half((unsigned short)(r1 & 0xffffu)),
+                               __ushort_as_half((unsigned short)(r1 >> 16))};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = hi ? pack_halves(o[i], v[4 + i]) : pack_halves(v[i], o[i]);
+        } else {
+          // pair block m = this lane's 8 channels: word i = (8m + i, 8m + 4 + i)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) w[i] = pack_halves(v[i], v[4 + i]);
+        }
+        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + (par ? kOffZk<BITS> : kOffSk<BITS>)) + c8) =
+            make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
       // keys of a chunk that is not a whole quantized group stay fp16
@@ -356,8 +378,8 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         }
         store_value_units<BITS>(&s_codes[row * RB], g, words);
         uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
-        reinterpret_cast<__half*>(tile + kOffSv<BITS>)[row * (kHeadDim / kGroup) + g] = p.sh;
-        reinterpret_cast<__half*>(tile + kOffZv<BITS>)[row * (kHeadDim / kGroup) + g] = p.zh;
+        reinterpret_cast<__half*>(tile + kOffSv<BITS>)[vscale_pos(row, g)] = p.sh;
+        reinterpret_cast<__half*>(tile + kOffZv<BITS>)[vscale_pos(row, g)] = p.zh;
       } else if (t >= vring) {
         __half* dst = cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 32 * g;
 #pragma unroll
@@ -505,8 +527,8 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
     const int row = (int)(u % kGroup);
     if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vbyte] = (uint8_t)q;
     if (lane == 0) {
-      reinterpret_cast<__half*>(tile + kOffSv<BITS>)[row * (kHeadDim / kGroup) + warp] = p.sh;
-      reinterpret_cast<__half*>(tile + kOffZv<BITS>)[row * (kHeadDim / kGroup) + warp] = p.zh;
+      reinterpret_cast<__half*>(tile + kOffSv<BITS>)[vscale_pos(row, warp)] = p.sh;
+      reinterpret_cast<__half*>(tile + kOffZv<BITS>)[vscale_pos(row, warp)] = p.zh;
     }
   }
   // the same thread read the slot above, so program order protects it
@@ -534,8 +556,8 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
         for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
         if (d % PER_BYTE == 0) tile[j * RB + d / PER_BYTE] = (uint8_t)q;
       }
-      reinterpret_cast<__half*>(tile + kOffSk<BITS>)[d] = p.sh;
-      reinterpret_cast<__half*>(tile + kOffZk<BITS>)[d] = p.zh;
+      reinterpret_cast<__half*>(tile + kOffSk<BITS>)[kscale_pos<BITS>(d)] = p.sh;
+      reinterpret_cast<__half*>(tile + kOffZk<BITS>)[kscale_pos<BITS>(d)] = p.zh;
     }
   }
 }

@@ -298,8 +298,9 @@ class KiviCache:
     def layout_views(self) -> dict:
         """Strided views of the arrays inside the tiles (no copies), with the
         tile axis kept: codes_k / codes_v [B][H][T/G][G][RB] (u8), scale_k /
-        zero_k [B][H][T/G][D], scale_v / zero_v [B][H][T/G][G][D/G] (fp16
-        bit patterns as int16), plus the rings."""
+        zero_k [B][H][T/G][D] in channel-pair order (see ``key_scale_pos``),
+        scale_v / zero_v [B][H][T/G][G * D/G] in token-pair order (see
+        ``value_scale_pos``), fp16 bit patterns as int16; plus the rings."""
         c = self.cfg
         B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
         rb = D * c.bits // 8
@@ -314,23 +315,46 @@ class KiviCache:
                "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), G * rb),
                "scale_k": i16.as_strided((B, H, nt, D), st16 + (1,), o_sk // 2),
                "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 2 * D) // 2),
-               "scale_v": i16.as_strided((B, H, nt, G, D // G), st16 + (D // G, 1), (o_sk + 4 * D) // 2),
-               "zero_v": i16.as_strided((B, H, nt, G, D // G), st16 + (D // G, 1), (o_sk + 6 * D) // 2)}
+               "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 4 * D) // 2),
+               "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 6 * D) // 2)}
         sv = self.state_views()
         out["ring_k"], out["ring_v"] = sv["ring_k"], sv["ring_v"]
         return out
 
     def logical_state(self) -> dict:
-        """The arrays in token-major shapes (device copies): codes_k / codes_v
-        [B][H][T][RB], scale_k / zero_k [B][H][T/G][D], scale_v / zero_v
-        [B][H][T][D/G], ring_k / ring_v [B][H][W][D]."""
+        """The arrays in token-major shapes and channel order (device
+        copies): codes_k / codes_v [B][H][T][RB], scale_k / zero_k
+        [B][H][T/G][D], scale_v / zero_v [B][H][T][D/G], ring_k / ring_v
+        [B][H][W][D]."""
         c = self.cfg
-        B, H, T = c.batch, c.n_kv_heads, c.max_tokens
+        B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
         lv = self.layout_views()
+        dev = self.buffers["tiles"].device
+        kidx = torch.tensor([key_scale_pos(ch, c.bits) for ch in range(D)], device=dev)
+        vidx = torch.tensor([value_scale_pos(t, gp) for t in range(G) for gp in range(D // G)], device=dev)
         out = {}
         for n, t in lv.items():
-            if n in ("codes_k", "codes_v", "scale_v", "zero_v"):
+            if n in ("codes_k", "codes_v"):
                 out[n] = t.reshape(B, H, T, t.shape[-1])
+            elif n in ("scale_k", "zero_k"):
+                out[n] = t.index_select(3, kidx)
+            elif n in ("scale_v", "zero_v"):
+                out[n] = t.index_select(3, vidx).reshape(B, H, T, D // G)
             else:
                 out[n] = t.clone()
         return out
+
+
+def key_scale_pos(c: int, bits: int) -> int:
+    """fp16 slot of channel c in a tile's key scale / zero block: 32-bit word
+    i of pair block m holds channels (P m + i, P m + i + P/2), P = 16 at 2 bits
+    and 8 at 4 bits (the pairs the score product's B fragments take)."""
+    P = 16 if bits == 2 else 8
+    return P * (c // P) + 2 * (c % (P // 2)) + (c % P) // (P // 2)
+
+
+def value_scale_pos(t: int, gp: int) -> int:
+    """fp16 slot of token t (within its tile), value group gp in a tile's
+    value scale / zero block: tokens (8a + r, 8a + r + 4), r < 4, share the
+    32-bit word 4 (4a + r) + gp."""
+    return 32 * (t // 8) + 8 * (t % 4) + 2 * gp + (t // 4) % 2

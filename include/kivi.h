@@ -47,6 +47,14 @@
  *                                  key group, one per channel),
  *                                  value scale [G][D/G], value zero [G][D/G]
  *                                  (one per G channels per token)
+ *           The f16 arrays are stored in the order the decode-attention
+ *           tensor-core fragments take them (G = 32, D = 128):
+ *             key scale / zero: 32-bit word i of pair block m holds channels
+ *               (P*m + i, P*m + i + P/2), P = 16 at 2 bits, 8 at 4 bits, i.e.
+ *               channel c is at f16 slot P*(c/P) + 2*(c%(P/2)) + (c%P)/(P/2);
+ *             value scale / zero: tokens (8a + r, 8a + r + 4), r < 4, share
+ *               32-bit word 4*(4a + r) + g for group g, i.e. token t, group g
+ *               is at f16 slot 32*(t/8) + 8*(t%4) + 2*g + (t/4)%2.
  *   ring_k  [B][H][W][D]     f16  residual keys, token t in slot t mod W
  *   ring_v  [B][H][W][D]     f16  residual values, token t in slot t mod W
  * Channel e of a key row is bits [(e*b)%8, (e*b)%8 + b) of byte (e*b)/8.

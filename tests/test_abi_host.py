@@ -65,6 +65,21 @@ def test_sizes(K):
     assert ss[0] == s[0] and ss[1] == ss[2] == units * (32 + 32) * 128 * 2
 
 
+def test_scale_slot_maps_are_permutations(K):
+    """The tile's fp16 scale / zero orders are bijections of the 128 slots,
+    and keep each 32-channel quarter in place (the tail split relies on it)."""
+    for bits in (2, 4):
+        pos = [K.key_scale_pos(c, bits) for c in range(128)]
+        assert sorted(pos) == list(range(128))
+        assert all(p // 32 == c // 32 for c, p in enumerate(pos))
+        # word i of a pair block: channels (P m + i, P m + i + P/2)
+        P = 16 if bits == 2 else 8
+        assert pos[P + 1] == P + 2 and pos[P + 1 + P // 2] == P + 3
+    vpos = [K.value_scale_pos(t, g) for t in range(32) for g in range(4)]
+    assert sorted(vpos) == list(range(128))
+    assert K.value_scale_pos(9, 2) + 1 == K.value_scale_pos(13, 2)  # pair (9, 13) in one word
+
+
 @pytest.mark.parametrize("bad,status", [
     (dict(policy=2), 1), (dict(policy=-1), 1),
     (dict(bits=3), 1), (dict(bits=8), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
