@@ -876,10 +876,14 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   const UnitSrc us = unit_src<BITS>(cv, unit);
   const int t_first = tile0 + warp;  // this warp's tiles: t_first + kWarps * k
   int issued = min(n_mine, kStages);
-  if (lane == 0)
-    for (int k = 0; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
+  // the first tile before the q tables, the other stages after them: at
+  // launch every warp of the GPU issues at once, and the first tile (and the
+  // tables) should not queue behind the later stages
+  if (lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
   build_q_tables<BITS>(ws, a, qv4);
   __syncthreads();
+  if (lane == 0)
+    for (int k = 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
   const float ks = ws.qscale[tig];
   float* pb = &ws.pbuf[warp][0][0];
 
