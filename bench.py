@@ -95,12 +95,14 @@ def kernel_traffic():
     """Per-launch DRAM bytes of the attention kernel from a committed ncu
     capture, valid only while the kernel source is unchanged."""
     p = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    src = os.path.join(ROOT, "bit_kv_cache_kivi_gb300", "csrc", "attention.cu")
+    csrc = os.path.join(ROOT, "bit_kv_cache_kivi_gb300", "csrc")
     try:
         with open(p) as f:
             rec = json.load(f)
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        return rec["bytes_per_launch"] if rec.get("source_sha256") == h else None
+        h = hashlib.sha256()
+        for name in ("attention.cu", "kivi_internal.cuh"):  # the kernel and the tile layout
+            h.update(open(os.path.join(csrc, name), "rb").read())
+        return rec["bytes_per_launch"] if rec.get("source_sha256") == h.hexdigest() else None
     except Exception:
         return None
 
