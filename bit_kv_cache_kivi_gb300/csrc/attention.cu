@@ -275,16 +275,17 @@ __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
 // notebook's fl(fl(c * s) + z) because c * s is exact in fp32.  Leaves the
 // partial of the CTA in warp 0's slots (the other warps' slots empty).
 template <int BITS>
-__device__ void tail_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
+__device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS>& sm,
+                           long unit, int b,
                            int j0, int nh, int c0, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;  // packed row bytes
   constexpr int CPR = RB / 16;             // 16-byte chunks per packed row
   TailSmem& ts = sm.tail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = min(kTailTok, a.l - c0);
-  const int nk = max(0, min(n, a.nq_k - c0));  // rows [0, nk) hold packed keys
-  const int nv = max(0, min(n, a.nq_v - c0));  // rows [0, nv) hold packed values
+  const int n = min(kTailTok, p.l - c0);
+  const int nk = max(0, min(n, p.nq_k - c0));  // rows [0, nk) hold packed keys
+  const int nv = max(0, min(n, p.nq_v - c0));  // rows [0, nv) hold packed values
 
   // ---- stage the round (c0 is a multiple of 32, so its packed keys span at
   //      most two key groups), and q ----
@@ -1038,7 +1039,8 @@ __device__ __forceinline__ void merge_partials(const float* po, const float* pml
 // one after another and are folded in, and the result is left as warp 0's
 // slot (the other warps' slots empty) for the CTA merge.
 template <int BITS>
-__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
+__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS>& sm,
+                           long unit, int b,
                            int j0, int nh, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
   const int d = threadIdx.x;
   float pm[kNH], pl[kNH], po[kNH];
@@ -1062,8 +1064,8 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
     po[j] = ot;
   }
   __syncthreads();  // the warps' slots are read; the tail may overwrite them
-  for (int c0 = a.t_tail; c0 < a.l; c0 += kTailTok) {
-    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, c0, s_m, s_l);
+  for (int c0 = p.t_tail; c0 < p.l; c0 += kTailTok) {
+    tail_split<BITS>(cv, a, p, sm, unit, b, j0, nh, c0, s_m, s_l);
     __syncthreads();
     const float* mo0 = merge_area(sm, 0, kPathTail);
 #pragma unroll
@@ -1091,7 +1093,7 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, SplitSmem<BIT
 
 // grid (splits, H * head_chunks, B), 128 threads.
 template <int BITS>
-__global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a) {
+__global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
   extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS>)
   SplitSmem<BITS>& sm = *reinterpret_cast<SplitSmem<BITS>*>(smem_raw);
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
@@ -1106,19 +1108,23 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
   const int nh = min(kNH, grp - hc * kNH);
   const long unit = (long)b * cv.H + h;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int path = s < a.tail_splits ? kPathTail : kPathMma;
+  // this sequence's plan; splits past its own count have nothing to do (and
+  // are not counted by its merge)
+  const SeqPlan p = lens.uniform >= 0 ? a.plan : make_plan(lens.l[b], cv.R, cv.policy, a.scfg);
+  if (s >= p.splits) return;
+  const int path = s < p.tail_splits ? kPathTail : kPathMma;
 
   if (path == kPathTail) {
-    tail_split<BITS>(cv, a, sm, unit, b, j0, nh, a.t_tail + s * kTailTok, s_m, s_l);
+    tail_split<BITS>(cv, a, p, sm, unit, b, j0, nh, p.t_tail + s * kTailTok, s_m, s_l);
   } else {
     // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
-    const int sp = s - a.tail_splits;
-    const int tile0 = sp * a.chunk / 32;
-    const int tile1 = min(a.t_tail, (sp + 1) * a.chunk) / 32;
+    const int sp = s - p.tail_splits;
+    const int tile0 = sp * p.chunk / 32;
+    const int tile1 = min(p.t_tail, (sp + 1) * p.chunk) / 32;
     packed_split<BITS>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
-  if (path == kPathMma && a.tail_fused && s == a.splits - 1) fused_tail<BITS>(cv, a, sm, unit, b, j0, nh, s_m, s_l);
+  if (path == kPathMma && p.tail_fused && s == p.splits - 1) fused_tail<BITS>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;
@@ -1147,9 +1153,9 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
 
   // ---- the last CTA of each group of kMergeGroup splits merges the group;
   //      with more than one group, the last group merges the group results ----
-  const int n_grp = (a.splits + kMergeGroup - 1) / kMergeGroup;
+  const int n_grp = (p.splits + kMergeGroup - 1) / kMergeGroup;
   const int grp_i = s / kMergeGroup;
-  const int g_lo = grp_i * kMergeGroup, g_n = min(kMergeGroup, a.splits - g_lo);
+  const int g_lo = grp_i * kMergeGroup, g_n = min(kMergeGroup, p.splits - g_lo);
   __syncthreads();
   if (threadIdx.x == 0) {
     int* counter = a.counters + gid * a.merge_groups + grp_i;
@@ -1199,22 +1205,23 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
 }  // namespace
 
 template <int BITS>
-cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
+                        cudaStream_t st) {
   // The shared-memory opt-in is a per-device function attribute; setting it
   // on every call costs a host call only.
   const cudaError_t e = cudaFuncSetAttribute(attn_kernel<BITS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(SplitSmem<BITS>));
   if (e != cudaSuccess) return e;
-  attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a);
+  attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a, lens);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, cudaStream_t st) {
+cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens, cudaStream_t st) {
   const int grp = a.Hq / cv.H;
   const int nhc = (grp + kNH - 1) / kNH;
   const dim3 grid(a.splits, cv.H * nhc, cv.B);
-  return cv.bits == 2 ? launch_bits<2>(grid, cv, a, st) : launch_bits<4>(grid, cv, a, st);
+  return cv.bits == 2 ? launch_bits<2>(grid, cv, a, lens, st) : launch_bits<4>(grid, cv, a, lens, st);
 }
 
 }  // namespace kivi

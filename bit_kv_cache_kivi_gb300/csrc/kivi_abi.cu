@@ -15,7 +15,9 @@
 struct kivi_cache {
   kivi_config cfg;
   kivi_buffers buf;
-  int length;
+  int length;               // every sequence's length while `uniform`
+  int uniform;              // 1: all sequences share `length`; 0: see lens
+  int* lens;                // [batch] per-sequence lengths while !uniform
   int splits_override;      // 0 = automatic
   const void* ws_ready;     // workspace whose counter area is known to be zero
 };
@@ -45,16 +47,41 @@ kivi_status check_config(const kivi_config* c) {
   return KIVI_OK;
 }
 
-// Quantized counts after l tokens.  ALG1 (chooblog KIVI review §3.2.2,
-// Algorithm 1): keys X_K[:l - l mod R], values X_V[:l - R].  SHARED
-// (veloxquant-mlx "KIVI" How it works, items 3-4): both G*floor((l - R)/G).
-int nq_k(int l, const kivi_config& c) {
-  if (c.policy == KIVI_POLICY_SHARED) return l > c.residual ? (l - c.residual) / c.group * c.group : 0;
-  return l - l % c.residual;
+// Sequence b's length.
+int len_of(const kivi_cache* c, int b) { return c->uniform ? c->length : c->lens[b]; }
+
+// The longest sequence.
+int max_len(const kivi_cache* c) {
+  if (c->uniform) return c->length;
+  int m = 0;
+  for (int b = 0; b < c->cfg.batch; ++b) m = c->lens[b] > m ? c->lens[b] : m;
+  return m;
 }
-int nq_v(int l, const kivi_config& c) {
-  if (c.policy == KIVI_POLICY_SHARED) return nq_k(l, c);
-  return l > c.residual ? l - c.residual : 0;
+
+// The lengths as a launch parameter.
+void seq_lens(const kivi_cache* c, kivi::SeqLens* out) {
+  out->uniform = c->uniform ? c->length : -1;
+  if (!c->uniform)
+    for (int b = 0; b < c->cfg.batch; ++b) out->l[b] = c->lens[b];
+}
+
+// Every sequence grows by n (host state after a successful launch).
+void grow(kivi_cache* c, int n) {
+  if (c->uniform) {
+    c->length += n;
+  } else {
+    for (int b = 0; b < c->cfg.batch; ++b) c->lens[b] += n;
+  }
+}
+
+// Set the lengths from a host array (uniform when they are all equal).
+void set_lens(kivi_cache* c, const int* l) {
+  bool same = true;
+  for (int b = 1; b < c->cfg.batch; ++b) same = same && l[b] == l[0];
+  c->uniform = same ? 1 : 0;
+  c->length = same ? l[0] : -1;
+  if (!same)
+    for (int b = 0; b < c->cfg.batch; ++b) c->lens[b] = l[b];
 }
 
 // Ring slots: R under ALG1, R + G under SHARED (up to R + G - 1 fp16 tokens).
@@ -73,6 +100,7 @@ kivi::CacheView view(const kivi_cache* c) {
   v.W = ring_slots(c->cfg);
   v.Tcap = c->cfg.max_tokens;
   v.bits = c->cfg.bits;
+  v.policy = c->cfg.policy;
   return v;
 }
 
@@ -113,48 +141,17 @@ int max_splits(const kivi_config& c) {
   return a > b ? a : b;
 }
 
-// Splits used at length l: tail splits of kTailTok tokens from t_tail, then
-// packed splits of `chunk` (32-aligned) tokens.  Automatic packed splits fill
-// the budget beside this length's tail splits, with at least 256 tokens and a
-// multiple of four tiles each, so that the four warps of a CTA get equal
-// shares; an override n asks for n splits in all.  When the budget cannot
-// hold a tail split beside one packed split, the tail rides on the last
-// packed split (*tail_fused, no tail splits).
-void split_plan(const kivi_cache* c, int l, int* tail_splits, int* splits, int* chunk, int* t_tail,
-                int* tail_fused) {
-  const int tt = (nq_v(l, c->cfg) / 32) * 32;
-  *t_tail = tt;
-  *tail_splits = (l - tt + kivi::kTailTok - 1) / kivi::kTailTok;
-  *tail_fused = 0;
-  const int tiles = tt / 32;
-  if (tiles == 0) {
-    *splits = *tail_splits;
-    *chunk = 32;
-    return;
-  }
-  const int budget = split_budget(c->cfg);
-  if (c->splits_override <= 0 && budget < *tail_splits + 1) {
-    *tail_fused = 1;
-    *tail_splits = 0;
-  }
-  int smax = budget - *tail_splits;
-  if (smax > max_splits(c->cfg) - *tail_splits) smax = max_splits(c->cfg) - *tail_splits;
-  if (smax < 1) smax = 1;
-  int per;  // tiles per packed split
-  if (c->splits_override > 0) {
-    int s = c->splits_override - *tail_splits;
-    if (s > smax) s = smax;
-    if (s > tiles) s = tiles;
-    if (s < 1) s = 1;
-    per = (tiles + s - 1) / s;
-  } else {
-    per = (tiles + smax - 1) / smax;
-    per = (per + 3) / 4 * 4;
-    if (per < 8) per = 8;
-  }
-  const int ch = per * 32;
-  *chunk = ch;
-  *splits = *tail_splits + (tt + ch - 1) / ch;  // no empty split
+// The cache's split configuration (kivi::make_plan plans one length with it).
+kivi::SplitCfg split_cfg(const kivi_cache* c) {
+  kivi::SplitCfg sc;
+  sc.budget = split_budget(c->cfg);
+  sc.max_splits = max_splits(c->cfg);
+  sc.override_splits = c->splits_override;
+  return sc;
+}
+
+kivi::SeqPlan plan_of(const kivi_cache* c, int l) {
+  return kivi::make_plan(l, c->cfg.residual, c->cfg.policy, split_cfg(c));
 }
 
 // Workspace layout (attention group gid = (b, kv-head, head chunk), S = max
@@ -216,70 +213,129 @@ KIVI_API kivi_status kivi_cache_init(const kivi_config* cfg, const kivi_buffers*
     if (!p || !aligned16(p)) return KIVI_EINVAL;
   kivi_cache* c = static_cast<kivi_cache*>(calloc(1, sizeof(kivi_cache)));
   if (!c) return KIVI_EINVAL;
+  c->lens = static_cast<int*>(calloc((size_t)cfg->batch, sizeof(int)));
+  if (!c->lens) {
+    free(c);
+    return KIVI_EINVAL;
+  }
   c->cfg = *cfg;
   c->buf = *bufs;
+  c->uniform = 1;
   *out = c;
   return KIVI_OK;
 }
 
+namespace {
+
+bool dtype_ok(kivi_dtype d) { return d == KIVI_F32 || d == KIVI_F16 || d == KIVI_BF16; }
+
+// Prefill of an empty cache; lens = nullptr: every sequence takes t_in tokens.
+kivi_status prefill(kivi_cache* c, const void* k, const void* v, kivi_dtype dtype, int t_in, const int* lens,
+                    void* stream) {
+  if (!c) return KIVI_EINVAL;
+  if (!dtype_ok(dtype)) return KIVI_EDTYPE;
+  if (c->uniform ? c->length != 0 : true) return KIVI_ESTATE;
+  if (t_in < 0) return KIVI_ESHAPE;
+  const int B = c->cfg.batch;
+  if (lens) {
+    for (int b = 0; b < B; ++b) {
+      if (lens[b] < 0 || lens[b] > c->cfg.max_tokens) return KIVI_ECAPACITY;
+      if (lens[b] > t_in) return KIVI_ESHAPE;
+    }
+    bool same = true;
+    for (int b = 1; b < B; ++b) same = same && lens[b] == lens[0];
+    if (!same && B > kivi::kMaxVarBatch) return KIVI_ESHAPE;
+  } else if (t_in > c->cfg.max_tokens) {
+    return KIVI_ECAPACITY;
+  }
+  if (t_in == 0) return KIVI_OK;
+  if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
+  kivi_cache tmp = *c;  // the lengths the launch will produce
+  if (lens) set_lens(&tmp, lens);
+  else tmp.length = t_in;
+  kivi::SeqLens sl;
+  seq_lens(&tmp, &sl);
+  kivi_status st = cuda_status(kivi::launch_quantize_prefill(view(c), k, v, (int)dtype, t_in, sl,
+                                                             static_cast<cudaStream_t>(stream)));
+  if (st != KIVI_OK) return st;
+  if (lens) set_lens(c, lens);
+  else c->length = t_in;
+  return KIVI_OK;
+}
+
+}  // namespace
+
 KIVI_API kivi_status kivi_quantize_prefill(kivi_cache* c, const void* k, const void* v,
                                            kivi_dtype dtype, int n_tokens, void* stream) {
-  if (!c) return KIVI_EINVAL;
-  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
-  if (c->length != 0) return KIVI_ESTATE;
-  if (n_tokens < 0) return KIVI_ESHAPE;
-  if (n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
-  if (n_tokens == 0) return KIVI_OK;
-  if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
-  kivi_status st = cuda_status(kivi::launch_quantize_prefill(
-      view(c), k, v, (int)dtype, n_tokens, nq_k(n_tokens, c->cfg), nq_v(n_tokens, c->cfg),
-      static_cast<cudaStream_t>(stream)));
-  if (st == KIVI_OK) c->length = n_tokens;
-  return st;
+  return prefill(c, k, v, dtype, n_tokens, nullptr, stream);
+}
+
+KIVI_API kivi_status kivi_quantize_prefill_varlen(kivi_cache* c, const void* k, const void* v,
+                                                  kivi_dtype dtype, int max_len, const int* lengths,
+                                                  void* stream) {
+  if (!c || !lengths) return KIVI_EINVAL;
+  return prefill(c, k, v, dtype, max_len, lengths, stream);
 }
 
 KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const void* v_new,
                                         kivi_dtype dtype, void* stream) {
   if (!c) return KIVI_EINVAL;
-  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (!k_new || !v_new) return KIVI_EINVAL;
-  if (c->length >= c->cfg.max_tokens) return KIVI_ECAPACITY;
-  const int l0 = c->length;
-  const kivi_config& f = c->cfg;
+  if (max_len(c) >= c->cfg.max_tokens) return KIVI_ECAPACITY;
+  kivi::SeqLens sl;
+  seq_lens(c, &sl);
   cudaError_t e;
-  if (f.policy == KIVI_POLICY_SHARED) {
+  if (c->cfg.policy == KIVI_POLICY_SHARED) {
     // the one-token case of the multi-token append: a whole group of keys and
     // values is quantized when nq grows, then the token goes to the ring
     if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_EINVAL;
-    e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, l0, 1, nq_k(l0, f), nq_k(l0 + 1, f),
-                                   nq_v(l0, f), nq_v(l0 + 1, f), static_cast<cudaStream_t>(stream));
+    e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, 1, sl, static_cast<cudaStream_t>(stream));
   } else {
-    e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, l0, static_cast<cudaStream_t>(stream));
+    e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, sl, static_cast<cudaStream_t>(stream));
   }
   kivi_status st = cuda_status(e);
-  if (st == KIVI_OK) c->length += 1;
+  if (st == KIVI_OK) grow(c, 1);
   return st;
 }
 
 KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void* v, kivi_dtype dtype,
                                         int n_tokens, void* stream) {
   if (!c) return KIVI_EINVAL;
-  if (dtype != KIVI_F32 && dtype != KIVI_F16 && dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
-  if ((long)c->length + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
-  const int l0 = c->length, L = l0 + n_tokens;
-  const kivi_config& f = c->cfg;
-  kivi_status st = cuda_status(kivi::launch_append_tokens(view(c), k, v, (int)dtype, l0, n_tokens,
-                                                          nq_k(l0, f), nq_k(L, f), nq_v(l0, f), nq_v(L, f),
-                                                          static_cast<cudaStream_t>(stream)));
-  if (st == KIVI_OK) c->length = L;
+  if ((long)max_len(c) + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  kivi::SeqLens sl;
+  seq_lens(c, &sl);
+  kivi_status st = cuda_status(
+      kivi::launch_append_tokens(view(c), k, v, (int)dtype, n_tokens, sl, static_cast<cudaStream_t>(stream)));
+  if (st == KIVI_OK) grow(c, n_tokens);
   return st;
 }
 
 KIVI_API kivi_status kivi_cache_set_length(kivi_cache* c, int length) {
   if (!c) return KIVI_EINVAL;
   if (length < 0 || length > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  c->uniform = 1;
   c->length = length;
+  return KIVI_OK;
+}
+
+KIVI_API kivi_status kivi_cache_set_lengths(kivi_cache* c, const int* lengths) {
+  if (!c || !lengths) return KIVI_EINVAL;
+  bool same = true;
+  for (int b = 0; b < c->cfg.batch; ++b) {
+    if (lengths[b] < 0 || lengths[b] > c->cfg.max_tokens) return KIVI_ECAPACITY;
+    same = same && lengths[b] == lengths[0];
+  }
+  if (!same && c->cfg.batch > kivi::kMaxVarBatch) return KIVI_ESHAPE;
+  set_lens(c, lengths);
+  return KIVI_OK;
+}
+
+KIVI_API kivi_status kivi_cache_lengths(const kivi_cache* c, int* lengths) {
+  if (!c || !lengths) return KIVI_EINVAL;
+  for (int b = 0; b < c->cfg.batch; ++b) lengths[b] = len_of(c, b);
   return KIVI_OK;
 }
 
@@ -296,59 +352,91 @@ KIVI_API kivi_status kivi_set_attention_splits(kivi_cache* c, int n_splits) {
 
 KIVI_API int kivi_attention_splits(const kivi_cache* c, int l) {
   if (!c || l <= 0) return 0;
-  int ts, s, ch, tt, tf;
-  split_plan(c, l, &ts, &s, &ch, &tt, &tf);
-  return s;
+  return plan_of(c, l).splits;
 }
+
+namespace {
+
+// The attention launch arguments that depend on the lengths and the
+// workspace; KIVI_ESTATE when some sequence is empty.
+kivi_status attn_args(const kivi_cache* c, const void* q, kivi_dtype q_dtype, void* out, float softmax_scale,
+                      char* ws, kivi::AttnArgs* a, kivi::SeqLens* sl) {
+  const int B = c->cfg.batch;
+  for (int b = 0; b < (c->uniform ? 1 : B); ++b)
+    if (len_of(c, b) <= 0) return KIVI_ESTATE;
+  a->q = q;
+  a->out = out;
+  a->q_dtype = (int)q_dtype;
+  a->Hq = c->cfg.n_q_heads;
+  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
+  a->scale_log2 = scale * 1.4426950408889634f;
+  a->scfg = split_cfg(c);
+  seq_lens(c, sl);
+  if (c->uniform) {
+    a->plan = plan_of(c, c->length);
+    a->splits = a->plan.splits;
+  } else {
+    a->plan = plan_of(c, c->lens[0]);
+    a->splits = 0;
+    for (int b = 0; b < B; ++b) {
+      const int s = plan_of(c, c->lens[b]).splits;
+      a->splits = s > a->splits ? s : a->splits;
+    }
+  }
+  const WsLayout w = ws_layout(c->cfg);
+  a->ws_o = reinterpret_cast<float*>(ws + w.o_off);
+  a->ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
+  a->ws_o1 = reinterpret_cast<float*>(ws + w.o1_off);
+  a->ws_ml1 = reinterpret_cast<float*>(ws + w.ml1_off);
+  a->merge_groups = w.groups;
+  a->counters = reinterpret_cast<int*>(ws + w.cnt_off);
+  a->counters2 = reinterpret_cast<int*>(ws + w.cnt2_off);
+  a->status = reinterpret_cast<int*>(ws + w.status_off);
+  return KIVI_OK;
+}
+
+}  // namespace
 
 KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dtype q_dtype,
                                            void* out, float softmax_scale, void* workspace,
                                            size_t ws_bytes, void* stream) {
   if (!c) return KIVI_EINVAL;
-  if (q_dtype != KIVI_F32 && q_dtype != KIVI_F16 && q_dtype != KIVI_BF16) return KIVI_EDTYPE;
+  if (!dtype_ok(q_dtype)) return KIVI_EDTYPE;
   if (!q || !out) return KIVI_EINVAL;
-  if (c->length <= 0) return KIVI_ESTATE;
+  if (c->uniform && c->length <= 0) return KIVI_ESTATE;
   if (!workspace || !aligned16(workspace) || ws_bytes < kivi_attention_workspace_bytes(c))
     return KIVI_EWORKSPACE;
   kivi::AttnArgs a;
-  a.q = q;
-  a.out = out;
-  a.q_dtype = (int)q_dtype;
-  a.Hq = c->cfg.n_q_heads;
-  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.l = c->length;
-  a.nq_k = nq_k(c->length, c->cfg);
-  a.nq_v = nq_v(c->length, c->cfg);
-  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
-  const WsLayout w = ws_layout(c->cfg);
-  char* ws = static_cast<char*>(workspace);
-  a.ws_o = reinterpret_cast<float*>(ws + w.o_off);
-  a.ws_ml = reinterpret_cast<float*>(ws + w.ml_off);
-  a.ws_o1 = reinterpret_cast<float*>(ws + w.o1_off);
-  a.ws_ml1 = reinterpret_cast<float*>(ws + w.ml1_off);
-  a.merge_groups = w.groups;
-  a.counters = reinterpret_cast<int*>(ws + w.cnt_off);
-  a.counters2 = reinterpret_cast<int*>(ws + w.cnt2_off);
-  a.status = reinterpret_cast<int*>(ws + w.status_off);
+  kivi::SeqLens sl;
+  kivi_status ast = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(workspace), &a, &sl);
+  if (ast != KIVI_OK) return ast;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->ws_ready != workspace) {
+    const WsLayout w = ws_layout(c->cfg);
     kivi_status z = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, st));
     if (z != KIVI_OK) return z;
     c->ws_ready = workspace;
   }
-  return cuda_status(kivi::launch_attention(view(c), a, st));
+  return cuda_status(kivi::launch_attention(view(c), a, sl, st));
 }
 
-KIVI_API int kivi_cache_length(const kivi_cache* c) { return c ? c->length : -1; }
+KIVI_API int kivi_cache_length(const kivi_cache* c) {
+  if (!c) return -1;
+  return c->uniform ? c->length : -2;
+}
 
 KIVI_API kivi_status kivi_cache_reset(kivi_cache* c) {
   if (!c) return KIVI_EINVAL;
+  c->uniform = 1;
   c->length = 0;
   return KIVI_OK;
 }
 
-KIVI_API void kivi_cache_destroy(kivi_cache* c) { free(c); }
+KIVI_API void kivi_cache_destroy(kivi_cache* c) {
+  if (!c) return;
+  free(c->lens);
+  free(c);
+}
 
 KIVI_API const char* kivi_status_string(kivi_status s) {
   switch (s) {
@@ -413,36 +501,20 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   if (!c) return KIVI_EINVAL;
   if (q_dtype != KIVI_F32 && q_dtype != KIVI_F16 && q_dtype != KIVI_BF16) return KIVI_EDTYPE;
   if (!q || !out) return KIVI_EINVAL;
-  if (c->length <= 0) return KIVI_ESTATE;
+  if (c->uniform && c->length <= 0) return KIVI_ESTATE;
   const WsLayout w = ws_layout(c->cfg);
   if (w.total > (size_t)KIVI_STATIC_WORKSPACE_BYTES) return KIVI_EWORKSPACE;
   void* ws = nullptr;
   kivi_status st = cuda_status(static_ws_address(&ws));
   if (st != KIVI_OK) return st;
   kivi::AttnArgs a;
-  a.q = q;
-  a.out = out;
-  a.q_dtype = (int)q_dtype;
-  a.Hq = c->cfg.n_q_heads;
-  const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)c->cfg.head_dim);
-  a.scale_log2 = scale * 1.4426950408889634f;
-  a.l = c->length;
-  a.nq_k = nq_k(c->length, c->cfg);
-  a.nq_v = nq_v(c->length, c->cfg);
-  split_plan(c, c->length, &a.tail_splits, &a.splits, &a.chunk, &a.t_tail, &a.tail_fused);
-  char* base = static_cast<char*>(ws);
-  a.ws_o = reinterpret_cast<float*>(base + w.o_off);
-  a.ws_ml = reinterpret_cast<float*>(base + w.ml_off);
-  a.ws_o1 = reinterpret_cast<float*>(base + w.o1_off);
-  a.ws_ml1 = reinterpret_cast<float*>(base + w.ml1_off);
-  a.merge_groups = w.groups;
-  a.counters = reinterpret_cast<int*>(base + w.cnt_off);
-  a.counters2 = reinterpret_cast<int*>(base + w.cnt2_off);
-  a.status = reinterpret_cast<int*>(base + w.status_off);
+  kivi::SeqLens sl;
+  st = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(ws), &a, &sl);
+  if (st != KIVI_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left; the split counters must
   // start at zero, so clear them on every call (a memset, not an allocation).
   st = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, s));
   if (st != KIVI_OK) return st;
-  return cuda_status(kivi::launch_attention(view(c), a, s));
+  return cuda_status(kivi::launch_attention(view(c), a, sl, s));
 }

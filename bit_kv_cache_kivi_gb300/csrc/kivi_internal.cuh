@@ -16,14 +16,98 @@ constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two leve
 constexpr int kTailTok = 64;       // tail tokens per tail split
 constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
 
+constexpr int kMaxVarBatch = 1024;  // batch limit for per-sequence lengths
+
 // Device view of one cache: the packed tile store, the two rings and the shape.
 struct CacheView {
   uint8_t* tiles;  // [B][H][Tcap / kGroup] tiles of kTileBytes<bits>
   __half* ring_k;
   __half* ring_v;
   int B, H, R, Tcap, bits;
-  int W;  // ring slots: token t of a unit is in slot t mod W
+  int W;       // ring slots: token t of a unit is in slot t mod W
+  int policy;  // 0: Algorithm 1 of the chooblog KIVI review; 1: shared window
 };
+
+// The lengths of the batch's sequences, passed by value to every launch:
+// one length for all, or one per sequence (batch <= kMaxVarBatch).
+struct SeqLens {
+  int uniform;  // >= 0: every sequence has this length; -1: l[b]
+  int l[kMaxVarBatch];
+};
+
+__host__ __device__ __forceinline__ int seq_len(const SeqLens& s, int b) {
+  return s.uniform >= 0 ? s.uniform : s.l[b];
+}
+
+// Quantized counts after l tokens.  Policy 0 (chooblog KIVI review §3.2.2,
+// Algorithm 1): keys X_K[:l - l mod R], values X_V[:l - R].  Policy 1
+// (veloxquant-mlx "KIVI" How it works, items 3-4): both G*floor((l - R)/G).
+__host__ __device__ __forceinline__ int policy_nq_k(int l, int R, int policy) {
+  if (policy == 1) return l > R ? (l - R) / kGroup * kGroup : 0;
+  return l - l % R;
+}
+__host__ __device__ __forceinline__ int policy_nq_v(int l, int R, int policy) {
+  if (policy == 1) return policy_nq_k(l, R, policy);
+  return l > R ? l - R : 0;
+}
+
+// Split configuration of a cache (a function of its shape): the one-wave
+// budget of splits per attention unit, the workspace's bound on splits, and
+// a caller's override (0 = automatic).
+struct SplitCfg {
+  int budget, max_splits, override_splits;
+};
+
+// How decode attention covers one sequence of length l: tail splits of
+// kTailTok tokens from t_tail = 32 floor(nq_v / 32) (CUDA cores), then packed
+// splits of `chunk` tokens over the tiles below t_tail (tensor cores).
+// Automatic packed splits fill the budget beside the tail splits, with at
+// least 8 tiles and a multiple of four each (the four warps of a CTA get
+// equal shares); an override asks for that many splits in all.  When the
+// budget cannot hold a tail split beside one packed split, the tail rides on
+// the last packed split (tail_fused, no tail splits).
+struct SeqPlan {
+  int l, nq_k, nq_v, t_tail, tail_splits, splits, chunk, tail_fused;
+};
+
+__host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const SplitCfg& sc) {
+  SeqPlan p;
+  p.l = l;
+  p.nq_k = policy_nq_k(l, R, policy);
+  p.nq_v = policy_nq_v(l, R, policy);
+  const int tt = p.nq_v / 32 * 32;
+  p.t_tail = tt;
+  p.tail_splits = (l - tt + kTailTok - 1) / kTailTok;
+  p.tail_fused = 0;
+  const int tiles = tt / 32;
+  if (tiles == 0) {
+    p.splits = p.tail_splits;
+    p.chunk = 32;
+    return p;
+  }
+  if (sc.override_splits <= 0 && sc.budget < p.tail_splits + 1) {
+    p.tail_fused = 1;
+    p.tail_splits = 0;
+  }
+  int smax = sc.budget - p.tail_splits;
+  if (smax > sc.max_splits - p.tail_splits) smax = sc.max_splits - p.tail_splits;
+  if (smax < 1) smax = 1;
+  int per;  // tiles per packed split
+  if (sc.override_splits > 0) {
+    int s = sc.override_splits - p.tail_splits;
+    if (s > smax) s = smax;
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    per = (tiles + s - 1) / s;
+  } else {
+    per = (tiles + smax - 1) / smax;
+    per = (per + 3) / 4 * 4;
+    if (per < 8) per = 8;
+  }
+  p.chunk = per * 32;
+  p.splits = p.tail_splits + (tt + p.chunk - 1) / p.chunk;  // no empty split
+  return p;
+}
 
 // A packed tile holds everything quantized about tokens [32j, 32j + 32) of a
 // unit, so that one bulk copy stages it:
@@ -78,19 +162,22 @@ __host__ __device__ __forceinline__ uint8_t* tile_at(const CacheView& cv, long u
 // Input dtype codes (same values as kivi_dtype).
 enum : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
 
-cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k,
-                                    const void* v, int dtype, int T, int nq_k,
-                                    int nq_v, cudaStream_t st);
+// Prefill of an empty cache: sequence b takes the first lens(b) of the
+// t_in rows of k, v ([B][H][t_in][D] of dtype).
+cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const void* v, int dtype,
+                                    int t_in, const SeqLens& lens, cudaStream_t st);
 
+// One token appended to every sequence (Algorithm 1 policy), at position
+// lens(b) of sequence b.
 cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
-                          int dtype, int t, cudaStream_t st);
+                          int dtype, const SeqLens& lens, cudaStream_t st);
 
-// n tokens appended to a cache of length l0 (k, v: [B][H][n][D] of dtype):
-// key groups [nq_k0, nq_k1) and value tokens [nq_v0, nq_v1) become
-// quantized, then the last min(n, R) tokens go to the ring.
+// n tokens appended to every sequence (k, v: [B][H][n][D] of dtype), to a
+// sequence of length l0 = lens(b): its key groups [nq_k(l0), nq_k(l0 + n))
+// and value tokens [nq_v(l0), nq_v(l0 + n)) become quantized, then its last
+// min(n, W) tokens go to the ring.
 cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype,
-                                 int l0, int n, int nq_k0, int nq_k1, int nq_v0, int nq_v1,
-                                 cudaStream_t st);
+                                 int n, const SeqLens& lens, cudaStream_t st);
 
 struct AttnArgs {
   const void* q;
@@ -98,15 +185,14 @@ struct AttnArgs {
   int q_dtype;
   int Hq;
   float scale_log2;  // softmax scale * log2(e)
-  int l, nq_k, nq_v;
-  // Context split: splits s < tail_splits cover the tail [t_tail, l) (t_tail
-  // = nq_v rounded down to 32), kTailTok tokens each from t_tail + s*kTailTok;
-  // split tail_splits + i covers the packed tiles [i*chunk, min(t_tail,
-  // (i+1)*chunk)).
-  // With tail_fused set there are no tail splits: the last packed split also
-  // takes the tail, after its tiles (when the one-wave budget leaves no room).
-  int t_tail;
-  int tail_splits, splits, chunk, tail_fused;
+  // Context split of a sequence (SeqPlan): splits s < tail_splits cover the
+  // tail [t_tail, l), kTailTok tokens each from t_tail + s*kTailTok; split
+  // tail_splits + i covers the packed tiles [i*chunk, min(t_tail,
+  // (i+1)*chunk)).  With tail_fused set there are no tail splits: the last
+  // packed split also takes the tail, after its tiles.
+  SeqPlan plan;   // of every sequence when the lengths are uniform
+  SplitCfg scfg;  // to plan each sequence on the device otherwise
+  int splits;     // grid width: the most splits of any sequence (workspace stride)
   // Split partials of attention group gid = (b, kv-head, head chunk):
   float* ws_o;        // [gid][splits][kHeadChunk][D]  output sums
   float* ws_ml;       // [gid][splits][kHeadChunk][2]  (max in log2 units, sum)
@@ -118,7 +204,7 @@ struct AttnArgs {
   int* status;        // set nonzero when a bounded wait for staged data timed out
 };
 
-cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a,
+cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
                              cudaStream_t st);
 
 }  // namespace kivi

@@ -400,7 +400,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
 template <int BITS, int DT>
 __global__ void __launch_bounds__(64)
 quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
-                        const void* __restrict__ vin, int T, int nq_k, int nq_v) {
+                        const void* __restrict__ vin, int t_in, const SeqLens lens) {
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int EB = DT == kF32 ? 4 : 2;
   constexpr int CPR = kHeadDim * EB / 16;
@@ -414,9 +414,12 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
+  const int T = seq_len(lens, b);  // this sequence's tokens: the first T of the t_in input rows
+  if (t0 >= T) return;
+  const int nq_k = policy_nq_k(T, cv.R, cv.policy), nq_v = policy_nq_v(T, cv.R, cv.policy);
   const int rows = min(32, T - t0);
   {
-    const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * T + t0) * (long)(kHeadDim * EB);
+    const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * t_in + t0) * (long)(kHeadDim * EB);
     for (int i = lane; i < rows * CPR; i += 32) {
       const int r = i / CPR, c = i % CPR;
       cp_async16(&s_in[r * CPR + (warp == 0 ? c : vswz<CPG>(r, c))], src + 16L * i);
@@ -436,8 +439,8 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
 // read of this step).  One CTA per (chunk c_lo + blockIdx.x, kv-head, b).
 template <int BITS, int DT>
 __global__ void __launch_bounds__(64)
-append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int l0, int n,
-                       int c_lo, int nq_k0, int nq_k1, int nq_v0, int nq_v1) {
+append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int n, int c_lo,
+                       const SeqLens lens) {
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int CPR = 16;  // staged as fp16: 16-byte chunks per row
   __shared__ __align__(16) uint4 s_in_all[2][32 * CPR];
@@ -449,7 +452,12 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
   const int chunk = c_lo + blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
-  const int L = l0 + n;
+  const int l0 = seq_len(lens, b), L = l0 + n;
+  const int nq_k0 = policy_nq_k(l0, cv.R, cv.policy), nq_k1 = policy_nq_k(L, cv.R, cv.policy);
+  const int nq_v0 = policy_nq_v(l0, cv.R, cv.policy), nq_v1 = policy_nq_v(L, cv.R, cv.policy);
+  // this sequence's chunks: those holding [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
+  const int lo = min(nq_k0, nq_v0), hi = max(nq_k1, nq_v1);
+  if (hi <= lo || t0 + 32 <= lo || t0 >= hi) return;
   const int rows = min(32, L - t0);
   const __half* ring = warp == 0 ? cv.ring_k : cv.ring_v;
   const void* in = warp == 0 ? kin : vin;
@@ -476,10 +484,12 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
 // kv-head, b); thread d owns channel d.
 template <int DT>
 __global__ void __launch_bounds__(128)
-append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int l0, int n) {
+append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int n,
+                   const SeqLens lens) {
   const int m = min(n, cv.W);
   const int i = n - m + blockIdx.x;  // input row
-  const int t = l0 + i, h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const int h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
+  const int t = seq_len(lens, b) + i;
   const long unit = (long)b * cv.H + h;
   const long src = (unit * n + i) * kHeadDim + d;
   const long dst = (unit * cv.W + t % cv.W) * kHeadDim + d;
@@ -495,13 +505,14 @@ append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __res
 //     t+1-R .. t in slot order: quantize each channel of each group.
 template <int BITS, int DT>
 __global__ void __launch_bounds__(128)
-append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int t) {
+append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, const SeqLens lens) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int PER_BYTE = 8 / BITS;
   const int h = blockIdx.x, b = blockIdx.y;
   const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const long unit = (long)b * cv.H + h;
+  const int t = seq_len(lens, b);  // the new token's position in its sequence
   const int R = cv.R, slot = t % R;
   const __half kx = load1<DT>(kin, unit * kHeadDim + d);
   const __half vx = load1<DT>(vin, unit * kHeadDim + d);
@@ -563,73 +574,81 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
 }
 
 template <int BITS>
-cudaError_t prefill_bits(const CacheView& cv, const void* k, const void* v, int dtype,
-                         int T, int nq_k, int nq_v, cudaStream_t st) {
-  const dim3 grid((T + 31) / 32, cv.H, cv.B);
+cudaError_t prefill_bits(const CacheView& cv, const void* k, const void* v, int dtype, int t_in,
+                         const SeqLens& lens, cudaStream_t st) {
+  const dim3 grid((t_in + 31) / 32, cv.H, cv.B);
   switch (dtype) {
-    case kF32: quantize_prefill_kernel<BITS, kF32><<<grid, 64, 0, st>>>(cv, k, v, T, nq_k, nq_v); break;
-    case kF16: quantize_prefill_kernel<BITS, kF16><<<grid, 64, 0, st>>>(cv, k, v, T, nq_k, nq_v); break;
-    default: quantize_prefill_kernel<BITS, kBF16><<<grid, 64, 0, st>>>(cv, k, v, T, nq_k, nq_v); break;
+    case kF32: quantize_prefill_kernel<BITS, kF32><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
+    case kF16: quantize_prefill_kernel<BITS, kF16><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
+    default: quantize_prefill_kernel<BITS, kBF16><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
   }
   return cudaGetLastError();
 }
 
 template <int BITS>
-cudaError_t append_bits(const CacheView& cv, const void* k, const void* v, int dtype, int t,
+cudaError_t append_bits(const CacheView& cv, const void* k, const void* v, int dtype, const SeqLens& lens,
                         cudaStream_t st) {
   const dim3 grid(cv.H, cv.B);
   switch (dtype) {
-    case kF32: append_kernel<BITS, kF32><<<grid, kHeadDim, 0, st>>>(cv, k, v, t); break;
-    case kF16: append_kernel<BITS, kF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, t); break;
-    default: append_kernel<BITS, kBF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, t); break;
+    case kF32: append_kernel<BITS, kF32><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
+    case kF16: append_kernel<BITS, kF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
+    default: append_kernel<BITS, kBF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
   }
   return cudaGetLastError();
 }
 
 template <int BITS, int DT>
-cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, int l0, int n, int c_lo,
-                             int c_hi, int nq_k0, int nq_k1, int nq_v0, int nq_v1, cudaStream_t st) {
+cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, int n, int c_lo, int c_hi,
+                             const SeqLens& lens, cudaStream_t st) {
   if (c_hi > c_lo)
-    append_quantize_kernel<BITS, DT><<<dim3(c_hi - c_lo, cv.H, cv.B), 64, 0, st>>>(cv, k, v, l0, n, c_lo, nq_k0,
-                                                                                  nq_k1, nq_v0, nq_v1);
-  append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, l0, n);
+    append_quantize_kernel<BITS, DT><<<dim3(c_hi - c_lo, cv.H, cv.B), 64, 0, st>>>(cv, k, v, n, c_lo, lens);
+  append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, n, lens);
   return cudaGetLastError();
 }
 
 template <int BITS>
-cudaError_t append_tokens_bits(const CacheView& cv, const void* k, const void* v, int dtype, int l0, int n,
-                               int c_lo, int c_hi, int nq_k0, int nq_k1, int nq_v0, int nq_v1,
-                               cudaStream_t st) {
+cudaError_t append_tokens_bits(const CacheView& cv, const void* k, const void* v, int dtype, int n, int c_lo,
+                               int c_hi, const SeqLens& lens, cudaStream_t st) {
   switch (dtype) {
-    case kF32: return append_tokens_dt<BITS, kF32>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
-    case kF16: return append_tokens_dt<BITS, kF16>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
-    default: return append_tokens_dt<BITS, kBF16>(cv, k, v, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+    case kF32: return append_tokens_dt<BITS, kF32>(cv, k, v, n, c_lo, c_hi, lens, st);
+    case kF16: return append_tokens_dt<BITS, kF16>(cv, k, v, n, c_lo, c_hi, lens, st);
+    default: return append_tokens_dt<BITS, kBF16>(cv, k, v, n, c_lo, c_hi, lens, st);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype, int l0, int n,
-                                 int nq_k0, int nq_k1, int nq_v0, int nq_v1, cudaStream_t st) {
+cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype, int n,
+                                 const SeqLens& lens, cudaStream_t st) {
   if (n <= 0) return cudaSuccess;
-  // the chunks holding [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
-  const int lo = min(nq_k0, nq_v0), hi = max(nq_k1, nq_v1);
-  const int c_lo = lo / 32, c_hi = hi > lo ? (hi + 31) / 32 : c_lo;
-  return cv.bits == 2 ? append_tokens_bits<2>(cv, k, v, dtype, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st)
-                      : append_tokens_bits<4>(cv, k, v, dtype, l0, n, c_lo, c_hi, nq_k0, nq_k1, nq_v0, nq_v1, st);
+  // the chunks holding some sequence's [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
+  int c_lo = INT_MAX, c_hi = 0;
+  const int nb = lens.uniform >= 0 ? 1 : cv.B;
+  for (int b = 0; b < nb; ++b) {
+    const int l0 = seq_len(lens, b), L = l0 + n;
+    const int lo = min(policy_nq_k(l0, cv.R, cv.policy), policy_nq_v(l0, cv.R, cv.policy));
+    const int hi = max(policy_nq_k(L, cv.R, cv.policy), policy_nq_v(L, cv.R, cv.policy));
+    if (hi > lo) {
+      c_lo = min(c_lo, lo / 32);
+      c_hi = max(c_hi, (hi + 31) / 32);
+    }
+  }
+  if (c_hi == 0) c_lo = 0;
+  return cv.bits == 2 ? append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st)
+                      : append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
 }
 
-cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const void* v,
-                                    int dtype, int T, int nq_k, int nq_v, cudaStream_t st) {
-  if (T <= 0) return cudaSuccess;
-  return cv.bits == 2 ? prefill_bits<2>(cv, k, v, dtype, T, nq_k, nq_v, st)
-                      : prefill_bits<4>(cv, k, v, dtype, T, nq_k, nq_v, st);
+cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const void* v, int dtype, int t_in,
+                                    const SeqLens& lens, cudaStream_t st) {
+  if (t_in <= 0) return cudaSuccess;
+  return cv.bits == 2 ? prefill_bits<2>(cv, k, v, dtype, t_in, lens, st)
+                      : prefill_bits<4>(cv, k, v, dtype, t_in, lens, st);
 }
 
-cudaError_t launch_append(const CacheView& cv, const void* k, const void* v, int dtype, int t,
+cudaError_t launch_append(const CacheView& cv, const void* k, const void* v, int dtype, const SeqLens& lens,
                           cudaStream_t st) {
-  return cv.bits == 2 ? append_bits<2>(cv, k, v, dtype, t, st)
-                      : append_bits<4>(cv, k, v, dtype, t, st);
+  return cv.bits == 2 ? append_bits<2>(cv, k, v, dtype, lens, st)
+                      : append_bits<4>(cv, k, v, dtype, lens, st);
 }
 
 }  // namespace kivi

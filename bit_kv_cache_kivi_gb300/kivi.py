@@ -68,6 +68,9 @@ def lib() -> C.CDLL:
                 "kivi_cache_init": (i32, [C.POINTER(kivi_config), C.POINTER(kivi_buffers),
                                           C.POINTER(vp)]),
                 "kivi_quantize_prefill": (i32, [vp, vp, vp, i32, i32, vp]),
+                "kivi_quantize_prefill_varlen": (i32, [vp, vp, vp, i32, i32, C.POINTER(i32), vp]),
+                "kivi_cache_set_lengths": (i32, [vp, C.POINTER(i32)]),
+                "kivi_cache_lengths": (i32, [vp, C.POINTER(i32)]),
                 "kivi_append_decode": (i32, [vp, vp, vp, i32, vp]),
                 "kivi_append_tokens": (i32, [vp, vp, vp, i32, i32, vp]),
                 "kivi_cache_set_length": (i32, [vp, i32]),
@@ -126,6 +129,23 @@ def kivi_cache_init(cfg: kivi_config, bufs: kivi_buffers) -> C.c_void_p:
 def kivi_quantize_prefill(h, k, v, dtype: int, n_tokens: int, stream=None) -> None:
     _check(lib().kivi_quantize_prefill(h, _ptr(k), _ptr(v), dtype, n_tokens, _stream(stream)),
            "kivi_quantize_prefill")
+
+
+def kivi_quantize_prefill_varlen(h, k, v, dtype: int, max_len: int, lengths, stream=None) -> None:
+    arr = (C.c_int * len(lengths))(*[int(x) for x in lengths])
+    _check(lib().kivi_quantize_prefill_varlen(h, _ptr(k), _ptr(v), dtype, max_len, arr, _stream(stream)),
+           "kivi_quantize_prefill_varlen")
+
+
+def kivi_cache_set_lengths(h, lengths) -> None:
+    arr = (C.c_int * len(lengths))(*[int(x) for x in lengths])
+    _check(lib().kivi_cache_set_lengths(h, arr), "kivi_cache_set_lengths")
+
+
+def kivi_cache_lengths(h, batch: int) -> list[int]:
+    arr = (C.c_int * batch)()
+    _check(lib().kivi_cache_lengths(h, arr), "kivi_cache_lengths")
+    return list(arr)
 
 
 def kivi_append_decode(h, k_new, v_new, dtype: int, stream=None) -> None:
@@ -213,7 +233,13 @@ class KiviCache:
     # -- shape helpers
     @property
     def length(self) -> int:
+        """Every sequence's length; -2 when the sequences' lengths differ."""
         return kivi_cache_length(self.handle)
+
+    @property
+    def lengths(self) -> list[int]:
+        """Per-sequence lengths."""
+        return kivi_cache_lengths(self.handle, self.cfg.batch)
 
     def _check_kv(self, x: torch.Tensor, T: int | None) -> int:
         c = self.cfg
@@ -228,12 +254,19 @@ class KiviCache:
         return _TORCH_DTYPE[x.dtype]
 
     # -- the hot path
-    def prefill(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    def prefill(self, k: torch.Tensor, v: torch.Tensor, lengths=None, stream=None) -> None:
+        """Prefill an empty cache from k, v [B][H][T][D]; with ``lengths``
+        (B ints), sequence b takes only its first lengths[b] rows."""
         T = k.shape[2]
         dt = self._check_kv(k, T)
         if self._check_kv(v, T) != dt:
             raise ValueError("K and V dtypes differ")
-        kivi_quantize_prefill(self.handle, k, v, dt, T, stream)
+        if lengths is None:
+            kivi_quantize_prefill(self.handle, k, v, dt, T, stream)
+        else:
+            if len(lengths) != self.cfg.batch:
+                raise ValueError(f"expected {self.cfg.batch} lengths")
+            kivi_quantize_prefill_varlen(self.handle, k, v, dt, T, lengths, stream)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
         k_new = k_new.reshape(self.cfg.batch, self.cfg.n_kv_heads, self.cfg.head_dim)
@@ -254,6 +287,12 @@ class KiviCache:
     def set_length(self, length: int) -> None:
         """The length of a state whose buffers were just restored."""
         kivi_cache_set_length(self.handle, length)
+
+    def set_lengths(self, lengths) -> None:
+        """Per-sequence lengths of a state whose buffers were just restored."""
+        if len(lengths) != self.cfg.batch:
+            raise ValueError(f"expected {self.cfg.batch} lengths")
+        kivi_cache_set_lengths(self.handle, lengths)
 
     def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
                   softmax_scale: float = 0.0, stream=None) -> torch.Tensor:

@@ -138,21 +138,38 @@ kivi_status kivi_cache_init(const kivi_config *cfg, const kivi_buffers *bufs,
 kivi_status kivi_quantize_prefill(kivi_cache *c, const void *k, const void *v,
                                   kivi_dtype dtype, int n_tokens, void *stream);
 
-/* Append one decoded token (review §1.3 decoding step 1; Algorithm 1
- * decoding phase).  k_new, v_new: device [B][H][D] of dtype.  Token t = length
- * goes to ring slot t mod W.  ALG1: if t >= R, the value token t-R leaves the
+/* Sequences of a batch may have different lengths (one per batch row; every
+ * call below applies the policy to each sequence at its own length).  With
+ * more than KIVI_MAX_VARLEN_BATCH sequences, all lengths must be equal. */
+#define KIVI_MAX_VARLEN_BATCH 1024
+
+/* Prefill with per-sequence lengths: k, v: device [B][H][max_len][D] of
+ * dtype, contiguous, 16-byte aligned; sequence b is its first lengths[b]
+ * rows (the others are ignored).  lengths: host int[B], each in [0,
+ * max_tokens] (KIVI_ECAPACITY) and <= max_len (KIVI_ESHAPE).  The cache must
+ * be empty.  Each sequence is quantized exactly as kivi_quantize_prefill
+ * would quantize it alone. */
+kivi_status kivi_quantize_prefill_varlen(kivi_cache *c, const void *k,
+                                         const void *v, kivi_dtype dtype,
+                                         int max_len, const int *lengths,
+                                         void *stream);
+
+/* Append one decoded token to every sequence (review §1.3 decoding step 1;
+ * Algorithm 1 decoding phase).  k_new, v_new: device [B][H][D] of dtype.
+ * Token t = the sequence's length goes to ring slot t mod W.  ALG1: if t >= R, the value token t-R leaves the
  * window and is quantized per token; if t+1 is a multiple of R, the R keys of
  * the ring (a whole number of groups) are quantized per channel.  SHARED:
  * when t+1-R reaches a positive multiple of G, the G oldest ring tokens are
  * quantized, keys per channel (one group) and values per token.  The
  * decision is taken on the host from the length alone.  KIVI_ECAPACITY when
- * the cache is full; under SHARED, KIVI_EINVAL unless k_new and v_new are
- * 16-byte aligned. */
+ * the longest sequence is at max_tokens; under SHARED, KIVI_EINVAL unless
+ * k_new and v_new are 16-byte aligned. */
 kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
                                const void *v_new, kivi_dtype dtype,
                                void *stream);
 
-/* Append n_tokens tokens at once (chunked prefill into a non-empty cache;
+/* Append n_tokens tokens at once to every sequence (chunked prefill into a
+ * non-empty cache;
  * the review §1.3 prefill step continued on a cache that already holds
  * tokens).  k, v: device [B][H][n_tokens][D] of dtype, contiguous,
  * 16-byte aligned.  The result is the cache that n_tokens calls of
@@ -160,8 +177,8 @@ kivi_status kivi_append_decode(kivi_cache *c, const void *k_new,
  * token), bit for bit: the key groups that become whole and the value tokens
  * that leave the window are quantized (old tokens read from the rings), then
  * the last min(n_tokens, R) tokens go to their ring slots.  Two kernel
- * launches on the stream.  KIVI_ECAPACITY if length + n_tokens > max_tokens,
- * KIVI_EINVAL if n_tokens <= 0. */
+ * launches on the stream.  KIVI_ECAPACITY if the longest sequence + n_tokens >
+ * max_tokens, KIVI_EINVAL if n_tokens <= 0. */
 kivi_status kivi_append_tokens(kivi_cache *c, const void *k, const void *v,
                                kivi_dtype dtype, int n_tokens, void *stream);
 
@@ -171,6 +188,14 @@ kivi_status kivi_append_tokens(kivi_cache *c, const void *k, const void *v,
  * The length of a state is kivi_cache_length() at save time.  Host only; no
  * device work.  KIVI_ECAPACITY if length is outside [0, max_tokens]. */
 kivi_status kivi_cache_set_length(kivi_cache *c, int length);
+
+/* The same with per-sequence lengths (host int[B]); KIVI_ECAPACITY if one is
+ * outside [0, max_tokens], KIVI_ESHAPE for unequal lengths past
+ * KIVI_MAX_VARLEN_BATCH sequences.  Host only. */
+kivi_status kivi_cache_set_lengths(kivi_cache *c, const int *lengths);
+
+/* Per-sequence lengths into lengths (host int[B]).  Host only. */
+kivi_status kivi_cache_lengths(const kivi_cache *c, int *lengths);
 
 /* Device workspace (bytes) kivi_decode_attention needs for this handle's
  * shape at any length: split-K partial results, merged groups of partials,
@@ -193,7 +218,8 @@ size_t kivi_attention_workspace_bytes(const kivi_cache *c);
  * given workspace pointer zeroes it (one cudaMemsetAsync on the stream) and
  * every call leaves it zero.  Do not write to the workspace between calls,
  * and do not share one workspace between calls that may overlap on the GPU.
- * KIVI_ESTATE on an empty cache. */
+ * Each sequence attends over its own length; KIVI_ESTATE when a sequence is
+ * empty. */
 kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
                                   kivi_dtype q_dtype, void *out,
                                   float softmax_scale, void *workspace,
@@ -212,7 +238,9 @@ kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 /* Splits the next kivi_decode_attention call will use at length l. */
 int kivi_attention_splits(const kivi_cache *c, int l);
 
-int kivi_cache_length(const kivi_cache *c); /* tokens held; -1 if c is NULL */
+/* Tokens held by every sequence; -2 when the sequences' lengths differ (see
+ * kivi_cache_lengths), -1 if c is NULL. */
+int kivi_cache_length(const kivi_cache *c);
 kivi_status kivi_cache_reset(kivi_cache *c); /* length := 0; no device work */
 void kivi_cache_destroy(kivi_cache *c);      /* NULL is a no-op */
 

@@ -185,3 +185,52 @@ def test_split_plan_and_workspace(K):
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 1024) == 5
     K.kivi_cache_destroy(h)
+
+
+def test_varlen_host_checks(K):
+    """Per-sequence lengths: argument checks and bookkeeping, all on the host
+    (every call here returns before any launch)."""
+    import ctypes as C
+    h = K.kivi_cache_init(cfg(K, batch=3), _fake_buffers(K))
+    lib = K.lib()
+    L = C.c_int * 3
+    try:
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 100, L(5, 4097, 3), None) == K.KIVI_ECAPACITY
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 100, L(5, 101, 3), None) == K.KIVI_ESHAPE
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 100, L(-1, 1, 3), None) == K.KIVI_ECAPACITY
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 100, None, None) == K.KIVI_EINVAL
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 0, L(0, 0, 0), None) == K.KIVI_OK
+        K.kivi_cache_set_lengths(h, [5, 0, 4096])
+        assert K.kivi_cache_lengths(h, 3) == [5, 0, 4096] and K.kivi_cache_length(h) == -2
+        # the longest sequence is full
+        assert lib.kivi_append_decode(h, 16, 16, 1, None) == K.KIVI_ECAPACITY
+        assert lib.kivi_append_tokens(h, 16, 16, 1, 1, None) == K.KIVI_ECAPACITY
+        # an empty sequence: attention is refused
+        need = K.kivi_attention_workspace_bytes(h)
+        assert lib.kivi_decode_attention(h, 16, 1, 16, 0.0, 1 << 20, need, None) == K.KIVI_ESTATE
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_lengths(h, [1, 4097, 0])
+        assert e.value.status == K.KIVI_ECAPACITY
+        assert K.kivi_cache_lengths(h, 3) == [5, 0, 4096]  # unchanged by the refused call
+        K.kivi_cache_set_lengths(h, [7, 7, 7])
+        assert K.kivi_cache_length(h) == 7
+        # prefill needs an empty cache
+        assert lib.kivi_quantize_prefill_varlen(h, 16, 16, 1, 100, L(1, 2, 3), None) == K.KIVI_ESTATE
+        K.kivi_cache_reset(h)
+        assert K.kivi_cache_lengths(h, 3) == [0, 0, 0] and K.kivi_cache_length(h) == 0
+    finally:
+        K.kivi_cache_destroy(h)
+
+
+def test_varlen_batch_limit(K):
+    """Unequal lengths are limited to KIVI_MAX_VARLEN_BATCH sequences; equal
+    lengths are not."""
+    h = K.kivi_cache_init(cfg(K, batch=1025, n_kv_heads=1, n_q_heads=1), _fake_buffers(K))
+    try:
+        with pytest.raises(K.KiviError) as e:
+            K.kivi_cache_set_lengths(h, [1] * 1024 + [2])
+        assert e.value.status == K.KIVI_ESHAPE
+        K.kivi_cache_set_lengths(h, [3] * 1025)
+        assert K.kivi_cache_length(h) == 3
+    finally:
+        K.kivi_cache_destroy(h)
