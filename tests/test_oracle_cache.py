@@ -87,7 +87,7 @@ def test_shared_policy_counts(oracle):
         assert nq % 16 == 0 and l - nq >= min(l, 32) and l - nq < 32 + 16
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_cache_dequant_within_bound(oracle, bits):
     """Every quantized element is within its group's bound; residual rows exact."""
     B, H, T, D, G, R = 1, 2, 200, 128, 32, 64

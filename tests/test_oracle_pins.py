@@ -73,7 +73,7 @@ def _brute_codes(x32, z, s, L):
     return np.array(out)
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_rounding_is_nearest_even_brute_force(oracle, bits):
     L = (1 << bits) - 1
     rng = np.random.default_rng(bits)
@@ -96,9 +96,12 @@ def test_exact_ties_round_to_even(oracle):
     # 4-bit, range 15 -> scale 1: 6.5 -> 6, 7.5 -> 8
     codes, _, _, _ = oracle.quantize_group(f16([0.0, 6.5, 7.5, 15.0]), 4)
     assert list(codes) == [0, 6, 8, 15]
+    # 8-bit, range 255 -> scale 1: 0.5 -> 0, 1.5 -> 2, 254.5 -> 254, 127.5 -> 128
+    codes, s16, _, _ = oracle.quantize_group(f16([0.0, 0.5, 1.5, 127.5, 254.5, 255.0]), 8)
+    assert oracle.f16_bits_to_f32(s16) == 1.0 and list(codes) == [0, 0, 2, 128, 254, 255]
 
 
-@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("bits", [2, 4, 8])
 def test_codes_in_range_and_error_bound(oracle, bits):
     """codes in [0, 2^b-1]; |x - xhat| <= s16/2 + L|s32 - s16| (+ fp32 rounding)."""
     L = (1 << bits) - 1
@@ -129,8 +132,11 @@ def test_zero_range_and_underflowing_scale(oracle):
 def test_pack_layout_lsb_first(oracle):
     assert list(oracle.pack_row(np.array([0, 1, 2, 3] * 4, np.uint8), 2)) == [0xE4] * 4
     assert list(oracle.pack_row(np.array([1, 2] * 4, np.uint8), 4)) == [0x21] * 4
+    # 8 bits: one byte per channel, in channel order
+    c8 = np.arange(128, dtype=np.uint8) * 2 + 1
+    assert np.array_equal(oracle.pack_row(c8, 8), c8)
     rng = np.random.default_rng(3)
-    for bits in (2, 4):
+    for bits in (2, 4, 8):
         c = rng.integers(0, 1 << bits, 128).astype(np.uint8)
         assert np.array_equal(oracle.unpack_row(oracle.pack_row(c, bits), 128, bits), c)
 
@@ -151,8 +157,14 @@ def test_value_row_interleave(oracle):
         for w in range(8):
             want = oracle.pack_row(codes[32 * gp + 4 * w: 32 * gp + 4 * w + 4], 4)
             assert list(row4[2 * (4 * w + gp): 2 * (4 * w + gp) + 2]) == list(want)
+    # 8 bits: a unit is the 4 bytes of channels 32*gp + 4*w .. +3
+    c8 = np.arange(128, dtype=np.uint8)
+    row8 = oracle.pack_row_v(c8, 8)
+    for gp in range(4):
+        for w in range(8):
+            assert list(row8[4 * (4 * w + gp): 4 * (4 * w + gp) + 4]) == list(range(32 * gp + 4 * w, 32 * gp + 4 * w + 4))
     rng = np.random.default_rng(4)
-    for bits in (2, 4):
+    for bits in (2, 4, 8):
         c = rng.integers(0, 1 << bits, 128).astype(np.uint8)
         assert np.array_equal(oracle.unpack_row_v(oracle.pack_row_v(c, bits), 128, bits), c)
     # with one channel group per unit the interleave is the identity
