@@ -295,13 +295,13 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
     const uint8_t* tile = tile_at<BITS>(cv, unit, t / kGroup);
     const int tr = (int)(t % kGroup);  // row within the tile
     if (r < nk) {
-      if (c < CPR) cp_async16(&ts.krow[r][c], tile + tr * RB + 16 * c);
+      if (c < CPR) cp_async16(&ts.krow[r][c], tile + tr * RB + 16 * krow_chunk<BITS>(tr, c));
     } else {
       cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
     }
     if (r < nv) {
       if (c < CPR) {
-        cp_async16(&ts.vrow[r][c], tile + kOffVc<BITS> + tr * RB + 16 * c);
+        cp_async16(&ts.vrow[r][c], tile + kOffVc<BITS> + tr * RB + 16 * vrow_chunk<BITS>(tr, c));
       }
     } else {
       cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
@@ -422,7 +422,8 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
       const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
       uint32_t cb;
       if constexpr (BITS == 2) cb = row[vpos];
-      else cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
+      else if constexpr (BITS == 4) cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
+      else cb = *reinterpret_cast<const uint32_t*>(row + 4 * vpos);
       const int vs = vscale_pos(r & 31, d >> 5);
       const float sv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][0])[vs]);
       const float zv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][1])[vs]);
@@ -474,16 +475,26 @@ __device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t w_sh) {
     static_assert(I >= 0 && I < 8, "eight bit pairs per half");
     if constexpr (I <= 4) return w & (0x00030003u << (2 * I));
     else return w_sh & (0x00030003u << (2 * (I - 5)));
-  } else {
+  } else if constexpr (BITS == 4) {
     static_assert(I >= 0 && I < 4, "four nibbles per half");
     if constexpr (I <= 1) return w & (0x000F000Fu << (4 * I));
     else return w_sh & (0x000F000Fu << (4 * (I - 2)));
+  } else {
+    static_assert(I >= 0 && I < 2, "two bytes per half");
+    return (I == 0 ? w : w_sh) & 0x00FF00FFu;
   }
+}
+
+// Byte J of a and of b as the fp16 pair {a_J * 2^-24, b_J * 2^-24} (an 8-bit
+// code in the low byte of each half, exponent field zero).
+template <int J>
+__device__ __forceinline__ uint32_t byte_pair(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, J | (J << 4) | ((4 + J) << 8) | ((4 + J) << 12)) & 0x00FF00FFu;
 }
 
 template <int BITS>
 __host__ __device__ constexpr int code_exp(int i) {
-  return BITS == 2 ? (i <= 4 ? i : i - 5) : (i & 1);
+  return BITS == 2 ? (i <= 4 ? i : i - 5) : (BITS == 4 ? (i & 1) : 0);
 }
 
 template <int BITS>
@@ -509,16 +520,21 @@ constexpr float kLazySlack = 1.0f;
 // lane: pair block m = tig + 4 blk, whose word i is the pair of code position
 // i -- 2 bits: channels (16m + i, 16m + 8 + i), i < 8; 4 bits: (8m + i, 8m +
 // 4 + i), i < 4.
+//
+// 8 bits: pair blocks of 4 channels, words (4m, 4m + 2) and (4m + 1, 4m + 3)
+// at word 2m and 2m + 1; k-step ks of lane tig takes block m = 8 tig + ks, so
+// block `blk` (k-steps 2 blk, 2 blk + 1) is the 4 words from 16 tig + 4 blk.
 template <int BITS>
 __device__ __forceinline__ void pair_words(const uint32_t* vec, int tig, int blk, uint32_t (&P)[8]) {
-  const int m = tig + 4 * blk;
   if constexpr (BITS == 2) {
+    const int m = tig + 4 * blk;
     const uint4 wa = *reinterpret_cast<const uint4*>(vec + 8 * m);
     const uint4 wb = *reinterpret_cast<const uint4*>(vec + 8 * m + 4);
     P[0] = wa.x; P[1] = wa.y; P[2] = wa.z; P[3] = wa.w;
     P[4] = wb.x; P[5] = wb.y; P[6] = wb.z; P[7] = wb.w;
   } else {
-    const uint4 wa = *reinterpret_cast<const uint4*>(vec + 4 * m);
+    const int m = tig + 4 * blk;
+    const uint4 wa = *reinterpret_cast<const uint4*>(vec + (BITS == 4 ? 4 * m : 16 * tig + 4 * blk));
     P[0] = wa.x; P[1] = wa.y; P[2] = wa.z; P[3] = wa.w;
     P[4] = P[5] = P[6] = P[7] = 0u;
   }
@@ -605,12 +621,27 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
   for (int mt = 0; mt < 2; ++mt) {
     const uint32_t* rg = tb.kc + (16 * mt + g) * RW;      // key row 16mt + g
     const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * RW;  // key row 16mt + g + 8
-    constexpr int NW = BITS;  // words of a row this lane reads: tig + 4j
+    // words of a row this lane reads: tig + 4j at 2 and 4 bits; at 8 bits the
+    // 8 words from 8 tig, as two 16-byte chunks of the (rotated) row
+    constexpr int NW = BITS;
     uint32_t wg[NW], w8[NW], sg[NW], s8[NW];
+    if constexpr (BITS == 8) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint4 a0 = reinterpret_cast<const uint4*>(rg)[krow_chunk<8>(g, 2 * tig + h)];
+        const uint4 a1 = reinterpret_cast<const uint4*>(r8)[krow_chunk<8>(g + 8, 2 * tig + h)];
+        wg[4 * h] = a0.x; wg[4 * h + 1] = a0.y; wg[4 * h + 2] = a0.z; wg[4 * h + 3] = a0.w;
+        w8[4 * h] = a1.x; w8[4 * h + 1] = a1.y; w8[4 * h + 2] = a1.z; w8[4 * h + 3] = a1.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < NW; ++j) {
+        wg[j] = rg[tig + 4 * j];
+        w8[j] = r8[tig + 4 * j];
+      }
+    }
 #pragma unroll
     for (int j = 0; j < NW; ++j) {
-      wg[j] = rg[tig + 4 * j];
-      w8[j] = r8[tig + 4 * j];
       sg[j] = wg[j] >> kShift<BITS>;
       s8[j] = w8[j] >> kShift<BITS>;
     }
@@ -623,7 +654,7 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
       KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 4) KIVI_KSTEP(3, 6)
       KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 4) KIVI_KSTEP(7, 6)
 #undef KIVI_KSTEP
-    } else {
+    } else if constexpr (BITS == 4) {
 #define KIVI_KSTEP(KS, I)                                                                       \
   mma16816(acc, ext<4, I>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I>(w8[(KS) >> 1], s8[(KS) >> 1]), \
            ext<4, I + 1>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I + 1>(w8[(KS) >> 1], s8[(KS) >> 1]), \
@@ -631,6 +662,13 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
       KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 0) KIVI_KSTEP(3, 2)
       KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 0) KIVI_KSTEP(7, 2)
 #undef KIVI_KSTEP
+    } else {
+      // k-step ks: word ks (channels 4m .. 4m + 3, m = 8 tig + ks), bytes 0 / 2
+      // then bytes 1 / 3 of each half
+#pragma unroll
+      for (int ksi = 0; ksi < 8; ++ksi)
+        mma16816(acc, ext<8, 0>(wg[ksi], sg[ksi]), ext<8, 0>(w8[ksi], s8[ksi]), ext<8, 1>(wg[ksi], sg[ksi]),
+                 ext<8, 1>(w8[ksi], s8[ksi]), bq[ksi][0], bq[ksi][1]);
     }
     sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
     sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
@@ -686,6 +724,7 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
     // t0 + 4), as the two 16-bit halves (2 bits: a byte per group, two groups
     // per word)
     uint32_t pa[2], Pp[4][2], az[2], u[2][4];
+    uint32_t v8a[2][4], v8b[2][4];  // 8 bits: unit words of groups 0..3 of tokens t0 and t0 + 4
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
       const int t0 = 16 * kk + 8 * aa + tig;  // tokens t0, t0 + 4
@@ -710,6 +749,13 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
         u[aa][0] = __byte_perm(w0, w1, 0x5410);  // groups 0, 1
         u[aa][1] = __byte_perm(w0, w1, 0x7632);  // groups 2, 3
         u[aa][2] = u[aa][3] = 0u;
+      } else if constexpr (BITS == 8) {
+        // interleaved words 4g .. 4g + 3 of a row (logical chunk g of the
+        // rotated row) hold channels 4g..4g+3 of groups 0..3, a byte each
+        const uint4 w0 = reinterpret_cast<const uint4*>(tb.vc + t0 * RW)[vrow_chunk<8>(t0, g)];
+        const uint4 w1 = reinterpret_cast<const uint4*>(tb.vc + (t0 + 4) * RW)[vrow_chunk<8>(t0 + 4, g)];
+        v8a[aa][0] = w0.x; v8a[aa][1] = w0.y; v8a[aa][2] = w0.z; v8a[aa][3] = w0.w;
+        v8b[aa][0] = w1.x; v8b[aa][1] = w1.y; v8b[aa][2] = w1.z; v8b[aa][3] = w1.w;
       } else {
         // interleaved words 2g, 2g+1 of a row hold, per 16-bit half,
         // channels 4g..4g+3 of groups 0..3
@@ -738,6 +784,17 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
           KIVI_VTILE(4, 0, 2) KIVI_VTILE(5, 2, 2) KIVI_VTILE(6, 4, 3) KIVI_VTILE(7, 6, 3)
         }
 #undef KIVI_VTILE
+      }
+    } else if constexpr (BITS == 8) {
+      // m-tile 2gp + hm: rows g / g + 8 are byte 2hm / 2hm + 1 of the unit
+      // words, k is the token pair (t0, t0 + 4) of aa = 0, then of aa = 1
+#pragma unroll
+      for (int gp = 0; gp < 4; ++gp) {
+        mma16816(O[2 * gp], byte_pair<0>(v8a[0][gp], v8b[0][gp]), byte_pair<1>(v8a[0][gp], v8b[0][gp]),
+                 byte_pair<0>(v8a[1][gp], v8b[1][gp]), byte_pair<1>(v8a[1][gp], v8b[1][gp]), Pp[gp][0], Pp[gp][1]);
+        mma16816(O[2 * gp + 1], byte_pair<2>(v8a[0][gp], v8b[0][gp]), byte_pair<3>(v8a[0][gp], v8b[0][gp]),
+                 byte_pair<2>(v8a[1][gp], v8b[1][gp]), byte_pair<3>(v8a[1][gp], v8b[1][gp]), Pp[gp][0],
+                 Pp[gp][1]);
       }
     } else {
 #pragma unroll
@@ -795,11 +852,16 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float
       i = 2 * (ks & 3) + r;
       c0 = 16 * m + i;
       c1 = c0 + 8;
-    } else {
+    } else if constexpr (BITS == 4) {
       const int m = tig + 4 * (ks >> 1);
       i = 2 * (ks & 1) + r;
       c0 = 8 * m + i;
       c1 = c0 + 4;
+    } else {
+      const int m = 8 * tig + ks;
+      i = r;
+      c0 = 4 * m + r;
+      c1 = c0 + 2;
     }
     const float f = code_scale<BITS>(i);
     const float q0 = ldexpf(s.qv[hh][c0], -s.qexp[hh]), q1 = ldexpf(s.qv[hh][c1], -s.qexp[hh]);
@@ -819,7 +881,10 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float
 }
 
 // The stage buffer mirrors the packed tile byte for byte.
-static_assert(sizeof(TileBuf<2>) == kTileBytes<2> && sizeof(TileBuf<4>) == kTileBytes<4>, "stage = tile");
+static_assert(sizeof(TileBuf<2>) == kTileBytes<2> && sizeof(TileBuf<4>) == kTileBytes<4> &&
+                  sizeof(TileBuf<8>) == kTileBytes<8>, "stage = tile");
+static_assert(offsetof(TileBuf<8>, vc) == kOffVc<8> && offsetof(TileBuf<8>, sk) == kOffSk<8> &&
+              offsetof(TileBuf<8>, zv) == kOffZv<8>, "stage layout (8 bits)");
 static_assert(offsetof(TileBuf<2>, vc) == kOffVc<2> && offsetof(TileBuf<2>, sk) == kOffSk<2> &&
               offsetof(TileBuf<2>, zk) == kOffZk<2> && offsetof(TileBuf<2>, sv) == kOffSv<2> &&
               offsetof(TileBuf<2>, zv) == kOffZv<2>, "stage layout (2 bits)");
@@ -1093,7 +1158,7 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
 
 // grid (splits, H * head_chunks, B), 128 threads.
 template <int BITS>
-__global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
+__global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
   extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS>)
   SplitSmem<BITS>& sm = *reinterpret_cast<SplitSmem<BITS>*>(smem_raw);
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
@@ -1204,6 +1269,12 @@ __global__ void __launch_bounds__(128, kAttnCtasPerSm) attn_kernel(CacheView cv,
 
 }  // namespace
 
+// attn_ctas_per_sm(BITS) CTAs must fit an SM's 228 KB of shared memory
+// (1 KB of it reserved per CTA).
+static_assert(4 * (sizeof(SplitSmem<2>) + 1024 + 256) <= 228 * 1024, "2-bit CTAs per SM");
+static_assert(4 * (sizeof(SplitSmem<4>) + 1024 + 256) <= 228 * 1024, "4-bit CTAs per SM");
+static_assert(2 * (sizeof(SplitSmem<8>) + 1024 + 256) <= 228 * 1024, "8-bit CTAs per SM");
+
 template <int BITS>
 cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
                         cudaStream_t st) {
@@ -1221,7 +1292,11 @@ cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLe
   const int grp = a.Hq / cv.H;
   const int nhc = (grp + kNH - 1) / kNH;
   const dim3 grid(a.splits, cv.H * nhc, cv.B);
-  return cv.bits == 2 ? launch_bits<2>(grid, cv, a, lens, st) : launch_bits<4>(grid, cv, a, lens, st);
+  switch (cv.bits) {
+    case 2: return launch_bits<2>(grid, cv, a, lens, st);
+    case 4: return launch_bits<4>(grid, cv, a, lens, st);
+    default: return launch_bits<8>(grid, cv, a, lens, st);
+  }
 }
 
 }  // namespace kivi

@@ -36,7 +36,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 kivi_status check_config(const kivi_config* c) {
   if (!c) return KIVI_EINVAL;
-  if (c->bits != 2 && c->bits != 4) return KIVI_EINVAL;
+  if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KIVI_EINVAL;
   if (c->group != kivi::kGroup || c->head_dim != kivi::kHeadDim) return KIVI_EINVAL;
   if (c->residual <= 0 || c->residual % c->group) return KIVI_ESHAPE;
   if (c->batch <= 0 || c->n_kv_heads <= 0 || c->n_q_heads <= 0) return KIVI_ESHAPE;
@@ -121,7 +121,7 @@ int max_tail_splits(const kivi_config& c) {
 // of a GB300, capped so that the partials merge in at most two levels.
 int split_budget(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (long)kivi::kAttnCtasPerSm * kivi::kTargetSMs / u;
+  long s = (long)kivi::attn_ctas_per_sm(c.bits) * kivi::kTargetSMs / u;
   if (s > kivi::kMaxSplits) s = kivi::kMaxSplits;
   return (int)s;
 }

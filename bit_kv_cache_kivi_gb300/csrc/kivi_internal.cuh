@@ -11,6 +11,9 @@ constexpr int kHeadDim = 128;  // D supported by the kernels
 constexpr int kGroup = 32;     // G supported by the kernels
 constexpr int kTargetSMs = 152;    // GB300 SM count used by the split policy
 constexpr int kAttnCtasPerSm = 4;  // attention CTAs resident per SM (registers, shared memory)
+// The same per bit width: at 8 bits two staged 9 KB tiles per warp leave
+// room for two CTAs per SM.
+__host__ __device__ constexpr int attn_ctas_per_sm(int bits) { return bits == 8 ? 2 : kAttnCtasPerSm; }
 constexpr int kHeadChunk = 4;      // query heads per attention CTA
 constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two levels at most)
 constexpr int kTailTok = 64;       // tail tokens per tail split
@@ -131,17 +134,40 @@ template <int BITS>
 constexpr int kOffZv = kOffSk<BITS> + 6 * kHeadDim;
 template <int BITS>
 constexpr int kTileBytes = kOffSk<BITS> + 8 * kHeadDim;
-static_assert(kTileBytes<2> == 3072 && kTileBytes<4> == 5120, "tile sizes");
+static_assert(kTileBytes<2> == 3072 && kTileBytes<4> == 5120 && kTileBytes<8> == 9216, "tile sizes");
+
+// At 8 bits a code row is 128 bytes, so that rows at a multiple of 128 bytes
+// would put the same word of every row in the same shared-memory bank.  The
+// rows are therefore stored rotated by whole 16-byte chunks: key row r by
+// (r & 1) chunks, value row r by 2 (r & 3) chunks -- logical chunk c of the
+// row sits at chunk (c + rot) mod 8.  At 2 and 4 bits nothing is rotated.
+template <int BITS>
+__host__ __device__ __forceinline__ int krow_chunk(int r, int c) {
+  return BITS == 8 ? (c + (r & 1)) & 7 : c;
+}
+template <int BITS>
+__host__ __device__ __forceinline__ int vrow_chunk(int r, int c) {
+  return BITS == 8 ? (c + 2 * (r & 3)) & 7 : c;
+}
+// Byte offset of logical byte i of key / value row r (within the row).
+template <int BITS>
+__host__ __device__ __forceinline__ int krow_byte(int r, int i) {
+  return 16 * krow_chunk<BITS>(r, i >> 4) + (i & 15);
+}
+template <int BITS>
+__host__ __device__ __forceinline__ int vrow_byte(int r, int i) {
+  return 16 * vrow_chunk<BITS>(r, i >> 4) + (i & 15);
+}
 static_assert(kGroup * (kHeadDim / kGroup) * 2 == 2 * kHeadDim, "value scale block size");
 
 // Key scales / zeros of a tile are stored in channel-pair order: 32-bit word
 // i of pair block m holds the fp16 pair (channel P m + i, channel P m + i +
-// P / 2), P = 16 at 2 bits and 8 at 4 bits -- the two values one B-fragment
-// register of the score product takes.  kscale_pos(c) is channel c's fp16
-// slot.
+// P / 2), P = 16 at 2 bits, 8 at 4 bits and 4 at 8 bits -- the two values one
+// B-fragment register of the score product takes.  kscale_pos(c) is channel
+// c's fp16 slot.
 template <int BITS>
 __host__ __device__ constexpr int kscale_pos(int c) {
-  constexpr int P = BITS == 2 ? 16 : 8;
+  constexpr int P = BITS == 2 ? 16 : (BITS == 4 ? 8 : 4);
   return P * (c / P) + 2 * (c % (P / 2)) + (c % P) / (P / 2);
 }
 

@@ -78,18 +78,29 @@ __device__ __forceinline__ uint32_t exact_code(float x, float z, float s, int L)
   return (uint32_t)min(max(q, 0), L);
 }
 
-// Exact codes of 8 key channels of one token (each channel its own group).
+// Exact codes of 8 key channels of one token (each channel its own group),
+// packed LSB-first: 8 * BITS bits, as two words (the second one used at 8
+// bits only).
 template <int BITS>
-__device__ __noinline__ uint32_t exact_key_slice(uint4 xb, const float* z, const float* s) {
+__device__ __noinline__ uint2 exact_key_slice(uint4 xb, const float* z, const float* s) {
   constexpr int L = (1 << BITS) - 1;
   const uint32_t w[4] = {xb.x, xb.y, xb.z, xb.w};
-  uint32_t acc = 0;
+  uint32_t acc[2] = {0u, 0u};
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     const float x = __half2float(__ushort_as_half((unsigned short)(w[e >> 1] >> (16 * (e & 1)))));
-    acc |= exact_code(x, z[e], s[e], L) << (BITS * e);
+    const int bit = BITS * e;
+    acc[bit >> 5] |= exact_code(x, z[e], s[e], L) << (bit & 31);
   }
-  return acc;
+  return make_uint2(acc[0], acc[1]);
+}
+
+// Store this lane's 8 key codes (8 * BITS bits) at dst.
+template <int BITS>
+__device__ __forceinline__ void store_key_slice(uint8_t* dst, uint2 acc) {
+  if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)acc.x;
+  else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(dst) = acc.x;
+  else *reinterpret_cast<uint2*>(dst) = acc;
 }
 
 // Exact codes of one value group (32 channels, one scale/zero).
@@ -163,8 +174,10 @@ __device__ __forceinline__ void store_value_units(uint8_t* row, int g, const uin
   for (int u = 0; u < 8; ++u) {
     if constexpr (BITS == 2)
       row[v_unit_pos(8 * g + u)] = (uint8_t)(words[u >> 2] >> (8 * (u & 3)));
-    else
+    else if constexpr (BITS == 4)
       reinterpret_cast<uint16_t*>(row)[v_unit_pos(8 * g + u)] = (uint16_t)(words[u >> 1] >> (16 * (u & 1)));
+    else
+      reinterpret_cast<uint32_t*>(row)[v_unit_pos(8 * g + u)] = words[u];
   }
 }
 
@@ -255,39 +268,39 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         sf[e] = gp[e].s;
         safe = safe && f.safe;
       }
-      constexpr uint32_t C = magic_sum(8, BITS);
+      // codes per 32-bit word, and the correction of a word's magic sum
+      constexpr int CW = BITS == 8 ? 4 : 8;
+      constexpr uint32_t C = magic_sum(CW, BITS);
       if (safe) {
 #pragma unroll 4
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
-          uint32_t acc = 0;
+          uint32_t acc[2] = {0u, 0u};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 f = __half22float2(x[i]);
-            acc += code_bits(f.x, zf[2 * i], sf[2 * i], inv[2 * i]) << (BITS * (2 * i));
-            acc += code_bits(f.y, zf[2 * i + 1], sf[2 * i + 1], inv[2 * i + 1]) << (BITS * (2 * i + 1));
+            const int e0 = 2 * i, e1 = 2 * i + 1;
+            acc[e0 / CW] += code_bits(f.x, zf[e0], sf[e0], inv[e0]) << (BITS * (e0 % CW));
+            acc[e1 / CW] += code_bits(f.y, zf[e1], sf[e1], inv[e1]) << (BITS * (e1 % CW));
           }
-          acc -= C;
-          uint8_t* dst = &s_codes[(2 * k + par) * RB + cl * BITS];
-          if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)acc;
-          else *reinterpret_cast<uint32_t*>(dst) = acc;
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS], make_uint2(acc[0] - C, acc[1] - C));
         }
       } else {
         // a channel group with an fp16-subnormal scale: IEEE division + clamp
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
-          const uint32_t acc = exact_key_slice<BITS>(h2x4_bits(x), zf, sf);
-          uint8_t* dst = &s_codes[(2 * k + par) * RB + cl * BITS];
-          if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(dst) = (uint16_t)acc;
-          else *reinterpret_cast<uint32_t*>(dst) = acc;
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS],
+                                exact_key_slice<BITS>(h2x4_bits(x), zf, sf));
         }
       }
       __syncwarp();
       uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
       uint4* gdst = reinterpret_cast<uint4*>(tile);
       const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
+      constexpr int CPRB = RB / 16;  // 16-byte chunks per code row
 #pragma unroll
-      for (int i = lane; i < 32 * RB / 16; i += 32) gdst[i] = ssrc[i];
+      for (int i = lane; i < 32 * CPRB; i += 32)
+        gdst[(i / CPRB) * CPRB + krow_chunk<BITS>(i / CPRB, i % CPRB)] = ssrc[i];
       {
         // scales (lanes of parity 0) and zeros (parity 1), in the tile's
         // channel-pair order (kscale_pos); the 16-byte store lands at c8 either way
@@ -310,10 +323,16 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
                                __ushort_as_half((unsigned short)(r1 >> 16))};
 #pragma unroll
           for (int i = 0; i < 4; ++i) w[i] = hi ? pack_halves(o[i], v[4 + i]) : pack_halves(v[i], o[i]);
-        } else {
+        } else if constexpr (BITS == 4) {
           // pair block m = this lane's 8 channels: word i = (8m + i, 8m + 4 + i)
 #pragma unroll
           for (int i = 0; i < 4; ++i) w[i] = pack_halves(v[i], v[4 + i]);
+        } else {
+          // pair blocks 2cl, 2cl + 1 of 4 channels: word i = (4m + i, 4m + 2 + i)
+          w[0] = pack_halves(v[0], v[2]);
+          w[1] = pack_halves(v[1], v[3]);
+          w[2] = pack_halves(v[4], v[6]);
+          w[3] = pack_halves(v[5], v[7]);
         }
         *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + (par ? kOffZk<BITS> : kOffSk<BITS>)) + c8) =
             make_uint4(w[0], w[1], w[2], w[3]);
@@ -390,7 +409,9 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
     const int r_lo = min(max(vlo - t0, 0), 32), r_hi = min(max(vhi - t0, 0), 32);
     uint4* gdst = reinterpret_cast<uint4*>(tile_at<BITS>(cv, unit, chunk) + kOffVc<BITS>);
     const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
-    for (int i = r_lo * RB / 16 + lane; i < r_hi * RB / 16; i += 32) gdst[i] = ssrc[i];
+    constexpr int CPRB = RB / 16;  // 16-byte chunks per code row
+    for (int i = r_lo * CPRB + lane; i < r_hi * CPRB; i += 32)
+      gdst[(i / CPRB) * CPRB + vrow_chunk<BITS>(i / CPRB, i % CPRB)] = ssrc[i];
   }
 }
 
@@ -536,7 +557,7 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
     const int vbyte = v_unit_pos(d / 4) * (BITS / 2) + (d % 4) / PER_BYTE;
     uint8_t* tile = tile_at<BITS>(cv, unit, u / kGroup);
     const int row = (int)(u % kGroup);
-    if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vbyte] = (uint8_t)q;
+    if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vrow_byte<BITS>(row, vbyte)] = (uint8_t)q;
     if (lane == 0) {
       reinterpret_cast<__half*>(tile + kOffSv<BITS>)[vscale_pos(row, warp)] = p.sh;
       reinterpret_cast<__half*>(tile + kOffZv<BITS>)[vscale_pos(row, warp)] = p.zh;
@@ -565,7 +586,7 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
         uint32_t q = encode(xs[j], p, L) << (BITS * (d % PER_BYTE));
 #pragma unroll
         for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-        if (d % PER_BYTE == 0) tile[j * RB + d / PER_BYTE] = (uint8_t)q;
+        if (d % PER_BYTE == 0) tile[j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
       }
       reinterpret_cast<__half*>(tile + kOffSk<BITS>)[kscale_pos<BITS>(d)] = p.sh;
       reinterpret_cast<__half*>(tile + kOffZk<BITS>)[kscale_pos<BITS>(d)] = p.zh;
@@ -634,21 +655,30 @@ cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void*
     }
   }
   if (c_hi == 0) c_lo = 0;
-  return cv.bits == 2 ? append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st)
-                      : append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+  switch (cv.bits) {
+    case 2: return append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+    case 4: return append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+    default: return append_tokens_bits<8>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+  }
 }
 
 cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const void* v, int dtype, int t_in,
                                     const SeqLens& lens, cudaStream_t st) {
   if (t_in <= 0) return cudaSuccess;
-  return cv.bits == 2 ? prefill_bits<2>(cv, k, v, dtype, t_in, lens, st)
-                      : prefill_bits<4>(cv, k, v, dtype, t_in, lens, st);
+  switch (cv.bits) {
+    case 2: return prefill_bits<2>(cv, k, v, dtype, t_in, lens, st);
+    case 4: return prefill_bits<4>(cv, k, v, dtype, t_in, lens, st);
+    default: return prefill_bits<8>(cv, k, v, dtype, t_in, lens, st);
+  }
 }
 
 cudaError_t launch_append(const CacheView& cv, const void* k, const void* v, int dtype, const SeqLens& lens,
                           cudaStream_t st) {
-  return cv.bits == 2 ? append_bits<2>(cv, k, v, dtype, lens, st)
-                      : append_bits<4>(cv, k, v, dtype, lens, st);
+  switch (cv.bits) {
+    case 2: return append_bits<2>(cv, k, v, dtype, lens, st);
+    case 4: return append_bits<4>(cv, k, v, dtype, lens, st);
+    default: return append_bits<8>(cv, k, v, dtype, lens, st);
+  }
 }
 
 }  // namespace kivi

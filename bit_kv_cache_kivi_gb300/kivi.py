@@ -339,7 +339,9 @@ class KiviCache:
         tile axis kept: codes_k / codes_v [B][H][T/G][G][RB] (u8), scale_k /
         zero_k [B][H][T/G][D] in channel-pair order (see ``key_scale_pos``),
         scale_v / zero_v [B][H][T/G][G * D/G] in token-pair order (see
-        ``value_scale_pos``), fp16 bit patterns as int16; plus the rings."""
+        ``value_scale_pos``), fp16 bit patterns as int16; plus the rings.  At
+        8 bits the code rows are stored rotated by 16-byte chunks (see
+        ``row_chunk_rotation``)."""
         c = self.cfg
         B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
         rb = D * c.bits // 8
@@ -374,6 +376,11 @@ class KiviCache:
         out = {}
         for n, t in lv.items():
             if n in ("codes_k", "codes_v"):
+                if c.bits == 8:  # undo the rows' chunk rotation
+                    idx = torch.tensor([[16 * ((ch + row_chunk_rotation(8, n == "codes_k", r)) % 8) + i
+                                         for ch in range(8) for i in range(16)] for r in range(G)],
+                                       device=dev)
+                    t = torch.gather(t, 4, idx.expand(B, H, t.shape[2], G, 128))
                 out[n] = t.reshape(B, H, T, t.shape[-1])
             elif n in ("scale_k", "zero_k"):
                 out[n] = t.index_select(3, kidx)
@@ -388,8 +395,17 @@ def key_scale_pos(c: int, bits: int) -> int:
     """fp16 slot of channel c in a tile's key scale / zero block: 32-bit word
     i of pair block m holds channels (P m + i, P m + i + P/2), P = 16 at 2 bits
     and 8 at 4 bits (the pairs the score product's B fragments take)."""
-    P = 16 if bits == 2 else 8
+    P = {2: 16, 4: 8, 8: 4}[bits]
     return P * (c // P) + 2 * (c % (P // 2)) + (c % P) // (P // 2)
+
+
+def row_chunk_rotation(bits: int, key: bool, r: int) -> int:
+    """16-byte chunks by which code row r of a tile is rotated: at 8 bits key
+    rows by r & 1, value rows by 2 (r & 3) (logical chunk c sits at chunk
+    (c + rotation) mod 8); none at 2 and 4 bits."""
+    if bits != 8:
+        return 0
+    return (r & 1) if key else 2 * (r & 3)
 
 
 def value_scale_pos(t: int, gp: int) -> int:

@@ -30,7 +30,7 @@
  *     reports a launch error (see kivi_last_cuda_error).
  *   - A handle is not thread-safe; calls on one handle must be serialized
  *     by the caller (the stream orders the device work).
- *   - Supported by this build: bits 2 or 4, group 32, head_dim 128,
+ *   - Supported by this build: bits 2, 4 or 8, group 32, head_dim 128,
  *     residual a multiple of 32, any batch / head counts with
  *     n_q_heads a multiple of n_kv_heads.
  *   - Inputs must be finite and within the fp16 range; every input element
@@ -47,10 +47,15 @@
  *                                  key group, one per channel),
  *                                  value scale [G][D/G], value zero [G][D/G]
  *                                  (one per G channels per token)
+ *           At 8 bits the code rows are stored rotated by whole 16-byte
+ *           chunks (key row r by r & 1 chunks, value row r by 2*(r & 3);
+ *           logical chunk c at chunk (c + rotation) mod 8), so that the
+ *           attention kernel's shared-memory reads avoid bank conflicts.
  *           The f16 arrays are stored in the order the decode-attention
  *           tensor-core fragments take them (G = 32, D = 128):
  *             key scale / zero: 32-bit word i of pair block m holds channels
- *               (P*m + i, P*m + i + P/2), P = 16 at 2 bits, 8 at 4 bits, i.e.
+ *               (P*m + i, P*m + i + P/2), P = 16 at 2 bits, 8 at 4 bits, 4 at
+ *               8 bits, i.e.
  *               channel c is at f16 slot P*(c/P) + 2*(c%(P/2)) + (c%P)/(P/2);
  *             value scale / zero: tokens (8a + r, 8a + r + 4), r < 4, share
  *               32-bit word 4*(4a + r) + g for group g, i.e. token t, group g
@@ -101,7 +106,7 @@ typedef enum { KIVI_POLICY_ALG1 = 0, KIVI_POLICY_SHARED = 1 } kivi_policy;
 /* Cache configuration (veloxquant-mlx "KIVI" usage: bit width, group size,
  * residual length) plus the tensor shape. */
 typedef struct {
-  int bits;        /* 2 or 4 */
+  int bits;        /* 2, 4 or 8 */
   int group;       /* G: 32 in this build */
   int residual;    /* R: fp16 window, a multiple of G */
   int head_dim;    /* D: 128 in this build */

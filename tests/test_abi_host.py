@@ -60,6 +60,8 @@ def test_sizes(K):
     assert s[1] == s[2] == units * 32 * 128 * 2
     s4 = K.kivi_cache_sizes(cfg(K, bits=4))
     assert s4[0] == units * (4096 // 32) * (2 * 32 * 64 + 8 * 128) and s4[1:] == s[1:]
+    s8 = K.kivi_cache_sizes(cfg(K, bits=8))
+    assert s8[0] == units * (4096 // 32) * (2 * 32 * 128 + 8 * 128) and s8[1:] == s[1:]
     # the shared-window policy keeps up to R + G - 1 fp16 tokens: R + G slots
     ss = K.kivi_cache_sizes(cfg(K, policy=1))
     assert ss[0] == s[0] and ss[1] == ss[2] == units * (32 + 32) * 128 * 2
@@ -68,12 +70,12 @@ def test_sizes(K):
 def test_scale_slot_maps_are_permutations(K):
     """The tile's fp16 scale / zero orders are bijections of the 128 slots,
     and keep each 32-channel quarter in place (the tail split relies on it)."""
-    for bits in (2, 4):
+    for bits in (2, 4, 8):
         pos = [K.key_scale_pos(c, bits) for c in range(128)]
         assert sorted(pos) == list(range(128))
         assert all(p // 32 == c // 32 for c, p in enumerate(pos))
         # word i of a pair block: channels (P m + i, P m + i + P/2)
-        P = 16 if bits == 2 else 8
+        P = {2: 16, 4: 8, 8: 4}[bits]
         assert pos[P + 1] == P + 2 and pos[P + 1 + P // 2] == P + 3
     vpos = [K.value_scale_pos(t, g) for t in range(32) for g in range(4)]
     assert sorted(vpos) == list(range(128))
@@ -82,7 +84,7 @@ def test_scale_slot_maps_are_permutations(K):
 
 @pytest.mark.parametrize("bad,status", [
     (dict(policy=2), 1), (dict(policy=-1), 1),
-    (dict(bits=3), 1), (dict(bits=8), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
+    (dict(bits=3), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
 ])
