@@ -241,6 +241,9 @@ struct orc_cache {
   uint8_t *codes_k, *codes_v; /* [B][H][Tcap][rowbytes] */
   uint16_t *sk, *zk; /* [B][H][Tcap/G][D] */
   uint16_t *sv, *zv; /* [B][H][Tcap][D/G] */
+  int n_out;         /* fp16 outlier key channels per key group (0: none) */
+  uint8_t *oidx;     /* [B][H][Tcap/G][n_out] channels, largest first */
+  uint16_t *oval;    /* [B][H][Tcap][n_out] their fp16 values */
 };
 
 orc_cache *orc_cache_new(int bits, int G, int R, int D, int B, int Hkv,
@@ -287,8 +290,34 @@ void orc_cache_free(orc_cache *c) {
   free(c->zk);
   free(c->sv);
   free(c->zv);
+  free(c->oidx);
+  free(c->oval);
   free(c);
 }
+
+/* Outlier-aware keys ([NB] Exercises, item 2: keep the top-1% of K channels
+ * at fp16 and quantise the rest).  Reading: per key group (G tokens; every
+ * channel is its own quantization group), the n_out channels with the
+ * largest max |x| over the group's tokens are kept as fp16 values, chosen
+ * largest first, ties to the lower channel.  Their codes, scales and zeros
+ * are stored as 0, so the packed group decodes to 0 on them, and the decoded
+ * key takes the kept value.  The other channels are quantized as without
+ * outliers.  On an empty cache only; n_out in [0, 8]. */
+int orc_cache_set_outliers(orc_cache *c, int n_out) {
+  if (c->l != 0 || n_out < 0 || n_out > 8 || n_out > c->D) return -1;
+  free(c->oidx);
+  free(c->oval);
+  c->oidx = NULL;
+  c->oval = NULL;
+  c->n_out = n_out;
+  if (n_out == 0) return 0;
+  size_t units = (size_t)c->B * c->H;
+  c->oidx = calloc(units * (c->Tcap / c->G) * n_out, 1);
+  c->oval = calloc(units * c->Tcap * n_out, sizeof(uint16_t));
+  return c->oidx && c->oval ? 0 : -1;
+}
+
+int orc_cache_outliers(const orc_cache *c) { return c->n_out; }
 
 long orc_cache_length(const orc_cache *c) { return c->l; }
 
@@ -309,6 +338,33 @@ static void quantize_k_group(orc_cache *c, int b, int h, long t0) {
     orc_quantize_group(x + d, G, D, c->bits, codes + d, D,
                        &c->sk[(u * (c->Tcap / G) + g) * D + d],
                        &c->zk[(u * (c->Tcap / G) + g) * D + d], NULL);
+  }
+  if (c->n_out > 0) {
+    float *amax = (float *)malloc((size_t)D * sizeof(float));
+    char *chosen = (char *)calloc((size_t)D, 1);
+    for (int d = 0; d < D; d++) {
+      float m = 0.0f;
+      for (int i = 0; i < G; i++) {
+        float a = fabsf(orc_f16_to_f32(x[(size_t)i * D + d]));
+        if (a > m) m = a;
+      }
+      amax[d] = m;
+    }
+    for (int o = 0; o < c->n_out; o++) {
+      int best = -1;
+      for (int d = 0; d < D; d++)
+        if (!chosen[d] && (best < 0 || amax[d] > amax[best])) best = d;
+      chosen[best] = 1;
+      c->oidx[(u * (c->Tcap / G) + g) * c->n_out + o] = (uint8_t)best;
+      c->sk[(u * (c->Tcap / G) + g) * D + best] = 0;
+      c->zk[(u * (c->Tcap / G) + g) * D + best] = 0;
+      for (int i = 0; i < G; i++) {
+        codes[(size_t)i * D + best] = 0;
+        c->oval[(u * c->Tcap + t0 + i) * c->n_out + o] = x[(size_t)i * D + best];
+      }
+    }
+    free(amax);
+    free(chosen);
   }
   for (int i = 0; i < G; i++)
     orc_pack_row(codes + (size_t)i * D, D, c->bits,
@@ -432,6 +488,20 @@ void orc_cache_export(const orc_cache *c, uint8_t *codes_k, uint16_t *scale_k,
   }
 }
 
+/* The outlier channels and values of the quantized key groups / rows
+ * (zeros elsewhere): idx [B][H][Tcap/G][n_out], val [B][H][Tcap][n_out]. */
+void orc_cache_export_outliers(const orc_cache *c, uint8_t *idx, uint16_t *val) {
+  const int G = c->G, n = c->n_out;
+  const size_t units = (size_t)c->B * c->H;
+  if (n == 0) return;
+  memset(idx, 0, units * (c->Tcap / G) * n);
+  memset(val, 0, units * c->Tcap * n * 2);
+  for (size_t u = 0; u < units; u++) {
+    memcpy(idx + u * (c->Tcap / G) * n, c->oidx + u * (c->Tcap / G) * n, (size_t)(c->nqk / G) * n);
+    memcpy(val + u * c->Tcap * n, c->oval + u * c->Tcap * n, (size_t)c->nqk * n * 2);
+  }
+}
+
 /* K-hat and V-hat of one (b, h): quantized rows decoded from the packed
  * bytes ([VQ] recon = q * scale + zero), residual rows widened from fp16. */
 void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
@@ -448,6 +518,9 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
         khat[t * D + d] =
             orc_dequant(codes[d], c->sk[(u * (c->Tcap / G) + g) * D + d],
                         c->zk[(u * (c->Tcap / G) + g) * D + d]);
+      for (int o = 0; o < c->n_out; o++)
+        khat[t * D + c->oidx[(u * (c->Tcap / G) + g) * c->n_out + o]] =
+            orc_f16_to_f32(c->oval[(u * c->Tcap + t) * c->n_out + o]);
     } else {
       for (int d = 0; d < D; d++)
         khat[t * D + d] = orc_f16_to_f32(c->x16_k[(u * c->Tcap + t) * D + d]);

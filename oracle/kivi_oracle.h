@@ -89,6 +89,11 @@ int orc_cache_append(orc_cache *c, const void *k1, const void *v1, int dtype);
 
 /* Copy the cache state out in the storage layout above.  Any pointer may be
  * NULL.  Rows/slots that hold no live token are written as zero. */
+/* Outlier-aware keys (fp16 outlier channels per key group); see the .c. */
+int orc_cache_set_outliers(orc_cache *c, int n_out);
+int orc_cache_outliers(const orc_cache *c);
+void orc_cache_export_outliers(const orc_cache *c, uint8_t *idx, uint16_t *val);
+
 void orc_cache_export(const orc_cache *c, uint8_t *codes_k, uint16_t *scale_k,
                       uint16_t *zero_k, uint8_t *codes_v, uint16_t *scale_v,
                       uint16_t *zero_v, uint16_t *ring_k, uint16_t *ring_v);

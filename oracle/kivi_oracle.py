@@ -67,6 +67,9 @@ def lib():
                 "orc_cache_prefill": (i32, [vp, vp, vp, i32, i64]),
                 "orc_cache_append": (i32, [vp, vp, vp, i32]),
                 "orc_cache_export": (None, [vp] * 9),
+                "orc_cache_set_outliers": (i32, [vp, i32]),
+                "orc_cache_outliers": (i32, [vp]),
+                "orc_cache_export_outliers": (None, [vp, vp, vp]),
                 "orc_cache_dequant": (None, [vp, i32, i32, vp, vp]),
                 "orc_decode_attention": (i32, [vp, vp, i32, f32, vp]),
                 "orc_attention_f64": (None, [vp, vp, vp, i64, i32, C.c_double, vp]),
@@ -173,13 +176,16 @@ class OracleCache:
 
     def __init__(self, bits: int, group: int, residual: int, head_dim: int,
                  batch: int, n_kv_heads: int, max_tokens: int,
-                 policy: int = POLICY_ALG1):
+                 policy: int = POLICY_ALG1, outliers: int = 0):
         self.bits, self.G, self.R, self.D = bits, group, residual, head_dim
         self.B, self.H, self.Tcap, self.policy = batch, n_kv_heads, max_tokens, policy
         self._h = lib().orc_cache_new(bits, group, residual, head_dim, batch,
                                       n_kv_heads, max_tokens, policy)
         if not self._h:
             raise ValueError("oracle rejected the cache configuration")
+        self.outliers = outliers
+        if outliers and lib().orc_cache_set_outliers(self._h, outliers) != 0:
+            raise ValueError("oracle rejected the outlier count")
 
     def __del__(self):
         h = getattr(self, "_h", None)
@@ -226,6 +232,11 @@ class OracleCache:
         order = ["codes_k", "scale_k", "zero_k", "codes_v", "scale_v", "zero_v",
                  "ring_k", "ring_v"]
         lib().orc_cache_export(self._h, *[_p(st[n]) for n in order])
+        if self.outliers:
+            n = self.outliers
+            st["outl_idx"] = np.zeros((B, H, T // G, n), np.uint8)
+            st["outl_val"] = np.zeros((B, H, T, n), np.uint16)
+            lib().orc_cache_export_outliers(self._h, _p(st["outl_idx"]), _p(st["outl_val"]))
         return st
 
     def dequant(self, b: int, h: int):
