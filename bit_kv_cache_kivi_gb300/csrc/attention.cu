@@ -76,13 +76,6 @@ __device__ __forceinline__ float h_hi(uint32_t w) {
   return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
 }
 
-__device__ __forceinline__ void halves4(uint2 u, float (&f)[4]) {
-  f[0] = h_lo(u.x);
-  f[1] = h_hi(u.x);
-  f[2] = h_lo(u.y);
-  f[3] = h_hi(u.y);
-}
-
 // fp16x2 arithmetic on raw 32-bit registers (round to nearest even).
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -147,6 +140,7 @@ struct TileBuf {
   uint32_t vc[128 * BITS];                // value codes (group-interleaved rows)
   uint32_t sk[64], zk[64];
   uint32_t sv[64], zv[64];
+  uint32_t outl[outlier_block_bytes(kMaxOutliers) / 4];  // outlier block, when the cache keeps outliers
 };
 template <int BITS>
 constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp
@@ -174,6 +168,7 @@ struct TailSmem {
   uint4 krow[kTailTok][16];
   uint4 vrow[kTailTok][16];
   uint32_t kg[2][2][64];                  // scale / zero of the (at most two) key groups
+  uint32_t ko[2][outlier_block_bytes(kMaxOutliers) / 4];  // their outlier blocks
   uint32_t vg[2][2][64];                  // value scale / zero blocks of the (at most two) tiles
   float4 p4[kTailTok];                    // per token: scores, then weights, of the kNH heads
   float mh[kNH], lh[kNH];                 // per head: max and sum of the weights
@@ -201,10 +196,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem));
-}
-
-__device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(smem)), "l"(gmem));
 }
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
@@ -310,6 +301,11 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
   // key scale / zero blocks of the packed key tiles, value scale / zero
   // blocks of the packed value tiles (at most two tiles each)
   const int ngk = (nk + kGroup - 1) / kGroup, ngv = (nv + kGroup - 1) / kGroup;
+  const int ocb = outlier_block_bytes(cv.n_out) / 16;  // 16-byte chunks of an outlier block
+  for (int i = tid; i < ngk * ocb; i += blockDim.x) {
+    const int gi = i / ocb, c = i % ocb;
+    cp_async16(&ts.ko[gi][4 * c], tile_at<BITS>(cv, unit, c0 / kGroup + gi) + kTileBytes<BITS> + 16 * c);
+  }
   for (int i = tid; i < (ngk + ngv) * 32; i += blockDim.x) {
     const bool key = i < ngk * 32;
     const int ii = key ? i : i - ngk * 32;
@@ -386,6 +382,19 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
       acc.y += __shfl_xor_sync(kFull, acc.y, sh);
       acc.z += __shfl_xor_sync(kFull, acc.z, sh);
       acc.w += __shfl_xor_sync(kFull, acc.w, sh);
+    }
+    if (qq == 0 && r < nk && cv.n_out > 0) {
+      // the group's fp16 outlier channels (their packed codes decode to 0)
+      const uint32_t iw = ts.ko[r >> 5][0];
+      const __half* ov = reinterpret_cast<const __half*>(&ts.ko[r >> 5][4]);
+      for (int o = 0; o < cv.n_out; ++o) {
+        const float x = __half2float(ov[(r & 31) * cv.n_out + o]);
+        const float4 qv = ts.q4[(iw >> (8 * o)) & 0xffu];
+        acc.x = fmaf(x, qv.x, acc.x);
+        acc.y = fmaf(x, qv.y, acc.y);
+        acc.z = fmaf(x, qv.z, acc.z);
+        acc.w = fmaf(x, qv.w, acc.w);
+      }
     }
     if (qq == 0 && r < n) ts.p4[r] = acc;
   }
@@ -589,7 +598,7 @@ __device__ __forceinline__ int pbuf_pos(int t) {
 // ks = 2^E_tig * scale * log2(e).
 template <int BITS>
 __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileBuf<BITS>& tb, int g, int tig,
-                                           float ks, float (&sc)[4]) {
+                                           float ks, int n_out, float scale_log2, float (&sc)[4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
   // ---- beta = zK x q: every A row is the zero vector, so D[., (tig, part)] = beta ----
   float beta4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -672,6 +681,21 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
     }
     sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
     sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
+  }
+  if (n_out > 0) {
+    // fp16 outlier channels (their codes, scales and zeros are 0 above)
+    const uint32_t iw = tb.outl[0];
+    const __half* ov = reinterpret_cast<const __half*>(&tb.outl[4]);  // [32 tokens][n_out]
+#pragma unroll
+    for (int o = 0; o < kMaxOutliers; ++o)
+      if (o < n_out) {
+        const float qo = ws.qv[tig][(iw >> (8 * o)) & 0xffu] * scale_log2;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int t = 16 * (r >> 1) + g + 8 * (r & 1);
+          sc[r] = fmaf(qo, __half2float(ov[t * n_out + o]), sc[r]);
+        }
+      }
   }
 }
 
@@ -881,8 +905,8 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float
 }
 
 // The stage buffer mirrors the packed tile byte for byte.
-static_assert(sizeof(TileBuf<2>) == kTileBytes<2> && sizeof(TileBuf<4>) == kTileBytes<4> &&
-                  sizeof(TileBuf<8>) == kTileBytes<8>, "stage = tile");
+static_assert(offsetof(TileBuf<2>, outl) == kTileBytes<2> && offsetof(TileBuf<4>, outl) == kTileBytes<4> &&
+                  offsetof(TileBuf<8>, outl) == kTileBytes<8>, "stage = tile (+ the largest outlier block)");
 static_assert(offsetof(TileBuf<8>, vc) == kOffVc<8> && offsetof(TileBuf<8>, sk) == kOffSk<8> &&
               offsetof(TileBuf<8>, zv) == kOffZv<8>, "stage layout (8 bits)");
 static_assert(offsetof(TileBuf<2>, vc) == kOffVc<2> && offsetof(TileBuf<2>, sk) == kOffSk<2> &&
@@ -895,19 +919,20 @@ static_assert(offsetof(TileBuf<4>, vc) == kOffVc<4> && offsetof(TileBuf<4>, sk) 
 // Copy source of one (batch, kv-head) unit: its first packed tile.
 struct UnitSrc {
   const uint8_t* tiles;
+  uint32_t tile_bytes;
 };
 
 template <int BITS>
 __device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
-  return UnitSrc{tile_at<BITS>(cv, unit, 0)};
+  return UnitSrc{tile_at<BITS>(cv, unit, 0), (uint32_t)cv.tile_bytes};
 }
 
 // One bulk copy of packed tile `tile` into a stage (one lane).
 template <int BITS>
 __device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long* bar, const UnitSrc& u,
                                            int tile) {
-  mbar_expect_tx(bar, (uint32_t)kTileBytes<BITS>);
-  bulk_g2s(&tb, u.tiles + (long)tile * kTileBytes<BITS>, (uint32_t)kTileBytes<BITS>, bar);
+  mbar_expect_tx(bar, u.tile_bytes);
+  bulk_g2s(&tb, u.tiles + (long)tile * u.tile_bytes, u.tile_bytes, bar);
 }
 
 __device__ __forceinline__ void fence_proxy_async() {
@@ -975,7 +1000,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     if (__any_sync(kFull, !ok)) {
       failed = true;
     } else {
-      key_scores<BITS>(ws, st[0], g, tig, ks, sc);
+      key_scores<BITS>(ws, st[0], g, tig, ks, cv.n_out, a.scale_log2, sc);
       softmax_p(sc, pb, g, tig, m_run, lsum, O, Z);
       __syncwarp();
     }
@@ -994,7 +1019,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
           failed = true;
         } else {
           float scn[4];
-          key_scores<BITS>(ws, st[sn], g, tig, ks, scn);
+          key_scores<BITS>(ws, st[sn], g, tig, ks, cv.n_out, a.scale_log2, scn);
           value_acc<BITS>(st[sg], pb, g, tig, O, Z);
           done = k + 1;
           __syncwarp();  // every lane is done with stage sg and the weight buffer

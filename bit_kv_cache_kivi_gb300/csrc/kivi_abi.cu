@@ -44,6 +44,7 @@ kivi_status check_config(const kivi_config* c) {
   if (c->max_tokens <= 0 || c->max_tokens % c->residual) return KIVI_ESHAPE;
   if (c->batch > 65535 || c->n_kv_heads > 4096) return KIVI_ESHAPE;  // grid limits
   if (c->policy != KIVI_POLICY_ALG1 && c->policy != KIVI_POLICY_SHARED) return KIVI_EINVAL;
+  if (c->outlier_channels < 0 || c->outlier_channels > kivi::kMaxOutliers) return KIVI_EINVAL;
   return KIVI_OK;
 }
 
@@ -101,6 +102,9 @@ kivi::CacheView view(const kivi_cache* c) {
   v.Tcap = c->cfg.max_tokens;
   v.bits = c->cfg.bits;
   v.policy = c->cfg.policy;
+  v.n_out = c->cfg.outlier_channels;
+  v.tile_bytes = 2 * c->cfg.group * (c->cfg.head_dim * c->cfg.bits / 8) + 8 * c->cfg.head_dim +
+                 kivi::outlier_block_bytes(c->cfg.outlier_channels);
   return v;
 }
 
@@ -194,7 +198,8 @@ KIVI_API kivi_status kivi_cache_sizes(const kivi_config* cfg, size_t bytes[3]) {
   const size_t T = cfg->max_tokens, D = cfg->head_dim, G = cfg->group;
   // a tile: key and value code rows of G tokens, key scale / zero [D], value
   // scale / zero [G][D / G] (f16)
-  const size_t tile = 2 * G * (D * cfg->bits / 8) + 4 * D * 2;
+  const size_t tile = 2 * G * (D * cfg->bits / 8) + 4 * D * 2 +
+                      (size_t)kivi::outlier_block_bytes(cfg->outlier_channels);
   bytes[0] = units * (T / G) * tile;            // tiles
   bytes[1] = units * ring_slots(*cfg) * D * 2;  // ring_k
   bytes[2] = bytes[1];                          // ring_v

@@ -20,15 +20,18 @@ constexpr int kTailTok = 64;       // tail tokens per tail split
 constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
 
 constexpr int kMaxVarBatch = 1024;  // batch limit for per-sequence lengths
+constexpr int kMaxOutliers = 4;     // fp16 outlier key channels per key group, at most
 
 // Device view of one cache: the packed tile store, the two rings and the shape.
 struct CacheView {
-  uint8_t* tiles;  // [B][H][Tcap / kGroup] tiles of kTileBytes<bits>
+  uint8_t* tiles;  // [B][H][Tcap / kGroup] tiles of tile_bytes
   __half* ring_k;
   __half* ring_v;
   int B, H, R, Tcap, bits;
-  int W;       // ring slots: token t of a unit is in slot t mod W
-  int policy;  // 0: Algorithm 1 of the chooblog KIVI review; 1: shared window
+  int W;           // ring slots: token t of a unit is in slot t mod W
+  int policy;      // 0: Algorithm 1 of the chooblog KIVI review; 1: shared window
+  int n_out;       // fp16 outlier key channels per key group (0..kMaxOutliers)
+  int tile_bytes;  // kTileBytes<bits> + outlier_block_bytes(n_out)
 };
 
 // The lengths of the batch's sequences, passed by value to every launch:
@@ -179,10 +182,17 @@ __host__ __device__ constexpr int vscale_pos(int t, int gp) {
   return 32 * (t / 8) + 8 * (t % 4) + 2 * gp + (t / 4) % 2;
 }
 
+// Outlier-aware keys (the "KIVI - 2-bit KV cache quantisation" notebook,
+// Exercises item 2): with n_out > 0 a tile ends with an outlier block --
+// 16 bytes of channel indices (n_out used, largest max |k| first), then
+// vals[32 tokens][n_out] fp16 -- and those channels' codes, scales and zeros
+// in the tile are 0.
+__host__ __device__ constexpr int outlier_block_bytes(int n_out) { return n_out > 0 ? 16 + 64 * n_out : 0; }
+
 // Tile `tile` (tokens [32 tile, 32 tile + 32)) of unit `unit`.
 template <int BITS>
 __host__ __device__ __forceinline__ uint8_t* tile_at(const CacheView& cv, long unit, long tile) {
-  return cv.tiles + (unit * (cv.Tcap / kGroup) + tile) * (long)kTileBytes<BITS>;
+  return cv.tiles + (unit * (cv.Tcap / kGroup) + tile) * (long)cv.tile_bytes;
 }
 
 // Input dtype codes (same values as kivi_dtype).

@@ -126,6 +126,16 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
   return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
+// Element e (0..7) of 8 halves held as 4 half2, without dynamic register
+// indexing.
+__device__ __forceinline__ __half pick_half(const __half2 (&v)[4], int e) {
+  __half2 p = v[0];
+  p = (e >> 1) == 1 ? v[1] : p;
+  p = (e >> 1) == 2 ? v[2] : p;
+  p = (e >> 1) == 3 ? v[3] : p;
+  return (e & 1) ? __high2half(p) : __low2half(p);
+}
+
 __device__ __forceinline__ uint4 h2x4_bits(const __half2 (&v)[4]) {
   return make_uint4(h2_bits(v[0]), h2_bits(v[1]), h2_bits(v[2]), h2_bits(v[3]));
 }
@@ -271,6 +281,54 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
       // codes per 32-bit word, and the correction of a word's magic sum
       constexpr int CW = BITS == 8 ? 4 : 8;
       constexpr uint32_t C = magic_sum(CW, BITS);
+      // Outlier-aware keys: the n_out channels of the group with the largest
+      // max |k| (largest first, ties to the lower channel) stay fp16; their
+      // codes, scales and zeros become 0.  Every lane takes part in each
+      // round's argmax (the two token parities hold the same channels).
+      int och[kMaxOutliers] = {0, 0, 0, 0};
+      uint32_t keep0 = ~0u, keep1 = ~0u;  // code bits of this lane's kept (non-outlier) channels
+      if (cv.n_out > 0) {
+        float am[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          am[2 * i] = fmaxf(fabsf(__low2float(mn[i])), fabsf(__low2float(mx[i])));
+          am[2 * i + 1] = fmaxf(fabsf(__high2float(mn[i])), fabsf(__high2float(mx[i])));
+        }
+        uint32_t mine = 0;  // bit e: channel c8 + e is an outlier
+#pragma unroll
+        for (int o = 0; o < kMaxOutliers; ++o) {
+          if (o < cv.n_out) {
+            float bv = -1.0f;
+            int bc = 0x7fffffff;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (!((mine >> e) & 1u) && am[e] > bv) {
+                bv = am[e];
+                bc = c8 + e;
+              }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) {
+              const float ov = __shfl_xor_sync(kFull, bv, off);
+              const int oc = __shfl_xor_sync(kFull, bc, off);
+              if (ov > bv || (ov == bv && oc < bc)) {
+                bv = ov;
+                bc = oc;
+              }
+            }
+            och[o] = bc;
+            if ((bc >> 3) == cl) mine |= 1u << (bc & 7);
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if ((mine >> e) & 1u) {
+            gp[e].sh = __ushort_as_half((unsigned short)0);
+            gp[e].zh = __ushort_as_half((unsigned short)0);
+            const uint32_t m = ((1u << BITS) - 1u) << (BITS * (e % CW));
+            if (e / CW == 0) keep0 &= ~m;
+            else keep1 &= ~m;
+          }
+      }
       if (safe) {
 #pragma unroll 4
         for (int k = 0; k < 16; ++k) {
@@ -283,14 +341,15 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
             acc[e0 / CW] += code_bits(f.x, zf[e0], sf[e0], inv[e0]) << (BITS * (e0 % CW));
             acc[e1 / CW] += code_bits(f.y, zf[e1], sf[e1], inv[e1]) << (BITS * (e1 % CW));
           }
-          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS], make_uint2(acc[0] - C, acc[1] - C));
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS],
+                                make_uint2((acc[0] - C) & keep0, (acc[1] - C) & keep1));
         }
       } else {
         // a channel group with an fp16-subnormal scale: IEEE division + clamp
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
-          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS],
-                                exact_key_slice<BITS>(h2x4_bits(x), zf, sf));
+          const uint2 ex = exact_key_slice<BITS>(h2x4_bits(x), zf, sf);
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS], make_uint2(ex.x & keep0, ex.y & keep1));
         }
       }
       __syncwarp();
@@ -301,6 +360,24 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
 #pragma unroll
       for (int i = lane; i < 32 * CPRB; i += 32)
         gdst[(i / CPRB) * CPRB + krow_chunk<BITS>(i / CPRB, i % CPRB)] = ssrc[i];
+      if (cv.n_out > 0) {
+        // the outlier block: channel indices, then row `lane`'s kept fp16 values
+        uint8_t* ob = tile + kTileBytes<BITS>;
+#pragma unroll
+        for (int o = 0; o < kMaxOutliers; ++o)
+          if (o < cv.n_out) {
+            __half2 xr[4];
+            smem8<DT>(&s_in[lane * CPR + (och[o] >> 3) * CPE], xr);
+            reinterpret_cast<__half*>(ob + 16)[lane * cv.n_out + o] = pick_half(xr, och[o] & 7);
+          }
+        if (lane == 0) {
+          uint32_t iw = 0;
+#pragma unroll
+          for (int o = 0; o < kMaxOutliers; ++o)
+            if (o < cv.n_out) iw |= (uint32_t)och[o] << (8 * o);
+          *reinterpret_cast<uint4*>(ob) = make_uint4(iw, 0u, 0u, 0u);
+        }
+      }
       {
         // scales (lanes of parity 0) and zeros (parity 1), in the tile's
         // channel-pair order (kscale_pos); the 16-byte store lands at c8 either way
@@ -579,17 +656,68 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
         mn = fminf(mn, xs[j]);
         mx = fmaxf(mx, xs[j]);
       }
-      const GroupParams p = group_params(mn, mx, L);
+      GroupParams p = group_params(mn, mx, L);
       uint8_t* tile = tile_at<BITS>(cv, unit, tb / kGroup + gi);
+      // outlier-aware keys: the n_out channels with the largest max |k| of
+      // the group (largest first, ties to the lower channel) stay fp16
+      int slot = -1;  // this channel's place among the outliers
+      if (cv.n_out > 0) {
+        __shared__ float s_bv[4];
+        __shared__ int s_bc[4];
+        __shared__ int s_ch[kMaxOutliers];
+        const float am = fmaxf(fabsf(mn), fabsf(mx));
+        for (int o = 0; o < cv.n_out; ++o) {
+          float bv = slot >= 0 ? -1.0f : am;
+          int bc = d;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, off);
+            const int oc = __shfl_xor_sync(kFull, bc, off);
+            if (ov > bv || (ov == bv && oc < bc)) {
+              bv = ov;
+              bc = oc;
+            }
+          }
+          if (lane == 0) {
+            s_bv[warp] = bv;
+            s_bc[warp] = bc;
+          }
+          __syncthreads();
+          if (d == 0) {
+            float v = s_bv[0];
+            int c = s_bc[0];
+            for (int w = 1; w < 4; ++w)
+              if (s_bv[w] > v || (s_bv[w] == v && s_bc[w] < c)) {
+                v = s_bv[w];
+                c = s_bc[w];
+              }
+            s_ch[o] = c;
+          }
+          __syncthreads();
+          if (s_ch[o] == d) slot = o;
+        }
+        if (slot >= 0) {
+          p.sh = __ushort_as_half((unsigned short)0);
+          p.zh = __ushort_as_half((unsigned short)0);
+          __half* ov = reinterpret_cast<__half*>(tile + kTileBytes<BITS> + 16);
+          for (int j = 0; j < kGroup; ++j) ov[j * cv.n_out + slot] = ringk[(gi * kGroup + j) * kHeadDim + d];
+        }
+        if (d == 0) {
+          uint32_t iw = 0;
+          for (int o = 0; o < cv.n_out; ++o) iw |= (uint32_t)s_ch[o] << (8 * o);
+          *reinterpret_cast<uint4*>(tile + kTileBytes<BITS>) = make_uint4(iw, 0u, 0u, 0u);
+        }
+      }
 #pragma unroll
       for (int j = 0; j < kGroup; ++j) {
-        uint32_t q = encode(xs[j], p, L) << (BITS * (d % PER_BYTE));
+        uint32_t q = (slot >= 0 ? 0u : encode(xs[j], p, L)) << (BITS * (d % PER_BYTE));
 #pragma unroll
         for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
         if (d % PER_BYTE == 0) tile[j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
       }
       reinterpret_cast<__half*>(tile + kOffSk<BITS>)[kscale_pos<BITS>(d)] = p.sh;
       reinterpret_cast<__half*>(tile + kOffZk<BITS>)[kscale_pos<BITS>(d)] = p.zh;
+      if (cv.n_out > 0) __syncthreads();  // s_ch is reused by the next group
     }
   }
 }

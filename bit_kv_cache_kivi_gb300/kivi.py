@@ -42,7 +42,8 @@ KIVI_POLICY_ALG1, KIVI_POLICY_SHARED = 0, 1
 class kivi_config(C.Structure):
     _fields_ = [("bits", C.c_int), ("group", C.c_int), ("residual", C.c_int),
                 ("head_dim", C.c_int), ("batch", C.c_int), ("n_kv_heads", C.c_int),
-                ("n_q_heads", C.c_int), ("max_tokens", C.c_int), ("policy", C.c_int)]
+                ("n_q_heads", C.c_int), ("max_tokens", C.c_int), ("policy", C.c_int),
+                ("outlier_channels", C.c_int)]
 
 
 class kivi_buffers(C.Structure):
@@ -209,9 +210,9 @@ class KiviCache:
 
     def __init__(self, *, batch: int, n_kv_heads: int, n_q_heads: int, max_tokens: int,
                  bits: int = 2, group: int = 32, residual: int = 32, head_dim: int = 128,
-                 policy: int = 0, device="cuda"):
+                 policy: int = 0, outliers: int = 0, device="cuda"):
         self.cfg = kivi_config(bits, group, residual, head_dim, batch, n_kv_heads,
-                               n_q_heads, max_tokens, policy)
+                               n_q_heads, max_tokens, policy, outliers)
         d = torch.device(device)
         if d.type == "cuda" and d.index is None:
             d = torch.device("cuda", torch.cuda.current_device())
@@ -318,6 +319,11 @@ class KiviCache:
     def reset(self) -> None:
         kivi_cache_reset(self.handle)
 
+    def _tile_bytes(self) -> int:
+        c = self.cfg
+        n = c.outlier_channels
+        return 2 * c.group * (c.head_dim * c.bits // 8) + 8 * c.head_dim + (16 + 64 * n if n else 0)
+
     def _ring_slots(self) -> int:
         c = self.cfg
         return c.residual + c.group if c.policy == KIVI_POLICY_SHARED else c.residual
@@ -328,7 +334,7 @@ class KiviCache:
         [B][H][T/G][tile bytes], the rings as fp16 bit patterns (int16)."""
         c = self.cfg
         B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
-        tb = 2 * G * (D * c.bits // 8) + 8 * D
+        tb = self._tile_bytes()
         W = self._ring_slots()
         return {"tiles": self.buffers["tiles"][:B * H * (T // G) * tb].view(B, H, T // G, tb),
                 "ring_k": self.buffers["ring_k"][:2 * B * H * W * D].view(torch.int16).view(B, H, W, D),
@@ -345,7 +351,7 @@ class KiviCache:
         c = self.cfg
         B, H, T, D, G = c.batch, c.n_kv_heads, c.max_tokens, c.head_dim, c.group
         rb = D * c.bits // 8
-        tb = 2 * G * rb + 8 * D
+        tb = self._tile_bytes()
         nt = T // G
         u8 = self.buffers["tiles"]
         i16 = u8[:(u8.numel() // 2) * 2].view(torch.int16)
@@ -358,6 +364,11 @@ class KiviCache:
                "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 2 * D) // 2),
                "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 4 * D) // 2),
                "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 6 * D) // 2)}
+        n = c.outlier_channels
+        if n:  # the outlier block after the base tile: indices, then values [G][n]
+            o_ob = 2 * G * rb + 8 * D
+            out["outl_idx"] = u8.as_strided((B, H, nt, n), st8 + (1,), o_ob)
+            out["outl_val"] = i16.as_strided((B, H, nt, G, n), st16 + (n, 1), (o_ob + 16) // 2)
         sv = self.state_views()
         out["ring_k"], out["ring_v"] = sv["ring_k"], sv["ring_v"]
         return out
@@ -386,6 +397,8 @@ class KiviCache:
                 out[n] = t.index_select(3, kidx)
             elif n in ("scale_v", "zero_v"):
                 out[n] = t.index_select(3, vidx).reshape(B, H, T, D // G)
+            elif n == "outl_val":
+                out[n] = t.reshape(B, H, T, t.shape[-1])
             else:
                 out[n] = t.clone()
         return out

@@ -47,6 +47,11 @@
  *                                  key group, one per channel),
  *                                  value scale [G][D/G], value zero [G][D/G]
  *                                  (one per G channels per token)
+ *           With kivi_config.outlier_channels = n > 0, a tile ends with an
+ *           outlier block of 16 + 64*n bytes: the n channel indices (u8,
+ *           largest max |k| first, zero padded to 16 bytes), then
+ *           value[G][n] (f16) -- the tile's fp16 outlier keys; those
+ *           channels' codes, key scales and key zeros in the tile are 0.
  *           At 8 bits the code rows are stored rotated by whole 16-byte
  *           chunks (key row r by r & 1 chunks, value row r by 2*(r & 3);
  *           logical chunk c at chunk (c + rotation) mod 8), so that the
@@ -115,6 +120,10 @@ typedef struct {
   int n_q_heads;   /* a multiple of n_kv_heads; query head j reads KV head j/(Hq/H) */
   int max_tokens;  /* capacity T, a multiple of R */
   int policy;      /* kivi_policy: KIVI_POLICY_ALG1 (0) or KIVI_POLICY_SHARED */
+  int outlier_channels; /* 0..4: per key group, this many channels with the
+                         * largest max |k| stay fp16 (the "KIVI - 2-bit KV
+                         * cache quantisation" notebook, Exercises item 2);
+                         * 0 = plain KIVI */
 } kivi_config;
 
 /* The three caller-owned device buffers, in the layout above. */

@@ -26,21 +26,21 @@ def nq_v(l, R, G=32, policy=ALG1):
 
 
 def gpu_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None,
-              policy: int = ALG1):
+              policy: int = ALG1, outliers: int = 0):
     from bit_kv_cache_kivi_gb300.kivi import KiviCache
     return KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq,
                      max_tokens=capacity or wl.capacity, bits=bits or wl.bits,
-                     group=wl.G, residual=wl.R, head_dim=wl.D, policy=policy)
+                     group=wl.G, residual=wl.R, head_dim=wl.D, policy=policy, outliers=outliers)
 
 
 def oracle_cache(wl: W.Workload, capacity: int | None = None, bits: int | None = None,
-                 units=None, policy: int = ALG1):
+                 units=None, policy: int = ALG1, outliers: int = 0):
     """Oracle cache of the whole batch, or of the (b, h) units listed (B=1, H=1 each)."""
     from oracle.kivi_oracle import OracleCache
     cap = capacity or wl.capacity
     if units is None:
-        return OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, wl.B, wl.Hkv, cap, policy)
-    return [OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, 1, 1, cap, policy) for _ in units]
+        return OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, wl.B, wl.Hkv, cap, policy, outliers)
+    return [OracleCache(bits or wl.bits, wl.G, wl.R, wl.D, 1, 1, cap, policy, outliers) for _ in units]
 
 
 def dev(x: np.ndarray, dtype: str) -> torch.Tensor:
@@ -79,6 +79,9 @@ def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None,
         chk("codes_k", slice(0, qk), slice(0, qk))
         chk("scale_k", slice(0, qk // G), slice(0, qk // G))
         chk("zero_k", slice(0, qk // G), slice(0, qk // G))
+        if "outl_idx" in o:  # outlier-aware keys: the kept channels and values
+            chk("outl_idx", slice(0, qk // G), slice(0, qk // G))
+            chk("outl_val", slice(0, qk), slice(0, qk))
         chk("codes_v", slice(0, qv), slice(0, qv))
         chk("scale_v", slice(0, qv), slice(0, qv))
         chk("zero_v", slice(0, qv), slice(0, qv))

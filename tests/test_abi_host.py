@@ -62,6 +62,9 @@ def test_sizes(K):
     assert s4[0] == units * (4096 // 32) * (2 * 32 * 64 + 8 * 128) and s4[1:] == s[1:]
     s8 = K.kivi_cache_sizes(cfg(K, bits=8))
     assert s8[0] == units * (4096 // 32) * (2 * 32 * 128 + 8 * 128) and s8[1:] == s[1:]
+    # outlier-aware keys: a 16-byte index block and 32 fp16 values per channel per tile
+    so = K.kivi_cache_sizes(cfg(K, outlier_channels=2))
+    assert so[0] == s[0] + units * (4096 // 32) * (16 + 32 * 2 * 2) and so[1:] == s[1:]
     # the shared-window policy keeps up to R + G - 1 fp16 tokens: R + G slots
     ss = K.kivi_cache_sizes(cfg(K, policy=1))
     assert ss[0] == s[0] and ss[1] == ss[2] == units * (32 + 32) * 128 * 2
@@ -83,7 +86,7 @@ def test_scale_slot_maps_are_permutations(K):
 
 
 @pytest.mark.parametrize("bad,status", [
-    (dict(policy=2), 1), (dict(policy=-1), 1),
+    (dict(policy=2), 1), (dict(policy=-1), 1), (dict(outlier_channels=5), 1), (dict(outlier_channels=-1), 1),
     (dict(bits=3), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
