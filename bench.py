@@ -322,6 +322,8 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, ev, peak, which=None
         res.update(attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, 4))
     if want("attn8"):
         res.update(attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, 8))
+    if want("outliers"):
+        res.update(attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, 2, outliers=2))
     if want("long"):
         res.update(long_context(args, torch, W, KiviCache, dev, stream, ev, peak))
     if want("streaming"):
@@ -329,16 +331,16 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, ev, peak, which=None
     return res
 
 
-def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits):
-    """Decode attention of a 4- or 8-bit cache on the Llama-3-8B shape
-    (context 4097)."""
+def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits, outliers=0):
+    """Decode attention of a 2-, 4- or 8-bit cache on the Llama-3-8B shape
+    (context 4097), optionally with fp16 outlier key channels."""
     res = {}
     wl = W.llama3_8b_decode(bits=bits)
     k, v = W.to_torch(wl.k, "f16", dev), W.to_torch(wl.v, "f16", dev)
 
     def new_cache():
         c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.capacity,
-                      bits=bits, residual=wl.R)
+                      bits=bits, residual=wl.R, outliers=outliers)
         c.prefill(k, v)
         c.append(W.to_torch(wl.k_new[0], "f16", dev), W.to_torch(wl.v_new[0], "f16", dev))
         return c
@@ -361,10 +363,14 @@ def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits):
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) * 1e-3 for a, b in recs]
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T + 1, wl.R, bits)
+    if outliers:  # the outlier blocks of the quantized key groups
+        nbytes += wl.B * wl.Hkv * (nq(wl.T + 1, wl.R)[0] // G) * (16 + 64 * outliers)
     gbs = nbytes / np.mean(times) / 1e9
-    res[f"attention_{bits}bit_llama3_8b"] = {
-        "what": f"{bits}-bit decode attention, batch 8, 32/8 heads, context 4097, R 32; "
-                f"{n_rep} cache replicas rotated",
+    key = f"attention_{bits}bit_llama3_8b" + (f"_outliers{outliers}" if outliers else "")
+    res[key] = {
+        "what": f"{bits}-bit decode attention" + (f" with {outliers} fp16 outlier key channels per group"
+                                                   if outliers else "")
+                + f", batch 8, 32/8 heads, context 4097, R 32; {n_rep} cache replicas rotated",
         "splits": caches[0].splits(), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
         "us": round(float(np.mean(times)) * 1e6, 2), "bytes": nbytes}
     del caches, c0
@@ -511,7 +517,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
-    ap.add_argument("--only", choices=["main", "quantize", "attn4", "attn8", "long", "streaming"],
+    ap.add_argument("--only", choices=["main", "quantize", "attn4", "attn8", "outliers", "long", "streaming"],
                     help="run one workload alone (for profiling); prints its numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quant-reps", type=int, default=10)

@@ -59,11 +59,20 @@ int max_len(const kivi_cache* c) {
   return m;
 }
 
-// The lengths as a launch parameter.
-void seq_lens(const kivi_cache* c, kivi::SeqLens* out) {
+// The lengths as a launch parameter, for a launch that appends n tokens to
+// every sequence.
+void seq_lens(const kivi_cache* c, kivi::SeqLens* out, int n = 0) {
   out->uniform = c->uniform ? c->length : -1;
-  if (!c->uniform)
+  out->n = n;
+  if (c->uniform) {
+    const int l = c->length, R = c->cfg.residual, p = c->cfg.policy;
+    out->u_nq[0] = kivi::policy_nq_k(l, R, p);
+    out->u_nq[1] = kivi::policy_nq_v(l, R, p);
+    out->u_nq[2] = kivi::policy_nq_k(l + n, R, p);
+    out->u_nq[3] = kivi::policy_nq_v(l + n, R, p);
+  } else {
     for (int b = 0; b < c->cfg.batch; ++b) out->l[b] = c->lens[b];
+  }
 }
 
 // Every sequence grows by n (host state after a successful launch).
@@ -289,7 +298,7 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
   if (!k_new || !v_new) return KIVI_EINVAL;
   if (max_len(c) >= c->cfg.max_tokens) return KIVI_ECAPACITY;
   kivi::SeqLens sl;
-  seq_lens(c, &sl);
+  seq_lens(c, &sl, 1);
   cudaError_t e;
   if (c->cfg.policy == KIVI_POLICY_SHARED) {
     // the one-token case of the multi-token append: a whole group of keys and
@@ -311,7 +320,7 @@ KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void
   if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
   if ((long)max_len(c) + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
   kivi::SeqLens sl;
-  seq_lens(c, &sl);
+  seq_lens(c, &sl, n_tokens);
   kivi_status st = cuda_status(
       kivi::launch_append_tokens(view(c), k, v, (int)dtype, n_tokens, sl, static_cast<cudaStream_t>(stream)));
   if (st == KIVI_OK) grow(c, n_tokens);

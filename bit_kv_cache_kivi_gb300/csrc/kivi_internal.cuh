@@ -38,6 +38,8 @@ struct CacheView {
 // one length for all, or one per sequence (batch <= kMaxVarBatch).
 struct SeqLens {
   int uniform;  // >= 0: every sequence has this length; -1: l[b]
+  int n;        // tokens the launch appends to each sequence (0 for attention)
+  int u_nq[4];  // uniform: nq_k(l), nq_v(l), nq_k(l + n), nq_v(l + n)
   int l[kMaxVarBatch];
 };
 
@@ -55,6 +57,18 @@ __host__ __device__ __forceinline__ int policy_nq_k(int l, int R, int policy) {
 __host__ __device__ __forceinline__ int policy_nq_v(int l, int R, int policy) {
   if (policy == 1) return policy_nq_k(l, R, policy);
   return l > R ? l - R : 0;
+}
+
+// Quantized counts of sequence b before and after the launch's n tokens:
+// nq_k(l), nq_v(l), nq_k(l + n), nq_v(l + n) (precomputed when uniform).
+__device__ __forceinline__ void seq_counts(const SeqLens& s, int b, int R, int policy, int (&c)[4]) {
+  if (s.uniform >= 0) {
+    c[0] = s.u_nq[0], c[1] = s.u_nq[1], c[2] = s.u_nq[2], c[3] = s.u_nq[3];
+  } else {
+    const int l = s.l[b];
+    c[0] = policy_nq_k(l, R, policy), c[1] = policy_nq_v(l, R, policy);
+    c[2] = policy_nq_k(l + s.n, R, policy), c[3] = policy_nq_v(l + s.n, R, policy);
+  }
 }
 
 // Split configuration of a cache (a function of its shape): the one-wave

@@ -226,7 +226,7 @@ __device__ __forceinline__ int vswz(int r, int c) {
 //           the two parities' min/max meet in one shuffle;
 //   values: lane l owns, in round rr, the whole 32-channel group l%4 of row
 //           8*rr + l/4, so min, max and the scale are computed once per group.
-template <int BITS, int DT>
+template <int BITS, int DT, bool OUTL>
 __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4* s_in, uint8_t* s_codes,
                                                long unit, int chunk, int T, bool kq, int kring, int vlo,
                                                int vhi, int vring) {
@@ -287,7 +287,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
       // round's argmax (the two token parities hold the same channels).
       int och[kMaxOutliers] = {0, 0, 0, 0};
       uint32_t keep0 = ~0u, keep1 = ~0u;  // code bits of this lane's kept (non-outlier) channels
-      if (cv.n_out > 0) {
+      if constexpr (OUTL) {
         float am[8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -341,15 +341,17 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
             acc[e0 / CW] += code_bits(f.x, zf[e0], sf[e0], inv[e0]) << (BITS * (e0 % CW));
             acc[e1 / CW] += code_bits(f.y, zf[e1], sf[e1], inv[e1]) << (BITS * (e1 % CW));
           }
-          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS],
-                                make_uint2((acc[0] - C) & keep0, (acc[1] - C) & keep1));
+          uint2 cw = make_uint2(acc[0] - C, acc[1] - C);
+          if constexpr (OUTL) cw = make_uint2(cw.x & keep0, cw.y & keep1);
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS], cw);
         }
       } else {
         // a channel group with an fp16-subnormal scale: IEEE division + clamp
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
           const uint2 ex = exact_key_slice<BITS>(h2x4_bits(x), zf, sf);
-          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS], make_uint2(ex.x & keep0, ex.y & keep1));
+          store_key_slice<BITS>(&s_codes[(2 * k + par) * RB + cl * BITS],
+                                OUTL ? make_uint2(ex.x & keep0, ex.y & keep1) : ex);
         }
       }
       __syncwarp();
@@ -360,7 +362,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
 #pragma unroll
       for (int i = lane; i < 32 * CPRB; i += 32)
         gdst[(i / CPRB) * CPRB + krow_chunk<BITS>(i / CPRB, i % CPRB)] = ssrc[i];
-      if (cv.n_out > 0) {
+      if constexpr (OUTL) {
         // the outlier block: channel indices, then row `lane`'s kept fp16 values
         uint8_t* ob = tile + kTileBytes<BITS>;
 #pragma unroll
@@ -495,10 +497,11 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
 // Prefill: one CTA per (32-token chunk, kv-head, b) stages the chunk's raw
 // key rows (warp 0) and value rows (warp 1) with cp.async and quantizes them
 // (keys of whole groups below nq_k, values below nq_v; the rest to the ring).
-template <int BITS, int DT>
+template <int BITS, int DT, bool OUTL>
 __global__ void __launch_bounds__(64)
 quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
-                        const void* __restrict__ vin, int t_in, const SeqLens lens) {
+                        const void* __restrict__ vin, int t_in, int T_u, int nqk_u, int nqv_u,
+                        const SeqLens lens) {
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int EB = DT == kF32 ? 4 : 2;
   constexpr int CPR = kHeadDim * EB / 16;
@@ -512,9 +515,16 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
   const int chunk = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
-  const int T = seq_len(lens, b);  // this sequence's tokens: the first T of the t_in input rows
-  if (t0 >= T) return;
-  const int nq_k = policy_nq_k(T, cv.R, cv.policy), nq_v = policy_nq_v(T, cv.R, cv.policy);
+  // this sequence's tokens: the first T of the t_in input rows.  A uniform
+  // batch passes T and its counts as plain arguments (reading them from the
+  // lengths parameter cost this kernel a few percent).
+  int T = T_u, nq_k = nqk_u, nq_v = nqv_u;
+  if (T_u < 0) {
+    T = lens.l[b];
+    if (t0 >= T) return;
+    nq_k = policy_nq_k(T, cv.R, cv.policy);
+    nq_v = policy_nq_v(T, cv.R, cv.policy);
+  }
   const int rows = min(32, T - t0);
   {
     const char* src = static_cast<const char*>(warp == 0 ? kin : vin) + (unit * t_in + t0) * (long)(kHeadDim * EB);
@@ -526,7 +536,7 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
     asm volatile("cp.async.wait_group 0;");
     __syncwarp();
   }
-  quantize_chunk<BITS, DT>(cv, s_in, s_codes, unit, chunk, T, t0 + 32 <= nq_k, nq_k, 0, nq_v, nq_v);
+  quantize_chunk<BITS, DT, OUTL>(cv, s_in, s_codes, unit, chunk, T, t0 + 32 <= nq_k, nq_k, 0, nq_v, nq_v);
 }
 
 // Appending n tokens to a cache of length l0 (L = l0 + n), step 1: the key
@@ -535,7 +545,7 @@ quantize_prefill_kernel(CacheView cv, const void* __restrict__ kin,
 // A token t < l0 is read from its ring slot, t >= l0 from the input (rounded
 // to fp16).  Nothing is written to the ring (step 2 does that after every
 // read of this step).  One CTA per (chunk c_lo + blockIdx.x, kv-head, b).
-template <int BITS, int DT>
+template <int BITS, int DT, bool OUTL>
 __global__ void __launch_bounds__(64)
 append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int n, int c_lo,
                        const SeqLens lens) {
@@ -551,8 +561,9 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
   const long unit = (long)b * cv.H + h;
   const int t0 = chunk * 32;
   const int l0 = seq_len(lens, b), L = l0 + n;
-  const int nq_k0 = policy_nq_k(l0, cv.R, cv.policy), nq_k1 = policy_nq_k(L, cv.R, cv.policy);
-  const int nq_v0 = policy_nq_v(l0, cv.R, cv.policy), nq_v1 = policy_nq_v(L, cv.R, cv.policy);
+  int cnt[4];
+  seq_counts(lens, b, cv.R, cv.policy, cnt);
+  const int nq_k0 = cnt[0], nq_v0 = cnt[1], nq_k1 = cnt[2], nq_v1 = cnt[3];
   // this sequence's chunks: those holding [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
   const int lo = min(nq_k0, nq_v0), hi = max(nq_k1, nq_v1);
   if (hi <= lo || t0 + 32 <= lo || t0 >= hi) return;
@@ -574,7 +585,8 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
   }
   __syncwarp();
   const bool kq = t0 >= nq_k0 && t0 + 32 <= nq_k1;
-  quantize_chunk<BITS, kF16>(cv, s_in, s_codes, unit, chunk, L, kq, INT_MAX, max(nq_v0, t0), nq_v1, INT_MAX);
+  quantize_chunk<BITS, kF16, OUTL>(cv, s_in, s_codes, unit, chunk, L, kq, INT_MAX, max(nq_v0, t0), nq_v1,
+                                   INT_MAX);
 }
 
 // Appending n tokens, step 2: the last min(n, W) of them go to their ring
@@ -726,10 +738,20 @@ template <int BITS>
 cudaError_t prefill_bits(const CacheView& cv, const void* k, const void* v, int dtype, int t_in,
                          const SeqLens& lens, cudaStream_t st) {
   const dim3 grid((t_in + 31) / 32, cv.H, cv.B);
-  switch (dtype) {
-    case kF32: quantize_prefill_kernel<BITS, kF32><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
-    case kF16: quantize_prefill_kernel<BITS, kF16><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
-    default: quantize_prefill_kernel<BITS, kBF16><<<grid, 64, 0, st>>>(cv, k, v, t_in, lens); break;
+  const int tu = lens.uniform;
+  // plain caches run the chunk quantizer without the outlier selection
+  if (cv.n_out > 0) {
+    switch (dtype) {
+      case kF32: quantize_prefill_kernel<BITS, kF32, true><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+      case kF16: quantize_prefill_kernel<BITS, kF16, true><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+      default: quantize_prefill_kernel<BITS, kBF16, true><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+    }
+  } else {
+    switch (dtype) {
+      case kF32: quantize_prefill_kernel<BITS, kF32, false><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+      case kF16: quantize_prefill_kernel<BITS, kF16, false><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+      default: quantize_prefill_kernel<BITS, kBF16, false><<<grid, 64, 0, st>>>(cv, k, v, t_in, tu, lens.u_nq[0], lens.u_nq[1], lens); break;
+    }
   }
   return cudaGetLastError();
 }
@@ -749,8 +771,11 @@ cudaError_t append_bits(const CacheView& cv, const void* k, const void* v, int d
 template <int BITS, int DT>
 cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, int n, int c_lo, int c_hi,
                              const SeqLens& lens, cudaStream_t st) {
-  if (c_hi > c_lo)
-    append_quantize_kernel<BITS, DT><<<dim3(c_hi - c_lo, cv.H, cv.B), 64, 0, st>>>(cv, k, v, n, c_lo, lens);
+  if (c_hi > c_lo) {
+    const dim3 grid(c_hi - c_lo, cv.H, cv.B);
+    if (cv.n_out > 0) append_quantize_kernel<BITS, DT, true><<<grid, 64, 0, st>>>(cv, k, v, n, c_lo, lens);
+    else append_quantize_kernel<BITS, DT, false><<<grid, 64, 0, st>>>(cv, k, v, n, c_lo, lens);
+  }
   append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, n, lens);
   return cudaGetLastError();
 }
