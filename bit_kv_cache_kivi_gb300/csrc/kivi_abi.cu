@@ -34,6 +34,26 @@ kivi_status cuda_status(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// A caller buffer that the kernels may read or write directly: device or
+// managed memory, or page-locked host memory, which unified addressing maps
+// into the device's address space at the same address (on a GB300 node the
+// kernels then reach it over NVLink-C2C, with no staging copy).  Pageable
+// host memory is refused before any launch.  Host only; no device work.
+bool device_accessible(const void* p) {
+  cudaPointerAttributes at;
+  const cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // do not leave the error for the next launch check
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return at.devicePointer == p;
+    default: return false;
+  }
+}
+
 kivi_status check_config(const kivi_config* c) {
   if (!c) return KIVI_EINVAL;
   if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KIVI_EINVAL;
@@ -264,6 +284,7 @@ kivi_status prefill(kivi_cache* c, const void* k, const void* v, kivi_dtype dtyp
   }
   if (t_in == 0) return KIVI_OK;
   if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
+  if (!device_accessible(k) || !device_accessible(v)) return KIVI_EINVAL;
   kivi_cache tmp = *c;  // the lengths the launch will produce
   if (lens) set_lens(&tmp, lens);
   else tmp.length = t_in;
@@ -297,13 +318,14 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
   if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (!k_new || !v_new) return KIVI_EINVAL;
   if (max_len(c) >= c->cfg.max_tokens) return KIVI_ECAPACITY;
+  if (c->cfg.policy == KIVI_POLICY_SHARED && (!aligned16(k_new) || !aligned16(v_new))) return KIVI_EINVAL;
+  if (!device_accessible(k_new) || !device_accessible(v_new)) return KIVI_EINVAL;
   kivi::SeqLens sl;
   seq_lens(c, &sl, 1);
   cudaError_t e;
   if (c->cfg.policy == KIVI_POLICY_SHARED) {
     // the one-token case of the multi-token append: a whole group of keys and
     // values is quantized when nq grows, then the token goes to the ring
-    if (!aligned16(k_new) || !aligned16(v_new)) return KIVI_EINVAL;
     e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, 1, sl, static_cast<cudaStream_t>(stream));
   } else {
     e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, sl, static_cast<cudaStream_t>(stream));
@@ -319,6 +341,7 @@ KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void
   if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
   if ((long)max_len(c) + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
+  if (!device_accessible(k) || !device_accessible(v)) return KIVI_EINVAL;
   kivi::SeqLens sl;
   seq_lens(c, &sl, n_tokens);
   kivi_status st = cuda_status(
@@ -424,6 +447,7 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   kivi::SeqLens sl;
   kivi_status ast = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(workspace), &a, &sl);
   if (ast != KIVI_OK) return ast;
+  if (!device_accessible(q) || !device_accessible(out)) return KIVI_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->ws_ready != workspace) {
     const WsLayout w = ws_layout(c->cfg);
@@ -525,6 +549,7 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   kivi::SeqLens sl;
   st = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(ws), &a, &sl);
   if (st != KIVI_OK) return st;
+  if (!device_accessible(q) || !device_accessible(out)) return KIVI_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left; the split counters must
   // start at zero, so clear them on every call (a memset, not an allocation).

@@ -99,8 +99,15 @@ def _check(status: int, what: str) -> None:
         raise KiviError(status, what)
 
 
-def _stream(stream) -> int:
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, device_index: int | None = None) -> int:
+    """The cudaStream_t to launch on: the given stream, else the current
+    stream of the device (read without building a Stream object)."""
     if stream is None:
+        if _raw_stream is not None:
+            return _raw_stream(torch.cuda.current_device() if device_index is None else device_index)
         return torch.cuda.current_stream().cuda_stream
     return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
@@ -223,6 +230,8 @@ class KiviCache:
         bufs = kivi_buffers(*[self.buffers[n].data_ptr() for n in BUFFER_NAMES])
         self.handle = kivi_cache_init(self.cfg, bufs)
         self.ws_bytes = kivi_attention_workspace_bytes(self.handle)
+        self._tok_shape = torch.Size((batch, n_kv_heads, head_dim))
+        self._q_shape = torch.Size((batch, n_q_heads, head_dim))
         self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
 
     def __del__(self):
@@ -242,13 +251,17 @@ class KiviCache:
         """Per-sequence lengths."""
         return kivi_cache_lengths(self.handle, self.cfg.batch)
 
+    def _reachable(self, x: torch.Tensor) -> bool:
+        """On the cache's device, or page-locked host memory (which the
+        kernels read and write directly; the C library checks it again)."""
+        return x.device == self.device or (x.device.type == "cpu" and x.is_pinned())
+
     def _check_kv(self, x: torch.Tensor, T: int | None) -> int:
         c = self.cfg
-        if x.device != self.device or not x.is_contiguous():
-            raise ValueError("K/V must be contiguous tensors on the cache's device")
-        want = (c.batch, c.n_kv_heads, T, c.head_dim) if T is not None else (
-            c.batch, c.n_kv_heads, c.head_dim)
-        if tuple(x.shape) != want:
+        if not self._reachable(x) or not x.is_contiguous():
+            raise ValueError("K/V must be contiguous tensors on the cache's device or in pinned host memory")
+        want = (c.batch, c.n_kv_heads, T, c.head_dim) if T is not None else self._tok_shape
+        if x.shape != want:
             raise ValueError(f"expected shape {want}, got {tuple(x.shape)}")
         if x.dtype not in _TORCH_DTYPE:
             raise ValueError(f"unsupported dtype {x.dtype}")
@@ -270,12 +283,15 @@ class KiviCache:
             kivi_quantize_prefill_varlen(self.handle, k, v, dt, T, lengths, stream)
 
     def append(self, k_new: torch.Tensor, v_new: torch.Tensor, stream=None) -> None:
-        k_new = k_new.reshape(self.cfg.batch, self.cfg.n_kv_heads, self.cfg.head_dim)
-        v_new = v_new.reshape(self.cfg.batch, self.cfg.n_kv_heads, self.cfg.head_dim)
+        shape = self._tok_shape
+        if k_new.shape != shape:
+            k_new = k_new.reshape(shape)
+        if v_new.shape != shape:
+            v_new = v_new.reshape(shape)
         dt = self._check_kv(k_new, None)
         if self._check_kv(v_new, None) != dt:
             raise ValueError("K and V dtypes differ")
-        kivi_append_decode(self.handle, k_new, v_new, dt, stream)
+        kivi_append_decode(self.handle, k_new, v_new, dt, _stream(stream, self.device.index))
 
     def append_tokens(self, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         """Append k, v [B][H][n][D] (n >= 1) to a cache of any length."""
@@ -297,17 +313,19 @@ class KiviCache:
 
     def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
                   softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
-        c = self.cfg
-        if tuple(q.shape) != (c.batch, c.n_q_heads, c.head_dim) or not q.is_contiguous():
-            raise ValueError(f"q must be contiguous {(c.batch, c.n_q_heads, c.head_dim)}")
+        if q.shape != self._q_shape or not q.is_contiguous():
+            raise ValueError(f"q must be contiguous {tuple(self._q_shape)}")
+        if not self._reachable(q):
+            raise ValueError("q must be on the cache's device or in pinned host memory")
         if q.dtype not in _TORCH_DTYPE:
             raise ValueError(f"unsupported q dtype {q.dtype}")
         if out is None:
-            out = torch.empty_like(q)
-        elif out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-            raise ValueError("out must match q")
+            out = torch.empty_like(q, pin_memory=q.device.type == "cpu")
+        elif (out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous()
+              or not self._reachable(out)):
+            raise ValueError("out must match q (and be on the device or in pinned host memory)")
         kivi_decode_attention(self.handle, q, _TORCH_DTYPE[q.dtype], out, softmax_scale,
-                              self.workspace, self.ws_bytes, stream)
+                              self.workspace, self.ws_bytes, _stream(stream, self.device.index))
         return out
 
     def set_splits(self, n: int) -> None:

@@ -22,6 +22,12 @@
  * Conventions shared by every call
  *   - Device memory is owned by the caller; the library never allocates
  *     device memory.  It allocates only the small host handle.
+ *   - Inputs and outputs passed per call (k, v, k_new, v_new, q, out) may be
+ *     device memory or page-locked host memory (cudaHostAlloc /
+ *     cudaHostRegister): under unified addressing the kernels read and write
+ *     such host buffers directly (on a GB300 node over NVLink-C2C), with no
+ *     staging copy.  Pageable host memory is refused with KIVI_EINVAL before
+ *     any launch (checked with cudaPointerGetAttributes).
  *   - All work is asynchronous on the given stream (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  No call synchronizes the
  *     device or reads device memory back.
