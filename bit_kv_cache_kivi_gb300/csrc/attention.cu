@@ -96,13 +96,22 @@ __device__ __forceinline__ uint32_t f2_to_h2(float lo, float hi) {
   return d;
 }
 
+// a * b - c in fp16x2 (one rounding; the negation folds into the FMA)
+__device__ __forceinline__ uint32_t hfms2u(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("{\n\t.reg .b32 nc;\n\tneg.f16x2 nc, %3;\n\tfma.rn.f16x2 %0, %1, %2, nc;\n}"
+      : "=r"(d)
+      : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // x * s for an fp32 x given as an fp16 pair (xa, xb) with x = xa + xb, split
 // again as hi + lo across lanes: a "hi" lane passes (xa = hi(x), xb = 0) and
 // gets fp16(x * s); a "lo" lane passes (xa = lo(x), xb = hi(x)) and gets
 // fp16(xa * s + (xb * s - fp16(xb * s))), the residual of the hi product being
-// exact in fp16.  xbn is -xb.  Three fp16x2 instructions, no select.
-__device__ __forceinline__ uint32_t split_mul(uint32_t xa, uint32_t xb, uint32_t xbn, uint32_t s) {
-  return hfma2u(xa, s, hfma2u(xb, s, hmul2u(xbn, s)));
+// exact in fp16.  Three fp16x2 instructions, no select.
+__device__ __forceinline__ uint32_t split_mul(uint32_t xa, uint32_t xb, uint32_t s) {
+  return hfma2u(xa, s, hfms2u(xb, s, hmul2u(xb, s)));
 }
 
 // Value rows are group-interleaved: the byte unit of channels 32*gp + 4*w ..
@@ -581,7 +590,7 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uin
       for (int wq = 0; wq < 4; ++wq) {
         const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
         bq[w >> 1][w & 1] =
-            split_mul(X0[wq], X1[wq], X1[wq] ^ 0x80008000u, P[word_pos<BITS>(w)]);
+            split_mul(X0[wq], X1[wq], P[word_pos<BITS>(w)]);
       }
     }
   }
@@ -758,14 +767,13 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
       // split_mul operands of this lane's part (see split_mul)
       pa[aa] = part ? l : h;
       const uint32_t pbh = part ? h : 0u;
-      const uint32_t pbn = pbh ^ 0x80008000u;
       // the scale / zero words of token pair (t0, t0 + 4) (see vscale_pos)
       const int pw = 4 * (4 * (2 * kk + aa) + tig);
       const uint4 S = *reinterpret_cast<const uint4*>(tb.sv + pw);  // groups 0..3
-      Pp[0][aa] = split_mul(pa[aa], pbh, pbn, S.x);
-      Pp[1][aa] = split_mul(pa[aa], pbh, pbn, S.y);
-      Pp[2][aa] = split_mul(pa[aa], pbh, pbn, S.z);
-      Pp[3][aa] = split_mul(pa[aa], pbh, pbn, S.w);
+      Pp[0][aa] = split_mul(pa[aa], pbh, S.x);
+      Pp[1][aa] = split_mul(pa[aa], pbh, S.y);
+      Pp[2][aa] = split_mul(pa[aa], pbh, S.z);
+      Pp[3][aa] = split_mul(pa[aa], pbh, S.w);
       az[aa] = tb.zv[pw + (g & 3)];
       if constexpr (BITS == 2) {
         // interleaved word g of a row holds, per byte, channels 4g..4g+3 of groups 0..3
@@ -969,12 +977,14 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   int issued = min(n_mine, kStages);
   // the first tile before the q tables, the other stages after them: at
   // launch every warp of the GPU issues at once, and the first tile (and the
-  // tables) should not queue behind the later stages
-  if (lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
+  // tables) should not queue behind the later stages.  A dependent launch
+  // builds the tables while the append runs and issues every copy after it.
+  if (!a.pdl && lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
   build_q_tables<BITS>(ws, a, qv4);
   __syncthreads();
+  if (a.pdl) grid_dependency_wait();
   if (lane == 0)
-    for (int k = 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
+    for (int k = a.pdl ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
   const float ks = ws.qscale[tig];
   float* pb = &ws.pbuf[warp][0][0];
 
@@ -1205,6 +1215,7 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
   const int path = s < p.tail_splits ? kPathTail : kPathMma;
 
   if (path == kPathTail) {
+    if (a.pdl) grid_dependency_wait();  // the tail reads the rings the append writes
     tail_split<BITS>(cv, a, p, sm, unit, b, j0, nh, p.t_tail + s * kTailTok, s_m, s_l);
   } else {
     // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
@@ -1309,8 +1320,22 @@ cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              (int)sizeof(SplitSmem<BITS>));
   if (e != cudaSuccess) return e;
-  attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a, lens);
-  return cudaGetLastError();
+  if (!a.pdl) {
+    attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a, lens);
+    return cudaGetLastError();
+  }
+  // a programmatic dependent of the kernel before it on the stream
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = grid;
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = sizeof(SplitSmem<BITS>);
+  lc.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = at;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, attn_kernel<BITS>, cv, a, lens);
 }
 
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens, cudaStream_t st) {

@@ -312,14 +312,20 @@ KIVI_API kivi_status kivi_quantize_prefill_varlen(kivi_cache* c, const void* k, 
   return prefill(c, k, v, dtype, max_len, lengths, stream);
 }
 
-KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const void* v_new,
-                                        kivi_dtype dtype, void* stream) {
+namespace {
+
+// The argument checks of a one-token append (before any launch).
+kivi_status append_checks(const kivi_cache* c, const void* k_new, const void* v_new, kivi_dtype dtype) {
   if (!c) return KIVI_EINVAL;
   if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (!k_new || !v_new) return KIVI_EINVAL;
   if (max_len(c) >= c->cfg.max_tokens) return KIVI_ECAPACITY;
   if (c->cfg.policy == KIVI_POLICY_SHARED && (!aligned16(k_new) || !aligned16(v_new))) return KIVI_EINVAL;
-  if (!device_accessible(k_new) || !device_accessible(v_new)) return KIVI_EINVAL;
+  return KIVI_OK;
+}
+
+// The launches of a checked one-token append; the lengths grow on success.
+kivi_status append_launch(kivi_cache* c, const void* k_new, const void* v_new, kivi_dtype dtype, void* stream) {
   kivi::SeqLens sl;
   seq_lens(c, &sl, 1);
   cudaError_t e;
@@ -333,6 +339,16 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
   kivi_status st = cuda_status(e);
   if (st == KIVI_OK) grow(c, 1);
   return st;
+}
+
+}  // namespace
+
+KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const void* v_new,
+                                        kivi_dtype dtype, void* stream) {
+  const kivi_status chk = append_checks(c, k_new, v_new, dtype);
+  if (chk != KIVI_OK) return chk;
+  if (!device_accessible(k_new) || !device_accessible(v_new)) return KIVI_EINVAL;
+  return append_launch(c, k_new, v_new, dtype, stream);
 }
 
 KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void* v, kivi_dtype dtype,
@@ -429,6 +445,7 @@ kivi_status attn_args(const kivi_cache* c, const void* q, kivi_dtype q_dtype, vo
   a->counters = reinterpret_cast<int*>(ws + w.cnt_off);
   a->counters2 = reinterpret_cast<int*>(ws + w.cnt2_off);
   a->status = reinterpret_cast<int*>(ws + w.status_off);
+  a->pdl = 0;
   return KIVI_OK;
 }
 
@@ -455,6 +472,39 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
     if (z != KIVI_OK) return z;
     c->ws_ready = workspace;
   }
+  return cuda_status(kivi::launch_attention(view(c), a, sl, st));
+}
+
+KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const void* v_new,
+                                      kivi_dtype kv_dtype, const void* q, kivi_dtype q_dtype, void* out,
+                                      float softmax_scale, void* workspace, size_t ws_bytes,
+                                      void* stream) {
+  // every check of both halves before any launch
+  const kivi_status chk = append_checks(c, k_new, v_new, kv_dtype);
+  if (chk != KIVI_OK) return chk;
+  if (!dtype_ok(q_dtype)) return KIVI_EDTYPE;
+  if (!q || !out) return KIVI_EINVAL;
+  if (!workspace || !aligned16(workspace) || ws_bytes < kivi_attention_workspace_bytes(c))
+    return KIVI_EWORKSPACE;
+  if (!device_accessible(k_new) || !device_accessible(v_new) || !device_accessible(q) ||
+      !device_accessible(out))
+    return KIVI_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (c->ws_ready != workspace) {
+    // before the append, so that the attention's only predecessor is the append
+    const WsLayout w = ws_layout(c->cfg);
+    kivi_status z =
+        cuda_status(cudaMemsetAsync(static_cast<char*>(workspace) + w.cnt_off, 0, w.total - w.cnt_off, st));
+    if (z != KIVI_OK) return z;
+    c->ws_ready = workspace;
+  }
+  kivi_status s1 = append_launch(c, k_new, v_new, kv_dtype, stream);
+  if (s1 != KIVI_OK) return s1;
+  kivi::AttnArgs a;
+  kivi::SeqLens sl;
+  kivi_status ast = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(workspace), &a, &sl);
+  if (ast != KIVI_OK) return ast;  // not reached: every sequence holds a token now
+  a.pdl = 1;
   return cuda_status(kivi::launch_attention(view(c), a, sl, st));
 }
 

@@ -252,7 +252,23 @@ struct AttnArgs {
   int* counters;      // [gid][merge_groups] CTAs finished per split group; 0 between calls
   int* counters2;     // [gid] split groups finished; 0 between calls
   int* status;        // set nonzero when a bounded wait for staged data timed out
+  // Nonzero when the launch is a programmatic dependent of the append kernel
+  // just before it on the stream: the CTAs may start while the append runs,
+  // load q and build their tables, and wait for the append's completion
+  // (griddepcontrol.wait) before reading the cache.
+  int pdl;
 };
+
+// Programmatic dependent launch (sm_90+).  The primary kernel lets its
+// dependent start early; the dependent waits for the primary's completion and
+// memory visibility before touching what the primary writes.  Both are no-ops
+// when the launch has no programmatic dependency.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
                              cudaStream_t st);

@@ -596,6 +596,7 @@ template <int DT>
 __global__ void __launch_bounds__(128)
 append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int n,
                    const SeqLens lens) {
+  grid_launch_dependents();  // a decode step's attention may start its prologue
   const int m = min(n, cv.W);
   const int i = n - m + blockIdx.x;  // input row
   const int h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
@@ -619,6 +620,7 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int PER_BYTE = 8 / BITS;
+  grid_launch_dependents();  // a decode step's attention may start its prologue
   const int h = blockIdx.x, b = blockIdx.y;
   const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const long unit = (long)b * cv.H + h;

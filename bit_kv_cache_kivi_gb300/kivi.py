@@ -85,6 +85,7 @@ def lib() -> C.CDLL:
                 "kivi_status_string": (C.c_char_p, [i32]),
                 "kivi_last_cuda_error": (i32, []),
                 "kivi_decode_attention_static": (i32, [vp, vp, i32, vp, f32, vp]),
+                "kivi_decode_step": (i32, [vp, vp, vp, i32, vp, i32, vp, f32, vp, sz, vp]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -179,6 +180,15 @@ def kivi_decode_attention(h, q, q_dtype: int, out, softmax_scale: float, workspa
     _check(lib().kivi_decode_attention(h, _ptr(q), q_dtype, _ptr(out), float(softmax_scale),
                                        _ptr(workspace), ws_bytes, _stream(stream)),
            "kivi_decode_attention")
+
+
+def kivi_decode_step(h, k_new, v_new, kv_dtype: int, q, q_dtype: int, out, softmax_scale: float,
+                     workspace, ws_bytes: int, stream=None) -> None:
+    """Append one token, then decode attention over the grown cache; the
+    attention launch overlaps the append (see kivi.h)."""
+    _check(lib().kivi_decode_step(h, _ptr(k_new), _ptr(v_new), kv_dtype, _ptr(q), q_dtype, _ptr(out),
+                                  float(softmax_scale), _ptr(workspace), ws_bytes, _stream(stream)),
+           "kivi_decode_step")
 
 
 def kivi_decode_attention_static(h, q, q_dtype: int, out, softmax_scale: float,
@@ -311,8 +321,7 @@ class KiviCache:
             raise ValueError(f"expected {self.cfg.batch} lengths")
         kivi_cache_set_lengths(self.handle, lengths)
 
-    def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
-                  softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    def _check_q_out(self, q: torch.Tensor, out: torch.Tensor | None) -> torch.Tensor:
         if q.shape != self._q_shape or not q.is_contiguous():
             raise ValueError(f"q must be contiguous {tuple(self._q_shape)}")
         if not self._reachable(q):
@@ -324,8 +333,32 @@ class KiviCache:
         elif (out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous()
               or not self._reachable(out)):
             raise ValueError("out must match q (and be on the device or in pinned host memory)")
+        return out
+
+    def attention(self, q: torch.Tensor, out: torch.Tensor | None = None,
+                  softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+        out = self._check_q_out(q, out)
         kivi_decode_attention(self.handle, q, _TORCH_DTYPE[q.dtype], out, softmax_scale,
                               self.workspace, self.ws_bytes, _stream(stream, self.device.index))
+        return out
+
+    def step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
+             out: torch.Tensor | None = None, softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+        """One decode step: append k_new, v_new ([B][H][D]), then decode
+        attention of q over the grown cache, in one call; the attention's
+        launch and query prologue overlap the append.  Same cache and output
+        as append() followed by attention()."""
+        shape = self._tok_shape
+        if k_new.shape != shape:
+            k_new = k_new.reshape(shape)
+        if v_new.shape != shape:
+            v_new = v_new.reshape(shape)
+        dt = self._check_kv(k_new, None)
+        if self._check_kv(v_new, None) != dt:
+            raise ValueError("K and V dtypes differ")
+        out = self._check_q_out(q, out)
+        kivi_decode_step(self.handle, k_new, v_new, dt, q, _TORCH_DTYPE[q.dtype], out, softmax_scale,
+                         self.workspace, self.ws_bytes, _stream(stream, self.device.index))
         return out
 
     def set_splits(self, n: int) -> None:

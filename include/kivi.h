@@ -245,6 +245,27 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
                                   float softmax_scale, void *workspace,
                                   size_t ws_bytes, void *stream);
 
+/* One decode step (review §1.3 decoding phase: the new token's key and value
+ * are concatenated to the cache, then out = softmax(q K^T * scale) V over all
+ * l + 1 tokens): kivi_append_decode(c, k_new, v_new, kv_dtype) followed by
+ * kivi_decode_attention(c, q, q_dtype, out, ...) on the same stream, with
+ * the same arguments, layouts and results (bit for bit).
+ * The attention is launched as a programmatic dependent of the append's last
+ * kernel: its CTAs start while the append runs, load q and build their query
+ * tables, and wait (griddepcontrol.wait) for the append to complete before
+ * they read the cache, so the attention's launch and prologue overlap the
+ * append.
+ * Errors: every check of both halves is made before any launch (nothing runs
+ * and the length is unchanged on KIVI_EINVAL, KIVI_EDTYPE, KIVI_ECAPACITY or
+ * KIVI_EWORKSPACE).  If the append launches and the attention launch then
+ * fails, the token stays appended (the length grows by one) and the call
+ * returns KIVI_ECUDA. */
+kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
+                             const void *v_new, kivi_dtype kv_dtype,
+                             const void *q, kivi_dtype q_dtype, void *out,
+                             float softmax_scale, void *workspace,
+                             size_t ws_bytes, void *stream);
+
 /* Override the number of context splits (0 = automatic).  The first splits
  * always take the tail of the context that is still fp16 (plus the partial
  * value group before it), 64 tokens each; the others share the packed

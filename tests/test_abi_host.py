@@ -137,6 +137,22 @@ def test_init_validation_and_host_state(K):
         ws = K.kivi_attention_workspace_bytes(h)
         assert lib.kivi_decode_attention(h, 16, K.KIVI_F16, 16, 0.0, 16, ws, None) == K.KIVI_ESTATE
         assert lib.kivi_decode_attention(h, 16, 5, 16, 0.0, 16, ws, None) == K.KIVI_EDTYPE
+        # the decode step makes every check of both halves before any launch
+        # and leaves the length unchanged on a refusal
+        step = lib.kivi_decode_step
+        assert step(None, 16, 16, 1, 16, 1, 16, 0.0, 16, ws, None) == K.KIVI_EINVAL
+        assert step(h, 16, 16, 9, 16, 1, 16, 0.0, 16, ws, None) == K.KIVI_EDTYPE
+        assert step(h, 16, 16, 1, 16, 7, 16, 0.0, 16, ws, None) == K.KIVI_EDTYPE
+        assert step(h, 0, 16, 1, 16, 1, 16, 0.0, 16, ws, None) == K.KIVI_EINVAL
+        assert step(h, 16, 16, 1, 0, 1, 16, 0.0, 16, ws, None) == K.KIVI_EINVAL
+        assert step(h, 16, 16, 1, 16, 1, 0, 0.0, 16, ws, None) == K.KIVI_EINVAL
+        assert step(h, 16, 16, 1, 16, 1, 16, 0.0, 16, ws - 16, None) == K.KIVI_EWORKSPACE
+        assert step(h, 16, 16, 1, 16, 1, 16, 0.0, 24, ws, None) == K.KIVI_EWORKSPACE
+        assert step(h, 16, 16, 1, 16, 1, 16, 0.0, 0, ws, None) == K.KIVI_EWORKSPACE
+        assert lib.kivi_cache_set_length(h, 4096) == K.KIVI_OK
+        assert step(h, 16, 16, 1, 16, 1, 16, 0.0, 16, ws, None) == K.KIVI_ECAPACITY
+        assert K.kivi_cache_length(h) == 4096
+        assert lib.kivi_cache_set_length(h, 0) == K.KIVI_OK
         assert K.kivi_cache_length(None) == -1
         K.kivi_cache_reset(h)
     finally:
