@@ -198,6 +198,94 @@ void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes)
   orc_unpack_row(tmp, D, bits, codes);
 }
 
+/* 3-bit rows.  A 3-bit code does not sit in whole bytes or nibbles, and the
+ * pages print no 3-bit packing (the notebook's bit-width sweep quantizes in
+ * fp32 only), so the storage is this build's choice: two planes per row.
+ *  - Bytes [0, D/4): the low two bits of every code, laid out exactly as a
+ *    2-bit row (keys LSB-first, values group-interleaved).
+ *  - Bytes [D/4, 3D/8): the high bit of every code, in 16-bit units (D =
+ *    128: eight units).  Keys: unit 2W + h (W = 0..3, h = 0..1) holds
+ *    channels 16m + 8h + i for m in {W, W + 4} and i = 0..7, with set
+ *    s = [m >= 4].  Values: unit w (w = 0..7) holds channels 32 gp + 4w + c
+ *    for groups gp = 0..3 and c = 0..3, with set s = gp / 2 and index
+ *    i = 4 (gp mod 2) + c.
+ *  - Inside a unit, (set s, index i) is at bit orc_hi_bit(s, i) =
+ *    2 (i mod 4) + 2 + [i >= 4], plus 8 modulo 16 when s = 1.  The 16 bits
+ *    of a unit are a permutation of its 16 (s, i) pairs.                 */
+int orc_hi_bit(int s, int i) {
+  int p = 2 * (i % 4) + 2 + (i >= 4 ? 1 : 0);
+  return s ? (p + 8) % 16 : p;
+}
+
+/* bit index (from the start of the high plane) of key channel e, D = 128 */
+static int hi_bit_key(int e) {
+  int m = e / 16, h = (e % 16) / 8, i = e % 8;
+  int W = m % 4, s = m / 4;
+  return 16 * (2 * W + h) + orc_hi_bit(s, i);
+}
+
+/* bit index (from the start of the high plane) of value channel e, G = 32 */
+static int hi_bit_value(int e) {
+  int gp = e / 32, w = (e % 32) / 4, c = e % 4;
+  return 16 * w + orc_hi_bit(gp / 2, 4 * (gp % 2) + c);
+}
+
+static void pack_row3(const uint8_t *codes, int D, int G, int value, uint8_t *out) {
+  uint8_t lo[4096];
+  for (int e = 0; e < D; e++) lo[e] = codes[e] & 3;
+  if (value)
+    orc_pack_row_v(lo, D, 2, G, out);
+  else
+    orc_pack_row(lo, D, 2, out);
+  uint8_t *hi = out + D / 4;
+  memset(hi, 0, (size_t)(D / 8));
+  for (int e = 0; e < D; e++) {
+    int bit = value ? hi_bit_value(e) : hi_bit_key(e);
+    hi[bit / 8] |= (uint8_t)(((codes[e] >> 2) & 1) << (bit % 8));
+  }
+}
+
+static void unpack_row3(const uint8_t *in, int D, int G, int value, uint8_t *codes) {
+  if (value)
+    orc_unpack_row_v(in, D, 2, G, codes);
+  else
+    orc_unpack_row(in, D, 2, codes);
+  const uint8_t *hi = in + D / 4;
+  for (int e = 0; e < D; e++) {
+    int bit = value ? hi_bit_value(e) : hi_bit_key(e);
+    codes[e] = (uint8_t)(codes[e] | (((hi[bit / 8] >> (bit % 8)) & 1) << 2));
+  }
+}
+
+/* A key or value row of the cache at any supported width. */
+void orc_pack_key_row(const uint8_t *codes, int D, int bits, uint8_t *out) {
+  if (bits == 3)
+    pack_row3(codes, D, 32, 0, out);
+  else
+    orc_pack_row(codes, D, bits, out);
+}
+
+void orc_unpack_key_row(const uint8_t *in, int D, int bits, uint8_t *codes) {
+  if (bits == 3)
+    unpack_row3(in, D, 32, 0, codes);
+  else
+    orc_unpack_row(in, D, bits, codes);
+}
+
+void orc_pack_value_row(const uint8_t *codes, int D, int bits, int G, uint8_t *out) {
+  if (bits == 3)
+    pack_row3(codes, D, G, 1, out);
+  else
+    orc_pack_row_v(codes, D, bits, G, out);
+}
+
+void orc_unpack_value_row(const uint8_t *in, int D, int bits, int G, uint8_t *codes) {
+  if (bits == 3)
+    unpack_row3(in, D, G, 1, codes);
+  else
+    orc_unpack_row_v(in, D, bits, G, codes);
+}
+
 /* ------------------------------------------------------------------ */
 /* Residual policy.
  * ALG1 ([RV] §3.2.2, Algorithm 1): K grouped part X_K[:l-r], r = l mod R;
@@ -248,9 +336,10 @@ struct orc_cache {
 
 orc_cache *orc_cache_new(int bits, int G, int R, int D, int B, int Hkv,
                          long Tcap, int policy) {
-  if ((bits != 2 && bits != 4 && bits != 8) || G <= 0 || R <= 0 || D <= 0 ||
-      B <= 0 || Hkv <= 0 || Tcap <= 0)
+  if ((bits != 2 && bits != 3 && bits != 4 && bits != 8) || G <= 0 || R <= 0 ||
+      D <= 0 || B <= 0 || Hkv <= 0 || Tcap <= 0)
     return NULL;
+  if (bits == 3 && (D != 128 || G != 32)) return NULL; /* the 3-bit planes */
   if (D % G || R % G || Tcap % G || G % 4 || (D * bits) % 8) return NULL;
   orc_cache *c = (orc_cache *)calloc(1, sizeof *c);
   if (!c) return NULL;
@@ -367,8 +456,8 @@ static void quantize_k_group(orc_cache *c, int b, int h, long t0) {
     free(chosen);
   }
   for (int i = 0; i < G; i++)
-    orc_pack_row(codes + (size_t)i * D, D, c->bits,
-                 c->codes_k + (u * c->Tcap + t0 + i) * c->rowbytes);
+    orc_pack_key_row(codes + (size_t)i * D, D, c->bits,
+                     c->codes_k + (u * c->Tcap + t0 + i) * c->rowbytes);
   free(codes);
 }
 
@@ -384,8 +473,8 @@ static void quantize_v_token(orc_cache *c, int b, int h, long t) {
                        &c->sv[(u * c->Tcap + t) * (D / G) + gg],
                        &c->zv[(u * c->Tcap + t) * (D / G) + gg], NULL);
   }
-  orc_pack_row_v(codes, D, c->bits, G,
-                 c->codes_v + (u * c->Tcap + t) * c->rowbytes);
+  orc_pack_value_row(codes, D, c->bits, G,
+                     c->codes_v + (u * c->Tcap + t) * c->rowbytes);
 }
 
 /* Bring the quantized parts up to the policy's counts for length l.
@@ -511,8 +600,8 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
   uint8_t codes[4096];
   for (long t = 0; t < c->l; t++) {
     if (t < c->nqk) {
-      orc_unpack_row(c->codes_k + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
-                     codes);
+      orc_unpack_key_row(c->codes_k + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
+                         codes);
       long g = t / G;
       for (int d = 0; d < D; d++)
         khat[t * D + d] =
@@ -526,8 +615,8 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
         khat[t * D + d] = orc_f16_to_f32(c->x16_k[(u * c->Tcap + t) * D + d]);
     }
     if (t < c->nqv) {
-      orc_unpack_row_v(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
-                       G, codes);
+      orc_unpack_value_row(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
+                           G, codes);
       for (int d = 0; d < D; d++)
         vhat[t * D + d] =
             orc_dequant(codes[d], c->sv[(u * c->Tcap + t) * (D / G) + d / G],

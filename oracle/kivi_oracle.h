@@ -68,6 +68,17 @@ int orc_v_unit_pos(int unit, int D, int G);
 void orc_pack_row_v(const uint8_t *codes, int D, int bits, int G, uint8_t *out);
 void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes);
 
+/* 3-bit rows: the low two bits of every code as a 2-bit row, then a plane of
+ * high bits in 16-bit units (see the definition in kivi_oracle.c);
+ * orc_hi_bit(s, i) is the bit of (set s, index i) inside a unit. */
+int orc_hi_bit(int s, int i);
+/* A cache's key / value row at any supported width (2, 3, 4, 8): the 3-bit
+ * planes, else orc_pack_row / orc_pack_row_v. */
+void orc_pack_key_row(const uint8_t *codes, int D, int bits, uint8_t *out);
+void orc_unpack_key_row(const uint8_t *in, int D, int bits, uint8_t *codes);
+void orc_pack_value_row(const uint8_t *codes, int D, int bits, int G, uint8_t *out);
+void orc_unpack_value_row(const uint8_t *in, int D, int bits, int G, uint8_t *codes);
+
 /* Token counts held quantized after l tokens under a policy. */
 long orc_nq_k(long l, int R, int G, int policy);
 long orc_nq_v(long l, int R, int G, int policy);

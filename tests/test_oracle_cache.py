@@ -68,6 +68,24 @@ def test_prefill_equals_streaming(oracle, policy):
             assert np.array_equal(got[name], want[name]), (T0, name)
 
 
+@pytest.mark.parametrize("policy", [0, 1])
+def test_prefill_equals_streaming_three_bit(oracle, policy):
+    """The same at 3 bits (the two-plane rows, D = 128, G = 32)."""
+    B, H, T, D, G, R = 1, 2, 130, 128, 32, 32
+    k, v = _rand_kv(B, H, T, D, 43)
+    ref = oracle.OracleCache(3, G, R, D, B, H, 192, policy)
+    ref.prefill(k, v)
+    want = ref.export()
+    for T0 in (0, 1, 31, 32, 33, 64, 97, 129):
+        c = oracle.OracleCache(3, G, R, D, B, H, 192, policy)
+        c.prefill(k[:, :, :T0], v[:, :, :T0])
+        for t in range(T0, T):
+            c.append(np.ascontiguousarray(k[:, :, t]), np.ascontiguousarray(v[:, :, t]))
+        got = c.export()
+        for name in want:
+            assert np.array_equal(got[name], want[name]), (T0, name)
+
+
 def test_determinism(oracle):
     k, v = _rand_kv(1, 2, 70, 128, 9)
     outs = []
@@ -87,7 +105,7 @@ def test_shared_policy_counts(oracle):
         assert nq % 16 == 0 and l - nq >= min(l, 32) and l - nq < 32 + 16
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_cache_dequant_within_bound(oracle, bits):
     """Every quantized element is within its group's bound; residual rows exact."""
     B, H, T, D, G, R = 1, 2, 200, 128, 32, 64

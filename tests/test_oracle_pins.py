@@ -73,7 +73,7 @@ def _brute_codes(x32, z, s, L):
     return np.array(out)
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_rounding_is_nearest_even_brute_force(oracle, bits):
     L = (1 << bits) - 1
     rng = np.random.default_rng(bits)
@@ -93,6 +93,9 @@ def test_exact_ties_round_to_even(oracle):
     codes, s16, z16, _ = oracle.quantize_group(f16([0.0, 0.5, 1.5, 2.5, 3.0]), 2)
     assert oracle.f16_bits_to_f32(s16) == 1.0 and oracle.f16_bits_to_f32(z16) == 0.0
     assert list(codes) == [0, 0, 2, 2, 3]
+    # 3-bit, range 7 -> scale 1: 2.5 -> 2, 3.5 -> 4, 6.5 -> 6
+    codes, s16, _, _ = oracle.quantize_group(f16([0.0, 2.5, 3.5, 6.5, 7.0]), 3)
+    assert oracle.f16_bits_to_f32(s16) == 1.0 and list(codes) == [0, 2, 4, 6, 7]
     # 4-bit, range 15 -> scale 1: 6.5 -> 6, 7.5 -> 8
     codes, _, _, _ = oracle.quantize_group(f16([0.0, 6.5, 7.5, 15.0]), 4)
     assert list(codes) == [0, 6, 8, 15]
@@ -101,7 +104,7 @@ def test_exact_ties_round_to_even(oracle):
     assert oracle.f16_bits_to_f32(s16) == 1.0 and list(codes) == [0, 0, 2, 128, 254, 255]
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_codes_in_range_and_error_bound(oracle, bits):
     """codes in [0, 2^b-1]; |x - xhat| <= s16/2 + L|s32 - s16| (+ fp32 rounding)."""
     L = (1 << bits) - 1
@@ -170,6 +173,44 @@ def test_value_row_interleave(oracle):
     # with one channel group per unit the interleave is the identity
     c = rng.integers(0, 4, 8).astype(np.uint8)
     assert np.array_equal(oracle.pack_row_v(c, 2, G=4), oracle.pack_row(c, 2))
+
+
+def test_three_bit_row_planes(oracle):
+    """3-bit rows (a storage choice; the pages print no 3-bit packing): the
+    low two bits of every code form exactly the 2-bit row, the high bits a
+    16-byte plane in which every channel owns one bit of its declared 16-bit
+    unit, and rows round-trip."""
+    # inside a unit, (set, index) -> bit is a permutation of the 16 bits
+    assert sorted(oracle.hi_bit(s, i) for s in (0, 1) for i in range(8)) == list(range(16))
+    rng = np.random.default_rng(3)
+    for value in (False, True):
+        pack = oracle.pack_value_row if value else oracle.pack_key_row
+        unpack = oracle.unpack_value_row if value else oracle.unpack_key_row
+        lo_row = (lambda c: oracle.pack_row_v(c, 2)) if value else (lambda c: oracle.pack_row(c, 2))
+        owner = {}
+        for e in range(128):
+            one = np.zeros(128, np.uint8)
+            one[e] = 4  # only the high bit of channel e
+            row = pack(one, 3)
+            assert row.size == 48 and not row[:32].any()
+            bits = np.flatnonzero(np.unpackbits(row[32:], bitorder="little"))
+            assert bits.size == 1
+            owner[int(bits[0])] = e
+            unit = int(bits[0]) // 16
+            if value:  # unit w holds channels 32 gp + 4 w + c
+                assert unit == (e % 32) // 4
+            else:      # unit 2 (m mod 4) + h holds channels 16 m + 8 h + i
+                assert unit == 2 * ((e // 16) % 4) + (e % 16) // 8
+        assert sorted(owner) == list(range(128))  # a bijection onto the plane
+        for _ in range(50):
+            c = rng.integers(0, 8, 128).astype(np.uint8)
+            row = pack(c, 3)
+            assert np.array_equal(row[:32], lo_row(c & 3))
+            assert np.array_equal(unpack(row, 128, 3), c)
+    # the other widths are the plain rows
+    c = rng.integers(0, 4, 128).astype(np.uint8)
+    assert np.array_equal(oracle.pack_key_row(c, 2), oracle.pack_row(c, 2))
+    assert np.array_equal(oracle.pack_value_row(c, 2), oracle.pack_row_v(c, 2))
 
 
 def test_key_per_channel_value_per_token_orientation(oracle):
@@ -303,3 +344,11 @@ def test_notebook_quality_checks(oracle):
     assert e4 < g["rel_err_4bit_below"]
     assert g["rel_err_2bit_above"] < e2 < g["rel_err_2bit_below"]
     assert e4 < e2
+    # the notebook's bit-width sweep (16, 8, 4, 3, 2): the error grows as the
+    # width falls, and the step from 3 to 2 bits is the largest
+    e3 = np.linalg.norm(Y - attn(_grouped_fake_quant(oracle, K, 0, 3),
+                                 _grouped_fake_quant(oracle, V, 1, 3))) / np.linalg.norm(Y)
+    e8 = np.linalg.norm(Y - attn(_grouped_fake_quant(oracle, K, 0, 8),
+                                 _grouped_fake_quant(oracle, V, 1, 8))) / np.linalg.norm(Y)
+    assert e8 < e4 < e3 < e2
+    assert e2 - e3 > e3 - e4
