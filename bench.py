@@ -17,7 +17,7 @@ about 5 us per launch on this GPU, reported beside it as
 ``per_launch_events``).  ``ms_per_step`` and ``tokens_per_s`` time the
 one-call decode step (append, then the attention as a programmatic
 dependent).  The same line carries the prefill quantizer on the 32k-token
-bf16 workload (2- and 4-bit), 4- and 8-bit attention, the 131k-token
+bf16 workload (2- and 4-bit), 3-, 4- and 8-bit attention, the 131k-token
 long-context attention and the 2048+512-step streaming decode.
 
 ``--impl reference`` times the CPU oracle (the plain C implementation the
@@ -405,6 +405,8 @@ def extra_workloads(args, torch, W, KiviCache, dev, stream, ev, peak, which=None
             "us": round(tg * 1e6, 2), "us_per_launch_events": round(float(np.mean(times)) * 1e6, 2),
             "bytes": nbytes}
         del c, k, v
+    if want("attn3"):
+        res.update(attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, 3))
     if want("attn4"):
         res.update(attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, 4))
     if want("attn8"):
@@ -619,7 +621,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
-    ap.add_argument("--only", choices=["main", "quantize", "attn4", "attn8", "outliers", "long", "streaming"],
+    ap.add_argument("--only", choices=["main", "quantize", "attn3", "attn4", "attn8", "outliers", "long", "streaming"],
                     help="run one workload alone (for profiling); prints its numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quant-reps", type=int, default=10)

@@ -152,7 +152,7 @@ struct TileBuf {
   uint32_t outl[outlier_block_bytes(kMaxOutliers) / 4];  // outlier block, when the cache keeps outliers
 };
 template <int BITS>
-constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp
+constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp (3 KB / 4-9 KB tiles)
 
 template <int BITS>
 struct WarpSmem {
@@ -345,6 +345,30 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
       // channels 32qq .. 32qq + 31 (kscale_pos keeps them in this block)
       const __half* sk = reinterpret_cast<const __half*>(ts.kg[gi][0]) + 32 * qq;
       const __half* zk = reinterpret_cast<const __half*>(ts.kg[gi][1]) + 32 * qq;
+      if constexpr (BITS == 3) {
+        // low two bits from the 2-bit plane, the high bit from its unit
+        const uint32_t* kr = reinterpret_cast<const uint32_t*>(&ts.krow[r][0]);
+#pragma unroll 4
+        for (int dq = 0; dq < 32; dq += 2) {
+          const float2 sp = make_float2(__half2float(sk[kscale_pos<BITS>(dq)]),
+                                        __half2float(sk[kscale_pos<BITS>(dq + 1)]));
+          const float2 zp = make_float2(__half2float(zk[kscale_pos<BITS>(dq)]),
+                                        __half2float(zk[kscale_pos<BITS>(dq + 1)]));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 32 * qq + dq + u;  // the channel
+            const uint32_t lo = (kr[e >> 4] >> (2 * (e & 15))) & 3u;
+            const uint32_t hi =
+                (kr[kHiPlane3 / 4 + ((e >> 4) & 3)] >> (16 * ((e >> 3) & 1) + hi_bit3(e >> 6, e & 7))) & 1u;
+            const float kx = fmaf((float)(lo | (hi << 2)), u ? sp.y : sp.x, u ? zp.y : zp.x);
+            const float4 qv = ts.q4[e];
+            acc.x = fmaf(kx, qv.x, acc.x);
+            acc.y = fmaf(kx, qv.y, acc.y);
+            acc.z = fmaf(kx, qv.z, acc.z);
+            acc.w = fmaf(kx, qv.w, acc.w);
+          }
+        }
+      } else {
 #pragma unroll
       for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
         const uint32_t cw = cw4[w];
@@ -367,6 +391,7 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
             acc.w = fmaf(kx, qv.w, acc.w);
           }
         }
+      }
       }
     } else if (r < n) {
 #pragma unroll
@@ -440,12 +465,21 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
       const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
       uint32_t cb;
       if constexpr (BITS == 2) cb = row[vpos];
+      else if constexpr (BITS == 3) cb = row[vpos] | ((uint32_t)*reinterpret_cast<const uint16_t*>(row + kHiPlane3 + 2 * ((d & 31) >> 2)) << 8);
       else if constexpr (BITS == 4) cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
       else cb = *reinterpret_cast<const uint32_t*>(row + 4 * vpos);
       const int vs = vscale_pos(r & 31, d >> 5);
       const float sv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][0])[vs]);
       const float zv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][1])[vs]);
-      const float cf = __uint_as_float(((cb >> vsh) & L) | 0x4B000000u) - 8388608.0f;
+      float cf;
+      if constexpr (BITS == 3) {
+        // low two bits from the unit's byte, the high bit from bits 8.. (the high unit)
+        const uint32_t lo = (cb >> (2 * (d & 3))) & 3u;
+        const uint32_t hi = (cb >> (8 + hi_bit3(d >> 6, 4 * ((d >> 5) & 1) + (d & 3)))) & 1u;
+        cf = (float)(lo | (hi << 2));
+      } else {
+        cf = __uint_as_float(((cb >> vsh) & L) | 0x4B000000u) - 8388608.0f;
+      }
       vx = fmaf(cf, sv, zv);
     } else {
       const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
@@ -503,6 +537,21 @@ __device__ __forceinline__ uint32_t ext(uint32_t w, uint32_t w_sh) {
   }
 }
 
+// The 3-bit code at position I (0..7) of a 2-bit word's halves: its low two
+// bits from lo (I < 4) or lo >> 8 (I >= 4), its high bit from hi (I < 4) or
+// hi >> 1 (I >= 4), where hi is the word's high-plane unit arranged so that
+// the high bit sits just above the low bits (see hi_bit3).  Read as fp16 the
+// pair is {c_lo * 4^e * 2^-24, c_hi * 4^e * 2^-24}, e = I mod 4.
+template <int I>
+__device__ __forceinline__ uint32_t ext3(uint32_t lo, uint32_t lo_sh, uint32_t hi, uint32_t hi_sh) {
+  static_assert(I >= 0 && I < 8, "eight code positions per half");
+  constexpr uint32_t ml = 0x00030003u << (2 * (I & 3)), mh = 0x00040004u << (2 * (I & 3));
+  return ((I < 4 ? lo : lo_sh) & ml) | ((I < 4 ? hi : hi_sh) & mh);
+}
+
+// Bytes swapped within each 16-bit half (set 1 of a high-plane unit).
+__device__ __forceinline__ uint32_t swap_half_bytes(uint32_t x) { return __byte_perm(x, 0u, 0x2301); }
+
 // Byte J of a and of b as the fp16 pair {a_J * 2^-24, b_J * 2^-24} (an 8-bit
 // code in the low byte of each half, exponent field zero).
 template <int J>
@@ -512,16 +561,17 @@ __device__ __forceinline__ uint32_t byte_pair(uint32_t a, uint32_t b) {
 
 template <int BITS>
 __host__ __device__ constexpr int code_exp(int i) {
-  return BITS == 2 ? (i <= 4 ? i : i - 5) : (BITS == 4 ? (i & 1) : 0);
+  return BITS == 2 ? (i <= 4 ? i : i - 5) : (BITS == 3 ? (i & 3) : (BITS == 4 ? (i & 1) : 0));
 }
 
 template <int BITS>
 constexpr int kShift = BITS == 2 ? 10 : 8;  // w_sh = w >> kShift
 
-// base^-e(i) as a float
+// base^-e(i) as a float; the base is 2^BITS, and 4 at 3 bits (whose low
+// bits sit on the 2-bit grid, the high bit just above them)
 template <int BITS>
 __host__ __device__ constexpr float code_scale(int i) {
-  return 1.0f / (float)(1 << (BITS * code_exp<BITS>(i)));
+  return 1.0f / (float)(1 << ((BITS == 3 ? 2 : BITS) * code_exp<BITS>(i)));
 }
 
 constexpr float kTwo24 = 16777216.0f;  // undoes the 2^-24 of the subnormal codes
@@ -544,7 +594,7 @@ constexpr float kLazySlack = 1.0f;
 // block `blk` (k-steps 2 blk, 2 blk + 1) is the 4 words from 16 tig + 4 blk.
 template <int BITS>
 __device__ __forceinline__ void pair_words(const uint32_t* vec, int tig, int blk, uint32_t (&P)[8]) {
-  if constexpr (BITS == 2) {
+  if constexpr (BITS == 2 || BITS == 3) {
     const int m = tig + 4 * blk;
     const uint4 wa = *reinterpret_cast<const uint4*>(vec + 8 * m);
     const uint4 wb = *reinterpret_cast<const uint4*>(vec + 8 * m + 4);
@@ -559,14 +609,14 @@ __device__ __forceinline__ void pair_words(const uint32_t* vec, int tig, int blk
 }
 
 template <int BITS>
-constexpr int kBlocks = BITS == 2 ? 2 : 4;       // q-table blocks
+constexpr int kBlocks = BITS <= 3 ? 2 : 4;       // q-table blocks
 template <int BITS>
-constexpr int kQuartersPerBlock = BITS == 2 ? 2 : 1;
+constexpr int kQuartersPerBlock = BITS <= 3 ? 2 : 1;
 
 // Code position of q-table word w (0..15).
 template <int BITS>
 __host__ __device__ constexpr int word_pos(int w) {
-  return BITS == 2 ? (w & 7) : (w & 3);
+  return BITS <= 3 ? (w & 7) : (w & 3);
 }
 
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
@@ -641,9 +691,17 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
     const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * RW;  // key row 16mt + g + 8
     // words of a row this lane reads: tig + 4j at 2 and 4 bits; at 8 bits the
     // 8 words from 8 tig, as two 16-byte chunks of the (rotated) row
-    constexpr int NW = BITS;
+    constexpr int NW = BITS == 3 ? 2 : BITS;
     uint32_t wg[NW], w8[NW], sg[NW], s8[NW];
-    if constexpr (BITS == 8) {
+    if constexpr (BITS == 3) {
+      // low planes: words tig, tig + 4 (as at 2 bits); high plane: word tig,
+      // unit 2 tig + half, holding the high bits of both words
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        wg[j] = rg[tig + 4 * j];
+        w8[j] = r8[tig + 4 * j];
+      }
+    } else if constexpr (BITS == 8) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint4 a0 = reinterpret_cast<const uint4*>(rg)[krow_chunk<8>(g, 2 * tig + h)];
@@ -664,7 +722,21 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
       s8[j] = w8[j] >> kShift<BITS>;
     }
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (BITS == 2) {
+    if constexpr (BITS == 3) {
+      const uint32_t hg0 = rg[kHiPlane3 / 4 + tig], h80 = r8[kHiPlane3 / 4 + tig];
+      const uint32_t hg1 = swap_half_bytes(hg0), h81 = swap_half_bytes(h80);
+      // high sources of word j (set j): h, h >> 1
+      const uint32_t hg[2] = {hg0, hg1}, h8[2] = {h80, h81};
+      const uint32_t hgs[2] = {hg0 >> 1, hg1 >> 1}, h8s[2] = {h80 >> 1, h81 >> 1};
+#define KIVI_KSTEP3(KS, I)                                                                                  \
+  mma16816(acc, ext3<I>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),                     \
+           ext3<I>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]),                          \
+           ext3<I + 1>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),                      \
+           ext3<I + 1>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]), bq[KS][0], bq[KS][1]);
+      KIVI_KSTEP3(0, 0) KIVI_KSTEP3(1, 2) KIVI_KSTEP3(2, 4) KIVI_KSTEP3(3, 6)
+      KIVI_KSTEP3(4, 0) KIVI_KSTEP3(5, 2) KIVI_KSTEP3(6, 4) KIVI_KSTEP3(7, 6)
+#undef KIVI_KSTEP3
+    } else if constexpr (BITS == 2) {
 #define KIVI_KSTEP(KS, I)                                                                       \
   mma16816(acc, ext<2, I>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I>(w8[(KS) >> 2], s8[(KS) >> 2]), \
            ext<2, I + 1>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I + 1>(w8[(KS) >> 2], s8[(KS) >> 2]), \
@@ -758,6 +830,7 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
     // per word)
     uint32_t pa[2], Pp[4][2], az[2], u[2][4];
     uint32_t v8a[2][4], v8b[2][4];  // 8 bits: unit words of groups 0..3 of tokens t0 and t0 + 4
+    uint32_t hv[2][2];              // 3 bits: high units of tokens (t0, t0 + 4), groups 0/1 and 2/3
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
       const int t0 = 16 * kk + 8 * aa + tig;  // tokens t0, t0 + 4
@@ -775,12 +848,20 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
       Pp[2][aa] = split_mul(pa[aa], pbh, S.z);
       Pp[3][aa] = split_mul(pa[aa], pbh, S.w);
       az[aa] = tb.zv[pw + (g & 3)];
-      if constexpr (BITS == 2) {
+      if constexpr (BITS == 2 || BITS == 3) {
         // interleaved word g of a row holds, per byte, channels 4g..4g+3 of groups 0..3
         const uint32_t w0 = tb.vc[t0 * RW + g], w1 = tb.vc[(t0 + 4) * RW + g];
         u[aa][0] = __byte_perm(w0, w1, 0x5410);  // groups 0, 1
         u[aa][1] = __byte_perm(w0, w1, 0x7632);  // groups 2, 3
         u[aa][2] = u[aa][3] = 0u;
+        if constexpr (BITS == 3) {
+          // high unit g (channels 4g..4g+3 of the four groups) of both tokens;
+          // groups 2, 3 (set 1) with the bytes of each half swapped
+          const uint32_t a0 = tb.vc[t0 * RW + kHiPlane3 / 4 + (g >> 1)];
+          const uint32_t a1 = tb.vc[(t0 + 4) * RW + kHiPlane3 / 4 + (g >> 1)];
+          hv[aa][0] = __byte_perm(a0, a1, (g & 1) ? 0x7632 : 0x5410);
+          hv[aa][1] = swap_half_bytes(hv[aa][0]);
+        }
       } else if constexpr (BITS == 8) {
         // interleaved words 4g .. 4g + 3 of a row (logical chunk g of the
         // rotated row) hold channels 4g..4g+3 of groups 0..3, a byte each
@@ -801,7 +882,25 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
     }
     // z-term: rows = value groups (g & 3), columns = (head, part) of p
     mma16816(Z, az[0], az[0], az[1], az[1], pa[0], pa[1]);
-    if constexpr (BITS == 2) {
+    if constexpr (BITS == 3) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t x0 = u[0][half], x1 = u[1][half];
+        const uint32_t x0s = x0 >> 8, x1s = x1 >> 8;
+        const uint32_t h0 = hv[0][half], h1 = hv[1][half];
+        const uint32_t h0s = h0 >> 1, h1s = h1 >> 1;
+        // m-tiles 4*half + {0,1,2,3}: groups 2*half (positions 0..3) and 2*half+1 (4..7)
+#define KIVI_VTILE3(MT, I, GP)                                                                       \
+  mma16816(O[MT], ext3<I>(x0, x0s, h0, h0s), ext3<I + 1>(x0, x0s, h0, h0s), ext3<I>(x1, x1s, h1, h1s), \
+           ext3<I + 1>(x1, x1s, h1, h1s), Pp[GP][0], Pp[GP][1]);
+        if (half == 0) {
+          KIVI_VTILE3(0, 0, 0) KIVI_VTILE3(1, 2, 0) KIVI_VTILE3(2, 4, 1) KIVI_VTILE3(3, 6, 1)
+        } else {
+          KIVI_VTILE3(4, 0, 2) KIVI_VTILE3(5, 2, 2) KIVI_VTILE3(6, 4, 3) KIVI_VTILE3(7, 6, 3)
+        }
+#undef KIVI_VTILE3
+      }
+    } else if constexpr (BITS == 2) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const uint32_t x0 = u[0][half], x1 = u[1][half];
@@ -879,7 +978,7 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float
     const int hh = idx >> 6;
     const int ks = word >> 1, r = word & 1;
     int c0, c1, i;  // the channel pair of the word and its code position
-    if constexpr (BITS == 2) {
+    if constexpr (BITS == 2 || BITS == 3) {
       const int m = tig + 4 * (ks >> 2);
       i = 2 * (ks & 3) + r;
       c0 = 16 * m + i;
@@ -920,6 +1019,10 @@ static_assert(offsetof(TileBuf<8>, vc) == kOffVc<8> && offsetof(TileBuf<8>, sk) 
 static_assert(offsetof(TileBuf<2>, vc) == kOffVc<2> && offsetof(TileBuf<2>, sk) == kOffSk<2> &&
               offsetof(TileBuf<2>, zk) == kOffZk<2> && offsetof(TileBuf<2>, sv) == kOffSv<2> &&
               offsetof(TileBuf<2>, zv) == kOffZv<2>, "stage layout (2 bits)");
+static_assert(offsetof(TileBuf<3>, vc) == kOffVc<3> && offsetof(TileBuf<3>, sk) == kOffSk<3> &&
+              offsetof(TileBuf<3>, zk) == kOffZk<3> && offsetof(TileBuf<3>, sv) == kOffSv<3> &&
+              offsetof(TileBuf<3>, zv) == kOffZv<3> && offsetof(TileBuf<3>, outl) == kTileBytes<3>,
+              "stage layout (3 bits)");
 static_assert(offsetof(TileBuf<4>, vc) == kOffVc<4> && offsetof(TileBuf<4>, sk) == kOffSk<4> &&
               offsetof(TileBuf<4>, zk) == kOffZk<4> && offsetof(TileBuf<4>, sv) == kOffSv<4> &&
               offsetof(TileBuf<4>, zv) == kOffZv<4>, "stage layout (4 bits)");
@@ -1082,7 +1185,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   for (int mt = 0; mt < 8; ++mt) {
     const int gp = mt >> 1, hm = mt & 1;
     // code positions of rows g and g + 8 of m-tile mt
-    const int i_lo = BITS == 2 ? 4 * (gp & 1) + 2 * hm : 2 * hm;
+    const int i_lo = BITS <= 3 ? 4 * (gp & 1) + 2 * hm : 2 * hm;
     const int ch = 32 * gp + 4 * g + 2 * hm;
     const float f_lo = kTwo24 * code_scale<BITS>(i_lo);
     const float f_hi = kTwo24 * code_scale<BITS>(i_lo + 1);
@@ -1308,6 +1411,7 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
 // attn_ctas_per_sm(BITS) CTAs must fit an SM's 228 KB of shared memory
 // (1 KB of it reserved per CTA).
 static_assert(4 * (sizeof(SplitSmem<2>) + 1024 + 256) <= 228 * 1024, "2-bit CTAs per SM");
+static_assert(4 * (sizeof(SplitSmem<3>) + 1024 + 256) <= 228 * 1024, "3-bit CTAs per SM");
 static_assert(4 * (sizeof(SplitSmem<4>) + 1024 + 256) <= 228 * 1024, "4-bit CTAs per SM");
 static_assert(2 * (sizeof(SplitSmem<8>) + 1024 + 256) <= 228 * 1024, "8-bit CTAs per SM");
 
@@ -1344,6 +1448,7 @@ cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLe
   const dim3 grid(a.splits, cv.H * nhc, cv.B);
   switch (cv.bits) {
     case 2: return launch_bits<2>(grid, cv, a, lens, st);
+    case 3: return launch_bits<3>(grid, cv, a, lens, st);
     case 4: return launch_bits<4>(grid, cv, a, lens, st);
     default: return launch_bits<8>(grid, cv, a, lens, st);
   }

@@ -56,7 +56,7 @@ bool device_accessible(const void* p) {
 
 kivi_status check_config(const kivi_config* c) {
   if (!c) return KIVI_EINVAL;
-  if (c->bits != 2 && c->bits != 4 && c->bits != 8) return KIVI_EINVAL;
+  if (c->bits != 2 && c->bits != 3 && c->bits != 4 && c->bits != 8) return KIVI_EINVAL;
   if (c->group != kivi::kGroup || c->head_dim != kivi::kHeadDim) return KIVI_EINVAL;
   if (c->residual <= 0 || c->residual % c->group) return KIVI_ESHAPE;
   if (c->batch <= 0 || c->n_kv_heads <= 0 || c->n_q_heads <= 0) return KIVI_ESHAPE;

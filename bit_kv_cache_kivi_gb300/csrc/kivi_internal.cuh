@@ -151,7 +151,26 @@ template <int BITS>
 constexpr int kOffZv = kOffSk<BITS> + 6 * kHeadDim;
 template <int BITS>
 constexpr int kTileBytes = kOffSk<BITS> + 8 * kHeadDim;
-static_assert(kTileBytes<2> == 3072 && kTileBytes<4> == 5120 && kTileBytes<8> == 9216, "tile sizes");
+static_assert(kTileBytes<2> == 3072 && kTileBytes<3> == 4096 && kTileBytes<4> == 5120 &&
+                  kTileBytes<8> == 9216,
+              "tile sizes");
+
+// 3-bit code rows (48 bytes) are two planes: bytes [0, 32) hold the low two
+// bits of every code exactly as a 2-bit row (keys LSB-first, values
+// group-interleaved), bytes [32, 48) the high bits in eight 16-bit units.
+// Key unit 2W + h (W = 0..3, h = 0..1) holds channels 16m + 8h + i for m in
+// {W, W + 4} (set s = m / 4) and i = 0..7; value unit w holds channels
+// 32 gp + 4w + c of the four groups (set s = gp / 2, i = 4 (gp mod 2) + c).
+// (s, i) sits at bit hi_bit3(s, i) of its unit.  With this placement the high
+// bit of position i of a 2-bit key word lands two bits above that code's low
+// bits after the same shift the low bits take (w for i < 4, w >> 8 above),
+// from the unit word as is (set 0, i < 4), shifted by one (set 0, i >= 4),
+// with its bytes swapped within each half (set 1, i < 4), or both (set 1,
+// i >= 4); the value units follow the same rule per group.
+__host__ __device__ constexpr int hi_bit3(int s, int i) {
+  return s ? (2 * (i & 3) + 2 + (i >> 2) + 8) & 15 : 2 * (i & 3) + 2 + (i >> 2);
+}
+constexpr int kHiPlane3 = 32;  // byte offset of the high plane in a 3-bit row
 
 // At 8 bits a code row is 128 bytes, so that rows at a multiple of 128 bytes
 // would put the same word of every row in the same shared-memory bank.  The
@@ -179,12 +198,12 @@ static_assert(kGroup * (kHeadDim / kGroup) * 2 == 2 * kHeadDim, "value scale blo
 
 // Key scales / zeros of a tile are stored in channel-pair order: 32-bit word
 // i of pair block m holds the fp16 pair (channel P m + i, channel P m + i +
-// P / 2), P = 16 at 2 bits, 8 at 4 bits and 4 at 8 bits -- the two values one
+// P / 2), P = 16 at 2 and 3 bits, 8 at 4 bits and 4 at 8 bits -- the two values one
 // B-fragment register of the score product takes.  kscale_pos(c) is channel
 // c's fp16 slot.
 template <int BITS>
 __host__ __device__ constexpr int kscale_pos(int c) {
-  constexpr int P = BITS == 2 ? 16 : (BITS == 4 ? 8 : 4);
+  constexpr int P = BITS <= 3 ? 16 : (BITS == 4 ? 8 : 4);
   return P * (c / P) + 2 * (c % (P / 2)) + (c % P) / (P / 2);
 }
 

@@ -287,6 +287,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
       // round's argmax (the two token parities hold the same channels).
       int och[kMaxOutliers] = {0, 0, 0, 0};
       uint32_t keep0 = ~0u, keep1 = ~0u;  // code bits of this lane's kept (non-outlier) channels
+      uint32_t keepm = 0xffu;             // bit e: channel c8 + e is kept
       if constexpr (OUTL) {
         float am[8];
 #pragma unroll
@@ -327,9 +328,40 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
             const uint32_t m = ((1u << BITS) - 1u) << (BITS * (e % CW));
             if (e / CW == 0) keep0 &= ~m;
             else keep1 &= ~m;
+            keepm &= ~(1u << e);
           }
       }
-      if (safe) {
+      if constexpr (BITS == 3) {
+        // two planes: the low two bits of channels c8 .. c8 + 7 at bytes 2 cl,
+        // 2 cl + 1 (a 2-bit row), their high bits in unit 2 (m mod 4) + h of
+        // the high plane (m = cl / 2, h = cl mod 2, set m / 4); the lanes of
+        // the two sets of a unit (cl and cl ^ 8) merge their bits
+        const int m = cl >> 1, hh = cl & 1, s3 = m >> 2;
+        (void)keepm;
+#pragma unroll 2
+        for (int k = 0; k < 16; ++k) {
+          smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
+          uint32_t lo = 0u, hb = 0u;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(x[i]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int e = 2 * i + u;
+              const float xv = u ? f.y : f.x;
+              uint32_t c = safe ? code_bits(xv, zf[e], sf[e], inv[e]) - kRoundMagicBits
+                                : exact_code(xv, zf[e], sf[e], L);
+              if constexpr (OUTL) c = ((keepm >> e) & 1u) ? c : 0u;
+              lo |= (c & 3u) << (2 * e);
+              hb |= (c >> 2) << hi_bit3(s3, e);
+            }
+          }
+          hb |= __shfl_xor_sync(kFull, hb, 8);
+          uint8_t* row = &s_codes[(2 * k + par) * RB];
+          *reinterpret_cast<uint16_t*>(row + 2 * cl) = (uint16_t)lo;
+          if (s3 == 0) *reinterpret_cast<uint16_t*>(row + kHiPlane3 + 4 * (m & 3) + 2 * hh) = (uint16_t)hb;
+        }
+      } else if (safe) {
 #pragma unroll 4
         for (int k = 0; k < 16; ++k) {
           smem8<DT>(&s_in[(2 * k + par) * CPR + cl * CPE], x);
@@ -387,7 +419,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
 #pragma unroll
         for (int e = 0; e < 8; ++e) v[e] = par == 0 ? gp[e].sh : gp[e].zh;
         uint32_t w[4];
-        if constexpr (BITS == 2) {
+        if constexpr (BITS == 2 || BITS == 3) {
           // pair block m = this lane's 8 channels and its neighbour's (cl ^ 1):
           // word i = (channel 16m + i, 16m + 8 + i); the lower lane writes
           // words 0..3, the upper one words 4..7, each sending the other the
@@ -452,6 +484,33 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
         const GroupParams p = group_params(fminf(__low2float(mn), __high2float(mn)),
                                            fmaxf(__low2float(mx), __high2float(mx)), L);
         const FastParams f = fast_params(p);
+        if constexpr (BITS == 3) {
+          // low two bits as the 2-bit row's units of group g; high bits of
+          // channels 4w + c of group g at unit w, bit hi_bit3(g / 2, 4 (g
+          // mod 2) + c), merged over the row's four lanes (one per group)
+          uint32_t lo[2] = {0u, 0u}, hw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float2 fv = __half22float2(x[e >> 3][(e & 7) >> 1]);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int ee = e + u, w = ee >> 2, c = ee & 3;
+              const float xv = u ? fv.y : fv.x;
+              const uint32_t q = f.safe ? code_bits(xv, p.z, p.s, f.inv) - kRoundMagicBits
+                                        : exact_code(xv, p.z, p.s, L);
+              lo[ee >> 4] |= (q & 3u) << (2 * (ee & 15));
+              hw[w >> 1] |= (q >> 2) << (hi_bit3(g >> 1, 4 * (g & 1) + c) + 16 * (w & 1));
+            }
+          }
+          const unsigned rmask = 0xfu << (lane & 28);  // the row's four lanes
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            hw[j] |= __shfl_xor_sync(rmask, hw[j], 1);
+            hw[j] |= __shfl_xor_sync(rmask, hw[j], 2);
+          }
+          store_value_units<2>(&s_codes[row * RB], g, lo);
+          if (g == 0) *reinterpret_cast<uint4*>(&s_codes[row * RB + kHiPlane3]) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        } else {
         uint32_t words[BITS];
         if (f.safe) {
 #pragma unroll
@@ -475,6 +534,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
           exact_value_group<BITS>(xw, p.z, p.s, words);
         }
         store_value_units<BITS>(&s_codes[row * RB], g, words);
+        }
         uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
         reinterpret_cast<__half*>(tile + kOffSv<BITS>)[vscale_pos(row, g)] = p.sh;
         reinterpret_cast<__half*>(tile + kOffZv<BITS>)[vscale_pos(row, g)] = p.zh;
@@ -641,14 +701,32 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
       mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, off));
     }
     const GroupParams p = group_params(mn, mx, L);
-    uint32_t q = encode(x, p, L) << (BITS * (d % PER_BYTE));
-#pragma unroll
-    for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-    // value rows are group-interleaved: channel d is in unit d / 4
-    const int vbyte = v_unit_pos(d / 4) * (BITS / 2) + (d % 4) / PER_BYTE;
     uint8_t* tile = tile_at<BITS>(cv, unit, u / kGroup);
     const int row = (int)(u % kGroup);
-    if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vrow_byte<BITS>(row, vbyte)] = (uint8_t)q;
+    if constexpr (BITS == 3) {
+      // the low two bits as a 2-bit row (unit d / 4 interleaved); the high
+      // bit of channel d at unit (d mod 32) / 4, bit hi_bit3(gp / 2, 4 (gp mod
+      // 2) + d mod 4) with gp = d / 32, merged over the four groups
+      __shared__ uint32_t s_vh[4];
+      if (d < 4) s_vh[d] = 0u;
+      __syncthreads();
+      const uint32_t c = encode(x, p, L);
+      uint32_t q = (c & 3u) << (2 * (d & 3));
+      q |= __shfl_xor_sync(kFull, q, 1);
+      q |= __shfl_xor_sync(kFull, q, 2);
+      if ((d & 3) == 0) tile[kOffVc<BITS> + row * RB + v_unit_pos(d / 4)] = (uint8_t)q;
+      const int w = (d & 31) >> 2;
+      if (c >> 2) atomicOr(&s_vh[w >> 1], 1u << (hi_bit3(warp >> 1, 4 * (warp & 1) + (d & 3)) + 16 * (w & 1)));
+      __syncthreads();
+      if (d < 4) reinterpret_cast<uint32_t*>(tile + kOffVc<BITS> + row * RB + kHiPlane3)[d] = s_vh[d];
+    } else {
+      uint32_t q = encode(x, p, L) << (BITS * (d % PER_BYTE));
+#pragma unroll
+      for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
+      // value rows are group-interleaved: channel d is in unit d / 4
+      const int vbyte = v_unit_pos(d / 4) * (BITS / 2) + (d % 4) / PER_BYTE;
+      if (d % PER_BYTE == 0) tile[kOffVc<BITS> + row * RB + vrow_byte<BITS>(row, vbyte)] = (uint8_t)q;
+    }
     if (lane == 0) {
       reinterpret_cast<__half*>(tile + kOffSv<BITS>)[vscale_pos(row, warp)] = p.sh;
       reinterpret_cast<__half*>(tile + kOffZv<BITS>)[vscale_pos(row, warp)] = p.zh;
@@ -722,12 +800,35 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
           *reinterpret_cast<uint4*>(tile + kTileBytes<BITS>) = make_uint4(iw, 0u, 0u, 0u);
         }
       }
+      if constexpr (BITS == 3) {
+        // the low two bits as a 2-bit row; the high bit of channel d = 16 m +
+        // 8 h + i at unit 2 (m mod 4) + h, bit hi_bit3(m / 4, i), merged over
+        // the CTA in shared memory
+        __shared__ uint32_t s_kh[kGroup][4];
+        for (int i = d; i < kGroup * 4; i += kHeadDim) (&s_kh[0][0])[i] = 0u;
+        __syncthreads();
+        const int m = d >> 4;
+        const int hpos = hi_bit3(m >> 2, d & 7) + 16 * ((d >> 3) & 1);
+#pragma unroll 4
+        for (int j = 0; j < kGroup; ++j) {
+          const uint32_t c = slot >= 0 ? 0u : encode(xs[j], p, L);
+          uint32_t q = (c & 3u) << (2 * (d & 3));
+          q |= __shfl_xor_sync(kFull, q, 1);
+          q |= __shfl_xor_sync(kFull, q, 2);
+          if ((d & 3) == 0) tile[j * RB + (d >> 2)] = (uint8_t)q;
+          if (c >> 2) atomicOr(&s_kh[j][m & 3], 1u << hpos);
+        }
+        __syncthreads();
+        reinterpret_cast<uint32_t*>(tile + (d >> 2) * RB + kHiPlane3)[d & 3] = s_kh[d >> 2][d & 3];
+        __syncthreads();  // s_kh is cleared again by the next group
+      } else {
 #pragma unroll
-      for (int j = 0; j < kGroup; ++j) {
-        uint32_t q = (slot >= 0 ? 0u : encode(xs[j], p, L)) << (BITS * (d % PER_BYTE));
+        for (int j = 0; j < kGroup; ++j) {
+          uint32_t q = (slot >= 0 ? 0u : encode(xs[j], p, L)) << (BITS * (d % PER_BYTE));
 #pragma unroll
-        for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-        if (d % PER_BYTE == 0) tile[j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
+          for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
+          if (d % PER_BYTE == 0) tile[j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
+        }
       }
       reinterpret_cast<__half*>(tile + kOffSk<BITS>)[kscale_pos<BITS>(d)] = p.sh;
       reinterpret_cast<__half*>(tile + kOffZk<BITS>)[kscale_pos<BITS>(d)] = p.zh;
@@ -812,6 +913,7 @@ cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void*
   if (c_hi == 0) c_lo = 0;
   switch (cv.bits) {
     case 2: return append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+    case 3: return append_tokens_bits<3>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
     case 4: return append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
     default: return append_tokens_bits<8>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
   }
@@ -822,6 +924,7 @@ cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const vo
   if (t_in <= 0) return cudaSuccess;
   switch (cv.bits) {
     case 2: return prefill_bits<2>(cv, k, v, dtype, t_in, lens, st);
+    case 3: return prefill_bits<3>(cv, k, v, dtype, t_in, lens, st);
     case 4: return prefill_bits<4>(cv, k, v, dtype, t_in, lens, st);
     default: return prefill_bits<8>(cv, k, v, dtype, t_in, lens, st);
   }
@@ -831,6 +934,7 @@ cudaError_t launch_append(const CacheView& cv, const void* k, const void* v, int
                           cudaStream_t st) {
   switch (cv.bits) {
     case 2: return append_bits<2>(cv, k, v, dtype, lens, st);
+    case 3: return append_bits<3>(cv, k, v, dtype, lens, st);
     case 4: return append_bits<4>(cv, k, v, dtype, lens, st);
     default: return append_bits<8>(cv, k, v, dtype, lens, st);
   }

@@ -457,9 +457,9 @@ class KiviCache:
 
 def key_scale_pos(c: int, bits: int) -> int:
     """fp16 slot of channel c in a tile's key scale / zero block: 32-bit word
-    i of pair block m holds channels (P m + i, P m + i + P/2), P = 16 at 2 bits
-    and 8 at 4 bits (the pairs the score product's B fragments take)."""
-    P = {2: 16, 4: 8, 8: 4}[bits]
+    i of pair block m holds channels (P m + i, P m + i + P/2), P = 16 at 2 and
+    3 bits, 8 at 4 bits (the pairs the score product's B fragments take)."""
+    P = {2: 16, 3: 16, 4: 8, 8: 4}[bits]
     return P * (c // P) + 2 * (c % (P // 2)) + (c % P) // (P // 2)
 
 

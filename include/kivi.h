@@ -1,7 +1,7 @@
 /*
  * kivi.h -- C ABI of the GB300 (sm_103a) KIVI KV-cache library.
  *
- * KIVI keeps the KV cache of a decoder in 2- or 4-bit codes: keys are
+ * KIVI keeps the KV cache of a decoder in low-bit codes (2, 3, 4 or 8 bits): keys are
  * quantized per channel (groups of G tokens along the token axis), values
  * per token (groups of G channels), each group with an fp16 scale and zero
  * point; the most recent tokens stay in an fp16 residual window.  Decode
@@ -36,7 +36,7 @@
  *     reports a launch error (see kivi_last_cuda_error).
  *   - A handle is not thread-safe; calls on one handle must be serialized
  *     by the caller (the stream orders the device work).
- *   - Supported by this build: bits 2, 4 or 8, group 32, head_dim 128,
+ *   - Supported by this build: bits 2, 3, 4 or 8, group 32, head_dim 128,
  *     residual a multiple of 32, any batch / head counts with
  *     n_q_heads a multiple of n_kv_heads.
  *   - Inputs must be finite and within the fp16 range; every input element
@@ -65,8 +65,8 @@
  *           The f16 arrays are stored in the order the decode-attention
  *           tensor-core fragments take them (G = 32, D = 128):
  *             key scale / zero: 32-bit word i of pair block m holds channels
- *               (P*m + i, P*m + i + P/2), P = 16 at 2 bits, 8 at 4 bits, 4 at
- *               8 bits, i.e.
+ *               (P*m + i, P*m + i + P/2), P = 16 at 2 and 3 bits, 8 at 4
+ *               bits, 4 at 8 bits, i.e.
  *               channel c is at f16 slot P*(c/P) + 2*(c%(P/2)) + (c%P)/(P/2);
  *             value scale / zero: tokens (8a + r, 8a + r + 4), r < 4, share
  *               32-bit word 4*(4a + r) + g for group g, i.e. token t, group g
@@ -78,6 +78,14 @@
  * unit of channels G*g + 4*w .. +3 sits at unit position 4*w + g, its
  * channels in ascending bit order.  A tile is one contiguous block so that
  * decode attention stages it with a single bulk copy.
+ * 3-bit rows (48 bytes; the pages print no 3-bit packing, so this is the
+ * library's choice) are two planes: bytes [0, 32) hold the low two bits of
+ * every code exactly as a 2-bit row, bytes [32, 48) the high bits in eight
+ * 16-bit units.  Key unit 2*W + h (W < 4, h < 2) holds channels 16*m + 8*h
+ * + i for m in {W, W + 4} and i < 8, with set s = m / 4; value unit w holds
+ * channels 32*g + 4*w + c of the four groups g, with s = g / 2 and
+ * i = 4*(g % 2) + c.  (s, i) sits at bit p = 2*(i%4) + 2 + (i >= 4) of its
+ * unit, or (p + 8) % 16 when s = 1.
  * Residual policy (kivi_config.policy):
  *   KIVI_POLICY_ALG1 (the chooblog review's Algorithm 1): after l tokens the
  *     first nq_k(l) = R*floor(l/R) keys and the first nq_v(l) = max(l-R, 0)
@@ -117,7 +125,7 @@ typedef enum { KIVI_POLICY_ALG1 = 0, KIVI_POLICY_SHARED = 1 } kivi_policy;
 /* Cache configuration (veloxquant-mlx "KIVI" usage: bit width, group size,
  * residual length) plus the tensor shape. */
 typedef struct {
-  int bits;        /* 2, 4 or 8 */
+  int bits;        /* 2, 3, 4 or 8 */
   int group;       /* G: 32 in this build */
   int residual;    /* R: fp16 window, a multiple of G */
   int head_dim;    /* D: 128 in this build */

@@ -73,12 +73,12 @@ def test_sizes(K):
 def test_scale_slot_maps_are_permutations(K):
     """The tile's fp16 scale / zero orders are bijections of the 128 slots,
     and keep each 32-channel quarter in place (the tail split relies on it)."""
-    for bits in (2, 4, 8):
+    for bits in (2, 3, 4, 8):
         pos = [K.key_scale_pos(c, bits) for c in range(128)]
         assert sorted(pos) == list(range(128))
         assert all(p // 32 == c // 32 for c, p in enumerate(pos))
         # word i of a pair block: channels (P m + i, P m + i + P/2)
-        P = {2: 16, 4: 8, 8: 4}[bits]
+        P = {2: 16, 3: 16, 4: 8, 8: 4}[bits]
         assert pos[P + 1] == P + 2 and pos[P + 1 + P // 2] == P + 3
     vpos = [K.value_scale_pos(t, g) for t in range(32) for g in range(4)]
     assert sorted(vpos) == list(range(128))
@@ -87,7 +87,7 @@ def test_scale_slot_maps_are_permutations(K):
 
 @pytest.mark.parametrize("bad,status", [
     (dict(policy=2), 1), (dict(policy=-1), 1), (dict(outlier_channels=5), 1), (dict(outlier_channels=-1), 1),
-    (dict(bits=3), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
+    (dict(bits=5), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
 ])

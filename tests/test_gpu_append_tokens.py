@@ -27,7 +27,7 @@ def _chunk(x, a, b):
     return np.ascontiguousarray(x[:, :, a:b])
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("R", [32, 64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
 def test_append_tokens_matches_token_by_token(bits, R, dtype):

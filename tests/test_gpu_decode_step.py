@@ -42,7 +42,7 @@ def _run(wl, steps, policy=T.ALG1, outliers=0, dtype="f16", cap=None, check_ever
 
 
 @pytest.mark.parametrize("policy", [T.ALG1, T.SHARED])
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_step_matches_append_then_attention(bits, policy):
     wl = W.synthetic("ds", B=2, Hq=8, Hkv=2, T=200, R=32, bits=bits, steps=70, seed=7 * bits + policy)
     a, b = _run(wl, wl.steps, policy=policy)

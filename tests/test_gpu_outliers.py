@@ -22,7 +22,7 @@ def _lib():
     torch.cuda.init()
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("n_out", [1, 2, 4])
 @pytest.mark.parametrize("policy", [T.ALG1, T.SHARED])
 def test_outliers_prefill_appends_attention(bits, n_out, policy):

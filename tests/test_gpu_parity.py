@@ -55,7 +55,7 @@ def test_single_head_notebook_workload():
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16", "f32"])
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("T_,R", [(1000, 32), (777, 64), (95, 32), (32, 32), (20, 32),
                                   (33, 32), (64, 64)])
 def test_prefill_state_bit_exact(dtype, bits, T_, R):
@@ -80,14 +80,14 @@ def test_prefill_extreme_values():
     k[0, 1, 64:96, 7] = rng.standard_normal(32) * 8e3          # large, within fp16
     v[0, 0, 60, 64:96] = np.array([0, 3] * 16)                  # 2-bit scale exactly 1
     v[0, 0, 60, 70] = 1.5                                       # an exact tie
-    for bits in (2, 4):
+    for bits in (2, 3, 4):
         wl = W.synthetic("x", B=1, Hq=2, Hkv=2, T=256, bits=bits, seed=1)
         wl.k, wl.v = k.astype(np.float16), v.astype(np.float16)
         g, o = run_prefill(wl)
         T.compare_state(T.gpu_state(g), o.export(), 256, 32, 32)
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_prefill_tie_heavy_lattices(bits, dtype):
     """Inputs on coarse dyadic lattices make (x - z)/s land exactly on, or
@@ -108,7 +108,7 @@ def test_prefill_tie_heavy_lattices(bits, dtype):
 
 # ---------------------------------------------------------------- append
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("R", [32, 64])
 def test_append_crosses_flushes(bits, R):
     """Decode appends through several K flushes and V evictions; state checked
@@ -168,7 +168,7 @@ def test_capacity_and_state_errors():
 # ---------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("Hq,Hkv", [(1, 1), (2, 1), (8, 2), (28, 4), (18, 1), (24, 2)])
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_attention_gqa_shapes(Hq, Hkv, bits):
     wl = W.synthetic("g", B=2, Hq=Hq, Hkv=Hkv, T=1100, R=32, bits=bits, seed=Hq * 10 + Hkv)
     g, o = run_prefill(wl)
@@ -184,7 +184,7 @@ def test_attention_short_contexts(T_):
 
 
 @pytest.mark.parametrize("R", [32, 128])
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_attention_tail_on_last_packed_split(R, bits):
     """320 (batch, kv-head) units leave no room in one wave for a tail split,
     so the last packed split also takes the tail (one or three 64-token

@@ -40,7 +40,7 @@ def unit_attention_err(out, wl, units, oracles, q):
     return worst
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_llama3_8b_decode_step(bits):
     """batch 8, 32/8 heads, context 4096 fp16: prefill, one append, attention;
     the whole batch against the oracle (2 bits, and the same step at 4 bits)."""
@@ -57,7 +57,7 @@ def test_llama3_8b_decode_step(bits):
     assert T.attn_err(out, o.attention(T.q_float(wl.q, "f16"))) <= T.ATTN_TOL
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_prefill_quantize_bf16_32k(bits):
     """batch 4, 8 KV heads, 32768 tokens of bf16 with V spikes: sampled units."""
     wl = W.prefill_quantize(bits)

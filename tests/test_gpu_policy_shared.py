@@ -27,7 +27,7 @@ def _check_attn(g, o, wl):
     assert T.attn_err(out, o.attention(T.q_float(wl.q, wl.q_dtype))) <= T.ATTN_TOL
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("R", [32, 64])
 @pytest.mark.parametrize("T_", [1, 31, 33, 63, 64, 65, 95, 96, 97, 500, 1031])
 def test_shared_prefill_state_and_attention(bits, R, T_):
@@ -41,7 +41,7 @@ def test_shared_prefill_state_and_attention(bits, R, T_):
     _check_attn(g, o, wl)
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("R", [32, 64])
 def test_shared_appends_across_flushes(bits, R):
     wl = W.synthetic("sa", B=2, Hq=8, Hkv=2, T=R + 5, R=R, bits=bits, steps=3 * 32 + 7,
@@ -64,7 +64,7 @@ def test_shared_appends_across_flushes(bits, R):
             assert T.attn_err(out, ref) <= T.ATTN_TOL
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 def test_shared_append_tokens_and_stream_equals_prefill(bits):
     """Chunks appended at once equal the oracle's token-by-token appends, and
     the final cache equals a one-shot prefill of all the tokens."""

@@ -62,7 +62,7 @@ def _append_all(g, oracles, kn, vn, dtype):
         o.append(np.ascontiguousarray(kn[b:b + 1]), np.ascontiguousarray(vn[b:b + 1]))
 
 
-@pytest.mark.parametrize("bits", [2, 4, 8])
+@pytest.mark.parametrize("bits", [2, 3, 4, 8])
 @pytest.mark.parametrize("policy", [T.ALG1, T.SHARED])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 def test_ragged_prefill_appends_attention(bits, policy, dtype):
