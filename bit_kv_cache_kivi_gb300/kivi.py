@@ -262,9 +262,12 @@ class KiviCache:
         return kivi_cache_lengths(self.handle, self.cfg.batch)
 
     def _reachable(self, x: torch.Tensor) -> bool:
-        """On the cache's device, or page-locked host memory (which the
-        kernels read and write directly; the C library checks it again)."""
-        return x.device == self.device or (x.device.type == "cpu" and x.is_pinned())
+        """On the cache's device, or host memory.  Host tensors must be
+        page-locked (the kernels read and write them in place); the C
+        library checks that with one pointer query per buffer and refuses
+        pageable memory with KIVI_EINVAL before any launch, so it is not
+        queried a second time here."""
+        return x.device == self.device or x.device.type == "cpu"
 
     def _check_kv(self, x: torch.Tensor, T: int | None) -> int:
         c = self.cfg

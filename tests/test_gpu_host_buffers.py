@@ -69,9 +69,12 @@ def test_pageable_host_memory_is_refused():
     st = lib.kivi_decode_attention(g.handle, page_q.ctypes.data, K.KIVI_F16, page_o.ctypes.data, 0.0,
                                    g.workspace.data_ptr(), g.ws_bytes, None)
     assert st == K.KIVI_EINVAL and not page_o.any()
-    # the binding refuses unpinned CPU tensors before the C call
-    with pytest.raises(ValueError):
+    # through the binding: the library's refusal, before any launch
+    with pytest.raises(K.KiviError) as e:
         g.append(torch.from_numpy(page_k), torch.from_numpy(page_v))
+    assert e.value.status == K.KIVI_EINVAL and g.length == 64
+    with pytest.raises(K.KiviError):
+        g.attention(torch.from_numpy(page_q))
     # and the cache still works
     q = T.dev(wl.q, "f16")
     o = T.oracle_cache(wl, capacity=128)
