@@ -178,6 +178,14 @@ def run_gpu(args):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
+    def fence():
+        """Both sides of a timed region: the device idle and, under N ranks,
+        every rank at the same point."""
+        torch.cuda.synchronize()
+        import torch.distributed as dist
+        if dist.is_available() and dist.is_initialized():
+            dist.barrier()
+
     # ---------------- main: decode step at context 4096 (+ a rewind window)
     K, Wm = args.steps, args.warmup
     window = 256
@@ -225,12 +233,12 @@ def run_gpu(args):
             caches[i % n_rep].attention(q, out)
     ctx_a = [caches[i % n_rep].length for i in range(K)]
     gA.replay()  # warm-up replay (attention leaves the caches unchanged)
-    torch.cuda.synchronize()
+    fence()
     e0, e1 = ev(), ev()
     e0.record(stream)
     gA.replay()
     e1.record(stream)
-    torch.cuda.synchronize()
+    fence()
     t_att_graph = e0.elapsed_time(e1) * 1e-3 / K
     att_b = np.array([attn_bytes(B, Hkv, Hq, D, t, R, 2) for t in ctx_a], float)
     attn_gbs = att_b.sum() / (t_att_graph * K) / 1e9
@@ -255,11 +263,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
     del gB
     gB, ctx_b = capture_steps()
+    fence()
     e0, e1 = ev(), ev()
     e0.record(stream)
     gB.replay()
     e1.record(stream)
-    torch.cuda.synchronize()
+    fence()
     step_graph_s = e0.elapsed_time(e1) * 1e-3 / K
     tokens_per_s = B / step_graph_s
     del gB
@@ -340,6 +349,7 @@ def run_gpu(args):
                           "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                           if peak_src == "measured" else "fallback 6800 GB/s",
                           "algorithmic_bytes_per_launch": int(att_b.mean())}
+    result["_attn"] = (float(att_b.sum()), t_att_graph * K)  # for the whole-job numbers of N ranks
     result["e2e"] = {"value": round(e2e_gbs, 2), "unit": "GB/s",
                      "h2d_bytes_per_step": int(kh.numel() * 2 * 2 + qh.numel() * 2),
                      "d2h_bytes_per_step": int(oh.numel() * 2)}
@@ -614,6 +624,26 @@ def run_oracle(steps, warmup, budget_s=None):
             "tokens_per_s": round(done / (t_app + t_att), 3), "steps": done}
 
 
+def combine_ranks(result: dict) -> dict:
+    """Whole-job numbers of a replicas-only run over the initialised process
+    group: the step time is the slowest rank's, and `value` the attention
+    bytes of every rank over the slowest rank's attention time (weak
+    scaling).  Reads result["_attn"] = (bytes, seconds) of this rank."""
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    b, sec = result["_attn"]
+    tot = torch.tensor([float(b)], dtype=torch.float64, device=dev)
+    mx = torch.tensor([float(sec), float(result["ms_per_step"])], dtype=torch.float64, device=dev)
+    dist.all_reduce(tot, op=dist.ReduceOp.SUM)
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    out = dict(result)
+    out["value"] = round(float(tot[0]) / float(mx[0]) / 1e9, 2)
+    out["ms_per_step"] = round(float(mx[1]), 5)
+    out["n_gpus"] = dist.get_world_size()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -650,8 +680,8 @@ def main():
         # device; no data-path collective exists.
         import torch
         import torch.distributed as dist
-        dist.init_process_group("nccl")
         torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        dist.init_process_group("nccl")
         dist.barrier()
     if args.only and args.only != "main":
         result = run_only(args)
@@ -659,14 +689,10 @@ def main():
         return
     result = run_gpu(args)
     if world > 1:
-        import torch
         import torch.distributed as dist
-        ms = torch.tensor([result["ms_per_step"]], device="cuda")
-        dist.all_reduce(ms, op=dist.ReduceOp.MAX)
-        result["ms_per_step"] = float(ms.item())
-        result["value"] = round(result["value"] * world, 2)
-        result["n_gpus"] = world
+        result = combine_ranks(result)
         dist.destroy_process_group()
+    result.pop("_attn", None)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             result["cpu_baseline"] = run_oracle(args.steps, 2, budget_s=12.0)
