@@ -1081,13 +1081,15 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   // the first tile before the q tables, the other stages after them: at
   // launch every warp of the GPU issues at once, and the first tile (and the
   // tables) should not queue behind the later stages.  A dependent launch
-  // builds the tables while the append runs and issues every copy after it.
-  if (!a.pdl && lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
+  // whose packed tiles the append may write builds the tables while the
+  // append runs and issues every copy after it.
+  const bool wait_first = a.pdl == kPdlAll;
+  if (!wait_first && lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
   build_q_tables<BITS>(ws, a, qv4);
   __syncthreads();
-  if (a.pdl) grid_dependency_wait();
+  if (wait_first) grid_dependency_wait();
   if (lane == 0)
-    for (int k = a.pdl ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
+    for (int k = wait_first ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
   const float ks = ws.qscale[tig];
   float* pb = &ws.pbuf[warp][0][0];
 
@@ -1328,7 +1330,10 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
     packed_split<BITS>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
-  if (path == kPathMma && p.tail_fused && s == p.splits - 1) fused_tail<BITS>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
+  if (path == kPathMma && p.tail_fused && s == p.splits - 1) {
+    if (a.pdl == kPdlTail) grid_dependency_wait();  // the tail reads what the append wrote
+    fused_tail<BITS>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
+  }
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;

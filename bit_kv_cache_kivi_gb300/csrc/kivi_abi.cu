@@ -504,7 +504,18 @@ KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const vo
   kivi::SeqLens sl;
   kivi_status ast = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(workspace), &a, &sl);
   if (ast != KIVI_OK) return ast;  // not reached: every sequence holds a token now
-  a.pdl = 1;
+  // Which tiles did the append write?  Under either policy, the only write
+  // below t_tail = 32 floor(nq_v(l) / 32) is on a step where l - R reaches a
+  // multiple of G: the value row leaving the window (Algorithm 1) or the
+  // group just quantized (shared window) then closes the last packed tile.
+  // On every other step the append writes ring slots and rows or key groups
+  // of the tail alone, and the packed splits need not wait for it.
+  bool packed_untouched = true;
+  for (int b = 0; b < (c->uniform ? 1 : c->cfg.batch); ++b) {
+    const int l = len_of(c, b);
+    if (l > c->cfg.residual && (l - c->cfg.residual) % c->cfg.group == 0) packed_untouched = false;
+  }
+  a.pdl = packed_untouched ? kivi::kPdlTail : kivi::kPdlAll;
   return cuda_status(kivi::launch_attention(view(c), a, sl, st));
 }
 

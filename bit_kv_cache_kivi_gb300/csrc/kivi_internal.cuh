@@ -271,12 +271,17 @@ struct AttnArgs {
   int* counters;      // [gid][merge_groups] CTAs finished per split group; 0 between calls
   int* counters2;     // [gid] split groups finished; 0 between calls
   int* status;        // set nonzero when a bounded wait for staged data timed out
-  // Nonzero when the launch is a programmatic dependent of the append kernel
-  // just before it on the stream: the CTAs may start while the append runs,
-  // load q and build their tables, and wait for the append's completion
-  // (griddepcontrol.wait) before reading the cache.
+  // A programmatic dependent of the append kernel just before it on the
+  // stream (the one-call decode step): the CTAs may start while the append
+  // runs.  kPdlAll: every CTA loads q and builds its tables, then waits for
+  // the append's completion (griddepcontrol.wait) before reading the cache.
+  // kPdlTail: this step's append writes nothing below t_tail (ring slots, a
+  // value row or key group inside the tail), so the packed splits never wait
+  // and only the tail's readers do.  0: an ordinary launch.
   int pdl;
 };
+
+enum : int { kPdlAll = 1, kPdlTail = 2 };
 
 // Programmatic dependent launch (sm_90+).  The primary kernel lets its
 // dependent start early; the dependent waits for the primary's completion and
