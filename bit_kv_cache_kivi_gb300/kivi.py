@@ -243,6 +243,8 @@ class KiviCache:
         self._tok_shape = torch.Size((batch, n_kv_heads, head_dim))
         self._q_shape = torch.Size((batch, n_q_heads, head_dim))
         self.workspace = torch.empty(max(self.ws_bytes, 16), dtype=torch.uint8, device=self.device)
+        self._ws_ptr = self.workspace.data_ptr()
+        self._step_fn = lib().kivi_decode_step  # the per-step call, looked up once
 
     def __del__(self):
         h = getattr(self, "handle", None)
@@ -360,8 +362,11 @@ class KiviCache:
         if self._check_kv(v_new, None) != dt:
             raise ValueError("K and V dtypes differ")
         out = self._check_q_out(q, out)
-        kivi_decode_step(self.handle, k_new, v_new, dt, q, _TORCH_DTYPE[q.dtype], out, softmax_scale,
-                         self.workspace, self.ws_bytes, _stream(stream, self.device.index))
+        st = self._step_fn(self.handle, k_new.data_ptr(), v_new.data_ptr(), dt, q.data_ptr(),
+                           _TORCH_DTYPE[q.dtype], out.data_ptr(), float(softmax_scale), self._ws_ptr,
+                           self.ws_bytes, _stream(stream, self.device.index))
+        if st != KIVI_OK:
+            raise KiviError(st, "kivi_decode_step")
         return out
 
     def set_splits(self, n: int) -> None:
