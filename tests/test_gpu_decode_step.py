@@ -63,6 +63,20 @@ def test_step_other_input_dtypes(dtype):
     _run(wl, wl.steps, dtype=dtype)
 
 
+@pytest.mark.parametrize("bits", [2, 3])
+def test_step_outlier_channels(bits):
+    """R = 32, GQA 4, outlier keys: most steps let the packed splits run
+    beside the append (only the tail waits), with key flushes that write the
+    outlier blocks; the cache must equal the oracle's."""
+    wl = W.synthetic("dq", B=2, Hq=8, Hkv=2, T=130, R=32, bits=bits, steps=70, seed=17 + bits)
+    a, _ = _run(wl, wl.steps, outliers=2)
+    o = T.oracle_cache(wl, capacity=a.cfg.max_tokens, outliers=2)
+    o.prefill(wl.k, wl.v)
+    for i in range(wl.steps):
+        o.append(wl.k_new[i], wl.v_new[i])
+    T.compare_state(T.gpu_state(a), o.export(), wl.T + wl.steps, wl.R, 32)
+
+
 def test_step_outlier_channels_and_long_residual():
     wl = W.synthetic("do", B=2, Hq=8, Hkv=2, T=300, R=128, steps=140, seed=11)
     _run(wl, wl.steps, outliers=2, check_every=7)
