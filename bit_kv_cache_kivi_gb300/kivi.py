@@ -184,8 +184,9 @@ def kivi_decode_attention(h, q, q_dtype: int, out, softmax_scale: float, workspa
 
 def kivi_decode_step(h, k_new, v_new, kv_dtype: int, q, q_dtype: int, out, softmax_scale: float,
                      workspace, ws_bytes: int, stream=None) -> None:
-    """Append one token, then decode attention over the grown cache; the
-    attention launch overlaps the append (see kivi.h)."""
+    """Append one token, then decode attention over the grown cache, the
+    attention launched as a programmatic dependent of the append (the C
+    header describes which of its CTAs wait for the append)."""
     _check(lib().kivi_decode_step(h, _ptr(k_new), _ptr(v_new), kv_dtype, _ptr(q), q_dtype, _ptr(out),
                                   float(softmax_scale), _ptr(workspace), ws_bytes, _stream(stream)),
            "kivi_decode_step")
@@ -350,9 +351,10 @@ class KiviCache:
     def step(self, k_new: torch.Tensor, v_new: torch.Tensor, q: torch.Tensor,
              out: torch.Tensor | None = None, softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
         """One decode step: append k_new, v_new ([B][H][D]), then decode
-        attention of q over the grown cache, in one call; the attention's
-        launch and query prologue overlap the append.  Same cache and output
-        as append() followed by attention()."""
+        attention of q over the grown cache, in one call; the attention is
+        launched as a programmatic dependent of the append, so its launch,
+        its query tables and (on most steps) its packed splits overlap the
+        append.  Same cache and output as append() followed by attention()."""
         shape = self._tok_shape
         if k_new.shape != shape:
             k_new = k_new.reshape(shape)

@@ -259,10 +259,12 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
  * kivi_decode_attention(c, q, q_dtype, out, ...) on the same stream, with
  * the same arguments, layouts and results (bit for bit).
  * The attention is launched as a programmatic dependent of the append's last
- * kernel: its CTAs start while the append runs, load q and build their query
- * tables, and wait (griddepcontrol.wait) for the append to complete before
- * they read the cache, so the attention's launch and prologue overlap the
- * append.
+ * kernel: its CTAs start while the append runs.  A CTA waits
+ * (griddepcontrol.wait) for the append to complete before it reads anything
+ * the append may have written: on a step where l - R reaches a multiple of
+ * G (the append closes the last packed tile) every CTA builds its query
+ * tables and then waits; on every other step only the CTAs that read the
+ * fp16 tail wait, and the packed splits run beside the append.
  * Errors: every check of both halves is made before any launch (nothing runs
  * and the length is unchanged on KIVI_EINVAL, KIVI_EDTYPE, KIVI_ECAPACITY or
  * KIVI_EWORKSPACE).  If the append launches and the attention launch then
