@@ -57,6 +57,29 @@ def test_step_matches_append_then_attention(bits, policy):
     assert T.attn_err(out, o.attention(T.q_float(wl.q, wl.q_dtype))) <= T.ATTN_TOL
 
 
+@pytest.mark.parametrize("policy", [T.ALG1, T.SHARED])
+def test_steps_from_an_empty_cache(policy):
+    """Lengths 1, 2, ... from nothing: only tail splits at first, then the
+    first flushes and the first packed tiles."""
+    wl = W.synthetic("de", B=2, Hq=8, Hkv=2, T=0, R=32, steps=100, seed=41 + policy)
+    cap = 128
+    a = T.gpu_cache(wl, capacity=cap, policy=policy)
+    b = T.gpu_cache(wl, capacity=cap, policy=policy)
+    q = T.dev(wl.q, wl.q_dtype)
+    o = T.oracle_cache(wl, capacity=cap, policy=policy)
+    for i in range(wl.steps):
+        kn, vn = T.dev(wl.k_new[i], "f16"), T.dev(wl.v_new[i], "f16")
+        oa = a.step(kn, vn, q)
+        b.append(kn, vn)
+        ob = b.attention(q)
+        o.append(wl.k_new[i], wl.v_new[i])
+        torch.cuda.synchronize()
+        assert torch.equal(oa, ob), f"step {i}"
+        if i in (0, 31, 32, 63, 64, 99):
+            T.compare_state(T.gpu_state(a), o.export(), i + 1, wl.R, 32, policy=policy)
+            assert T.attn_err(T.out_float(oa), o.attention(T.q_float(wl.q, wl.q_dtype))) <= T.ATTN_TOL
+
+
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_step_other_input_dtypes(dtype):
     wl = W.synthetic("dt", B=1, Hq=4, Hkv=1, T=95, R=32, steps=40, seed=3, dtype=dtype)
