@@ -20,6 +20,7 @@ struct kivi_cache {
   int* lens;                // [batch] per-sequence lengths while !uniform
   int splits_override;      // 0 = automatic
   const void* ws_ready;     // workspace whose counter area is known to be zero
+  int device;               // the buffers' device (kNoDevice until the first launching call)
 };
 
 namespace {
@@ -34,12 +35,16 @@ kivi_status cuda_status(cudaError_t e) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// A caller buffer that the kernels may read or write directly: device or
-// managed memory, or page-locked host memory, which unified addressing maps
-// into the device's address space at the same address (on a GB300 node the
-// kernels then reach it over NVLink-C2C, with no staging copy).  Pageable
-// host memory is refused before any launch.  Host only; no device work.
-bool device_accessible(const void* p) {
+constexpr int kNoDevice = -1;   // not yet known
+constexpr int kAnyDevice = -2;  // managed buffers: reachable from every device
+
+// A caller buffer that the kernels, launched on `device`, may read or write
+// directly: device memory of that device, managed memory, or page-locked
+// host memory, which unified addressing maps into the device's address space
+// at the same address (on a GB300 node the kernels then reach it over
+// NVLink-C2C, with no staging copy).  Pageable host memory and another
+// device's memory are refused before any launch.  Host only; no device work.
+bool device_accessible(const void* p, int device) {
   cudaPointerAttributes at;
   const cudaError_t e = cudaPointerGetAttributes(&at, p);
   if (e != cudaSuccess) {
@@ -47,7 +52,7 @@ bool device_accessible(const void* p) {
     return false;
   }
   switch (at.type) {
-    case cudaMemoryTypeDevice:
+    case cudaMemoryTypeDevice: return at.device == device;
     case cudaMemoryTypeManaged: return true;
     case cudaMemoryTypeHost: return at.devicePointer == p;
     default: return false;
@@ -65,6 +70,30 @@ kivi_status check_config(const kivi_config* c) {
   if (c->batch > 65535 || c->n_kv_heads > 4096) return KIVI_ESHAPE;  // grid limits
   if (c->policy != KIVI_POLICY_ALG1 && c->policy != KIVI_POLICY_SHARED) return KIVI_EINVAL;
   if (c->outlier_channels < 0 || c->outlier_channels > kivi::kMaxOutliers) return KIVI_EINVAL;
+  return KIVI_OK;
+}
+
+// The calling thread's current device, which must be the one holding the
+// cache's buffers (found from the tile buffer on the first launching call):
+// KIVI_EINVAL otherwise, before any launch.
+kivi_status launch_device(kivi_cache* c, int* device) {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return KIVI_ECUDA;
+  }
+  if (c->device == kNoDevice) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, c->buf.tiles) != cudaSuccess) {
+      cudaGetLastError();
+      return KIVI_EINVAL;
+    }
+    if (at.type == cudaMemoryTypeDevice) c->device = at.device;
+    else if (at.type == cudaMemoryTypeManaged) c->device = kAnyDevice;
+    else return KIVI_EINVAL;  // the cache itself must live in device memory
+  }
+  if (c->device != kAnyDevice && c->device != d) return KIVI_EINVAL;
+  *device = d;
   return KIVI_OK;
 }
 
@@ -255,6 +284,7 @@ KIVI_API kivi_status kivi_cache_init(const kivi_config* cfg, const kivi_buffers*
   c->cfg = *cfg;
   c->buf = *bufs;
   c->uniform = 1;
+  c->device = kNoDevice;
   *out = c;
   return KIVI_OK;
 }
@@ -284,7 +314,10 @@ kivi_status prefill(kivi_cache* c, const void* k, const void* v, kivi_dtype dtyp
   }
   if (t_in == 0) return KIVI_OK;
   if (!k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
-  if (!device_accessible(k) || !device_accessible(v)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(k, dev) || !device_accessible(v, dev)) return KIVI_EINVAL;
   kivi_cache tmp = *c;  // the lengths the launch will produce
   if (lens) set_lens(&tmp, lens);
   else tmp.length = t_in;
@@ -347,7 +380,10 @@ KIVI_API kivi_status kivi_append_decode(kivi_cache* c, const void* k_new, const 
                                         kivi_dtype dtype, void* stream) {
   const kivi_status chk = append_checks(c, k_new, v_new, dtype);
   if (chk != KIVI_OK) return chk;
-  if (!device_accessible(k_new) || !device_accessible(v_new)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(k_new, dev) || !device_accessible(v_new, dev)) return KIVI_EINVAL;
   return append_launch(c, k_new, v_new, dtype, stream);
 }
 
@@ -357,7 +393,10 @@ KIVI_API kivi_status kivi_append_tokens(kivi_cache* c, const void* k, const void
   if (!dtype_ok(dtype)) return KIVI_EDTYPE;
   if (n_tokens <= 0 || !k || !v || !aligned16(k) || !aligned16(v)) return KIVI_EINVAL;
   if ((long)max_len(c) + n_tokens > c->cfg.max_tokens) return KIVI_ECAPACITY;
-  if (!device_accessible(k) || !device_accessible(v)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(k, dev) || !device_accessible(v, dev)) return KIVI_EINVAL;
   kivi::SeqLens sl;
   seq_lens(c, &sl, n_tokens);
   kivi_status st = cuda_status(
@@ -464,9 +503,13 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
   kivi::SeqLens sl;
   kivi_status ast = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(workspace), &a, &sl);
   if (ast != KIVI_OK) return ast;
-  if (!device_accessible(q) || !device_accessible(out)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(q, dev) || !device_accessible(out, dev)) return KIVI_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->ws_ready != workspace) {
+    if (!device_accessible(workspace, dev)) return KIVI_EWORKSPACE;
     const WsLayout w = ws_layout(c->cfg);
     kivi_status z = cuda_status(cudaMemsetAsync(a.counters, 0, w.total - w.cnt_off, st));
     if (z != KIVI_OK) return z;
@@ -486,11 +529,15 @@ KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const vo
   if (!q || !out) return KIVI_EINVAL;
   if (!workspace || !aligned16(workspace) || ws_bytes < kivi_attention_workspace_bytes(c))
     return KIVI_EWORKSPACE;
-  if (!device_accessible(k_new) || !device_accessible(v_new) || !device_accessible(q) ||
-      !device_accessible(out))
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(k_new, dev) || !device_accessible(v_new, dev) || !device_accessible(q, dev) ||
+      !device_accessible(out, dev))
     return KIVI_EINVAL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (c->ws_ready != workspace) {
+    if (!device_accessible(workspace, dev)) return KIVI_EWORKSPACE;
     // before the append, so that the attention's only predecessor is the append
     const WsLayout w = ws_layout(c->cfg);
     kivi_status z =
@@ -610,7 +657,10 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   kivi::SeqLens sl;
   st = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(ws), &a, &sl);
   if (st != KIVI_OK) return st;
-  if (!device_accessible(q) || !device_accessible(out)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(q, dev) || !device_accessible(out, dev)) return KIVI_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left; the split counters must
   // start at zero, so clear them on every call (a memset, not an allocation).

@@ -28,6 +28,11 @@
  *     such host buffers directly (on a GB300 node over NVLink-C2C), with no
  *     staging copy.  Pageable host memory is refused with KIVI_EINVAL before
  *     any launch (checked with cudaPointerGetAttributes).
+ *   - Calls that launch work must be made with the device that holds the
+ *     cache's buffers current (the device is read from the tile buffer on
+ *     the first such call), and device buffers passed per call (inputs,
+ *     outputs, workspace) must live on that device; otherwise KIVI_EINVAL
+ *     (KIVI_EWORKSPACE for the workspace) before any launch.
  *   - All work is asynchronous on the given stream (a cudaStream_t passed as
  *     void*; NULL is the legacy default stream).  No call synchronizes the
  *     device or reads device memory back.

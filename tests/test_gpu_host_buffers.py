@@ -80,3 +80,21 @@ def test_pageable_host_memory_is_refused():
     o = T.oracle_cache(wl, capacity=128)
     o.prefill(wl.k, wl.v)
     assert T.attn_err(T.out_float(g.attention(q)), o.attention(T.q_float(wl.q, "f16"))) <= T.ATTN_TOL
+
+
+def test_cache_buffers_in_pageable_memory_are_refused():
+    """The cache's own buffers must be device (or managed) memory: a handle
+    over ordinary host memory is refused at its first launching call, before
+    any launch."""
+    from bit_kv_cache_kivi_gb300 import kivi as K
+    cfg = K.kivi_config(2, 32, 32, 128, 1, 1, 4, 64)
+    sizes = K.kivi_cache_sizes(cfg)
+    host = [np.zeros(n + 16, np.uint8) for n in sizes]
+    ptrs = [a.ctypes.data + (-a.ctypes.data) % 16 for a in host]  # 16-byte aligned
+    h = K.kivi_cache_init(cfg, K.kivi_buffers(*ptrs))
+    try:
+        k = T.dev(np.zeros((1, 1, 32, 128), np.float16), "f16")
+        st = K.lib().kivi_quantize_prefill(h, k.data_ptr(), k.data_ptr(), K.KIVI_F16, 32, None)
+        assert st == K.KIVI_EINVAL and K.kivi_cache_length(h) == 0
+    finally:
+        K.kivi_cache_destroy(h)
