@@ -68,6 +68,9 @@ kivi_status check_config(const kivi_config* c) {
   if (c->n_q_heads % c->n_kv_heads) return KIVI_ESHAPE;
   if (c->max_tokens <= 0 || c->max_tokens % c->residual) return KIVI_ESHAPE;
   if (c->batch > 65535 || c->n_kv_heads > 4096) return KIVI_ESHAPE;  // grid limits
+  // the attention grid's y extent: kv-heads x chunks of kHeadChunk query heads
+  if ((long)c->n_kv_heads * ((c->n_q_heads / c->n_kv_heads + kivi::kHeadChunk - 1) / kivi::kHeadChunk) > 65535)
+    return KIVI_ESHAPE;
   if (c->policy != KIVI_POLICY_ALG1 && c->policy != KIVI_POLICY_SHARED) return KIVI_EINVAL;
   if (c->outlier_channels < 0 || c->outlier_channels > kivi::kMaxOutliers) return KIVI_EINVAL;
   return KIVI_OK;

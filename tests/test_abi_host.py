@@ -90,6 +90,7 @@ def test_scale_slot_maps_are_permutations(K):
     (dict(bits=5), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
+    (dict(n_kv_heads=4096, n_q_heads=4096 * 68), 2),  # attention grid y: 4096 x 17 chunks
 ])
 def test_config_validation(K, bad, status):
     with pytest.raises(K.KiviError) as e:
