@@ -154,8 +154,15 @@ def test_compression_closed_form(oracle):
     assert kb == notebook
     assert fp16 / kb >= g["compression_at_least"]
     assert fp16 / kb == pytest.approx(16 / (2 + 32 / 32))
+    # b bits per element + 32 bits of (min, scale) per G elements, every width
+    for bits in (2, 3, 4, 8):
+        kb_b, _ = _live_bytes(oracle, 1024, 128, bits, 32, 32)
+        assert fp16 / kb_b == pytest.approx(16 / (bits + 32 / 32))
+        c = oracle.OracleCache(bits, 32, 32, 128, 1, 1, 64)
+        c.prefill(*_rand_kv(1, 1, 64, 128, bits))
+        assert c.export()["codes_k"].shape[-1] == 128 * bits // 8  # the live row is D*b/8 bytes
     for l in (1, 31, 32, 33, 1000, 4097):
-        for bits in (2, 4):
+        for bits in (2, 3, 4, 8):
             r64 = sum(_live_bytes(oracle, l, 64, bits, 32, 32)) / (2 * l * 64 * 2)
             r128 = sum(_live_bytes(oracle, l, 128, bits, 32, 32)) / (2 * l * 128 * 2)
             assert r64 == pytest.approx(r128)
