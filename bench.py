@@ -95,18 +95,29 @@ def peak_hbm():
         return 6800.0, "fallback"
 
 
+def kernel_source_hash() -> str:
+    """sha256 of the attention kernel's sources (the kernel and the tile
+    layout) with comments and whitespace removed: a comment edit keeps a
+    recorded capture valid, a code edit does not."""
+    import re
+    csrc = os.path.join(ROOT, "bit_kv_cache_kivi_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("attention.cu", "kivi_internal.cuh"):
+        src = open(os.path.join(csrc, name)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)  # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                # line comments
+        h.update(" ".join(src.split()).encode())
+    return h.hexdigest()
+
+
 def kernel_traffic():
     """Per-launch DRAM bytes of the attention kernel from a committed ncu
-    capture, valid only while the kernel source is unchanged."""
+    capture, valid only while the kernel's code is unchanged."""
     p = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    csrc = os.path.join(ROOT, "bit_kv_cache_kivi_gb300", "csrc")
     try:
         with open(p) as f:
             rec = json.load(f)
-        h = hashlib.sha256()
-        for name in ("attention.cu", "kivi_internal.cuh"):  # the kernel and the tile layout
-            h.update(open(os.path.join(csrc, name), "rb").read())
-        return rec["bytes_per_launch"] if rec.get("source_sha256") == h.hexdigest() else None
+        return rec["bytes_per_launch"] if rec.get("source_sha256") == kernel_source_hash() else None
     except Exception:
         return None
 

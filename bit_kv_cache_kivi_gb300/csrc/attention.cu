@@ -14,14 +14,15 @@
 // group, and with more than one group the last group merges the groups;
 // nothing ever waits on another CTA.
 //
-// Packed tiles at 2 bits run on the tensor cores (mma.sync m16n8k16, fp16
-// operands, fp32 accumulation).  Each warp streams its tiles through its own
-// ring of staged tiles (one lane issues a bulk copy per array and tile,
-// completion on an mbarrier) and keeps an online softmax per head:
+// Packed tiles (2, 3, 4 or 8 bits) run on the tensor cores (mma.sync
+// m16n8k16, fp16 operands, fp32 accumulation).  Each warp streams its tiles
+// through its own ring of staged tiles (one lane issues one bulk copy per
+// tile, completion on an mbarrier) and keeps an online softmax per head:
 //   scores  S[t, j] = sum_d c_td (q_jd s_d) + beta_j, beta_j = sum_d q_jd z_d
 //   output  O[d, j] = sum_t c_td (p_jt s_t,g(d)) + sum_t p_jt z_t,g(d)
-// The codes c enter the MMA as fp16 subnormals c * 4^i * 2^-24 (the masked
-// code bits are the whole encoding); the fp32 factors q*s and p*s enter as an
+// The codes c enter the MMA as fp16 subnormals c * base^i * 2^-24 (the masked
+// code bits are the whole encoding; base 4 at 2 and 3 bits, 16 at 4, 1 at 8);
+// the fp32 factors q*s and p*s enter as an
 // fp16 hi/lo pair (hi = fp16(x), lo = fp16(x - hi)) in the 8 columns of the
 // n=8 operand as (head, hi) and (head, lo): four query heads per MMA, and the
 // sum hi + lo recovers x to about 2^-22.  Each query head is first scaled by a
