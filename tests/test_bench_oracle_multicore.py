@@ -1,0 +1,28 @@
+"""The all-cores oracle timing of bench.py: the (batch, KV head) units are
+split over spawned host processes, each unit exactly once, so the bytes the
+processes report add up to the whole batch's decode-attention bytes at every
+timed step.  CPU only (no GPU, no kernel)."""
+import sys
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from bit_kv_cache_kivi_gb300 import workloads as W  # noqa: E402
+
+
+def test_units_partition_and_bytes():
+    wl = W.synthetic("mc", B=3, Hq=8, Hkv=2, T=70, R=32, steps=4, seed=5)
+    r = bench.run_oracle_multicore(steps=3, warmup=1, wl=wl, max_procs=4)
+    assert r["cores"] == 4 and r["steps"] == 3 and r["kind"] == "oracle"
+    # timed steps 1..3 follow one warm-up append: contexts T+2, T+3, T+4
+    want = sum(bench.attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T + 2 + i, wl.R, 2) for i in range(3))
+    assert r["bytes"] == want
+    assert r["value"] > 0 and "6 (batch, KV head) units" in r["sample"]
+
+
+def test_more_processes_than_units_is_capped():
+    wl = W.synthetic("mc1", B=1, Hq=4, Hkv=1, T=40, R=32, steps=2, seed=6)
+    r = bench.run_oracle_multicore(steps=1, warmup=1, wl=wl, max_procs=8)
+    assert r["cores"] == 1 and r["steps"] == 1
+    assert r["bytes"] == bench.attn_bytes(1, 1, 4, wl.D, wl.T + 2, wl.R, 2)
