@@ -637,27 +637,52 @@ def run_oracle(steps, warmup, budget_s=None):
             "tokens_per_s": round(done / (t_app + t_att), 3), "steps": done}
 
 
-def _oracle_units_worker(units, R, D, cap, barrier, results, warmup, steps, budget_s):
-    """One host process of the multi-core oracle run: its (b, kv-head) units,
-    each an untouched single-unit oracle cache (4 query heads), prefilled
-    outside the timed region; `warmup` untimed decode steps (append +
-    attention on every unit), then from the shared start `steps` timed ones,
-    or fewer once `budget_s` has passed."""
+def _oracle_units_worker(job, units, cfg, barrier, results, warmup, steps, budget_s):
+    """One host process of a multi-process oracle run over (b, kv-head) units,
+    each an untouched single-unit oracle cache.  Everything before the shared
+    start (a barrier) is untimed.  cfg = (bits, R, D, capacity).
+
+    job "decode": units (k, v, k_new, v_new, q); prefill, `warmup` decode
+      steps (append + attention on every unit), then `steps` timed ones, or
+      fewer once `budget_s` has passed; bytes are the attention's.
+    job "prefill": units (k, v); one unit prefilled as a warm-up, then every
+      unit's prefill timed; bytes are the quantizer's.
+    job "attention": units (k, v, q); prefill, then `steps` timed attention
+      calls per unit."""
     try:
         from oracle.kivi_oracle import OracleCache
-        caches = []
-        for k, v, kn, vn, q in units:
-            o = OracleCache(2, G, R, D, 1, 1, cap)
-            o.prefill(k, v)
-            caches.append((o, kn, vn, q))
+        bits, R, D, cap = cfg
+        caches = [OracleCache(bits, G, R, D, 1, 1, cap) for _ in units]
+        if job == "prefill":
+            OracleCache(bits, G, R, D, 1, 1, cap).prefill(units[0][0], units[0][1])
+            barrier.wait(timeout=600)
+            t0 = time.perf_counter()
+            nbytes = 0
+            for o, (k, v) in zip(caches, units):
+                o.prefill(k, v)
+                nbytes += prefill_bytes(1, 1, D, k.shape[2], R, bits, k.dtype.itemsize)
+            results.put(("ok", nbytes, time.perf_counter() - t0, 1))
+            return
+        for o, u in zip(caches, units):
+            o.prefill(u[0], u[1])
+        if job == "attention":
+            barrier.wait(timeout=600)
+            t0 = time.perf_counter()
+            nbytes = 0
+            for _ in range(steps):
+                for o, (_, _, q) in zip(caches, units):
+                    o.attention(q)
+                    nbytes += attn_bytes(1, 1, q.shape[1], D, o.length, R, bits)
+            results.put(("ok", nbytes, time.perf_counter() - t0, steps))
+            return
 
         def one(i):
             nb = 0
-            for o, kn, vn, q in caches:
+            for o, (_, _, kn, vn, q) in zip(caches, units):
                 t = o.length
                 o.append(kn[i], vn[i])
                 o.attention(q)
-                nb += attn_bytes(1, 1, q.shape[1], D, t + 1, R, 2)
+                nb += attn_bytes(1, 1, q.shape[1], D, t + 1, R, bits)
             return nb
 
         for i in range(warmup):
@@ -675,34 +700,23 @@ def _oracle_units_worker(units, R, D, cap, barrier, results, warmup, steps, budg
         results.put(("error", repr(e), 0.0, 0))
 
 
-def run_oracle_multicore(steps=64, warmup=1, budget_s=None, wl=None, max_procs=None):
-    """The CPU oracle on every host core: the main workload's 64 (batch, KV
-    head) units split over one spawned process per core (spawn, since the GPU
-    is already in use in this process), each timing decode steps of its units
-    concurrently.  value = attention bytes of all processes / the slowest
-    process's wall time."""
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def oracle_pool(job, units, cfg, nproc, warmup=0, steps=1, budget_s=None):
+    """Runs `job` over `units` on `nproc` spawned processes (spawn: the GPU is
+    already in use in this process), unit i on process i mod nproc, all
+    starting the timed part together.  Returns (bytes of all processes, the
+    slowest process's seconds, sorted steps per process)."""
     import multiprocessing as mp
-    from bit_kv_cache_kivi_gb300 import workloads as W
-    if wl is None:
-        wl = W.llama3_8b_decode(steps=warmup + steps)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
-    nproc = max(1, min(cores, len(pairs), max_procs or len(pairs)))
-    g = wl.Hq // wl.Hkv
+    nproc = max(1, min(nproc, len(units)))
     ctx = mp.get_context("spawn")
     barrier, results = ctx.Barrier(nproc), ctx.Queue()
     procs = []
     for w in range(nproc):
-        units = []
-        for b, h in pairs[w::nproc]:
-            units.append((np.ascontiguousarray(wl.k[b:b + 1, h:h + 1]),
-                          np.ascontiguousarray(wl.v[b:b + 1, h:h + 1]),
-                          np.ascontiguousarray(wl.k_new[:, b:b + 1, h:h + 1]),
-                          np.ascontiguousarray(wl.v_new[:, b:b + 1, h:h + 1]),
-                          np.ascontiguousarray(wl.q[b:b + 1, h * g:(h + 1) * g].astype(np.float32))))
         p = ctx.Process(target=_oracle_units_worker,
-                        args=(units, wl.R, wl.D, wl.capacity, barrier, results, warmup, steps,
-                              budget_s))
+                        args=(job, units[w::nproc], cfg, barrier, results, warmup, steps, budget_s))
         p.start()
         procs.append(p)
     got = []
@@ -717,15 +731,107 @@ def run_oracle_multicore(steps=64, warmup=1, budget_s=None, wl=None, max_procs=N
                 p.join()
     errs = [r[1] for r in got if r[0] != "ok"]
     if errs:
-        raise RuntimeError(f"multi-core oracle run failed: {errs[0]}")
-    nbytes = sum(r[1] for r in got)
-    wall = max(r[2] for r in got)
-    steps = sorted(r[3] for r in got)
+        raise RuntimeError(f"oracle {job} run failed: {errs[0]}")
+    return sum(r[1] for r in got), max(r[2] for r in got), sorted(r[3] for r in got)
+
+
+def _unit(a, b, h):
+    return np.ascontiguousarray(a[b:b + 1, h:h + 1])
+
+
+def _decode_units(wl, pairs):
+    g = wl.Hq // wl.Hkv
+    return [(_unit(wl.k, b, h), _unit(wl.v, b, h),
+             np.ascontiguousarray(wl.k_new[:, b:b + 1, h:h + 1]),
+             np.ascontiguousarray(wl.v_new[:, b:b + 1, h:h + 1]),
+             np.ascontiguousarray(wl.q[b:b + 1, h * g:(h + 1) * g].astype(np.float32)))
+            for b, h in pairs]
+
+
+def run_oracle_multicore(steps=64, warmup=1, budget_s=None, wl=None, max_procs=None):
+    """The CPU oracle on every host core: the main workload's 64 (batch, KV
+    head) units split over one process per core, each timing decode steps of
+    its units concurrently.  value = attention bytes of all processes / the
+    slowest process's wall time."""
+    from bit_kv_cache_kivi_gb300 import workloads as W
+    if wl is None:
+        wl = W.llama3_8b_decode(steps=warmup + steps)
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+    nproc = max(1, min(host_cores(), len(pairs), max_procs or len(pairs)))
+    nbytes, wall, steps = oracle_pool("decode", _decode_units(wl, pairs), (wl.bits, wl.R, wl.D, wl.capacity),
+                                      nproc, warmup, steps, budget_s)
     return {"value": round(nbytes / wall / 1e9, 4), "unit": "GB/s", "cores": nproc, "kind": "oracle",
             "sample": f"all {len(pairs)} (batch, KV head) units of {wl.name} at context "
                       f"~{wl.T + warmup}, {len(pairs) // nproc}-{-(-len(pairs) // nproc)} units per process, "
                       f"{nproc} processes, {steps[0]}-{steps[-1]} decode steps (append + attention) each",
             "steps": steps[0], "bytes": nbytes, "tokens_per_s": round(wl.B * sum(steps) / len(steps) / wall, 3)}
+
+
+def _cpu_entry(nbytes, wall, nproc, sample, unit_tokens=None):
+    e = {"gbs": round(nbytes / wall / 1e9, 4), "seconds": round(wall, 3), "cores": nproc,
+         "kind": "oracle", "sample": sample}
+    if unit_tokens is not None:
+        e["tokens_per_s"] = round(unit_tokens / wall, 3)
+    return e
+
+
+def oracle_workload_baselines(res: dict, cores=None, quant_units=2) -> None:
+    """The oracle beside the GPU numbers of the other workloads, each on a
+    bounded sample: the 32k-token bf16 prefill quantizer (2- and 4-bit) on
+    `quant_units` (b, kv-head) units single-threaded and on all 32 units over
+    every core; the 131k-token attention on one unit single-threaded and on
+    all 8 over the cores; the streaming decode (GQA 7, 2048 + 512 steps of
+    append + attention) on one unit per core.  Adds "cpu_oracle" to the
+    entries of `res` (a workloads dict) that exist."""
+    from bit_kv_cache_kivi_gb300 import workloads as W
+    cores = cores or host_cores()
+    if any(f"prefill_quantize_{b}bit" in res for b in (2, 4)):
+        wl = W.prefill_quantize(2)
+        pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+        units = [(_unit(wl.k, b, h), _unit(wl.v, b, h)) for b, h in pairs]
+        del wl.k, wl.v
+        for bits in (2, 4):
+            key = f"prefill_quantize_{bits}bit"
+            if key not in res:
+                continue
+            cfg = (bits, wl.R, wl.D, wl.capacity)
+            n1, w1, _ = oracle_pool("prefill", units[:quant_units], cfg, 1)
+            nm = min(cores, len(units))
+            nb, wm, _ = oracle_pool("prefill", units, cfg, nm)
+            res[key]["cpu_oracle"] = {
+                "single": _cpu_entry(n1, w1, 1, f"prefill of {quant_units} of the {len(units)} "
+                                                f"(batch, KV head) units, one thread"),
+                "multicore": _cpu_entry(nb, wm, nm, f"prefill of all {len(units)} units, "
+                                                    f"{nm} processes")}
+        del units
+    if "long_context_attention" in res:
+        wl = W.long_context()
+        g = wl.Hq // wl.Hkv
+        units = [(_unit(wl.k, 0, h), _unit(wl.v, 0, h),
+                  np.ascontiguousarray(wl.q[0:1, h * g:(h + 1) * g].astype(np.float32)))
+                 for h in range(wl.Hkv)]
+        del wl.k, wl.v
+        cfg = (wl.bits, wl.R, wl.D, wl.capacity)
+        n1, w1, _ = oracle_pool("attention", units[:1], cfg, 1)
+        nm = min(cores, len(units))
+        nb, wm, _ = oracle_pool("attention", units, cfg, nm)
+        res["long_context_attention"]["cpu_oracle"] = {
+            "single": _cpu_entry(n1, w1, 1, f"one attention over KV head 0 ({g} query heads) at "
+                                            f"context {wl.T}, one thread"),
+            "multicore": _cpu_entry(nb, wm, nm, f"one attention over all {wl.Hkv} KV heads, {nm} processes")}
+        del units
+    if "streaming_decode" in res:
+        wl = W.streaming()
+        pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+        nm = min(cores, len(pairs))
+        units = _decode_units(wl, pairs[:nm])
+        cfg = (wl.bits, wl.R, wl.D, wl.capacity)
+        nb, wm, st = oracle_pool("decode", units, cfg, nm, 0, wl.steps)
+        res["streaming_decode"]["cpu_oracle"] = {
+            "multicore": _cpu_entry(nb, wm, nm, f"{nm} of the {len(pairs)} (batch, KV head) units, one per "
+                                                f"process, all {st[0]} steps (append + attention) from "
+                                                f"context {wl.T}; tokens_per_s counts a token per "
+                                                f"{wl.Hkv} unit-steps", nm * st[0] / wl.Hkv)}
 
 
 def combine_ranks(result: dict) -> dict:
@@ -801,6 +907,8 @@ def main():
         if not args.no_cpu_baseline and world == 1:
             result["cpu_baseline"] = run_oracle(args.steps, 2, budget_s=12.0)
             result["cpu_baseline"]["multicore"] = run_oracle_multicore(budget_s=8.0)
+            if "workloads" in result:
+                oracle_workload_baselines(result["workloads"])
         print(json.dumps(result))
 
 

@@ -1,7 +1,8 @@
-"""The all-cores oracle timing of bench.py: the (batch, KV head) units are
-split over spawned host processes, each unit exactly once, so the bytes the
-processes report add up to the whole batch's decode-attention bytes at every
-timed step.  CPU only (no GPU, no kernel)."""
+"""The multi-process oracle timing of bench.py: the (batch, KV head) units
+are split over spawned host processes, each unit exactly once, so the bytes
+the processes report add up to the whole batch's -- decode-attention bytes at
+every timed step, the quantizer's bytes of a prefill, the attention's bytes
+of every timed call.  CPU only (no GPU, no kernel)."""
 import sys
 
 from conftest import ROOT
@@ -26,3 +27,18 @@ def test_more_processes_than_units_is_capped():
     r = bench.run_oracle_multicore(steps=1, warmup=1, wl=wl, max_procs=8)
     assert r["cores"] == 1 and r["steps"] == 1
     assert r["bytes"] == bench.attn_bytes(1, 1, 4, wl.D, wl.T + 2, wl.R, 2)
+
+
+def test_prefill_and_attention_jobs_count_every_unit():
+    wl = W.synthetic("mc2", B=2, Hq=6, Hkv=3, T=200, R=64, steps=0, seed=7, dtype="bf16")
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+    cfg = (4, wl.R, wl.D, wl.capacity)
+    units = [(bench._unit(wl.k, b, h), bench._unit(wl.v, b, h)) for b, h in pairs]
+    nb, wall, _ = bench.oracle_pool("prefill", units, cfg, 4)
+    assert nb == bench.prefill_bytes(wl.B, wl.Hkv, wl.D, wl.T, wl.R, 4, 2) and wall > 0
+    g = wl.Hq // wl.Hkv
+    qs = [wl.q[b:b + 1, h * g:(h + 1) * g].astype("float32") for b, h in pairs]
+    units = [u + (q,) for u, q in zip(units, qs)]
+    nb, _, steps = bench.oracle_pool("attention", units, cfg, 3, steps=2)
+    assert steps == [2, 2, 2]
+    assert nb == 2 * bench.attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T, wl.R, 4)
