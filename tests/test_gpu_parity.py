@@ -203,6 +203,23 @@ def test_attention_split_count_invariance():
         assert T.attn_err(x, outs[0]) <= T.ATTN_TOL
 
 
+def test_attention_maximum_splits():
+    """The split cap: one (batch, kv-head) unit at 65320 tokens (2040 packed
+    tiles and a 40-token tail) plans 255 packed splits of 8 tiles and one
+    tail split, so 256 partials merge in two full levels of 16.  Overrides
+    of 241 and 17 plan 228 splits (a last group of 4) and 17 (a last group
+    of one)."""
+    wl = W.synthetic("mx", B=1, Hq=4, Hkv=1, T=65320, R=32, seed=29)
+    g, o = run_prefill(wl, capacity=65536)
+    assert g.splits() == 256
+    outs = [check_attention(g, o, wl)]
+    for s, planned in ((241, 228), (17, 17)):
+        outs.append(check_attention(g, o, wl, splits=s))
+        assert g.splits() == planned
+    for x in outs[1:]:
+        assert T.attn_err(x, outs[0]) <= T.ATTN_TOL
+
+
 @pytest.mark.parametrize("q_dtype", ["f32", "bf16"])
 def test_attention_query_dtypes(q_dtype):
     wl = W.synthetic("qd", B=2, Hq=4, Hkv=2, T=500, R=32, q_dtype=q_dtype, seed=21)

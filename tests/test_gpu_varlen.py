@@ -118,6 +118,25 @@ def test_ragged_large_batch(R):
     _check_attention(g, o, wl)
 
 
+def test_ragged_maximum_batch():
+    """The per-sequence length limit, 1024 sequences, lengths 0..300 (some
+    empty until the first append), three single-token appends, then every
+    sequence against its own oracle cache."""
+    rng = np.random.default_rng(1024)
+    lens = [int(x) for x in rng.integers(0, 301, 1024)]
+    lens[:3] = [0, 31, 32]
+    wl = W.synthetic("vm", B=1024, Hq=4, Hkv=1, T=max(lens), R=32, steps=3, seed=77)
+    cap = 320
+    g = T.gpu_cache(wl, capacity=cap)
+    g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"), lengths=lens)
+    o = _oracles(wl, lens, cap, 2, T.ALG1)
+    for i in range(wl.steps):
+        _append_all(g, o, wl.k_new[i], wl.v_new[i], "f16")
+    assert g.lengths == [l + wl.steps for l in lens]
+    _check_state(g, o, 32, T.ALG1)
+    _check_attention(g, o, wl)
+
+
 def test_ragged_split_override():
     """A fixed split count with ragged lengths: sequences shorter than the
     count use fewer splits; the merge counts each sequence's own."""
