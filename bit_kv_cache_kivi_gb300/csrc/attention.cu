@@ -266,6 +266,19 @@ __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
   }
 }
 
+// Diagnostics: one thread waits, with the bounded wait above, on phase 0 of
+// an mbarrier that nothing completes (no copy is issued, no thread arrives),
+// and records the timeout in *status as a packed split does in the
+// workspace status word.
+__global__ void wait_probe_kernel(int* status) {
+  __shared__ __align__(8) unsigned long long bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+    if (!mbar_wait(&bar, 0u)) atomicOr(status, 1);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // A tail split on CUDA cores: tokens [c0, c0 + n), n <= kTailTok, of the tail
 // [t_tail, l), staged in one round of copies (fp16 residual rows, packed rows
@@ -1446,6 +1459,11 @@ cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a
   lc.attrs = at;
   lc.numAttrs = 1;
   return cudaLaunchKernelEx(&lc, attn_kernel<BITS>, cv, a, lens);
+}
+
+cudaError_t launch_wait_probe(int* status, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens, cudaStream_t st) {

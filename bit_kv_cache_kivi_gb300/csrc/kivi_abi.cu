@@ -603,6 +603,17 @@ KIVI_API const char* kivi_status_string(kivi_status s) {
 
 KIVI_API int kivi_last_cuda_error(void) { return g_last_cuda_error; }
 
+// The attention's bounded wait on a barrier phase nothing completes: the
+// probe returns after the wait limit with 1 ORed into *status.
+KIVI_API kivi_status kivi_check_bounded_wait(int* status, void* stream) {
+  if (!status || ((uintptr_t)status & 3u)) return KIVI_EINVAL;
+  int dev = 0;
+  const kivi_status ds = cuda_status(cudaGetDevice(&dev));
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(status, dev)) return KIVI_EINVAL;
+  return cuda_status(kivi::launch_wait_probe(status, static_cast<cudaStream_t>(stream)));
+}
+
 // ---------------------------------------------------------------------------
 // Decode attention without a caller-provided workspace.
 //

@@ -296,5 +296,8 @@ __device__ __forceinline__ void grid_dependency_wait() {
 
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
                              cudaStream_t st);
+// One CTA runs the attention's bounded mbarrier wait on a phase that nothing
+// completes and ORs 1 into *status (device memory) when it gives up.
+cudaError_t launch_wait_probe(int* status, cudaStream_t st);
 
 }  // namespace kivi

@@ -86,6 +86,7 @@ def lib() -> C.CDLL:
                 "kivi_last_cuda_error": (i32, []),
                 "kivi_decode_attention_static": (i32, [vp, vp, i32, vp, f32, vp]),
                 "kivi_decode_step": (i32, [vp, vp, vp, i32, vp, i32, vp, f32, vp, sz, vp]),
+                "kivi_check_bounded_wait": (i32, [vp, vp]),
             }
             for name, (res, args) in sigs.items():
                 fn = getattr(L, name)
@@ -121,6 +122,14 @@ def _ptr(t) -> int:
 
 def kivi_status_string(status: int) -> str:
     return lib().kivi_status_string(status).decode()
+
+
+def kivi_check_bounded_wait(status: torch.Tensor, stream=None) -> None:
+    """Runs the attention's bounded wait on a barrier phase nothing completes;
+    ORs 1 into status (one int32 on the current device) when it gives up."""
+    if not (isinstance(status, torch.Tensor) and status.dtype == torch.int32 and status.numel() >= 1):
+        raise KiviError(KIVI_EINVAL, "kivi_check_bounded_wait: status must be an int32 tensor")
+    _check(lib().kivi_check_bounded_wait(status.data_ptr(), _stream(stream)), "kivi_check_bounded_wait")
 
 
 def kivi_cache_sizes(cfg: kivi_config) -> list[int]:

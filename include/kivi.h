@@ -303,6 +303,21 @@ void kivi_cache_destroy(kivi_cache *c);      /* NULL is a no-op */
 const char *kivi_status_string(kivi_status s);
 int kivi_last_cuda_error(void); /* cudaError_t of the last failed launch on this thread */
 
+/* Diagnostics for the attention's failure path (no counterpart on the pages).
+ * A packed split waits for each staged tile on an mbarrier, for at most
+ * 200 ms; if a wait gives up, the split stops issuing copies, ORs 1 into the
+ * workspace status word and still completes the merge protocol, so the
+ * launch ends and the context stays usable.  This call runs that same
+ * bounded wait in one CTA on a barrier phase that nothing completes (no
+ * copy is issued and no thread arrives), then ORs 1 into *status.
+ * - status: one int, 4-byte aligned, device memory on the current device,
+ *   or managed or mapped pinned host memory; the caller owns it and reads it
+ *   after the stream has run the probe.
+ * - Asynchronous on stream; the probe occupies one SM for about 200 ms.
+ * - KIVI_EINVAL for a null, misaligned or unreachable pointer (nothing is
+ *   launched); KIVI_ECUDA if the launch fails. */
+kivi_status kivi_check_bounded_wait(int *status, void *stream);
+
 /* Size of the library's fixed device scratch area used by
  * kivi_decode_attention_static: 8 MiB, held on every GPU that loads the
  * library until the process exits. */

@@ -256,3 +256,11 @@ def test_varlen_batch_limit(K):
         assert K.kivi_cache_length(h) == 3
     finally:
         K.kivi_cache_destroy(h)
+
+
+def test_bounded_wait_probe_refusals(K):
+    """The wait probe checks its status pointer before anything else: null
+    and misaligned pointers are refused without a launch (no GPU needed)."""
+    lib = K.lib()
+    assert lib.kivi_check_bounded_wait(None, None) == K.KIVI_EINVAL
+    assert lib.kivi_check_bounded_wait(0x10002, None) == K.KIVI_EINVAL
