@@ -427,18 +427,21 @@ class KiviCache:
         i16 = u8[:(u8.numel() // 2) * 2].view(torch.int16)
         st8 = (H * nt * tb, nt * tb, tb)
         st16 = tuple(x // 2 for x in st8)
+        # as_strided offsets count from the start of the storage, and the
+        # tile buffer may itself be a view into a larger allocation
+        b8, b16 = u8.storage_offset(), i16.storage_offset()
         o_sk = 2 * G * rb  # byte offset of the key scales in a tile
-        out = {"codes_k": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), 0),
-               "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), G * rb),
-               "scale_k": i16.as_strided((B, H, nt, D), st16 + (1,), o_sk // 2),
-               "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 2 * D) // 2),
-               "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 4 * D) // 2),
-               "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), (o_sk + 6 * D) // 2)}
+        out = {"codes_k": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8),
+               "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8 + G * rb),
+               "scale_k": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + o_sk // 2),
+               "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 2 * D) // 2),
+               "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 4 * D) // 2),
+               "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 6 * D) // 2)}
         n = c.outlier_channels
         if n:  # the outlier block after the base tile: indices, then values [G][n]
             o_ob = 2 * G * rb + 8 * D
-            out["outl_idx"] = u8.as_strided((B, H, nt, n), st8 + (1,), o_ob)
-            out["outl_val"] = i16.as_strided((B, H, nt, G, n), st16 + (n, 1), (o_ob + 16) // 2)
+            out["outl_idx"] = u8.as_strided((B, H, nt, n), st8 + (1,), b8 + o_ob)
+            out["outl_val"] = i16.as_strided((B, H, nt, G, n), st16 + (n, 1), b16 + (o_ob + 16) // 2)
         sv = self.state_views()
         out["ring_k"], out["ring_v"] = sv["ring_k"], sv["ring_v"]
         return out

@@ -1,0 +1,29 @@
+"""The binding's inspection views read the arrays inside the cache's own
+buffers wherever those buffers start: a tile buffer that is a view into a
+larger allocation (as when a caller hands the cache part of a pool) gives the
+same views as a fresh buffer holding the same bytes.  CPU only: the C handle
+is made over host buffers and no kernel runs."""
+import pytest
+import torch
+
+
+@pytest.mark.parametrize("bits,n_out", [(2, 0), (3, 0), (4, 2), (8, 0)])
+def test_views_of_an_offset_buffer(bits, n_out):
+    from bit_kv_cache_kivi_gb300 import kivi as K
+    kw = dict(batch=2, n_kv_heads=2, n_q_heads=4, max_tokens=128, bits=bits, outliers=n_out,
+              device="cpu")
+    fresh, offset = K.KiviCache(**kw), K.KiviCache(**kw)
+    gen = torch.Generator().manual_seed(bits)
+    for n in K.BUFFER_NAMES:
+        src = torch.randint(0, 256, fresh.buffers[n].shape, dtype=torch.uint8, generator=gen)
+        fresh.buffers[n].copy_(src)
+        pool = torch.zeros(src.numel() + 8192, dtype=torch.uint8)
+        offset.buffers[n] = pool[4096:4096 + src.numel()]
+        offset.buffers[n].copy_(src)
+    a, b = fresh.layout_views(), offset.layout_views()
+    assert a.keys() == b.keys()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    la, lb = fresh.logical_state(), offset.logical_state()
+    for k in la:
+        assert torch.equal(la[k], lb[k]), k
