@@ -264,3 +264,30 @@ def test_bounded_wait_probe_refusals(K):
     lib = K.lib()
     assert lib.kivi_check_bounded_wait(None, None) == K.KIVI_EINVAL
     assert lib.kivi_check_bounded_wait(0x10002, None) == K.KIVI_EINVAL
+
+
+@pytest.mark.parametrize("batch,n_kv,n_q,R,bits,cap", [
+    (1, 1, 4, 32, 2, 4096), (8, 8, 32, 32, 2, 4224), (1, 8, 32, 128, 2, 8192),
+    (64, 4, 28, 32, 2, 2592), (200, 8, 32, 64, 4, 1024), (3, 2, 8, 32, 8, 2048),
+    (2, 2, 16, 32, 3, 2048)])
+def test_split_plan_invariants(K, batch, n_kv, n_q, R, bits, cap):
+    """At every length up to the capacity: at least one split and at most
+    256; no more than one wave of the grid (attn_ctas_per_sm CTAs on each of
+    152 SMs over the (batch, kv-head, head chunk) units), except for lengths
+    held entirely in the tail, which take their tail splits; and a workspace
+    that holds every split's partial."""
+    c = cfg(K, batch=batch, n_kv_heads=n_kv, n_q_heads=n_q, residual=R, bits=bits, max_tokens=cap)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    try:
+        units = batch * n_kv * -(-(n_q // n_kv) // 4)
+        budget = max(min((2 if bits == 8 else 4) * 152 // units, 256), 1)
+        max_tail = -(-(R + 31) // 64)
+        most = 0
+        for l in range(1, cap + 1):
+            s = K.kivi_attention_splits(h, l)
+            assert 1 <= s <= 256, l
+            assert s <= max(budget, max_tail), (l, s, budget)
+            most = max(most, s)
+        assert K.kivi_attention_workspace_bytes(h) >= units * most * 4 * (128 + 2) * 4
+    finally:
+        K.kivi_cache_destroy(h)
