@@ -31,6 +31,7 @@ import argparse
 import hashlib
 import json
 import os
+import queue
 import subprocess
 import sys
 import threading
@@ -697,6 +698,7 @@ def _oracle_units_worker(job, units, cfg, barrier, results, warmup, steps, budge
                 break
         results.put(("ok", nbytes, time.perf_counter() - t0, done))
     except Exception as e:  # reported to the parent, which fails the run
+        barrier.abort()  # the other processes stop waiting for this one
         results.put(("error", repr(e), 0.0, 0))
 
 
@@ -721,8 +723,16 @@ def oracle_pool(job, units, cfg, nproc, warmup=0, steps=1, budget_s=None):
         procs.append(p)
     got = []
     try:
-        for _ in range(nproc):
-            got.append(results.get(timeout=900))
+        deadline = time.monotonic() + 900
+        while len(got) < nproc:
+            try:
+                got.append(results.get(timeout=1.0))
+            except queue.Empty:
+                # a process that ended without reporting (a crash) fails the run
+                dead = [p.exitcode for p in procs if p.exitcode not in (None, 0)]
+                if dead or time.monotonic() > deadline:
+                    raise RuntimeError(f"oracle {job} run: a process ended without a result "
+                                       f"(exit codes {dead})" if dead else f"oracle {job} run timed out")
     finally:
         for p in procs:
             p.join(timeout=30)

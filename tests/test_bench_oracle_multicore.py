@@ -42,3 +42,19 @@ def test_prefill_and_attention_jobs_count_every_unit():
     nb, _, steps = bench.oracle_pool("attention", units, cfg, 3, steps=2)
     assert steps == [2, 2, 2]
     assert nb == 2 * bench.attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T, wl.R, 4)
+
+
+def test_worker_failure_before_the_start_fails_fast():
+    """A process whose prefill fails before the shared start aborts the
+    barrier, so the run fails at once instead of after the barrier's
+    timeout (a planted error: K and V of different lengths)."""
+    import time
+    import numpy as np
+    import pytest
+    wl = W.synthetic("mf", B=2, Hq=4, Hkv=1, T=40, R=32, steps=0, seed=8)
+    good = (bench._unit(wl.k, 0, 0), bench._unit(wl.v, 0, 0))
+    bad = (bench._unit(wl.k, 1, 0), np.ascontiguousarray(bench._unit(wl.v, 1, 0)[:, :, :39]))
+    t0 = time.monotonic()
+    with pytest.raises(RuntimeError, match="oracle prefill run failed"):
+        bench.oracle_pool("prefill", [good, bad], (2, wl.R, wl.D, wl.capacity), 2)
+    assert time.monotonic() - t0 < 60
