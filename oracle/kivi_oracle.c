@@ -159,7 +159,8 @@ float orc_dequant(int q, uint16_t scale16, uint16_t zero16) {
 }
 
 void orc_pack_row(const uint8_t *codes, int D, int bits, uint8_t *out) {
-  memset(out, 0, (size_t)(D * bits / 8));
+  if (D <= 0 || bits <= 0) return; /* an empty row packs to nothing */
+  memset(out, 0, (size_t)D * (size_t)bits / 8u);
   for (int e = 0; e < D; e++)
     out[(e * bits) / 8] |= (uint8_t)(codes[e] << ((e * bits) % 8));
 }
@@ -230,15 +231,17 @@ static int hi_bit_value(int e) {
   return 16 * w + orc_hi_bit(gp / 2, 4 * (gp % 2) + c);
 }
 
+/* rows of 1..4096 channels (the caches use D = 128); others pack nothing */
 static void pack_row3(const uint8_t *codes, int D, int G, int value, uint8_t *out) {
   uint8_t lo[4096];
+  if (D <= 0 || D > 4096) return;
   for (int e = 0; e < D; e++) lo[e] = codes[e] & 3;
   if (value)
     orc_pack_row_v(lo, D, 2, G, out);
   else
     orc_pack_row(lo, D, 2, out);
   uint8_t *hi = out + D / 4;
-  memset(hi, 0, (size_t)(D / 8));
+  memset(hi, 0, (size_t)D / 8u);
   for (int e = 0; e < D; e++) {
     int bit = value ? hi_bit_value(e) : hi_bit_key(e);
     hi[bit / 8] |= (uint8_t)(((codes[e] >> 2) & 1) << (bit % 8));
