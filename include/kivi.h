@@ -41,7 +41,7 @@
  *     reports a launch error (see kivi_last_cuda_error).
  *   - A handle is not thread-safe; calls on one handle must be serialized
  *     by the caller (the stream orders the device work).
- *   - Supported by this build: bits 2, 3, 4 or 8, group 32, head_dim 128,
+ *   - Supported by this library: bits 2, 3, 4 or 8, group 32, head_dim 128,
  *     residual a multiple of 32, any batch / head counts with
  *     n_q_heads a multiple of n_kv_heads.
  *   - Inputs must be finite and within the fp16 range; every input element
@@ -131,9 +131,9 @@ typedef enum { KIVI_POLICY_ALG1 = 0, KIVI_POLICY_SHARED = 1 } kivi_policy;
  * residual length) plus the tensor shape. */
 typedef struct {
   int bits;        /* 2, 3, 4 or 8 */
-  int group;       /* G: 32 in this build */
+  int group;       /* G: 32 in this library */
   int residual;    /* R: fp16 window, a multiple of G */
-  int head_dim;    /* D: 128 in this build */
+  int head_dim;    /* D: 128 in this library */
   int batch;       /* B */
   int n_kv_heads;  /* H */
   int n_q_heads;   /* a multiple of n_kv_heads; query head j reads KV head j/(Hq/H) */
@@ -154,7 +154,7 @@ typedef struct {
 typedef struct kivi_cache kivi_cache; /* opaque host handle */
 
 /* Bytes each buffer needs, in kivi_buffers order.  Host only; no GPU.
- * Returns KIVI_EINVAL / KIVI_ESHAPE for a config this build rejects. */
+ * Returns KIVI_EINVAL / KIVI_ESHAPE for a config this library rejects. */
 kivi_status kivi_cache_sizes(const kivi_config *cfg, size_t bytes[3]);
 
 /* Validate cfg, bind the buffers and create an empty handle (length 0).

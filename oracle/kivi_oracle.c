@@ -201,7 +201,7 @@ void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes)
 
 /* 3-bit rows.  A 3-bit code does not sit in whole bytes or nibbles, and the
  * pages print no 3-bit packing (the notebook's bit-width sweep quantizes in
- * fp32 only), so the storage is this build's choice: two planes per row.
+ * fp32 only), so the storage is this implementation's choice: two planes per row.
  *  - Bytes [0, D/4): the low two bits of every code, laid out exactly as a
  *    2-bit row (keys LSB-first, values group-interleaved).
  *  - Bytes [D/4, 3D/8): the high bit of every code, in 16-bit units (D =
