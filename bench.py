@@ -237,26 +237,39 @@ def run_gpu(args):
     torch.cuda.synchronize()
 
     # ---------------- timed (value): one replay of a CUDA graph holding K
-    # decode attention launches, launch i on replica i mod n_rep
+    # decode attention launches, launch i on replica i mod n_rep.  The
+    # launches may overlap (kivi_set_attention_overlap: no launch writes
+    # another's q or cache, so each starts as the one before it drains and
+    # waits for it only before its first write); the same graph without the
+    # overlap is timed beside it.
     per_rep = -(-K // n_rep)
     for c in caches:
         rewind_if_needed(c, 2 * per_rep + 1)
-    gA = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gA):
-        for i in range(K):
-            caches[i % n_rep].attention(q, out)
+
+    def time_attention_graph(overlap):
+        for c in caches:
+            c.set_overlap(overlap)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(K):
+                caches[i % n_rep].attention(q, out)
+        g.replay()  # warm-up replay (attention leaves the caches unchanged)
+        fence()
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        fence()
+        for c in caches:
+            c.set_overlap(False)
+        del g
+        return e0.elapsed_time(e1) * 1e-3 / K
+
     ctx_a = [caches[i % n_rep].length for i in range(K)]
-    gA.replay()  # warm-up replay (attention leaves the caches unchanged)
-    fence()
-    e0, e1 = ev(), ev()
-    e0.record(stream)
-    gA.replay()
-    e1.record(stream)
-    fence()
-    t_att_graph = e0.elapsed_time(e1) * 1e-3 / K
+    t_att_serial = time_attention_graph(False)
+    t_att_graph = time_attention_graph(True)
     att_b = np.array([attn_bytes(B, Hkv, Hq, D, t, R, 2) for t in ctx_a], float)
     attn_gbs = att_b.sum() / (t_att_graph * K) / 1e9
-    del gA
 
     # ---------------- timed (steps): the one-call decode step (append, then
     # the attention as a programmatic dependent of the append), K steps per
@@ -349,6 +362,7 @@ def run_gpu(args):
         "tokens_per_s": round(tokens_per_s, 1),
         "step_us": round(step_graph_s * 1e6, 3),
         "attention_us": round(t_att_graph * 1e6, 3),
+        "attention_us_no_overlap": round(t_att_serial * 1e6, 3),
         "per_launch_events": {
             "attention_us": round(float(t_att.mean()) * 1e6, 3),
             "append_us": round(float(t_app.mean()) * 1e6, 3),
@@ -375,11 +389,14 @@ def run_gpu(args):
     return result
 
 
-def graph_per_launch(torch, stream, ev, calls):
+def graph_per_launch(torch, stream, ev, calls, overlap=()):
     """Per-launch time of `calls` (functions that each enqueue one library
     call on the current stream, replayable: they leave the same state each
     time): captured in one CUDA graph, replayed once as warm-up, then one
-    replay timed with CUDA events on `stream`."""
+    replay timed with CUDA events on `stream`.  The caches in `overlap` let
+    their attention launches overlap the launch before them while captured."""
+    for c in overlap:
+        c.set_overlap(True)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         for f in calls:
@@ -393,6 +410,8 @@ def graph_per_launch(torch, stream, ev, calls):
     torch.cuda.synchronize()
     t = e0.elapsed_time(e1) * 1e-3 / len(calls)
     del g
+    for c in overlap:
+        c.set_overlap(False)
     return t
 
 
@@ -476,7 +495,8 @@ def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits, outli
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) * 1e-3 for a, b in recs]
     tg = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)])
+                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          overlap=caches)
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T + 1, wl.R, bits)
     if outliers:  # the outlier blocks of the quantized key groups
         nbytes += wl.B * wl.Hkv * (nq(wl.T + 1, wl.R)[0] // G) * (16 + 64 * outliers)
@@ -521,7 +541,8 @@ def long_context(args, torch, W, KiviCache, dev, stream, ev, peak):
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) * 1e-3 for a, b in recs]
     tg = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)])
+                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          overlap=caches)
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T, wl.R, 2)
     gbs = nbytes / tg / 1e9
     res["long_context_attention"] = {
@@ -573,7 +594,8 @@ def streaming(args, torch, W, KiviCache, dev, stream, ev, peak):
     n_steps = sum(len(ctx) for ctx, _ in chunks)
     # the attention alone at the final context (2560 tokens), replicas rotated
     ta = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(4 * n_rep)])
+                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(4 * n_rep)],
+                          overlap=caches)
     ab = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, caches[0].length, wl.R, 2)
     res["streaming_decode"] = {
         "what": "batch 64, 28/4 heads (GQA 7), 2048 prefill then 512 decode steps (append + "

@@ -12,7 +12,9 @@
 // 32-token tiles [0, t_tail).  Partials are merged in the same launch: the
 // CTA that finishes last in a group of up to kMergeGroup splits merges the
 // group, and with more than one group the last group merges the groups;
-// nothing ever waits on another CTA.
+// nothing ever waits on another CTA.  A CTA serves a chunk of up to eight
+// query heads of one KV head, so every tile is decoded once for up to eight
+// heads.
 //
 // Packed tiles (2, 3, 4 or 8 bits) run on the tensor cores (mma.sync
 // m16n8k16, fp16 operands, fp32 accumulation).  Each warp streams its tiles
@@ -21,14 +23,18 @@
 //   scores  S[t, j] = sum_d c_td (q_jd s_d) + beta_j, beta_j = sum_d q_jd z_d
 //   output  O[d, j] = sum_t c_td (p_jt s_t,g(d)) + sum_t p_jt z_t,g(d)
 // The codes c enter the MMA as fp16 subnormals c * base^i * 2^-24 (the masked
-// code bits are the whole encoding; base 4 at 2 and 3 bits, 16 at 4, 1 at 8);
-// the fp32 factors q*s and p*s enter as an
-// fp16 hi/lo pair (hi = fp16(x), lo = fp16(x - hi)) in the 8 columns of the
-// n=8 operand as (head, hi) and (head, lo): four query heads per MMA, and the
-// sum hi + lo recovers x to about 2^-22.  Each query head is first scaled by a
-// power of two so that max |q| < 1, and a head's running max trails its
-// scores by at most 0.5 (log2 units), so neither q*s nor p*s can overflow
-// fp16.
+// code bits are the whole encoding; base 4 at 2 and 3 bits, 16 at 4, 1 at 8).
+// On the key side the fp32 factor q*s enters as an fp16 hi/lo pair (hi =
+// fp16(x), lo = fp16(x - hi), together x to about 2^-22) in the 8 columns of
+// the n=8 operand as (head, hi) and (head, lo), four heads per MMA: a single
+// fp16 there would cost up to 2.1e-3 of relative output error on the
+// streaming workload.  On the value side the weight p and p*s enter as one
+// fp16 each, eight heads per MMA (at most 1.0e-3 on the same workloads; a
+// CPU model of the rounding measured both); the weights' sums come out of the
+// same product (ones in the z-term rows), so numerator and denominator use
+// the same rounded p.  Each query head is first scaled by a power of two so
+// that max |q| < 1, and a head's running max trails its scores by at most
+// 0.5 (log2 units), so neither q*s nor p*s can overflow fp16.
 #include <cuda_bf16.h>
 
 #include <cstddef>
@@ -41,6 +47,7 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 4;
 constexpr int kNH = kHeadChunk;  // query heads per CTA (one "head chunk")
+constexpr uint32_t kOnesH2 = 0x3C003C00u;  // the fp16 pair {1, 1}
 // A bounded wait for staged data gives up after this long (the copies take
 // microseconds); the CTA then records the failure in the status word.
 constexpr unsigned long long kWaitLimitNs = 200ull * 1000ull * 1000ull;
@@ -119,23 +126,17 @@ __device__ __forceinline__ uint32_t split_mul(uint32_t xa, uint32_t xb, uint32_t
 // +3 sits at unit position 4*w + gp (units are bits/2 bytes).
 __device__ __forceinline__ int v_unit_pos(int unit) { return 4 * (unit & 7) + (unit >> 3); }
 
-// v[i] for a lane-dependent i without dynamic register indexing.
-__device__ __forceinline__ float pick4(const float (&v)[4], int i) {
-  float r = v[0];
-  r = i == 1 ? v[1] : r;
-  r = i == 2 ? v[2] : r;
-  r = i == 3 ? v[3] : r;
-  return r;
-}
+
 
 // ---------------------------------------------------------------------------
 // Shared memory.
 
-// q tables in MMA fragment order.  Lane (g, tig) reads the 16 words of
-// column g (head g >> 1, part g & 1) for its tig, as four 16-byte quarters;
-// the layout [quarter][column][tig] spreads the 8 lanes of a shared-memory
-// phase over distinct banks.  Word w (k-step ks = w >> 1) of (column, tig)
-// holds the channel pair of code position i:
+// q tables in MMA fragment order, one set per key block nb (query heads
+// 4 nb .. 4 nb + 3).  Lane (g, tig) reads the 16 words of column g (head
+// 4 nb + (g >> 1), part g & 1) for its tig, as four 16-byte quarters; the
+// layout [quarter][column][tig] spreads the 8 lanes of a shared-memory phase
+// over distinct banks.  Word w (k-step ks = w >> 1) of (column, tig) holds
+// the channel pair of code position i:
 //   2 bits: word m = tig + 4*(ks >> 2) of a key row, i = 2*(ks & 3) + (w & 1),
 //           channels (16m + i, 16m + i + 8);
 //   4 bits: word m = tig + 4*(ks >> 1), i = 2*(ks & 1) + (w & 1),
@@ -155,50 +156,57 @@ struct TileBuf {
 template <int BITS>
 constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp (3 KB / 4-9 KB tiles)
 
-template <int BITS>
+template <int BITS, int NB>
 struct WarpSmem {
   TileBuf<BITS> st[kWarps][kStagesOf<BITS>];  // per-warp rings of staged tiles
-  uint4 qs[2][4][8][4];                   // q * base^-e(i) as split_mul operands (xa, xb)
-  uint4 qb[4][8][4];                      // q hi / lo
-  float pbuf[kWarps][kNH][34];            // one tile's weights per warp, token order
-                                          // 8 (t & 3) + 4 (t >> 4) + 2 ((t >> 3) & 1) + ((t >> 2) & 1)
+  uint4 qs[NB][2][4][8][4];               // q * base^-e(i) as split_mul operands (xa, xb)
+  uint4 qb[NB][4][8][4];                  // q hi / lo (words of a quarter in the order 0, 2, 1, 3)
   float qv[kNH][kHeadDim];                // q, staged for the tables
   float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
   int qexp[kNH];                          // E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
   unsigned long long bar[kWarps][kStagesOf<BITS>];
 };
 
-// A tail split: up to kTailTok tokens, each staged as a 256-byte key row and
-// a 256-byte value row -- an fp16 residual row (16-byte chunks XOR-swizzled by
-// row), or the packed codes at the row start; the scale / zero blocks of the
-// packed tiles involved are staged whole (kg, vg), in the tiles' order.
-static_assert(kNH == 4, "the tail split keeps the heads of a channel / token in one float4");
+// A tail split: up to kTailTok tokens.  Its packed rows arrive as the whole
+// code blocks of the (at most two) tiles involved (kpk, vpk, in the tiles'
+// own layout), its fp16 residual rows as one or two runs of ring slots
+// (kring, vring: token r of the split at row r), and the scale / zero blocks
+// of those tiles whole (kg, vg), all by bulk copies on one mbarrier.
+static_assert(kNH == 8, "the tail split keeps the heads of a channel / token in two float4");
+template <int BITS>
 struct TailSmem {
-  float4 q4[kHeadDim];                    // q * scale * log2(e): the kNH heads of channel d
-  uint4 krow[kTailTok][16];
-  uint4 vrow[kTailTok][16];
+  float4 q8[kHeadDim][2];                 // q * scale * log2(e): the kNH heads of channel d
+  __half kring[kTailTok][kHeadDim];       // fp16 key rows of the residual tokens
+  __half vring[kTailTok][kHeadDim];       // fp16 value rows of the residual tokens
+  uint8_t kpk[2][kGroup * kRowBytes<BITS>];  // key code blocks of the (at most two) tiles
+  uint8_t vpk[2][kGroup * kRowBytes<BITS>];  // value code blocks
   uint32_t kg[2][2][64];                  // scale / zero of the (at most two) key groups
   uint32_t ko[2][outlier_block_bytes(kMaxOutliers) / 4];  // their outlier blocks
   uint32_t vg[2][2][64];                  // value scale / zero blocks of the (at most two) tiles
-  float4 p4[kTailTok];                    // per token: scores, then weights, of the kNH heads
+  float4 p8[kTailTok][2];                 // per token: scores, then weights, of the kNH heads
   float mh[kNH], lh[kNH];                 // per head: max and sum of the weights
+  unsigned long long bar;                 // completion of the round's copies
 };
 
-template <int BITS>
+template <int BITS, int NB>
 union SplitSmem {
-  WarpSmem<BITS> ws;
-  TailSmem tail;
+  WarpSmem<BITS, NB> ws;
+  TailSmem<BITS> tail;
 };
 
 enum Path { kPathMma = 1, kPathTail = 2 };
 
 // Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the CTA
 // is done with (its staged tiles or tail rows).
-template <int BITS>
-__device__ __forceinline__ float* merge_area(SplitSmem<BITS>& sm, int warp, int path) {
+static_assert(kWarps * kNH * kHeadDim * 4 <= 2 * kTailTok * kHeadDim, "tail merge areas");
+template <int BITS, int NB>
+__device__ __forceinline__ float* merge_area(SplitSmem<BITS, NB>& sm, int warp, int path) {
   if (path == kPathMma) return reinterpret_cast<float*>(&sm.ws.st[warp][0]);
-  return reinterpret_cast<float*>(&sm.tail.krow[0][0]) + warp * kNH * kHeadDim;
+  return reinterpret_cast<float*>(&sm.tail.kring[0][0]) + warp * kNH * kHeadDim;
 }
+static_assert(kNH * kHeadDim * 4 <= (int)sizeof(TileBuf<2>) * kStagesOf<2> &&
+                  kNH * kHeadDim * 4 <= (int)sizeof(TileBuf<3>) * kStagesOf<3>,
+              "a warp's staged tiles hold its merge area");
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -221,6 +229,18 @@ __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t coun
 
 __device__ __forceinline__ void mbar_fence_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// An mbarrier whose phases are all complete, invalidated before its shared
+// memory is used for anything else.
+__device__ __forceinline__ void mbar_inval(unsigned long long* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Orders this thread's earlier ordinary shared-memory accesses before later
+// bulk copies into the same memory.
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(unsigned long long* bar, uint32_t bytes) {
@@ -282,183 +302,220 @@ __global__ void wait_probe_kernel(int* status) {
 // ---------------------------------------------------------------------------
 // A tail split on CUDA cores: tokens [c0, c0 + n), n <= kTailTok, of the tail
 // [t_tail, l), staged in one round of copies (fp16 residual rows, packed rows
-// and the key groups' scales / zeros); then scores with four threads per
-// token (32 channels each), the softmax of a head per warp, and the value sum
-// with one thread per channel.  Keys and values of packed rows are
-// dequantized as c * s + z with a single rounding, which equals the
-// notebook's fl(fl(c * s) + z) because c * s is exact in fp32.  Leaves the
-// partial of the CTA in warp 0's slots (the other warps' slots empty).
+// and the key groups' scales / zeros), for the chunk's 4 NQ query heads.
+// Scores: warp w takes tokens w, w + 4, ..., lane l channels 4l .. 4l + 3,
+// and one transposing butterfly over the lanes sums the 4 NQ heads at once;
+// the softmax of a head is one warp; values take one thread per channel.
+// Keys and values of packed rows are dequantized as c * s + z with a single
+// rounding, which equals the notebook's fl(fl(c * s) + z) because c * s is
+// exact in fp32.  Leaves the partial of the CTA in warp 0's slots (the other
+// warps' slots empty) and its output rows in `mo0` ([kNH][kHeadDim], inside
+// the staged key rows).
+
+// The codes of channels 4 lane .. 4 lane + 3 of packed key row `row` of a
+// tile (the row's bytes as stored in the tile; channel e at bits
+// (e * BITS) mod 8 of logical byte e * BITS / 8; at 3 bits the low two bits
+// from the 2-bit plane, the high bit from its unit).
 template <int BITS>
-__device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS>& sm,
-                           long unit, int b,
-                           int j0, int nh, int c0, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
+__device__ __forceinline__ void key_codes4(const uint8_t* rowp, int row, int lane, uint32_t (&c)[4]) {
+  if constexpr (BITS == 2) {
+    const uint32_t w = rowp[lane];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (w >> (2 * i)) & 3u;
+  } else if constexpr (BITS == 4) {
+    const uint32_t w = reinterpret_cast<const uint16_t*>(rowp)[lane];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (w >> (4 * i)) & 15u;
+  } else if constexpr (BITS == 8) {
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(rowp + krow_byte<8>(row, 4 * lane));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = (w >> (8 * i)) & 255u;
+  } else {
+    const uint32_t w = rowp[lane];
+    const uint32_t* rw = reinterpret_cast<const uint32_t*>(rowp);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = 4 * lane + i;  // the channel
+      const uint32_t hi =
+          (rw[kHiPlane3 / 4 + ((e >> 4) & 3)] >> (16 * ((e >> 3) & 1) + hi_bit3(e >> 6, e & 7))) & 1u;
+      c[i] = ((w >> (2 * i)) & 3u) | (hi << 2);
+    }
+  }
+}
+
+// Sum of v[0..H) over the 32 lanes, H heads at once: each butterfly level
+// halves the values a lane carries (the lanes with bit `o` set keep the upper
+// half), then plain levels finish the sums.  Every lane of a block of 32 / H
+// lanes ends with the total of head `head`.
+template <int H>
+__device__ __forceinline__ float reduce_heads(const float (&v)[H], int lane, int& head) {
+  float cur[H];
+#pragma unroll
+  for (int i = 0; i < H; ++i) cur[i] = v[i];
+  head = 0;
+  int o = 16;
+#pragma unroll
+  for (int half = H / 2; half >= 1; half >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float keep = up ? cur[i + half] : cur[i];
+      const float send = up ? cur[i] : cur[i + half];
+      cur[i] = keep + __shfl_xor_sync(kFull, send, o);
+    }
+    head += up ? half : 0;
+    o >>= 1;
+  }
+#pragma unroll
+  for (; o > 0; o >>= 1) cur[0] += __shfl_xor_sync(kFull, cur[0], o);
+  return cur[0];
+}
+
+template <int BITS, int NQ>
+__device__ __noinline__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan p, TailSmem<BITS>& ts,
+                                        float* mo0, long unit, int b, int j0, int nh, int c0, uint32_t round,
+                                        float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;  // packed row bytes
-  constexpr int CPR = RB / 16;             // 16-byte chunks per packed row
-  TailSmem& ts = sm.tail;
+  constexpr int H = 4 * NQ;                // heads of this tail
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = min(kTailTok, p.l - c0);
   const int nk = max(0, min(n, p.nq_k - c0));  // rows [0, nk) hold packed keys
   const int nv = max(0, min(n, p.nq_v - c0));  // rows [0, nv) hold packed values
-
-  // ---- stage the round (c0 is a multiple of 32, so its packed keys span at
-  //      most two key groups), and q ----
-  for (int i = tid; i < n * 16; i += blockDim.x) {
-    const int r = i >> 4, c = i & 15;
-    const long t = c0 + r;
-    const uint8_t* tile = tile_at<BITS>(cv, unit, t / kGroup);
-    const int tr = (int)(t % kGroup);  // row within the tile
-    if (r < nk) {
-      if (c < CPR) cp_async16(&ts.krow[r][c], tile + tr * RB + 16 * krow_chunk<BITS>(tr, c));
-    } else {
-      cp_async16(&ts.krow[r][c ^ (r & 7)], cv.ring_k + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
-    }
-    if (r < nv) {
-      if (c < CPR) {
-        cp_async16(&ts.vrow[r][c], tile + kOffVc<BITS> + tr * RB + 16 * vrow_chunk<BITS>(tr, c));
-      }
-    } else {
-      cp_async16(&ts.vrow[r][c ^ (r & 7)], cv.ring_v + (unit * cv.W + t % cv.W) * kHeadDim + 8 * c);
-    }
-  }
-  // key scale / zero blocks of the packed key tiles, value scale / zero
-  // blocks of the packed value tiles (at most two tiles each)
   const int ngk = (nk + kGroup - 1) / kGroup, ngv = (nv + kGroup - 1) / kGroup;
-  const int ocb = outlier_block_bytes(cv.n_out) / 16;  // 16-byte chunks of an outlier block
-  for (int i = tid; i < ngk * ocb; i += blockDim.x) {
-    const int gi = i / ocb, c = i % ocb;
-    cp_async16(&ts.ko[gi][4 * c], tile_at<BITS>(cv, unit, c0 / kGroup + gi) + kTileBytes<BITS> + 16 * c);
+  const int tile0 = c0 / kGroup;  // c0 is a multiple of 32: packed rows span at most two tiles
+
+  // ---- stage the round with bulk copies (thread 0), and q ----
+  if (tid == 0) {
+    if (round == 0) {
+      mbar_init(&ts.bar, 1);
+      mbar_fence_init();
+    }
+    fence_proxy_async();  // the buffers were last used by ordinary loads and stores
+    const int ob = outlier_block_bytes(cv.n_out);
+    const int wk = n - nk, wv = n - nv;  // residual rows of keys / values
+    const int sk0 = (int)((c0 + nk) % cv.W), sv0 = (int)((c0 + nv) % cv.W);
+    const int k1 = min(wk, cv.W - sk0), v1 = min(wv, cv.W - sv0);  // first runs of ring slots
+    const uint32_t bytes = (uint32_t)(ngk * (kGroup * RB + 4 * kHeadDim + ob) + ngv * (kGroup * RB + 4 * kHeadDim) +
+                                      (wk + wv) * 2 * kHeadDim);
+    mbar_expect_tx(&ts.bar, bytes);
+    for (int gi = 0; gi < ngk; ++gi) {
+      const uint8_t* tile = tile_at<BITS>(cv, unit, tile0 + gi);
+      bulk_g2s(ts.kpk[gi], tile, kGroup * RB, &ts.bar);
+      bulk_g2s(ts.kg[gi], tile + kOffSk<BITS>, 4 * kHeadDim, &ts.bar);  // scales, then zeros
+      if (ob) bulk_g2s(ts.ko[gi], tile + kTileBytes<BITS>, ob, &ts.bar);
+    }
+    for (int gi = 0; gi < ngv; ++gi) {
+      const uint8_t* tile = tile_at<BITS>(cv, unit, tile0 + gi);
+      bulk_g2s(ts.vpk[gi], tile + kOffVc<BITS>, kGroup * RB, &ts.bar);
+      bulk_g2s(ts.vg[gi], tile + kOffSv<BITS>, 4 * kHeadDim, &ts.bar);
+    }
+    const __half* rk = cv.ring_k + unit * cv.W * kHeadDim;
+    const __half* rv = cv.ring_v + unit * cv.W * kHeadDim;
+    if (k1 > 0) bulk_g2s(ts.kring[nk], rk + (long)sk0 * kHeadDim, k1 * 2 * kHeadDim, &ts.bar);
+    if (wk > k1) bulk_g2s(ts.kring[nk + k1], rk, (wk - k1) * 2 * kHeadDim, &ts.bar);
+    if (v1 > 0) bulk_g2s(ts.vring[nv], rv + (long)sv0 * kHeadDim, v1 * 2 * kHeadDim, &ts.bar);
+    if (wv > v1) bulk_g2s(ts.vring[nv + v1], rv, (wv - v1) * 2 * kHeadDim, &ts.bar);
   }
-  for (int i = tid; i < (ngk + ngv) * 32; i += blockDim.x) {
-    const bool key = i < ngk * 32;
-    const int ii = key ? i : i - ngk * 32;
-    const int gi = ii >> 5, arr = (ii >> 4) & 1, c = ii & 15;
-    const uint8_t* tile = tile_at<BITS>(cv, unit, c0 / kGroup + gi);
-    if (key) cp_async16(&ts.kg[gi][arr][4 * c], tile + (arr ? kOffZk<BITS> : kOffSk<BITS>) + 16 * c);
-    else cp_async16(&ts.vg[gi][arr][4 * c], tile + (arr ? kOffZv<BITS> : kOffSv<BITS>) + 16 * c);
-  }
-  cp_async_commit();
   {
     float qj[kNH];
 #pragma unroll
     for (int j = 0; j < kNH; ++j)
       qj[j] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + tid, a.q_dtype) * a.scale_log2 : 0.0f;
-    ts.q4[tid] = make_float4(qj[0], qj[1], qj[2], qj[3]);
+    ts.q8[tid][0] = make_float4(qj[0], qj[1], qj[2], qj[3]);
+    ts.q8[tid][1] = make_float4(qj[4], qj[5], qj[6], qj[7]);
   }
-  cp_async_wait<0>();
-  __syncthreads();
+  __syncthreads();  // q staged; the barrier initialized before anyone waits on it
+  if (!mbar_wait(&ts.bar, round & 1u) && tid == 0) atomicOr(a.status, 1);
 
-  // ---- scores: thread (token r, quarter qq) sums channels 32qq .. +31 ----
-#pragma unroll 1
-  for (int it = 0; it < kTailTok / 32; ++it) {
-    const int r = (tid >> 2) + 32 * it, qq = tid & 3;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nk) {
-      const int gi = r >> 5;
-      const uint32_t* cw4 = reinterpret_cast<const uint32_t*>(&ts.krow[r][0]) + qq * BITS;
-      // channels 32qq .. 32qq + 31 (kscale_pos keeps them in this block)
-      const __half* sk = reinterpret_cast<const __half*>(ts.kg[gi][0]) + 32 * qq;
-      const __half* zk = reinterpret_cast<const __half*>(ts.kg[gi][1]) + 32 * qq;
-      if constexpr (BITS == 3) {
-        // low two bits from the 2-bit plane, the high bit from its unit
-        const uint32_t* kr = reinterpret_cast<const uint32_t*>(&ts.krow[r][0]);
-#pragma unroll 4
-        for (int dq = 0; dq < 32; dq += 2) {
-          const float2 sp = make_float2(__half2float(sk[kscale_pos<BITS>(dq)]),
-                                        __half2float(sk[kscale_pos<BITS>(dq + 1)]));
-          const float2 zp = make_float2(__half2float(zk[kscale_pos<BITS>(dq)]),
-                                        __half2float(zk[kscale_pos<BITS>(dq + 1)]));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int e = 32 * qq + dq + u;  // the channel
-            const uint32_t lo = (kr[e >> 4] >> (2 * (e & 15))) & 3u;
-            const uint32_t hi =
-                (kr[kHiPlane3 / 4 + ((e >> 4) & 3)] >> (16 * ((e >> 3) & 1) + hi_bit3(e >> 6, e & 7))) & 1u;
-            const float kx = fmaf((float)(lo | (hi << 2)), u ? sp.y : sp.x, u ? zp.y : zp.x);
-            const float4 qv = ts.q4[e];
-            acc.x = fmaf(kx, qv.x, acc.x);
-            acc.y = fmaf(kx, qv.y, acc.y);
-            acc.z = fmaf(kx, qv.z, acc.z);
-            acc.w = fmaf(kx, qv.w, acc.w);
-          }
-        }
-      } else {
-#pragma unroll
-      for (int w = 0; w < BITS; ++w) {  // 32-bit words of this quarter's codes
-        const uint32_t cw = cw4[w];
-#pragma unroll
-        for (int e = 0; e < 32 / BITS; e += 2) {
-          const int dq = w * (32 / BITS) + e;  // even channel of the quarter
-          const float2 sp = make_float2(__half2float(sk[kscale_pos<BITS>(dq)]),
-                                        __half2float(sk[kscale_pos<BITS>(dq + 1)]));
-          const float2 zp = make_float2(__half2float(zk[kscale_pos<BITS>(dq)]),
-                                        __half2float(zk[kscale_pos<BITS>(dq + 1)]));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            // the code as an exact float: its bits under the exponent of 2^23
-            const float cf = __uint_as_float(((cw >> (BITS * (e + u))) & L) | 0x4B000000u) - 8388608.0f;
-            const float kx = fmaf(cf, u ? sp.y : sp.x, u ? zp.y : zp.x);
-            const float4 qv = ts.q4[32 * qq + dq + u];
-            acc.x = fmaf(kx, qv.x, acc.x);
-            acc.y = fmaf(kx, qv.y, acc.y);
-            acc.z = fmaf(kx, qv.z, acc.z);
-            acc.w = fmaf(kx, qv.w, acc.w);
-          }
-        }
-      }
-      }
-    } else if (r < n) {
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const int c = 4 * qq + c4;
-        const uint4 kv = ts.krow[r][c ^ (r & 7)];
-        const float kf[8] = {h_lo(kv.x), h_hi(kv.x), h_lo(kv.y), h_hi(kv.y),
-                             h_lo(kv.z), h_hi(kv.z), h_lo(kv.w), h_hi(kv.w)};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float4 qv = ts.q4[8 * c + e];
-          acc.x = fmaf(kf[e], qv.x, acc.x);
-          acc.y = fmaf(kf[e], qv.y, acc.y);
-          acc.z = fmaf(kf[e], qv.z, acc.z);
-          acc.w = fmaf(kf[e], qv.w, acc.w);
-        }
-      }
-    }
-#pragma unroll
-    for (int sh = 1; sh <= 2; sh <<= 1) {
-      acc.x += __shfl_xor_sync(kFull, acc.x, sh);
-      acc.y += __shfl_xor_sync(kFull, acc.y, sh);
-      acc.z += __shfl_xor_sync(kFull, acc.z, sh);
-      acc.w += __shfl_xor_sync(kFull, acc.w, sh);
-    }
-    if (qq == 0 && r < nk && cv.n_out > 0) {
-      // the group's fp16 outlier channels (their packed codes decode to 0)
-      const uint32_t iw = ts.ko[r >> 5][0];
-      const __half* ov = reinterpret_cast<const __half*>(&ts.ko[r >> 5][4]);
-      for (int o = 0; o < cv.n_out; ++o) {
-        const float x = __half2float(ov[(r & 31) * cv.n_out + o]);
-        const float4 qv = ts.q4[(iw >> (8 * o)) & 0xffu];
-        acc.x = fmaf(x, qv.x, acc.x);
-        acc.y = fmaf(x, qv.y, acc.y);
-        acc.z = fmaf(x, qv.z, acc.z);
-        acc.w = fmaf(x, qv.w, acc.w);
-      }
-    }
-    if (qq == 0 && r < n) ts.p4[r] = acc;
-  }
-  __syncthreads();
-
-  // ---- softmax of head `warp` over the round ----
+  // ---- scores: warp w takes tokens w, w + 4, ... (two at a time); lane l
+  //      channels 4l..4l+3 ----
   {
-    const int j = warp;  // kWarps == kNH
-    float* pj = reinterpret_cast<float*>(ts.p4) + j;
-    const float x0 = lane < n ? pj[4 * lane] : -INFINITY;
-    const float x1 = lane + 32 < n ? pj[4 * (lane + 32)] : -INFINITY;
+    float qr[4][H];  // q of this lane's channels, the tail's heads
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int nq = 0; nq < NQ; ++nq) {
+        const float4 v = ts.q8[4 * lane + c][nq];
+        qr[c][4 * nq] = v.x;
+        qr[c][4 * nq + 1] = v.y;
+        qr[c][4 * nq + 2] = v.z;
+        qr[c][4 * nq + 3] = v.w;
+      }
+    // scales / zeros of this lane's channels in the (at most two) key groups
+    float ks_[2][4], kz_[2][4];
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int pos = kscale_pos<BITS>(4 * lane + c);
+        ks_[gi][c] = gi < ngk ? __half2float(reinterpret_cast<const __half*>(ts.kg[gi][0])[pos]) : 0.0f;
+        kz_[gi][c] = gi < ngk ? __half2float(reinterpret_cast<const __half*>(ts.kg[gi][1])[pos]) : 0.0f;
+      }
+    auto score = [&](int r, float (&acc)[H]) {
+      float kx[4];
+      if (r < nk) {
+        uint32_t cd[4];
+        key_codes4<BITS>(ts.kpk[r >> 5] + (r & 31) * RB, r & 31, lane, cd);
+        const int gi = r >> 5;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          kx[c] = fmaf(__uint_as_float(cd[c] | 0x4B000000u) - 8388608.0f, gi ? ks_[1][c] : ks_[0][c],
+                       gi ? kz_[1][c] : kz_[0][c]);
+      } else {
+        const uint2 h4 = *reinterpret_cast<const uint2*>(&ts.kring[r][4 * lane]);
+        kx[0] = h_lo(h4.x);
+        kx[1] = h_hi(h4.x);
+        kx[2] = h_lo(h4.y);
+        kx[3] = h_hi(h4.y);
+      }
+#pragma unroll
+      for (int j = 0; j < H; ++j) {
+        acc[j] = kx[0] * qr[0][j];
+#pragma unroll
+        for (int c = 1; c < 4; ++c) acc[j] = fmaf(kx[c], qr[c][j], acc[j]);
+      }
+      if (lane == 0 && r < nk && cv.n_out > 0) {
+        // the group's fp16 outlier channels (their packed codes decode to 0)
+        const uint32_t iw = ts.ko[r >> 5][0];
+        const __half* ov = reinterpret_cast<const __half*>(&ts.ko[r >> 5][4]);
+        for (int o = 0; o < cv.n_out; ++o) {
+          const float x = __half2float(ov[(r & 31) * cv.n_out + o]);
+          const float* qo = reinterpret_cast<const float*>(&ts.q8[(iw >> (8 * o)) & 0xffu][0]);
+#pragma unroll
+          for (int j = 0; j < H; ++j) acc[j] = fmaf(x, qo[j], acc[j]);
+        }
+      }
+    };
+#pragma unroll 1
+    for (int r = warp; r < n; r += 2 * kWarps) {
+      const int r1 = r + kWarps < n ? r + kWarps : r;  // a second token (or the first again)
+      float acc0[H], acc1[H];
+      score(r, acc0);
+      score(r1, acc1);
+      int head;
+      const float s0 = reduce_heads<H>(acc0, lane, head);
+      const float s1 = reduce_heads<H>(acc1, lane, head);
+      if ((lane & (32 / H - 1)) == 0) {
+        reinterpret_cast<float*>(ts.p8)[r * kNH + head] = s0;
+        reinterpret_cast<float*>(ts.p8)[r1 * kNH + head] = s1;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- softmax of heads `warp` (and `warp` + 4) over the round ----
+#pragma unroll
+  for (int hh = 0; hh < NQ; ++hh) {
+    const int j = warp + kWarps * hh;
+    float* pj = reinterpret_cast<float*>(ts.p8) + j;  // [token][kNH]
+    const float x0 = lane < n ? pj[kNH * lane] : -INFINITY;
+    const float x1 = lane + 32 < n ? pj[kNH * (lane + 32)] : -INFINITY;
     const float mx = warp_max(fmaxf(x0, x1));
     const float e0 = lane < n ? fast_exp2(x0 - mx) : 0.0f;
     const float e1 = lane + 32 < n ? fast_exp2(x1 - mx) : 0.0f;
-    pj[4 * lane] = e0;
-    pj[4 * (lane + 32)] = e1;
+    pj[kNH * lane] = e0;
+    pj[kNH * (lane + 32)] = e1;
     const float sum = warp_sum(e0 + e1);
     if (lane == 0) {
       ts.mh[j] = mx;
@@ -467,21 +524,23 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
   }
   __syncthreads();
 
-  // ---- values: thread d accumulates channel d of the kNH heads ----
+  // ---- values: thread d accumulates channel d of the tail's heads ----
   const int d = tid;
   const int vpos = v_unit_pos(d >> 2);
   const int vsh = BITS * (d & 3);
-  float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
+  float o[H];
+#pragma unroll
+  for (int j = 0; j < H; ++j) o[j] = 0.0f;
+#pragma unroll 2
   for (int r = 0; r < n; ++r) {
     float vx;
     if (r < nv) {
-      const uint8_t* row = reinterpret_cast<const uint8_t*>(&ts.vrow[r][0]);
+      const uint8_t* row = ts.vpk[r >> 5] + (r & 31) * RB;
       uint32_t cb;
       if constexpr (BITS == 2) cb = row[vpos];
       else if constexpr (BITS == 3) cb = row[vpos] | ((uint32_t)*reinterpret_cast<const uint16_t*>(row + kHiPlane3 + 2 * ((d & 31) >> 2)) << 8);
       else if constexpr (BITS == 4) cb = *reinterpret_cast<const uint16_t*>(row + 2 * vpos);
-      else cb = *reinterpret_cast<const uint32_t*>(row + 4 * vpos);
+      else cb = *reinterpret_cast<const uint32_t*>(row + vrow_byte<8>(r & 31, 4 * vpos));
       const int vs = vscale_pos(r & 31, d >> 5);
       const float sv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][0])[vs]);
       const float zv = __half2float(reinterpret_cast<const __half*>(ts.vg[r >> 5][1])[vs]);
@@ -496,30 +555,29 @@ __device__ void tail_split(const CacheView& cv, const AttnArgs& a, const SeqPlan
       }
       vx = fmaf(cf, sv, zv);
     } else {
-      const __half* row = reinterpret_cast<const __half*>(&ts.vrow[r][(d >> 3) ^ (r & 7)]);
-      vx = __half2float(row[d & 7]);
+      vx = __half2float(ts.vring[r][d]);
     }
-    const float4 pr = ts.p4[r];
-    o.x = fmaf(pr.x, vx, o.x);
-    o.y = fmaf(pr.y, vx, o.y);
-    o.z = fmaf(pr.z, vx, o.z);
-    o.w = fmaf(pr.w, vx, o.w);
+#pragma unroll
+    for (int nq = 0; nq < NQ; ++nq) {
+      const float4 pr = ts.p8[r][nq];
+      o[4 * nq] = fmaf(pr.x, vx, o[4 * nq]);
+      o[4 * nq + 1] = fmaf(pr.y, vx, o[4 * nq + 1]);
+      o[4 * nq + 2] = fmaf(pr.z, vx, o[4 * nq + 2]);
+      o[4 * nq + 3] = fmaf(pr.w, vx, o[4 * nq + 3]);
+    }
   }
   __syncthreads();  // every thread is done with the staged rows (the merge area)
 
-  float* mo0 = merge_area(sm, 0, kPathTail);
-  mo0[0 * kHeadDim + d] = o.x;
-  mo0[1 * kHeadDim + d] = o.y;
-  mo0[2 * kHeadDim + d] = o.z;
-  mo0[3 * kHeadDim + d] = o.w;
+#pragma unroll
+  for (int j = 0; j < H; ++j) mo0[j * kHeadDim + d] = o[j];
   if (lane < kNH) {
-    s_m[warp][lane] = warp == 0 ? ts.mh[lane] : -INFINITY;
-    s_l[warp][lane] = warp == 0 ? ts.lh[lane] : 0.0f;
+    s_m[warp][lane] = warp == 0 && lane < H ? ts.mh[lane] : -INFINITY;
+    s_l[warp][lane] = warp == 0 && lane < H ? ts.lh[lane] : 0.0f;
   }
 }
 
 // ---------------------------------------------------------------------------
-// Tensor-core path (packed tiles, 2 or 4 bits).
+// Tensor-core path (packed tiles).
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
@@ -527,6 +585,21 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// D = A x B (no accumulator input: the C operand is the literal zero, which
+// the tensor instruction reads as the zero register), or D += A x B.
+template <bool kFirst>
+__device__ __forceinline__ void mma_acc(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+  if constexpr (kFirst) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f), "f"(0.0f), "f"(0.0f));
+  } else {
+    mma16816(d, a0, a1, a2, a3, b0, b1);
+  }
 }
 
 // Code position I (bit pair at 2 bits, nibble at 4 bits) of both 16-bit
@@ -634,12 +707,12 @@ __host__ __device__ constexpr int word_pos(int w) {
 }
 
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane
-// (head g >> 1, part g & 1), in the order of the q tables.  The q table is
-// pre-scaled by base^-e(i) to cancel the power that the code extraction
-// leaves in the A operand.
-template <int BITS>
-__device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uint32_t* sk, int g, int tig,
-                                             uint32_t (&bq)[8][2]) {
+// in every key block (head 4 nb + (g >> 1), part g & 1), in the order of the
+// q tables.  The q table is pre-scaled by base^-e(i) to cancel the power that
+// the code extraction leaves in the A operand.
+template <int BITS, int NB>
+__device__ __forceinline__ void build_qprime(const WarpSmem<BITS, NB>& ws, const uint32_t* sk, int g, int tig,
+                                             uint32_t (&bq)[NB][8][2]) {
 #pragma unroll
   for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
     uint32_t P[8];
@@ -647,62 +720,78 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS>& ws, const uin
 #pragma unroll
     for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
       const int quarter = kQuartersPerBlock<BITS> * blk + qq;
-      const uint4 x0 = ws.qs[0][quarter][g][tig];
-      const uint4 x1 = ws.qs[1][quarter][g][tig];
-      const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-      for (int wq = 0; wq < 4; ++wq) {
-        const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
-        bq[w >> 1][w & 1] =
-            split_mul(X0[wq], X1[wq], P[word_pos<BITS>(w)]);
+      for (int nb = 0; nb < NB; ++nb) {
+        const uint4 x0 = ws.qs[nb][0][quarter][g][tig];
+        const uint4 x1 = ws.qs[nb][1][quarter][g][tig];
+        const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+        for (int wq = 0; wq < 4; ++wq) {
+          const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
+          bq[nb][w >> 1][w & 1] = split_mul(X0[wq], X1[wq], P[word_pos<BITS>(w)]);
+        }
       }
     }
   }
 }
 
-// Position of token t (0..31) in a warp's weight buffer: the value product
-// reads tokens t0 = 16kk + 8aa + tig and t0 + 4 as one 8-byte pair.
-__device__ __forceinline__ int pbuf_pos(int t) {
-  return 8 * (t & 3) + 4 * (t >> 4) + 2 * ((t >> 3) & 1) + ((t >> 2) & 1);
-}
+// Row of the score product: m-tile row g of a 16-token m-tile takes token
+// tau(g) of it and row g + 8 token tau(g) + 4, so that the lane holding the
+// scores of rows (g, g + 8) holds exactly the token pair (t, t + 4) that one
+// B-fragment register of the value product takes.
+__device__ __forceinline__ int score_row(int g) { return (g & 3) + 8 * (g >> 2); }
 
-// Scores of one staged 32-token tile for the four heads of the CTA: lane
-// (g, tig) gets head tig at tokens g + 8r (sc[r], log2 units);
-// ks = 2^E_tig * scale * log2(e).
-template <int BITS>
-__device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileBuf<BITS>& tb, int g, int tig,
-                                           float ks, int n_out, float scale_log2, float (&sc)[4]) {
+// Scores of one staged 32-token tile, per key block nb: lane (g, tig) gets
+// head 4 nb + tig at tokens 16 (r >> 1) + score_row(g) + 4 (r & 1) in
+// sc[nb][r] (log2 units), less mb[nb]; ks = 2^E * scale * log2(e) of that
+// head.
+template <int BITS, int NB>
+__device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
+                                           const float (&ks)[NB], const float (&mb)[NB], int n_out,
+                                           float scale_log2, float (&sc)[NB][4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
-  // ---- beta = zK x q: every A row is the zero vector, so D[., (tig, part)] = beta ----
-  float beta4[4] = {0.f, 0.f, 0.f, 0.f};
+  // ---- beta = zK x q.  The A operand of a quarter is its four zero-point
+  //      words Z0..Z3 as loaded (rows g: Z0, Z2; rows g + 8: Z1, Z3); one
+  //      MMA takes the q words of Z0 / Z2 (its rows g are beta's share), a
+  //      second the q words of Z1 / Z3 (its rows g + 8), so
+  //      beta = D_a[g, (tig, hi)] + D_a[g, (tig, lo)] + D_b[g + 8, ..] ----
+  float kbm[NB];  // beta * ks - mb, the score offset of the tile
+  {
+    float ba[NB][4], bb[NB][4];
 #pragma unroll
-  for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
-    uint32_t P[8];
-    pair_words<BITS>(tb.zk, tig, blk, P);
+    for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
+      uint32_t P[8];
+      pair_words<BITS>(tb.zk, tig, blk, P);
 #pragma unroll
-    for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
-      const int quarter = kQuartersPerBlock<BITS> * blk + qq;
-      const uint4 qb = ws.qb[quarter][g][tig];
-      const uint32_t QB[4] = {qb.x, qb.y, qb.z, qb.w};
+      for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
+        const int quarter = kQuartersPerBlock<BITS> * blk + qq;
+        const uint32_t* Z = P + 4 * qq;
 #pragma unroll
-      for (int kh = 0; kh < 2; ++kh) {  // the quarter's two k-steps
-        const int w0 = 4 * quarter + 2 * kh;
-        const uint32_t z0 = P[word_pos<BITS>(w0)];
-        const uint32_t z1 = P[word_pos<BITS>(w0 + 1)];
-        mma16816(beta4, z0, z0, z1, z1, QB[2 * kh], QB[2 * kh + 1]);
+        for (int nb = 0; nb < NB; ++nb) {
+          const uint4 qb = ws.qb[nb][quarter][g][tig];  // q words of Z0, Z2, Z1, Z3
+          if (quarter == 0) {
+            mma_acc<true>(ba[nb], Z[0], Z[1], Z[2], Z[3], qb.x, qb.y);
+            mma_acc<true>(bb[nb], Z[0], Z[1], Z[2], Z[3], qb.z, qb.w);
+          } else {
+            mma_acc<false>(ba[nb], Z[0], Z[1], Z[2], Z[3], qb.x, qb.y);
+            mma_acc<false>(bb[nb], Z[0], Z[1], Z[2], Z[3], qb.z, qb.w);
+          }
+        }
       }
     }
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) kbm[nb] = fmaf((ba[nb][0] + ba[nb][1]) + (bb[nb][2] + bb[nb][3]), ks[nb], -mb[nb]);
   }
-  const float kb = (beta4[0] + beta4[1]) * ks;
-  const float k24 = ks * kTwo24;
 
   // ---- scores S = codes x Q' + beta ----
-  uint32_t bq[8][2];
-  build_qprime<BITS>(ws, tb.sk, g, tig, bq);
+  uint32_t bq[NB][8][2];
+  build_qprime<BITS, NB>(ws, tb.sk, g, tig, bq);
+  const int tr = score_row(g);
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt) {
-    const uint32_t* rg = tb.kc + (16 * mt + g) * RW;      // key row 16mt + g
-    const uint32_t* r8 = tb.kc + (16 * mt + g + 8) * RW;  // key row 16mt + g + 8
+    const int r0 = 16 * mt + tr, r1 = r0 + 4;  // the key rows of m-tile rows g and g + 8
+    const uint32_t* rg = tb.kc + r0 * RW;
+    const uint32_t* r8 = tb.kc + r1 * RW;
     // words of a row this lane reads: tig + 4j at 2 and 4 bits; at 8 bits the
     // 8 words from 8 tig, as two 16-byte chunks of the (rotated) row
     constexpr int NW = BITS == 3 ? 2 : BITS;
@@ -718,8 +807,8 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
     } else if constexpr (BITS == 8) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const uint4 a0 = reinterpret_cast<const uint4*>(rg)[krow_chunk<8>(g, 2 * tig + h)];
-        const uint4 a1 = reinterpret_cast<const uint4*>(r8)[krow_chunk<8>(g + 8, 2 * tig + h)];
+        const uint4 a0 = reinterpret_cast<const uint4*>(rg)[krow_chunk<8>(r0, 2 * tig + h)];
+        const uint4 a1 = reinterpret_cast<const uint4*>(r8)[krow_chunk<8>(r1, 2 * tig + h)];
         wg[4 * h] = a0.x; wg[4 * h + 1] = a0.y; wg[4 * h + 2] = a0.z; wg[4 * h + 3] = a0.w;
         w8[4 * h] = a1.x; w8[4 * h + 1] = a1.y; w8[4 * h + 2] = a1.z; w8[4 * h + 3] = a1.w;
       }
@@ -735,47 +824,58 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
       sg[j] = wg[j] >> kShift<BITS>;
       s8[j] = w8[j] >> kShift<BITS>;
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[NB][4];  // written first by k-step 0 (no accumulator input)
+#define KIVI_MMA_NB(KS, A0, A1, A2, A3)                                                      \
+  {                                                                                          \
+    const uint32_t a0_ = (A0), a1_ = (A1), a2_ = (A2), a3_ = (A3);                           \
+    _Pragma("unroll") for (int nb = 0; nb < NB; ++nb)                                        \
+        mma_acc<(KS) == 0>(acc[nb], a0_, a1_, a2_, a3_, bq[nb][KS][0], bq[nb][KS][1]);       \
+  }
     if constexpr (BITS == 3) {
       const uint32_t hg0 = rg[kHiPlane3 / 4 + tig], h80 = r8[kHiPlane3 / 4 + tig];
       const uint32_t hg1 = swap_half_bytes(hg0), h81 = swap_half_bytes(h80);
       // high sources of word j (set j): h, h >> 1
       const uint32_t hg[2] = {hg0, hg1}, h8[2] = {h80, h81};
       const uint32_t hgs[2] = {hg0 >> 1, hg1 >> 1}, h8s[2] = {h80 >> 1, h81 >> 1};
-#define KIVI_KSTEP3(KS, I)                                                                                  \
-  mma16816(acc, ext3<I>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),                     \
-           ext3<I>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]),                          \
-           ext3<I + 1>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),                      \
-           ext3<I + 1>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]), bq[KS][0], bq[KS][1]);
+#define KIVI_KSTEP3(KS, I)                                                                    \
+  KIVI_MMA_NB(KS, ext3<I>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),       \
+              ext3<I>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]),           \
+              ext3<I + 1>(wg[(KS) >> 2], sg[(KS) >> 2], hg[(KS) >> 2], hgs[(KS) >> 2]),       \
+              ext3<I + 1>(w8[(KS) >> 2], s8[(KS) >> 2], h8[(KS) >> 2], h8s[(KS) >> 2]))
       KIVI_KSTEP3(0, 0) KIVI_KSTEP3(1, 2) KIVI_KSTEP3(2, 4) KIVI_KSTEP3(3, 6)
       KIVI_KSTEP3(4, 0) KIVI_KSTEP3(5, 2) KIVI_KSTEP3(6, 4) KIVI_KSTEP3(7, 6)
 #undef KIVI_KSTEP3
     } else if constexpr (BITS == 2) {
-#define KIVI_KSTEP(KS, I)                                                                       \
-  mma16816(acc, ext<2, I>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I>(w8[(KS) >> 2], s8[(KS) >> 2]), \
-           ext<2, I + 1>(wg[(KS) >> 2], sg[(KS) >> 2]), ext<2, I + 1>(w8[(KS) >> 2], s8[(KS) >> 2]), \
-           bq[KS][0], bq[KS][1]);
+#define KIVI_KSTEP(KS, I)                                                                     \
+  KIVI_MMA_NB(KS, (ext<2, I>(wg[(KS) >> 2], sg[(KS) >> 2])), (ext<2, I>(w8[(KS) >> 2], s8[(KS) >> 2])), \
+              (ext<2, I + 1>(wg[(KS) >> 2], sg[(KS) >> 2])), (ext<2, I + 1>(w8[(KS) >> 2], s8[(KS) >> 2])))
       KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 4) KIVI_KSTEP(3, 6)
       KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 4) KIVI_KSTEP(7, 6)
 #undef KIVI_KSTEP
     } else if constexpr (BITS == 4) {
-#define KIVI_KSTEP(KS, I)                                                                       \
-  mma16816(acc, ext<4, I>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I>(w8[(KS) >> 1], s8[(KS) >> 1]), \
-           ext<4, I + 1>(wg[(KS) >> 1], sg[(KS) >> 1]), ext<4, I + 1>(w8[(KS) >> 1], s8[(KS) >> 1]), \
-           bq[KS][0], bq[KS][1]);
+#define KIVI_KSTEP(KS, I)                                                                     \
+  KIVI_MMA_NB(KS, (ext<4, I>(wg[(KS) >> 1], sg[(KS) >> 1])), (ext<4, I>(w8[(KS) >> 1], s8[(KS) >> 1])), \
+              (ext<4, I + 1>(wg[(KS) >> 1], sg[(KS) >> 1])), (ext<4, I + 1>(w8[(KS) >> 1], s8[(KS) >> 1])))
       KIVI_KSTEP(0, 0) KIVI_KSTEP(1, 2) KIVI_KSTEP(2, 0) KIVI_KSTEP(3, 2)
       KIVI_KSTEP(4, 0) KIVI_KSTEP(5, 2) KIVI_KSTEP(6, 0) KIVI_KSTEP(7, 2)
 #undef KIVI_KSTEP
     } else {
       // k-step ks: word ks (channels 4m .. 4m + 3, m = 8 tig + ks), bytes 0 / 2
       // then bytes 1 / 3 of each half
-#pragma unroll
-      for (int ksi = 0; ksi < 8; ++ksi)
-        mma16816(acc, ext<8, 0>(wg[ksi], sg[ksi]), ext<8, 0>(w8[ksi], s8[ksi]), ext<8, 1>(wg[ksi], sg[ksi]),
-                 ext<8, 1>(w8[ksi], s8[ksi]), bq[ksi][0], bq[ksi][1]);
+#define KIVI_KSTEP8(KS)                                                                       \
+  KIVI_MMA_NB(KS, (ext<8, 0>(wg[KS], sg[KS])), (ext<8, 0>(w8[KS], s8[KS])), (ext<8, 1>(wg[KS], sg[KS])), \
+              (ext<8, 1>(w8[KS], s8[KS])))
+      KIVI_KSTEP8(0) KIVI_KSTEP8(1) KIVI_KSTEP8(2) KIVI_KSTEP8(3)
+      KIVI_KSTEP8(4) KIVI_KSTEP8(5) KIVI_KSTEP8(6) KIVI_KSTEP8(7)
+#undef KIVI_KSTEP8
     }
-    sc[2 * mt] = fmaf(acc[0] + acc[1], k24, kb);      // token 16mt + g
-    sc[2 * mt + 1] = fmaf(acc[2] + acc[3], k24, kb);  // token 16mt + g + 8
+#undef KIVI_MMA_NB
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const float k24 = ks[nb] * kTwo24;
+      sc[nb][2 * mt] = fmaf(acc[nb][0] + acc[nb][1], k24, kbm[nb]);      // token r0
+      sc[nb][2 * mt + 1] = fmaf(acc[nb][2] + acc[nb][3], k24, kbm[nb]);  // token r0 + 4
+    }
   }
   if (n_out > 0) {
     // fp16 outlier channels (their codes, scales and zeros are 0 above)
@@ -784,83 +884,133 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS>& ws, const TileB
 #pragma unroll
     for (int o = 0; o < kMaxOutliers; ++o)
       if (o < n_out) {
-        const float qo = ws.qv[tig][(iw >> (8 * o)) & 0xffu] * scale_log2;
+        const int ch = (iw >> (8 * o)) & 0xffu;
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int t = 16 * (r >> 1) + g + 8 * (r & 1);
-          sc[r] = fmaf(qo, __half2float(ov[t * n_out + o]), sc[r]);
+        for (int nb = 0; nb < NB; ++nb) {
+          const float qo = ws.qv[4 * nb + tig][ch] * scale_log2;
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            const int t = 16 * (r >> 1) + tr + 4 * (r & 1);
+            sc[nb][r] = fmaf(qo, __half2float(ov[t * n_out + o]), sc[nb][r]);
+          }
         }
       }
   }
 }
 
-// Online softmax of head tig over one tile's scores (8 lanes share a head):
-// when a score exceeds the running max by more than kLazyMax, the max is
-// raised to the tile max plus kLazySlack and what the earlier tiles left in
-// lsum, O and Z is rescaled.  The weights p = 2^(S - max) <= 2^kLazyMax go to
-// the warp's weight buffer.
-__device__ __forceinline__ void softmax_p(const float (&sc)[4], float* pb, int g, int tig, float& m_run,
-                                          float& lsum, float (&O)[8][4], float (&Z)[4]) {
-  float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 4));
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 8));
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 16));
-  if (__any_sync(kFull, tmax > m_run + kLazyMax)) {
-    const float mnew = tmax > m_run + kLazyMax ? tmax + kLazySlack : m_run;
-    const float corr = fast_exp2(m_run - mnew);  // 0 on the first tile
-    m_run = mnew;
-    lsum *= corr;
+// Online softmax over one tile's scores (lane (g, tig) holds head 4 nb + tig
+// at four tokens; 8 lanes share a head): when a score exceeds a head's
+// running max by more than kLazyMax, the max is raised to the tile max plus
+// kLazySlack and what the earlier tiles left in O and Z is rescaled.  The
+// weights p = 2^(S - max) <= 2^kLazyMax are rounded to fp16 pairs and moved
+// to the value product's B fragments: lane (g, tig) gets head g at tokens
+// (16 kk + 8 aa + tig, + 4) in pb[kk][aa].
+// The scores arrive as x = S - mb with mb = m_run, or 0 while m_run is still
+// -inf (before the first tile).
+template <int NB>
+__device__ __forceinline__ void softmax_p(float (&x)[NB][4], int g, int tig, float (&m_run)[NB],
+                                          float (&O)[8][4], float (&Z)[4], uint32_t (&pb)[2][2]) {
+  float mx = -INFINITY;
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
+  for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) O[mt][i] *= corr;
+    for (int r = 0; r < 4; ++r) mx = fmaxf(mx, x[nb][r]);
+  bool first = false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) Z[i] *= corr;
+  for (int nb = 0; nb < NB; ++nb) first |= m_run[nb] == -INFINITY;
+  if (__any_sync(kFull, first || mx > kLazyMax)) {
+    float corr[NB];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const float mb = m_run[nb] == -INFINITY ? 0.0f : m_run[nb];
+      float t = fmaxf(fmaxf(x[nb][0], x[nb][1]), fmaxf(x[nb][2], x[nb][3]));
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 4));
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 8));
+      t = fmaxf(t, __shfl_xor_sync(kFull, t, 16));
+      t += mb;  // the tile max of head 4 nb + tig
+      const float mnew = t > m_run[nb] + kLazyMax ? t + kLazySlack : m_run[nb];
+      corr[nb] = fast_exp2(m_run[nb] - mnew);  // 0 on the first tile
+      m_run[nb] = mnew;
+      const float dm = mb - mnew;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[nb][r] += dm;
+    }
+    // the O and Z columns of this lane are heads 2 tig and 2 tig + 1, whose
+    // softmax state sits in lane (2 tig) & 3 / (2 tig + 1) & 3 of block tig >> 1
+    float cA = __shfl_sync(kFull, corr[0], (2 * tig) & 3);
+    float cB = __shfl_sync(kFull, corr[0], (2 * tig + 1) & 3);
+    if constexpr (NB == 2) {
+      const float cA1 = __shfl_sync(kFull, corr[1], (2 * tig) & 3);
+      const float cB1 = __shfl_sync(kFull, corr[1], (2 * tig + 1) & 3);
+      if (tig >= 2) {
+        cA = cA1;
+        cB = cB1;
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      O[mt][0] *= cA;
+      O[mt][1] *= cB;
+      O[mt][2] *= cA;
+      O[mt][3] *= cB;
+    }
+    Z[0] *= cA;
+    Z[1] *= cB;
+    Z[2] *= cA;
+    Z[3] *= cB;
   }
-  float* prow = pb + tig * 34;
+  uint32_t P2[NB][2];  // fp16 weights of tokens (16 mt + score_row(g), + 4)
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const float p = fast_exp2(sc[r] - m_run);  // token g + 8r
-    lsum += p;
-    prow[pbuf_pos(g + 8 * r)] = p;
-  }
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+      P2[nb][mt] = f2_to_h2(fast_exp2(x[nb][2 * mt]), fast_exp2(x[nb][2 * mt + 1]));
+  // token 16 kk + 8 aa + tig is row score_row^-1(8 aa + tig) = tig + 4 aa of
+  // m-tile kk; head g is lane (.., g & 3) of block g >> 2
+#pragma unroll
+  for (int kk = 0; kk < 2; ++kk)
+#pragma unroll
+    for (int aa = 0; aa < 2; ++aa) {
+      const int src = 4 * (tig + 4 * aa) + (g & 3);
+      const uint32_t v0 = __shfl_sync(kFull, P2[0][kk], src);
+      if constexpr (NB == 2) {
+        const uint32_t v1 = __shfl_sync(kFull, P2[NB - 1][kk], src);
+        pb[kk][aa] = g >= 4 ? v1 : v0;
+      } else {
+        pb[kk][aa] = v0;  // columns 4..7 repeat heads 0..3 and are not used
+      }
+    }
 }
 
-// Values of one staged tile: O += codes^T x (p * sV), Z += zV^T x p, with p
-// from the warp's weight buffer (O and Z of head tig).  The k rows (2tig,
-// 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows (2tig+8,
-// 2tig+9) tokens t0 + 8 and t0 + 12.  M-tile 2gp + hm covers value group gp:
-// row g is channel 32gp + 4g + 2hm, row g + 8 the next channel.
+// Values of one staged tile: O += codes^T x (p * sV), Z += [zV; 1]^T x p,
+// with the fp16 weights pb of the tile (column g = head g).  The k rows
+// (2tig, 2tig+1) of k-step kk hold tokens t0 = 16kk + tig and t0 + 4, rows
+// (2tig+8, 2tig+9) tokens t0 + 8 and t0 + 12.  M-tile 2gp + hm covers value
+// group gp: row g is channel 32gp + 4g + 2hm, row g + 8 the next channel.
+// Row g of the z-term product is value group g & 3, row g + 8 all ones, so
+// Z[2], Z[3] accumulate the sums of the weights of this lane's heads.
 template <int BITS>
-__device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* pb, int g, int tig,
+__device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const uint32_t (&pb)[2][2], int g, int tig,
                                           float (&O)[8][4], float (&Z)[4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
-  const int part = g & 1;
-  const float* pv = pb + (g >> 1) * 34 + 8 * tig;
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk) {
     // u[aa][gp]: the codes of channels 4g..4g+3 of group gp for tokens (t0,
     // t0 + 4), as the two 16-bit halves (2 bits: a byte per group, two groups
     // per word)
-    uint32_t pa[2], Pp[4][2], az[2], u[2][4];
+    uint32_t Pp[4][2], az[2], u[2][4];
     uint32_t v8a[2][4], v8b[2][4];  // 8 bits: unit words of groups 0..3 of tokens t0 and t0 + 4
     uint32_t hv[2][2];              // 3 bits: high units of tokens (t0, t0 + 4), groups 0/1 and 2/3
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
       const int t0 = 16 * kk + 8 * aa + tig;  // tokens t0, t0 + 4
-      const float2 x = *reinterpret_cast<const float2*>(pv + 4 * kk + 2 * aa);
-      const uint32_t h = f2_to_h2(x.x, x.y);
-      const uint32_t l = f2_to_h2(x.x - h_lo(h), x.y - h_hi(h));
-      // split_mul operands of this lane's part (see split_mul)
-      pa[aa] = part ? l : h;
-      const uint32_t pbh = part ? h : 0u;
       // the scale / zero words of token pair (t0, t0 + 4) (see vscale_pos)
       const int pw = 4 * (4 * (2 * kk + aa) + tig);
       const uint4 S = *reinterpret_cast<const uint4*>(tb.sv + pw);  // groups 0..3
-      Pp[0][aa] = split_mul(pa[aa], pbh, S.x);
-      Pp[1][aa] = split_mul(pa[aa], pbh, S.y);
-      Pp[2][aa] = split_mul(pa[aa], pbh, S.z);
-      Pp[3][aa] = split_mul(pa[aa], pbh, S.w);
+      Pp[0][aa] = hmul2u(pb[kk][aa], S.x);
+      Pp[1][aa] = hmul2u(pb[kk][aa], S.y);
+      Pp[2][aa] = hmul2u(pb[kk][aa], S.z);
+      Pp[3][aa] = hmul2u(pb[kk][aa], S.w);
       az[aa] = tb.zv[pw + (g & 3)];
       if constexpr (BITS == 2 || BITS == 3) {
         // interleaved word g of a row holds, per byte, channels 4g..4g+3 of groups 0..3
@@ -894,8 +1044,8 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
         u[aa][3] = __byte_perm(w0.y, w1.y, 0x7632);
       }
     }
-    // z-term: rows = value groups (g & 3), columns = (head, part) of p
-    mma16816(Z, az[0], az[0], az[1], az[1], pa[0], pa[1]);
+    // z-term and weight sums: rows g = value group g & 3, rows g + 8 = ones
+    mma16816(Z, az[0], kOnesH2, az[1], kOnesH2, pb[kk][0], pb[kk][1]);
     if constexpr (BITS == 3) {
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
@@ -956,40 +1106,49 @@ __device__ __forceinline__ void value_acc(const TileBuf<BITS>& tb, const float* 
 }
 
 // q of the CTA's heads: staged once in shared memory, per-head exponents
-// (warp w takes head w), then the tables in fragment order.  Thread (head,
-// tig, word) builds the pair words of both parts.
-static_assert(kWarps == kNH, "warp w loads and scales head w");
+// (warp w takes heads w and w + 4), then the tables in fragment order.
+// Thread (block, head, tig, word) builds the pair words of both parts.
+static_assert(kNH == 2 * kWarps, "warp w loads and scales heads w and w + 4");
 
-// Channels 4 lane .. 4 lane + 3 of the CTA's head `warp` (zeros past the last
-// head).  Issued before the first tile copies, so that the load does not
-// queue behind them.
-__device__ __forceinline__ void load_q4(const AttnArgs& a, int b, int j0, int nh, float (&v)[4]) {
+// Channels 4 lane .. 4 lane + 3 of the CTA's heads `warp` (v[0..3]) and
+// `warp` + 4 (v[4..7]), zeros past the last head.  Issued before the first
+// tile copies, so that the load does not queue behind them.
+__device__ __forceinline__ void load_q8(const AttnArgs& a, int b, int j0, int nh, float (&v)[8]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    v[i] = warp < nh ? load_q(a.q, ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane + i, a.q_dtype) : 0.0f;
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = warp + kWarps * hh;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      v[4 * hh + i] = j < nh ? load_q(a.q, ((long)b * a.Hq + j0 + j) * kHeadDim + 4 * lane + i, a.q_dtype) : 0.0f;
+  }
 }
 
-template <int BITS>
-__device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float (&v)[4]) {
+template <int BITS, int NB>
+__device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const float (&v)[8]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  {
-    *reinterpret_cast<float4*>(&s.qv[warp][4 * lane]) = make_float4(v[0], v[1], v[2], v[3]);
-    const float amax = warp_max(fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3]))));
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = warp + kWarps * hh;
+    const float* vj = v + 4 * hh;
+    *reinterpret_cast<float4*>(&s.qv[j][4 * lane]) = make_float4(vj[0], vj[1], vj[2], vj[3]);
+    const float amax = warp_max(fmaxf(fmaxf(fabsf(vj[0]), fabsf(vj[1])), fmaxf(fabsf(vj[2]), fabsf(vj[3]))));
     if (lane == 0) {
       const int be = (int)((__float_as_uint(amax) >> 23) & 0xffu);
       // amax in [2^(be-127), 2^(be-126)) for normal amax; a subnormal amax is
       // below 2^-126, a zero row keeps E = 0
       const int E = amax == 0.0f ? 0 : (be == 0 ? -126 : be - 126);
-      s.qexp[warp] = E;
-      s.qscale[warp] = ldexpf(a.scale_log2, E);
+      s.qexp[j] = E;
+      s.qscale[j] = ldexpf(a.scale_log2, E);
     }
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < kNH * 4 * 16; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < NB * 4 * 4 * 16; idx += blockDim.x) {
     const int word = idx & 15;                // ks * 2 + r
     const int tig = (idx >> 4) & 3;
-    const int hh = idx >> 6;
+    const int hh = (idx >> 6) & 3;            // head within the key block
+    const int nb = idx >> 8;
+    const int j = 4 * nb + hh;
     const int ks = word >> 1, r = word & 1;
     int c0, c1, i;  // the channel pair of the word and its code position
     if constexpr (BITS == 2 || BITS == 3) {
@@ -1009,19 +1168,21 @@ __device__ void build_q_tables(WarpSmem<BITS>& s, const AttnArgs& a, const float
       c1 = c0 + 2;
     }
     const float f = code_scale<BITS>(i);
-    const float q0 = ldexpf(s.qv[hh][c0], -s.qexp[hh]), q1 = ldexpf(s.qv[hh][c1], -s.qexp[hh]);
+    const float q0 = ldexpf(s.qv[j][c0], -s.qexp[j]), q1 = ldexpf(s.qv[j][c1], -s.qexp[j]);
     const uint32_t qh = f2_to_h2(q0, q1);
     const uint32_t ql = f2_to_h2(q0 - h_lo(qh), q1 - h_hi(qh));
     const uint32_t sh = f2_to_h2(q0 * f, q1 * f);
     const uint32_t sl = f2_to_h2(q0 * f - h_lo(sh), q1 * f - h_hi(sh));
     const int quarter = word >> 2, wq = word & 3;
     // hi lane: (xa, xb) = (hi, 0); lo lane: (lo, hi)
-    reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh][tig])[wq] = sh;
-    reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh][tig])[wq] = 0u;
-    reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh + 1][tig])[wq] = sl;
-    reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh + 1][tig])[wq] = sh;
-    reinterpret_cast<uint32_t*>(&s.qb[quarter][2 * hh][tig])[wq] = qh;
-    reinterpret_cast<uint32_t*>(&s.qb[quarter][2 * hh + 1][tig])[wq] = ql;
+    reinterpret_cast<uint32_t*>(&s.qs[nb][0][quarter][2 * hh][tig])[wq] = sh;
+    reinterpret_cast<uint32_t*>(&s.qs[nb][1][quarter][2 * hh][tig])[wq] = 0u;
+    reinterpret_cast<uint32_t*>(&s.qs[nb][0][quarter][2 * hh + 1][tig])[wq] = sl;
+    reinterpret_cast<uint32_t*>(&s.qs[nb][1][quarter][2 * hh + 1][tig])[wq] = sh;
+    // the beta MMAs take words (0, 2) and (1, 3) of a quarter as B pairs
+    const int wb = wq == 1 ? 2 : (wq == 2 ? 1 : wq);
+    reinterpret_cast<uint32_t*>(&s.qb[nb][quarter][2 * hh][tig])[wb] = qh;
+    reinterpret_cast<uint32_t*>(&s.qb[nb][quarter][2 * hh + 1][tig])[wb] = ql;
   }
 }
 
@@ -1060,28 +1221,32 @@ __device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long
   bulk_g2s(&tb, u.tiles + (long)tile * u.tile_bytes, u.tile_bytes, bar);
 }
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// The same from a source address.
+template <int BITS>
+__device__ __forceinline__ void issue_tile_at(TileBuf<BITS>& tb, unsigned long long* bar, const uint8_t* src,
+                                              uint32_t bytes) {
+  mbar_expect_tx(bar, bytes);
+  bulk_g2s(&tb, src, bytes, bar);
 }
 
 // Packed tiles [tile0, tile1) of one (batch, kv-head, head chunk) on the
 // tensor cores.  Warp w takes tiles tile0 + w, + kWarps, ... through its own
 // ring of staged tiles (lane 0 issues the copies; no CTA barrier in the
-// loop).  Leaves each warp's (max, sum) in s_m / s_l and its output in its
-// merge area.
-template <int BITS>
-__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS>& sm, long unit, int b,
+// loop).  Leaves each warp's (max, sum) per head in s_m / s_l and its output
+// in its merge area.
+template <int BITS, int NB>
+__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS, NB>& sm, long unit, int b,
                              int j0, int nh, int tile0, int tile1, float (&s_m)[kWarps][kNH],
                              float (&s_l)[kWarps][kNH]) {
   constexpr int kStages = kStagesOf<BITS>;
-  WarpSmem<BITS>& ws = sm.ws;
+  WarpSmem<BITS, NB>& ws = sm.ws;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
   TileBuf<BITS>* st = ws.st[warp];
   unsigned long long* bars = ws.bar[warp];
-  float qv4[4];
-  load_q4(a, b, j0, nh, qv4);
+  float qv8[8];
+  load_q8(a, b, j0, nh, qv8);
 
   if (lane == 0) {
 #pragma unroll
@@ -1099,15 +1264,19 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   // append runs and issues every copy after it.
   const bool wait_first = a.pdl == kPdlAll;
   if (!wait_first && lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
-  build_q_tables<BITS>(ws, a, qv4);
+  build_q_tables<BITS, NB>(ws, a, qv8);
   __syncthreads();
   if (wait_first) grid_dependency_wait();
   if (lane == 0)
     for (int k = wait_first ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
-  const float ks = ws.qscale[tig];
-  float* pb = &ws.pbuf[warp][0][0];
+  float ks[NB], m_run[NB];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb) {
+    ks[nb] = ws.qscale[4 * nb + tig];
+    m_run[nb] = -INFINITY;
+  }
 
-  float O[8][4], Z[4], m_run = -INFINITY, lsum = 0.0f;
+  float O[8][4], Z[4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
@@ -1118,60 +1287,57 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   // Tile k's scores are computed one iteration ahead of its values: the
   // scores of tile k + 1 and the values of tile k form one straight-line
   // block (the wait for tile k + 1 comes first), so that their independent
-  // MMA chains can interleave.  The ring is walked kStages tiles per round so
-  // that every stage address is a constant.
+  // MMA chains can interleave.  One loop body walks the ring with the stage
+  // as a run-time index.
   int done = 0;
   bool failed = false;
-  float sc[4];
+  uint32_t pb[2][2];  // the staged tile's weights as value B fragments
   if (n_mine > 0) {
     bool ok = mbar_try_wait(&bars[0], 0u);
     if (!ok) ok = mbar_wait(&bars[0], 0u);
     if (__any_sync(kFull, !ok)) {
       failed = true;
     } else {
-      key_scores<BITS>(ws, st[0], g, tig, ks, cv.n_out, a.scale_log2, sc);
-      softmax_p(sc, pb, g, tig, m_run, lsum, O, Z);
-      __syncwarp();
+      float sc[NB][4], mb[NB];
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) mb[nb] = 0.0f;
+      key_scores<BITS, NB>(ws, st[0], g, tig, ks, mb, cv.n_out, a.scale_log2, sc);
+      softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
     }
   }
-  int k = 0;  // tile whose values are next
-  while (k + 1 < n_mine && !failed) {
-#pragma unroll
-    for (int sg = 0; sg < kStages; ++sg) {
-      // tile k sits in stage sg (k is a multiple of kStages at sg == 0)
-      if (k + 1 < n_mine && !failed) {
-        const int sn = sg + 1 == kStages ? 0 : sg + 1;  // stage of tile k + 1
-        const uint32_t parn = (uint32_t)(((k + 1) / kStages) & 1);
-        bool ok = mbar_try_wait(&bars[sn], parn);
-        if (!ok) ok = mbar_wait(&bars[sn], parn);
-        if (__any_sync(kFull, !ok)) {
-          failed = true;
-        } else {
-          float scn[4];
-          key_scores<BITS>(ws, st[sn], g, tig, ks, cv.n_out, a.scale_log2, scn);
-          value_acc<BITS>(st[sg], pb, g, tig, O, Z);
-          done = k + 1;
-          __syncwarp();  // every lane is done with stage sg and the weight buffer
-          if (k + kStages < n_mine) {
-            if (lane == 0) {
-              fence_proxy_async();
-              issue_tile<BITS>(st[sg], &bars[sg], us, t_first + kWarps * (k + kStages));
-            }
-            ++issued;
-          }
-          softmax_p(scn, pb, g, tig, m_run, lsum, O, Z);
-          __syncwarp();
-          ++k;
-        }
-      }
+  int k = 0, sk = 0;     // tile whose values are next, and its stage
+  uint32_t parn = 0;     // phase parity of the stage of tile k + 1
+  // source of the next tile to stage (tile k + kStages of this warp)
+  const long src_step = (long)kWarps * us.tile_bytes;
+  const uint8_t* next_src = us.tiles + (long)(t_first + kWarps * kStages) * us.tile_bytes;
+  while (!failed && k + 1 < n_mine) {
+    const int sn = sk + 1 == kStages ? 0 : sk + 1;  // stage of tile k + 1
+    if (sn == 0) parn ^= 1u;
+    bool ok = mbar_try_wait(&bars[sn], parn);
+    if (!ok) ok = mbar_wait(&bars[sn], parn);
+    if (__any_sync(kFull, !ok)) {
+      failed = true;
+      break;
     }
+    float sc[NB][4];
+    key_scores<BITS, NB>(ws, st[sn], g, tig, ks, m_run, cv.n_out, a.scale_log2, sc);
+    value_acc<BITS>(st[sk], pb, g, tig, O, Z);
+    done = k + 1;
+    __syncwarp();  // every lane is done with stage sk
+    if (k + kStages < n_mine) {
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_tile_at<BITS>(st[sk], &bars[sk], next_src, us.tile_bytes);
+      }
+      next_src += src_step;
+      ++issued;
+    }
+    softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
+    ++k;
+    sk = sn;
   }
   if (!failed && n_mine > 0) {
-    // the last tile's values (its stage: (n_mine - 1) % kStages)
-    const int sl = (n_mine - 1) % kStages;
-#pragma unroll
-    for (int sg = 0; sg < kStages; ++sg)
-      if (sg == sl) value_acc<BITS>(st[sg], pb, g, tig, O, Z);
+    value_acc<BITS>(st[sk], pb, g, tig, O, Z);  // the last tile's values
     done = n_mine;
   }
   if (done < n_mine) {
@@ -1180,23 +1346,32 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     if (lane == 0) atomicOr(a.status, 1);
     for (int kk = done; kk < issued; ++kk) mbar_wait(&bars[kk % kStages], (uint32_t)((kk / kStages) & 1));
     __syncwarp();
+  } else if (lane == 0) {
+    // every copy has landed: the barriers' memory may be reused
+#pragma unroll
+    for (int kk = 0; kk < kStages; ++kk) mbar_inval(&bars[kk]);
   }
 
-  // ---- this warp's partial: max, sum and output of head tig ----
-  // lsum of head tig over tokens g + 8r: sum over g
-  lsum += __shfl_xor_sync(kFull, lsum, 4);
-  lsum += __shfl_xor_sync(kFull, lsum, 8);
-  lsum += __shfl_xor_sync(kFull, lsum, 16);
+  // ---- this warp's partial: max, sum and output per head ----
+  // The value columns of lane (g, tig) are heads 2 tig and 2 tig + 1: their
+  // weight sums are Z[2], Z[3] (the all-ones rows); the running max of head
+  // 4 nb + tig is m_run[nb] of the lanes with this tig.
   if (g == 0) {
-    s_m[warp][tig] = m_run;
-    s_l[warp][tig] = lsum;
-  }
-  // z-term of value group gp for head tig sits in lane (gp, tig)
-  const float zmine = Z[0] + Z[1];
-  float zt[4];
 #pragma unroll
-  for (int gp = 0; gp < 4; ++gp) zt[gp] = __shfl_sync(kFull, zmine, 4 * gp + tig);
-  float* orow = merge_area(sm, warp, kPathMma) + tig * kHeadDim;
+    for (int nb = 0; nb < 2; ++nb) s_m[warp][4 * nb + tig] = nb < NB && n_mine > 0 ? m_run[nb < NB ? nb : 0] : -INFINITY;
+    s_l[warp][2 * tig] = Z[2];
+    s_l[warp][2 * tig + 1] = Z[3];
+  }
+  // z-term of value group gp for heads (2 tig, 2 tig + 1): Z[0], Z[1] of lane (gp, tig)
+  float zt[4][2];
+#pragma unroll
+  for (int gp = 0; gp < 4; ++gp) {
+    zt[gp][0] = __shfl_sync(kFull, Z[0], 4 * gp + tig);
+    zt[gp][1] = __shfl_sync(kFull, Z[1], 4 * gp + tig);
+  }
+  if (n_mine == 0) return;  // no tile: the area stays unwritten (max -inf)
+  float* oa = merge_area(sm, warp, kPathMma) + (2 * tig) * kHeadDim;
+  float* ob = oa + kHeadDim;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const int gp = mt >> 1, hm = mt & 1;
@@ -1205,15 +1380,13 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     const int ch = 32 * gp + 4 * g + 2 * hm;
     const float f_lo = kTwo24 * code_scale<BITS>(i_lo);
     const float f_hi = kTwo24 * code_scale<BITS>(i_lo + 1);
-    orow[ch] = (O[mt][0] + O[mt][1]) * f_lo + zt[gp];
-    orow[ch + 1] = (O[mt][2] + O[mt][3]) * f_hi + zt[gp];
+    oa[ch] = O[mt][0] * f_lo + zt[gp][0];
+    ob[ch] = O[mt][1] * f_lo + zt[gp][1];
+    oa[ch + 1] = O[mt][2] * f_hi + zt[gp][0];
+    ob[ch + 1] = O[mt][3] * f_hi + zt[gp][1];
   }
 }
 
-// Merge n <= kMergeGroup partials [n][kNH][D] (outputs) and [n][kNH][2]
-// (max, sum): warp w takes head w, lane l channels 4l..4l+3; every load is
-// issued before the first is used.  Returns the merged (unnormalized) output
-// quad, max and sum of head `warp`.
 // Count a CTA in (thread 0, after a CTA barrier that follows the CTA's
 // partial writes); returns the count before.  Release: the barrier orders
 // every thread's writes before this atomic, so they are visible to whichever
@@ -1225,18 +1398,20 @@ __device__ __forceinline__ int count_in(int* counter) {
   return old;
 }
 
-__device__ __forceinline__ void merge_partials(const float* po, const float* pml, int n, int nh, float4& o4,
+// Merge n <= kMergeGroup partials [n][kNH][D] (outputs) and [n][kNH][2]
+// (max, sum) of head j: lane l takes channels 4l..4l+3; every load is issued
+// before the first is used.  Returns the merged (unnormalized) output quad,
+// max and sum of head j.
+__device__ __forceinline__ void merge_partials(const float* po, const float* pml, int n, int j, float4& o4,
                                                float& m_out, float& l_out) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31;
   float4 v[kMergeGroup];
 #pragma unroll
   for (int k = 0; k < kMergeGroup; ++k)
-    v[k] = (k < n && warp < nh)
-               ? __ldcg(reinterpret_cast<const float4*>(po + ((long)k * kNH + warp) * kHeadDim) + lane)
-               : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float2 ml = (lane < n && warp < nh)
-                        ? __ldcg(reinterpret_cast<const float2*>(pml + ((long)lane * kNH + warp) * 2))
-                        : make_float2(-INFINITY, 0.0f);
+    v[k] = k < n ? __ldcg(reinterpret_cast<const float4*>(po + ((long)k * kNH + j) * kHeadDim) + lane)
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float2 ml = lane < n ? __ldcg(reinterpret_cast<const float2*>(pml + ((long)lane * kNH + j) * 2))
+                             : make_float2(-INFINITY, 0.0f);
   const float M = warp_max(ml.x);
   const float e = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - M);
   l_out = warp_sum(e * ml.y);
@@ -1257,10 +1432,10 @@ __device__ __forceinline__ void merge_partials(const float* po, const float* pml
 // the warps' packed partials are merged into registers, the tail rounds run
 // one after another and are folded in, and the result is left as warp 0's
 // slot (the other warps' slots empty) for the CTA merge.
-template <int BITS>
-__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS>& sm,
-                           long unit, int b,
-                           int j0, int nh, float (&s_m)[kWarps][kNH], float (&s_l)[kWarps][kNH]) {
+template <int BITS, int NB>
+__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS, NB>& sm,
+                           long unit, int b, int j0, int nh, float (&s_m)[kWarps][kNH],
+                           float (&s_l)[kWarps][kNH]) {
   const int d = threadIdx.x;
   float pm[kNH], pl[kNH], po[kNH];
 #pragma unroll
@@ -1283,17 +1458,19 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
     po[j] = ot;
   }
   __syncthreads();  // the warps' slots are read; the tail may overwrite them
-  for (int c0 = p.t_tail; c0 < p.l; c0 += kTailTok) {
-    tail_split<BITS>(cv, a, p, sm, unit, b, j0, nh, c0, s_m, s_l);
+  float* mo0 = merge_area(sm, 0, kPathTail);
+  uint32_t round = 0;
+  for (int c0 = p.t_tail; c0 < p.l; c0 += kTailTok, ++round) {
+    tail_split<BITS, NB>(cv, a, p, sm.tail, mo0, unit, b, j0, nh, c0, round, s_m, s_l);
     __syncthreads();
-    const float* mo0 = merge_area(sm, 0, kPathTail);
 #pragma unroll
     for (int j = 0; j < kNH; ++j) {
       const float tm = s_m[0][j];
       const float M = fmaxf(pm[j], tm);
       const float e1 = pm[j] == -INFINITY ? 0.0f : fast_exp2(pm[j] - M);
       const float e2 = tm == -INFINITY ? 0.0f : fast_exp2(tm - M);
-      po[j] = po[j] * e1 + mo0[j * kHeadDim + d] * e2;
+      // (rows of heads the tail does not serve are not written: max -inf)
+      po[j] = po[j] * e1 + (tm == -INFINITY ? 0.0f : mo0[j * kHeadDim + d] * e2);
       pl[j] = pl[j] * e1 + s_l[0][j] * e2;
       pm[j] = M;
     }
@@ -1304,20 +1481,31 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
   for (int j = 0; j < kNH; ++j) out0[j * kHeadDim + d] = po[j];
   if (d < kWarps * kNH) {
     const int w = d / kNH, j = d % kNH;
-    s_m[w][j] = w == 0 ? pick4(pm, j) : -INFINITY;
-    s_l[w][j] = w == 0 ? pick4(pl, j) : 0.0f;
+    float mj = pm[0], lj = pl[0];
+#pragma unroll
+    for (int i = 1; i < kNH; ++i) {
+      mj = j == i ? pm[i] : mj;
+      lj = j == i ? pl[i] : lj;
+    }
+    s_m[w][j] = w == 0 ? mj : -INFINITY;
+    s_l[w][j] = w == 0 ? lj : 0.0f;
   }
   __syncthreads();
 }
 
 // grid (splits, H * head_chunks, B), 128 threads.
-template <int BITS>
-__global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS>)
-  SplitSmem<BITS>& sm = *reinterpret_cast<SplitSmem<BITS>*>(smem_raw);
+template <int BITS, int NB>
+__global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
+    attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS, NB>)
+  SplitSmem<BITS, NB>& sm = *reinterpret_cast<SplitSmem<BITS, NB>*>(smem_raw);
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
   __shared__ bool s_last;
 
+  // A programmatic dependent of this launch (another attention call) may
+  // start its CTAs as this launch's CTAs finish; it waits for this launch
+  // before its own first write.
+  grid_launch_dependents();
   const int s = blockIdx.x;
   const int nhc = gridDim.y / cv.H;
   const int h = blockIdx.y / nhc, hc = blockIdx.y % nhc;
@@ -1334,20 +1522,25 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
   const int path = s < p.tail_splits ? kPathTail : kPathMma;
 
   if (path == kPathTail) {
-    if (a.pdl) grid_dependency_wait();  // the tail reads the rings the append writes
-    tail_split<BITS>(cv, a, p, sm, unit, b, j0, nh, p.t_tail + s * kTailTok, s_m, s_l);
+    // the tail reads the rings the append writes
+    if (a.pdl == kPdlAll || a.pdl == kPdlTail) grid_dependency_wait();
+    tail_split<BITS, NB>(cv, a, p, sm.tail, merge_area(sm, 0, kPathTail), unit, b, j0, nh,
+                         p.t_tail + s * kTailTok, 0u, s_m, s_l);
   } else {
     // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
     const int sp = s - p.tail_splits;
     const int tile0 = sp * p.chunk / 32;
     const int tile1 = min(p.t_tail, (sp + 1) * p.chunk) / 32;
-    packed_split<BITS>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
+    packed_split<BITS, NB>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
   if (path == kPathMma && p.tail_fused && s == p.splits - 1) {
     if (a.pdl == kPdlTail) grid_dependency_wait();  // the tail reads what the append wrote
-    fused_tail<BITS>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
+    fused_tail<BITS, NB>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
   }
+  // an overlapping launch waits for the launch before it only here, before
+  // its first global write
+  if (a.pdl == kPdlOverlap) grid_dependency_wait();
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;
@@ -1387,18 +1580,28 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
   }
   __syncthreads();
   if (!s_last) return;
-  float4 o4;
-  float lsum_h, m_h;
-  merge_partials(a.ws_o + (gid * a.splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.splits + g_lo) * kNH * 2,
-                 g_n, nh, o4, m_h, lsum_h);
+  // warp w merges heads w and w + kWarps
+  float4 o4[2];
+  float lsum_h[2], m_h[2];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = warp + kWarps * hh;
+    if (j < nh)
+      merge_partials(a.ws_o + (gid * a.splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.splits + g_lo) * kNH * 2,
+                     g_n, j, o4[hh], m_h[hh], lsum_h[hh]);
+  }
   if (n_grp > 1) {
     // a group result: write it, then count the group in
-    if (warp < nh) {
-      const long pidx = (gid * a.merge_groups + grp_i) * kNH + warp;
-      *reinterpret_cast<float4*>(a.ws_o1 + pidx * kHeadDim + 4 * lane) = o4;
-      if (lane == 0) {
-        a.ws_ml1[pidx * 2] = m_h;
-        a.ws_ml1[pidx * 2 + 1] = lsum_h;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = warp + kWarps * hh;
+      if (j < nh) {
+        const long pidx = (gid * a.merge_groups + grp_i) * kNH + j;
+        *reinterpret_cast<float4*>(a.ws_o1 + pidx * kHeadDim + 4 * lane) = o4[hh];
+        if (lane == 0) {
+          a.ws_ml1[pidx * 2] = m_h[hh];
+          a.ws_ml1[pidx * 2 + 1] = lsum_h[hh];
+        }
       }
     }
     __syncthreads();
@@ -1409,13 +1612,21 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
     }
     __syncthreads();
     if (!s_last) return;
-    merge_partials(a.ws_o1 + gid * a.merge_groups * kNH * kHeadDim, a.ws_ml1 + gid * a.merge_groups * kNH * 2,
-                   n_grp, nh, o4, m_h, lsum_h);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int j = warp + kWarps * hh;
+      if (j < nh)
+        merge_partials(a.ws_o1 + gid * a.merge_groups * kNH * kHeadDim, a.ws_ml1 + gid * a.merge_groups * kNH * 2,
+                       n_grp, j, o4[hh], m_h[hh], lsum_h[hh]);
+    }
   }
-  if (warp < nh) {
-    const float inv = 1.0f / lsum_h;
-    const float r[4] = {o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv};
-    const long oi = ((long)b * a.Hq + j0 + warp) * kHeadDim + 4 * lane;
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = warp + kWarps * hh;
+    if (j >= nh) continue;
+    const float inv = 1.0f / lsum_h[hh];
+    const float r[4] = {o4[hh].x * inv, o4[hh].y * inv, o4[hh].z * inv, o4[hh].w * inv};
+    const long oi = ((long)b * a.Hq + j0 + j) * kHeadDim + 4 * lane;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (a.q_dtype == kF32) static_cast<float*>(a.out)[oi + i] = r[i];
@@ -1427,38 +1638,40 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS)) attn_kernel(Cache
 
 }  // namespace
 
-// attn_ctas_per_sm(BITS) CTAs must fit an SM's 228 KB of shared memory
+// attn_ctas_per_sm(BITS, NB) CTAs must fit an SM's 228 KB of shared memory
 // (1 KB of it reserved per CTA).
-static_assert(4 * (sizeof(SplitSmem<2>) + 1024 + 256) <= 228 * 1024, "2-bit CTAs per SM");
-static_assert(4 * (sizeof(SplitSmem<3>) + 1024 + 256) <= 228 * 1024, "3-bit CTAs per SM");
-static_assert(4 * (sizeof(SplitSmem<4>) + 1024 + 256) <= 228 * 1024, "4-bit CTAs per SM");
-static_assert(2 * (sizeof(SplitSmem<8>) + 1024 + 256) <= 228 * 1024, "8-bit CTAs per SM");
+template <int BITS, int NB>
+constexpr bool kFitsSm =
+    attn_ctas_per_sm(BITS, NB) * (sizeof(SplitSmem<BITS, NB>) + 1024 + 512) <= 228 * 1024;
+static_assert(kFitsSm<2, 1> && kFitsSm<2, 2>, "2-bit CTAs per SM");
+static_assert(kFitsSm<3, 1> && kFitsSm<3, 2>, "3-bit CTAs per SM");
+static_assert(kFitsSm<4, 1> && kFitsSm<4, 2>, "4-bit CTAs per SM");
+static_assert(kFitsSm<8, 1> && kFitsSm<8, 2>, "8-bit CTAs per SM");
 
-template <int BITS>
+template <int BITS, int NB>
 cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
                         cudaStream_t st) {
   // The shared-memory opt-in is a per-device function attribute; setting it
   // on every call costs a host call only.
-  const cudaError_t e = cudaFuncSetAttribute(attn_kernel<BITS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(SplitSmem<BITS>));
+  const cudaError_t e = cudaFuncSetAttribute(attn_kernel<BITS, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)sizeof(SplitSmem<BITS, NB>));
   if (e != cudaSuccess) return e;
   if (!a.pdl) {
-    attn_kernel<BITS><<<grid, 128, sizeof(SplitSmem<BITS>), st>>>(cv, a, lens);
+    attn_kernel<BITS, NB><<<grid, 128, sizeof(SplitSmem<BITS, NB>), st>>>(cv, a, lens);
     return cudaGetLastError();
   }
   // a programmatic dependent of the kernel before it on the stream
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = dim3(128);
-  lc.dynamicSmemBytes = sizeof(SplitSmem<BITS>);
+  lc.dynamicSmemBytes = sizeof(SplitSmem<BITS, NB>);
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = at;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, attn_kernel<BITS>, cv, a, lens);
+  return cudaLaunchKernelEx(&lc, attn_kernel<BITS, NB>, cv, a, lens);
 }
 
 cudaError_t launch_wait_probe(int* status, cudaStream_t st) {
@@ -1466,16 +1679,22 @@ cudaError_t launch_wait_probe(int* status, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+template <int NB>
+cudaError_t launch_nb(const dim3& grid, const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
+                      cudaStream_t st) {
+  switch (cv.bits) {
+    case 2: return launch_bits<2, NB>(grid, cv, a, lens, st);
+    case 3: return launch_bits<3, NB>(grid, cv, a, lens, st);
+    case 4: return launch_bits<4, NB>(grid, cv, a, lens, st);
+    default: return launch_bits<8, NB>(grid, cv, a, lens, st);
+  }
+}
+
 cudaError_t launch_attention(const CacheView& cv, const AttnArgs& a, const SeqLens& lens, cudaStream_t st) {
   const int grp = a.Hq / cv.H;
   const int nhc = (grp + kNH - 1) / kNH;
   const dim3 grid(a.splits, cv.H * nhc, cv.B);
-  switch (cv.bits) {
-    case 2: return launch_bits<2>(grid, cv, a, lens, st);
-    case 3: return launch_bits<3>(grid, cv, a, lens, st);
-    case 4: return launch_bits<4>(grid, cv, a, lens, st);
-    default: return launch_bits<8>(grid, cv, a, lens, st);
-  }
+  return attn_key_blocks(grp) == 2 ? launch_nb<2>(grid, cv, a, lens, st) : launch_nb<1>(grid, cv, a, lens, st);
 }
 
 }  // namespace kivi

@@ -19,6 +19,7 @@ struct kivi_cache {
   int uniform;              // 1: all sequences share `length`; 0: see lens
   int* lens;                // [batch] per-sequence lengths while !uniform
   int splits_override;      // 0 = automatic
+  int overlap;              // kivi_set_attention_overlap
   const void* ws_ready;     // workspace whose counter area is known to be zero
   int device;               // the buffers' device (kNoDevice until the first launching call)
 };
@@ -182,11 +183,12 @@ int max_tail_splits(const kivi_config& c) {
   return (c.residual + 31 + kivi::kTailTok - 1) / kivi::kTailTok;
 }
 
-// Splits per attention unit in one wave of kivi::kAttnCtasPerSm CTAs per SM
-// of a GB300, capped so that the partials merge in at most two levels.
+// Splits per attention unit in one wave of kivi::attn_ctas_per_sm CTAs per
+// SM of a GB300, capped so that the partials merge in at most two levels.
 int split_budget(const kivi_config& c) {
   const long u = attention_units(c);
-  long s = (long)kivi::attn_ctas_per_sm(c.bits) * kivi::kTargetSMs / u;
+  const int nb = kivi::attn_key_blocks(c.n_q_heads / c.n_kv_heads);
+  long s = (long)kivi::attn_ctas_per_sm(c.bits, nb) * kivi::kTargetSMs / u;
   if (s > kivi::kMaxSplits) s = kivi::kMaxSplits;
   return (int)s;
 }
@@ -518,7 +520,14 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
     if (z != KIVI_OK) return z;
     c->ws_ready = workspace;
   }
+  if (c->overlap) a.pdl = kivi::kPdlOverlap;
   return cuda_status(kivi::launch_attention(view(c), a, sl, st));
+}
+
+KIVI_API kivi_status kivi_set_attention_overlap(kivi_cache* c, int enable) {
+  if (!c || (enable != 0 && enable != 1)) return KIVI_EINVAL;
+  c->overlap = enable;
+  return KIVI_OK;
 }
 
 KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const void* v_new,

@@ -10,11 +10,18 @@ namespace kivi {
 constexpr int kHeadDim = 128;  // D supported by the kernels
 constexpr int kGroup = 32;     // G supported by the kernels
 constexpr int kTargetSMs = 152;    // GB300 SM count used by the split policy
-constexpr int kAttnCtasPerSm = 4;  // attention CTAs resident per SM (registers, shared memory)
-// The same per bit width: at 8 bits two staged 9 KB tiles per warp leave
-// room for two CTAs per SM.
-__host__ __device__ constexpr int attn_ctas_per_sm(int bits) { return bits == 8 ? 2 : kAttnCtasPerSm; }
-constexpr int kHeadChunk = 4;      // query heads per attention CTA
+constexpr int kHeadChunk = 8;      // query heads per attention CTA
+// Key blocks of a head chunk: the score product takes four query heads per
+// MMA (each as an fp16 hi / lo pair of columns), so chunks of up to four
+// heads need one block and chunks of five to eight need two.
+__host__ __device__ constexpr int attn_key_blocks(int grp) { return (grp < kHeadChunk ? grp : kHeadChunk) > 4 ? 2 : 1; }
+// Attention CTAs resident per SM (registers, shared memory): four, except
+// that two 9 KB staged tiles per warp at 8 bits leave room for two, and the
+// two key blocks' query tables beside two 5 KB stages per warp at 4 bits for
+// three.
+__host__ __device__ constexpr int attn_ctas_per_sm(int bits, int nb) {
+  return bits == 8 ? 2 : (bits == 4 && nb == 2 ? 3 : 4);
+}
 constexpr int kMergeGroup = 16;    // split partials merged by one CTA (two levels at most)
 constexpr int kTailTok = 64;       // tail tokens per tail split
 constexpr int kMaxSplits = kMergeGroup * kMergeGroup;
@@ -277,11 +284,16 @@ struct AttnArgs {
   // the append's completion (griddepcontrol.wait) before reading the cache.
   // kPdlTail: this step's append writes nothing below t_tail (ring slots, a
   // value row or key group inside the tail), so the packed splits never wait
-  // and only the tail's readers do.  0: an ordinary launch.
+  // and only the tail's readers do.  kPdlOverlap: see below.  0: an
+  // ordinary launch.
   int pdl;
 };
 
-enum : int { kPdlAll = 1, kPdlTail = 2 };
+// kPdlOverlap: launched after other work on the stream that writes neither
+// q nor the cache (for instance another attention call): the CTAs read the
+// cache and q at once and wait for that work only before their first global
+// write (the split partials, the counters, the output).
+enum : int { kPdlAll = 1, kPdlTail = 2, kPdlOverlap = 3 };
 
 // Programmatic dependent launch (sm_90+).  The primary kernel lets its
 // dependent start early; the dependent waits for the primary's completion and

@@ -79,6 +79,7 @@ def lib() -> C.CDLL:
                 "kivi_decode_attention": (i32, [vp, vp, i32, vp, f32, vp, sz, vp]),
                 "kivi_set_attention_splits": (i32, [vp, i32]),
                 "kivi_attention_splits": (i32, [vp, i32]),
+                "kivi_set_attention_overlap": (i32, [vp, i32]),
                 "kivi_cache_length": (i32, [vp]),
                 "kivi_cache_reset": (i32, [vp]),
                 "kivi_cache_destroy": (None, [vp]),
@@ -216,6 +217,10 @@ def kivi_set_attention_splits(h, n_splits: int) -> None:
 
 def kivi_attention_splits(h, l: int) -> int:
     return int(lib().kivi_attention_splits(h, l))
+
+
+def kivi_set_attention_overlap(h, enable: int) -> None:
+    _check(lib().kivi_set_attention_overlap(h, int(enable)), "kivi_set_attention_overlap")
 
 
 def kivi_cache_length(h) -> int:
@@ -382,6 +387,11 @@ class KiviCache:
 
     def set_splits(self, n: int) -> None:
         kivi_set_attention_splits(self.handle, n)
+
+    def set_overlap(self, enable: bool) -> None:
+        """Let attention() calls overlap the kernel before them on the stream
+        (see kivi_set_attention_overlap in kivi.h for when that is safe)."""
+        kivi_set_attention_overlap(self.handle, 1 if enable else 0)
 
     def splits(self, l: int | None = None) -> int:
         return kivi_attention_splits(self.handle, self.length if l is None else l)

@@ -285,14 +285,29 @@ kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
  * always take the tail of the context that is still fp16 (plus the partial
  * value group before it), 64 tokens each; the others share the packed
  * 32-token tiles.  The automatic choice keeps the whole grid within one wave
- * of four CTAs per SM of a 152-SM GB300, with at least eight tiles per packed
- * split and a multiple of four.  An override n asks for n splits in all; it
+ * of a 152-SM GB300 (four CTAs per SM; three at 4 bits with more than four
+ * query heads per KV head, two at 8 bits), with at least eight tiles per
+ * packed split and a multiple of four.  An override n asks for n splits in all; it
  * is clamped to the workspace bound, to one packed split per 32-token tile
  * and to at least one packed split. */
 kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 
 /* Splits the next kivi_decode_attention call will use at length l. */
 int kivi_attention_splits(const kivi_cache *c, int l);
+
+/* Let kivi_decode_attention calls on this handle overlap the kernel enqueued
+ * just before them on the stream (enable = 1; 0, the default, turns it off;
+ * KIVI_EINVAL for other values).  No counterpart on the pages: a launch-order
+ * setting.  The attention is then launched as a programmatic dependent of
+ * that kernel: its CTAs start as the earlier kernel's CTAs finish, read q and
+ * the cache at once, and wait for the earlier kernel to complete only before
+ * their first global write (the split partials, the counters and out).  So
+ * enable it only when the work enqueued before each attention call on the
+ * stream writes neither that call's q nor this cache -- for instance a
+ * sequence of attention calls over caches and queries that were all written
+ * earlier.  kivi_decode_step and kivi_decode_attention_static ignore it.
+ * Host only; no device work. */
+kivi_status kivi_set_attention_overlap(kivi_cache *c, int enable);
 
 /* Tokens held by every sequence; -2 when the sequences' lengths differ (see
  * kivi_cache_lengths), -1 if c is NULL. */

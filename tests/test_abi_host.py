@@ -90,7 +90,7 @@ def test_scale_slot_maps_are_permutations(K):
     (dict(bits=5), 1), (dict(bits=1), 1), (dict(group=16), 1), (dict(head_dim=64), 1),
     (dict(residual=48), 2), (dict(residual=0), 2), (dict(n_q_heads=6), 2),
     (dict(max_tokens=4016, residual=64), 2), (dict(batch=0), 2), (dict(n_kv_heads=0), 2),
-    (dict(n_kv_heads=4096, n_q_heads=4096 * 68), 2),  # attention grid y: 4096 x 17 chunks
+    (dict(n_kv_heads=4096, n_q_heads=4096 * 136), 2),  # attention grid y: 4096 x 17 chunks of 8
 ])
 def test_config_validation(K, bad, status):
     with pytest.raises(K.KiviError) as e:
@@ -176,9 +176,10 @@ def test_split_plan_and_workspace(K):
         assert K.kivi_attention_splits(h, 4097) == 9
         assert K.kivi_attention_splits(h, 100) == 2   # tail + one 64-token split
         assert K.kivi_attention_splits(h, 40) == 1    # everything is tail
-        # 64 groups x (9 split partials + 1 merged group) x 4 heads x (128 + 2)
-        # floats, one counter per split group and per group, the status slot
-        assert K.kivi_attention_workspace_bytes(h) == 64 * (9 + 1) * 4 * (128 + 2) * 4 + 64 * 4 * 2 + 16
+        # 64 groups x (9 split partials + 1 merged group) x 8 heads (a chunk)
+        # x (128 + 2) floats, one counter per split group and per group, the
+        # status slot
+        assert K.kivi_attention_workspace_bytes(h) == 64 * (9 + 1) * 8 * (128 + 2) * 4 + 64 * 4 * 2 + 16
         K.kivi_set_attention_splits(h, 3)
         assert K.kivi_attention_splits(h, 4097) == 3
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
@@ -269,7 +270,7 @@ def test_bounded_wait_probe_refusals(K):
 @pytest.mark.parametrize("batch,n_kv,n_q,R,bits,cap", [
     (1, 1, 4, 32, 2, 4096), (8, 8, 32, 32, 2, 4224), (1, 8, 32, 128, 2, 8192),
     (64, 4, 28, 32, 2, 2592), (200, 8, 32, 64, 4, 1024), (3, 2, 8, 32, 8, 2048),
-    (2, 2, 16, 32, 3, 2048)])
+    (2, 2, 16, 32, 3, 2048), (16, 4, 28, 32, 4, 1024), (8, 1, 18, 32, 2, 1024)])
 def test_split_plan_invariants(K, batch, n_kv, n_q, R, bits, cap):
     """At every length up to the capacity: at least one split and at most
     256; no more than one wave of the grid (attn_ctas_per_sm CTAs on each of
@@ -279,8 +280,11 @@ def test_split_plan_invariants(K, batch, n_kv, n_q, R, bits, cap):
     c = cfg(K, batch=batch, n_kv_heads=n_kv, n_q_heads=n_q, residual=R, bits=bits, max_tokens=cap)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     try:
-        units = batch * n_kv * -(-(n_q // n_kv) // 4)
-        budget = max(min((2 if bits == 8 else 4) * 152 // units, 256), 1)
+        grp = n_q // n_kv
+        units = batch * n_kv * -(-grp // 8)  # chunks of up to 8 query heads
+        two_blocks = min(grp, 8) > 4         # two key blocks of 4 heads
+        per_sm = 2 if bits == 8 else (3 if bits == 4 and two_blocks else 4)
+        budget = max(min(per_sm * 152 // units, 256), 1)
         max_tail = -(-(R + 31) // 64)
         most = 0
         for l in range(1, cap + 1):
@@ -288,6 +292,22 @@ def test_split_plan_invariants(K, batch, n_kv, n_q, R, bits, cap):
             assert 1 <= s <= 256, l
             assert s <= max(budget, max_tail), (l, s, budget)
             most = max(most, s)
-        assert K.kivi_attention_workspace_bytes(h) >= units * most * 4 * (128 + 2) * 4
+        assert K.kivi_attention_workspace_bytes(h) >= units * most * 8 * (128 + 2) * 4
     finally:
         K.kivi_cache_destroy(h)
+
+
+def test_attention_overlap_setting(K):
+    """kivi_set_attention_overlap takes 0 or 1 on a live handle (host only)."""
+    c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=4, max_tokens=64)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    try:
+        K.kivi_set_attention_overlap(h, 1)
+        K.kivi_set_attention_overlap(h, 0)
+        for bad in (2, -1):
+            with pytest.raises(K.KiviError) as e:
+                K.kivi_set_attention_overlap(h, bad)
+            assert e.value.status == K.KIVI_EINVAL
+    finally:
+        K.kivi_cache_destroy(h)
+    assert K.lib().kivi_set_attention_overlap(None, 1) == K.KIVI_EINVAL
