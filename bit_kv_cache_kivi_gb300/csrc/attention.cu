@@ -159,11 +159,14 @@ constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp (3 KB 
 template <int BITS, int NB>
 struct WarpSmem {
   TileBuf<BITS> st[kWarps][kStagesOf<BITS>];  // per-warp rings of staged tiles
-  uint4 qs[NB][2][4][8][4];               // q * base^-e(i) as split_mul operands (xa, xb)
+  // q * base^-e(i) per column: one key block (NB = 1, columns (head, part)):
+  // [0] / [1] the split_mul operands (xa, xb); two key blocks (NB = 2,
+  // columns = heads): [0] / [1] the hi / lo part
+  uint4 qs[2][4][8][4];
   uint4 qb[NB][4][8][4];                  // q hi / lo (words of a quarter in the order 0, 2, 1, 3)
   float qv[kNH][kHeadDim];                // q, staged for the tables
   float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
-  int qexp[kNH];                          // E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
+  float qinv[kNH];                        // 2^-E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
   unsigned long long bar[kWarps][kStagesOf<BITS>];
 };
 
@@ -667,8 +670,11 @@ constexpr float kTwo24 = 16777216.0f;  // undoes the 2^-24 of the subnormal code
 // maximum for any fp16 scale s = range / 3.
 constexpr float kLazyMax = 0.5f;
 // A raised running max is set this far above the tile max (log2 units), so
-// that later tiles rarely raise it again.
-constexpr float kLazySlack = 1.0f;
+// that later tiles rarely raise it again (on the Llama-3-8B decode shape
+// about 4% of the tiles after the first raise it, against 37% with a slack
+// of 1).  The weights then lie in (0, 2^0.5], and right after a raise the
+// largest is 2^-3: fp16 keeps its full relative precision for p * s.
+constexpr float kLazySlack = 3.0f;
 
 // The channel-pair words of a per-channel fp16 vector stored in pair order
 // (key scales or zeros, see kscale_pos) behind q-table block `blk` of this
@@ -706,10 +712,11 @@ __host__ __device__ constexpr int word_pos(int w) {
   return BITS <= 3 ? (w & 7) : (w & 3);
 }
 
-// Q' = q * sK of one key group as MMA B fragments for column g of this lane
-// in every key block (head 4 nb + (g >> 1), part g & 1), in the order of the
-// q tables.  The q table is pre-scaled by base^-e(i) to cancel the power that
-// the code extraction leaves in the A operand.
+// Q' = q * sK of one key group as MMA B fragments for column g of this lane,
+// in the order of the q tables: one key block, head g >> 1, part g & 1 (one
+// fp16 of the pair per lane); two key blocks, head g, both parts (bq[0] hi,
+// bq[1] lo).  The q table is pre-scaled by base^-e(i) to cancel the power
+// that the code extraction leaves in the A operand.
 template <int BITS, int NB>
 __device__ __forceinline__ void build_qprime(const WarpSmem<BITS, NB>& ws, const uint32_t* sk, int g, int tig,
                                              uint32_t (&bq)[NB][8][2]) {
@@ -720,15 +727,20 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS, NB>& ws, const
 #pragma unroll
     for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
       const int quarter = kQuartersPerBlock<BITS> * blk + qq;
+      const uint4 x0 = ws.qs[0][quarter][g][tig];
+      const uint4 x1 = ws.qs[1][quarter][g][tig];
+      const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-      for (int nb = 0; nb < NB; ++nb) {
-        const uint4 x0 = ws.qs[nb][0][quarter][g][tig];
-        const uint4 x1 = ws.qs[nb][1][quarter][g][tig];
-        const uint32_t X0[4] = {x0.x, x0.y, x0.z, x0.w}, X1[4] = {x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-        for (int wq = 0; wq < 4; ++wq) {
-          const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
-          bq[nb][w >> 1][w & 1] = split_mul(X0[wq], X1[wq], P[word_pos<BITS>(w)]);
+      for (int wq = 0; wq < 4; ++wq) {
+        const int w = 4 * quarter + wq;  // table word: k-step w >> 1, half w & 1
+        const uint32_t sp = P[word_pos<BITS>(w)];
+        if constexpr (NB == 1) {
+          bq[0][w >> 1][w & 1] = split_mul(X0[wq], X1[wq], sp);
+        } else {
+          // both parts of head g: hi = fp16(qh s), lo = fp16(ql s + (qh s - hi))
+          const uint32_t hi = hmul2u(X0[wq], sp);
+          bq[0][w >> 1][w & 1] = hi;
+          bq[NB - 1][w >> 1][w & 1] = hfma2u(X1[wq], sp, hfms2u(X0[wq], sp, hi));
         }
       }
     }
@@ -741,10 +753,10 @@ __device__ __forceinline__ void build_qprime(const WarpSmem<BITS, NB>& ws, const
 // B-fragment register of the value product takes.
 __device__ __forceinline__ int score_row(int g) { return (g & 3) + 8 * (g >> 2); }
 
-// Scores of one staged 32-token tile, per key block nb: lane (g, tig) gets
-// head 4 nb + tig at tokens 16 (r >> 1) + score_row(g) + 4 (r & 1) in
-// sc[nb][r] (log2 units), less mb[nb]; ks = 2^E * scale * log2(e) of that
-// head.
+// Scores of one staged 32-token tile: lane (g, tig) gets head hd(nb) at
+// tokens 16 (r >> 1) + score_row(g) + 4 (r & 1) in sc[nb][r] (log2 units),
+// less mb[nb], where hd(nb) = tig with one key block and 2 tig + nb with two;
+// ks = 2^E * scale * log2(e) of that head.
 template <int BITS, int NB>
 __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
                                            const float (&ks)[NB], const float (&mb)[NB], int n_out,
@@ -780,7 +792,13 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const T
       }
     }
 #pragma unroll
-    for (int nb = 0; nb < NB; ++nb) kbm[nb] = fmaf((ba[nb][0] + ba[nb][1]) + (bb[nb][2] + bb[nb][3]), ks[nb], -mb[nb]);
+    for (int nb = 0; nb < NB; ++nb) {
+      // one key block: head tig's beta is its (hi, lo) columns; two key
+      // blocks: head 2 tig + nb's beta is column nb of both parts
+      const float beta = NB == 1 ? (ba[0][0] + ba[0][1]) + (bb[0][2] + bb[0][3])
+                                 : (ba[0][nb] + ba[NB - 1][nb]) + (bb[0][2 + nb] + bb[NB - 1][2 + nb]);
+      kbm[nb] = fmaf(beta, ks[nb], -mb[nb]);
+    }
   }
 
   // ---- scores S = codes x Q' + beta ----
@@ -873,8 +891,10 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const T
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
       const float k24 = ks[nb] * kTwo24;
-      sc[nb][2 * mt] = fmaf(acc[nb][0] + acc[nb][1], k24, kbm[nb]);      // token r0
-      sc[nb][2 * mt + 1] = fmaf(acc[nb][2] + acc[nb][3], k24, kbm[nb]);  // token r0 + 4
+      const float s0 = NB == 1 ? acc[0][0] + acc[0][1] : acc[0][nb] + acc[NB - 1][nb];
+      const float s1 = NB == 1 ? acc[0][2] + acc[0][3] : acc[0][2 + nb] + acc[NB - 1][2 + nb];
+      sc[nb][2 * mt] = fmaf(s0, k24, kbm[nb]);      // token r0
+      sc[nb][2 * mt + 1] = fmaf(s1, k24, kbm[nb]);  // token r0 + 4
     }
   }
   if (n_out > 0) {
@@ -887,7 +907,7 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const T
         const int ch = (iw >> (8 * o)) & 0xffu;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const float qo = ws.qv[4 * nb + tig][ch] * scale_log2;
+          const float qo = ws.qv[NB == 1 ? tig : 2 * tig + nb][ch] * scale_log2;
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int t = 16 * (r >> 1) + tr + 4 * (r & 1);
@@ -898,8 +918,8 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const T
   }
 }
 
-// Online softmax over one tile's scores (lane (g, tig) holds head 4 nb + tig
-// at four tokens; 8 lanes share a head): when a score exceeds a head's
+// Online softmax over one tile's scores (lane (g, tig) holds head hd(nb) of
+// key_scores at four tokens; 8 lanes share a head): when a score exceeds a head's
 // running max by more than kLazyMax, the max is raised to the tile max plus
 // kLazySlack and what the earlier tiles left in O and Z is rescaled.  The
 // weights p = 2^(S - max) <= 2^kLazyMax are rounded to fp16 pairs and moved
@@ -935,17 +955,16 @@ __device__ __forceinline__ void softmax_p(float (&x)[NB][4], int g, int tig, flo
 #pragma unroll
       for (int r = 0; r < 4; ++r) x[nb][r] += dm;
     }
-    // the O and Z columns of this lane are heads 2 tig and 2 tig + 1, whose
-    // softmax state sits in lane (2 tig) & 3 / (2 tig + 1) & 3 of block tig >> 1
-    float cA = __shfl_sync(kFull, corr[0], (2 * tig) & 3);
-    float cB = __shfl_sync(kFull, corr[0], (2 * tig + 1) & 3);
+    // the O and Z columns of this lane are heads 2 tig and 2 tig + 1: with
+    // two key blocks its own heads; with one, heads held by lanes (2 tig) & 3
+    // and (2 tig + 1) & 3 (the columns of heads 4..7 are unused)
+    float cA, cB;
     if constexpr (NB == 2) {
-      const float cA1 = __shfl_sync(kFull, corr[1], (2 * tig) & 3);
-      const float cB1 = __shfl_sync(kFull, corr[1], (2 * tig + 1) & 3);
-      if (tig >= 2) {
-        cA = cA1;
-        cB = cB1;
-      }
+      cA = corr[0];
+      cB = corr[NB - 1];
+    } else {
+      cA = __shfl_sync(kFull, corr[0], (2 * tig) & 3);
+      cB = __shfl_sync(kFull, corr[0], (2 * tig + 1) & 3);
     }
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -966,16 +985,17 @@ __device__ __forceinline__ void softmax_p(float (&x)[NB][4], int g, int tig, flo
     for (int mt = 0; mt < 2; ++mt)
       P2[nb][mt] = f2_to_h2(fast_exp2(x[nb][2 * mt]), fast_exp2(x[nb][2 * mt + 1]));
   // token 16 kk + 8 aa + tig is row score_row^-1(8 aa + tig) = tig + 4 aa of
-  // m-tile kk; head g is lane (.., g & 3) of block g >> 2
+  // m-tile kk; head g is held by lane (.., g & 3) (one key block, block 0)
+  // or lane (.., g >> 1), block g & 1 (two key blocks)
 #pragma unroll
   for (int kk = 0; kk < 2; ++kk)
 #pragma unroll
     for (int aa = 0; aa < 2; ++aa) {
-      const int src = 4 * (tig + 4 * aa) + (g & 3);
+      const int src = 4 * (tig + 4 * aa) + (NB == 2 ? g >> 1 : g & 3);
       const uint32_t v0 = __shfl_sync(kFull, P2[0][kk], src);
       if constexpr (NB == 2) {
         const uint32_t v1 = __shfl_sync(kFull, P2[NB - 1][kk], src);
-        pb[kk][aa] = g >= 4 ? v1 : v0;
+        pb[kk][aa] = (g & 1) ? v1 : v0;
       } else {
         pb[kk][aa] = v0;  // columns 4..7 repeat heads 0..3 and are not used
       }
@@ -1138,17 +1158,18 @@ __device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const f
       // amax in [2^(be-127), 2^(be-126)) for normal amax; a subnormal amax is
       // below 2^-126, a zero row keeps E = 0
       const int E = amax == 0.0f ? 0 : (be == 0 ? -126 : be - 126);
-      s.qexp[j] = E;
+      s.qinv[j] = ldexpf(1.0f, -E);  // exact: a power of two (subnormal for E > 126)
       s.qscale[j] = ldexpf(a.scale_log2, E);
     }
   }
   __syncthreads();
+  // one key block: heads 0..3, each in columns (2 hh, 2 hh + 1) as (hi, lo);
+  // two key blocks: heads 0..7 in columns 0..7, one table per part
   for (int idx = threadIdx.x; idx < NB * 4 * 4 * 16; idx += blockDim.x) {
     const int word = idx & 15;                // ks * 2 + r
     const int tig = (idx >> 4) & 3;
-    const int hh = (idx >> 6) & 3;            // head within the key block
-    const int nb = idx >> 8;
-    const int j = 4 * nb + hh;
+    const int j = idx >> 6;                   // the head
+    const int hh = j & 3;
     const int ks = word >> 1, r = word & 1;
     int c0, c1, i;  // the channel pair of the word and its code position
     if constexpr (BITS == 2 || BITS == 3) {
@@ -1168,21 +1189,28 @@ __device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const f
       c1 = c0 + 2;
     }
     const float f = code_scale<BITS>(i);
-    const float q0 = ldexpf(s.qv[j][c0], -s.qexp[j]), q1 = ldexpf(s.qv[j][c1], -s.qexp[j]);
+    const float q0 = s.qv[j][c0] * s.qinv[j], q1 = s.qv[j][c1] * s.qinv[j];  // exact scalings
     const uint32_t qh = f2_to_h2(q0, q1);
     const uint32_t ql = f2_to_h2(q0 - h_lo(qh), q1 - h_hi(qh));
     const uint32_t sh = f2_to_h2(q0 * f, q1 * f);
     const uint32_t sl = f2_to_h2(q0 * f - h_lo(sh), q1 * f - h_hi(sh));
     const int quarter = word >> 2, wq = word & 3;
-    // hi lane: (xa, xb) = (hi, 0); lo lane: (lo, hi)
-    reinterpret_cast<uint32_t*>(&s.qs[nb][0][quarter][2 * hh][tig])[wq] = sh;
-    reinterpret_cast<uint32_t*>(&s.qs[nb][1][quarter][2 * hh][tig])[wq] = 0u;
-    reinterpret_cast<uint32_t*>(&s.qs[nb][0][quarter][2 * hh + 1][tig])[wq] = sl;
-    reinterpret_cast<uint32_t*>(&s.qs[nb][1][quarter][2 * hh + 1][tig])[wq] = sh;
     // the beta MMAs take words (0, 2) and (1, 3) of a quarter as B pairs
     const int wb = wq == 1 ? 2 : (wq == 2 ? 1 : wq);
-    reinterpret_cast<uint32_t*>(&s.qb[nb][quarter][2 * hh][tig])[wb] = qh;
-    reinterpret_cast<uint32_t*>(&s.qb[nb][quarter][2 * hh + 1][tig])[wb] = ql;
+    if constexpr (NB == 1) {
+      // hi lane: (xa, xb) = (hi, 0); lo lane: (lo, hi)
+      reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh][tig])[wq] = sh;
+      reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh][tig])[wq] = 0u;
+      reinterpret_cast<uint32_t*>(&s.qs[0][quarter][2 * hh + 1][tig])[wq] = sl;
+      reinterpret_cast<uint32_t*>(&s.qs[1][quarter][2 * hh + 1][tig])[wq] = sh;
+      reinterpret_cast<uint32_t*>(&s.qb[0][quarter][2 * hh][tig])[wb] = qh;
+      reinterpret_cast<uint32_t*>(&s.qb[0][quarter][2 * hh + 1][tig])[wb] = ql;
+    } else {
+      reinterpret_cast<uint32_t*>(&s.qs[0][quarter][j][tig])[wq] = sh;
+      reinterpret_cast<uint32_t*>(&s.qs[1][quarter][j][tig])[wq] = sl;
+      reinterpret_cast<uint32_t*>(&s.qb[0][quarter][j][tig])[wb] = qh;
+      reinterpret_cast<uint32_t*>(&s.qb[NB - 1][quarter][j][tig])[wb] = ql;
+    }
   }
 }
 
@@ -1221,12 +1249,20 @@ __device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long
   bulk_g2s(&tb, u.tiles + (long)tile * u.tile_bytes, u.tile_bytes, bar);
 }
 
-// The same from a source address.
+// The same from a source address, issued by the lanes where `p` holds (one
+// lane) with predicated instructions, so that the warp does not diverge;
+// the proxy fence orders the warp's earlier reads of the stage before the
+// copy's writes.
 template <int BITS>
-__device__ __forceinline__ void issue_tile_at(TileBuf<BITS>& tb, unsigned long long* bar, const uint8_t* src,
-                                              uint32_t bytes) {
-  mbar_expect_tx(bar, bytes);
-  bulk_g2s(&tb, src, bytes, bar);
+__device__ __forceinline__ void issue_tile_if(bool p, TileBuf<BITS>& tb, unsigned long long* bar,
+                                              const uint8_t* src, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t"
+      "@p fence.proxy.async.shared::cta;\n\t"
+      "@p mbarrier.arrive.expect_tx.shared::cta.b64 _, [%3], %4;\n\t"
+      "@p cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%1], [%2], %4, [%3];\n\t}"
+      ::"r"((int)p), "r"(smem_u32(&tb)), "l"(src), "r"(smem_u32(bar)), "r"(bytes)
+      : "memory");
 }
 
 // Packed tiles [tile0, tile1) of one (batch, kv-head, head chunk) on the
@@ -1272,7 +1308,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   float ks[NB], m_run[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
-    ks[nb] = ws.qscale[4 * nb + tig];
+    ks[nb] = ws.qscale[NB == 1 ? tig : 2 * tig + nb];
     m_run[nb] = -INFINITY;
   }
 
@@ -1313,25 +1349,22 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   while (!failed && k + 1 < n_mine) {
     const int sn = sk + 1 == kStages ? 0 : sk + 1;  // stage of tile k + 1
     if (sn == 0) parn ^= 1u;
-    bool ok = mbar_try_wait(&bars[sn], parn);
-    if (!ok) ok = mbar_wait(&bars[sn], parn);
-    if (__any_sync(kFull, !ok)) {
-      failed = true;
-      break;
+    if (!__all_sync(kFull, mbar_try_wait(&bars[sn], parn))) {
+      const bool ok = mbar_wait(&bars[sn], parn);
+      if (__any_sync(kFull, !ok)) {
+        failed = true;
+        break;
+      }
     }
     float sc[NB][4];
     key_scores<BITS, NB>(ws, st[sn], g, tig, ks, m_run, cv.n_out, a.scale_log2, sc);
     value_acc<BITS>(st[sk], pb, g, tig, O, Z);
     done = k + 1;
     __syncwarp();  // every lane is done with stage sk
-    if (k + kStages < n_mine) {
-      if (lane == 0) {
-        fence_proxy_async();
-        issue_tile_at<BITS>(st[sk], &bars[sk], next_src, us.tile_bytes);
-      }
-      next_src += src_step;
-      ++issued;
-    }
+    const bool more = k + kStages < n_mine;
+    issue_tile_if<BITS>(more && lane == 0, st[sk], &bars[sk], next_src, us.tile_bytes);
+    next_src += src_step;
+    issued += more;
     softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
     ++k;
     sk = sn;
@@ -1355,10 +1388,13 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   // ---- this warp's partial: max, sum and output per head ----
   // The value columns of lane (g, tig) are heads 2 tig and 2 tig + 1: their
   // weight sums are Z[2], Z[3] (the all-ones rows); the running max of head
-  // 4 nb + tig is m_run[nb] of the lanes with this tig.
+  // hd(nb) of key_scores is m_run[nb] of the lanes with this tig.
   if (g == 0) {
 #pragma unroll
-    for (int nb = 0; nb < 2; ++nb) s_m[warp][4 * nb + tig] = nb < NB && n_mine > 0 ? m_run[nb < NB ? nb : 0] : -INFINITY;
+    for (int i = 0; i < 2; ++i) {
+      if constexpr (NB == 2) s_m[warp][2 * tig + i] = n_mine > 0 ? m_run[i] : -INFINITY;
+      else s_m[warp][4 * i + tig] = i == 0 && n_mine > 0 ? m_run[0] : -INFINITY;
+    }
     s_l[warp][2 * tig] = Z[2];
     s_l[warp][2 * tig + 1] = Z[3];
   }
@@ -1508,7 +1544,8 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   grid_launch_dependents();
   const int s = blockIdx.x;
   const int nhc = gridDim.y / cv.H;
-  const int h = blockIdx.y / nhc, hc = blockIdx.y % nhc;
+  const int h = nhc == 1 ? (int)blockIdx.y : (int)blockIdx.y / nhc;
+  const int hc = nhc == 1 ? 0 : (int)blockIdx.y % nhc;
   const int b = blockIdx.z;
   const int grp = a.Hq / cv.H;
   const int j0 = h * grp + hc * kNH;

@@ -627,10 +627,9 @@ KIVI_API kivi_status kivi_check_bounded_wait(int* status, void* stream) {
 // Decode attention without a caller-provided workspace.
 //
 // Some callers cannot allocate device memory at the point where they run
-// attention: a step being recorded into a CUDA graph (an allocation there
-// would break or serialize the capture), a plugin inside a host framework
-// whose memory is handed out only by that framework's own pool, or a latency
-// path that must not pay cudaMalloc's implicit synchronization.  For them the
+// attention: a plugin inside a host framework whose device memory is handed
+// out only by that framework's own pool, or a latency-critical path that must
+// not pay cudaMalloc's implicit device-wide synchronization.  For them the
 // library keeps one fixed scratch area in device global memory, declared
 // below, and kivi_decode_attention_static uses it instead of a workspace
 // argument.  Every GPU that loads this library holds the area until the
@@ -673,6 +672,14 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   if (c->uniform && c->length <= 0) return KIVI_ESTATE;
   const WsLayout w = ws_layout(c->cfg);
   if (w.total > (size_t)KIVI_STATIC_WORKSPACE_BYTES) return KIVI_EWORKSPACE;
+  // every check first, so that a refused call does no CUDA work (the area's
+  // address lookup may load the module on the current device)
+  int dev = 0;
+  const kivi_status ds = launch_device(c, &dev);
+  if (ds != KIVI_OK) return ds;
+  if (!device_accessible(q, dev) || !device_accessible(out, dev)) return KIVI_EINVAL;
+  for (int b = 0; b < (c->uniform ? 1 : c->cfg.batch); ++b)
+    if (len_of(c, b) <= 0) return KIVI_ESTATE;
   void* ws = nullptr;
   kivi_status st = cuda_status(static_ws_address(&ws));
   if (st != KIVI_OK) return st;
@@ -680,10 +687,6 @@ KIVI_API kivi_status kivi_decode_attention_static(kivi_cache* c, const void* q,
   kivi::SeqLens sl;
   st = attn_args(c, q, q_dtype, out, softmax_scale, static_cast<char*>(ws), &a, &sl);
   if (st != KIVI_OK) return st;
-  int dev = 0;
-  const kivi_status ds = launch_device(c, &dev);
-  if (ds != KIVI_OK) return ds;
-  if (!device_accessible(q, dev) || !device_accessible(out, dev)) return KIVI_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The area keeps whatever the previous call left; the split counters must
   // start at zero, so clear them on every call (a memset, not an allocation).

@@ -458,7 +458,8 @@ class KiviCache:
 
     def logical_state(self) -> dict:
         """The arrays in token-major shapes and channel order (device
-        copies): codes_k / codes_v [B][H][T][RB], scale_k / zero_k
+        copies): codes_k / codes_v [B][H][T][RB] as plain rows (channel e at
+        bits [e*bits, e*bits + bits), LSB first), scale_k / zero_k
         [B][H][T/G][D], scale_v / zero_v [B][H][T][D/G], ring_k / ring_v
         [B][H][W][D]."""
         c = self.cfg
@@ -475,7 +476,7 @@ class KiviCache:
                                          for ch in range(8) for i in range(16)] for r in range(G)],
                                        device=dev)
                     t = torch.gather(t, 4, idx.expand(B, H, t.shape[2], G, 128))
-                out[n] = t.reshape(B, H, T, t.shape[-1])
+                out[n] = plain_rows(t.reshape(B, H, T, t.shape[-1]), c.bits, n == "codes_v")
             elif n in ("scale_k", "zero_k"):
                 out[n] = t.index_select(3, kidx)
             elif n in ("scale_v", "zero_v"):
@@ -485,6 +486,63 @@ class KiviCache:
             else:
                 out[n] = t.clone()
         return out
+
+
+def _hi_bit3(s: int, i: int) -> int:
+    """Bit of (set s, index i) inside a 16-bit unit of a 3-bit row's high plane."""
+    p = 2 * (i % 4) + 2 + (1 if i >= 4 else 0)
+    return (p + 8) % 16 if s else p
+
+
+def tile_row_bit(e: int, j: int, bits: int, value: bool, D: int = 128, G: int = 32) -> int:
+    """Bit (from the row start) holding bit j of channel e's code in a code
+    row of a tile (after undoing the 8-bit chunk rotation).  Key rows at 2, 4
+    and 8 bits are plain (channel e at bits e*bits + j).  Value rows keep the
+    same order inside units of 4 channels and interleave the units by group:
+    the unit of channels G*gp + 4w .. +3 sits at unit position 4w + gp.  A
+    3-bit row is two planes: the low two bits as a 2-bit row of the same
+    kind, then the high bits in 16-bit units (keys: unit 2(m mod 4) + h
+    holds channels 16m + 8h + i, set m // 4; values: unit w holds channels
+    32gp + 4w + c, set gp // 2, index 4(gp mod 2) + c)."""
+    lbits = 2 if bits == 3 else bits
+    if bits == 3 and j == 2:
+        if value:
+            gp, w, c = e // 32, (e % 32) // 4, e % 4
+            return D * 2 + 16 * w + _hi_bit3(gp // 2, 4 * (gp % 2) + c)
+        m, h, i = e // 16, (e % 16) // 8, e % 8
+        return D * 2 + 16 * (2 * (m % 4) + h) + _hi_bit3(m // 4, i)
+    if not value:
+        return e * lbits + j
+    u, c = e // 4, e % 4
+    pos = 4 * (u % (G // 4)) + u // (G // 4)
+    return pos * 4 * lbits + c * lbits + j
+
+
+_PLAIN_MAPS: dict = {}
+
+
+def plain_rows(rows: torch.Tensor, bits: int, value: bool) -> torch.Tensor:
+    """Code rows of a tile ([..., D*bits/8] u8) as plain rows: channel e at
+    bits [e*bits, e*bits + bits), LSB first (a fresh tensor)."""
+    RB = rows.shape[-1]
+    D = RB * 8 // bits
+    if bits != 3 and not value:
+        return rows.clone()
+    key = (bits, value, D, rows.device)
+    if key not in _PLAIN_MAPS:
+        src = [tile_row_bit(e, j, bits, value, D) for e in range(D) for j in range(bits)]
+        _PLAIN_MAPS[key] = torch.tensor(src, dtype=torch.long, device=rows.device)
+    src = _PLAIN_MAPS[key]
+    shifts = torch.arange(8, dtype=torch.uint8, device=rows.device)
+    flat = rows.reshape(-1, RB)
+    out = torch.empty_like(flat)
+    step = max(1, (64 << 20) // (RB * 8))  # rows per chunk: about 64 MB of bits
+    for i in range(0, flat.shape[0], step):
+        blk = flat[i:i + step]
+        b = ((blk.unsqueeze(-1) >> shifts) & 1).reshape(blk.shape[0], RB * 8)
+        p = b.index_select(1, src).reshape(blk.shape[0], RB, 8)
+        out[i:i + step] = (p << shifts).sum(dim=-1, dtype=torch.uint8)
+    return out.reshape(rows.shape)
 
 
 def key_scale_pos(c: int, bits: int) -> int:

@@ -339,12 +339,13 @@ kivi_status kivi_check_bounded_wait(int *status, void *stream);
 #define KIVI_STATIC_WORKSPACE_BYTES (8u << 20)
 
 /* Decode attention for callers that cannot allocate device memory where they
- * run it -- for example while recording a CUDA graph, inside a plugin whose
- * memory must come from its host framework's pool, or on a path that cannot
- * afford cudaMalloc's synchronization.  No counterpart on the pages: it is
- * kivi_decode_attention with the split-K scratch taken from the library's
- * own fixed device area (KIVI_STATIC_WORKSPACE_BYTES) instead of a caller
- * workspace.  Same q/out/scale contract and results as kivi_decode_attention.
+ * run it -- for example a plugin whose device memory must come from its host
+ * framework's own pool, or a latency-critical path that cannot afford
+ * cudaMalloc's implicit device-wide synchronization.  No counterpart on the
+ * pages: it is kivi_decode_attention with the split-K scratch taken from the
+ * library's own fixed device area (KIVI_STATIC_WORKSPACE_BYTES) instead of a
+ * caller workspace.  Same q/out/scale contract and results as
+ * kivi_decode_attention (bit for bit).
  * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  * - Needs kivi_attention_workspace_bytes(c) <= KIVI_STATIC_WORKSPACE_BYTES,
  *   else KIVI_EWORKSPACE and nothing is launched.
@@ -355,7 +356,12 @@ kivi_status kivi_check_bounded_wait(int *status, void *stream);
  * - All calls share the one area and it keeps the last call's contents:
  *   calls that may overlap on the GPU (different streams, or different
  *   handles without ordering between them) race on it and must not be
- *   issued; serialize them on one stream. */
+ *   issued; serialize them on one stream.
+ * - A staged-data wait that gives up (which only a device fault can cause)
+ *   is recorded in the area's own status word, which no call reads back:
+ *   use kivi_decode_attention with a workspace to observe it.
+ * - Every argument check (device, pointers, lengths, size) is made before
+ *   any CUDA call; a refused call does no device work. */
 kivi_status kivi_decode_attention_static(kivi_cache *c, const void *q,
                                          kivi_dtype q_dtype, void *out,
                                          float softmax_scale, void *stream);

@@ -158,135 +158,30 @@ float orc_dequant(int q, uint16_t scale16, uint16_t zero16) {
   return p + orc_f16_to_f32(zero16);
 }
 
+/* Packing ([SURVEY] layout, the plain reading of "codes packed to uint8"):
+ * channel e of a row occupies bits [e*bits, e*bits + bits) of the row, LSB
+ * first -- byte e*bits/8 at bit offset (e*bits) mod 8, a 3-bit code crossing
+ * into the next byte when its offset is 6 or 7.  Keys and values, every
+ * width, use this one layout. */
 void orc_pack_row(const uint8_t *codes, int D, int bits, uint8_t *out) {
   if (D <= 0 || bits <= 0) return; /* an empty row packs to nothing */
-  memset(out, 0, (size_t)D * (size_t)bits / 8u);
+  memset(out, 0, ((size_t)D * (size_t)bits + 7u) / 8u);
   for (int e = 0; e < D; e++)
-    out[(e * bits) / 8] |= (uint8_t)(codes[e] << ((e * bits) % 8));
+    for (int j = 0; j < bits; j++) {
+      const int bit = e * bits + j;
+      out[bit / 8] |= (uint8_t)(((codes[e] >> j) & 1) << (bit % 8));
+    }
 }
 
 void orc_unpack_row(const uint8_t *in, int D, int bits, uint8_t *codes) {
-  const int mask = (1 << bits) - 1;
-  for (int e = 0; e < D; e++)
-    codes[e] = (uint8_t)((in[(e * bits) / 8] >> ((e * bits) % 8)) & mask);
-}
-
-/* Value rows are stored group-interleaved: the row is split into units of 4
- * consecutive channels (bits/2 bytes each); unit w of channel group gp
- * (channels G*gp + 4*w .. +3) is stored at unit position w*(D/G) + gp.
- * With D = 128 and G = 32 one 32-bit word at 2 bits (two at 4 bits) holds
- * the same 4-channel slice of all four groups.  Within a unit the layout is
- * LSB-first like a key row.  The permutation is a storage choice only. */
-int orc_v_unit_pos(int unit, int D, int G) {
-  const int per_group = G / 4; /* units of 4 channels in a group */
-  int gp = unit / per_group, w = unit % per_group;
-  return w * (D / G) + gp;
-}
-
-void orc_pack_row_v(const uint8_t *codes, int D, int bits, int G, uint8_t *out) {
-  uint8_t tmp[4096];
-  orc_pack_row(codes, D, bits, tmp);
-  const int ub = bits / 2; /* bytes per unit of 4 channels */
-  for (int u = 0; u < D / 4; u++)
-    memcpy(out + orc_v_unit_pos(u, D, G) * ub, tmp + u * ub, (size_t)ub);
-}
-
-void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes) {
-  uint8_t tmp[4096];
-  const int ub = bits / 2;
-  for (int u = 0; u < D / 4; u++)
-    memcpy(tmp + u * ub, in + orc_v_unit_pos(u, D, G) * ub, (size_t)ub);
-  orc_unpack_row(tmp, D, bits, codes);
-}
-
-/* 3-bit rows.  A 3-bit code does not sit in whole bytes or nibbles, and the
- * pages print no 3-bit packing (the notebook's bit-width sweep quantizes in
- * fp32 only), so the storage is this implementation's choice: two planes per row.
- *  - Bytes [0, D/4): the low two bits of every code, laid out exactly as a
- *    2-bit row (keys LSB-first, values group-interleaved).
- *  - Bytes [D/4, 3D/8): the high bit of every code, in 16-bit units (D =
- *    128: eight units).  Keys: unit 2W + h (W = 0..3, h = 0..1) holds
- *    channels 16m + 8h + i for m in {W, W + 4} and i = 0..7, with set
- *    s = [m >= 4].  Values: unit w (w = 0..7) holds channels 32 gp + 4w + c
- *    for groups gp = 0..3 and c = 0..3, with set s = gp / 2 and index
- *    i = 4 (gp mod 2) + c.
- *  - Inside a unit, (set s, index i) is at bit orc_hi_bit(s, i) =
- *    2 (i mod 4) + 2 + [i >= 4], plus 8 modulo 16 when s = 1.  The 16 bits
- *    of a unit are a permutation of its 16 (s, i) pairs.                 */
-int orc_hi_bit(int s, int i) {
-  int p = 2 * (i % 4) + 2 + (i >= 4 ? 1 : 0);
-  return s ? (p + 8) % 16 : p;
-}
-
-/* bit index (from the start of the high plane) of key channel e, D = 128 */
-static int hi_bit_key(int e) {
-  int m = e / 16, h = (e % 16) / 8, i = e % 8;
-  int W = m % 4, s = m / 4;
-  return 16 * (2 * W + h) + orc_hi_bit(s, i);
-}
-
-/* bit index (from the start of the high plane) of value channel e, G = 32 */
-static int hi_bit_value(int e) {
-  int gp = e / 32, w = (e % 32) / 4, c = e % 4;
-  return 16 * w + orc_hi_bit(gp / 2, 4 * (gp % 2) + c);
-}
-
-/* rows of 1..4096 channels (the caches use D = 128); others pack nothing */
-static void pack_row3(const uint8_t *codes, int D, int G, int value, uint8_t *out) {
-  uint8_t lo[4096];
-  if (D <= 0 || D > 4096) return;
-  for (int e = 0; e < D; e++) lo[e] = codes[e] & 3;
-  if (value)
-    orc_pack_row_v(lo, D, 2, G, out);
-  else
-    orc_pack_row(lo, D, 2, out);
-  uint8_t *hi = out + D / 4;
-  memset(hi, 0, (size_t)D / 8u);
   for (int e = 0; e < D; e++) {
-    int bit = value ? hi_bit_value(e) : hi_bit_key(e);
-    hi[bit / 8] |= (uint8_t)(((codes[e] >> 2) & 1) << (bit % 8));
+    int c = 0;
+    for (int j = 0; j < bits; j++) {
+      const int bit = e * bits + j;
+      c |= ((in[bit / 8] >> (bit % 8)) & 1) << j;
+    }
+    codes[e] = (uint8_t)c;
   }
-}
-
-static void unpack_row3(const uint8_t *in, int D, int G, int value, uint8_t *codes) {
-  if (value)
-    orc_unpack_row_v(in, D, 2, G, codes);
-  else
-    orc_unpack_row(in, D, 2, codes);
-  const uint8_t *hi = in + D / 4;
-  for (int e = 0; e < D; e++) {
-    int bit = value ? hi_bit_value(e) : hi_bit_key(e);
-    codes[e] = (uint8_t)(codes[e] | (((hi[bit / 8] >> (bit % 8)) & 1) << 2));
-  }
-}
-
-/* A key or value row of the cache at any supported width. */
-void orc_pack_key_row(const uint8_t *codes, int D, int bits, uint8_t *out) {
-  if (bits == 3)
-    pack_row3(codes, D, 32, 0, out);
-  else
-    orc_pack_row(codes, D, bits, out);
-}
-
-void orc_unpack_key_row(const uint8_t *in, int D, int bits, uint8_t *codes) {
-  if (bits == 3)
-    unpack_row3(in, D, 32, 0, codes);
-  else
-    orc_unpack_row(in, D, bits, codes);
-}
-
-void orc_pack_value_row(const uint8_t *codes, int D, int bits, int G, uint8_t *out) {
-  if (bits == 3)
-    pack_row3(codes, D, G, 1, out);
-  else
-    orc_pack_row_v(codes, D, bits, G, out);
-}
-
-void orc_unpack_value_row(const uint8_t *in, int D, int bits, int G, uint8_t *codes) {
-  if (bits == 3)
-    unpack_row3(in, D, G, 1, codes);
-  else
-    orc_unpack_row_v(in, D, bits, G, codes);
 }
 
 /* ------------------------------------------------------------------ */
@@ -342,7 +237,6 @@ orc_cache *orc_cache_new(int bits, int G, int R, int D, int B, int Hkv,
   if ((bits != 2 && bits != 3 && bits != 4 && bits != 8) || G <= 0 || R <= 0 ||
       D <= 0 || B <= 0 || Hkv <= 0 || Tcap <= 0)
     return NULL;
-  if (bits == 3 && (D != 128 || G != 32)) return NULL; /* the 3-bit planes */
   if (D % G || R % G || Tcap % G || G % 4 || (D * bits) % 8) return NULL;
   orc_cache *c = (orc_cache *)calloc(1, sizeof *c);
   if (!c) return NULL;
@@ -459,8 +353,7 @@ static void quantize_k_group(orc_cache *c, int b, int h, long t0) {
     free(chosen);
   }
   for (int i = 0; i < G; i++)
-    orc_pack_key_row(codes + (size_t)i * D, D, c->bits,
-                     c->codes_k + (u * c->Tcap + t0 + i) * c->rowbytes);
+    orc_pack_row(codes + (size_t)i * D, D, c->bits, c->codes_k + (u * c->Tcap + t0 + i) * c->rowbytes);
   free(codes);
 }
 
@@ -476,8 +369,7 @@ static void quantize_v_token(orc_cache *c, int b, int h, long t) {
                        &c->sv[(u * c->Tcap + t) * (D / G) + gg],
                        &c->zv[(u * c->Tcap + t) * (D / G) + gg], NULL);
   }
-  orc_pack_value_row(codes, D, c->bits, G,
-                     c->codes_v + (u * c->Tcap + t) * c->rowbytes);
+  orc_pack_row(codes, D, c->bits, c->codes_v + (u * c->Tcap + t) * c->rowbytes);
 }
 
 /* Bring the quantized parts up to the policy's counts for length l.
@@ -603,8 +495,7 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
   uint8_t codes[4096];
   for (long t = 0; t < c->l; t++) {
     if (t < c->nqk) {
-      orc_unpack_key_row(c->codes_k + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
-                         codes);
+      orc_unpack_row(c->codes_k + (u * c->Tcap + t) * c->rowbytes, D, c->bits, codes);
       long g = t / G;
       for (int d = 0; d < D; d++)
         khat[t * D + d] =
@@ -618,8 +509,7 @@ void orc_cache_dequant(const orc_cache *c, int b, int h, float *khat,
         khat[t * D + d] = orc_f16_to_f32(c->x16_k[(u * c->Tcap + t) * D + d]);
     }
     if (t < c->nqv) {
-      orc_unpack_value_row(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits,
-                           G, codes);
+      orc_unpack_row(c->codes_v + (u * c->Tcap + t) * c->rowbytes, D, c->bits, codes);
       for (int d = 0; d < D; d++)
         vhat[t * D + d] =
             orc_dequant(codes[d], c->sv[(u * c->Tcap + t) * (D / G) + d / G],

@@ -12,17 +12,16 @@
  * -ffp-contract=off so that no multiply-add is fused.  A double-precision
  * brute-force attention is provided for tiny inputs.
  *
- * Storage layout produced by the oracle (identical in meaning to the one the
- * CUDA library documents, written here from that specification alone):
+ * Storage layout of the oracle's cache (the plain reading; the pages fix no
+ * packing):
  *   codes_k [B][Hkv][Tcap][D*bits/8]   token-major packed rows
  *   scale_k, zero_k [B][Hkv][Tcap/G][D] fp16 bit patterns
  *   codes_v [B][Hkv][Tcap][D*bits/8]
  *   scale_v, zero_v [B][Hkv][Tcap][D/G] fp16 bit patterns
  *   ring_k, ring_v  [B][Hkv][R][D]      fp16, token t in slot t mod R
- * Channel e of a packed key row sits in byte (e*bits)/8 at bit (e*bits)%8.
- * Value rows use the same bit order within units of 4 channels, with the
- * units group-interleaved: the unit holding channels G*gp + 4*w .. +3 is
- * stored at unit position w * (D/G) + gp (see orc_pack_row_v).
+ * Channel e of a packed row (keys and values, every width) occupies bits
+ * [e*bits, e*bits + bits), LSB first: byte (e*bits)/8 at bit (e*bits)%8, a
+ * 3-bit code crossing into the next byte when that offset is 6 or 7.
  */
 #ifndef KIVI_ORACLE_H
 #define KIVI_ORACLE_H
@@ -59,25 +58,10 @@ void orc_quantize_group(const uint16_t *x, long n, long stride, int bits,
 /* Dequantize one code: fl(fl(q*s) + z), no fused multiply-add. */
 float orc_dequant(int q, uint16_t scale16, uint16_t zero16);
 
-/* Pack / unpack a row of D codes (LSB-first, channel e at bit e*bits). */
+/* Pack / unpack a row of D codes (LSB-first, channel e at bits
+ * [e*bits, e*bits + bits) of the row). */
 void orc_pack_row(const uint8_t *codes, int D, int bits, uint8_t *out);
 void orc_unpack_row(const uint8_t *in, int D, int bits, uint8_t *codes);
-
-/* Value rows: group-interleaved units of 4 channels (see the header). */
-int orc_v_unit_pos(int unit, int D, int G);
-void orc_pack_row_v(const uint8_t *codes, int D, int bits, int G, uint8_t *out);
-void orc_unpack_row_v(const uint8_t *in, int D, int bits, int G, uint8_t *codes);
-
-/* 3-bit rows: the low two bits of every code as a 2-bit row, then a plane of
- * high bits in 16-bit units (see the definition in kivi_oracle.c);
- * orc_hi_bit(s, i) is the bit of (set s, index i) inside a unit. */
-int orc_hi_bit(int s, int i);
-/* A cache's key / value row at any supported width (2, 3, 4, 8): the 3-bit
- * planes, else orc_pack_row / orc_pack_row_v. */
-void orc_pack_key_row(const uint8_t *codes, int D, int bits, uint8_t *out);
-void orc_unpack_key_row(const uint8_t *in, int D, int bits, uint8_t *codes);
-void orc_pack_value_row(const uint8_t *codes, int D, int bits, int G, uint8_t *out);
-void orc_unpack_value_row(const uint8_t *in, int D, int bits, int G, uint8_t *codes);
 
 /* Token counts held quantized after l tokens under a policy. */
 long orc_nq_k(long l, int R, int G, int policy);

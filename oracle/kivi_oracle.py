@@ -56,14 +56,6 @@ def lib():
                 "orc_dequant": (f32, [i32, C.c_uint16, C.c_uint16]),
                 "orc_pack_row": (None, [vp, i32, i32, vp]),
                 "orc_unpack_row": (None, [vp, i32, i32, vp]),
-                "orc_v_unit_pos": (i32, [i32, i32, i32]),
-                "orc_pack_row_v": (None, [vp, i32, i32, i32, vp]),
-                "orc_unpack_row_v": (None, [vp, i32, i32, i32, vp]),
-                "orc_hi_bit": (i32, [i32, i32]),
-                "orc_pack_key_row": (None, [vp, i32, i32, vp]),
-                "orc_unpack_key_row": (None, [vp, i32, i32, vp]),
-                "orc_pack_value_row": (None, [vp, i32, i32, i32, vp]),
-                "orc_unpack_value_row": (None, [vp, i32, i32, i32, vp]),
                 "orc_nq_k": (i64, [i64, i32, i32, i32]),
                 "orc_nq_v": (i64, [i64, i32, i32, i32]),
                 "orc_cache_new": (vp, [i32, i32, i32, i32, i32, i32, i64, i32]),
@@ -130,7 +122,7 @@ def dequant(q: int, s16: int, z16: int) -> float:
 
 def pack_row(codes: np.ndarray, bits: int) -> np.ndarray:
     c = np.ascontiguousarray(codes, dtype=np.uint8)
-    out = np.zeros(c.size * bits // 8, np.uint8)
+    out = np.zeros((c.size * bits + 7) // 8, np.uint8)
     lib().orc_pack_row(_p(c), c.size, bits, _p(out))
     return out
 
@@ -139,55 +131,6 @@ def unpack_row(packed: np.ndarray, D: int, bits: int) -> np.ndarray:
     p = np.ascontiguousarray(packed, dtype=np.uint8)
     out = np.zeros(D, np.uint8)
     lib().orc_unpack_row(_p(p), D, bits, _p(out))
-    return out
-
-
-def pack_row_v(codes: np.ndarray, bits: int, G: int = 32) -> np.ndarray:
-    c = np.ascontiguousarray(codes, dtype=np.uint8)
-    out = np.zeros(c.size * bits // 8, np.uint8)
-    lib().orc_pack_row_v(_p(c), c.size, bits, G, _p(out))
-    return out
-
-
-def unpack_row_v(packed: np.ndarray, D: int, bits: int, G: int = 32) -> np.ndarray:
-    p = np.ascontiguousarray(packed, dtype=np.uint8)
-    out = np.zeros(D, np.uint8)
-    lib().orc_unpack_row_v(_p(p), D, bits, G, _p(out))
-    return out
-
-
-def hi_bit(s: int, i: int) -> int:
-    """Bit of (set s, index i) inside a 16-bit unit of a 3-bit row's high plane."""
-    return int(lib().orc_hi_bit(s, i))
-
-
-def pack_key_row(codes: np.ndarray, bits: int) -> np.ndarray:
-    """A cache key row at any supported width (3 bits: the two planes)."""
-    c = np.ascontiguousarray(codes, dtype=np.uint8)
-    out = np.zeros(c.size * bits // 8, np.uint8)
-    lib().orc_pack_key_row(_p(c), c.size, bits, _p(out))
-    return out
-
-
-def unpack_key_row(packed: np.ndarray, D: int, bits: int) -> np.ndarray:
-    p = np.ascontiguousarray(packed, dtype=np.uint8)
-    out = np.zeros(D, np.uint8)
-    lib().orc_unpack_key_row(_p(p), D, bits, _p(out))
-    return out
-
-
-def pack_value_row(codes: np.ndarray, bits: int, G: int = 32) -> np.ndarray:
-    """A cache value row at any supported width (3 bits: the two planes)."""
-    c = np.ascontiguousarray(codes, dtype=np.uint8)
-    out = np.zeros(c.size * bits // 8, np.uint8)
-    lib().orc_pack_value_row(_p(c), c.size, bits, G, _p(out))
-    return out
-
-
-def unpack_value_row(packed: np.ndarray, D: int, bits: int, G: int = 32) -> np.ndarray:
-    p = np.ascontiguousarray(packed, dtype=np.uint8)
-    out = np.zeros(D, np.uint8)
-    lib().orc_unpack_value_row(_p(p), D, bits, G, _p(out))
     return out
 
 

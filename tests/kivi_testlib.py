@@ -91,11 +91,20 @@ def compare_state(gst: dict, ost: dict, l: int, R: int, G: int, units=None,
                 chk(name, slots, slots)
 
 
-def attn_err(out: np.ndarray, ref: np.ndarray) -> float:
-    """Worst (over batch, head) of max |o - r| / max |r|."""
+def attn_err(out: np.ndarray, ref: np.ndarray, out_dtype: str | None = None) -> float:
+    """Worst (over batch, head) of max |o - r| / max |r|.  With out_dtype
+    "bf16" the output carries its own rounding, up to half a bf16 ulp of each
+    element (8 significant bits), which is taken off each element's error
+    first (a comparison with the reference rounded to bf16 would not do: a
+    result and a reference on either side of a rounding boundary round a
+    whole ulp, 2^-7 of the value, apart)."""
     o = out.astype(np.float64).reshape(-1, out.shape[-1])
     r = ref.astype(np.float64).reshape(-1, ref.shape[-1])
-    return float((np.abs(o - r).max(axis=1) / np.abs(r).max(axis=1)).max())
+    d = np.abs(o - r)
+    if out_dtype == "bf16":
+        half_ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(r), np.abs(o)))[1] - 9)
+        d = np.maximum(d - half_ulp, 0.0)
+    return float((d.max(axis=1) / np.abs(r).max(axis=1)).max())
 
 
 def q_float(q: np.ndarray, dtype: str) -> np.ndarray:
@@ -112,3 +121,39 @@ def out_float(out: torch.Tensor) -> np.ndarray:
 def slice_unit(x: np.ndarray, b: int, h: int) -> np.ndarray:
     """[B, H, ...] -> [1, 1, ...] contiguous copy of one unit."""
     return np.ascontiguousarray(x[b:b + 1, h:h + 1])
+
+
+# ---------------------------------------------------------------- oracle pool
+
+def _oracle_unit(task):
+    """One (batch, kv-head) unit through a B=1, H=1 oracle cache (runs in a
+    worker process).  task: dict with bits, G, R, D, cap, k, v and optionally
+    kn, vn ([steps][1][1][D]: appended after the prefill), q ({step: [1][grp][D]
+    f32}: attention after that append; key -1 = after the prefill)."""
+    from oracle.kivi_oracle import OracleCache
+    o = OracleCache(task["bits"], task["G"], task["R"], task["D"], 1, 1, task["cap"])
+    o.prefill(task["k"], task["v"])
+    qs = task.get("q", {})
+    outs = {}
+    if -1 in qs:
+        outs[-1] = o.attention(qs[-1])
+    kn, vn = task.get("kn"), task.get("vn")
+    if kn is not None:
+        for i in range(kn.shape[0]):
+            o.append(kn[i], vn[i])
+            if i in qs:
+                outs[i] = o.attention(qs[i])
+    return o.export(), outs
+
+
+def oracle_units(tasks):
+    """_oracle_unit over tasks on a pool of spawned processes (spawned, not
+    forked: the parent already uses the GPU), in order."""
+    import multiprocessing as mp
+    import os
+    n = max(1, min(len(tasks), len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                   else os.cpu_count() or 1))
+    with mp.get_context("spawn").Pool(n) as pool:
+        # bounded: a worker that cannot start makes the pool respawn it
+        # forever, so the result is awaited with a time limit
+        return pool.map_async(_oracle_unit, tasks, chunksize=1).get(timeout=1800)

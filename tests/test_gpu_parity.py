@@ -37,10 +37,8 @@ def check_attention(g, o, wl, q=None, splits=None):
         g.set_splits(splits)
     out = T.out_float(g.attention(T.dev(q, wl.q_dtype)))
     ref = o.attention(T.q_float(q, wl.q_dtype))
-    err = T.attn_err(out, ref)
-    # a bf16 output alone is rounded by up to half an ulp: 2^-9 of its magnitude
-    tol = T.ATTN_TOL + (2.0 ** -9 if wl.q_dtype == "bf16" else 0.0)
-    assert err <= tol, err
+    err = T.attn_err(out, ref, wl.q_dtype)
+    assert err <= T.ATTN_TOL, err
     return out
 
 

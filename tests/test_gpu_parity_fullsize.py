@@ -1,6 +1,6 @@
 """Parity at the full sizes of the five workloads, in the launch configuration
-the benchmark times.  Where the oracle would take minutes on the whole batch,
-whole (batch, kv-head) units are sampled and the oracle runs on those alone."""
+the benchmark times: every (batch, kv-head) unit against the oracle (the
+larger workloads run the oracle one unit per process)."""
 import numpy as np
 import pytest
 import torch
@@ -57,9 +57,26 @@ def test_llama3_8b_decode_step(bits):
     assert T.attn_err(out, o.attention(T.q_float(wl.q, "f16"))) <= T.ATTN_TOL
 
 
-@pytest.mark.parametrize("bits", [2, 3, 4, 8])
+def _unit_task(wl, b, h, bits=None, cap=None):
+    return {"bits": bits or wl.bits, "G": wl.G, "R": wl.R, "D": wl.D, "cap": cap or wl.capacity,
+            "k": T.slice_unit(wl.k, b, h), "v": T.slice_unit(wl.v, b, h)}
+
+
+@pytest.mark.parametrize("bits", [2, 4])
 def test_prefill_quantize_bf16_32k(bits):
-    """batch 4, 8 KV heads, 32768 tokens of bf16 with V spikes: sampled units."""
+    """batch 4, 8 KV heads, 32768 tokens of bf16 with V spikes, 2 and 4 bits:
+    the state of every unit bit for bit."""
+    wl = W.prefill_quantize(bits)
+    g = T.gpu_cache(wl)
+    g.prefill(T.dev(wl.k, "bf16"), T.dev(wl.v, "bf16"))
+    units = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+    res = T.oracle_units([_unit_task(wl, b, h) for b, h in units])
+    T.compare_state(T.gpu_state(g), [st for st, _ in res], wl.T, wl.R, wl.G, units=units)
+
+
+@pytest.mark.parametrize("bits", [3, 8])
+def test_prefill_quantize_bf16_32k_other_widths(bits):
+    """The same workload at 3 and 8 bits: sampled units."""
     wl = W.prefill_quantize(bits)
     g = T.gpu_cache(wl)
     g.prefill(T.dev(wl.k, "bf16"), T.dev(wl.v, "bf16"))
@@ -69,43 +86,61 @@ def test_prefill_quantize_bf16_32k(bits):
 
 
 def test_long_context_131k():
-    """batch 1, 32/8 heads, 131072 tokens, R=128: sampled units, split-K attention."""
+    """batch 1, 32/8 heads, 131072 tokens, R=128: every unit's state bit for
+    bit and its split-K attention in tolerance."""
     wl = W.long_context()
     g = T.gpu_cache(wl)
     g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
     assert g.splits() > 16
-    units = [(0, 0), (0, 5)]
-    orc = unit_oracles(wl, units)
-    T.compare_state(T.gpu_state(g), [o.export() for o in orc], wl.T, wl.R, wl.G, units=units)
+    grp = wl.Hq // wl.Hkv
+    units = [(0, h) for h in range(wl.Hkv)]
+    qf = T.q_float(wl.q, wl.q_dtype)
+    tasks = []
+    for b, h in units:
+        t = _unit_task(wl, b, h)
+        t["q"] = {-1: np.ascontiguousarray(qf[b:b + 1, h * grp:(h + 1) * grp])}
+        tasks.append(t)
+    res = T.oracle_units(tasks)
+    T.compare_state(T.gpu_state(g), [st for st, _ in res], wl.T, wl.R, wl.G, units=units)
     out = T.out_float(g.attention(T.dev(wl.q, "f16")))
-    assert unit_attention_err(out, wl, units, orc, wl.q) <= T.ATTN_TOL
+    for (b, h), (_, outs) in zip(units, res):
+        assert T.attn_err(out[b:b + 1, h * grp:(h + 1) * grp], outs[-1]) <= T.ATTN_TOL, h
 
 
 def test_streaming_2048_plus_512():
     """batch 64, 28/4 heads: 512 decode steps after a 2048 prefill.  Attention
-    at the flush boundaries against the oracle (sampled units); the final cache
-    bit-identical to a one-shot prefill of the same 2560 tokens."""
+    of every unit at the flush boundaries against the oracle; the final state
+    of every unit bit for bit against the oracle, and against a one-shot
+    prefill of the same 2560 tokens."""
     wl = W.streaming()
     g = T.gpu_cache(wl)
     g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
-    units = [(0, 0), (37, 3)]
-    orc = unit_oracles(wl, units)
-    check_at = {0, 1, 31, 32, 63, 64, 255, 511}
+    grp = wl.Hq // wl.Hkv
+    units = [(b, h) for b in range(wl.B) for h in range(wl.Hkv)]
+    check_at = [0, 1, 31, 32, 63, 64, 255, 511]
+    qs = {i: T.q_float(wl.q_for_step(i), wl.q_dtype) for i in check_at}
+    tasks = []
+    for b, h in units:
+        t = _unit_task(wl, b, h)
+        t["kn"] = np.ascontiguousarray(wl.k_new[:, b:b + 1, h:h + 1])
+        t["vn"] = np.ascontiguousarray(wl.v_new[:, b:b + 1, h:h + 1])
+        t["q"] = {i: np.ascontiguousarray(qs[i][b:b + 1, h * grp:(h + 1) * grp]) for i in check_at}
+        tasks.append(t)
+    res = T.oracle_units(tasks)
     kn_all = T.dev(wl.k_new, "f16")
     vn_all = T.dev(wl.v_new, "f16")
     for i in range(wl.steps):
         g.append(kn_all[i], vn_all[i])
-        for (b, h), o in zip(units, orc):
-            o.append(T.slice_unit(wl.k_new[i], b, h), T.slice_unit(wl.v_new[i], b, h))
-        if i in check_at:
-            q = wl.q_for_step(i)
-            out = T.out_float(g.attention(T.dev(q, "f16")))
-            assert unit_attention_err(out, wl, units, orc, q) <= T.ATTN_TOL, i
+        if i in qs:
+            out = T.out_float(g.attention(T.dev(wl.q_for_step(i), "f16")))
+            worst = max(T.attn_err(out[b:b + 1, h * grp:(h + 1) * grp], outs[i])
+                        for (b, h), (_, outs) in zip(units, res))
+            assert worst <= T.ATTN_TOL, (i, worst)
         else:
             g.attention(T.dev(wl.q, "f16"))
     l = wl.T + wl.steps
     st = T.gpu_state(g)
-    T.compare_state(st, [o.export() for o in orc], l, wl.R, wl.G, units=units)
+    T.compare_state(st, [s_ for s_, _ in res], l, wl.R, wl.G, units=units)
     k_all = np.concatenate([wl.k, wl.k_new.transpose(1, 2, 0, 3)], axis=2)
     v_all = np.concatenate([wl.v, wl.v_new.transpose(1, 2, 0, 3)], axis=2)
     one = T.gpu_cache(wl)

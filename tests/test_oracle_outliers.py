@@ -55,9 +55,9 @@ def test_outlier_selection_and_storage(oracle, bits, n_out):
                 assert not so["scale_k"][b, h, g, want].any() and not so["zero_k"][b, h, g, want].any()
                 assert np.array_equal(so["scale_k"][b, h, g, keep], sp["scale_k"][b, h, g, keep])
                 assert np.array_equal(so["zero_k"][b, h, g, keep], sp["zero_k"][b, h, g, keep])
-                codes_o = np.array([oracle.unpack_key_row(so["codes_k"][b, h, t], D, bits)
+                codes_o = np.array([oracle.unpack_row(so["codes_k"][b, h, t], D, bits)
                                     for t in range(g * G, (g + 1) * G)])
-                codes_p = np.array([oracle.unpack_key_row(sp["codes_k"][b, h, t], D, bits)
+                codes_p = np.array([oracle.unpack_row(sp["codes_k"][b, h, t], D, bits)
                                     for t in range(g * G, (g + 1) * G)])
                 assert not codes_o[:, want].any()
                 assert np.array_equal(codes_o[:, keep], codes_p[:, keep])
