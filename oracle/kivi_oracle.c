@@ -24,8 +24,7 @@
  *  [CQ]  "KV Cache Compression > Cache Quantization" (Brenndoerfer), the
  *        uniform quantization and dequantization formulas.
  *
- * Readings where the pages are silent or disagree (each also listed in the
- * design notes):
+ * Readings where the pages are silent or disagree:
  *  - every input element is first rounded to fp16 (the residual window is
  *    fp16 [VQ item 3]); codes are computed from those fp16 values widened;
  *  - round() is round-half-to-even (torch.round in [NB]);
@@ -158,7 +157,8 @@ float orc_dequant(int q, uint16_t scale16, uint16_t zero16) {
   return p + orc_f16_to_f32(zero16);
 }
 
-/* Packing ([SURVEY] layout, the plain reading of "codes packed to uint8"):
+/* Packing (the pages fix no bit layout; this is the plain reading of "codes
+ * packed to uint8"):
  * channel e of a row occupies bits [e*bits, e*bits + bits) of the row, LSB
  * first -- byte e*bits/8 at bit offset (e*bits) mod 8, a 3-bit code crossing
  * into the next byte when its offset is 6 or 7.  Keys and values, every
