@@ -153,22 +153,28 @@ struct TileBuf {
   uint32_t sv[64], zv[64];
   uint32_t outl[outlier_block_bytes(kMaxOutliers) / 4];  // outlier block, when the cache keeps outliers
 };
-template <int BITS>
-constexpr int kStagesOf = BITS == 2 ? 3 : 2;  // tiles in flight per warp (3 KB / 4-9 KB tiles)
+constexpr int kMaxStages = 6;  // staged tiles per warp, at most
 
-template <int BITS, int NB>
-struct WarpSmem {
-  TileBuf<BITS> st[kWarps][kStagesOf<BITS>];  // per-warp rings of staged tiles
+// The packed splits' shared memory: per-warp rings of S staged tiles of
+// `stride` bytes (the cache's tile size: a stage mirrors a tile byte for byte;
+// S is chosen per launch to fill the CTA's share of the SM, see
+// attn_stages), then this block.  q itself is staged for the table build in
+// the stage buffers of stage 1, which no copy fills before the tables exist.
+template <int NB>
+struct PackedState {
   // q * base^-e(i) per column: one key block (NB = 1, columns (head, part)):
   // [0] / [1] the split_mul operands (xa, xb); two key blocks (NB = 2,
   // columns = heads): [0] / [1] the hi / lo part
   uint4 qs[2][4][8][4];
   uint4 qb[NB][4][8][4];                  // q hi / lo (words of a quarter in the order 0, 2, 1, 3)
-  float qv[kNH][kHeadDim];                // q, staged for the tables
   float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
   float qinv[kNH];                        // 2^-E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
-  unsigned long long bar[kWarps][kStagesOf<BITS>];
+  unsigned long long bar[kWarps][kMaxStages];
 };
+
+__host__ __device__ constexpr uint32_t packed_state_off(int S, uint32_t stride) {
+  return ((uint32_t)kWarps * (uint32_t)S * stride + 15u) / 16u * 16u;
+}
 
 // A tail split: up to kTailTok tokens.  Its packed rows arrive as the whole
 // code blocks of the (at most two) tiles involved (kpk, vpk, in the tiles'
@@ -191,25 +197,40 @@ struct TailSmem {
   unsigned long long bar;                 // completion of the round's copies
 };
 
-template <int BITS, int NB>
-union SplitSmem {
-  WarpSmem<BITS, NB> ws;
-  TailSmem<BITS> tail;
-};
-
 enum Path { kPathMma = 1, kPathTail = 2 };
 
-// Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the CTA
-// is done with (its staged tiles or tail rows).
-static_assert(kWarps * kNH * kHeadDim * 4 <= 2 * kTailTok * kHeadDim, "tail merge areas");
+// The CTA's dynamic shared memory: the tail split's layout, or the packed
+// splits' (stage rings, then PackedState), from the same base.
 template <int BITS, int NB>
-__device__ __forceinline__ float* merge_area(SplitSmem<BITS, NB>& sm, int warp, int path) {
-  if (path == kPathMma) return reinterpret_cast<float*>(&sm.ws.st[warp][0]);
-  return reinterpret_cast<float*>(&sm.tail.kring[0][0]) + warp * kNH * kHeadDim;
-}
-static_assert(kNH * kHeadDim * 4 <= (int)sizeof(TileBuf<2>) * kStagesOf<2> &&
-                  kNH * kHeadDim * 4 <= (int)sizeof(TileBuf<3>) * kStagesOf<3>,
-              "a warp's staged tiles hold its merge area");
+struct SmemView {
+  unsigned char* base;
+  int S;            // stages per warp
+  uint32_t stride;  // bytes per stage
+
+  __device__ __forceinline__ TileBuf<BITS>* ring(int w) const {
+    return reinterpret_cast<TileBuf<BITS>*>(base + (size_t)w * S * stride);
+  }
+  __device__ __forceinline__ TileBuf<BITS>& stage(int w, int k) const {
+    return *reinterpret_cast<TileBuf<BITS>*>(base + ((size_t)w * S + k) * stride);
+  }
+  __device__ __forceinline__ PackedState<NB>& ps() const {
+    return *reinterpret_cast<PackedState<NB>*>(base + packed_state_off(S, stride));
+  }
+  __device__ __forceinline__ TailSmem<BITS>& tail() const { return *reinterpret_cast<TailSmem<BITS>*>(base); }
+  // q of head j, staged for the tables: in stage 1 of warp j >> 1
+  __device__ __forceinline__ float* qv(int j) const {
+    return reinterpret_cast<float*>(base + ((size_t)(j >> 1) * S + 1) * stride + (j & 1) * 4 * kHeadDim);
+  }
+  // Per-warp merge area: [kNH][kHeadDim] floats inside buffers that the CTA
+  // is done with (the warp's staged tiles, or the tail's rows).
+  __device__ __forceinline__ float* merge_area(int warp, int path) const {
+    if (path == kPathMma) return reinterpret_cast<float*>(base + (size_t)warp * S * stride);
+    return reinterpret_cast<float*>(&tail().kring[0][0]) + warp * kNH * kHeadDim;
+  }
+};
+static_assert(kWarps * kNH * kHeadDim * 4 <= 2 * kTailTok * kHeadDim, "tail merge areas");
+// (a warp's merge area takes 4 KB: its S >= 2 stages of >= 3 KB hold it;
+// two heads' q take 1 KB of its stage 1)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -712,13 +733,25 @@ __host__ __device__ constexpr int word_pos(int w) {
   return BITS <= 3 ? (w & 7) : (w & 3);
 }
 
+// q of the CTA's heads in global memory, times scale * log2(e) (read for
+// the fp16 outlier channels, at most four per tile).
+struct QRows {
+  const void* q;
+  long row0;  // element index of the chunk's first head
+  int dtype;
+  float scale_log2;
+  __device__ __forceinline__ float at(int head, int ch) const {
+    return load_q(q, row0 + (long)head * kHeadDim + ch, dtype) * scale_log2;
+  }
+};
+
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane,
 // in the order of the q tables: one key block, head g >> 1, part g & 1 (one
 // fp16 of the pair per lane); two key blocks, head g, both parts (bq[0] hi,
 // bq[1] lo).  The q table is pre-scaled by base^-e(i) to cancel the power
 // that the code extraction leaves in the A operand.
 template <int BITS, int NB>
-__device__ __forceinline__ void build_qprime(const WarpSmem<BITS, NB>& ws, const uint32_t* sk, int g, int tig,
+__device__ __forceinline__ void build_qprime(const PackedState<NB>& ws, const uint32_t* sk, int g, int tig,
                                              uint32_t (&bq)[NB][8][2]) {
 #pragma unroll
   for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
@@ -758,9 +791,9 @@ __device__ __forceinline__ int score_row(int g) { return (g & 3) + 8 * (g >> 2);
 // less mb[nb], where hd(nb) = tig with one key block and 2 tig + nb with two;
 // ks = 2^E * scale * log2(e) of that head.
 template <int BITS, int NB>
-__device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
+__device__ __forceinline__ void key_scores(const PackedState<NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
                                            const float (&ks)[NB], const float (&mb)[NB], int n_out,
-                                           float scale_log2, float (&sc)[NB][4]) {
+                                           const QRows& qr, float (&sc)[NB][4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
   // ---- beta = zK x q.  The A operand of a quarter is its four zero-point
   //      words Z0..Z3 as loaded (rows g: Z0, Z2; rows g + 8: Z1, Z3); one
@@ -907,7 +940,7 @@ __device__ __forceinline__ void key_scores(const WarpSmem<BITS, NB>& ws, const T
         const int ch = (iw >> (8 * o)) & 0xffu;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const float qo = ws.qv[NB == 1 ? tig : 2 * tig + nb][ch] * scale_log2;
+          const float qo = qr.at(NB == 1 ? tig : 2 * tig + nb, ch);
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int t = 16 * (r >> 1) + tr + 4 * (r & 1);
@@ -1145,13 +1178,14 @@ __device__ __forceinline__ void load_q8(const AttnArgs& a, int b, int j0, int nh
 }
 
 template <int BITS, int NB>
-__device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const float (&v)[8]) {
+__device__ void build_q_tables(const SmemView<BITS, NB>& sv, const AttnArgs& a, const float (&v)[8]) {
+  PackedState<NB>& s = sv.ps();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
   for (int hh = 0; hh < 2; ++hh) {
     const int j = warp + kWarps * hh;
     const float* vj = v + 4 * hh;
-    *reinterpret_cast<float4*>(&s.qv[j][4 * lane]) = make_float4(vj[0], vj[1], vj[2], vj[3]);
+    *reinterpret_cast<float4*>(sv.qv(j) + 4 * lane) = make_float4(vj[0], vj[1], vj[2], vj[3]);
     const float amax = warp_max(fmaxf(fmaxf(fabsf(vj[0]), fabsf(vj[1])), fmaxf(fabsf(vj[2]), fabsf(vj[3]))));
     if (lane == 0) {
       const int be = (int)((__float_as_uint(amax) >> 23) & 0xffu);
@@ -1189,7 +1223,7 @@ __device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const f
       c1 = c0 + 2;
     }
     const float f = code_scale<BITS>(i);
-    const float q0 = s.qv[j][c0] * s.qinv[j], q1 = s.qv[j][c1] * s.qinv[j];  // exact scalings
+    const float q0 = sv.qv(j)[c0] * s.qinv[j], q1 = sv.qv(j)[c1] * s.qinv[j];  // exact scalings
     const uint32_t qh = f2_to_h2(q0, q1);
     const uint32_t ql = f2_to_h2(q0 - h_lo(qh), q1 - h_hi(qh));
     const uint32_t sh = f2_to_h2(q0 * f, q1 * f);
@@ -1212,6 +1246,7 @@ __device__ void build_q_tables(WarpSmem<BITS, NB>& s, const AttnArgs& a, const f
       reinterpret_cast<uint32_t*>(&s.qb[NB - 1][quarter][j][tig])[wb] = ql;
     }
   }
+  fence_proxy_async();  // q staged in stage buffers that bulk copies fill next
 }
 
 // The stage buffer mirrors the packed tile byte for byte.
@@ -1271,21 +1306,22 @@ __device__ __forceinline__ void issue_tile_if(bool p, TileBuf<BITS>& tb, unsigne
 // loop).  Leaves each warp's (max, sum) per head in s_m / s_l and its output
 // in its merge area.
 template <int BITS, int NB>
-__device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<BITS, NB>& sm, long unit, int b,
+__device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemView<BITS, NB>& sv, long unit, int b,
                              int j0, int nh, int tile0, int tile1, float (&s_m)[kWarps][kNH],
                              float (&s_l)[kWarps][kNH]) {
-  constexpr int kStages = kStagesOf<BITS>;
-  WarpSmem<BITS, NB>& ws = sm.ws;
+  const int kStages = sv.S;
+  PackedState<NB>& ws = sv.ps();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
   const int n_mine = tile0 + warp < tile1 ? (tile1 - tile0 - warp + kWarps - 1) / kWarps : 0;
-  TileBuf<BITS>* st = ws.st[warp];
+  unsigned char* const ring = reinterpret_cast<unsigned char*>(sv.ring(warp));
+  auto st = [&](int k) -> TileBuf<BITS>& { return *reinterpret_cast<TileBuf<BITS>*>(ring + (size_t)k * sv.stride); };
   unsigned long long* bars = ws.bar[warp];
+  const QRows qr{a.q, ((long)b * a.Hq + j0) * kHeadDim, a.q_dtype, a.scale_log2};
   float qv8[8];
   load_q8(a, b, j0, nh, qv8);
 
   if (lane == 0) {
-#pragma unroll
     for (int k = 0; k < kStages; ++k) mbar_init(&bars[k], 1);
     mbar_fence_init();
   }
@@ -1299,12 +1335,12 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
   // whose packed tiles the append may write builds the tables while the
   // append runs and issues every copy after it.
   const bool wait_first = a.pdl == kPdlAll;
-  if (!wait_first && lane == 0 && issued > 0) issue_tile<BITS>(st[0], &bars[0], us, t_first);
-  build_q_tables<BITS, NB>(ws, a, qv8);
+  if (!wait_first && lane == 0 && issued > 0) issue_tile<BITS>(st(0), &bars[0], us, t_first);
+  build_q_tables<BITS, NB>(sv, a, qv8);
   __syncthreads();
   if (wait_first) grid_dependency_wait();
   if (lane == 0)
-    for (int k = wait_first ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st[k], &bars[k], us, t_first + kWarps * k);
+    for (int k = wait_first ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st(k), &bars[k], us, t_first + kWarps * k);
   float ks[NB], m_run[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
@@ -1337,7 +1373,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
       float sc[NB][4], mb[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) mb[nb] = 0.0f;
-      key_scores<BITS, NB>(ws, st[0], g, tig, ks, mb, cv.n_out, a.scale_log2, sc);
+      key_scores<BITS, NB>(ws, st(0), g, tig, ks, mb, cv.n_out, qr, sc);
       softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
     }
   }
@@ -1357,12 +1393,12 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
       }
     }
     float sc[NB][4];
-    key_scores<BITS, NB>(ws, st[sn], g, tig, ks, m_run, cv.n_out, a.scale_log2, sc);
-    value_acc<BITS>(st[sk], pb, g, tig, O, Z);
+    key_scores<BITS, NB>(ws, st(sn), g, tig, ks, m_run, cv.n_out, qr, sc);
+    value_acc<BITS>(st(sk), pb, g, tig, O, Z);
     done = k + 1;
     __syncwarp();  // every lane is done with stage sk
     const bool more = k + kStages < n_mine;
-    issue_tile_if<BITS>(more && lane == 0, st[sk], &bars[sk], next_src, us.tile_bytes);
+    issue_tile_if<BITS>(more && lane == 0, st(sk), &bars[sk], next_src, us.tile_bytes);
     next_src += src_step;
     issued += more;
     softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
@@ -1370,7 +1406,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     sk = sn;
   }
   if (!failed && n_mine > 0) {
-    value_acc<BITS>(st[sk], pb, g, tig, O, Z);  // the last tile's values
+    value_acc<BITS>(st(sk), pb, g, tig, O, Z);  // the last tile's values
     done = n_mine;
   }
   if (done < n_mine) {
@@ -1381,7 +1417,6 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     __syncwarp();
   } else if (lane == 0) {
     // every copy has landed: the barriers' memory may be reused
-#pragma unroll
     for (int kk = 0; kk < kStages; ++kk) mbar_inval(&bars[kk]);
   }
 
@@ -1406,7 +1441,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, SplitSmem<B
     zt[gp][1] = __shfl_sync(kFull, Z[1], 4 * gp + tig);
   }
   if (n_mine == 0) return;  // no tile: the area stays unwritten (max -inf)
-  float* oa = merge_area(sm, warp, kPathMma) + (2 * tig) * kHeadDim;
+  float* oa = sv.merge_area(warp, kPathMma) + (2 * tig) * kHeadDim;
   float* ob = oa + kHeadDim;
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
@@ -1469,7 +1504,7 @@ __device__ __forceinline__ void merge_partials(const float* po, const float* pml
 // one after another and are folded in, and the result is left as warp 0's
 // slot (the other warps' slots empty) for the CTA merge.
 template <int BITS, int NB>
-__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan p, SplitSmem<BITS, NB>& sm,
+__device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan p, const SmemView<BITS, NB>& sv,
                            long unit, int b, int j0, int nh, float (&s_m)[kWarps][kNH],
                            float (&s_l)[kWarps][kNH]) {
   const int d = threadIdx.x;
@@ -1486,7 +1521,7 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
         if (s_m[w][j] == -INFINITY) continue;
         const float e = fast_exp2(s_m[w][j] - M);
         lt += e * s_l[w][j];
-        ot += e * merge_area(sm, w, kPathMma)[j * kHeadDim + d];
+        ot += e * sv.merge_area(w, kPathMma)[j * kHeadDim + d];
       }
     }
     pm[j] = M;
@@ -1494,10 +1529,10 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
     po[j] = ot;
   }
   __syncthreads();  // the warps' slots are read; the tail may overwrite them
-  float* mo0 = merge_area(sm, 0, kPathTail);
+  float* mo0 = sv.merge_area(0, kPathTail);
   uint32_t round = 0;
   for (int c0 = p.t_tail; c0 < p.l; c0 += kTailTok, ++round) {
-    tail_split<BITS, NB>(cv, a, p, sm.tail, mo0, unit, b, j0, nh, c0, round, s_m, s_l);
+    tail_split<BITS, NB>(cv, a, p, sv.tail(), mo0, unit, b, j0, nh, c0, round, s_m, s_l);
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kNH; ++j) {
@@ -1512,7 +1547,7 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
     }
     __syncthreads();  // before the next round overwrites the staged rows
   }
-  float* out0 = merge_area(sm, 0, kPathMma);
+  float* out0 = sv.merge_area(0, kPathMma);
 #pragma unroll
   for (int j = 0; j < kNH; ++j) out0[j * kHeadDim + d] = po[j];
   if (d < kWarps * kNH) {
@@ -1533,8 +1568,8 @@ __device__ void fused_tail(const CacheView& cv, const AttnArgs& a, const SeqPlan
 template <int BITS, int NB>
 __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
     attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];  // sizeof(SplitSmem<BITS, NB>)
-  SplitSmem<BITS, NB>& sm = *reinterpret_cast<SplitSmem<BITS, NB>*>(smem_raw);
+  extern __shared__ __align__(16) unsigned char smem_raw[];  // attn_stages: the tail or the packed layout
+  const SmemView<BITS, NB> sv{smem_raw, a.stages, (uint32_t)cv.tile_bytes};
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
   __shared__ bool s_last;
 
@@ -1561,19 +1596,19 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   if (path == kPathTail) {
     // the tail reads the rings the append writes
     if (a.pdl == kPdlAll || a.pdl == kPdlTail) grid_dependency_wait();
-    tail_split<BITS, NB>(cv, a, p, sm.tail, merge_area(sm, 0, kPathTail), unit, b, j0, nh,
+    tail_split<BITS, NB>(cv, a, p, sv.tail(), sv.merge_area(0, kPathTail), unit, b, j0, nh,
                          p.t_tail + s * kTailTok, 0u, s_m, s_l);
   } else {
     // ---- tensor cores: packed tiles [sp*chunk, min(t_tail, (sp+1)*chunk)) ----
     const int sp = s - p.tail_splits;
     const int tile0 = sp * p.chunk / 32;
     const int tile1 = min(p.t_tail, (sp + 1) * p.chunk) / 32;
-    packed_split<BITS, NB>(cv, a, sm, unit, b, j0, nh, tile0, tile1, s_m, s_l);
+    packed_split<BITS, NB>(cv, a, sv, unit, b, j0, nh, tile0, tile1, s_m, s_l);
   }
   __syncthreads();
   if (path == kPathMma && p.tail_fused && s == p.splits - 1) {
     if (a.pdl == kPdlTail) grid_dependency_wait();  // the tail reads what the append wrote
-    fused_tail<BITS, NB>(cv, a, p, sm, unit, b, j0, nh, s_m, s_l);
+    fused_tail<BITS, NB>(cv, a, p, sv, unit, b, j0, nh, s_m, s_l);
   }
   // an overlapping launch waits for the launch before it only here, before
   // its first global write
@@ -1593,7 +1628,7 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
         if (s_m[w][j] == -INFINITY) continue;  // an empty warp (its area is not written)
         const float e = fast_exp2(s_m[w][j] - M);
         lt += e * s_l[w][j];
-        ot += e * merge_area(sm, w, path)[j * kHeadDim + d];
+        ot += e * sv.merge_area(w, path)[j * kHeadDim + d];
       }
     }
     const long pidx = (gid * a.splits + s) * kNH + j;
@@ -1675,33 +1710,56 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
 
 }  // namespace
 
-// attn_ctas_per_sm(BITS, NB) CTAs must fit an SM's 228 KB of shared memory
-// (1 KB of it reserved per CTA).
+// Stages per warp for a tile of `stride` bytes: as many as attn_ctas_per_sm
+// CTAs per SM leave room for (228 KB of shared memory per SM; per CTA 1 KB
+// reserved by the system and the kernel's static arrays), at least two and
+// at most kMaxStages; *smem is the dynamic size (the packed layout, or the
+// tail split's if larger).
 template <int BITS, int NB>
-constexpr bool kFitsSm =
-    attn_ctas_per_sm(BITS, NB) * (sizeof(SplitSmem<BITS, NB>) + 1024 + 512) <= 228 * 1024;
-static_assert(kFitsSm<2, 1> && kFitsSm<2, 2>, "2-bit CTAs per SM");
-static_assert(kFitsSm<3, 1> && kFitsSm<3, 2>, "3-bit CTAs per SM");
-static_assert(kFitsSm<4, 1> && kFitsSm<4, 2>, "4-bit CTAs per SM");
-static_assert(kFitsSm<8, 1> && kFitsSm<8, 2>, "8-bit CTAs per SM");
+int attn_stages(uint32_t stride, size_t* smem) {
+  const size_t per_cta = (size_t)228 * 1024 / attn_ctas_per_sm(BITS, NB) - 1024 - 512;
+  const size_t fixed = sizeof(PackedState<NB>) + 16;
+  int S = (int)((per_cta - fixed) / ((size_t)kWarps * stride));
+  S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
+  const size_t packed = packed_state_off(S, stride) + sizeof(PackedState<NB>);
+  *smem = packed > sizeof(TailSmem<BITS>) ? packed : sizeof(TailSmem<BITS>);
+  return S;
+}
 
 template <int BITS, int NB>
-cudaError_t launch_bits(const dim3& grid, const CacheView& cv, const AttnArgs& a, const SeqLens& lens,
+constexpr bool kTailFits =
+    attn_ctas_per_sm(BITS, NB) * (sizeof(TailSmem<BITS>) + 1024 + 512) <= 228 * 1024;
+static_assert(kTailFits<2, 1> && kTailFits<2, 2> && kTailFits<3, 1> && kTailFits<3, 2> && kTailFits<4, 1> &&
+                  kTailFits<4, 2> && kTailFits<8, 1> && kTailFits<8, 2>,
+              "the tail split's layout fits the CTAs of an SM");
+
+template <int BITS, int NB>
+cudaError_t launch_bits(const dim3& grid, const CacheView& cv, AttnArgs a, const SeqLens& lens,
                         cudaStream_t st) {
-  // The shared-memory opt-in is a per-device function attribute; setting it
-  // on every call costs a host call only.
-  const cudaError_t e = cudaFuncSetAttribute(attn_kernel<BITS, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)sizeof(SplitSmem<BITS, NB>));
+  size_t smem = 0, cap = 0;
+  a.stages = attn_stages<BITS, NB>((uint32_t)cv.tile_bytes, &smem);
+  // The shared-memory opt-in is a per-device function attribute: set to the
+  // largest size any outlier count asks for (the same on every call, so
+  // that calls from several host threads cannot shrink it under another's
+  // launch); setting it costs a host call only.
+  const uint32_t plain = (uint32_t)(cv.tile_bytes - outlier_block_bytes(cv.n_out));
+  for (int n = 0; n <= kMaxOutliers; ++n) {
+    size_t sz = 0;
+    attn_stages<BITS, NB>(plain + (uint32_t)outlier_block_bytes(n), &sz);
+    cap = sz > cap ? sz : cap;
+  }
+  const cudaError_t e =
+      cudaFuncSetAttribute(attn_kernel<BITS, NB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)cap);
   if (e != cudaSuccess) return e;
   if (!a.pdl) {
-    attn_kernel<BITS, NB><<<grid, 128, sizeof(SplitSmem<BITS, NB>), st>>>(cv, a, lens);
+    attn_kernel<BITS, NB><<<grid, 128, smem, st>>>(cv, a, lens);
     return cudaGetLastError();
   }
   // a programmatic dependent of the kernel before it on the stream
   cudaLaunchConfig_t lc = {};
   lc.gridDim = grid;
   lc.blockDim = dim3(128);
-  lc.dynamicSmemBytes = sizeof(SplitSmem<BITS, NB>);
+  lc.dynamicSmemBytes = smem;
   lc.stream = st;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

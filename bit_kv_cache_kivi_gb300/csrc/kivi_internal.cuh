@@ -278,6 +278,7 @@ struct AttnArgs {
   int* counters;      // [gid][merge_groups] CTAs finished per split group; 0 between calls
   int* counters2;     // [gid] split groups finished; 0 between calls
   int* status;        // set nonzero when a bounded wait for staged data timed out
+  int stages;         // staged tiles per warp (set at launch from the tile size)
   // A programmatic dependent of the append kernel just before it on the
   // stream (the one-call decode step): the CTAs may start while the append
   // runs.  kPdlAll: every CTA loads q and builds its tables, then waits for
