@@ -655,6 +655,50 @@ def streaming(args, torch, W, KiviCache, dev, stream, ev, peak):
     return res
 
 
+def append_window(torch, W, KiviCache, dev, stream, ev):
+    """The decode append alone on the Llama-3-8B decode shape: 32 appends
+    from context 4096 on one cache, eager, each followed by the attention;
+    the last append completes a 32-token key residual and quantizes it (the
+    K flush of Algorithm 1).  Events around every append, with a GPU spin
+    before it so that host latency stays outside them.  Launch order: the
+    prefill, then 32 x (append_kernel, attn_kernel), so that the 31st append
+    is a plain step and the 32nd the flush step."""
+    wl = W.llama3_8b_decode(steps=32)
+    B, Hkv, D, R, T0 = wl.B, wl.Hkv, wl.D, wl.R, wl.T
+    c = KiviCache(batch=B, n_kv_heads=Hkv, n_q_heads=wl.Hq, max_tokens=T0 + 32, bits=2, residual=R)
+    c.prefill(W.to_torch(wl.k, "f16", dev), W.to_torch(wl.v, "f16", dev))
+    kn, vn = W.to_torch(wl.k_new, "f16", dev), W.to_torch(wl.v_new, "f16", dev)
+    q = W.to_torch(wl.q, "f16", dev)
+    out = torch.empty_like(q)
+    recs = []
+    for i in range(32):
+        t = c.length
+        torch.cuda._sleep(SPIN_CYCLES)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        c.append(kn[i], vn[i])
+        e1.record(stream)
+        c.attention(q, out)
+        recs.append((t, e0, e1))
+    torch.cuda.synchronize()
+    us = {t: a.elapsed_time(b) * 1e3 for t, a, b in recs}
+    flush_t = [t for t in us if (t + 1) % R == 0]
+    assert len(flush_t) == 1 and flush_t[0] == T0 + 31
+    plain = np.array([us[t] for t in us if t not in flush_t])
+    tf = flush_t[0]
+    return {"append_window": {
+        "workload": "llama3_8b_decode append: batch 8, 8 kv heads, 2-bit, residual 32; "
+                    "32 appends from context 4096, the last one flushing the key residual",
+        "plain_us_median": round(float(np.median(plain)), 3),
+        "plain_bytes": append_bytes(B, Hkv, D, T0 + 1, R, 2),
+        "plain_gbs": round(append_bytes(B, Hkv, D, T0 + 1, R, 2) / (np.median(plain) * 1e-6) / 1e9, 2),
+        "flush_us": round(us[tf], 3),
+        "flush_bytes": append_bytes(B, Hkv, D, tf, R, 2),
+        "flush_gbs": round(append_bytes(B, Hkv, D, tf, R, 2) / (us[tf] * 1e-6) / 1e9, 2),
+        "window_us": round(float(sum(us.values())), 3),
+        "note": "events around a single launch add a few us on this GPU"}}
+
+
 def run_only(args):
     """One of the secondary workloads alone (used for profiling captures)."""
     import torch
@@ -667,6 +711,8 @@ def run_only(args):
     def ev():
         return torch.cuda.Event(enable_timing=True)
 
+    if args.only == "append":
+        return append_window(torch, W, KiviCache, dev, torch.cuda.current_stream(), ev)
     return extra_workloads(args, torch, W, KiviCache, dev, torch.cuda.current_stream(), ev, peak,
                            which=args.only)
 
@@ -938,7 +984,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
-    ap.add_argument("--only", choices=["main", "quantize", "attn3", "attn4", "attn8", "outliers", "long", "streaming"],
+    ap.add_argument("--only", choices=["main", "quantize", "attn3", "attn4", "attn8", "outliers", "long", "streaming",
+                                       "append"],
                     help="run one workload alone (for profiling); prints its numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quant-reps", type=int, default=10)

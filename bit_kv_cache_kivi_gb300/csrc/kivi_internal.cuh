@@ -83,14 +83,15 @@ __device__ __forceinline__ void seq_counts(const SeqLens& s, int b, int R, int p
 // a caller's override (0 = automatic).
 struct SplitCfg {
   int budget, max_splits, override_splits;
+  int min_tiles;  // packed tiles per automatic split, at least
 };
 
 // How decode attention covers one sequence of length l: tail splits of
 // kTailTok tokens from t_tail = 32 floor(nq_v / 32) (CUDA cores), then packed
 // splits of `chunk` tokens over the tiles below t_tail (tensor cores).
 // Automatic packed splits fill the budget beside the tail splits, with at
-// least 8 tiles and a multiple of four each (the four warps of a CTA get
-// equal shares); an override asks for that many splits in all.  When the
+// least min_tiles tiles and a multiple of four each (the four warps of a CTA
+// get equal shares); an override asks for that many splits in all.  When the
 // budget cannot hold a tail split beside one packed split, the tail rides on
 // the last packed split (tail_fused, no tail splits).
 struct SeqPlan {
@@ -122,14 +123,14 @@ __host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const Spl
   int per;  // tiles per packed split
   if (sc.override_splits > 0) {
     int s = sc.override_splits - p.tail_splits;
-    if (s > smax) s = smax;
+    if (s > sc.max_splits - p.tail_splits) s = sc.max_splits - p.tail_splits;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
     per = (tiles + s - 1) / s;
   } else {
     per = (tiles + smax - 1) / smax;
     per = (per + 3) / 4 * 4;
-    if (per < 8) per = 8;
+    if (per < sc.min_tiles) per = sc.min_tiles;
   }
   p.chunk = per * 32;
   p.splits = p.tail_splits + (tt + p.chunk - 1) / p.chunk;  // no empty split

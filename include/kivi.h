@@ -287,12 +287,19 @@ kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
  * 32-token tiles.  The automatic choice keeps the whole grid within one wave
  * of a 152-SM GB300 (four CTAs per SM; three at 4 bits with more than four
  * query heads per KV head, two at 8 bits), with at least eight tiles per
- * packed split and a multiple of four.  An override n asks for n splits in all; it
- * is clamped to the workspace bound, to one packed split per 32-token tile
+ * packed split and a multiple of four.  With the overlap on (see
+ * kivi_set_attention_overlap) the automatic choice takes half that budget
+ * and at least 64 tiles per packed split, and rides the tail on the packed
+ * split when the budget holds no tail split beside it: the CTAs of
+ * consecutive launches then share the SMs, and fewer, longer splits pay the
+ * fixed cost of a split (query tables, first tile, merge) fewer times.  An
+ * override n asks for n splits in all, with or without the overlap; it is
+ * clamped to the workspace bound, to one packed split per 32-token tile
  * and to at least one packed split. */
 kivi_status kivi_set_attention_splits(kivi_cache *c, int n_splits);
 
-/* Splits the next kivi_decode_attention call will use at length l. */
+/* Splits the next kivi_decode_attention call will use at length l (with the
+ * handle's current overlap setting). */
 int kivi_attention_splits(const kivi_cache *c, int l);
 
 /* Let kivi_decode_attention calls on this handle overlap the kernel enqueued
@@ -305,7 +312,10 @@ int kivi_attention_splits(const kivi_cache *c, int l);
  * enable it only when the work enqueued before each attention call on the
  * stream writes neither that call's q nor this cache -- for instance a
  * sequence of attention calls over caches and queries that were all written
- * earlier.  kivi_decode_step and kivi_decode_attention_static ignore it.
+ * earlier.  The automatic split count changes with it (see
+ * kivi_set_attention_splits), so results may differ in the last bits from
+ * those of the setting off; with an explicit split count they are the same
+ * bit for bit.  kivi_decode_step and kivi_decode_attention_static ignore it.
  * Host only; no device work. */
 kivi_status kivi_set_attention_overlap(kivi_cache *c, int enable);
 

@@ -184,6 +184,18 @@ def test_split_plan_and_workspace(K):
         assert K.kivi_attention_splits(h, 4097) == 3
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
         assert K.kivi_attention_splits(h, 4097) == 9
+        # overlapped launches: half the budget (4) and >= 64 tiles per packed
+        # split -> the tail split and 2 packed splits; an override is planned
+        # the same way with or without the overlap
+        K.kivi_set_attention_splits(h, 0)
+        K.kivi_set_attention_overlap(h, 1)
+        assert K.kivi_attention_splits(h, 4097) == 3
+        for n in (2, 7, 9, 1000):
+            K.kivi_set_attention_splits(h, n)
+            with_ov = K.kivi_attention_splits(h, 4097)
+            K.kivi_set_attention_overlap(h, 0)
+            assert K.kivi_attention_splits(h, 4097) == with_ov == min(n, 9), n
+            K.kivi_set_attention_overlap(h, 1)
     finally:
         K.kivi_cache_destroy(h)
     # long context, R = 128: 8 units -> 76 splits per unit in one wave; the
@@ -192,18 +204,33 @@ def test_split_plan_and_workspace(K):
     c = cfg(K, batch=1, n_kv_heads=8, n_q_heads=32, residual=128, max_tokens=131072)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 131072) == 76
+    # overlapped: budget 38 -> 2 tail splits and 36 packed splits of 116 tiles
+    K.kivi_set_attention_overlap(h, 1)
+    assert K.kivi_attention_splits(h, 131072) == 38
     K.kivi_cache_destroy(h)
     # 320 units: one split per unit fits the wave, so the tail rides on the
     # packed split
     c = cfg(K, batch=80, n_kv_heads=4, n_q_heads=8, residual=128, max_tokens=512)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 450) == 1
+    K.kivi_set_attention_overlap(h, 1)
+    assert K.kivi_attention_splits(h, 450) == 1
+    K.kivi_set_attention_overlap(h, 0)
     # an explicit count keeps separate tail splits: the 130 tail tokens take 3,
     # plus at least one packed split
     K.kivi_set_attention_splits(h, 3)
     assert K.kivi_attention_splits(h, 450) == 4
     K.kivi_cache_destroy(h)
-    # GQA 18 -> five chunks of four query heads
+    # batch 64, 28 / 4 heads (GQA 7, one chunk of 8 heads): 256 units -> a
+    # budget of 2, one tail split beside one packed split; overlapped, the
+    # budget of 1 fuses the tail into the packed split
+    c = cfg(K, batch=64, n_kv_heads=4, n_q_heads=28, max_tokens=2560)
+    h = K.kivi_cache_init(c, _fake_buffers(K))
+    assert K.kivi_attention_splits(h, 2560) == 2
+    K.kivi_set_attention_overlap(h, 1)
+    assert K.kivi_attention_splits(h, 2560) == 1
+    K.kivi_cache_destroy(h)
+    # GQA 18 -> three chunks of at most eight query heads
     c = cfg(K, batch=1, n_kv_heads=1, n_q_heads=18, max_tokens=1024)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 1024) == 5

@@ -1,8 +1,9 @@
 """Attention calls that may overlap the launch before them on the stream
 (kivi_set_attention_overlap) give the same outputs, bit for bit, as
-ordinary launches: eagerly and inside a CUDA graph, over several caches and
-with the same cache (and so the same workspace) called twice in a row; and
-they match the oracle."""
+ordinary launches of the same split plan: eagerly and inside a CUDA graph,
+over several caches and with the same cache (and so the same workspace)
+called twice in a row.  Their own automatic plan (fewer, longer splits)
+matches the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -36,25 +37,33 @@ def test_overlapping_attention_calls(bits, Hq, Hkv, T_, R):
         caches.append(g)
     qs_np = _queries(wl, 3)
     qs = [T.dev(x, wl.q_dtype) for x in qs_np]
-    # ordinary launches: the reference outputs, and the oracle check
     o = T.oracle_cache(wl)
     o.prefill(wl.k, wl.v)
+    refs = [o.attention(T.q_float(x, wl.q_dtype)) for x in qs_np]
+    seq = [(0, 0), (0, 1), (1, 2), (2, 0), (1, 1), (0, 2), (0, 0)]
+
+    def run_seq(outs):
+        for (ci, qi), out in zip(seq, outs):
+            caches[ci].attention(qs[qi], out)
+
+    # An explicit split count plans the same splits with and without the
+    # overlap, so the outputs must agree bit for bit.  Ordinary launches
+    # first: the reference outputs, and the oracle check.
+    for c in caches:
+        c.set_splits(3)
     serial = {}
     for ci in range(3):
         for qi in range(3):
-            out = caches[ci].attention(qs[qi])
-            serial[ci, qi] = out.clone()
+            serial[ci, qi] = caches[ci].attention(qs[qi]).clone()
     torch.cuda.synchronize()
     for qi in range(3):
-        err = T.attn_err(T.out_float(serial[0, qi]), o.attention(T.q_float(qs_np[qi], wl.q_dtype)))
+        err = T.attn_err(T.out_float(serial[0, qi]), refs[qi])
         assert err <= T.ATTN_TOL, err
     # overlapping launches: cache 0 twice in a row (one workspace), then the others
-    seq = [(0, 0), (0, 1), (1, 2), (2, 0), (1, 1), (0, 2), (0, 0)]
     for c in caches:
         c.set_overlap(True)
     outs = [torch.empty_like(qs[0]) for _ in seq]
-    for (ci, qi), out in zip(seq, outs):
-        caches[ci].attention(qs[qi], out)
+    run_seq(outs)
     torch.cuda.synchronize()
     for (ci, qi), out in zip(seq, outs):
         assert torch.equal(out, serial[ci, qi]), (ci, qi)
@@ -62,8 +71,7 @@ def test_overlapping_attention_calls(bits, Hq, Hkv, T_, R):
     outs_g = [torch.zeros_like(qs[0]) for _ in seq]
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        for (ci, qi), out in zip(seq, outs_g):
-            caches[ci].attention(qs[qi], out)
+        run_seq(outs_g)
     for _ in range(2):
         for out in outs_g:
             out.zero_()
@@ -71,6 +79,24 @@ def test_overlapping_attention_calls(bits, Hq, Hkv, T_, R):
         torch.cuda.synchronize()
         for (ci, qi), out in zip(seq, outs_g):
             assert torch.equal(out, serial[ci, qi]), (ci, qi)
+    del graph
+    # the automatic plan of overlapped launches (fewer, longer splits): the
+    # oracle's outputs within tolerance, eagerly and replayed from a graph
+    for c in caches:
+        c.set_splits(0)
+    outs_a = [torch.empty_like(qs[0]) for _ in seq]
+    run_seq(outs_a)
+    torch.cuda.synchronize()
+    for (ci, qi), out in zip(seq, outs_a):
+        err = T.attn_err(T.out_float(out), refs[qi])
+        assert err <= T.ATTN_TOL, (ci, qi, err)
+    outs_ag = [torch.zeros_like(qs[0]) for _ in seq]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run_seq(outs_ag)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a_, b_ in zip(outs_a, outs_ag):
+        assert torch.equal(a_, b_)
     for c in caches:
         c.set_overlap(False)
-
