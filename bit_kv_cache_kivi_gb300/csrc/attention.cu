@@ -149,11 +149,12 @@ template <int BITS>
 struct TileBuf {
   uint32_t kc[128 * BITS];                // key codes
   uint32_t vc[128 * BITS];                // value codes (group-interleaved rows)
-  uint32_t sk[64], zk[64];
+  uint32_t sk[64];                        // key scales (the key zeros are not staged)
   uint32_t sv[64], zv[64];
   uint32_t outl[outlier_block_bytes(kMaxOutliers) / 4];  // outlier block, when the cache keeps outliers
 };
 constexpr int kMaxStages = 6;  // staged tiles per warp, at most
+constexpr int kBetaTiles = 32;  // tiles of a warp whose beta = zK x q is held at once
 
 // The packed splits' shared memory: per-warp rings of S staged tiles of
 // `stride` bytes (the cache's tile size: a stage mirrors a tile byte for byte;
@@ -169,6 +170,9 @@ struct PackedState {
   uint4 qb[NB][4][8][4];                  // q hi / lo (words of a quarter in the order 0, 2, 1, 3)
   float qscale[kNH];                      // 2^E_j * softmax scale * log2(e)
   float qinv[kNH];                        // 2^-E_j: max |q_j| * 2^-E_j lies in [0.5, 1)
+  // beta = zK x q of tile k of warp w at [w][k mod kBetaTiles][head hd]
+  // (hd = tig with one key block, 2 tig + nb with two)
+  float beta[kWarps][kBetaTiles][4 * NB];
   unsigned long long bar[kWarps][kMaxStages];
 };
 
@@ -229,7 +233,7 @@ struct SmemView {
   }
 };
 static_assert(kWarps * kNH * kHeadDim * 4 <= 2 * kTailTok * kHeadDim, "tail merge areas");
-// (a warp's merge area takes 4 KB: its S >= 2 stages of >= 3 KB hold it;
+// (a warp's merge area takes 4 KB: its S >= 2 stages of >= 2.75 KB hold it;
 // two heads' q take 1 KB of its stage 1)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -425,8 +429,9 @@ __device__ __noinline__ void tail_split(const CacheView& cv, const AttnArgs& a, 
     mbar_expect_tx(&ts.bar, bytes);
     for (int gi = 0; gi < ngk; ++gi) {
       const uint8_t* tile = tile_at<BITS>(cv, unit, tile0 + gi);
-      bulk_g2s(ts.kpk[gi], tile, kGroup * RB, &ts.bar);
-      bulk_g2s(ts.kg[gi], tile + kOffSk<BITS>, 4 * kHeadDim, &ts.bar);  // scales, then zeros
+      bulk_g2s(ts.kpk[gi], tile + kOffKc<BITS>, kGroup * RB, &ts.bar);
+      bulk_g2s(ts.kg[gi][0], tile + kOffSk<BITS>, 2 * kHeadDim, &ts.bar);  // scales
+      bulk_g2s(ts.kg[gi][1], tile + kOffZk, 2 * kHeadDim, &ts.bar);        // zeros
       if (ob) bulk_g2s(ts.ko[gi], tile + kTileBytes<BITS>, ob, &ts.bar);
     }
     for (int gi = 0; gi < ngv; ++gi) {
@@ -793,45 +798,15 @@ __device__ __forceinline__ int score_row(int g) { return (g & 3) + 8 * (g >> 2);
 template <int BITS, int NB>
 __device__ __forceinline__ void key_scores(const PackedState<NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
                                            const float (&ks)[NB], const float (&mb)[NB], int n_out,
-                                           const QRows& qr, float (&sc)[NB][4]) {
+                                           const QRows& qr, const float* brow, float (&sc)[NB][4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
-  // ---- beta = zK x q.  The A operand of a quarter is its four zero-point
-  //      words Z0..Z3 as loaded (rows g: Z0, Z2; rows g + 8: Z1, Z3); one
-  //      MMA takes the q words of Z0 / Z2 (its rows g are beta's share), a
-  //      second the q words of Z1 / Z3 (its rows g + 8), so
-  //      beta = D_a[g, (tig, hi)] + D_a[g, (tig, lo)] + D_b[g + 8, ..] ----
-  float kbm[NB];  // beta * ks - mb, the score offset of the tile
-  {
-    float ba[NB][4], bb[NB][4];
-#pragma unroll
-    for (int blk = 0; blk < kBlocks<BITS>; ++blk) {
-      uint32_t P[8];
-      pair_words<BITS>(tb.zk, tig, blk, P);
-#pragma unroll
-      for (int qq = 0; qq < kQuartersPerBlock<BITS>; ++qq) {
-        const int quarter = kQuartersPerBlock<BITS> * blk + qq;
-        const uint32_t* Z = P + 4 * qq;
-#pragma unroll
-        for (int nb = 0; nb < NB; ++nb) {
-          const uint4 qb = ws.qb[nb][quarter][g][tig];  // q words of Z0, Z2, Z1, Z3
-          if (quarter == 0) {
-            mma_acc<true>(ba[nb], Z[0], Z[1], Z[2], Z[3], qb.x, qb.y);
-            mma_acc<true>(bb[nb], Z[0], Z[1], Z[2], Z[3], qb.z, qb.w);
-          } else {
-            mma_acc<false>(ba[nb], Z[0], Z[1], Z[2], Z[3], qb.x, qb.y);
-            mma_acc<false>(bb[nb], Z[0], Z[1], Z[2], Z[3], qb.z, qb.w);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int nb = 0; nb < NB; ++nb) {
-      // one key block: head tig's beta is its (hi, lo) columns; two key
-      // blocks: head 2 tig + nb's beta is column nb of both parts
-      const float beta = NB == 1 ? (ba[0][0] + ba[0][1]) + (bb[0][2] + bb[0][3])
-                                 : (ba[0][nb] + ba[NB - 1][nb]) + (bb[0][2 + nb] + bb[NB - 1][2 + nb]);
-      kbm[nb] = fmaf(beta, ks[nb], -mb[nb]);
-    }
+  float kbm[NB];  // beta * ks - mb, the score offset of the tile (beta from brow, see beta_mma)
+  if constexpr (NB == 1) {
+    kbm[0] = fmaf(brow[tig], ks[0], -mb[0]);
+  } else {
+    const float2 b2 = *reinterpret_cast<const float2*>(brow + 2 * tig);
+    kbm[0] = fmaf(b2.x, ks[0], -mb[0]);
+    kbm[NB - 1] = fmaf(b2.y, ks[NB - 1], -mb[NB - 1]);
   }
 
   // ---- scores S = codes x Q' + beta ----
@@ -1249,39 +1224,96 @@ __device__ void build_q_tables(const SmemView<BITS, NB>& sv, const AttnArgs& a, 
   fence_proxy_async();  // q staged in stage buffers that bulk copies fill next
 }
 
-// The stage buffer mirrors the packed tile byte for byte.
-static_assert(offsetof(TileBuf<2>, outl) == kTileBytes<2> && offsetof(TileBuf<4>, outl) == kTileBytes<4> &&
-                  offsetof(TileBuf<8>, outl) == kTileBytes<8>, "stage = tile (+ the largest outlier block)");
-static_assert(offsetof(TileBuf<8>, vc) == kOffVc<8> && offsetof(TileBuf<8>, sk) == kOffSk<8> &&
-              offsetof(TileBuf<8>, zv) == kOffZv<8>, "stage layout (8 bits)");
-static_assert(offsetof(TileBuf<2>, vc) == kOffVc<2> && offsetof(TileBuf<2>, sk) == kOffSk<2> &&
-              offsetof(TileBuf<2>, zk) == kOffZk<2> && offsetof(TileBuf<2>, sv) == kOffSv<2> &&
-              offsetof(TileBuf<2>, zv) == kOffZv<2>, "stage layout (2 bits)");
-static_assert(offsetof(TileBuf<3>, vc) == kOffVc<3> && offsetof(TileBuf<3>, sk) == kOffSk<3> &&
-              offsetof(TileBuf<3>, zk) == kOffZk<3> && offsetof(TileBuf<3>, sv) == kOffSv<3> &&
-              offsetof(TileBuf<3>, zv) == kOffZv<3> && offsetof(TileBuf<3>, outl) == kTileBytes<3>,
-              "stage layout (3 bits)");
-static_assert(offsetof(TileBuf<4>, vc) == kOffVc<4> && offsetof(TileBuf<4>, sk) == kOffSk<4> &&
-              offsetof(TileBuf<4>, zk) == kOffZk<4> && offsetof(TileBuf<4>, sv) == kOffSv<4> &&
-              offsetof(TileBuf<4>, zv) == kOffZv<4>, "stage layout (4 bits)");
+// The stage buffer mirrors the packed tile from kStageOff on, byte for byte.
+template <int BITS>
+constexpr bool kStageMirrorsTile =
+    offsetof(TileBuf<BITS>, vc) == kOffVc<BITS> - kStageOff && offsetof(TileBuf<BITS>, sk) == kOffSk<BITS> - kStageOff &&
+    offsetof(TileBuf<BITS>, sv) == kOffSv<BITS> - kStageOff && offsetof(TileBuf<BITS>, zv) == kOffZv<BITS> - kStageOff &&
+    offsetof(TileBuf<BITS>, outl) == kTileBytes<BITS> - kStageOff && kOffKc<BITS> == kStageOff;
+static_assert(kStageMirrorsTile<2> && kStageMirrorsTile<3> && kStageMirrorsTile<4> && kStageMirrorsTile<8>,
+              "stage layout");
 
-// Copy source of one (batch, kv-head) unit: its first packed tile.
+// The packed tiles of one (batch, kv-head) unit: tile 0, the tile stride, and
+// the bytes a stage takes (from kStageOff to the tile's end).
 struct UnitSrc {
   const uint8_t* tiles;
-  uint32_t tile_bytes;
+  uint32_t stride;
+  uint32_t copy;
 };
 
 template <int BITS>
 __device__ __forceinline__ UnitSrc unit_src(const CacheView& cv, long unit) {
-  return UnitSrc{tile_at<BITS>(cv, unit, 0), (uint32_t)cv.tile_bytes};
+  return UnitSrc{tile_at<BITS>(cv, unit, 0), (uint32_t)cv.tile_bytes, (uint32_t)(cv.tile_bytes - kStageOff)};
 }
 
 // One bulk copy of packed tile `tile` into a stage (one lane).
 template <int BITS>
 __device__ __forceinline__ void issue_tile(TileBuf<BITS>& tb, unsigned long long* bar, const UnitSrc& u,
                                            int tile) {
-  mbar_expect_tx(bar, u.tile_bytes);
-  bulk_g2s(&tb, u.tiles + (long)tile * u.tile_bytes, u.tile_bytes, bar);
+  mbar_expect_tx(bar, u.copy);
+  bulk_g2s(&tb, u.tiles + (long)tile * u.stride + kStageOff, u.copy, bar);
+}
+
+// beta = zK x q of the key group of each tile does not depend on the token,
+// so it is taken apart from the scores, for sixteen tiles of a warp per MMA:
+// rows g and g + 8 of the A operand are the key zeros of tiles k0 + g and
+// k0 + g + 8 of the warp, read from global memory (the stages do not hold
+// them), k runs over the channels of a quarter, and B is the q table of the
+// quarter (q hi / lo, the words of zero-point words 0 and 2, then 1 and 3).
+// Lane (g, tig) loads, of the zero vector (channel-pair order, see
+// pair_words), the 16-byte chunk zk_chunk(tig, quarter): the words Z0..Z3
+// that its A fragments take.  Rows past the warp's last tile load zeros.
+template <int BITS>
+__device__ __forceinline__ int zk_chunk(int tig, int q) {
+  // pair_words: block q >> 1, words 4 (q & 1) .. + 3 of pair block tig + 4
+  // (q >> 1) at 2 and 3 bits; block q, pair block tig + 4 q at 4 bits; the
+  // four words from 16 tig + 4 q at 8 bits
+  return BITS <= 3 ? 2 * tig + 8 * (q >> 1) + (q & 1) : (BITS == 4 ? tig + 4 * q : 4 * tig + q);
+}
+
+template <int BITS>
+__device__ __forceinline__ void load_zk(const UnitSrc& us, int t_first, int n_mine, int k0, int g, int tig,
+                                        uint4 (&z)[2][4]) {
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int k = k0 + g + 8 * r;
+    const uint4* v = reinterpret_cast<const uint4*>(us.tiles + (long)(t_first + kWarps * k) * us.stride + kOffZk);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      z[r][q] = k < n_mine ? __ldg(v + zk_chunk<BITS>(tig, q)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The MMAs of one sixteen-tile block: D[row][column] accumulates beta of the
+// row's tile for the table's column (one key block: (head, hi / lo); two:
+// head, one table per part), summed over the parts into the warp's beta rows
+// (k0 mod kBetaTiles) + g and + g + 8.
+template <int NB>
+__device__ __forceinline__ void beta_mma(const PackedState<NB>& ws, const uint4 (&z)[2][4], int g, int tig,
+                                         float* rows) {
+  float D[NB][4];
+#pragma unroll
+  for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) D[nb][i] = 0.0f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+      const uint4 qb = ws.qb[nb][q][g][tig];
+      mma16816(D[nb], z[0][q].x, z[1][q].x, z[0][q].z, z[1][q].z, qb.x, qb.y);
+      mma16816(D[nb], z[0][q].y, z[1][q].y, z[0][q].w, z[1][q].w, qb.z, qb.w);
+    }
+  if constexpr (NB == 1) {
+    rows[g * 4 + tig] = D[0][0] + D[0][1];
+    rows[(g + 8) * 4 + tig] = D[0][2] + D[0][3];
+  } else {
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      rows[g * 8 + 2 * tig + i] = D[0][i] + D[NB - 1][i];
+      rows[(g + 8) * 8 + 2 * tig + i] = D[0][2 + i] + D[NB - 1][2 + i];
+    }
+  }
 }
 
 // The same from a source address, issued by the lanes where `p` holds (one
@@ -1336,11 +1368,25 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
   // append runs and issues every copy after it.
   const bool wait_first = a.pdl == kPdlAll;
   if (!wait_first && lane == 0 && issued > 0) issue_tile<BITS>(st(0), &bars[0], us, t_first);
+  // the key zeros of the first sixteen tiles are loaded before the tables
+  // are built (unless the tiles may still be written by the kernel before)
+  uint4 z[2][4];
+  if (!wait_first) load_zk<BITS>(us, t_first, n_mine, 0, g, tig, z);
   build_q_tables<BITS, NB>(sv, a, qv8);
   __syncthreads();
   if (wait_first) grid_dependency_wait();
   if (lane == 0)
     for (int k = wait_first ? 0 : 1; k < issued; ++k) issue_tile<BITS>(st(k), &bars[k], us, t_first + kWarps * k);
+  float* const brows = &ws.beta[warp][0][0];
+  if (n_mine > 0) {
+    if (wait_first) load_zk<BITS>(us, t_first, n_mine, 0, g, tig, z);
+    beta_mma<NB>(ws, z, g, tig, brows);
+    if (n_mine > 16) {
+      load_zk<BITS>(us, t_first, n_mine, 16, g, tig, z);
+      beta_mma<NB>(ws, z, g, tig, brows + 16 * 4 * NB);
+    }
+    __syncwarp();
+  }
   float ks[NB], m_run[NB];
 #pragma unroll
   for (int nb = 0; nb < NB; ++nb) {
@@ -1373,15 +1419,15 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
       float sc[NB][4], mb[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) mb[nb] = 0.0f;
-      key_scores<BITS, NB>(ws, st(0), g, tig, ks, mb, cv.n_out, qr, sc);
+      key_scores<BITS, NB>(ws, st(0), g, tig, ks, mb, cv.n_out, qr, brows, sc);
       softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
     }
   }
   int k = 0, sk = 0;     // tile whose values are next, and its stage
   uint32_t parn = 0;     // phase parity of the stage of tile k + 1
   // source of the next tile to stage (tile k + kStages of this warp)
-  const long src_step = (long)kWarps * us.tile_bytes;
-  const uint8_t* next_src = us.tiles + (long)(t_first + kWarps * kStages) * us.tile_bytes;
+  const long src_step = (long)kWarps * us.stride;
+  const uint8_t* next_src = us.tiles + (long)(t_first + kWarps * kStages) * us.stride + kStageOff;
   while (!failed && k + 1 < n_mine) {
     const int sn = sk + 1 == kStages ? 0 : sk + 1;  // stage of tile k + 1
     if (sn == 0) parn ^= 1u;
@@ -1392,13 +1438,26 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
         break;
       }
     }
+    const int kb = (k + 1) % kBetaTiles;  // beta row of tile k + 1
+    if (kb == 0) {
+      // the next block of kBetaTiles tiles (every row of the last one is read)
+      __syncwarp();
+      uint4 zz[2][4];
+      load_zk<BITS>(us, t_first, n_mine, k + 1, g, tig, zz);
+      beta_mma<NB>(ws, zz, g, tig, brows);
+      if (k + 17 < n_mine) {
+        load_zk<BITS>(us, t_first, n_mine, k + 17, g, tig, zz);
+        beta_mma<NB>(ws, zz, g, tig, brows + 16 * 4 * NB);
+      }
+      __syncwarp();
+    }
     float sc[NB][4];
-    key_scores<BITS, NB>(ws, st(sn), g, tig, ks, m_run, cv.n_out, qr, sc);
+    key_scores<BITS, NB>(ws, st(sn), g, tig, ks, m_run, cv.n_out, qr, brows + kb * 4 * NB, sc);
     value_acc<BITS>(st(sk), pb, g, tig, O, Z);
     done = k + 1;
     __syncwarp();  // every lane is done with stage sk
     const bool more = k + kStages < n_mine;
-    issue_tile_if<BITS>(more && lane == 0, st(sk), &bars[sk], next_src, us.tile_bytes);
+    issue_tile_if<BITS>(more && lane == 0, st(sk), &bars[sk], next_src, us.copy);
     next_src += src_step;
     issued += more;
     softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
@@ -1569,7 +1628,7 @@ template <int BITS, int NB>
 __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
     attn_kernel(CacheView cv, AttnArgs a, const SeqLens lens) {
   extern __shared__ __align__(16) unsigned char smem_raw[];  // attn_stages: the tail or the packed layout
-  const SmemView<BITS, NB> sv{smem_raw, a.stages, (uint32_t)cv.tile_bytes};
+  const SmemView<BITS, NB> sv{smem_raw, a.stages, (uint32_t)(cv.tile_bytes - kStageOff)};
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
   __shared__ bool s_last;
 
@@ -1737,12 +1796,12 @@ template <int BITS, int NB>
 cudaError_t launch_bits(const dim3& grid, const CacheView& cv, AttnArgs a, const SeqLens& lens,
                         cudaStream_t st) {
   size_t smem = 0, cap = 0;
-  a.stages = attn_stages<BITS, NB>((uint32_t)cv.tile_bytes, &smem);
+  a.stages = attn_stages<BITS, NB>((uint32_t)(cv.tile_bytes - kStageOff), &smem);
   // The shared-memory opt-in is a per-device function attribute: set to the
   // largest size any outlier count asks for (the same on every call, so
   // that calls from several host threads cannot shrink it under another's
   // launch); setting it costs a host call only.
-  const uint32_t plain = (uint32_t)(cv.tile_bytes - outlier_block_bytes(cv.n_out));
+  const uint32_t plain = (uint32_t)(cv.tile_bytes - kStageOff - outlier_block_bytes(cv.n_out));
   for (int n = 0; n <= kMaxOutliers; ++n) {
     size_t sz = 0;
     attn_stages<BITS, NB>(plain + (uint32_t)outlier_block_bytes(n), &sz);

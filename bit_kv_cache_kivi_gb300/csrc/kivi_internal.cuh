@@ -138,27 +138,33 @@ __host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const Spl
 }
 
 // A packed tile holds everything quantized about tokens [32j, 32j + 32) of a
-// unit, so that one bulk copy stages it:
-//   [0, 32 RB)                key code rows (RB = D * bits / 8 bytes each)
-//   [32 RB, 64 RB)            value code rows (group-interleaved)
-//   kOffSk: scale[D] (f16)    of the tile's key group, one per channel
-//   kOffZk: zero[D]
+// unit:
+//   kOffZk: zero[D] (f16)     of the tile's key group, one per channel
+//   kOffKc: 32 key code rows  (RB = D * bits / 8 bytes each)
+//   kOffVc: 32 value code rows (group-interleaved)
+//   kOffSk: scale[D]          of the tile's key group
 //   kOffSv: scale[32][D / G]  value groups, per token
 //   kOffZv: zero[32][D / G]
+//   then the outlier block, if the cache keeps outlier channels.
+// The decode attention stages [kStageOff, tile end) with one bulk copy; it
+// reads the key zeros apart, for sixteen tiles at a time (see beta_pass),
+// so they lead the tile.
 template <int BITS>
 constexpr int kRowBytes = kHeadDim * BITS / 8;
+constexpr int kOffZk = 0;
+constexpr int kStageOff = 2 * kHeadDim;
 template <int BITS>
-constexpr int kOffVc = kGroup * kRowBytes<BITS>;
+constexpr int kOffKc = kStageOff;
 template <int BITS>
-constexpr int kOffSk = 2 * kGroup * kRowBytes<BITS>;
+constexpr int kOffVc = kOffKc<BITS> + kGroup * kRowBytes<BITS>;
 template <int BITS>
-constexpr int kOffZk = kOffSk<BITS> + 2 * kHeadDim;
+constexpr int kOffSk = kOffKc<BITS> + 2 * kGroup * kRowBytes<BITS>;
 template <int BITS>
-constexpr int kOffSv = kOffSk<BITS> + 4 * kHeadDim;
+constexpr int kOffSv = kOffSk<BITS> + 2 * kHeadDim;
 template <int BITS>
-constexpr int kOffZv = kOffSk<BITS> + 6 * kHeadDim;
+constexpr int kOffZv = kOffSk<BITS> + 4 * kHeadDim;
 template <int BITS>
-constexpr int kTileBytes = kOffSk<BITS> + 8 * kHeadDim;
+constexpr int kTileBytes = kOffSk<BITS> + 6 * kHeadDim;
 static_assert(kTileBytes<2> == 3072 && kTileBytes<3> == 4096 && kTileBytes<4> == 5120 &&
                   kTileBytes<8> == 9216,
               "tile sizes");

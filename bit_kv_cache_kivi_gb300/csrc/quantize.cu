@@ -388,7 +388,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
       }
       __syncwarp();
       uint8_t* tile = tile_at<BITS>(cv, unit, chunk);
-      uint4* gdst = reinterpret_cast<uint4*>(tile);
+      uint4* gdst = reinterpret_cast<uint4*>(tile + kOffKc<BITS>);
       const uint4* ssrc = reinterpret_cast<const uint4*>(s_codes);
       constexpr int CPRB = RB / 16;  // 16-byte chunks per code row
 #pragma unroll
@@ -445,7 +445,7 @@ __device__ __forceinline__ void quantize_chunk(const CacheView& cv, const uint4*
           w[2] = pack_halves(v[4], v[6]);
           w[3] = pack_halves(v[5], v[7]);
         }
-        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + (par ? kOffZk<BITS> : kOffSk<BITS>)) + c8) =
+        *reinterpret_cast<uint4*>(reinterpret_cast<__half*>(tile + (par ? kOffZk : kOffSk<BITS>)) + c8) =
             make_uint4(w[0], w[1], w[2], w[3]);
       }
     } else {
@@ -815,11 +815,11 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
           uint32_t q = (c & 3u) << (2 * (d & 3));
           q |= __shfl_xor_sync(kFull, q, 1);
           q |= __shfl_xor_sync(kFull, q, 2);
-          if ((d & 3) == 0) tile[j * RB + (d >> 2)] = (uint8_t)q;
+          if ((d & 3) == 0) tile[kOffKc<BITS> + j * RB + (d >> 2)] = (uint8_t)q;
           if (c >> 2) atomicOr(&s_kh[j][m & 3], 1u << hpos);
         }
         __syncthreads();
-        reinterpret_cast<uint32_t*>(tile + (d >> 2) * RB + kHiPlane3)[d & 3] = s_kh[d >> 2][d & 3];
+        reinterpret_cast<uint32_t*>(tile + kOffKc<BITS> + (d >> 2) * RB + kHiPlane3)[d & 3] = s_kh[d >> 2][d & 3];
         __syncthreads();  // s_kh is cleared again by the next group
       } else {
 #pragma unroll
@@ -827,11 +827,11 @@ append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict
           uint32_t q = (slot >= 0 ? 0u : encode(xs[j], p, L)) << (BITS * (d % PER_BYTE));
 #pragma unroll
           for (int off = 1; off < PER_BYTE; off <<= 1) q |= __shfl_xor_sync(kFull, q, off);
-          if (d % PER_BYTE == 0) tile[j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
+          if (d % PER_BYTE == 0) tile[kOffKc<BITS> + j * RB + krow_byte<BITS>(j, d / PER_BYTE)] = (uint8_t)q;
         }
       }
       reinterpret_cast<__half*>(tile + kOffSk<BITS>)[kscale_pos<BITS>(d)] = p.sh;
-      reinterpret_cast<__half*>(tile + kOffZk<BITS>)[kscale_pos<BITS>(d)] = p.zh;
+      reinterpret_cast<__half*>(tile + kOffZk)[kscale_pos<BITS>(d)] = p.zh;
       if (cv.n_out > 0) __syncthreads();  // s_ch is reused by the next group
     }
   }

@@ -440,13 +440,16 @@ class KiviCache:
         # as_strided offsets count from the start of the storage, and the
         # tile buffer may itself be a view into a larger allocation
         b8, b16 = u8.storage_offset(), i16.storage_offset()
-        o_sk = 2 * G * rb  # byte offset of the key scales in a tile
-        out = {"codes_k": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8),
-               "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8 + G * rb),
+        # byte offsets in a tile: key zeros, key codes, value codes, key
+        # scales, value scales, value zeros
+        o_kc = 2 * D
+        o_sk = o_kc + 2 * G * rb
+        out = {"codes_k": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8 + o_kc),
+               "codes_v": u8.as_strided((B, H, nt, G, rb), st8 + (rb, 1), b8 + o_kc + G * rb),
                "scale_k": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + o_sk // 2),
-               "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 2 * D) // 2),
-               "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 4 * D) // 2),
-               "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 6 * D) // 2)}
+               "zero_k": i16.as_strided((B, H, nt, D), st16 + (1,), b16),
+               "scale_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 2 * D) // 2),
+               "zero_v": i16.as_strided((B, H, nt, D), st16 + (1,), b16 + (o_sk + 4 * D) // 2)}
         n = c.outlier_channels
         if n:  # the outlier block after the base tile: indices, then values [G][n]
             o_ob = 2 * G * rb + 8 * D

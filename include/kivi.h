@@ -52,12 +52,16 @@
  * RB = D*b/8 bytes per packed row):
  *   tiles   [B][H][T/G] tiles of 2*G*RB + 8*D bytes: tile j holds all the
  *           quantized state of tokens [G*j, G*j + G) of a (batch, kv-head):
- *             [0, G*RB)            key code rows, token-major
- *             [G*RB, 2*G*RB)       value code rows, token-major
- *             then f16 arrays:     key scale [D], key zero [D] (the tile's
- *                                  key group, one per channel),
+ *             [0, 2*D)             key zero [D] (f16; the tile's key group,
+ *                                  one per channel)
+ *             [2*D, 2*D + G*RB)    key code rows, token-major
+ *             then                 value code rows, token-major (G*RB bytes)
+ *             then f16 arrays:     key scale [D],
  *                                  value scale [G][D/G], value zero [G][D/G]
  *                                  (one per G channels per token)
+ *           (the key zeros lead: the decode attention stages the rest of a
+ *           tile with one bulk copy and reads the zeros of sixteen tiles at
+ *           once for the term zero x q)
  *           With kivi_config.outlier_channels = n > 0, a tile ends with an
  *           outlier block of 16 + 64*n bytes: the n channel indices (u8,
  *           largest max |k| first, zero padded to 16 bytes), then
