@@ -210,19 +210,22 @@ int max_splits(const kivi_config& c) {
 
 // The cache's split configuration (kivi::make_plan plans one length with it).
 // Launches that overlap the attention launch before them (`overlapped`)
-// take half the budget and at least 64 tiles per packed split: the CTAs of
-// consecutive launches then share the SMs, and the cost that every split
-// pays once (its q tables, the wait for its first tile, its share of the
-// merge) weighs more than the CTAs a launch leaves idle.  Measured on a
-// GB300 with overlapped launches: the Llama-3-8B decode shape (8 units of
-// 128 tiles per sequence) takes 8.9 us with 2 packed splits per unit
-// against 10.9 us with 8; 131k tokens (4096 tiles, 8 units) 23.1 us with
-// 37 against 25.3 us with 75.
+// take half the budget and at least 64 tiles per packed split, and a tail
+// of one split rides on the last packed split: the CTAs of consecutive
+// launches then share the SMs, and the cost that every split pays once (its
+// q tables, the wait for its first tile, its share of the merge) weighs
+// more than the CTAs a launch leaves idle.  Measured on a GB300 with
+// overlapped launches: the Llama-3-8B decode shape (8 units of 128 tiles
+// per sequence) takes 8.6 us with 2 packed splits per unit and the tail
+// fused, 8.9 us with a separate tail split, 10.9 us with 8 packed splits;
+// 131k tokens (4096 tiles, 8 units) 23.2 us with 35 packed splits against
+// 25.3 us with 74 (its three tail splits stay separate: fused, 30 us).
 kivi::SplitCfg split_cfg(const kivi_cache* c, bool overlapped) {
   kivi::SplitCfg sc;
   const int budget = split_budget(c->cfg);
   sc.budget = overlapped ? (budget / 2 > 1 ? budget / 2 : 1) : budget;
   sc.min_tiles = overlapped ? 64 : 8;
+  sc.fuse_single_tail = overlapped ? 1 : 0;
   sc.max_splits = max_splits(c->cfg);
   sc.override_splits = c->splits_override;
   return sc;

@@ -83,7 +83,8 @@ __device__ __forceinline__ void seq_counts(const SeqLens& s, int b, int R, int p
 // a caller's override (0 = automatic).
 struct SplitCfg {
   int budget, max_splits, override_splits;
-  int min_tiles;  // packed tiles per automatic split, at least
+  int min_tiles;         // packed tiles per automatic split, at least
+  int fuse_single_tail;  // automatic plans ride a one-split tail on the last packed split
 };
 
 // How decode attention covers one sequence of length l: tail splits of
@@ -92,8 +93,9 @@ struct SplitCfg {
 // Automatic packed splits fill the budget beside the tail splits, with at
 // least min_tiles tiles and a multiple of four each (the four warps of a CTA
 // get equal shares); an override asks for that many splits in all.  When the
-// budget cannot hold a tail split beside one packed split, the tail rides on
-// the last packed split (tail_fused, no tail splits).
+// budget cannot hold a tail split beside one packed split, or the tail is one
+// split and fuse_single_tail is set, the tail rides on the last packed split
+// (tail_fused, no tail splits).
 struct SeqPlan {
   int l, nq_k, nq_v, t_tail, tail_splits, splits, chunk, tail_fused;
 };
@@ -113,7 +115,8 @@ __host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const Spl
     p.chunk = 32;
     return p;
   }
-  if (sc.override_splits <= 0 && sc.budget < p.tail_splits + 1) {
+  if (sc.override_splits <= 0 &&
+      (sc.budget < p.tail_splits + 1 || (sc.fuse_single_tail && p.tail_splits == 1))) {
     p.tail_fused = 1;
     p.tail_splits = 0;
   }

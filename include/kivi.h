@@ -293,8 +293,9 @@ kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
  * query heads per KV head, two at 8 bits), with at least eight tiles per
  * packed split and a multiple of four.  With the overlap on (see
  * kivi_set_attention_overlap) the automatic choice takes half that budget
- * and at least 64 tiles per packed split, and rides the tail on the packed
- * split when the budget holds no tail split beside it: the CTAs of
+ * and at least 64 tiles per packed split, and rides the tail on the last
+ * packed split when the tail is a single split or the budget holds no tail
+ * split beside it: the CTAs of
  * consecutive launches then share the SMs, and fewer, longer splits pay the
  * fixed cost of a split (query tables, first tile, merge) fewer times.  An
  * override n asks for n splits in all, with or without the overlap; it is

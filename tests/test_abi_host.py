@@ -185,11 +185,11 @@ def test_split_plan_and_workspace(K):
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
         assert K.kivi_attention_splits(h, 4097) == 9
         # overlapped launches: half the budget (4) and >= 64 tiles per packed
-        # split -> the tail split and 2 packed splits; an override is planned
-        # the same way with or without the overlap
+        # split -> 2 packed splits, the one-split tail riding on the last;
+        # an override is planned the same way with or without the overlap
         K.kivi_set_attention_splits(h, 0)
         K.kivi_set_attention_overlap(h, 1)
-        assert K.kivi_attention_splits(h, 4097) == 3
+        assert K.kivi_attention_splits(h, 4097) == 2
         for n in (2, 7, 9, 1000):
             K.kivi_set_attention_splits(h, n)
             with_ov = K.kivi_attention_splits(h, 4097)
