@@ -273,8 +273,8 @@ def run_gpu(args):
 
     # ---------------- timed (steps): the one-call decode step (append, then
     # the attention as a programmatic dependent of the append), K steps per
-    # graph; a first graph of K steps is replayed as warm-up, a second one of
-    # the next K steps is timed
+    # graph, launch i on replica i mod n_rep; a first graph of K steps is
+    # replayed as warm-up, a second one of the next K steps is timed
     def capture_steps():
         g, ctx = torch.cuda.CUDAGraph(), []
         with torch.cuda.graph(g):
@@ -393,7 +393,9 @@ def run_gpu(args):
                          f"({n_rep} x {probe_bytes / 2**20:.0f} MiB), no flush",
                    "context": [int(min(ctx_a + ctx_b)), int(max(ctx_a + ctx_b)) + 1],
                    "timing": "CUDA events around one replay of a CUDA graph of K launches "
-                             "(value: K attention launches; ms_per_step: K decode steps)"},
+                             "(value: K attention launches, each overlapping the one before it "
+                             "(kivi_set_attention_overlap), the same without the overlap beside it; "
+                             "ms_per_step: K decode steps)"},
         "pct_of_peak": round(100 * attn_gbs / peak, 2),
         "tokens_per_s": round(tokens_per_s, 1),
         "flush_window_tokens_per_s": round(B / flush_step_s, 1),

@@ -1632,10 +1632,16 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   __shared__ float s_m[kWarps][kNH], s_l[kWarps][kNH];
   __shared__ bool s_last;
 
-  // A programmatic dependent of this launch (another attention call) may
-  // start its CTAs as this launch's CTAs finish; it waits for this launch
-  // before its own first write.
-  grid_launch_dependents();
+  // Programmatic dependents of this launch (an overlapping attention call,
+  // the next decode step's append) may start early.  An ordinary or an
+  // overlapping launch lets them start at once: it writes nothing they read
+  // (its workspace and out aside, which they wait for before writing), and
+  // every kernel before it has completed or writes nothing it reads.  A
+  // decode step's attention lets them start only once its append has
+  // completed (before the merge below), so that no early start ever runs
+  // ahead of a cache write.
+  const bool step_launch = a.pdl == kPdlAll || a.pdl == kPdlTail;
+  if (!step_launch) grid_launch_dependents();
   const int s = blockIdx.x;
   const int nhc = gridDim.y / cv.H;
   const int h = nhc == 1 ? (int)blockIdx.y : (int)blockIdx.y / nhc;
@@ -1671,7 +1677,8 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   }
   // an overlapping launch waits for the launch before it only here, before
   // its first global write
-  if (a.pdl == kPdlOverlap) grid_dependency_wait();
+  if (a.pdl == kPdlOverlap || step_launch) grid_dependency_wait();
+  if (step_launch) grid_launch_dependents();
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;

@@ -377,16 +377,21 @@ kivi_status append_checks(const kivi_cache* c, const void* k_new, const void* v_
 }
 
 // The launches of a checked one-token append; the lengths grow on success.
-kivi_status append_launch(kivi_cache* c, const void* k_new, const void* v_new, kivi_dtype dtype, void* stream) {
+// trig: the append lets the launch after it (a decode step's attention)
+// start at once; 0: nothing starts before the append completes (see
+// kivi::launch_append).
+kivi_status append_launch(kivi_cache* c, const void* k_new, const void* v_new, kivi_dtype dtype, void* stream,
+                          int trig = 0) {
   kivi::SeqLens sl;
   seq_lens(c, &sl, 1);
   cudaError_t e;
   if (c->cfg.policy == KIVI_POLICY_SHARED) {
     // the one-token case of the multi-token append: a whole group of keys and
     // values is quantized when nq grows, then the token goes to the ring
-    e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, 1, sl, static_cast<cudaStream_t>(stream));
+    e = kivi::launch_append_tokens(view(c), k_new, v_new, (int)dtype, 1, sl, static_cast<cudaStream_t>(stream),
+                                   trig);
   } else {
-    e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, sl, static_cast<cudaStream_t>(stream));
+    e = kivi::launch_append(view(c), k_new, v_new, (int)dtype, sl, static_cast<cudaStream_t>(stream), trig);
   }
   kivi_status st = cuda_status(e);
   if (st == KIVI_OK) grow(c, 1);
@@ -571,7 +576,9 @@ KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const vo
     if (z != KIVI_OK) return z;
     c->ws_ready = workspace;
   }
-  kivi_status s1 = append_launch(c, k_new, v_new, kv_dtype, stream);
+  // the append lets the attention start at once (its prologue, and the
+  // packed splits on most steps, run beside the append)
+  kivi_status s1 = append_launch(c, k_new, v_new, kv_dtype, stream, 1);
   if (s1 != KIVI_OK) return s1;
   kivi::AttnArgs a;
   kivi::SeqLens sl;

@@ -255,15 +255,19 @@ cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const vo
 
 // One token appended to every sequence (Algorithm 1 policy), at position
 // lens(b) of sequence b.
+// trig: let a programmatic dependent (a decode step's attention) start at
+// once; 0: no dependent launch starts before the append completes.
 cudaError_t launch_append(const CacheView& cv, const void* k, const void* v,
-                          int dtype, const SeqLens& lens, cudaStream_t st);
+                          int dtype, const SeqLens& lens, cudaStream_t st, int trig = 0);
 
 // n tokens appended to every sequence (k, v: [B][H][n][D] of dtype), to a
 // sequence of length l0 = lens(b): its key groups [nq_k(l0), nq_k(l0 + n))
 // and value tokens [nq_v(l0), nq_v(l0 + n)) become quantized, then its last
-// min(n, W) tokens go to the ring.
+// min(n, W) tokens go to the ring.  trig: the ring kernel lets a dependent
+// launch (a decode step's attention) start at once; 0: none starts before
+// it completes.
 cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype,
-                                 int n, const SeqLens& lens, cudaStream_t st);
+                                 int n, const SeqLens& lens, cudaStream_t st, int trig = 0);
 
 struct AttnArgs {
   const void* q;

@@ -655,8 +655,10 @@ append_quantize_kernel(CacheView cv, const void* __restrict__ kin, const void* _
 template <int DT>
 __global__ void __launch_bounds__(128)
 append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, int n,
-                   const SeqLens lens) {
-  grid_launch_dependents();  // a decode step's attention may start its prologue
+                   const SeqLens lens, int trig) {
+  // a decode step's attention may start its prologue (trig); otherwise no
+  // dependent launch starts before this kernel completes
+  if (trig) grid_launch_dependents();
   const int m = min(n, cv.W);
   const int i = n - m + blockIdx.x;  // input row
   const int h = blockIdx.y, b = blockIdx.z, d = threadIdx.x;
@@ -676,11 +678,14 @@ append_ring_kernel(CacheView cv, const void* __restrict__ kin, const void* __res
 //     t+1-R .. t in slot order: quantize each channel of each group.
 template <int BITS, int DT>
 __global__ void __launch_bounds__(128)
-append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, const SeqLens lens) {
+append_kernel(CacheView cv, const void* __restrict__ kin, const void* __restrict__ vin, const SeqLens lens,
+              int trig) {
   constexpr int L = (1 << BITS) - 1;
   constexpr int RB = kHeadDim * BITS / 8;
   constexpr int PER_BYTE = 8 / BITS;
-  grid_launch_dependents();  // a decode step's attention may start its prologue
+  // trig: a decode step's attention may start its prologue at once; with
+  // trig 0 no dependent launch starts before this kernel completes
+  if (trig) grid_launch_dependents();
   const int h = blockIdx.x, b = blockIdx.y;
   const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
   const long unit = (long)b * cv.H + h;
@@ -861,42 +866,42 @@ cudaError_t prefill_bits(const CacheView& cv, const void* k, const void* v, int 
 
 template <int BITS>
 cudaError_t append_bits(const CacheView& cv, const void* k, const void* v, int dtype, const SeqLens& lens,
-                        cudaStream_t st) {
+                        cudaStream_t st, int trig) {
   const dim3 grid(cv.H, cv.B);
   switch (dtype) {
-    case kF32: append_kernel<BITS, kF32><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
-    case kF16: append_kernel<BITS, kF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
-    default: append_kernel<BITS, kBF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens); break;
+    case kF32: append_kernel<BITS, kF32><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens, trig); break;
+    case kF16: append_kernel<BITS, kF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens, trig); break;
+    default: append_kernel<BITS, kBF16><<<grid, kHeadDim, 0, st>>>(cv, k, v, lens, trig); break;
   }
   return cudaGetLastError();
 }
 
 template <int BITS, int DT>
 cudaError_t append_tokens_dt(const CacheView& cv, const void* k, const void* v, int n, int c_lo, int c_hi,
-                             const SeqLens& lens, cudaStream_t st) {
+                             const SeqLens& lens, cudaStream_t st, int trig) {
   if (c_hi > c_lo) {
     const dim3 grid(c_hi - c_lo, cv.H, cv.B);
     if (cv.n_out > 0) append_quantize_kernel<BITS, DT, true><<<grid, 64, 0, st>>>(cv, k, v, n, c_lo, lens);
     else append_quantize_kernel<BITS, DT, false><<<grid, 64, 0, st>>>(cv, k, v, n, c_lo, lens);
   }
-  append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, n, lens);
+  append_ring_kernel<DT><<<dim3(min(n, cv.W), cv.H, cv.B), kHeadDim, 0, st>>>(cv, k, v, n, lens, trig);
   return cudaGetLastError();
 }
 
 template <int BITS>
 cudaError_t append_tokens_bits(const CacheView& cv, const void* k, const void* v, int dtype, int n, int c_lo,
-                               int c_hi, const SeqLens& lens, cudaStream_t st) {
+                               int c_hi, const SeqLens& lens, cudaStream_t st, int trig) {
   switch (dtype) {
-    case kF32: return append_tokens_dt<BITS, kF32>(cv, k, v, n, c_lo, c_hi, lens, st);
-    case kF16: return append_tokens_dt<BITS, kF16>(cv, k, v, n, c_lo, c_hi, lens, st);
-    default: return append_tokens_dt<BITS, kBF16>(cv, k, v, n, c_lo, c_hi, lens, st);
+    case kF32: return append_tokens_dt<BITS, kF32>(cv, k, v, n, c_lo, c_hi, lens, st, trig);
+    case kF16: return append_tokens_dt<BITS, kF16>(cv, k, v, n, c_lo, c_hi, lens, st, trig);
+    default: return append_tokens_dt<BITS, kBF16>(cv, k, v, n, c_lo, c_hi, lens, st, trig);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void* v, int dtype, int n,
-                                 const SeqLens& lens, cudaStream_t st) {
+                                 const SeqLens& lens, cudaStream_t st, int trig) {
   if (n <= 0) return cudaSuccess;
   // the chunks holding some sequence's [min(nq_k0, nq_v0), max(nq_k1, nq_v1))
   int c_lo = INT_MAX, c_hi = 0;
@@ -912,10 +917,10 @@ cudaError_t launch_append_tokens(const CacheView& cv, const void* k, const void*
   }
   if (c_hi == 0) c_lo = 0;
   switch (cv.bits) {
-    case 2: return append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
-    case 3: return append_tokens_bits<3>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
-    case 4: return append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
-    default: return append_tokens_bits<8>(cv, k, v, dtype, n, c_lo, c_hi, lens, st);
+    case 2: return append_tokens_bits<2>(cv, k, v, dtype, n, c_lo, c_hi, lens, st, trig);
+    case 3: return append_tokens_bits<3>(cv, k, v, dtype, n, c_lo, c_hi, lens, st, trig);
+    case 4: return append_tokens_bits<4>(cv, k, v, dtype, n, c_lo, c_hi, lens, st, trig);
+    default: return append_tokens_bits<8>(cv, k, v, dtype, n, c_lo, c_hi, lens, st, trig);
   }
 }
 
@@ -931,12 +936,12 @@ cudaError_t launch_quantize_prefill(const CacheView& cv, const void* k, const vo
 }
 
 cudaError_t launch_append(const CacheView& cv, const void* k, const void* v, int dtype, const SeqLens& lens,
-                          cudaStream_t st) {
+                          cudaStream_t st, int trig) {
   switch (cv.bits) {
-    case 2: return append_bits<2>(cv, k, v, dtype, lens, st);
-    case 3: return append_bits<3>(cv, k, v, dtype, lens, st);
-    case 4: return append_bits<4>(cv, k, v, dtype, lens, st);
-    default: return append_bits<8>(cv, k, v, dtype, lens, st);
+    case 2: return append_bits<2>(cv, k, v, dtype, lens, st, trig);
+    case 3: return append_bits<3>(cv, k, v, dtype, lens, st, trig);
+    case 4: return append_bits<4>(cv, k, v, dtype, lens, st, trig);
+    default: return append_bits<8>(cv, k, v, dtype, lens, st, trig);
   }
 }
 

@@ -274,6 +274,10 @@ kivi_status kivi_decode_attention(kivi_cache *c, const void *q,
  * G (the append closes the last packed tile) every CTA builds its query
  * tables and then waits; on every other step only the CTAs that read the
  * fp16 tail wait, and the packed splits run beside the append.
+ * The step's attention lets a launch after it start early only once its
+ * append has completed, so that an overlapping attention call enqueued
+ * after the step (kivi_set_attention_overlap) never reads a cache before the
+ * step's write to it lands.  The step ignores the overlap setting.
  * Errors: every check of both halves is made before any launch (nothing runs
  * and the length is unchanged on KIVI_EINVAL, KIVI_EDTYPE, KIVI_ECAPACITY or
  * KIVI_EWORKSPACE).  If the append launches and the attention launch then
@@ -320,7 +324,15 @@ int kivi_attention_splits(const kivi_cache *c, int l);
  * earlier.  The automatic split count changes with it (see
  * kivi_set_attention_splits), so results may differ in the last bits from
  * those of the setting off; with an explicit split count they are the same
- * bit for bit.  kivi_decode_step and kivi_decode_attention_static ignore it.
+ * bit for bit.  kivi_decode_step and kivi_decode_attention_static ignore
+ * it.  Overlapping calls enqueued back to back start one another early, so
+ * a call may run beside any of them: the contract covers all the work
+ * enqueued since the last launch that is not an overlapping attention call
+ * (none of it may write this call's q or this cache).  That launch itself
+ * has completed by then if it is one of this library's: the kernels that
+ * write a cache (prefill, appends) let no launch start before they
+ * complete, except a decode step's own attention, and that attention lets
+ * later launches start only after its append has completed.
  * Host only; no device work. */
 kivi_status kivi_set_attention_overlap(kivi_cache *c, int enable);
 

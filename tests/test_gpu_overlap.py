@@ -100,3 +100,80 @@ def test_overlapping_attention_calls(bits, Hq, Hkv, T_, R):
         assert torch.equal(a_, b_)
     for c in caches:
         c.set_overlap(False)
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+def test_overlapping_calls_after_decode_steps(bits):
+    """Overlapping attention calls mixed with decode steps and plain appends
+    on three caches, across key flushes: an overlapping call that follows a
+    step or an append of its own cache (directly, or behind overlapping
+    calls on other caches) must see that write.  Against the same sequence
+    without the overlap (explicit split counts, so that the plans agree), bit
+    for bit, eagerly and replayed from a CUDA graph; the last outputs match
+    the oracle."""
+    wl = W.synthetic("ovs", B=2, Hq=8, Hkv=2, T=300, R=32, bits=bits, steps=40, seed=5 + bits)
+    cap = 384
+    # (kind, cache): s = decode step, a = plain append, o = attention call
+    ops = [("s", 0), ("o", 1), ("o", 0), ("s", 1), ("s", 1), ("o", 2), ("o", 1), ("a", 2), ("o", 0),
+           ("o", 2), ("s", 2), ("o", 2), ("s", 0), ("o", 0)] * 12  # 24 appends a cache: past a key flush
+    qs_np = _queries(wl, 2)
+    qs = [T.dev(x, wl.q_dtype) for x in qs_np]
+    toks = {}
+    seen = [0, 0, 0]
+    for i, (kind, ci) in enumerate(ops):
+        if kind in "sa":
+            j = seen[ci] % wl.steps
+            toks[i] = (T.dev(wl.k_new[j], "f16"), T.dev(wl.v_new[j], "f16"))
+            seen[ci] += 1
+
+    def fresh(overlap):
+        cs = []
+        for _ in range(3):
+            g = T.gpu_cache(wl, capacity=cap)
+            g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
+            g.set_splits(3)
+            g.set_overlap(overlap)
+            g.attention(qs[0])  # zeroes the workspace outside any graph
+            cs.append(g)
+        torch.cuda.synchronize()
+        return cs
+
+    def run(cs, outs):
+        for i, ((kind, ci), out) in enumerate(zip(ops, outs)):
+            if kind == "s":
+                cs[ci].step(*toks[i], qs[ci % 2], out)
+            elif kind == "a":
+                cs[ci].append(*toks[i])
+            else:
+                cs[ci].attention(qs[ci % 2], out)
+
+    ref_c = fresh(False)
+    ref = [torch.zeros_like(qs[0]) for _ in ops]
+    run(ref_c, ref)
+    torch.cuda.synchronize()
+    ov_c = fresh(True)
+    outs = [torch.zeros_like(qs[0]) for _ in ops]
+    run(ov_c, outs)
+    torch.cuda.synchronize()
+    for i, (a_, b_) in enumerate(zip(outs, ref)):
+        assert torch.equal(a_, b_), (i, ops[i])
+    for ci in range(3):
+        assert ov_c[ci].length == ref_c[ci].length == wl.T + seen[ci]
+        T.compare_state(T.gpu_state(ov_c[ci]), T.gpu_state(ref_c[ci]), ov_c[ci].length, wl.R, 32)
+    gr_c = fresh(True)
+    outs_g = [torch.zeros_like(qs[0]) for _ in ops]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(gr_c, outs_g)
+    graph.replay()
+    torch.cuda.synchronize()
+    for i, (a_, b_) in enumerate(zip(outs_g, ref)):
+        assert torch.equal(a_, b_), (i, ops[i])
+    for ci in range(3):
+        o = T.oracle_cache(wl, capacity=cap)
+        o.prefill(wl.k, wl.v)
+        for j in range(seen[ci]):
+            o.append(wl.k_new[j % wl.steps], wl.v_new[j % wl.steps])
+        last = max(i for i, (kind, c) in enumerate(ops) if c == ci and kind in "so")
+        err = T.attn_err(T.out_float(outs[last]), o.attention(T.q_float(qs_np[ci % 2], wl.q_dtype)))
+        assert err <= T.ATTN_TOL, (ci, err)
