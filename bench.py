@@ -657,6 +657,42 @@ def streaming(args, torch, W, KiviCache, dev, stream, ev, peak):
     return res
 
 
+def streaming_attention(args, torch, W, KiviCache, dev, stream, ev, peak):
+    """The streaming workload's attention alone at its final context: batch
+    64, 28/4 heads (GQA 7), the 2048 + 512 tokens prefilled at once (the same
+    cache as the 512 steps leave, see test_streaming_2048_plus_512); for
+    profiling captures of the launch the streaming line times."""
+    wl = W.streaming()
+    k = np.ascontiguousarray(np.concatenate([wl.k, wl.k_new.transpose(1, 2, 0, 3)], axis=2))
+    v = np.ascontiguousarray(np.concatenate([wl.v, wl.v_new.transpose(1, 2, 0, 3)], axis=2))
+    T = k.shape[2]
+    kd, vd = W.to_torch(k, "f16", dev), W.to_torch(v, "f16", dev)
+
+    def new_cache():
+        c = KiviCache(batch=wl.B, n_kv_heads=wl.Hkv, n_q_heads=wl.Hq, max_tokens=wl.capacity, bits=2,
+                      residual=wl.R)
+        c.prefill(kd, vd)
+        return c
+    c0 = new_cache()
+    n_rep = n_replicas(sum(t.numel() * t.element_size() for t in c0.state_views().values()))
+    caches = [c0] + [new_cache() for _ in range(n_rep - 1)]
+    q = W.to_torch(wl.q, "f16", dev)
+    out = torch.empty_like(q)
+    for i in range(3):
+        caches[i % n_rep].attention(q, out)
+    torch.cuda.synchronize()
+    tg = graph_per_launch(torch, stream, ev,
+                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          overlap=caches)
+    nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, T, wl.R, 2)
+    gbs = nbytes / tg / 1e9
+    return {"streaming_attention_2560": {
+        "what": f"batch 64, 28/4 heads (GQA 7), context {T} prefilled, R 32; {n_rep} cache replicas "
+                "rotated; graph replay",
+        "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2), "us": round(tg * 1e6, 2),
+        "bytes": nbytes}}
+
+
 def append_window(torch, W, KiviCache, dev, stream, ev):
     """The decode append alone on the Llama-3-8B decode shape: 32 appends
     from context 4096 on one cache, eager, each followed by the attention;
@@ -715,6 +751,8 @@ def run_only(args):
 
     if args.only == "append":
         return append_window(torch, W, KiviCache, dev, torch.cuda.current_stream(), ev)
+    if args.only == "stream_attn":
+        return streaming_attention(args, torch, W, KiviCache, dev, torch.cuda.current_stream(), ev, peak)
     return extra_workloads(args, torch, W, KiviCache, dev, torch.cuda.current_stream(), ev, peak,
                            which=args.only)
 
@@ -987,7 +1025,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--main-only", action="store_true", help="skip the other workloads")
     ap.add_argument("--only", choices=["main", "quantize", "attn3", "attn4", "attn8", "outliers", "long", "streaming",
-                                       "append"],
+                                       "append", "stream_attn"],
                     help="run one workload alone (for profiling); prints its numbers")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quant-reps", type=int, default=10)
