@@ -220,12 +220,20 @@ int max_splits(const kivi_config& c) {
 // fused, 8.9 us with a separate tail split, 10.9 us with 8 packed splits;
 // 131k tokens (4096 tiles, 8 units) 23.2 us with 35 packed splits against
 // 25.3 us with 74 (its three tail splits stay separate: fused, 30 us).
+// Tiles fewer for the packed split that carries a fused tail in overlapped
+// plans: its fp16 tail round runs after its tiles.  Measured on the
+// Llama-3-8B decode shape (2 packed splits of 127 tiles per unit): 8.6 us
+// per launch with even splits, 8.1 us with 72 + 55 tiles (a discount of 32
+// or 40), 8.6 us again with 96 + 31.
+constexpr int kFusedDiscount = 32;
+
 kivi::SplitCfg split_cfg(const kivi_cache* c, bool overlapped) {
   kivi::SplitCfg sc;
   const int budget = split_budget(c->cfg);
   sc.budget = overlapped ? (budget / 2 > 1 ? budget / 2 : 1) : budget;
   sc.min_tiles = overlapped ? 64 : 8;
   sc.fuse_single_tail = overlapped ? 1 : 0;
+  sc.fused_discount = overlapped ? kFusedDiscount : 0;
   sc.max_splits = max_splits(c->cfg);
   sc.override_splits = c->splits_override;
   return sc;

@@ -85,6 +85,7 @@ struct SplitCfg {
   int budget, max_splits, override_splits;
   int min_tiles;         // packed tiles per automatic split, at least
   int fuse_single_tail;  // automatic plans ride a one-split tail on the last packed split
+  int fused_discount;    // tiles fewer for the packed split that carries a fused tail
 };
 
 // How decode attention covers one sequence of length l: tail splits of
@@ -134,6 +135,14 @@ __host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const Spl
     per = (tiles + smax - 1) / smax;
     per = (per + 3) / 4 * 4;
     if (per < sc.min_tiles) per = sc.min_tiles;
+    if (p.tail_fused && sc.fused_discount > 0) {
+      // the last split runs the tail after its tiles: spread fused_discount
+      // of its tiles over the others (as long as the split count holds)
+      const int n = (tiles + per - 1) / per;
+      int per2 = (tiles + sc.fused_discount + n - 1) / n;
+      per2 = (per2 + 3) / 4 * 4;
+      if (n > 1 && per2 > per && (n - 1) * per2 < tiles) per = per2;
+    }
   }
   p.chunk = per * 32;
   p.splits = p.tail_splits + (tt + p.chunk - 1) / p.chunk;  // no empty split

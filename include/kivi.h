@@ -299,7 +299,7 @@ kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
  * kivi_set_attention_overlap) the automatic choice takes half that budget
  * and at least 64 tiles per packed split, and rides the tail on the last
  * packed split when the tail is a single split or the budget holds no tail
- * split beside it: the CTAs of
+ * split beside it (that split then takes up to 32 tiles fewer): the CTAs of
  * consecutive launches then share the SMs, and fewer, longer splits pay the
  * fixed cost of a split (query tables, first tile, merge) fewer times.  An
  * override n asks for n splits in all, with or without the overlap; it is
