@@ -246,13 +246,15 @@ def run_gpu(args):
     for c in caches:
         rewind_if_needed(c, 2 * per_rep + 1)
 
+    outs = [torch.empty_like(q) for _ in range(K)]  # overlapping calls write distinct outputs
+
     def time_attention_graph(overlap):
         for c in caches:
             c.set_overlap(overlap)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             for i in range(K):
-                caches[i % n_rep].attention(q, out)
+                caches[i % n_rep].attention(q, outs[i])
         g.replay()  # warm-up replay (attention leaves the caches unchanged)
         fence()
         e0, e1 = ev(), ev()
@@ -542,7 +544,7 @@ def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits, outli
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) * 1e-3 for a, b in recs]
     tg = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          [lambda c=caches[i % n_rep], o=torch.empty_like(q): c.attention(q, o) for i in range(args.attn_reps)],
                           overlap=caches)
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T + 1, wl.R, bits)
     if outliers:  # the outlier blocks of the quantized key groups
@@ -588,7 +590,7 @@ def long_context(args, torch, W, KiviCache, dev, stream, ev, peak):
     torch.cuda.synchronize()
     times = [a.elapsed_time(b) * 1e-3 for a, b in recs]
     tg = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          [lambda c=caches[i % n_rep], o=torch.empty_like(q): c.attention(q, o) for i in range(args.attn_reps)],
                           overlap=caches)
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, wl.T, wl.R, 2)
     gbs = nbytes / tg / 1e9
@@ -641,7 +643,7 @@ def streaming(args, torch, W, KiviCache, dev, stream, ev, peak):
     n_steps = sum(len(ctx) for ctx, _ in chunks)
     # the attention alone at the final context (2560 tokens), replicas rotated
     ta = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(4 * n_rep)],
+                          [lambda c=caches[i % n_rep], o=torch.empty_like(q): c.attention(q, o) for i in range(4 * n_rep)],
                           overlap=caches)
     ab = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, caches[0].length, wl.R, 2)
     res["streaming_decode"] = {
@@ -682,7 +684,7 @@ def streaming_attention(args, torch, W, KiviCache, dev, stream, ev, peak):
         caches[i % n_rep].attention(q, out)
     torch.cuda.synchronize()
     tg = graph_per_launch(torch, stream, ev,
-                          [lambda c=caches[i % n_rep]: c.attention(q, out) for i in range(args.attn_reps)],
+                          [lambda c=caches[i % n_rep], o=torch.empty_like(q): c.attention(q, o) for i in range(args.attn_reps)],
                           overlap=caches)
     nbytes = attn_bytes(wl.B, wl.Hkv, wl.Hq, wl.D, T, wl.R, 2)
     gbs = nbytes / tg / 1e9

@@ -240,15 +240,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem));
-}
-
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;"); }
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N)); }
-
 // mbarrier + bulk copy (one elected thread issues; the barrier's transaction
 // count completes the phase when every byte has landed).
 __device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
@@ -285,6 +276,23 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// The epoch protocol of overlapping calls on one workspace (thread 0): wait
+// until the group's slot holds `want` (the previous call's epoch, published
+// with release semantics after its last read of the group's slots), bounded
+// like the staging waits; false when the wait gave up.  The call that
+// publishes it belongs to an earlier launch on the stream, all of whose CTAs
+// have started before any CTA of this one (a programmatic dependent starts
+// only once every CTA of the launch before it has started), so the wait
+// cannot hold up the CTA it waits for.
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -318,12 +326,46 @@ __device__ __noinline__ bool mbar_wait(unsigned long long* bar, uint32_t parity)
 // an mbarrier that nothing completes (no copy is issued, no thread arrives),
 // and records the timeout in *status as a packed split does in the
 // workspace status word.
+constexpr unsigned kGenMask = 0xFFFFFFu;  // generations count modulo 2^24 (tickets wrap at 2^32)
+
+// This launch's generation for group gid on its workspace, from a ticket:
+// every launch that takes tickets (overlapping launches and decode steps'
+// attention) adds kMaxSplits to the group's count (CTA 0 adds what the grid's
+// other splits do not), and every CTA of such a launch has its ticket before
+// any CTA of a later launch can start (the launch releases its dependents
+// only after thread 0 has consumed the ticket), so ticket / kMaxSplits
+// numbers these launches in stream order, CUDA graphs replayed included.
+// Ordinary launches take none: they overlap no other launch, so what the
+// count says stays true across them.  Thread 0 issues the atomic here and
+// consumes it with ticket_gen.
+__device__ __forceinline__ unsigned take_ticket(const AttnArgs& a, long gid) {
+  const unsigned add = blockIdx.x == 0 ? (unsigned)(kMaxSplits - (int)gridDim.x + 1) : 1u;
+  return atomicAdd(a.epochs + 2 * gid, add);
+}
+__device__ __forceinline__ unsigned ticket_gen(unsigned ticket) {
+  return (ticket / (unsigned)kMaxSplits) & kGenMask;
+}
+
+__device__ bool epoch_wait(const unsigned* slot, unsigned want) {
+  if (ld_acquire_u32(slot) == want) return true;
+  const unsigned long long t0 = global_ns();
+  while (ld_acquire_u32(slot) != want) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+    __nanosleep(256);
+  }
+  return true;
+}
+
+// The slot the epoch probe waits on: it stays 0, and the probe waits for 1.
+__device__ unsigned g_probe_epoch;
+
 __global__ void wait_probe_kernel(int* status) {
   __shared__ __align__(8) unsigned long long bar;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
     if (!mbar_wait(&bar, 0u)) atomicOr(status, 1);
+    if (!epoch_wait(&g_probe_epoch, 1u)) atomicOr(status, 2);
   }
 }
 
@@ -1641,21 +1683,37 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   // completed (before the merge below), so that no early start ever runs
   // ahead of a cache write.
   const bool step_launch = a.pdl == kPdlAll || a.pdl == kPdlTail;
-  if (!step_launch) grid_launch_dependents();
   const int s = blockIdx.x;
   const int nhc = gridDim.y / cv.H;
   const int h = nhc == 1 ? (int)blockIdx.y : (int)blockIdx.y / nhc;
   const int hc = nhc == 1 ? 0 : (int)blockIdx.y % nhc;
   const int b = blockIdx.z;
+  const long gid = (long)b * gridDim.y + blockIdx.y;  // (batch, kv-head, head chunk)
+  // An overlapping launch releases its dependents at once, once its
+  // generation ticket is taken (take_ticket); a decode step's attention
+  // releases them once its append has completed (before the merge below),
+  // an ordinary launch at its exit.
+  const bool tickets = a.epoch_on && a.pdl != 0;
+  unsigned gen = 0;  // thread 0: this launch's generation for the group
+  if (tickets && threadIdx.x == 0) gen = take_ticket(a, gid);
+  if (a.pdl == kPdlOverlap) {
+    if (threadIdx.x == 0) gen = ticket_gen(gen);
+    __syncthreads();
+    grid_launch_dependents();
+  }
   const int grp = a.Hq / cv.H;
   const int j0 = h * grp + hc * kNH;
   const int nh = min(kNH, grp - hc * kNH);
   const long unit = (long)b * cv.H + h;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  (void)gid;
   // this sequence's plan; splits past its own count have nothing to do (and
   // are not counted by its merge)
   const SeqPlan p = lens.uniform >= 0 ? a.plan : make_plan(lens.l[b], cv.R, cv.policy, a.scfg);
-  if (s >= p.splits) return;
+  if (s >= p.splits) {
+    if (step_launch && threadIdx.x == 0) gen = ticket_gen(gen);  // the ticket is in before the exit
+    return;
+  }
   const int path = s < p.tail_splits ? kPathTail : kPathMma;
 
   if (path == kPathTail) {
@@ -1675,14 +1733,24 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
     if (a.pdl == kPdlTail) grid_dependency_wait();  // the tail reads what the append wrote
     fused_tail<BITS, NB>(cv, a, p, sv, unit, b, j0, nh, s_m, s_l);
   }
-  // an overlapping launch waits for the launch before it only here, before
-  // its first global write
-  if (a.pdl == kPdlOverlap || step_launch) grid_dependency_wait();
-  if (step_launch) grid_launch_dependents();
+  // a decode step's attention releases its dependents once its append has
+  // completed
+  if (step_launch) {
+    grid_dependency_wait();
+    if (threadIdx.x == 0) gen = ticket_gen(gen);
+    __syncthreads();
+    grid_launch_dependents();
+  }
+  // an overlapping launch orders its first workspace write of the group after
+  // the previous call on this workspace has finished with the group's slots
+  // (see epoch_wait); a wait that gives up sets bit 2 of the status word
+  if (a.pdl == kPdlOverlap && a.epoch_on) {
+    if (threadIdx.x == 0 && !epoch_wait(a.epochs + 2 * gid + 1, gen)) atomicOr(a.status, 2);
+    __syncthreads();
+  }
 
   // ---- merge the warps of this CTA into one partial per head ----
   const int d = threadIdx.x;
-  const long gid = (long)b * gridDim.y + blockIdx.y;  // (batch, kv-head, head chunk)
   for (int j = 0; j < nh; ++j) {
     float M = -INFINITY;
 #pragma unroll
@@ -1772,6 +1840,17 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
       else static_cast<__nv_bfloat16*>(a.out)[oi + i] = __float2bfloat16_rn(r[i]);
     }
   }
+  // the group's slots are free for the next call on this workspace: every
+  // thread's reads of them precede the barrier, the release orders them
+  if (tickets) {
+    __syncthreads();
+    if (threadIdx.x == 0) st_release_u32(a.epochs + 2 * gid + 1, (gen + 1u) & kGenMask);
+  }
+  // An overlapping launch completes only after the launch before it: group
+  // 0's final CTA waits for it last of all, so that whatever follows this
+  // launch on the stream (a copy, a memset, a host read after a sync) also
+  // follows every launch before it; the other CTAs exit at once.
+  if (a.pdl == kPdlOverlap && gid == 0) grid_dependency_wait();
 }
 
 }  // namespace

@@ -251,7 +251,7 @@ kivi::SeqPlan plan_of(const kivi_cache* c, int l, bool overlapped) {
 //   16-byte slot whose first int is the status word (nonzero after a
 //   timed-out wait).
 struct WsLayout {
-  size_t o_off, ml_off, o1_off, ml1_off, cnt_off, cnt2_off, status_off, total;
+  size_t o_off, ml_off, o1_off, ml1_off, cnt_off, cnt2_off, epoch_off, status_off, total;
   int groups;
 };
 
@@ -268,7 +268,8 @@ WsLayout ws_layout(const kivi_config& c) {
   w.ml1_off = w.o1_off + units * G * C * D * 4;
   w.cnt_off = w.ml1_off + units * G * C * 2 * 4;
   w.cnt2_off = w.cnt_off + units * G * 4;
-  w.status_off = (w.cnt2_off + units * 4 + 15) / 16 * 16;
+  w.epoch_off = w.cnt2_off + units * 4;
+  w.status_off = (w.epoch_off + units * 8 + 15) / 16 * 16;
   w.total = w.status_off + 16;
   return w;
 }
@@ -516,6 +517,8 @@ kivi_status attn_args(const kivi_cache* c, const void* q, kivi_dtype q_dtype, vo
   a->counters = reinterpret_cast<int*>(ws + w.cnt_off);
   a->counters2 = reinterpret_cast<int*>(ws + w.cnt2_off);
   a->status = reinterpret_cast<int*>(ws + w.status_off);
+  a->epochs = reinterpret_cast<unsigned*>(ws + w.epoch_off);
+  a->epoch_on = 0;
   a->pdl = 0;
   return KIVI_OK;
 }
@@ -548,6 +551,7 @@ KIVI_API kivi_status kivi_decode_attention(kivi_cache* c, const void* q, kivi_dt
     c->ws_ready = workspace;
   }
   if (c->overlap) a.pdl = kivi::kPdlOverlap;
+  a.epoch_on = 1;  // every call on the cache's workspace keeps its generations
   return cuda_status(kivi::launch_attention(view(c), a, sl, st));
 }
 
@@ -604,6 +608,7 @@ KIVI_API kivi_status kivi_decode_step(kivi_cache* c, const void* k_new, const vo
     if (l > c->cfg.residual && (l - c->cfg.residual) % c->cfg.group == 0) packed_untouched = false;
   }
   a.pdl = packed_untouched ? kivi::kPdlTail : kivi::kPdlAll;
+  a.epoch_on = 1;
   return cuda_status(kivi::launch_attention(view(c), a, sl, st));
 }
 

@@ -300,7 +300,13 @@ struct AttnArgs {
   int merge_groups;   // stride of the group arrays (ceil(max splits / kMergeGroup))
   int* counters;      // [gid][merge_groups] CTAs finished per split group; 0 between calls
   int* counters2;     // [gid] split groups finished; 0 between calls
-  int* status;        // set nonzero when a bounded wait for staged data timed out
+  int* status;        // bit 1: a bounded wait for staged data timed out; bit 2: an epoch wait did
+  // [gid][2]: tickets taken by the calls' CTAs (kMaxSplits per call), and the
+  // generation up to which calls have finished with the group's slots (both
+  // 0 after the workspace was zeroed); epoch_on = 0: none of it (a scratch
+  // area zeroed for each call)
+  unsigned* epochs;
+  int epoch_on;
   int stages;         // staged tiles per warp (set at launch from the tile size)
   // A programmatic dependent of the append kernel just before it on the
   // stream (the one-call decode step): the CTAs may start while the append
@@ -315,8 +321,9 @@ struct AttnArgs {
 
 // kPdlOverlap: launched after other work on the stream that writes neither
 // q nor the cache (for instance another attention call): the CTAs read the
-// cache and q at once and wait for that work only before their first global
-// write (the split partials, the counters, the output).
+// cache and q at once; before a group's first workspace write they wait
+// (bounded) until the previous call on this workspace has published the
+// group's epoch, so that only the calls on the same workspace are ordered.
 enum : int { kPdlAll = 1, kPdlTail = 2, kPdlOverlap = 3 };
 
 // Programmatic dependent launch (sm_90+).  The primary kernel lets its

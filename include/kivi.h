@@ -236,10 +236,12 @@ kivi_status kivi_cache_lengths(const kivi_cache *c, int *lengths);
 
 /* Device workspace (bytes) kivi_decode_attention needs for this handle's
  * shape at any length: split-K partial results, merged groups of partials,
- * counters, and a status word (the int at byte offset bytes - 16: nonzero
- * after a kernel gave up waiting for its staged data, which only a device
- * fault can cause; it stays set until the workspace is next cleared).
- * Host only. */
+ * counters, one epoch per (batch, kv-head, head chunk) for overlapping calls,
+ * and a status word (the int at byte offset bytes - 16: bit 1 after a kernel
+ * gave up waiting for its staged data, which only a device fault can cause;
+ * bit 2 after an overlapping call gave up waiting for the previous call's
+ * epoch, which only a broken contract can cause; it stays set until the
+ * workspace is next cleared).  Host only. */
 size_t kivi_attention_workspace_bytes(const kivi_cache *c);
 
 /* Decode attention over the cache (review §1.3 decoding step 2:
@@ -315,25 +317,31 @@ int kivi_attention_splits(const kivi_cache *c, int l);
  * just before them on the stream (enable = 1; 0, the default, turns it off;
  * KIVI_EINVAL for other values).  No counterpart on the pages: a launch-order
  * setting.  The attention is then launched as a programmatic dependent of
- * that kernel: its CTAs start as the earlier kernel's CTAs finish, read q and
- * the cache at once, and wait for the earlier kernel to complete only before
- * their first global write (the split partials, the counters and out).  So
- * enable it only when the work enqueued before each attention call on the
- * stream writes neither that call's q nor this cache -- for instance a
- * sequence of attention calls over caches and queries that were all written
- * earlier.  The automatic split count changes with it (see
+ * that kernel: its CTAs start as the earlier kernel's CTAs finish and read q
+ * and the cache at once.  Calls on the same workspace are ordered by an
+ * epoch per (batch, kv-head, head chunk) kept in the workspace: a call's CTAs
+ * write the group's partials only once the previous call on that workspace
+ * has finished with them (a bounded wait, see kivi_check_bounded_wait), and
+ * the other CTAs do not wait for the kernel before.  A launch still
+ * completes only after the one before it (one CTA waits for it last), so
+ * whatever follows on the stream follows them all.
+ * The contract:
+ * - the work enqueued since the last launch that is not an overlapping
+ *   attention call writes neither this call's q nor this cache
+ *   (overlapping calls enqueued back to back start one another early, so a
+ *   call may run beside any of them) -- for instance a sequence of
+ *   attention calls over caches and queries that were all written earlier;
+ * - calls that may overlap write distinct outputs, and every cache has its
+ *   own workspace (the handle's epochs are per workspace).
+ * That last non-overlapping launch has itself completed if it is one of
+ * this library's: the kernels that write a cache (prefill, appends) let no
+ * launch start before they complete, except a decode step's own attention,
+ * and that attention lets later launches start only after its append has
+ * completed.  The automatic split count changes with the setting (see
  * kivi_set_attention_splits), so results may differ in the last bits from
  * those of the setting off; with an explicit split count they are the same
  * bit for bit.  kivi_decode_step and kivi_decode_attention_static ignore
- * it.  Overlapping calls enqueued back to back start one another early, so
- * a call may run beside any of them: the contract covers all the work
- * enqueued since the last launch that is not an overlapping attention call
- * (none of it may write this call's q or this cache).  That launch itself
- * has completed by then if it is one of this library's: the kernels that
- * write a cache (prefill, appends) let no launch start before they
- * complete, except a decode step's own attention, and that attention lets
- * later launches start only after its append has completed.
- * Host only; no device work. */
+ * it.  Host only; no device work. */
 kivi_status kivi_set_attention_overlap(kivi_cache *c, int enable);
 
 /* Tokens held by every sequence; -2 when the sequences' lengths differ (see
@@ -349,13 +357,18 @@ int kivi_last_cuda_error(void); /* cudaError_t of the last failed launch on this
  * A packed split waits for each staged tile on an mbarrier, for at most
  * 200 ms; if a wait gives up, the split stops issuing copies, ORs 1 into the
  * workspace status word and still completes the merge protocol, so the
- * launch ends and the context stays usable.  This call runs that same
- * bounded wait in one CTA on a barrier phase that nothing completes (no
- * copy is issued and no thread arrives), then ORs 1 into *status.
+ * launch ends and the context stays usable.  An overlapping call (see
+ * kivi_set_attention_overlap) waits, for at most 200 ms too, until the
+ * previous call on its workspace has finished with a group's slots; if that
+ * wait gives up it ORs 2 into the status word and goes on.  This call runs
+ * the same bounded mbarrier wait in one CTA on a barrier phase that nothing
+ * completes (no copy is issued and no thread arrives), then ORs 1 into
+ * *status; then the same bounded epoch wait on an epoch that nothing
+ * publishes, then ORs 2 into *status.
  * - status: one int, 4-byte aligned, device memory on the current device,
  *   or managed or mapped pinned host memory; the caller owns it and reads it
  *   after the stream has run the probe.
- * - Asynchronous on stream; the probe occupies one SM for about 200 ms.
+ * - Asynchronous on stream; the probe occupies one SM for about 400 ms.
  * - KIVI_EINVAL for a null, misaligned or unreachable pointer (nothing is
  *   launched); KIVI_ECUDA if the launch fails. */
 kivi_status kivi_check_bounded_wait(int *status, void *stream);

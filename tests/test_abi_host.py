@@ -177,9 +177,9 @@ def test_split_plan_and_workspace(K):
         assert K.kivi_attention_splits(h, 100) == 2   # tail + one 64-token split
         assert K.kivi_attention_splits(h, 40) == 1    # everything is tail
         # 64 groups x (9 split partials + 1 merged group) x 8 heads (a chunk)
-        # x (128 + 2) floats, one counter per split group and per group, the
-        # status slot
-        assert K.kivi_attention_workspace_bytes(h) == 64 * (9 + 1) * 8 * (128 + 2) * 4 + 64 * 4 * 2 + 16
+        # x (128 + 2) floats, one counter per split group and per group, two
+        # generation words per group, the status slot
+        assert K.kivi_attention_workspace_bytes(h) == 64 * (9 + 1) * 8 * (128 + 2) * 4 + 64 * 4 * 4 + 16
         K.kivi_set_attention_splits(h, 3)
         assert K.kivi_attention_splits(h, 4097) == 3
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
