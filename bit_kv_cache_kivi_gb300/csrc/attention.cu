@@ -5,22 +5,26 @@
 // quantisation"; dequantization is fused into both products (review §3.2
 // "System-Level": no separate dequantize pass).
 //
-// The context is split along the tokens (flash-decoding).  Split 0 of every
-// (batch, kv-head, head chunk) takes the tail [t_tail, l) -- the tokens whose
-// keys or values are still fp16 in the residual rings, plus the partial value
-// group before them -- on CUDA cores.  Splits 1.. take the fully packed
-// 32-token tiles [0, t_tail).  Partials are merged in the same launch: the
-// CTA that finishes last in a group of up to kMergeGroup splits merges the
-// group, and with more than one group the last group merges the groups;
-// nothing ever waits on another CTA.  A CTA serves a chunk of up to eight
-// query heads of one KV head, so every tile is decoded once for up to eight
-// heads.
+// The context is split along the tokens (flash-decoding).  The tail
+// [t_tail, l) -- the tokens whose keys or values are still fp16 in the
+// residual rings, plus the partial value group before them -- runs on CUDA
+// cores, in the first splits of every (batch, kv-head, head chunk) or after
+// the tiles of its last packed split; the packed splits take the fully
+// packed 32-token tiles [0, t_tail).  Partials are merged in the same
+// launch: the CTA that finishes last in a group of up to kMergeGroup splits
+// merges the group, and with more than one group the last group merges the
+// groups; no CTA waits for another CTA of its launch.  (A launch that
+// overlaps the launch before it waits, bounded, for the previous call on its
+// workspace to publish a group's generation: see take_ticket.)  A CTA serves
+// a chunk of up to eight query heads of one KV head, so every tile is decoded
+// once for up to eight heads.
 //
 // Packed tiles (2, 3, 4 or 8 bits) run on the tensor cores (mma.sync
 // m16n8k16, fp16 operands, fp32 accumulation).  Each warp streams its tiles
 // through its own ring of staged tiles (one lane issues one bulk copy per
 // tile, completion on an mbarrier) and keeps an online softmax per head:
 //   scores  S[t, j] = sum_d c_td (q_jd s_d) + beta_j, beta_j = sum_d q_jd z_d
+//           (beta per tile, for sixteen tiles per MMA in the split's prologue)
 //   output  O[d, j] = sum_t c_td (p_jt s_t,g(d)) + sum_t p_jt z_t,g(d)
 // The codes c enter the MMA as fp16 subnormals c * base^i * 2^-24 (the masked
 // code bits are the whole encoding; base 4 at 2 and 3 bits, 16 at 4, 1 at 8).

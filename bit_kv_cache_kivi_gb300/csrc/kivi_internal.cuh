@@ -78,9 +78,10 @@ __device__ __forceinline__ void seq_counts(const SeqLens& s, int b, int R, int p
   }
 }
 
-// Split configuration of a cache (a function of its shape): the one-wave
-// budget of splits per attention unit, the workspace's bound on splits, and
-// a caller's override (0 = automatic).
+// Split configuration of a cache (a function of its shape and of whether
+// the launch overlaps the one before it): the budget of splits per attention
+// unit, the workspace's bound on splits, a caller's override (0 =
+// automatic), and the automatic plan's knobs below.
 struct SplitCfg {
   int budget, max_splits, override_splits;
   int min_tiles;         // packed tiles per automatic split, at least
@@ -159,8 +160,8 @@ __host__ __device__ inline SeqPlan make_plan(int l, int R, int policy, const Spl
 //   kOffZv: zero[32][D / G]
 //   then the outlier block, if the cache keeps outlier channels.
 // The decode attention stages [kStageOff, tile end) with one bulk copy; it
-// reads the key zeros apart, for sixteen tiles at a time (see beta_pass),
-// so they lead the tile.
+// reads the key zeros apart, for sixteen tiles at a time (load_zk and
+// beta_mma in attention.cu), so they lead the tile.
 template <int BITS>
 constexpr int kRowBytes = kHeadDim * BITS / 8;
 constexpr int kOffZk = 0;
