@@ -1769,7 +1769,7 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
         ot += e * sv.merge_area(w, path)[j * kHeadDim + d];
       }
     }
-    const long pidx = (gid * a.splits + s) * kNH + j;
+    const long pidx = (gid * a.scfg.max_splits + s) * kNH + j;
     a.ws_o[pidx * kHeadDim + d] = ot;
     if (d == 0) {
       a.ws_ml[pidx * 2] = M;
@@ -1797,7 +1797,7 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
   for (int hh = 0; hh < 2; ++hh) {
     const int j = warp + kWarps * hh;
     if (j < nh)
-      merge_partials(a.ws_o + (gid * a.splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.splits + g_lo) * kNH * 2,
+      merge_partials(a.ws_o + (gid * a.scfg.max_splits + g_lo) * kNH * kHeadDim, a.ws_ml + (gid * a.scfg.max_splits + g_lo) * kNH * 2,
                      g_n, j, o4[hh], m_h[hh], lsum_h[hh]);
   }
   if (n_grp > 1) {

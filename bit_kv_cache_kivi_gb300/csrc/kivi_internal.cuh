@@ -292,10 +292,13 @@ struct AttnArgs {
   // packed split also takes the tail, after its tiles.
   SeqPlan plan;   // of every sequence when the lengths are uniform
   SplitCfg scfg;  // to plan each sequence on the device otherwise
-  int splits;     // grid width: the most splits of any sequence (workspace stride)
+  int splits;     // grid width: the most splits of any sequence
   // Split partials of attention group gid = (b, kv-head, head chunk):
-  float* ws_o;        // [gid][splits][kHeadChunk][D]  output sums
-  float* ws_ml;       // [gid][splits][kHeadChunk][2]  (max in log2 units, sum)
+  // per-split partials, [gid][scfg.max_splits][...]: a fixed stride per group,
+  // so that calls with different split counts on one workspace use the same
+  // slots for the same group (overlapping calls are ordered per group)
+  float* ws_o;        // [gid][max splits][kHeadChunk][D]  output sums
+  float* ws_ml;       // [gid][max splits][kHeadChunk][2]  (max in log2 units, sum)
   float* ws_o1;       // [gid][merge_groups][kHeadChunk][D]  merged groups of kMergeGroup splits
   float* ws_ml1;      // [gid][merge_groups][kHeadChunk][2]
   int merge_groups;   // stride of the group arrays (ceil(max splits / kMergeGroup))

@@ -177,3 +177,68 @@ def test_overlapping_calls_after_decode_steps(bits):
         last = max(i for i, (kind, c) in enumerate(ops) if c == ci and kind in "so")
         err = T.attn_err(T.out_float(outs[last]), o.attention(T.q_float(qs_np[ci % 2], wl.q_dtype)))
         assert err <= T.ATTN_TOL, (ci, err)
+
+
+def test_overlapping_call_generations_under_replay():
+    """Many overlapping calls back to back on two caches (a uniform one and
+    one of ragged lengths), the same cache often twice or three times in a
+    row, with explicit split counts changing between calls (so the grids
+    differ and the generation tickets of a launch are padded differently):
+    eagerly and replayed three times from one CUDA graph, every output equals
+    the same call made as an ordinary launch, and no bounded wait gives up."""
+    wl = W.synthetic("ovg", B=3, Hq=16, Hkv=4, T=1500, R=32, bits=2, seed=77)
+    cap = 1536
+    lens = [1500, 37, 900]
+    cs = []
+    for ragged in (False, True):
+        g = T.gpu_cache(wl, capacity=cap)
+        if ragged:
+            g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"), lengths=lens)
+        else:
+            g.prefill(T.dev(wl.k, "f16"), T.dev(wl.v, "f16"))
+        g.attention(T.dev(wl.q, "f16"))  # zeroes the workspace outside any graph
+        cs.append(g)
+    torch.cuda.synchronize()
+    qs_np = _queries(wl, 3)
+    qs = [T.dev(x, wl.q_dtype) for x in qs_np]
+    # explicit split counts (an automatic count differs between overlapped and
+    # ordinary launches, and with it the last bits)
+    splits = [1, 3, 2, 9, 2, 6, 17, 5]
+    seq = [(i % 7 % 2, i % 3, splits[i % len(splits)]) for i in range(40)]
+    seq += [(0, 1, 7)] * 3 + [(1, 2, 4)] * 3
+
+    ref = []
+    for ci, qi, sp in seq:
+        cs[ci].set_overlap(False)
+        cs[ci].set_splits(sp)
+        ref.append(cs[ci].attention(qs[qi]).clone())
+    torch.cuda.synchronize()
+
+    outs = [torch.zeros_like(qs[0]) for _ in seq]
+
+    def run():
+        for (ci, qi, sp), out in zip(seq, outs):
+            cs[ci].set_splits(sp)
+            cs[ci].attention(qs[qi], out)
+
+    for c in cs:
+        c.set_overlap(True)
+    run()
+    torch.cuda.synchronize()
+    for i, (a_, b_) in enumerate(zip(outs, ref)):
+        assert torch.equal(a_, b_), (i, seq[i])
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run()
+    for rep in range(3):
+        for o in outs:
+            o.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for i, (a_, b_) in enumerate(zip(outs, ref)):
+            assert torch.equal(a_, b_), (rep, i, seq[i])
+    for c in cs:
+        c.set_overlap(False)
+        c.set_splits(0)
+    for c in cs:  # the status word (bytes - 16): no bounded wait gave up
+        assert c.workspace[c.ws_bytes - 16:c.ws_bytes - 12].view(torch.int32).item() == 0
