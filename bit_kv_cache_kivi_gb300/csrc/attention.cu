@@ -225,6 +225,12 @@ struct SmemView {
     return *reinterpret_cast<PackedState<NB>*>(base + packed_state_off(S, stride));
   }
   __device__ __forceinline__ TailSmem<BITS>& tail() const { return *reinterpret_cast<TailSmem<BITS>*>(base); }
+  // q * scale * log2(e) of the chunk's heads, [kNH][kHeadDim], after the
+  // packed state: kept for the fp16 outlier key channels (present when the
+  // cache keeps outlier channels, see attn_stages)
+  __device__ __forceinline__ float* qo() const {
+    return reinterpret_cast<float*>(base + packed_state_off(S, stride) + sizeof(PackedState<NB>));
+  }
   // q of head j, staged for the tables: in stage 1 of warp j >> 1
   __device__ __forceinline__ float* qv(int j) const {
     return reinterpret_cast<float*>(base + ((size_t)(j >> 1) * S + 1) * stride + (j & 1) * 4 * kHeadDim);
@@ -784,18 +790,6 @@ __host__ __device__ constexpr int word_pos(int w) {
   return BITS <= 3 ? (w & 7) : (w & 3);
 }
 
-// q of the CTA's heads in global memory, times scale * log2(e) (read for
-// the fp16 outlier channels, at most four per tile).
-struct QRows {
-  const void* q;
-  long row0;  // element index of the chunk's first head
-  int dtype;
-  float scale_log2;
-  __device__ __forceinline__ float at(int head, int ch) const {
-    return load_q(q, row0 + (long)head * kHeadDim + ch, dtype) * scale_log2;
-  }
-};
-
 // Q' = q * sK of one key group as MMA B fragments for column g of this lane,
 // in the order of the q tables: one key block, head g >> 1, part g & 1 (one
 // fp16 of the pair per lane); two key blocks, head g, both parts (bq[0] hi,
@@ -844,7 +838,7 @@ __device__ __forceinline__ int score_row(int g) { return (g & 3) + 8 * (g >> 2);
 template <int BITS, int NB>
 __device__ __forceinline__ void key_scores(const PackedState<NB>& ws, const TileBuf<BITS>& tb, int g, int tig,
                                            const float (&ks)[NB], const float (&mb)[NB], int n_out,
-                                           const QRows& qr, const float* brow, float (&sc)[NB][4]) {
+                                           const float* qo, const float* brow, float (&sc)[NB][4]) {
   constexpr int RW = 4 * BITS;  // 32-bit words per code row
   float kbm[NB];  // beta * ks - mb, the score offset of the tile (beta from brow, see beta_mma)
   if constexpr (NB == 1) {
@@ -961,11 +955,11 @@ __device__ __forceinline__ void key_scores(const PackedState<NB>& ws, const Tile
         const int ch = (iw >> (8 * o)) & 0xffu;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) {
-          const float qo = qr.at(NB == 1 ? tig : 2 * tig + nb, ch);
+          const float qx = qo[(NB == 1 ? tig : 2 * tig + nb) * kHeadDim + ch];
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const int t = 16 * (r >> 1) + tr + 4 * (r & 1);
-            sc[nb][r] = fmaf(qo, __half2float(ov[t * n_out + o]), sc[nb][r]);
+            sc[nb][r] = fmaf(qx, __half2float(ov[t * n_out + o]), sc[nb][r]);
           }
         }
       }
@@ -1199,7 +1193,7 @@ __device__ __forceinline__ void load_q8(const AttnArgs& a, int b, int j0, int nh
 }
 
 template <int BITS, int NB>
-__device__ void build_q_tables(const SmemView<BITS, NB>& sv, const AttnArgs& a, const float (&v)[8]) {
+__device__ void build_q_tables(const SmemView<BITS, NB>& sv, const AttnArgs& a, const float (&v)[8], bool keep_q) {
   PackedState<NB>& s = sv.ps();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -1207,6 +1201,11 @@ __device__ void build_q_tables(const SmemView<BITS, NB>& sv, const AttnArgs& a, 
     const int j = warp + kWarps * hh;
     const float* vj = v + 4 * hh;
     *reinterpret_cast<float4*>(sv.qv(j) + 4 * lane) = make_float4(vj[0], vj[1], vj[2], vj[3]);
+    if (keep_q) {
+      const float sl = a.scale_log2;
+      *reinterpret_cast<float4*>(sv.qo() + j * kHeadDim + 4 * lane) =
+          make_float4(vj[0] * sl, vj[1] * sl, vj[2] * sl, vj[3] * sl);
+    }
     const float amax = warp_max(fmaxf(fmaxf(fabsf(vj[0]), fabsf(vj[1])), fmaxf(fabsf(vj[2]), fabsf(vj[3]))));
     if (lane == 0) {
       const int be = (int)((__float_as_uint(amax) >> 23) & 0xffu);
@@ -1395,7 +1394,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
   unsigned char* const ring = reinterpret_cast<unsigned char*>(sv.ring(warp));
   auto st = [&](int k) -> TileBuf<BITS>& { return *reinterpret_cast<TileBuf<BITS>*>(ring + (size_t)k * sv.stride); };
   unsigned long long* bars = ws.bar[warp];
-  const QRows qr{a.q, ((long)b * a.Hq + j0) * kHeadDim, a.q_dtype, a.scale_log2};
+  const float* const qo = sv.qo();  // q for the outlier channels (when the cache keeps them)
   float qv8[8];
   load_q8(a, b, j0, nh, qv8);
 
@@ -1418,7 +1417,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
   // are built (unless the tiles may still be written by the kernel before)
   uint4 z[2][4];
   if (!wait_first) load_zk<BITS>(us, t_first, n_mine, 0, g, tig, z);
-  build_q_tables<BITS, NB>(sv, a, qv8);
+  build_q_tables<BITS, NB>(sv, a, qv8, cv.n_out > 0);
   __syncthreads();
   if (wait_first) grid_dependency_wait();
   if (lane == 0)
@@ -1465,7 +1464,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
       float sc[NB][4], mb[NB];
 #pragma unroll
       for (int nb = 0; nb < NB; ++nb) mb[nb] = 0.0f;
-      key_scores<BITS, NB>(ws, st(0), g, tig, ks, mb, cv.n_out, qr, brows, sc);
+      key_scores<BITS, NB>(ws, st(0), g, tig, ks, mb, cv.n_out, qo, brows, sc);
       softmax_p<NB>(sc, g, tig, m_run, O, Z, pb);
     }
   }
@@ -1498,7 +1497,7 @@ __device__ void packed_split(const CacheView& cv, const AttnArgs& a, const SmemV
       __syncwarp();
     }
     float sc[NB][4];
-    key_scores<BITS, NB>(ws, st(sn), g, tig, ks, m_run, cv.n_out, qr, brows + kb * 4 * NB, sc);
+    key_scores<BITS, NB>(ws, st(sn), g, tig, ks, m_run, cv.n_out, qo, brows + kb * 4 * NB, sc);
     value_acc<BITS>(st(sk), pb, g, tig, O, Z);
     done = k + 1;
     __syncwarp();  // every lane is done with stage sk
@@ -1862,15 +1861,17 @@ __global__ void __launch_bounds__(128, attn_ctas_per_sm(BITS, NB))
 // Stages per warp for a tile of `stride` bytes: as many as attn_ctas_per_sm
 // CTAs per SM leave room for (228 KB of shared memory per SM; per CTA 1 KB
 // reserved by the system and the kernel's static arrays), at least two and
-// at most kMaxStages; *smem is the dynamic size (the packed layout, or the
-// tail split's if larger).
+// at most kMaxStages; *smem is the dynamic size (the packed layout, with
+// the copy of q when the cache keeps n_out > 0 outlier channels, or the tail
+// split's if larger).
 template <int BITS, int NB>
-int attn_stages(uint32_t stride, size_t* smem) {
+int attn_stages(uint32_t stride, int n_out, size_t* smem) {
   const size_t per_cta = (size_t)228 * 1024 / attn_ctas_per_sm(BITS, NB) - 1024 - 512;
-  const size_t fixed = sizeof(PackedState<NB>) + 16;
+  const size_t q_copy = n_out > 0 ? (size_t)kNH * kHeadDim * 4 : 0;
+  const size_t fixed = sizeof(PackedState<NB>) + q_copy + 16;
   int S = (int)((per_cta - fixed) / ((size_t)kWarps * stride));
   S = S < 2 ? 2 : (S > kMaxStages ? kMaxStages : S);
-  const size_t packed = packed_state_off(S, stride) + sizeof(PackedState<NB>);
+  const size_t packed = packed_state_off(S, stride) + sizeof(PackedState<NB>) + q_copy;
   *smem = packed > sizeof(TailSmem<BITS>) ? packed : sizeof(TailSmem<BITS>);
   return S;
 }
@@ -1886,7 +1887,7 @@ template <int BITS, int NB>
 cudaError_t launch_bits(const dim3& grid, const CacheView& cv, AttnArgs a, const SeqLens& lens,
                         cudaStream_t st) {
   size_t smem = 0, cap = 0;
-  a.stages = attn_stages<BITS, NB>((uint32_t)(cv.tile_bytes - kStageOff), &smem);
+  a.stages = attn_stages<BITS, NB>((uint32_t)(cv.tile_bytes - kStageOff), cv.n_out, &smem);
   // The shared-memory opt-in is a per-device function attribute: set to the
   // largest size any outlier count asks for (the same on every call, so
   // that calls from several host threads cannot shrink it under another's
@@ -1894,7 +1895,7 @@ cudaError_t launch_bits(const dim3& grid, const CacheView& cv, AttnArgs a, const
   const uint32_t plain = (uint32_t)(cv.tile_bytes - kStageOff - outlier_block_bytes(cv.n_out));
   for (int n = 0; n <= kMaxOutliers; ++n) {
     size_t sz = 0;
-    attn_stages<BITS, NB>(plain + (uint32_t)outlier_block_bytes(n), &sz);
+    attn_stages<BITS, NB>(plain + (uint32_t)outlier_block_bytes(n), n, &sz);
     cap = sz > cap ? sz : cap;
   }
   const cudaError_t e =
