@@ -210,16 +210,17 @@ int max_splits(const kivi_config& c) {
 
 // The cache's split configuration (kivi::make_plan plans one length with it).
 // Launches that overlap the attention launch before them (`overlapped`)
-// take half the budget and at least 64 tiles per packed split, and a tail
-// of one split rides on the last packed split: the CTAs of consecutive
-// launches then share the SMs, and the cost that every split pays once (its
-// q tables, the wait for its first tile, its share of the merge) weighs
-// more than the CTAs a launch leaves idle.  Measured on a GB300 with
-// overlapped launches: the Llama-3-8B decode shape (8 units of 128 tiles
-// per sequence) takes 8.6 us with 2 packed splits per unit and the tail
-// fused, 8.9 us with a separate tail split, 10.9 us with 8 packed splits;
-// 131k tokens (4096 tiles, 8 units) 23.2 us with 35 packed splits against
-// 25.3 us with 74 (its three tail splits stay separate: fused, 30 us).
+// take a third of the budget and at least 128 tiles per packed split, and a
+// tail of one split rides on the last packed split: the CTAs of several
+// consecutive launches share the SMs, and the cost that every split pays
+// once (its q tables, the wait for its first tile, its share of the merge)
+// weighs more than the CTAs a launch leaves idle.  Measured on a GB300 with
+// overlapped launches (per-group generations, no launch-wide waits): the
+// Llama-3-8B decode shape (8 units of 127 tiles per sequence) takes 7.1 us
+// with one packed split per unit carrying the tail, 7.8 us with two, 9.1 us
+// with four; 131k tokens (4092 tiles, 8 units) 21.5 us with 23 packed
+// splits, 22.2 us with 36, 22.5 us with 10 (its three tail splits stay
+// separate).
 // Tiles fewer for the packed split that carries a fused tail in overlapped
 // plans: its fp16 tail round runs after its tiles.  Measured on the
 // Llama-3-8B decode shape (2 packed splits of 127 tiles per unit): 8.6 us
@@ -230,8 +231,8 @@ constexpr int kFusedDiscount = 32;
 kivi::SplitCfg split_cfg(const kivi_cache* c, bool overlapped) {
   kivi::SplitCfg sc;
   const int budget = split_budget(c->cfg);
-  sc.budget = overlapped ? (budget / 2 > 1 ? budget / 2 : 1) : budget;
-  sc.min_tiles = overlapped ? 64 : 8;
+  sc.budget = overlapped ? (budget / 3 > 1 ? budget / 3 : 1) : budget;
+  sc.min_tiles = overlapped ? 128 : 8;
   sc.fuse_single_tail = overlapped ? 1 : 0;
   sc.fused_discount = overlapped ? kFusedDiscount : 0;
   sc.max_splits = max_splits(c->cfg);

@@ -298,8 +298,8 @@ kivi_status kivi_decode_step(kivi_cache *c, const void *k_new,
  * of a 152-SM GB300 (four CTAs per SM; three at 4 bits with more than four
  * query heads per KV head, two at 8 bits), with at least eight tiles per
  * packed split and a multiple of four.  With the overlap on (see
- * kivi_set_attention_overlap) the automatic choice takes half that budget
- * and at least 64 tiles per packed split, and rides the tail on the last
+ * kivi_set_attention_overlap) the automatic choice takes a third of that
+ * budget and at least 128 tiles per packed split, and rides the tail on the last
  * packed split when the tail is a single split or the budget holds no tail
  * split beside it (that split then takes up to 32 tiles fewer): the CTAs of
  * consecutive launches then share the SMs, and fewer, longer splits pay the

@@ -184,12 +184,12 @@ def test_split_plan_and_workspace(K):
         assert K.kivi_attention_splits(h, 4097) == 3
         K.kivi_set_attention_splits(h, 1000)  # clamped to the workspace bound
         assert K.kivi_attention_splits(h, 4097) == 9
-        # overlapped launches: half the budget (4) and >= 64 tiles per packed
-        # split -> 2 packed splits, the one-split tail riding on the last;
+        # overlapped launches: a third of the budget (3) and >= 128 tiles per
+        # packed split -> 1 packed split, the one-split tail riding on it;
         # an override is planned the same way with or without the overlap
         K.kivi_set_attention_splits(h, 0)
         K.kivi_set_attention_overlap(h, 1)
-        assert K.kivi_attention_splits(h, 4097) == 2
+        assert K.kivi_attention_splits(h, 4097) == 1
         for n in (2, 7, 9, 1000):
             K.kivi_set_attention_splits(h, n)
             with_ov = K.kivi_attention_splits(h, 4097)
@@ -204,9 +204,9 @@ def test_split_plan_and_workspace(K):
     c = cfg(K, batch=1, n_kv_heads=8, n_q_heads=32, residual=128, max_tokens=131072)
     h = K.kivi_cache_init(c, _fake_buffers(K))
     assert K.kivi_attention_splits(h, 131072) == 76
-    # overlapped: budget 38 -> 2 tail splits and 36 packed splits of 116 tiles
+    # overlapped: budget 25 -> 2 tail splits and 23 packed splits of 180 tiles
     K.kivi_set_attention_overlap(h, 1)
-    assert K.kivi_attention_splits(h, 131072) == 38
+    assert K.kivi_attention_splits(h, 131072) == 25
     K.kivi_cache_destroy(h)
     # 320 units: one split per unit fits the wave, so the tail rides on the
     # packed split
