@@ -464,6 +464,15 @@ def graph_per_launch(torch, stream, ev, calls, overlap=()):
     return t
 
 
+def plan_splits(c):
+    """Splits per unit of the launches graph_per_launch times (overlapped),
+    and of ordinary launches."""
+    c.set_overlap(True)
+    ov = c.splits()
+    c.set_overlap(False)
+    return {"splits": ov, "splits_ordinary": c.splits()}
+
+
 def extra_workloads(args, torch, W, KiviCache, dev, stream, ev, peak, which=None):
     res = {}
     want = (lambda n: which is None or which == n)
@@ -555,7 +564,7 @@ def attention_bits(args, torch, W, KiviCache, dev, stream, ev, peak, bits, outli
         "what": f"{bits}-bit decode attention" + (f" with {outliers} fp16 outlier key channels per group"
                                                    if outliers else "")
                 + f", batch 8, 32/8 heads, context 4097, R 32; {n_rep} cache replicas rotated; graph replay",
-        "splits": caches[0].splits(), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
+        **plan_splits(caches[0]), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
         "us": round(tg * 1e6, 2), "us_per_launch_events": round(float(np.mean(times)) * 1e6, 2),
         "bytes": nbytes}
     del caches, c0
@@ -597,7 +606,7 @@ def long_context(args, torch, W, KiviCache, dev, stream, ev, peak):
     res["long_context_attention"] = {
         "what": "batch 1, 32/8 heads, context 131072, R 128; split-K decode attention; "
                 f"{n_rep} cache replicas rotated; graph replay",
-        "splits": caches[0].splits(), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
+        **plan_splits(caches[0]), "gbs": round(gbs, 2), "pct_of_peak": round(100 * gbs / peak, 2),
         "us": round(tg * 1e6, 2), "us_per_launch_events": round(float(np.mean(times)) * 1e6, 2),
         "bytes": nbytes}
     del caches, c0
